@@ -1,0 +1,164 @@
+"""fp64 CPU oracle of the gated delta rule -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of ``bench.py`` may
+import this package.  The CUDA library and its Python binding never import it, and the
+two share no code: the oracle is the plain token loop in ``dr_oracle.c`` (decay, predict,
+write the residual, read), the recurrence
+
+    S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,   o_t = S_t^T q_t
+
+as the page "NLP: linear attention summary" writes it for KDA (scalar alpha: Gated
+DeltaNet, alpha = 1: DeltaNet), taken in the order of the teaching loop
+``gated_delta_rule`` on the page "linear-attention gated-deltanet guide" (section 4).
+
+Every input is first converted exactly to float64 (bf16 and fp32 values are exactly
+representable), so the oracle sees the quantised values a GPU kernel sees.
+
+Parity pins (tests/test_oracle.py) tie every function here to facts fixed by the pages
+and by the mathematics; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dr_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+GATE_NONE, GATE_SCALAR, GATE_CHANNEL = 0, 1, 2
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``dr_oracle.c`` with gcc into ``oracle/_build/liboracle.so``.
+
+    fp64, ``-ffp-contract=off`` so that no multiply-add is fused on either host
+    architecture.  The shared object is written to a temporary name and renamed, so
+    concurrent builders never see a half-written file.
+    """
+    if not force and os.path.exists(_LIB_PATH) and \
+            os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_BUILD_DIR)
+    os.close(fd)
+    cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-pthread", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(cmd, check=True, capture_output=True, text=True)
+        os.replace(tmp, _LIB_PATH)
+    except subprocess.CalledProcessError as e:
+        os.unlink(tmp)
+        raise RuntimeError(f"oracle build failed:\n{e.stderr}") from e
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        dp = ctypes.POINTER(ctypes.c_double)
+        i64 = ctypes.c_int64
+        lib.oracle_forward.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int,
+                                       dp, dp, dp, dp, dp, dp, dp, dp,
+                                       ctypes.c_int, i64]
+        lib.oracle_forward.restype = ctypes.c_int
+        lib.oracle_step.argtypes = [i64, i64, i64, i64, ctypes.c_int,
+                                    dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
+        lib.oracle_step.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def to_f64(x) -> np.ndarray | None:
+    """Exact conversion of a torch tensor (any float dtype, any device) or array to a
+    contiguous float64 numpy array."""
+    if x is None:
+        return None
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.detach().to("cpu", torch.float64).numpy())
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _gate_of(log_alpha, shape_bth, dk) -> int:
+    if log_alpha is None:
+        return GATE_NONE
+    if tuple(log_alpha.shape) == tuple(shape_bth):
+        return GATE_SCALAR
+    if tuple(log_alpha.shape) == tuple(shape_bth) + (dk,):
+        return GATE_CHANNEL
+    raise ValueError(f"log_alpha shape {log_alpha.shape} fits neither {shape_bth} "
+                     f"nor {tuple(shape_bth) + (dk,)}")
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def forward(q, k, v, log_alpha, beta, init_state=None, *, nthreads: int | None = None,
+            col_block: int = 0):
+    """Token-by-token fp64 forward.
+
+    q, k [B,T,H,dk]; v [B,T,H,dv]; beta [B,T,H]; log_alpha None, [B,T,H] or [B,T,H,dk];
+    init_state None or [B,H,dk,dv].  Returns (out [B,T,H,dv], final_state [B,H,dk,dv]),
+    both float64 numpy arrays.
+    """
+    q, k, v, beta = to_f64(q), to_f64(k), to_f64(v), to_f64(beta)
+    log_alpha, init_state = to_f64(log_alpha), to_f64(init_state)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, T, H) or beta.shape != (B, T, H):
+        raise ValueError("inconsistent shapes")
+    if init_state is not None and init_state.shape != (B, H, dk, dv):
+        raise ValueError("init_state must be [B,H,dk,dv]")
+    gate = _gate_of(log_alpha, (B, T, H), dk)
+    out = np.zeros((B, T, H, dv), dtype=np.float64)
+    final = np.zeros((B, H, dk, dv), dtype=np.float64)
+    rc = _load().oracle_forward(B, T, H, dk, dv, gate, _ptr(q), _ptr(k), _ptr(v),
+                                _ptr(log_alpha), _ptr(beta), _ptr(init_state),
+                                _ptr(out), _ptr(final),
+                                nthreads or default_threads(), col_block)
+    if rc != 0:
+        raise RuntimeError(f"oracle_forward returned {rc}")
+    return out, final
+
+
+def step(q, k, v, log_alpha, beta, state, *, nthreads: int | None = None):
+    """One decode step (the loop body once).
+
+    q, k [B,H,dk]; v [B,H,dv]; beta [B,H]; log_alpha None, [B,H] or [B,H,dk];
+    state [B,H,dk,dv].  Returns (out [B,H,dv], new_state [B,H,dk,dv]) as float64;
+    the input state is not modified.
+    """
+    q, k, v, beta = to_f64(q), to_f64(k), to_f64(v), to_f64(beta)
+    log_alpha = to_f64(log_alpha)
+    st = to_f64(state).copy()
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if st.shape != (B, H, dk, dv):
+        raise ValueError("state must be [B,H,dk,dv]")
+    gate = _gate_of(log_alpha, (B, H), dk)
+    out = np.zeros((B, H, dv), dtype=np.float64)
+    rc = _load().oracle_step(B, H, dk, dv, gate, _ptr(q), _ptr(k), _ptr(v),
+                             _ptr(log_alpha), _ptr(beta), _ptr(st), _ptr(out),
+                             nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_step returned {rc}")
+    return out, st
