@@ -1,0 +1,61 @@
+// chunk_layout.h -- problem record and workspace layout of the chunkwise forward.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dr {
+
+// A validated chunk-forward problem (all pointers are device pointers).
+struct ChunkProblem {
+    const void *q, *k, *v;
+    const float *log_alpha;
+    const void *beta;
+    const float *init_state;
+    void *out;
+    float *final_state;
+    int64_t B, T, H;
+    int dk, dv, C, NC, gate;
+    bool in_bf16, out_bf16;
+};
+
+// fp32 intermediates of the two-kernel CUDA-core path, one slab per (b, h, chunk) n:
+//   W  [n][C][dk]   T diag(beta) (K*G)
+//   U  [n][C][dv]   T diag(beta) V
+//   Qg [n][C][dk]   Q*G
+//   Kd [n][C][dk]   K*G_C/G
+//   P  [n][C][C]    lower-triangular intra-chunk read matrix
+//   gam [n][dk]     G_C
+struct ChunkWorkspace {
+    float *W, *U, *Qg, *Kd, *P, *gam;
+};
+
+inline size_t simt_workspace_floats(int64_t B, int64_t H, int64_t NC, int64_t C, int64_t dk,
+                                    int64_t dv) {
+    const int64_t n = B * H * NC;
+    return (size_t)(n * (C * dk * 3 + C * dv + C * C + dk));
+}
+
+// Carve the workspace; every slab starts on a 16-byte boundary because each slab size is
+// a multiple of 4 floats (C, dk, dv are multiples of 16).
+inline ChunkWorkspace simt_workspace_carve(void *base, int64_t B, int64_t H, int64_t NC,
+                                           int64_t C, int64_t dk, int64_t dv) {
+    const int64_t n = B * H * NC;
+    float *p = (float *)base;
+    ChunkWorkspace w;
+    w.W = p;   p += n * C * dk;
+    w.U = p;   p += n * C * dv;
+    w.Qg = p;  p += n * C * dk;
+    w.Kd = p;  p += n * C * dk;
+    w.P = p;   p += n * C * C;
+    w.gam = p;
+    return w;
+}
+
+int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStream_t stream);
+int launch_decode(int64_t BH, int dk, int dv, int in_bf16, int out_bf16, int gate,
+                  const void *q, const void *k, const void *v, const float *la,
+                  const void *beta, float *state, void *out, cudaStream_t s);
+
+}  // namespace dr

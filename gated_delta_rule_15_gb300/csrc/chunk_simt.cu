@@ -1,0 +1,389 @@
+// chunk_simt.cu -- chunkwise forward of the gated delta rule on the fp32 CUDA cores.
+//
+// Chunk form (derived from the recurrence S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} +
+// b_t k_t v_t^T, o_t = S_t^T q_t of the page "NLP: linear attention summary", KDA section;
+// the pages name the technique -- chunks computed in parallel inside, state carried
+// between them, WY representation and a triangular solve -- on the pages "Transformer
+// notes (5): linear attention optimisations" and "linear-attention gated-deltanet guide",
+// section 5, but print no chunk equations).  Inside a chunk of C tokens started from
+// S_0, with g_r = sum_{u<=r} log a_u (scalar or per key channel) and G_r = exp(g_r):
+//
+//   e_r = b_r (v_r - (Diag(a_r) S_{r-1})^T k_r)               (written residual)
+//   (I + A) E = diag(b) (V - (K*G) S_0),  A_rs = b_r (k_r*G_r).(k_s/G_s), s < r
+//   T = (I + A)^{-1},  W = T diag(b) (K*G),  U = T diag(b) V,  E = U - W S_0
+//   O = (Q*G) S_0 + P E,  P_rs = (q_r*G_r).(k_s/G_s) for s <= r, else 0
+//   S_C = Diag(G_C) S_0 + (K * G_C/G)^T E
+//
+// Two kernels:
+//   chunk_prep_kernel   one CTA per (b, h, chunk), all chunks in parallel: cumulative log
+//                       decay, A and P, the forward substitution for T, W and U; writes
+//                       W, U, P, Q*G, K*G_C/G and G_C to the workspace (fp32).
+//   chunk_state_kernel  one CTA per (b, h, 32 state columns), sequential over chunks:
+//                       E = U - W S, O = (Q*G) S + P E, S <- Diag(G_C) S + (K*G_C/G)^T E.
+//
+// Exponents: every factor exp(x) taken here has x <= 0, except inside one 16-token
+// sub-chunk, where x is bounded by 16 max|log a|.  For the per-channel gate the pair term
+// exp(g_r - g_s) of A and P is split at the last position p of the sub-chunk before the
+// one holding s (s <= p < r):  exp(g_r - ref_i) * exp(ref_i - ref_j) * exp(ref_j - g_s),
+// ref_j = g_{16 j - 1} (0 for j = 0), so no product divides by a tiny cumulative decay
+// (the log-space, two-level chunking remedy named on the "Transformer notes (5)" page).
+#include "common.cuh"
+#include "chunk_layout.h"
+
+namespace dr {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kLd = 132;   // padded fp32 row stride of [64][<=128] smem tiles
+constexpr int kLdA = 65;   // padded row stride of [64][64] smem tiles
+constexpr int kSub = 16;   // sub-chunk length of the exponent reference points
+
+struct PrepArgs {
+    const void *q, *k, *v;
+    const float *log_alpha;
+    const void *beta;
+    int64_t B, T, H;
+    int dv, C, NC, gate;
+    ChunkWorkspace ws;
+};
+
+struct StateArgs {
+    const float *init_state;
+    void *out;
+    float *final_state;
+    int64_t B, T, H;
+    int dv, C, NC;
+    ChunkWorkspace ws;
+};
+
+size_t prep_smem_bytes(int dk) {
+    return sizeof(float) * (size_t)(3 * 64 * kLd + 64 * dk + 16 * dk + 2 * 64 * kLdA + 64 + 64);
+}
+
+template <int DK, typename Tin>
+__global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
+    extern __shared__ float4 smem4[];
+    float *sK = reinterpret_cast<float *>(smem4);  // k, then left factor of A
+    float *sQ = sK + 64 * kLd;                     // q, then left factor of P
+    float *sR = sQ + 64 * kLd;                     // right factor, then b*K*G, then b*V
+    float *sG = sR + 64 * kLd;                     // [64][DK] cumulative log decay (channel)
+    float *sF = sG + 64 * DK;                      // [16][DK] sub-chunk pair factors
+    float *sA = sF + 16 * DK;                      // [64][kLdA] A
+    float *sT = sA + 64 * kLdA;                    // [64][kLdA] T = (I + A)^-1
+    float *sB = sT + 64 * kLdA;                    // [64] beta
+    float *sg = sB + 64;                           // [64] cumulative log decay (scalar)
+
+    const Tin *q = (const Tin *)a.q, *k = (const Tin *)a.k, *v = (const Tin *)a.v;
+    const Tin *beta = (const Tin *)a.beta;
+    const int C = a.C, NC = a.NC, dv = a.dv, tid = threadIdx.x;
+    const int gate = a.gate;
+    const int64_t n = blockIdx.x;            // (b*H + h)*NC + c
+    const int c = (int)(n % NC);
+    const int64_t bh = n / NC;
+    const int64_t h = bh % a.H, b = bh / a.H;
+    const int64_t t0 = (int64_t)c * C;
+    const int Lc = (int)(a.T - t0 < (int64_t)C ? a.T - t0 : (int64_t)C);
+    auto tok = [&](int r) -> int64_t { return (b * a.T + t0 + r) * a.H + h; };
+
+    // 1. beta and the cumulative log decay (padded rows: beta = 0, log a = 0).
+    for (int r = tid; r < C; r += kThreads) sB[r] = r < Lc ? to_f32(beta[tok(r)]) : 0.f;
+    if (gate == 2) {
+        for (int ch = tid; ch < DK; ch += kThreads) {
+            float acc = 0.f;
+            for (int r = 0; r < C; ++r) {
+                if (r < Lc) acc += a.log_alpha[tok(r) * DK + ch];
+                sG[r * DK + ch] = acc;
+            }
+        }
+    } else if (tid == 0) {
+        float acc = 0.f;
+        for (int r = 0; r < C; ++r) {
+            if (gate == 1 && r < Lc) acc += a.log_alpha[tok(r)];
+            sg[r] = acc;
+        }
+    }
+    // 2. k and q rows as fp32.
+    for (int idx = tid; idx < C * (DK / 4); idx += kThreads) {
+        const int r = idx / (DK / 4), c4 = 4 * (idx % (DK / 4));
+        float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), qq = kk;
+        if (r < Lc) {
+            kk = load4(k + tok(r) * DK + c4);
+            qq = load4(q + tok(r) * DK + c4);
+        }
+        *reinterpret_cast<float4 *>(sK + r * kLd + c4) = kk;
+        *reinterpret_cast<float4 *>(sQ + r * kLd + c4) = qq;
+    }
+    __syncthreads();
+
+    auto G = [&](int r, int ch) -> float { return gate == 2 ? sG[r * DK + ch] : sg[r]; };
+
+    // 3. G_C, K*G_C/G and Q*G to the workspace.
+    const int64_t wofs = n * (int64_t)C * DK;
+    for (int ch = tid; ch < DK; ch += kThreads) a.ws.gam[n * DK + ch] = expf(G(C - 1, ch));
+    for (int idx = tid; idx < C * DK; idx += kThreads) {
+        const int r = idx / DK, ch = idx % DK;
+        const float gr = G(r, ch);
+        a.ws.Kd[wofs + idx] = sK[r * kLd + ch] * expf(G(C - 1, ch) - gr);
+        a.ws.Qg[wofs + idx] = sQ[r * kLd + ch] * expf(gr);
+    }
+    __syncthreads();
+
+    // 4. A (strictly lower) and P (lower, diagonal included).
+    const int nsub = C / kSub;
+    if (gate == 2) {
+        auto ref = [&](int j, int ch) -> float { return j == 0 ? 0.f : sG[(kSub * j - 1) * DK + ch]; };
+        for (int idx = tid; idx < C * DK; idx += kThreads) {
+            const int r = idx / DK, ch = idx % DK, i = r / kSub;
+            const float gr = sG[r * DK + ch], ri = ref(i, ch);
+            sR[r * kLd + ch] = sK[r * kLd + ch] * expf(ri - gr);  // exponent in [0, 16 max|log a|]
+        }
+        for (int idx = tid; idx < 16 * DK; idx += kThreads) {
+            const int pr = idx / DK, ch = idx % DK, i = pr / 4, j = pr % 4;
+            sF[idx] = (j < i && i < nsub) ? expf(ref(i, ch) - ref(j, ch)) : 1.f;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < C * DK; idx += kThreads) {
+            const int r = idx / DK, ch = idx % DK;
+            const float f = expf(sG[r * DK + ch] - ref(r / kSub, ch));   // exponent <= 0
+            sK[r * kLd + ch] *= f;
+            sQ[r * kLd + ch] *= f;
+        }
+        __syncthreads();
+    }
+    {
+        const int r = tid >> 2;
+        const int64_t pofs = n * (int64_t)C * C;
+        for (int m = 0; m < 16; ++m) {
+            const int s = (tid & 3) + 4 * m;
+            if (r >= C || s >= C) continue;
+            float ak = 0.f, aq = 0.f;
+            if (s <= r) {
+                const float *lk = sK + r * kLd, *lq = sQ + r * kLd;
+                if (gate == 2) {
+                    const float *rs = sR + s * kLd;
+                    const int i = r / kSub, j = s / kSub;
+                    if (i == j) {
+                        for (int ch = 0; ch < DK; ch += 4) {
+                            const float4 x = *reinterpret_cast<const float4 *>(lk + ch);
+                            const float4 y = *reinterpret_cast<const float4 *>(lq + ch);
+                            const float4 z = *reinterpret_cast<const float4 *>(rs + ch);
+                            ak += x.x * z.x + x.y * z.y + x.z * z.z + x.w * z.w;
+                            aq += y.x * z.x + y.y * z.y + y.z * z.z + y.w * z.w;
+                        }
+                    } else {
+                        const float *f = sF + (i * 4 + j) * DK;
+                        for (int ch = 0; ch < DK; ch += 4) {
+                            const float4 x = *reinterpret_cast<const float4 *>(lk + ch);
+                            const float4 y = *reinterpret_cast<const float4 *>(lq + ch);
+                            const float4 z = *reinterpret_cast<const float4 *>(rs + ch);
+                            const float4 w = *reinterpret_cast<const float4 *>(f + ch);
+                            const float4 zw = make_float4(z.x * w.x, z.y * w.y, z.z * w.z, z.w * w.w);
+                            ak += x.x * zw.x + x.y * zw.y + x.z * zw.z + x.w * zw.w;
+                            aq += y.x * zw.x + y.y * zw.y + y.z * zw.z + y.w * zw.w;
+                        }
+                    }
+                } else {
+                    const float *rs = sK + s * kLd;
+                    for (int ch = 0; ch < DK; ch += 4) {
+                        const float4 x = *reinterpret_cast<const float4 *>(lk + ch);
+                        const float4 y = *reinterpret_cast<const float4 *>(lq + ch);
+                        const float4 z = *reinterpret_cast<const float4 *>(rs + ch);
+                        ak += x.x * z.x + x.y * z.y + x.z * z.z + x.w * z.w;
+                        aq += y.x * z.x + y.y * z.y + y.z * z.z + y.w * z.w;
+                    }
+                    const float sc = expf(sg[r] - sg[s]);   // exponent <= 0
+                    ak *= sc;
+                    aq *= sc;
+                }
+            }
+            sA[r * kLdA + s] = (s < r) ? sB[r] * ak : 0.f;
+            a.ws.P[pofs + r * C + s] = aq;   // zero above the diagonal
+        }
+    }
+    __syncthreads();
+
+    // 5. T = (I + A)^{-1} by forward substitution, column j by the 4 lanes tid/4 == j:
+    //    T_rj = delta_rj - sum_{j <= s < r} A_rs T_sj.
+    {
+        const int j = tid >> 2, part = tid & 3;
+        for (int r = part; r < C; r += 4)
+            if (j < C) sT[r * kLdA + j] = (r == j) ? 1.f : 0.f;
+        __syncwarp();
+        for (int r = 1; r < C; ++r) {
+            float acc = 0.f;
+            if (j < r)
+                for (int s = j + part; s < r; s += 4) acc += sA[r * kLdA + s] * sT[s * kLdA + j];
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (part == 0 && j < r) sT[r * kLdA + j] = -acc;
+            __syncwarp();
+        }
+    }
+    // 6. W = T diag(b) (K*G):  rows b_s k_s exp(g_s) (exponent <= 0), k reloaded raw.
+    for (int idx = tid; idx < C * DK; idx += kThreads) {
+        const int s = idx / DK, ch = idx % DK;
+        sR[s * kLd + ch] = s < Lc ? sB[s] * to_f32(k[tok(s) * DK + ch]) * expf(G(s, ch)) : 0.f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < C * DK; idx += kThreads) {
+        const int r = idx / DK, ch = idx % DK;
+        float acc = 0.f;
+        for (int s = 0; s <= r; ++s) acc += sT[r * kLdA + s] * sR[s * kLd + ch];
+        a.ws.W[wofs + idx] = acc;
+    }
+    __syncthreads();
+    //    U = T diag(b) V.
+    for (int idx = tid; idx < C * dv; idx += kThreads) {
+        const int s = idx / dv, j = idx % dv;
+        sR[s * kLd + j] = s < Lc ? sB[s] * to_f32(v[tok(s) * dv + j]) : 0.f;
+    }
+    __syncthreads();
+    const int64_t uofs = n * (int64_t)C * dv;
+    for (int idx = tid; idx < C * dv; idx += kThreads) {
+        const int r = idx / dv, j = idx % dv;
+        float acc = 0.f;
+        for (int s = 0; s <= r; ++s) acc += sT[r * kLdA + s] * sR[s * kLd + j];
+        a.ws.U[uofs + idx] = acc;
+    }
+}
+
+constexpr int kDvt = 32;   // state columns per CTA of the state pass
+
+size_t state_smem_bytes(int dk) {
+    return sizeof(float) * (size_t)(dk * kDvt + 3 * 64 * (dk + 4) + 2 * 64 * kDvt + 64 * kLdA + dk);
+}
+
+template <int DK, typename Tout>
+__global__ void __launch_bounds__(kThreads) chunk_state_kernel(StateArgs a) {
+    constexpr int LD = DK + 4;
+    extern __shared__ float4 smem4[];
+    float *sS = reinterpret_cast<float *>(smem4);  // [DK][32] state columns
+    float *sW = sS + DK * kDvt;                    // [64][LD]
+    float *sQg = sW + 64 * LD;                     // [64][LD]
+    float *sKd = sQg + 64 * LD;                    // [64][LD]
+    float *sU = sKd + 64 * LD;                     // [64][32]
+    float *sE = sU + 64 * kDvt;                    // [64][32]
+    float *sP = sE + 64 * kDvt;                    // [64][kLdA]
+    float *sGam = sP + 64 * kLdA;                  // [DK]
+
+    const int tiles = a.dv / kDvt;
+    const int jt = blockIdx.x % tiles;
+    const int64_t bh = blockIdx.x / tiles;
+    const int64_t h = bh % a.H, b = bh / a.H;
+    const int C = a.C, NC = a.NC, dv = a.dv, tid = threadIdx.x;
+    const int j = tid & 31, rg = tid >> 5;  // column in tile, row group (8 groups)
+    const int col = jt * kDvt + j;
+    Tout *out = (Tout *)a.out;
+
+    for (int i = rg; i < DK; i += 8)
+        sS[i * kDvt + j] = a.init_state ? a.init_state[(bh * DK + i) * dv + col] : 0.f;
+
+    for (int c = 0; c < NC; ++c) {
+        const int64_t n = bh * NC + c;
+        const int64_t t0 = (int64_t)c * C;
+        const int Lc = (int)(a.T - t0 < (int64_t)C ? a.T - t0 : (int64_t)C);
+        const float *W = a.ws.W + n * (int64_t)C * DK;
+        const float *Qg = a.ws.Qg + n * (int64_t)C * DK;
+        const float *Kd = a.ws.Kd + n * (int64_t)C * DK;
+        const float *U = a.ws.U + n * (int64_t)C * dv;
+        const float *P = a.ws.P + n * (int64_t)C * C;
+        __syncthreads();   // previous chunk's readers of the staged tiles are done
+        for (int idx = tid; idx < C * (DK / 4); idx += kThreads) {
+            const int r = idx / (DK / 4), c4 = 4 * (idx % (DK / 4));
+            *reinterpret_cast<float4 *>(sW + r * LD + c4) = load4(W + r * DK + c4);
+            *reinterpret_cast<float4 *>(sQg + r * LD + c4) = load4(Qg + r * DK + c4);
+            *reinterpret_cast<float4 *>(sKd + r * LD + c4) = load4(Kd + r * DK + c4);
+        }
+        for (int idx = tid; idx < C * kDvt; idx += kThreads)
+            sU[idx] = U[(idx / kDvt) * dv + jt * kDvt + idx % kDvt];
+        for (int idx = tid; idx < C * C; idx += kThreads) sP[(idx / C) * kLdA + idx % C] = P[idx];
+        for (int i = tid; i < DK; i += kThreads) sGam[i] = a.ws.gam[n * DK + i];
+        __syncthreads();
+
+        // E = U - W S and the inter-chunk read (Q*G) S, rows r = rg + 8m.
+        float e[8], o[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) { e[m] = 0.f; o[m] = 0.f; }
+        for (int i = 0; i < DK; i += 4) {
+            const float s0 = sS[(i + 0) * kDvt + j], s1 = sS[(i + 1) * kDvt + j];
+            const float s2 = sS[(i + 2) * kDvt + j], s3 = sS[(i + 3) * kDvt + j];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int r = rg + 8 * m;
+                if (r < C) {
+                    const float4 w = *reinterpret_cast<const float4 *>(sW + r * LD + i);
+                    const float4 qg = *reinterpret_cast<const float4 *>(sQg + r * LD + i);
+                    e[m] += w.x * s0 + w.y * s1 + w.z * s2 + w.w * s3;
+                    o[m] += qg.x * s0 + qg.y * s1 + qg.z * s2 + qg.w * s3;
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int r = rg + 8 * m;
+            if (r < C) sE[r * kDvt + j] = sU[r * kDvt + j] - e[m];
+        }
+        __syncthreads();
+        // O = (Q*G) S + P E  (P lower triangular, diagonal included).
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int r = rg + 8 * m;
+            if (r < C) {
+                float acc = o[m];
+                for (int s = 0; s <= r; ++s) acc += sP[r * kLdA + s] * sE[s * kDvt + j];
+                if (r < Lc) out[((b * a.T + t0 + r) * a.H + h) * dv + col] = from_f32<Tout>(acc);
+            }
+        }
+        // S <- Diag(G_C) S + (K*G_C/G)^T E.
+        for (int i = rg; i < DK; i += 8) {
+            float acc = sGam[i] * sS[i * kDvt + j];
+            for (int r = 0; r < C; ++r) acc += sKd[r * LD + i] * sE[r * kDvt + j];
+            sS[i * kDvt + j] = acc;
+        }
+    }
+    if (a.final_state) {
+        __syncthreads();
+        for (int i = rg; i < DK; i += 8) a.final_state[(bh * DK + i) * dv + col] = sS[i * kDvt + j];
+    }
+}
+
+template <int DK, typename Tin, typename Tout>
+int launch_simt_t(const PrepArgs &pa, const StateArgs &sa, cudaStream_t stream) {
+    const size_t ps = prep_smem_bytes(DK), ss = state_smem_bytes(DK);
+    if (cudaFuncSetAttribute(chunk_prep_kernel<DK, Tin>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps) != cudaSuccess)
+        return kErrCuda;
+    if (cudaFuncSetAttribute(chunk_state_kernel<DK, Tout>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss) != cudaSuccess)
+        return kErrCuda;
+    const int64_t nprep = pa.B * pa.H * pa.NC;
+    const int64_t nstate = sa.B * sa.H * (sa.dv / kDvt);
+    if (nprep > 0) chunk_prep_kernel<DK, Tin><<<(unsigned)nprep, kThreads, ps, stream>>>(pa);
+    chunk_state_kernel<DK, Tout><<<(unsigned)nstate, kThreads, ss, stream>>>(sa);
+    return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+}
+
+}  // namespace
+
+int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStream_t stream) {
+    PrepArgs pa{p.q, p.k, p.v, p.log_alpha, p.beta, p.B, p.T, p.H, p.dv, p.C, p.NC, p.gate, ws};
+    StateArgs sa{p.init_state, p.out, p.final_state, p.B, p.T, p.H, p.dv, p.C, p.NC, ws};
+    using bf = __nv_bfloat16;
+    const bool ib = p.in_bf16, ob = p.out_bf16;
+    if (p.dk == 128) {
+        if (ib && ob) return launch_simt_t<128, bf, bf>(pa, sa, stream);
+        if (ib) return launch_simt_t<128, bf, float>(pa, sa, stream);
+        if (ob) return launch_simt_t<128, float, bf>(pa, sa, stream);
+        return launch_simt_t<128, float, float>(pa, sa, stream);
+    }
+    if (p.dk == 64) {
+        if (ib && ob) return launch_simt_t<64, bf, bf>(pa, sa, stream);
+        if (ib) return launch_simt_t<64, bf, float>(pa, sa, stream);
+        if (ob) return launch_simt_t<64, float, bf>(pa, sa, stream);
+        return launch_simt_t<64, float, float>(pa, sa, stream);
+    }
+    return kErrUnsupported;
+}
+
+}  // namespace dr

@@ -1,0 +1,129 @@
+// dr_api.cu -- the C ABI of libdr.so (declared in include/dr.h): argument validation,
+// workspace sizing and dispatch to the kernels.  Nothing here allocates device memory or
+// synchronises, except dr_get_device_status.
+#include "../../include/dr.h"
+#include "chunk_layout.h"
+#include "common.cuh"
+
+namespace dr {
+
+// Sticky device status word written by kernels whose waits are bounded.
+__device__ int g_device_status = 0;
+
+namespace {
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool dim_ok(int64_t d) { return d == 64 || d == 128; }
+bool dtype_ok(int32_t t) { return t == DR_F32 || t == DR_BF16; }
+
+// Common checks of a chunk descriptor; fills the problem's sizes.
+int check_chunk_desc(const dr_chunk_desc *d, ChunkProblem *p) {
+    if (!d) return kErrInvalid;
+    if (d->B < 1 || d->H < 1 || d->T < 0 || d->dk < 1 || d->dv < 1) return kErrInvalid;
+    if (!dtype_ok(d->in_dtype) || !dtype_ok(d->out_dtype)) return kErrInvalid;
+    if (d->gate < DR_GATE_NONE || d->gate > DR_GATE_CHANNEL) return kErrInvalid;
+    if (d->chunk != 0 && d->chunk != 16 && d->chunk != 32 && d->chunk != 64) {
+        return d->chunk < 0 ? kErrInvalid : kErrUnsupported;
+    }
+    if (!dim_ok(d->dk) || !dim_ok(d->dv)) return kErrUnsupported;
+    // Grid sizes are 1-D 32-bit; B*H*ceil(T/16) must fit.
+    if (d->B > (1 << 20) || d->H > (1 << 16) || d->T > ((int64_t)1 << 31)) return kErrUnsupported;
+    const int C = d->chunk == 0 ? 64 : d->chunk;
+    const int64_t NC = (d->T + C - 1) / C;
+    if (d->B * d->H * NC > 0x7fffffffLL) return kErrUnsupported;
+    p->B = d->B; p->T = d->T; p->H = d->H;
+    p->dk = (int)d->dk; p->dv = (int)d->dv; p->C = C; p->NC = (int)NC; p->gate = d->gate;
+    p->in_bf16 = d->in_dtype == DR_BF16;
+    p->out_bf16 = d->out_dtype == DR_BF16;
+    return kOk;
+}
+
+}  // namespace
+}  // namespace dr
+
+using namespace dr;
+
+extern "C" int dr_version(void) { return (0 << 16) | 1; }
+
+extern "C" int dr_chunk_fwd_workspace_bytes(const dr_chunk_desc *desc, size_t *bytes) {
+    if (!bytes) return kErrInvalid;
+    ChunkProblem p{};
+    const int rc = check_chunk_desc(desc, &p);
+    if (rc != kOk) return rc;
+    *bytes = sizeof(float) * simt_workspace_floats(p.B, p.H, p.NC, p.C, p.dk, p.dv);
+    return kOk;
+}
+
+extern "C" int dr_chunk_fwd(const dr_chunk_desc *desc, const void *q, const void *k,
+                            const void *v, const float *log_alpha, const void *beta,
+                            const float *init_state, void *out, float *final_state,
+                            void *workspace, size_t workspace_bytes, dr_stream_t stream) {
+    ChunkProblem p{};
+    int rc = check_chunk_desc(desc, &p);
+    if (rc != kOk) return rc;
+    if (p.T > 0 && (!q || !k || !v || !beta || !out)) return kErrInvalid;
+    if (p.gate != DR_GATE_NONE && p.T > 0 && !log_alpha) return kErrInvalid;
+    const void *ptrs[] = {q, k, v, log_alpha, beta, init_state, out, final_state, workspace};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return kErrInvalid;
+    if (final_state && init_state && final_state != init_state) {
+        const size_t sb = sizeof(float) * (size_t)(p.B * p.H * p.dk * p.dv);
+        const char *a0 = (const char *)init_state, *b0 = (const char *)final_state;
+        if (a0 < b0 + sb && b0 < a0 + sb) return kErrInvalid;   // partial overlap
+    }
+    size_t need = 0;
+    dr_chunk_fwd_workspace_bytes(desc, &need);
+    if (need > 0 && p.NC > 0 && (!workspace || workspace_bytes < need)) return kErrWorkspace;
+
+    p.q = q; p.k = k; p.v = v; p.log_alpha = p.gate == DR_GATE_NONE ? nullptr : log_alpha;
+    p.beta = beta; p.init_state = init_state; p.out = out; p.final_state = final_state;
+    const ChunkWorkspace ws = simt_workspace_carve(workspace, p.B, p.H, p.NC, p.C, p.dk, p.dv);
+    if (p.NC == 0 && !final_state) return kOk;
+    return launch_chunk_simt(p, ws, (cudaStream_t)stream);
+}
+
+extern "C" int dr_recurrent_step(const dr_step_desc *d, const void *q, const void *k,
+                                 const void *v, const float *log_alpha, const void *beta,
+                                 float *state, void *out, dr_stream_t stream) {
+    if (!d) return kErrInvalid;
+    if (d->B < 1 || d->H < 1 || d->dk < 1 || d->dv < 1 || d->reserved != 0) return kErrInvalid;
+    if (!dtype_ok(d->in_dtype) || !dtype_ok(d->out_dtype)) return kErrInvalid;
+    if (d->gate < DR_GATE_NONE || d->gate > DR_GATE_CHANNEL) return kErrInvalid;
+    if (!dim_ok(d->dk) || !dim_ok(d->dv)) return kErrUnsupported;
+    if (d->B * d->H > 0x7fffffffLL) return kErrUnsupported;
+    if (!q || !k || !v || !beta || !state || !out) return kErrInvalid;
+    if (d->gate != DR_GATE_NONE && !log_alpha) return kErrInvalid;
+    const void *ptrs[] = {q, k, v, log_alpha, beta, state, out};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return kErrInvalid;
+    const size_t sb = sizeof(float) * (size_t)(d->B * d->H * d->dk * d->dv);
+    const size_t ob = (size_t)(d->B * d->H * d->dv) * (d->out_dtype == DR_BF16 ? 2 : 4);
+    const char *s0 = (const char *)state, *o0 = (const char *)out;
+    if (s0 < o0 + ob && o0 < s0 + sb) return kErrInvalid;
+    return launch_decode(d->B * d->H, (int)d->dk, (int)d->dv, d->in_dtype == DR_BF16,
+                         d->out_dtype == DR_BF16, d->gate, q, k, v,
+                         d->gate == DR_GATE_NONE ? nullptr : log_alpha, beta, state, out,
+                         (cudaStream_t)stream);
+}
+
+extern "C" int dr_get_device_status(dr_stream_t stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return kErrCuda;
+    int st = 0;
+    if (cudaMemcpyFromSymbol(&st, g_device_status, sizeof(int)) != cudaSuccess) return kErrCuda;
+    const int zero = 0;
+    if (st != 0 && cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess)
+        return kErrCuda;
+    return st;
+}
+
+extern "C" const char *dr_strerror(int status) {
+    switch (status) {
+        case DR_OK: return "ok";
+        case DR_ERR_INVALID: return "invalid argument (null, size, alignment, overlap or enum)";
+        case DR_ERR_UNSUPPORTED: return "unsupported configuration (dk, dv in {64,128}; chunk in {16,32,64})";
+        case DR_ERR_CUDA: return "CUDA runtime or launch error";
+        case DR_ERR_TIMEOUT: return "a bounded device-side wait expired";
+        case DR_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}

@@ -1,0 +1,252 @@
+"""ctypes binding of libdr.so (include/dr.h).
+
+Argument marshalling only: shapes and dtypes are read off torch tensors, pointers and the
+current CUDA stream are passed to the C ABI, and every step of the computation runs in the
+library's CUDA kernels.  There is no CPU path: importing this module loads libdr.so and
+raises ImportError if it has not been built.
+
+Host (CPU) tensors are accepted by the ``*_host`` helpers only, which copy inputs to the
+device on the current stream, call the same entry point and copy the results back: that
+is the end-to-end path a caller with host buffers takes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libdr.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libdr.so is not built ({LIB_PATH}); run "
+                      "`python -c 'import __graft_entry__ as g; g.build()'`")
+_lib = ctypes.CDLL(LIB_PATH)
+
+DR_F32, DR_BF16 = 0, 1
+DR_GATE_NONE, DR_GATE_SCALAR, DR_GATE_CHANNEL = 0, 1, 2
+DR_OK, DR_ERR_INVALID, DR_ERR_UNSUPPORTED, DR_ERR_CUDA, DR_ERR_TIMEOUT, DR_ERR_WORKSPACE = \
+    0, -1, -2, -3, -4, -5
+
+# Symbols of include/dr.h (checked by tests/test_abi.py against the header).
+EXPORTED = ("dr_version", "dr_chunk_fwd_workspace_bytes", "dr_chunk_fwd",
+            "dr_recurrent_step", "dr_get_device_status", "dr_strerror")
+
+
+class ChunkDesc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64),
+                ("dk", ctypes.c_int64), ("dv", ctypes.c_int64),
+                ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("gate", ctypes.c_int32), ("chunk", ctypes.c_int32)]
+
+
+class StepDesc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("dk", ctypes.c_int64),
+                ("dv", ctypes.c_int64), ("in_dtype", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32), ("gate", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_vp = ctypes.c_void_p
+_lib.dr_version.argtypes = []
+_lib.dr_version.restype = ctypes.c_int
+_lib.dr_chunk_fwd_workspace_bytes.argtypes = [ctypes.POINTER(ChunkDesc),
+                                              ctypes.POINTER(ctypes.c_size_t)]
+_lib.dr_chunk_fwd_workspace_bytes.restype = ctypes.c_int
+_lib.dr_chunk_fwd.argtypes = [ctypes.POINTER(ChunkDesc), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                              _vp, _vp, ctypes.c_size_t, _vp]
+_lib.dr_chunk_fwd.restype = ctypes.c_int
+_lib.dr_recurrent_step.argtypes = [ctypes.POINTER(StepDesc), _vp, _vp, _vp, _vp, _vp, _vp,
+                                   _vp, _vp]
+_lib.dr_recurrent_step.restype = ctypes.c_int
+_lib.dr_get_device_status.argtypes = [_vp]
+_lib.dr_get_device_status.restype = ctypes.c_int
+_lib.dr_strerror.argtypes = [ctypes.c_int]
+_lib.dr_strerror.restype = ctypes.c_char_p
+
+_DT = {torch.float32: DR_F32, torch.bfloat16: DR_BF16}
+_TORCH_DT = {DR_F32: torch.float32, DR_BF16: torch.bfloat16}
+
+
+class DrError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {strerror(status)} (status {status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def version() -> int:
+    return _lib.dr_version()
+
+
+def strerror(status: int) -> str:
+    return _lib.dr_strerror(status).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _gate_of(log_alpha, bth_shape, dk):
+    if log_alpha is None:
+        return DR_GATE_NONE
+    if tuple(log_alpha.shape) == tuple(bth_shape):
+        return DR_GATE_SCALAR
+    if tuple(log_alpha.shape) == tuple(bth_shape) + (dk,):
+        return DR_GATE_CHANNEL
+    raise ValueError(f"log_alpha shape {tuple(log_alpha.shape)} fits neither "
+                     f"{tuple(bth_shape)} nor {tuple(bth_shape) + (dk,)}")
+
+
+def _check_dev(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def chunk_desc(B, T, H, dk, dv, in_dtype, out_dtype, gate, chunk=64) -> ChunkDesc:
+    return ChunkDesc(B, T, H, dk, dv, in_dtype, out_dtype, gate, chunk)
+
+
+def workspace_bytes(desc: ChunkDesc) -> int:
+    n = ctypes.c_size_t(0)
+    rc = _lib.dr_chunk_fwd_workspace_bytes(ctypes.byref(desc), ctypes.byref(n))
+    if rc != DR_OK:
+        raise DrError(rc, "dr_chunk_fwd_workspace_bytes")
+    return n.value
+
+
+def chunk_fwd(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
+              out_dtype=None, return_final_state: bool = True, out=None,
+              final_state=None, workspace=None, stream=None):
+    """Chunkwise forward (dr_chunk_fwd) on device tensors.
+
+    q, k [B,T,H,dk]; v [B,T,H,dv]; beta [B,T,H] (q's dtype); log_alpha None, fp32
+    [B,T,H] or [B,T,H,dk]; init_state None or fp32 [B,H,dk,dv].  Returns
+    (out [B,T,H,dv], final_state [B,H,dk,dv] fp32 or None).  ``final_state`` may be the
+    ``init_state`` tensor for an in-place carry.
+    """
+    _check_dev(q, k, v, log_alpha, beta, init_state, out, final_state, workspace)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
+        raise ValueError("q, k, v, beta must share one dtype (float32 or bfloat16)")
+    if tuple(k.shape) != (B, T, H, dk) or tuple(v.shape[:3]) != (B, T, H) \
+            or tuple(beta.shape) != (B, T, H):
+        raise ValueError("inconsistent shapes")
+    if log_alpha is not None and log_alpha.dtype != torch.float32:
+        raise ValueError("log_alpha must be float32")
+    if init_state is not None and (init_state.dtype != torch.float32
+                                   or tuple(init_state.shape) != (B, H, dk, dv)):
+        raise ValueError("init_state must be float32 [B,H,dk,dv]")
+    gate = _gate_of(log_alpha, (B, T, H), dk)
+    odt = _DT[out_dtype or q.dtype]
+    desc = chunk_desc(B, T, H, dk, dv, _DT[q.dtype], odt, gate, chunk)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=_TORCH_DT[odt], device=q.device)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    need = workspace_bytes(desc)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _lib.dr_chunk_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                           _ptr(beta), _ptr(init_state), _ptr(out), _ptr(final_state),
+                           _ptr(workspace), wbytes, _stream_handle(stream))
+    if rc != DR_OK:
+        raise DrError(rc, "dr_chunk_fwd")
+    return out, final_state
+
+
+def recurrent_step(q, k, v, log_alpha, beta, state, *, out=None, out_dtype=None,
+                   stream=None):
+    """One decode step (dr_recurrent_step); ``state`` [B,H,dk,dv] fp32 is updated in
+    place.  q, k [B,H,dk]; v [B,H,dv]; beta [B,H]; log_alpha None, [B,H] or [B,H,dk].
+    Returns out [B,H,dv]."""
+    _check_dev(q, k, v, log_alpha, beta, state, out)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
+        raise ValueError("q, k, v, beta must share one dtype (float32 or bfloat16)")
+    if state.dtype != torch.float32 or tuple(state.shape) != (B, H, dk, dv):
+        raise ValueError("state must be float32 [B,H,dk,dv]")
+    if log_alpha is not None and log_alpha.dtype != torch.float32:
+        raise ValueError("log_alpha must be float32")
+    gate = _gate_of(log_alpha, (B, H), dk)
+    odt = _DT[out_dtype or q.dtype]
+    desc = StepDesc(B, H, dk, dv, _DT[q.dtype], odt, gate, 0)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=_TORCH_DT[odt], device=q.device)
+    rc = _lib.dr_recurrent_step(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v),
+                                _ptr(log_alpha), _ptr(beta), _ptr(state), _ptr(out),
+                                _stream_handle(stream))
+    if rc != DR_OK:
+        raise DrError(rc, "dr_recurrent_step")
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the sticky device status word."""
+    return _lib.dr_get_device_status(_stream_handle(stream))
+
+
+class HostChunkRunner:
+    """End-to-end chunk forward for callers holding HOST buffers.
+
+    Owns device staging buffers and pinned host result buffers for one problem shape.
+    Each call copies the inputs host -> device on the current stream, runs dr_chunk_fwd,
+    copies out and final_state device -> host, and synchronises.  Returns the pinned host
+    result tensors (reused across calls)."""
+
+    def __init__(self, like: dict, *, chunk: int = 64, out_dtype=None, device="cuda"):
+        def mk(t):
+            return None if t is None else torch.empty(t.shape, dtype=t.dtype, device=device)
+        self.dev = {k_: mk(t) for k_, t in like.items()}
+        q, v = like["q"], like["v"]
+        B, T, H, dk = q.shape
+        dv = v.shape[-1]
+        odt = out_dtype or q.dtype
+        self.out = torch.empty((B, T, H, dv), dtype=odt, device=device)
+        self.fin = torch.empty((B, H, dk, dv), dtype=torch.float32, device=device)
+        self.out_h = torch.empty(self.out.shape, dtype=odt, pin_memory=True)
+        self.fin_h = torch.empty(self.fin.shape, dtype=torch.float32, pin_memory=True)
+        self.chunk = chunk
+        gate = _gate_of(like["log_alpha"], (B, T, H), dk)
+        desc = chunk_desc(B, T, H, dk, dv, _DT[q.dtype], _DT[odt], gate, chunk)
+        n = workspace_bytes(desc)
+        self.ws = torch.empty(n, dtype=torch.uint8, device=device) if n else None
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in like.values()
+                             if t is not None)
+        self.d2h_bytes = (self.out_h.numel() * self.out_h.element_size()
+                          + self.fin_h.numel() * self.fin_h.element_size())
+
+    def __call__(self, host: dict, sync: bool = True):
+        for k_, t in host.items():
+            if t is not None:
+                self.dev[k_].copy_(t, non_blocking=True)
+        g = self.dev
+        chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g.get("init_state"),
+                  chunk=self.chunk, out=self.out, final_state=self.fin, workspace=self.ws)
+        self.out_h.copy_(self.out, non_blocking=True)
+        self.fin_h.copy_(self.fin, non_blocking=True)
+        if sync:
+            torch.cuda.current_stream().synchronize()
+        return self.out_h, self.fin_h
+
+
+def chunk_fwd_host(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
+                   out_dtype=None):
+    """One-shot end-to-end call for host tensors (see HostChunkRunner)."""
+    like = {"q": q, "k": k, "v": v, "log_alpha": log_alpha, "beta": beta,
+            "init_state": init_state}
+    return HostChunkRunner(like, chunk=chunk, out_dtype=out_dtype)(like)

@@ -1,0 +1,143 @@
+/*
+ * dr.h -- C ABI of the GB300 (sm_103a) gated delta rule library, libdr.so.
+ *
+ * The operation (page "NLP: linear attention summary", sections "DeltaNet", "Gated
+ * DeltaNet" and "Kimi Delta Attention"):
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
+ *     o_t = S_t^T q_t,
+ *
+ * per (batch b, head h), with the state S in R^{dk x dv}.  alpha_t is a scalar per head and
+ * token (Gated DeltaNet), a dk-vector (KDA, per-channel gate) or 1 (DeltaNet).  The order
+ * is decay, predict with the decayed state, write the beta-scaled residual, read after the
+ * write (teaching loop `gated_delta_rule`, page "linear-attention gated-deltanet guide",
+ * section 4).  The chunkwise-parallel form evaluated by dr_chunk_fwd (section 5 of the same
+ * page; the WY representation and triangular solve named on the page "Transformer notes
+ * (5): linear attention optimisations") reaches the same result up to rounding.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc / torch CUDA memory) on the
+ *     current device, contiguous, row-major, 16-byte aligned.  The caller owns every
+ *     buffer; the library never allocates, frees or synchronises (except
+ *     dr_get_device_status) and keeps no host-side state between calls.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream).  A status of DR_OK means the work was validated and enqueued.
+ *   - Token-major layouts, the layout a projection GEMM writes:
+ *       q, k        [B, T, H, dk]    in_dtype
+ *       v           [B, T, H, dv]    in_dtype
+ *       beta        [B, T, H]        in_dtype, values in [0, 1]
+ *       log_alpha   [B, T, H] (DR_GATE_SCALAR) or [B, T, H, dk] (DR_GATE_CHANNEL), fp32,
+ *                   values <= 0; NULL for DR_GATE_NONE
+ *       out         [B, T, H, dv]    out_dtype
+ *       states      [B, H, dk, dv]   fp32 (row i = key channel, column j = value channel)
+ *     The decode entry point drops the T axis.
+ *   - Inputs are assumed finite; log_alpha <= 0 and beta in [0, 1] are not checked.
+ *   - Errors are returned before anything is enqueued: nothing is launched on a
+ *     negative status.
+ */
+#ifndef DR_H_
+#define DR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle as cudaStream_t. */
+typedef struct CUstream_st *dr_stream_t;
+
+/* Storage dtypes. */
+enum { DR_F32 = 0, DR_BF16 = 1 };
+
+/* Gate kinds: no gate (DeltaNet), scalar per head and token (Gated DeltaNet),
+   per key channel (KDA). */
+enum { DR_GATE_NONE = 0, DR_GATE_SCALAR = 1, DR_GATE_CHANNEL = 2 };
+
+/* Status codes. */
+enum {
+    DR_OK = 0,
+    DR_ERR_INVALID = -1,      /* null pointer, bad size, misaligned pointer, bad enum   */
+    DR_ERR_UNSUPPORTED = -2,  /* valid but not built: dk, dv not in {64, 128}, chunk    */
+    DR_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed                   */
+    DR_ERR_TIMEOUT = -4,      /* a bounded device-side wait expired (device status)     */
+    DR_ERR_WORKSPACE = -5     /* workspace missing or smaller than the query's answer   */
+};
+
+/* Problem descriptor of the chunkwise forward. */
+typedef struct {
+    int64_t B, T, H, dk, dv;  /* B, H >= 1; T >= 0; dk, dv in {64, 128}                */
+    int32_t in_dtype;         /* DR_F32 or DR_BF16: q, k, v, beta                       */
+    int32_t out_dtype;        /* DR_F32 or DR_BF16: out                                 */
+    int32_t gate;             /* DR_GATE_*                                              */
+    int32_t chunk;            /* chunk length C: 16, 32 or 64; 0 selects 64             */
+} dr_chunk_desc;
+
+/* Problem descriptor of one decode step. */
+typedef struct {
+    int64_t B, H, dk, dv;     /* B, H >= 1; dk, dv in {64, 128}                         */
+    int32_t in_dtype;         /* DR_F32 or DR_BF16: q, k, v, beta                       */
+    int32_t out_dtype;        /* DR_F32 or DR_BF16: out                                 */
+    int32_t gate;             /* DR_GATE_*                                              */
+    int32_t reserved;         /* must be 0                                              */
+} dr_step_desc;
+
+/* Library version, (major << 16) | minor. */
+int dr_version(void);
+
+/* Bytes of device workspace dr_chunk_fwd needs for *desc; written to *bytes.  The answer
+   depends only on the descriptor.  Returns DR_OK, DR_ERR_INVALID or DR_ERR_UNSUPPORTED. */
+int dr_chunk_fwd_workspace_bytes(const dr_chunk_desc *desc, size_t *bytes);
+
+/*
+ * Chunkwise forward over T tokens for all B x H chains.
+ *
+ *   init_state   NULL = zero initial state, else [B, H, dk, dv] fp32 (read only)
+ *   out          [B, T, H, dv] out_dtype (written)
+ *   final_state  NULL = not returned, else [B, H, dk, dv] fp32 (written); may equal
+ *                init_state for an in-place carry, must not overlap it otherwise
+ *   workspace    device scratch of at least dr_chunk_fwd_workspace_bytes(); may be NULL
+ *                when that size is 0.  Contents on entry are ignored; it must not be
+ *                used by other work until this call's kernels finish on `stream`.
+ *
+ * The chunk length C only changes rounding, never the result's definition.  A tail chunk
+ * (T not a multiple of C) is padded with identity steps (k = 0, beta = 0, log_alpha = 0),
+ * which leave S unchanged; their outputs are not written.
+ * Returns DR_OK, DR_ERR_INVALID, DR_ERR_UNSUPPORTED, DR_ERR_WORKSPACE or DR_ERR_CUDA.
+ */
+int dr_chunk_fwd(const dr_chunk_desc *desc,
+                 const void *q, const void *k, const void *v,
+                 const float *log_alpha, const void *beta,
+                 const float *init_state, void *out, float *final_state,
+                 void *workspace, size_t workspace_bytes, dr_stream_t stream);
+
+/*
+ * One decode step for B x H chains, one token each (the loop body of the recurrence
+ * once).  Streams the fp32 state through HBM once: it is read, decayed, updated and
+ * written back in place.
+ *
+ *   q, k   [B, H, dk] in_dtype;  v [B, H, dv] in_dtype;  beta [B, H] in_dtype
+ *   log_alpha  NULL (DR_GATE_NONE), [B, H] (scalar) or [B, H, dk] (channel), fp32
+ *   state  [B, H, dk, dv] fp32, read and overwritten
+ *   out    [B, H, dv] out_dtype (must not overlap state)
+ * Returns DR_OK, DR_ERR_INVALID, DR_ERR_UNSUPPORTED or DR_ERR_CUDA.
+ */
+int dr_recurrent_step(const dr_step_desc *desc,
+                      const void *q, const void *k, const void *v,
+                      const float *log_alpha, const void *beta,
+                      float *state, void *out, dr_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the library's sticky device status word
+   on the current device (DR_OK, or DR_ERR_TIMEOUT if a bounded device wait expired), or
+   DR_ERR_CUDA if the synchronisation itself failed. */
+int dr_get_device_status(dr_stream_t stream);
+
+/* Static, human-readable text of a status code (never NULL). */
+const char *dr_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DR_H_ */

@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: the library loads, exports every function include/dr.h
+declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def dr():
+    from gated_delta_rule_15_gb300 import build
+    build.build()
+    import gated_delta_rule_15_gb300.dr as m
+    return m
+
+
+def header_functions():
+    names = set()
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if not hdr.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", hdr)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(dr_\w+)\s*\(", text, re.M))
+    return names
+
+
+def test_header_declares_the_binding_symbols(dr):
+    assert header_functions() == set(dr.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(dr):
+    lib = dr.lib()
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_strerror(dr):
+    assert dr.version() >= 1
+    for st in (0, -1, -2, -3, -4, -5, 17):
+        assert isinstance(dr.strerror(st), str) and dr.strerror(st)
+
+
+def _desc(dr, **kw):
+    d = dict(B=2, T=100, H=3, dk=128, dv=128, in_dtype=dr.DR_BF16, out_dtype=dr.DR_BF16,
+             gate=dr.DR_GATE_SCALAR, chunk=64)
+    d.update(kw)
+    return dr.ChunkDesc(**d)
+
+
+def test_workspace_query(dr):
+    n = dr.workspace_bytes(_desc(dr))
+    assert n > 0 and n % 16 == 0
+    assert dr.workspace_bytes(_desc(dr, T=0)) == 0
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(dk=96), -2), (dict(dv=32), -2), (dict(chunk=48), -2), (dict(chunk=-1), -1),
+    (dict(B=0), -1), (dict(H=0), -1), (dict(T=-1), -1), (dict(gate=3), -1),
+    (dict(in_dtype=7), -1), (dict(out_dtype=-1), -1)])
+def test_bad_descriptors_rejected(dr, bad, status):
+    n = ctypes.c_size_t(0)
+    rc = dr.lib().dr_chunk_fwd_workspace_bytes(ctypes.byref(_desc(dr, **bad)), ctypes.byref(n))
+    assert rc == status
+
+
+# The next two tests pass fake (never dereferenced) device addresses and expect host-side
+# rejection.  They are kept off machines with a GPU, where a validation bug would turn
+# them into a launch on unmapped memory.
+no_gpu_only = pytest.mark.skipif(
+    __import__("torch").cuda.is_available(), reason="fake-pointer checks run only without a GPU")
+
+
+@no_gpu_only
+def test_chunk_fwd_host_side_errors(dr):
+    lib = dr.lib()
+    d = _desc(dr)
+    fake = ctypes.c_void_p(1 << 20)        # aligned, never dereferenced: rejected first
+    mis = ctypes.c_void_p((1 << 20) + 8)   # misaligned
+    null = None
+    args = lambda **o: [o.get(n, fake) for n in
+                        ("q", "k", "v", "la", "beta", "s0", "out", "fin", "ws")]
+    call = lambda a, wb=1 << 40: lib.dr_chunk_fwd(ctypes.byref(d), *a, wb, None)
+    assert lib.dr_chunk_fwd(None, *args(), 0, None) == dr.DR_ERR_INVALID
+    assert call(args(q=null)) == dr.DR_ERR_INVALID
+    assert call(args(la=null)) == dr.DR_ERR_INVALID          # scalar gate needs log_alpha
+    assert call(args(out=mis)) == dr.DR_ERR_INVALID
+    assert call(args(ws=null)) == dr.DR_ERR_WORKSPACE
+    assert call(args(), wb=16) == dr.DR_ERR_WORKSPACE
+    # final_state partially overlapping init_state
+    assert call(args(s0=ctypes.c_void_p(1 << 20), fin=ctypes.c_void_p((1 << 20) + 1024))) \
+        == dr.DR_ERR_INVALID
+
+
+@no_gpu_only
+def test_recurrent_step_host_side_errors(dr):
+    lib = dr.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    d = dr.StepDesc(4, 2, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_CHANNEL, 0)
+    call = lambda desc, **o: lib.dr_recurrent_step(
+        ctypes.byref(desc), *[o.get(n, fake) for n in ("q", "k", "v", "la", "beta")],
+        o.get("state", ctypes.c_void_p(1 << 30)), o.get("out", ctypes.c_void_p(1 << 32)), None)
+    assert call(d, la=None) == dr.DR_ERR_INVALID
+    assert call(d, state=None) == dr.DR_ERR_INVALID
+    assert call(d, out=ctypes.c_void_p((1 << 30) + 64)) == dr.DR_ERR_INVALID  # overlaps state
+    d2 = dr.StepDesc(4, 2, 128, 80, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_CHANNEL, 0)
+    assert call(d2) == dr.DR_ERR_UNSUPPORTED
+    d3 = dr.StepDesc(4, 2, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_CHANNEL, 1)
+    assert call(d3) == dr.DR_ERR_INVALID
+
+
+def test_python_binding_rejects_host_tensors(dr):
+    import torch
+    x = torch.zeros(1, 4, 1, 64)
+    with pytest.raises(ValueError):
+        dr.chunk_fwd(x, x, x, None, torch.zeros(1, 4, 1))

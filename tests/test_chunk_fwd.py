@@ -1,0 +1,152 @@
+"""GPU parity of dr_chunk_fwd against the fp64 oracle (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_15_gb300 import inputs
+from parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dr():
+    import gated_delta_rule_15_gb300.dr as m
+    return m
+
+
+def dev(d):
+    return {k: (None if v is None else v.cuda()) for k, v in d.items()}
+
+
+def run(dr, d, **kw):
+    g = dev(d)
+    out, fin = dr.chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"],
+                            g["init_state"], **kw)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    return out, fin
+
+
+def check(dr, d, dtype, chunk=64, out_dtype=None):
+    out, fin = run(dr, d, chunk=chunk, out_dtype=out_dtype)
+    o_ref, f_ref = oracle.forward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                  d["init_state"])
+    e1 = assert_close(out, o_ref, dtype, "out")
+    e2 = assert_close(fin, f_ref, dtype, "final_state")
+    return e1, e2
+
+
+# fp32, single sequence, single head, d = 64, T = 256, zero initial state
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_f32_single_head(dr, chunk):
+    w = inputs.WORKLOADS["gdn_f32_B1_H1_T256_d64"]
+    check(dr, inputs.workload_inputs(w), "f32", chunk=chunk)
+
+
+@pytest.mark.parametrize("gate", ["none", "scalar", "channel"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128), (128, 64), (64, 64)])
+def test_small_shapes(dr, gate, dtype, dk, dv):
+    # T = 150: two full chunks and a ragged tail of 22 tokens; nonzero initial state.
+    d = inputs.chunk_inputs(2, 150, 3, dk, dv, gate=gate, dtype=dtype, init_state=True,
+                            seed=11)
+    check(dr, d, dtype)
+
+
+@pytest.mark.parametrize("T", [0, 1, 15, 63, 64, 65, 127, 129])
+def test_edge_lengths(dr, T):
+    d = inputs.chunk_inputs(1, T, 2, 128, 128, gate="channel", dtype="f32",
+                            init_state=True, seed=T)
+    out, fin = run(dr, d)
+    o_ref, f_ref = oracle.forward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                  d["init_state"])
+    assert out.shape == (1, T, 2, 128)
+    if T:
+        assert_close(out, o_ref, "f32", "out")
+    assert_close(fin, f_ref, "f32", "final_state")
+
+
+@pytest.mark.parametrize("gate", ["scalar", "channel"])
+def test_strong_decay(dr, gate):
+    """log alpha ~ -U(0, 5): cumulative decays underflow inside a chunk."""
+    d = inputs.chunk_inputs(1, 200, 2, 128, 128, gate=gate, dtype="f32", init_state=True,
+                            seed=3, log_alpha_range=(0.0, 5.0))
+    check(dr, d, "f32")
+
+
+def test_beta_extremes_and_no_decay(dr):
+    """beta in {0, 1} and alpha = 1 (DeltaNet) with unit keys."""
+    d = inputs.chunk_inputs(1, 130, 2, 64, 64, gate="none", dtype="f32", init_state=True,
+                            seed=5)
+    d["beta"] = (torch.arange(130 * 2).reshape(1, 130, 2) % 3 == 0).float()
+    check(dr, d, "f32")
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_chunk_size_invariance_bf16(dr, chunk):
+    d = inputs.chunk_inputs(2, 256, 4, 128, 128, gate="channel", dtype="bf16", seed=21)
+    check(dr, d, "bf16", chunk=chunk)
+
+
+def test_fp32_output_for_bf16_inputs(dr):
+    d = inputs.chunk_inputs(2, 256, 4, 128, 128, gate="scalar", dtype="bf16", seed=22)
+    out, _ = run(dr, d, out_dtype=torch.float32)
+    assert out.dtype == torch.float32
+    o_ref, _ = oracle.forward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], None)
+    assert_close(out, o_ref, "bf16", "out")
+
+
+def test_carry_over_split(dr):
+    """chunk_fwd(x[:T1]) then chunk_fwd(x[T1:], init = its final state) equals the oracle
+    over the whole sequence (T1 not a multiple of the chunk)."""
+    d = inputs.chunk_inputs(2, 300, 2, 128, 128, gate="scalar", dtype="f32",
+                            init_state=True, seed=9)
+    g = dev(d)
+    sl = lambda t, a, b: None if t is None else t[:, a:b].contiguous()
+    o1, f1 = dr.chunk_fwd(sl(g["q"], 0, 100), sl(g["k"], 0, 100), sl(g["v"], 0, 100),
+                          sl(g["log_alpha"], 0, 100), sl(g["beta"], 0, 100), g["init_state"])
+    o2, f2 = dr.chunk_fwd(sl(g["q"], 100, 300), sl(g["k"], 100, 300), sl(g["v"], 100, 300),
+                          sl(g["log_alpha"], 100, 300), sl(g["beta"], 100, 300), f1,
+                          final_state=f1)   # in-place carry
+    torch.cuda.synchronize()
+    o_ref, f_ref = oracle.forward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                  d["init_state"])
+    assert_close(torch.cat([o1, o2], 1), o_ref, "f32", "out")
+    assert_close(f2, f_ref, "f32", "final_state")
+
+
+def test_deterministic(dr):
+    d = inputs.chunk_inputs(2, 200, 2, 128, 128, gate="channel", dtype="bf16", seed=4)
+    o1, f1 = run(dr, d)
+    o2, f2 = run(dr, d)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
+# ------------------------------------------------------------ full-size workloads
+def sampled_chains(w, n, seed=0):
+    rng = np.random.default_rng(seed)
+    chains = rng.choice(w.B * w.H, size=n, replace=False)
+    return [(int(c) // w.H, int(c) % w.H) for c in chains]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,nsample", [
+    ("gdn_bf16_B8_H16_T4096_d128", 6),
+    ("kda_bf16_B4_H32_T8192_d128", 4),
+    ("gdn_bf16_B1_H16_T65536_d128_init", 2)])
+def test_full_size_sampled_chains(dr, name, nsample):
+    """The workload at full size, in the launch configuration the benchmark times; the
+    oracle recomputes a sample of whole (b, h) chains."""
+    w = inputs.WORKLOADS[name]
+    d = inputs.workload_inputs(w)
+    out, fin = run(dr, d, chunk=w.chunk)
+    out_h, fin_h = out.cpu(), fin.cpu()
+    for b, h in sampled_chains(w, nsample):
+        pick = lambda t: None if t is None else t[b:b + 1, :, h:h + 1].contiguous()
+        s0 = None if d["init_state"] is None else d["init_state"][b:b + 1, h:h + 1]
+        o_ref, f_ref = oracle.forward(pick(d["q"]), pick(d["k"]), pick(d["v"]),
+                                      pick(d["log_alpha"]), pick(d["beta"]), s0)
+        assert_close(out_h[b:b + 1, :, h:h + 1], o_ref, "bf16", f"out chain {(b, h)}")
+        assert_close(fin_h[b:b + 1, h:h + 1], f_ref, "bf16", f"state chain {(b, h)}")
