@@ -31,7 +31,8 @@ DR_OK, DR_ERR_INVALID, DR_ERR_UNSUPPORTED, DR_ERR_CUDA, DR_ERR_TIMEOUT, DR_ERR_W
 
 # Symbols of include/dr.h (checked by tests/test_abi.py against the header).
 EXPORTED = ("dr_version", "dr_chunk_fwd_workspace_bytes", "dr_chunk_fwd",
-            "dr_recurrent_step", "dr_get_device_status", "dr_strerror")
+            "dr_recurrent_step", "dr_get_device_status", "dr_strerror",
+            "dr_chunk_fwd_noalloc")
 
 
 class ChunkDesc(ctypes.Structure):
@@ -64,6 +65,10 @@ _lib.dr_get_device_status.argtypes = [_vp]
 _lib.dr_get_device_status.restype = ctypes.c_int
 _lib.dr_strerror.argtypes = [ctypes.c_int]
 _lib.dr_strerror.restype = ctypes.c_char_p
+_lib.dr_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(ChunkDesc), _vp, _vp, _vp, _vp, _vp, _vp,
+                                      _vp, _vp, _vp]
+_lib.dr_chunk_fwd_noalloc.restype = ctypes.c_int
+NOALLOC_SCRATCH_BYTES = 64 << 20   # DR_NOALLOC_SCRATCH_BYTES of include/dr.h
 
 _DT = {torch.float32: DR_F32, torch.bfloat16: DR_BF16}
 _TORCH_DT = {DR_F32: torch.float32, DR_BF16: torch.bfloat16}
@@ -166,6 +171,25 @@ def chunk_fwd(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
     if rc != DR_OK:
         raise DrError(rc, "dr_chunk_fwd")
     return out, final_state
+
+
+def chunk_fwd_noalloc(q, k, v, log_alpha, beta, init_state, out, final_state, *,
+                      chunk: int = 64, stream=None):
+    """dr_chunk_fwd_noalloc: the chunk forward for callers that cannot allocate device
+    memory (a host framework that owns all memory through its own pool, a plugin whose
+    execute callback must not allocate, a loop that cannot pay cudaMalloc's implicit
+    synchronisation).  The caller passes preallocated ``out`` and ``final_state`` (or
+    None); the library's static 64 MiB device scratch replaces the workspace.  Calls that
+    overlap on the GPU race on that scratch; the first call on a device must precede any
+    stream capture.  Returns the status code (0 on success)."""
+    _check_dev(q, k, v, log_alpha, beta, init_state, out, final_state)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    desc = chunk_desc(B, T, H, dk, dv, _DT[q.dtype], _DT[out.dtype],
+                      _gate_of(log_alpha, (B, T, H), dk), chunk)
+    return _lib.dr_chunk_fwd_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(log_alpha), _ptr(beta), _ptr(init_state),
+                                     _ptr(out), _ptr(final_state), _stream_handle(stream))
 
 
 def recurrent_step(q, k, v, log_alpha, beta, state, *, out=None, out_dtype=None,

@@ -128,6 +128,33 @@ int dr_recurrent_step(const dr_step_desc *desc,
                       const float *log_alpha, const void *beta,
                       float *state, void *out, dr_stream_t stream);
 
+/*
+ * dr_chunk_fwd without a caller-provided workspace.  The pages have no counterpart of
+ * this entry point: it exists for callers that cannot allocate device memory -- code
+ * whose host framework owns all device memory through a pre-reserved pool, plugin
+ * interfaces whose execute callback must not allocate, latency-bound loops that cannot
+ * pay cudaMalloc's implicit synchronisation.  They still pass inputs and outputs exactly
+ * as for dr_chunk_fwd; the scratch comes from one static device array of
+ * DR_NOALLOC_SCRATCH_BYTES that libdr.so holds on every GPU it is loaded on until exit.
+ *
+ *   - Problems whose dr_chunk_fwd_workspace_bytes() exceeds DR_NOALLOC_SCRATCH_BYTES are
+ *     rejected with DR_ERR_WORKSPACE before anything is enqueued.  (dk = dv = 128, C = 64
+ *     needs 147,968 bytes per (b, h, chunk), so B * H * ceil(T / 64) <= 453.)
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call shares the array.  Calls whose work overlaps on the GPU (other streams,
+ *     other host threads) race on it; the caller must serialise them.  No contents need
+ *     clearing between calls: every scratch element read is first written by the call.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * Returns the statuses of dr_chunk_fwd, and DR_ERR_CUDA if the address lookup fails.
+ */
+#define DR_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int dr_chunk_fwd_noalloc(const dr_chunk_desc *desc,
+                         const void *q, const void *k, const void *v,
+                         const float *log_alpha, const void *beta,
+                         const float *init_state, void *out, float *final_state,
+                         dr_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the library's sticky device status word
    on the current device (DR_OK, or DR_ERR_TIMEOUT if a bounded device wait expired), or
    DR_ERR_CUDA if the synchronisation itself failed. */
