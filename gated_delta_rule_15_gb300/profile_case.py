@@ -1,0 +1,68 @@
+"""Run one kernel of the library a few times on a chosen workload, for profilers.
+
+    python -m gated_delta_rule_15_gb300.profile_case --what decode --B 128 --iters 3
+    python -m gated_delta_rule_15_gb300.profile_case --what chunk \
+        --workload gdn_bf16_B8_H16_T4096_d128 --B 2 --iters 3
+
+Sizes default to the named workload; --B / --T / --H shrink it (keep inputs larger than
+L2 for meaningful DRAM counters).  Prints the CUDA-event time per launch (a number taken
+under a profiler is not a benchmark result).
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import os
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--what", choices=["chunk", "decode"], required=True)
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--B", type=int, default=None)
+    ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--H", type=int, default=None)
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args()
+
+    import torch
+    from gated_delta_rule_15_gb300 import dr, inputs
+
+    torch.cuda.set_device(0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if args.what == "chunk":
+        w = inputs.WORKLOADS[args.workload or "gdn_bf16_B8_H16_T4096_d128"]
+        w = dataclasses.replace(w, **{k: getattr(args, k) for k in ("B", "T", "H")
+                                      if getattr(args, k) is not None})
+        d = inputs.workload_inputs(w)
+        g = {k: (None if t is None else t.cuda()) for k, t in d.items()}
+        run = lambda: dr.chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"],
+                                   g["init_state"], chunk=w.chunk)
+    else:
+        w = inputs.DECODE_WORKLOADS[args.workload or "decode_scalar_B256_H32_d128"]
+        w = dataclasses.replace(w, **({"B": args.B} if args.B else {}))
+        s = inputs.decode_workload_inputs(w, steps=max(1, args.iters))
+        st = s["state"].cuda()
+        g = {k: (None if t is None else t.cuda()) for k, t in s.items() if k != "state"}
+        i = [0]
+
+        def run():
+            t = i[0] % g["q"].shape[0]
+            i[0] += 1
+            la = None if g["log_alpha"] is None else g["log_alpha"][t]
+            dr.recurrent_step(g["q"][t], g["k"][t], g["v"][t], la, g["beta"][t], st)
+    run()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.iters):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    print(f"{w.name} {dataclasses.asdict(w)}: {e0.elapsed_time(e1) / args.iters:.4f} ms/launch")
+
+
+if __name__ == "__main__":
+    main()
