@@ -55,6 +55,12 @@ def csrc_hash():
     return h.hexdigest()[:16]
 
 
+def tc_path(w):
+    """The fused tensor-core kernel serves bf16, d_k = d_v = 128, C = 64, scalar or no gate."""
+    return (w.dtype == "bf16" and w.dk == 128 and w.dv == 128 and w.chunk == 64
+            and w.gate in ("none", "scalar") and w.T > 0)
+
+
 # ------------------------------------------------------------------ algorithmic counts
 def chunk_bytes(w):
     """Each input read once, each output written once; a zero initial state is not read."""
@@ -280,7 +286,8 @@ def run_native(args):
     ach_gbs = byts / (ms * 1e-3) / 1e9
     e2e_ms, h2d, d2h = bench_chunk_e2e(w, r["host_inputs"], max(2, args.steps // 2),
                                        max(3, args.warmup), world)
-    launches_per_call = 2   # chunk_prep_kernel + chunk_state_kernel
+    tc = tc_path(w)
+    launches_per_call = 1 if tc else 2
 
     extra = {}
     if not args.quick:
@@ -325,7 +332,8 @@ def run_native(args):
         "roofline": {"bound": "hbm", "achieved": ach_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": ach_gbs / hbm, "peak_source": pk_kind,
                      "traffic": (tr["bytes"] if tr and tr["src"] == src else None),
-                     "kernel": "dr_chunk_fwd (chunk_prep_kernel + chunk_state_kernel)",
+                     "kernel": ("chunk_tc_kernel (fused tcgen05, one launch per call)" if tc else
+                                "chunk_prep_kernel + chunk_state_kernel"),
                      "algorithmic_bytes": byts,
                      "tensor_tflops": flops / (ms * 1e-3) / 1e12,
                      "tensor_frac": flops / (ms * 1e-3) / 1e12 / tc},

@@ -12,6 +12,19 @@ __device__ int g_device_status = 0;
 
 namespace {
 
+// Device address of g_device_status on the current device (looked up once per device).
+int *device_status_ptr() {
+    static int *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        addr[dev] = (int *)p;
+    }
+    return addr[dev];
+}
+
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 bool dim_ok(int64_t d) { return d == 64 || d == 128; }
 bool dtype_ok(int32_t t) { return t == DR_F32 || t == DR_BF16; }
@@ -50,7 +63,9 @@ extern "C" int dr_chunk_fwd_workspace_bytes(const dr_chunk_desc *desc, size_t *b
     ChunkProblem p{};
     const int rc = check_chunk_desc(desc, &p);
     if (rc != kOk) return rc;
-    *bytes = sizeof(float) * simt_workspace_floats(p.B, p.H, p.NC, p.C, p.dk, p.dv);
+    *bytes = chunk_tc_supported(p)
+                 ? 0
+                 : sizeof(float) * simt_workspace_floats(p.B, p.H, p.NC, p.C, p.dk, p.dv);
     return kOk;
 }
 
@@ -77,8 +92,13 @@ extern "C" int dr_chunk_fwd(const dr_chunk_desc *desc, const void *q, const void
 
     p.q = q; p.k = k; p.v = v; p.log_alpha = p.gate == DR_GATE_NONE ? nullptr : log_alpha;
     p.beta = beta; p.init_state = init_state; p.out = out; p.final_state = final_state;
-    const ChunkWorkspace ws = simt_workspace_carve(workspace, p.B, p.H, p.NC, p.C, p.dk, p.dv);
     if (p.NC == 0 && !final_state) return kOk;
+    if (chunk_tc_supported(p)) {
+        int *status = device_status_ptr();
+        if (!status) return kErrCuda;
+        return launch_chunk_tc(p, status, (cudaStream_t)stream);
+    }
+    const ChunkWorkspace ws = simt_workspace_carve(workspace, p.B, p.H, p.NC, p.C, p.dk, p.dv);
     return launch_chunk_simt(p, ws, (cudaStream_t)stream);
 }
 

@@ -150,3 +150,43 @@ def test_full_size_sampled_chains(dr, name, nsample):
                                       pick(d["log_alpha"]), pick(d["beta"]), s0)
         assert_close(out_h[b:b + 1, :, h:h + 1], o_ref, "bf16", f"out chain {(b, h)}")
         assert_close(fin_h[b:b + 1, h:h + 1], f_ref, "bf16", f"state chain {(b, h)}")
+
+
+# ------------------------------------------------------------ tensor-core path
+# bf16 inputs, d_k = d_v = 128, C = 64, scalar gate or none run on the fused tcgen05 kernel.
+@pytest.mark.parametrize("T", [1, 15, 63, 64, 65, 127, 129, 200])
+def test_tc_edge_lengths(dr, T):
+    d = inputs.chunk_inputs(2, T, 3, 128, 128, gate="scalar", dtype="bf16",
+                            init_state=True, seed=100 + T)
+    check(dr, d, "bf16")
+
+
+@pytest.mark.parametrize("gate", ["none", "scalar"])
+def test_tc_many_heads(dr, gate):
+    d = inputs.chunk_inputs(3, 333, 5, 128, 128, gate=gate, dtype="bf16", init_state=True,
+                            seed=7)
+    check(dr, d, "bf16")
+
+
+def test_tc_strong_decay(dr):
+    d = inputs.chunk_inputs(2, 300, 2, 128, 128, gate="scalar", dtype="bf16",
+                            init_state=True, seed=12, log_alpha_range=(0.0, 5.0))
+    check(dr, d, "bf16")
+
+
+def test_tc_fp32_output_strict(dr):
+    d = inputs.chunk_inputs(2, 500, 4, 128, 128, gate="scalar", dtype="bf16",
+                            init_state=True, seed=13)
+    check(dr, d, "bf16", out_dtype=torch.float32)
+
+
+def test_tc_deterministic(dr):
+    d = inputs.chunk_inputs(2, 300, 3, 128, 128, gate="scalar", dtype="bf16", seed=14)
+    o1, f1 = run(dr, d)
+    o2, f2 = run(dr, d)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
+def test_tc_needs_no_workspace(dr):
+    desc = dr.chunk_desc(8, 4096, 16, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_SCALAR, 64)
+    assert dr.workspace_bytes(desc) == 0
