@@ -45,8 +45,9 @@ def test_version_and_strerror(dr):
 
 
 def _desc(dr, **kw):
+    # per-channel gate: the CUDA-core path, which needs a workspace
     d = dict(B=2, T=100, H=3, dk=128, dv=128, in_dtype=dr.DR_BF16, out_dtype=dr.DR_BF16,
-             gate=dr.DR_GATE_SCALAR, chunk=64)
+             gate=dr.DR_GATE_CHANNEL, chunk=64)
     d.update(kw)
     return dr.ChunkDesc(**d)
 
@@ -55,6 +56,9 @@ def test_workspace_query(dr):
     n = dr.workspace_bytes(_desc(dr))
     assert n > 0 and n % 16 == 0
     assert dr.workspace_bytes(_desc(dr, T=0)) == 0
+    # the fused tensor-core path (bf16, d = 128, C = 64, scalar gate) needs none
+    assert dr.workspace_bytes(_desc(dr, gate=dr.DR_GATE_SCALAR)) == 0
+    assert dr.workspace_bytes(_desc(dr, gate=dr.DR_GATE_SCALAR, in_dtype=dr.DR_F32)) > 0
 
 
 @pytest.mark.parametrize("bad,status", [
@@ -86,7 +90,7 @@ def test_chunk_fwd_host_side_errors(dr):
     call = lambda a, wb=1 << 40: lib.dr_chunk_fwd(ctypes.byref(d), *a, wb, None)
     assert lib.dr_chunk_fwd(None, *args(), 0, None) == dr.DR_ERR_INVALID
     assert call(args(q=null)) == dr.DR_ERR_INVALID
-    assert call(args(la=null)) == dr.DR_ERR_INVALID          # scalar gate needs log_alpha
+    assert call(args(la=null)) == dr.DR_ERR_INVALID          # a gate needs log_alpha
     assert call(args(out=mis)) == dr.DR_ERR_INVALID
     assert call(args(ws=null)) == dr.DR_ERR_WORKSPACE
     assert call(args(), wb=16) == dr.DR_ERR_WORKSPACE
