@@ -11,22 +11,26 @@
 //
 //   X   = [Q; K] K^T                     (128 x 64)  raw q.k and k.k products
 //   P   = tril(exp(g_r - g_s) Q K^T)     (64 x 64)   read matrix, diagonal included
-//   A   = stril(beta_r exp(g_r - g_s) K K^T),  T = (I + A)^-1   (fp32 forward substitution)
+//   A   = stril(beta_r exp(g_r - g_s) K K^T),  T = (I + A)^-1   (fp32, blocked, see below)
 //   U^T = V^T (T diag beta)^T            (128 x 64)  = (T diag(beta) V)^T
 //   W^T = K^T (T diag(beta G))^T         (128 x 64)  = (T diag(beta) (K*G))^T
-//   D   = S^T [W; Q*G]^T                 (128 x 128) = [(W S)^T | (Q*G S)^T]
+//   D   = S^T [W; Q]^T                   (128 x 128) = [(W S)^T | (Q S)^T]
 //   E^T = U^T - (W S)^T
 //   S^T <- gamma S^T + (E^T diag(delta)) K                 (state carried to the next chunk)
-//   O^T = (Q*G S)^T + E^T P^T                              (chunk output)
+//   O^T = (Q S)^T diag(G) + E^T P^T                        (chunk output)
 //
 // Precision: P, E^T and E^T diag(delta) enter their products as a bf16 pair (high part and
 // the bf16 rounding of the remainder), so those products carry ~2^-16 relative error
-// instead of bf16's 2^-8; S^T, W, Q*G and the T factors enter as single bf16 operands.  A
+// instead of bf16's 2^-8; S^T, W and the T factors enter as single bf16 operands, Q exactly
+// (its decay G is applied to Q S in fp32).  A
 // rounding model of this arithmetic against the fp64 oracle puts the output error at
 // ~1e-2 x RMS (about 3e-2 without the pairs).
 //
 // One CTA per (b, h), 256 threads, the whole TMEM (512 columns): S^T [0,128), D [128,256),
-// X [256,320), U^T [320,384), W^T [384,448).  q, k, v tiles (64 tokens x 128, bf16) arrive
+// X [256,320) (later E^T P^T), U^T [320,384), W^T [384,448).  T = (I + A)^-1 is built by
+// 16 x 16 blocks: the diagonal blocks by right-looking substitution (one thread per column),
+// the blocks below them by warp-level TF32 mma.sync chains, T_ij = -T_ii sum_k A_ik T_kj,
+// one warp per block column (no cross-warp dependence).  q, k, v tiles (64 tokens x 128, bf16) arrive
 // by TMA with 128-byte swizzle into a double-buffered stage; the next chunk's tiles load
 // while the current chunk computes.  Operands written by the CUDA cores (P, T diag beta,
 // W, Q*G, S^T, E^T) use the same swizzled K-major layout; V and K tiles also serve as
@@ -50,21 +54,28 @@ constexpr int kThreads = 256;
 constexpr uint32_t kStageBytes = 49152;
 // stage layout: [Q kb0 | K kb0 | Q kb1 | K kb1 | V kb0 | V kb1], 8 KB each (64 x 64 bf16)
 constexpr uint32_t OFF_K0 = 8192, OFF_V0 = 32768;
-constexpr uint32_t SM_B2 = 2 * kStageBytes;   // [W; Q*G] 128 x 128 K-major, 2 K-blocks;
-                                              // after its MMA: low parts of E^T, E^T diag(delta)
-constexpr uint32_t SM_ST = SM_B2 + 32768;     // S^T 128 x 128 K-major; fp32 T during the solve
-constexpr uint32_t SM_ET = SM_ST + 32768;     // E^T (high part) 128 x 64; fp32 A during the solve
-constexpr uint32_t SM_ET2 = SM_ET + 16384;    // E^T diag(delta) (high); T diag beta (+G) before
+constexpr uint32_t SM_W = 2 * kStageBytes;    // W 64 x 128 K-major (2 K-blocks of 8 KB);
+                                              // after its MMA: low part of E^T
+constexpr uint32_t SM_ST = SM_W + 16384;      // S^T 128 x 128 K-major; fp32 T during the solve;
+                                              // after its MMA: low part of E^T diag(delta)
+constexpr uint32_t SM_ET = SM_ST + 32768;     // E^T (high) 128 x 64
+constexpr uint32_t SM_ET2 = SM_ET + 16384;    // E^T diag(delta) (high); fp32 A during the solve,
+                                              // then T diag beta (+G)
+                                              // SM_ET..SM_ET2 + 16 KB: the output tile at the end
 constexpr uint32_t SM_P = SM_ET2 + 16384;     // P (high part) 64 x 64 K-major
 constexpr uint32_t SM_PLO = SM_P + 8192;      // P (low part)
-constexpr uint32_t SM_ETLO = SM_B2, SM_ET2LO = SM_B2 + 16384;
-constexpr uint32_t SM_SMALL = SM_PLO + 8192;  // g, G, delta, beta: fp32 [64] each
-constexpr uint32_t SM_TOTAL = SM_SMALL + 1024;
-constexpr uint32_t TM_S = 0, TM_D = 128, TM_X = 256, TM_U = 320, TM_W = 384;
+constexpr uint32_t SM_ETLO = SM_W, SM_ET2LO = SM_ST, SM_OUT = SM_ET;
+constexpr uint32_t SM_SMALL = SM_PLO + 8192;  // per-token vectors and solve scratch
+constexpr uint32_t SM_A = SM_ET2, SM_TB = SM_ET2;   // fp32 A, then T diag beta (+G)
+constexpr uint32_t SM_TOTAL = SM_SMALL + 8192;
+constexpr uint32_t TM_S = 0, TM_D = 128, TM_X = 256, TM_U = 320, TM_W = 384, TM_PE = 448;
+// TM_D: [ (W S)^T | (Q S)^T ];  TM_X: [Q; K] K^T;  TM_PE: E^T P^T
 constexpr long long kWaitCycles = 2000000000LL;   // ~1 s at the loaded SM clock
+// Largest in-chunk log-decay span for which exp(g_r - g_s) is formed as a product of two
+// exponentials around the chunk's middle token (both factors stay within fp32 range).
+constexpr float kFactorSpan = 80.f;
 
 constexpr uint32_t ID_KK_N64 = idesc_bf16(128, 64, false, false);
-constexpr uint32_t ID_KK_N128 = idesc_bf16(128, 128, false, false);
 constexpr uint32_t ID_MK_N64 = idesc_bf16(128, 64, true, false);
 constexpr uint32_t ID_KM_N128 = idesc_bf16(128, 128, false, true);
 
@@ -72,7 +83,6 @@ struct TcArgs {
     const float *log_alpha;
     const __nv_bfloat16 *beta;
     const float *init_state;
-    void *out;
     float *final_state;
     int *status;
     int T, H, NC;
@@ -100,38 +110,164 @@ __device__ __forceinline__ void pack_hi_lo(float a, float b, uint32_t &hi, uint3
     lo = pack_bf16(a - __bfloat162float(ha), b - __bfloat162float(hb));
 }
 
-__device__ __forceinline__ uint4 scale_bf16x8(uint4 raw, float s) {
-    uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+// d += a (16 x 8, row) * b (8 x 8, col), TF32 operands, fp32 accumulate (one warp).
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// acc (16 x 16, mma.sync C fragment) += L (16 x 16 nk) * R (16 nk x 16); one warp.
+// L(r, k) and R(k, n) return fp32 elements; operands are rounded to TF32.
+template <class FL, class FR>
+__device__ __forceinline__ void warp_mm16(float (&acc)[2][4], FL L, FR R, int nk, int g, int t4) {
+    for (int kt = 0; kt < 2 * nk; ++kt) {
+        const int kc = 8 * kt;
+        const uint32_t af[4] = {to_tf32(L(g, kc + t4)), to_tf32(L(g + 8, kc + t4)),
+                                to_tf32(L(g, kc + t4 + 4)), to_tf32(L(g + 8, kc + t4 + 4))};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[i]));
-        w[i] = pack_bf16(f.x * s, f.y * s);
+        for (int nt = 0; nt < 2; ++nt)
+            mma_tf32_16x8x8(acc[nt], af, to_tf32(R(kc + t4, 8 * nt + g)),
+                            to_tf32(R(kc + t4 + 4, 8 * nt + g)));
     }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+// Writes sign * acc through st(r, n, v).
+template <class FS>
+__device__ __forceinline__ void warp_store16(const float (&acc)[2][4], float sign, FS st, int g, int t4) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int n = 8 * nt + 2 * t4;
+        st(g, n, sign * acc[nt][0]);
+        st(g, n + 1, sign * acc[nt][1]);
+        st(g + 8, n, sign * acc[nt][2]);
+        st(g + 8, n + 1, sign * acc[nt][3]);
+    }
+}
+
+// Element (r, s) of the fp32 A matrix: rows of 64, 16-byte groups XOR-swizzled by r % 16.
+__device__ __forceinline__ int a_index(int r, int s) {
+    return r * 64 + ((((s >> 2) ^ (r & 15)) << 2) | (s & 3));
+}
+
+// T = (I + A)^-1 for a strictly lower-triangular 64 x 64 A (fp32), T stored [64][65].
+//   1. the four diagonal 16 x 16 blocks by right-looking substitution, four threads per
+//      column (each owns four rows; the pivot row's value is broadcast by a shuffle);
+//   2. T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (two warps);
+//   3. lower-left 32 x 32 quarter: M = A[32:64, 0:32] T[0:32, 0:32], then
+//      T[32:64, 0:32] = -T[32:64, 32:64] M (four warps, one 16 x 16 tile each).
+// Products use TF32 mma.sync with fp32 accumulation.  M needs 1024 floats.  Called by all
+// 256 threads; starts after and ends with a barrier.
+__device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, float *M, int tid) {
+    auto a = [&](int r, int s) { return A[a_index(r, s)]; };
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+    {
+        const int o = 16 * (tid >> 6), c = (tid >> 2) & 15, part = tid & 3;
+        const int owner = lane & ~3;
+        float y[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) y[m] = (part + 4 * m == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < 15; ++s2) {
+            const float xs = __shfl_sync(0xffffffffu, y[s2 >> 2], owner | (s2 & 3));
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int r = part + 4 * m;
+                if (r > s2) y[m] = fmaf(-a(o + r, o + s2), xs, y[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) T[(o + part + 4 * m) * 65 + o + c] = y[m];
+        // zero the six blocks above the diagonal: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+        for (int idx = tid; idx < 6 * 256; idx += kThreads) {
+            const int blk = idx >> 8, e = idx & 255;
+            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            T[(16 * bi + (e >> 4)) * 65 + 16 * bj + (e & 15)] = 0.f;
+        }
+    }
+    __syncthreads();
+    if (warp < 2) {
+        const int i = 2 * warp + 1, j = 2 * warp;
+        float *Ms = M + 256 * warp;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        warp_mm16(acc, [&](int r, int k) { return a(16 * i + r, 16 * j + k); },
+                  [&](int k, int n) { return T[(16 * j + k) * 65 + 16 * j + n]; }, 1, g, t4);
+        warp_store16(acc, 1.f, [&](int r, int n, float v) { Ms[r * 16 + n] = v; }, g, t4);
+        __syncwarp();
+        float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        warp_mm16(acc2, [&](int r, int k) { return T[(16 * i + r) * 65 + 16 * i + k]; },
+                  [&](int k, int n) { return Ms[k * 16 + n]; }, 1, g, t4);
+        warp_store16(acc2, -1.f, [&](int r, int n, float v) { T[(16 * i + r) * 65 + 16 * j + n] = v; },
+                     g, t4);
+    }
+    __syncthreads();
+    if (warp < 4) {   // M tile (rb, cb) = sum_{k = cb}^{1} A_{rb,k} T_{k,cb},  rb = 2 + w/2, cb = w%2
+        const int rb = 2 + (warp >> 1), cb = warp & 1;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        warp_mm16(acc, [&](int r, int k) { return a(16 * rb + r, 16 * cb + k); },
+                  [&](int k, int n) { return T[(16 * cb + k) * 65 + 16 * cb + n]; }, 2 - cb, g, t4);
+        float *Mt = M + 256 * warp;
+        warp_store16(acc, 1.f, [&](int r, int n, float v) { Mt[r * 16 + n] = v; }, g, t4);
+    }
+    __syncthreads();
+    if (warp < 4) {   // T_{rb,cb} = -sum_{k = 2}^{rb} T_{rb,k} M_{k,cb}
+        const int rb = 2 + (warp >> 1), cb = warp & 1;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        warp_mm16(acc, [&](int r, int k) { return T[(16 * rb + r) * 65 + 32 + k]; },
+                  [&](int k, int n) { return M[256 * (((k >> 4) << 1) | cb) + (k & 15) * 16 + n]; },
+                  rb - 1, g, t4);
+        warp_store16(acc, -1.f, [&](int r, int n, float v) { T[(16 * rb + r) * 65 + 16 * cb + n] = v; },
+                     g, t4);
+    }
+    __syncthreads();
 }
 
 template <typename Tout, int GATE>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                const __grid_constant__ CUtensorMap tv, const TcArgs a) {
+                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                const TcArgs a) {
     extern __shared__ unsigned char dsm_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
-    __shared__ uint64_t bar_tma[2], bar_mma;
+    // mbarriers: TMA stages, and one per MMA group (each completes once per chunk)
+    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_s;
     __shared__ uint32_t tmem_base_s;
-    __shared__ int abort_s;
+    __shared__ int abort_s, factored_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
     const int row = 32 * quarter + lane;        // the TMEM lane this thread reads and writes
     const int bh = blockIdx.x;
     const int h = bh % a.H, b = bh / a.H;
-    float *sG = reinterpret_cast<float *>(sm + SM_SMALL);
-    float *sGam = sG + 64, *sDel = sG + 128, *sBeta = sG + 192;
+    constexpr int kTmaThread = 224;              // lane 0 of warp 7 issues the TMA loads
+    float *sG = reinterpret_cast<float *>(sm + SM_SMALL);   // g_r (cumulative log decay)
+    float *sGam = sG + 64;     // exp(g_r)
+    float *sDel = sG + 128;    // exp(g_63 - g_r)
+    float *sBeta = sG + 192;   // beta_r
+    float *sE = sG + 256;      // exp(g_r - g_31)
+    float *sF = sG + 320;      // exp(g_31 - g_r)
+    float *sM = sG + 384;      // 1024 floats of solve scratch
+    // raw gate words of two chunks: [slot][beta word | log alpha][64 tokens]
+    uint32_t *sGate = reinterpret_cast<uint32_t *>(sG + 1408);
+    float *sGamOut = sG + 1664;   // exp(g_r) of the chunk whose outputs are pending
+    constexpr int kOutBoxes = sizeof(Tout) == 2 ? 2 : 4;   // 128-byte rows per output box
+    constexpr bool kWideOut = sizeof(Tout) == 4;           // fp32 tile covers SM_ET and SM_ET2
 
     if (tid == 0) {
         mbar_init(&bar_tma[0], 1);
         mbar_init(&bar_tma[1], 1);
-        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_x, 1);
+        mbar_init(&bar_uw, 1);
+        mbar_init(&bar_d, 1);
+        mbar_init(&bar_s, 1);
         abort_s = 0;
         fence_mbar_init();
     }
@@ -157,9 +293,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tmem_wait_st();
     }
 
-    auto issue_tma = [&](int c, int s) {
+    auto issue_tma = [&](int c) {
+        const int s = c & 1;
         unsigned char *st = sm + s * kStageBytes;
-        fence_proxy_async();
         mbar_arrive_expect_tx(&bar_tma[s], kStageBytes);
         const int t0 = c * 64;
         for (int kb = 0; kb < 2; ++kb) {
@@ -168,57 +304,99 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             tma_load_4d(st + OFF_V0 + kb * 8192, &tv, &bar_tma[s], 64 * kb, h, t0, b);
         }
     };
-    if (tid == 0) issue_tma(0, 0);
+    // beta (the aligned 32-bit word holding it) and log alpha of chunk c, two tokens per
+    // lane of warp 0, copied asynchronously one chunk ahead
+    const size_t ntok = (size_t)gridDim.x * a.T;   // B * T * H beta values
+    auto issue_gate = [&](int c) {
+        uint32_t *dst = sGate + (c & 1) * 128;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 2 * lane + e, t = c * 64 + r;
+            const bool valid = t < a.T;
+            const size_t tok = valid ? ((size_t)b * a.T + t) * a.H + h : 0;
+            if (valid && tok + 1 == ntok && ((2 * tok) & 3) == 0) {
+                // the 32-bit word would run past the end of beta: load this value alone
+                dst[r] = (uint32_t)__bfloat16_as_ushort(a.beta[tok]);
+            } else {
+                cp_async4(dst + r, reinterpret_cast<const char *>(a.beta) + ((2 * tok) & ~(size_t)3),
+                          valid ? 4 : 0);
+            }
+            cp_async4(dst + 64 + r, GATE == 1 ? (const void *)(a.log_alpha + tok) : (const void *)a.beta,
+                      (GATE == 1 && valid) ? 4 : 0);
+        }
+        cp_async_commit();
+    };
+    if (tid == kTmaThread) issue_tma(0);
+    if (warp == 0) issue_gate(0);
 
-    uint32_t mma_phase = 0;
-    int last_c = -1;                       // chunk whose prefetch may still be in flight
-    bool mma_outstanding = false;
+    bool out_pending = false;       // chunk whose outputs wait in TMEM for the write-out
+    bool store_outstanding = false; // a TMA store may still be reading SM_OUT
+    bool tma_pending = true;        // a TMA load was issued and not yet waited for
+    int last_tma_c = 0;             // chunk of the most recent TMA load
+    bool s_outstanding = false;     // MMA group S (state update, E^T P^T) committed, not waited
+    int cur_t0 = 0;                 // t0 of the chunk whose outputs are pending
     auto fail = [&]() {
         abort_s = 1;
         atomicExch(a.status, kErrTimeout);
     };
-    auto wait_mma = [&]() {
-        const bool ok = wait_cycles(&bar_mma, mma_phase);
-        mma_phase ^= 1;
-        if (ok) mma_outstanding = false; else fail();
+    auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
+        if (!wait_cycles(bar, parity)) fail();
         tc_fence_after();
+    };
+
+    // Output of the chunk at t0: o = G_r (Q S)^T + E^T P^T, staged row-major at SM_OUT in
+    // 128-byte swizzled boxes and written by TMA (rows past T are skipped).  Needs group S.
+    auto write_out = [&](int t0) {
+        float o[32], pe[32];
+        tmem_ld32(tm + TM_D + 64 + 32 * half, o);
+        tmem_ld32(tm + TM_PE + 32 * half, pe);
+        tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 32; ++u) o[u] = fmaf(sGamOut[32 * half + u], o[u], pe[u]);
+        const int j = row;
+        if (sizeof(Tout) == 2) {
+            unsigned char *dst = sm + SM_OUT + (j >> 6) * 8192;
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, j & 63)) =
+                    __float2bfloat16_rn(o[u]);
+        } else {
+            unsigned char *dst = sm + SM_OUT + (j >> 5) * 8192;
+            const int cj = j & 31;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int r = 32 * half + u;
+                *reinterpret_cast<float *>(dst + r * 128 + ((((cj >> 2) ^ (r & 7)) & 7) << 4) +
+                                           ((cj & 3) << 2)) = o[u];
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
+#pragma unroll
+            for (int kb = 0; kb < kOutBoxes; ++kb)
+                tma_store_4d(&to, sm + SM_OUT + kb * 8192, cols * kb, h, t0, b);
+            bulk_commit();
+            store_outstanding = true;
+            if (kWideOut) {   // the fp32 tile also covers SM_A, written next by P/A
+                bulk_wait_read_all();
+                store_outstanding = false;
+            }
+        }
+        if (kWideOut) __syncthreads();
     };
 
     for (int c = 0; c < a.NC; ++c) {
         const int s = c & 1;
+        const uint32_t par = c & 1;               // parity of this chunk's MMA barriers
         unsigned char *st = sm + s * kStageBytes;
         const int t0 = c * 64;
-        const int Lc = min(64, a.T - t0);
-        last_c = c;
 
-        // ---- next chunk's tiles; beta and the cumulative log decay of this chunk
-        if (tid == 0 && c + 1 < a.NC) issue_tma(c + 1, s ^ 1);
-        if (tid < 64) {
-            const bool valid = tid < Lc;
-            const size_t tok = ((size_t)b * a.T + t0 + tid) * a.H + h;
-            float g = (GATE == 1 && valid) ? a.log_alpha[tok] : 0.f;
-            sBeta[tid] = valid ? __bfloat162float(a.beta[tok]) : 0.f;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, g, o);
-                if (lane >= o) g += y;
-            }
-            sG[tid] = g;
-        }
-        __syncthreads();
-        if (tid >= 32 && tid < 64) sG[tid] += sG[31];
-        __syncthreads();
-        if (tid < 64) {
-            const float g = sG[tid];
-            sGam[tid] = __expf(g);
-            sDel[tid] = __expf(sG[63] - g);
-        }
-        const float gamma = __expf(sG[63]);
+        // ---- 1. this chunk's tiles; X = [Q; K] K^T
         if (!wait_cycles(&bar_tma[s], (c >> 1) & 1)) fail();
-        __syncthreads();
-        if (abort_s) break;
-
-        // ---- X = [Q; K] K^T
+        tma_pending = false;
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
@@ -227,33 +405,91 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 mma_bf16(tmem_base_s + TM_X, smem_desc_sw128(smem_u32(st + o), 16, 1024),
                          smem_desc_sw128(smem_u32(st + OFF_K0 + o), 16, 1024), ID_KK_N64, ks > 0);
             }
-            mma_commit(&bar_mma);
+            mma_commit(&bar_x);
         }
-        mma_outstanding = true;
-        // Q*G into rows 64..127 of [W; Q*G] (same swizzle phase: (64 + r) % 8 == r % 8)
-        for (int task = tid; task < 1024; task += kThreads) {
-            const int r = task >> 4, kb = (task >> 3) & 1, ch = task & 7;
-            const uint32_t off = kb * 16384 + r * 128 + (ch << 4);
-            const uint4 raw = *reinterpret_cast<const uint4 *>(st + off);
-            *reinterpret_cast<uint4 *>(sm + SM_B2 + 64 * 128 + off) = scale_bf16x8(raw, sGam[r]);
+        // ---- 2. cumulative log decay of this chunk (warp 0; its gates arrived by cp.async)
+        if (warp == 0) {
+            cp_async_wait_all();
+            __syncwarp();
+            const uint32_t *gw = sGate + s * 128;
+            float l[2], bt[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = 2 * lane + e, t = t0 + r;
+                const size_t tok = t < a.T ? ((size_t)b * a.T + t) * a.H + h : 0;
+                const uint32_t wd = gw[r];
+                const uint16_t hb = (uint16_t)(((2 * tok) & 2) ? (wd >> 16) : (wd & 0xffffu));
+                bt[e] = __bfloat162float(__ushort_as_bfloat16(hb));
+                l[e] = __uint_as_float(gw[64 + r]);
+            }
+            __syncwarp();
+            if (c + 1 < a.NC) issue_gate(c + 1);
+            float p = l[0] + l[1];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, p, o);
+                if (lane >= o) p += y;
+            }
+            const float g1 = p, g0 = p - l[1];                     // g_{2l}, g_{2l+1}
+            const float glast = __shfl_sync(0xffffffffu, g1, 31);  // g_63
+            const float gmid = __shfl_sync(0xffffffffu, g1, 15);   // g_31
+            const float gfirst = __shfl_sync(0xffffffffu, g0, 0);  // g_0
+            const int r = 2 * lane;
+            sG[r] = g0; sG[r + 1] = g1;
+            sBeta[r] = bt[0]; sBeta[r + 1] = bt[1];
+            sGam[r] = __expf(g0); sGam[r + 1] = __expf(g1);
+            sDel[r] = __expf(glast - g0); sDel[r + 1] = __expf(glast - g1);
+            const bool fac = gfirst - glast < kFactorSpan;
+            if (fac) {
+                sE[r] = __expf(g0 - gmid); sE[r + 1] = __expf(g1 - gmid);
+                sF[r] = __expf(gmid - g0); sF[r + 1] = __expf(gmid - g1);
+            }
+            if (lane == 0) factored_s = fac;
         }
-        wait_mma();
+        // ---- 3. previous chunk: wait for its state update, write its outputs; then the
+        //         stage it used is free for the next chunk's tiles
+        if (s_outstanding) {
+            wait_bar(&bar_s, par ^ 1);
+            s_outstanding = false;
+        }
+        __syncthreads();            // gate vectors published; previous chunk's MMAs done
+        if (abort_s) break;
+        if (out_pending) write_out(cur_t0);
+        if (tid == kTmaThread && c + 1 < a.NC) {
+            issue_tma(c + 1);
+            tma_pending = true;
+            last_tma_c = c + 1;
+        }
+        // keep this chunk's exp(g_r) for its deferred write-out (write_out above ended with
+        // a barrier, so no thread still reads the previous values)
+        if (tid < 64) sGamOut[tid] = sGam[tid];
 
-        // ---- P (bf16, rows 0..63 of X) and A (fp32, rows 64..127 of X)
+        // ---- 4. P (rows 0..63 of X, bf16 high/low) and A (rows 64..127 of X, fp32)
+        wait_bar(&bar_x, par);
         {
             float x[32];
             tmem_ld32(tm + TM_X + 32 * half, x);
             tmem_wait_ld();
             const int c0 = 32 * half;
-            if (quarter < 2) {
-                const int r = row;
+            const bool fac = factored_s;
+            const int r = quarter < 2 ? row : row - 64;
+            float dec[32];   // exp(g_r - g_s), s = c0 + u
+            if (fac) {
+                const float er = sE[r];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) dec[u] = er * sF[c0 + u];
+            } else {
                 const float gr = sG[r];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) dec[u] = __expf(fminf(gr - sG[c0 + u], 0.f));
+            }
+            if (quarter < 2) {
                 uint32_t pk[16], pl[16];
 #pragma unroll
                 for (int u = 0; u < 32; u += 2) {
                     const int s0 = c0 + u;
-                    const float p0 = s0 <= r ? __expf(gr - sG[s0]) * x[u] : 0.f;
-                    const float p1 = s0 + 1 <= r ? __expf(gr - sG[s0 + 1]) * x[u + 1] : 0.f;
+                    const float p0 = s0 <= r ? dec[u] * x[u] : 0.f;
+                    const float p1 = s0 + 1 <= r ? dec[u + 1] * x[u + 1] : 0.f;
                     pack_hi_lo(p0, p1, pk[u >> 1], pl[u >> 1]);
                 }
 #pragma unroll
@@ -265,13 +501,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                         make_uint4(pl[4 * q4], pl[4 * q4 + 1], pl[4 * q4 + 2], pl[4 * q4 + 3]);
                 }
             } else {
-                const int r = row - 64;
-                const float gr = sG[r], br = sBeta[r];
-                float *sA = reinterpret_cast<float *>(sm + SM_ET);
+                const float br = sBeta[r];
+                float *sA = reinterpret_cast<float *>(sm + SM_A);
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int s2 = c0 + u;
-                    sA[r * 64 + (s2 ^ (r & 31))] = s2 < r ? br * __expf(gr - sG[s2]) * x[u] : 0.f;
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    float4 v4;
+                    const int s0 = c0 + 4 * q4;
+                    v4.x = s0 < r ? br * dec[4 * q4] * x[4 * q4] : 0.f;
+                    v4.y = s0 + 1 < r ? br * dec[4 * q4 + 1] * x[4 * q4 + 1] : 0.f;
+                    v4.z = s0 + 2 < r ? br * dec[4 * q4 + 2] * x[4 * q4 + 2] : 0.f;
+                    v4.w = s0 + 3 < r ? br * dec[4 * q4 + 3] * x[4 * q4 + 3] : 0.f;
+                    *reinterpret_cast<float4 *>(sA + a_index(r, s0)) = v4;
                 }
             }
         }
@@ -279,28 +519,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tc_fence_before();
         __syncthreads();
 
-        // ---- T = (I + A)^-1: column j by the 4 lanes tid/4 == j,
-        //      T_rj = delta_rj - sum_{j <= s < r} A_rs T_sj  (fp32, stride 65)
-        {
-            const float *sA = reinterpret_cast<const float *>(sm + SM_ET);
-            float *sT = reinterpret_cast<float *>(sm + SM_ST);
-            const int j = tid >> 2, part = tid & 3;
-            for (int r = part; r < 64; r += 4) sT[r * 65 + j] = (r == j) ? 1.f : 0.f;
-            __syncwarp();
-            for (int r = 1; r < 64; ++r) {
-                float acc = 0.f;
-                if (j < r)
-                    for (int s2 = j + part; s2 < r; s2 += 4)
-                        acc += sA[r * 64 + (s2 ^ (r & 31))] * sT[s2 * 65 + j];
-                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                if (part == 0 && j < r) sT[r * 65 + j] = -acc;
-                __syncwarp();
-            }
-        }
-        __syncthreads();
+        // ---- 5. T = (I + A)^-1 (fp32, [64][65] at SM_ST)
+        solve_unit_lower64(reinterpret_cast<const float *>(sm + SM_A),
+                           reinterpret_cast<float *>(sm + SM_ST), sM, tid);
 
-        // ---- T diag(beta) and T diag(beta G) as bf16 K-major operands (64 x 64)
+        // ---- 6. T diag(beta) and T diag(beta G) as bf16 K-major operands (64 x 64)
         {
             const float *sT = reinterpret_cast<const float *>(sm + SM_ST);
             for (int task = tid; task < 512; task += kThreads) {
@@ -315,48 +538,30 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     p2[u >> 1] = pack_bf16(t0v * sGam[s0], t1v * sGam[s0 + 1]);
                 }
                 const uint32_t off = sw128_off(r, 8 * ch);
-                *reinterpret_cast<uint4 *>(sm + SM_ET2 + off) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-                *reinterpret_cast<uint4 *>(sm + SM_ET2 + 8192 + off) =
+                *reinterpret_cast<uint4 *>(sm + SM_TB + off) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+                *reinterpret_cast<uint4 *>(sm + SM_TB + 8192 + off) =
                     make_uint4(p2[0], p2[1], p2[2], p2[3]);
             }
         }
         fence_proxy_async();
         __syncthreads();
 
-        // ---- U^T = V^T (T diag beta)^T,  W^T = K^T (T diag(beta G))^T
+        // ---- 7. U^T = V^T (T diag beta)^T,  W^T = K^T (T diag(beta G))^T
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 mma_bf16(tmem_base_s + TM_U, smem_desc_sw128(smem_u32(st + OFF_V0 + ks * 2048), 8192, 1024),
-                         smem_desc_sw128(smem_u32(sm + SM_ET2 + ks * 32), 16, 1024), ID_MK_N64, ks > 0);
+                         smem_desc_sw128(smem_u32(sm + SM_TB + ks * 32), 16, 1024), ID_MK_N64, ks > 0);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 mma_bf16(tmem_base_s + TM_W, smem_desc_sw128(smem_u32(st + OFF_K0 + ks * 2048), 16384, 1024),
-                         smem_desc_sw128(smem_u32(sm + SM_ET2 + 8192 + ks * 32), 16, 1024), ID_MK_N64, ks > 0);
-            mma_commit(&bar_mma);
+                         smem_desc_sw128(smem_u32(sm + SM_TB + 8192 + ks * 32), 16, 1024), ID_MK_N64, ks > 0);
+            mma_commit(&bar_uw);
         }
-        mma_outstanding = true;
-        wait_mma();
-        // W (rows 0..63 of [W; Q*G]) from W^T: lane i = key channel, columns = tokens r
+        // ---- 8. meanwhile: S^T to bf16 (MMA operand at SM_ST); S^T <- gamma S^T in TMEM
         {
-            float w[32];
-            tmem_ld32(tm + TM_W + 32 * half, w);
-            tmem_wait_ld();
-            const int i = row, kb = i >> 6, ci = i & 63;
-            unsigned char *dst = sm + SM_B2 + kb * 16384;
-#pragma unroll
-            for (int u = 0; u < 32; ++u)
-                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, ci)) =
-                    __float2bfloat16_rn(w[u]);
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        if (abort_s) break;
-
-        // ---- S^T to bf16 (MMA operand); S^T <- gamma S^T in TMEM
-        {
+            const float gamma = sGam[63];
             float v[32];
             unsigned char *dst = sm + SM_ST + half * 16384;
             for (int part = 0; part < 2; ++part) {
@@ -376,25 +581,46 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             }
             tmem_wait_st();
         }
+        // ---- 9. W from W^T: lane i = key channel, columns = tokens r
+        wait_bar(&bar_uw, par);
+        {
+            float w[32];
+            tmem_ld32(tm + TM_W + 32 * half, w);
+            tmem_wait_ld();
+            const int i = row, kb = i >> 6, ci = i & 63;
+            unsigned char *dst = sm + SM_W + kb * 8192;
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, ci)) =
+                    __float2bfloat16_rn(w[u]);
+        }
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
+        if (abort_s) break;
 
-        // ---- D = S^T [W; Q*G]^T
+        // ---- 10. D = S^T [W; Q]^T  (Q straight from the stage)
         if (tid == 0) {
+            if (store_outstanding) {   // the previous output tile must have left SM_OUT
+                bulk_wait_read_all();  // before E^T is written there
+                store_outstanding = false;
+            }
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_bf16(tmem_base_s + TM_D, smem_desc_sw128(smem_u32(sm + SM_ST + o), 16, 1024),
-                         smem_desc_sw128(smem_u32(sm + SM_B2 + o), 16, 1024), ID_KK_N128, ks > 0);
+                const uint64_t adesc = smem_desc_sw128(smem_u32(sm + SM_ST + o), 16, 1024);
+                mma_bf16(tmem_base_s + TM_D, adesc,
+                         smem_desc_sw128(smem_u32(sm + SM_W + (ks >> 2) * 8192 + (ks & 3) * 32), 16, 1024),
+                         ID_KK_N64, ks > 0);
+                mma_bf16(tmem_base_s + TM_D + 64, adesc, smem_desc_sw128(smem_u32(st + o), 16, 1024),
+                         ID_KK_N64, ks > 0);
             }
-            mma_commit(&bar_mma);
+            mma_commit(&bar_d);
         }
-        mma_outstanding = true;
-        wait_mma();
+        wait_bar(&bar_d, par);
 
-        // ---- E^T = U^T - (W S)^T, and E^T diag(delta)
+        // ---- 11. E^T = U^T - (W S)^T, and E^T diag(delta)  (bf16 high/low pairs)
         {
             float ws[32], uu[32];
             tmem_ld32(tm + TM_D + 32 * half, ws);
@@ -427,7 +653,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tc_fence_before();
         __syncthreads();
 
-        // ---- S^T += (E^T diag delta) K ;  O^T = (Q*G S)^T + E^T P^T  (high/low pairs)
+        // ---- 12. S^T += (E^T diag delta) K ;  PE = E^T P^T  (high/low pairs); completes
+        //          while the next chunk starts, whose step 3 waits for it
         if (tid == 0) {
             tc_fence_after();
             const uint32_t e2[2] = {SM_ET2, SM_ET2LO};
@@ -442,37 +669,27 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             for (int part = 0; part < 3; ++part)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem_base_s + TM_D + 64, smem_desc_sw128(smem_u32(sm + ea[part] + ks * 32), 16, 1024),
-                             smem_desc_sw128(smem_u32(sm + pb[part] + ks * 32), 16, 1024), ID_KK_N64, 1);
-            mma_commit(&bar_mma);
+                    mma_bf16(tmem_base_s + TM_PE, smem_desc_sw128(smem_u32(sm + ea[part] + ks * 32), 16, 1024),
+                             smem_desc_sw128(smem_u32(sm + pb[part] + ks * 32), 16, 1024), ID_KK_N64,
+                             (part | ks) != 0);
+            mma_commit(&bar_s);
         }
-        mma_outstanding = true;
-        wait_mma();
-
-        // ---- outputs: lane j = value channel, columns = tokens
-        {
-            float o[32];
-            tmem_ld32(tm + TM_D + 64 + 32 * half, o);
-            tmem_wait_ld();
-            Tout *out = reinterpret_cast<Tout *>(a.out);
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int r = 32 * half + u;
-                if (r < Lc) out[(((size_t)b * a.T + t0 + r) * a.H + h) * 128 + row] = from_f32<Tout>(o[u]);
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (abort_s) break;
+        s_outstanding = true;
+        out_pending = true;
+        cur_t0 = t0;
     }
 
+    if (!abort_s && s_outstanding) {
+        wait_bar(&bar_s, (a.NC - 1) & 1);
+        s_outstanding = false;
+        __syncthreads();
+        if (!abort_s && out_pending) write_out(cur_t0);
+    }
     if (abort_s) {
         // Drain this CTA's own asynchronous work (bounded) before TMEM is freed.
-        if (tid == 0) {
-            if (last_c >= 0 && last_c + 1 < a.NC)
-                wait_cycles(&bar_tma[(last_c + 1) & 1], ((last_c + 1) >> 1) & 1);
-            if (mma_outstanding) wait_cycles(&bar_mma, mma_phase);
-        }
+        if (tid == kTmaThread && tma_pending)
+            wait_cycles(&bar_tma[last_tma_c & 1], (last_tma_c >> 1) & 1);
+        if (tid == 0 && s_outstanding) wait_cycles(&bar_s, (a.NC - 1) & 1);
     } else if (a.final_state) {
         float v[32];
         for (int part = 0; part < 2; ++part) {
@@ -483,6 +700,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             for (int u = 0; u < 32; ++u) a.final_state[((size_t)bh * 128 + i0 + u) * 128 + row] = v[u];
         }
     }
+    if (warp == 0) cp_async_wait_all();
+    if (tid == 0 && store_outstanding) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -504,28 +723,30 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// [B, T, H, 128] bf16 viewed as 4-D (128, H, T, B); box 64 x 1 x 64 x 1, 128-byte swizzle,
-// rows past T read as zeros.
-bool make_map(CUtensorMap *m, const void *base, int64_t B, int64_t T, int64_t H) {
+// [B, T, H, 128] viewed as 4-D (128, H, T, B); box of 128-byte rows x 1 x 64 tokens x 1,
+// 128-byte swizzle; loads read rows past T as zeros, stores skip them.
+bool make_map(CUtensorMap *m, const void *base, int64_t B, int64_t T, int64_t H, bool fp32) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
+    const cuuint64_t e = fp32 ? 4 : 2;
     cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-    cuuint64_t strides[3] = {256, (cuuint64_t)H * 256, (cuuint64_t)(T * H) * 256};
-    cuuint32_t box[4] = {64, 1, 64, 1};
+    cuuint64_t strides[3] = {128 * e, (cuuint64_t)H * 128 * e, (cuuint64_t)(T * H) * 128 * e};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / e), 1, 64, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+               const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename Tout, int GATE>
-int launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const TcArgs &ta,
-             unsigned grid, cudaStream_t stream) {
+int launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+             const CUtensorMap &mo, const TcArgs &ta, unsigned grid, cudaStream_t stream) {
     const int smem = (int)SM_TOTAL + 1024;
     if (cudaFuncSetAttribute(chunk_tc_kernel<Tout, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
         return kErrCuda;
-    chunk_tc_kernel<Tout, GATE><<<grid, kThreads, smem, stream>>>(mq, mk, mv, ta);
+    chunk_tc_kernel<Tout, GATE><<<grid, kThreads, smem, stream>>>(mq, mk, mv, mo, ta);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
@@ -537,18 +758,19 @@ bool chunk_tc_supported(const ChunkProblem &p) {
 }
 
 int launch_chunk_tc(const ChunkProblem &p, int *status_word, cudaStream_t stream) {
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, p.q, p.B, p.T, p.H) || !make_map(&mk, p.k, p.B, p.T, p.H) ||
-        !make_map(&mv, p.v, p.B, p.T, p.H))
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, p.q, p.B, p.T, p.H, false) || !make_map(&mk, p.k, p.B, p.T, p.H, false) ||
+        !make_map(&mv, p.v, p.B, p.T, p.H, false) ||
+        !make_map(&mo, p.out, p.B, p.T, p.H, !p.out_bf16))
         return kErrCuda;
-    TcArgs ta{p.log_alpha, (const __nv_bfloat16 *)p.beta, p.init_state, p.out, p.final_state,
+    TcArgs ta{p.log_alpha, (const __nv_bfloat16 *)p.beta, p.init_state, p.final_state,
               status_word, (int)p.T, (int)p.H, p.NC};
     const unsigned grid = (unsigned)(p.B * p.H);
     if (p.out_bf16)
-        return p.gate == 1 ? launch_t<__nv_bfloat16, 1>(mq, mk, mv, ta, grid, stream)
-                           : launch_t<__nv_bfloat16, 0>(mq, mk, mv, ta, grid, stream);
-    return p.gate == 1 ? launch_t<float, 1>(mq, mk, mv, ta, grid, stream)
-                       : launch_t<float, 0>(mq, mk, mv, ta, grid, stream);
+        return p.gate == 1 ? launch_t<__nv_bfloat16, 1>(mq, mk, mv, mo, ta, grid, stream)
+                           : launch_t<__nv_bfloat16, 0>(mq, mk, mv, mo, ta, grid, stream);
+    return p.gate == 1 ? launch_t<float, 1>(mq, mk, mv, mo, ta, grid, stream)
+                       : launch_t<float, 0>(mq, mk, mv, mo, ta, grid, stream);
 }
 
 }  // namespace dr
