@@ -90,7 +90,7 @@ def decode_bytes(w):
 
 # ------------------------------------------------------------------ clocks sampler
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every 20 ms around the soak and the timed region."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
@@ -102,7 +102,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -162,8 +162,12 @@ def barrier(world):
 
 
 # ------------------------------------------------------------------ native arm
-def time_calls(fn, steps, warmup, world, sampler_index=None):
-    """CUDA-event time of `steps` calls on the current stream after `warmup` calls."""
+def time_calls(fn, steps, warmup, world, sampler_index=None, soak_s=1.0):
+    """CUDA-event time of `steps` calls on the current stream after `warmup` calls.
+
+    With a sampler, nvidia-smi records clocks every 20 ms from before a ~`soak_s` second
+    back-to-back run of the same call (untimed) through the end of the timed calls, so the
+    samples describe the GPU under this load; the timed calls follow the soak directly."""
     import torch
     for _ in range(warmup):
         fn()
@@ -174,7 +178,16 @@ def time_calls(fn, steps, warmup, world, sampler_index=None):
     sampler = ClockSampler(sampler_index) if sampler_index is not None else None
     if sampler:
         sampler.__enter__()
-    torch.cuda.synchronize()
+        # soak: repeat the call until ~soak_s seconds of device time are queued and done
+        e0.record(s)
+        fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        per = max(e0.elapsed_time(e1), 1e-3)
+        for _ in range(max(1, int(soak_s * 1e3 / per))):
+            fn()
+    else:
+        torch.cuda.synchronize()
     e0.record(s)
     for _ in range(steps):
         fn()
@@ -286,8 +299,8 @@ def run_native(args):
     ach_gbs = byts / (ms * 1e-3) / 1e9
     e2e_ms, h2d, d2h = bench_chunk_e2e(w, r["host_inputs"], max(2, args.steps // 2),
                                        max(3, args.warmup), world)
-    tc = tc_path(w)
-    launches_per_call = 1 if tc else 2
+    on_tc = tc_path(w)
+    launches_per_call = 1 if on_tc else 2
 
     extra = {}
     if not args.quick:
@@ -332,7 +345,7 @@ def run_native(args):
         "roofline": {"bound": "hbm", "achieved": ach_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": ach_gbs / hbm, "peak_source": pk_kind,
                      "traffic": (tr["bytes"] if tr and tr["src"] == src else None),
-                     "kernel": ("chunk_tc_kernel (fused tcgen05, one launch per call)" if tc else
+                     "kernel": ("chunk_tc_kernel (fused tcgen05, one launch per call)" if on_tc else
                                 "chunk_prep_kernel + chunk_state_kernel"),
                      "algorithmic_bytes": byts,
                      "tensor_tflops": flops / (ms * 1e-3) / 1e12,

@@ -54,19 +54,20 @@ constexpr int kThreads = 256;
 constexpr uint32_t kStageBytes = 49152;
 // stage layout: [Q kb0 | K kb0 | Q kb1 | K kb1 | V kb0 | V kb1], 8 KB each (64 x 64 bf16)
 constexpr uint32_t OFF_K0 = 8192, OFF_V0 = 32768;
-constexpr uint32_t SM_W = 2 * kStageBytes;    // W 64 x 128 K-major (2 K-blocks of 8 KB);
-                                              // after its MMA: low part of E^T
+constexpr uint32_t SM_W = 2 * kStageBytes;    // T diag beta (+G) for the U/W products, then
+                                              // W 64 x 128 K-major (2 K-blocks of 8 KB), then
+                                              // the low part of E^T
 constexpr uint32_t SM_ST = SM_W + 16384;      // S^T 128 x 128 K-major; fp32 T during the solve;
                                               // after its MMA: low part of E^T diag(delta)
 constexpr uint32_t SM_ET = SM_ST + 32768;     // E^T (high) 128 x 64
-constexpr uint32_t SM_ET2 = SM_ET + 16384;    // E^T diag(delta) (high); fp32 A during the solve,
-                                              // then T diag beta (+G)
+constexpr uint32_t SM_ET2 = SM_ET + 16384;    // E^T diag(delta) (high); fp32 A during the solve
                                               // SM_ET..SM_ET2 + 16 KB: the output tile at the end
 constexpr uint32_t SM_P = SM_ET2 + 16384;     // P (high part) 64 x 64 K-major
 constexpr uint32_t SM_PLO = SM_P + 8192;      // P (low part)
 constexpr uint32_t SM_ETLO = SM_W, SM_ET2LO = SM_ST, SM_OUT = SM_ET;
 constexpr uint32_t SM_SMALL = SM_PLO + 8192;  // per-token vectors and solve scratch
-constexpr uint32_t SM_A = SM_ET2, SM_TB = SM_ET2;   // fp32 A, then T diag beta (+G)
+constexpr uint32_t SM_A = SM_ET2;   // fp32 A during the solve
+constexpr uint32_t SM_TB = SM_W;    // T diag(beta), T diag(beta G) until the U/W products
 constexpr uint32_t SM_TOTAL = SM_SMALL + 8192;
 constexpr uint32_t TM_S = 0, TM_D = 128, TM_X = 256, TM_U = 320, TM_W = 384, TM_PE = 448;
 // TM_D: [ (W S)^T | (Q S)^T ];  TM_X: [Q; K] K^T;  TM_PE: E^T P^T
@@ -152,25 +153,52 @@ __device__ __forceinline__ void warp_store16(const float (&acc)[2][4], float sig
     }
 }
 
+constexpr int kTs = 68;   // row stride (floats) of the fp32 T matrix: 16-byte aligned rows
+
 // Element (r, s) of the fp32 A matrix: rows of 64, 16-byte groups XOR-swizzled by r % 16.
 __device__ __forceinline__ int a_index(int r, int s) {
     return r * 64 + ((((s >> 2) ^ (r & 15)) << 2) | (s & 3));
 }
 
-// T = (I + A)^-1 for a strictly lower-triangular 64 x 64 A (fp32), T stored [64][65].
+// T = (I + A)^-1 for a strictly lower-triangular 64 x 64 A (fp32), T stored [64][kTs].
 //   1. the four diagonal 16 x 16 blocks by right-looking substitution, four threads per
 //      column (each owns four rows; the pivot row's value is broadcast by a shuffle);
 //   2. T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (two warps);
 //   3. lower-left 32 x 32 quarter: M = A[32:64, 0:32] T[0:32, 0:32], then
 //      T[32:64, 0:32] = -T[32:64, 32:64] M (four warps, one 16 x 16 tile each).
+// Each element is written, once final, also as T diag(beta) and T diag(beta G) in bf16
+// (128-byte-swizzled K-major 64 x 64 tiles at TB and TB + 8192): the U and W operands.
 // Products use TF32 mma.sync with fp32 accumulation.  M needs 1024 floats.  Called by all
 // 256 threads; starts after and ends with a barrier.
-__device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, float *M, int tid) {
+__device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, float *M,
+                                                   unsigned char *TB, const float *beta,
+                                                   const float *gam, int tid) {
     auto a = [&](int r, int s) { return A[a_index(r, s)]; };
+    // final element (r, s) of T: fp32 copy for the later levels, and the two bf16 MMA
+    // operands T diag(beta) (at TB) and T diag(beta G) (at TB + 8192)
+    auto fin = [&](int r, int s, float v) {
+        T[r * kTs + s] = v;
+        const float vb = v * beta[s];
+        const uint32_t off = sw128_off(r, s);
+        *reinterpret_cast<__nv_bfloat16 *>(TB + off) = __float2bfloat16_rn(vb);
+        *reinterpret_cast<__nv_bfloat16 *>(TB + 8192 + off) = __float2bfloat16_rn(vb * gam[s]);
+    };
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
     {
         const int o = 16 * (tid >> 6), c = (tid >> 2) & 15, part = tid & 3;
         const int owner = lane & ~3;
+        // this thread's four rows of the diagonal block, o + part + 4m, columns o .. o + 15
+        float ar[4][16];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int r = o + part + 4 * m;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(A + a_index(r, o + 4 * q));
+                ar[m][4 * q] = v4.x; ar[m][4 * q + 1] = v4.y;
+                ar[m][4 * q + 2] = v4.z; ar[m][4 * q + 3] = v4.w;
+            }
+        }
         float y[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) y[m] = (part + 4 * m == c) ? 1.f : 0.f;
@@ -178,19 +206,20 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         for (int s2 = 0; s2 < 15; ++s2) {
             const float xs = __shfl_sync(0xffffffffu, y[s2 >> 2], owner | (s2 & 3));
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int r = part + 4 * m;
-                if (r > s2) y[m] = fmaf(-a(o + r, o + s2), xs, y[m]);
-            }
+            for (int m = 0; m < 4; ++m)
+                if (part + 4 * m > s2) y[m] = fmaf(-ar[m][s2], xs, y[m]);
         }
 #pragma unroll
-        for (int m = 0; m < 4; ++m) T[(o + part + 4 * m) * 65 + o + c] = y[m];
-        // zero the six blocks above the diagonal: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-        for (int idx = tid; idx < 6 * 256; idx += kThreads) {
-            const int blk = idx >> 8, e = idx & 255;
+        for (int m = 0; m < 4; ++m) fin(o + part + 4 * m, o + c, y[m]);
+        // the six blocks above the diagonal are zero in the bf16 operands (the fp32 copy
+        // of those blocks is never read): (0,1) (0,2) (0,3) (1,2) (1,3) (2,3), 8 per task
+        for (int idx = tid; idx < 6 * 32; idx += kThreads) {
+            const int blk = idx >> 5, e = idx & 31;
             const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
             const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            T[(16 * bi + (e >> 4)) * 65 + 16 * bj + (e & 15)] = 0.f;
+            const uint32_t off = sw128_off(16 * bi + (e >> 1), 16 * bj + 8 * (e & 1));
+            *reinterpret_cast<uint4 *>(TB + off) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(TB + 8192 + off) = make_uint4(0u, 0u, 0u, 0u);
         }
     }
     __syncthreads();
@@ -199,21 +228,20 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         float *Ms = M + 256 * warp;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         warp_mm16(acc, [&](int r, int k) { return a(16 * i + r, 16 * j + k); },
-                  [&](int k, int n) { return T[(16 * j + k) * 65 + 16 * j + n]; }, 1, g, t4);
+                  [&](int k, int n) { return T[(16 * j + k) * kTs + 16 * j + n]; }, 1, g, t4);
         warp_store16(acc, 1.f, [&](int r, int n, float v) { Ms[r * 16 + n] = v; }, g, t4);
         __syncwarp();
         float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_mm16(acc2, [&](int r, int k) { return T[(16 * i + r) * 65 + 16 * i + k]; },
+        warp_mm16(acc2, [&](int r, int k) { return T[(16 * i + r) * kTs + 16 * i + k]; },
                   [&](int k, int n) { return Ms[k * 16 + n]; }, 1, g, t4);
-        warp_store16(acc2, -1.f, [&](int r, int n, float v) { T[(16 * i + r) * 65 + 16 * j + n] = v; },
-                     g, t4);
+        warp_store16(acc2, -1.f, [&](int r, int n, float v) { fin(16 * i + r, 16 * j + n, v); }, g, t4);
     }
     __syncthreads();
     if (warp < 4) {   // M tile (rb, cb) = sum_{k = cb}^{1} A_{rb,k} T_{k,cb},  rb = 2 + w/2, cb = w%2
         const int rb = 2 + (warp >> 1), cb = warp & 1;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         warp_mm16(acc, [&](int r, int k) { return a(16 * rb + r, 16 * cb + k); },
-                  [&](int k, int n) { return T[(16 * cb + k) * 65 + 16 * cb + n]; }, 2 - cb, g, t4);
+                  [&](int k, int n) { return T[(16 * cb + k) * kTs + 16 * cb + n]; }, 2 - cb, g, t4);
         float *Mt = M + 256 * warp;
         warp_store16(acc, 1.f, [&](int r, int n, float v) { Mt[r * 16 + n] = v; }, g, t4);
     }
@@ -221,12 +249,12 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
     if (warp < 4) {   // T_{rb,cb} = -sum_{k = 2}^{rb} T_{rb,k} M_{k,cb}
         const int rb = 2 + (warp >> 1), cb = warp & 1;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_mm16(acc, [&](int r, int k) { return T[(16 * rb + r) * 65 + 32 + k]; },
+        warp_mm16(acc, [&](int r, int k) { return T[(16 * rb + r) * kTs + 32 + k]; },
                   [&](int k, int n) { return M[256 * (((k >> 4) << 1) | cb) + (k & 15) * 16 + n]; },
                   rb - 1, g, t4);
-        warp_store16(acc, -1.f, [&](int r, int n, float v) { T[(16 * rb + r) * 65 + 16 * cb + n] = v; },
-                     g, t4);
+        warp_store16(acc, -1.f, [&](int r, int n, float v) { fin(16 * rb + r, 16 * cb + n, v); }, g, t4);
     }
+    fence_proxy_async();   // the bf16 operands are read next by the tensor core
     __syncthreads();
 }
 
@@ -248,6 +276,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const int bh = blockIdx.x;
     const int h = bh % a.H, b = bh / a.H;
     constexpr int kTmaThread = 224;              // lane 0 of warp 7 issues the TMA loads
+    constexpr int kGateWarp = 1;                 // warp 1 scans the gates; thread 0 issues MMAs
     float *sG = reinterpret_cast<float *>(sm + SM_SMALL);   // g_r (cumulative log decay)
     float *sGam = sG + 64;     // exp(g_r)
     float *sDel = sG + 128;    // exp(g_63 - g_r)
@@ -305,7 +334,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
     };
     // beta (the aligned 32-bit word holding it) and log alpha of chunk c, two tokens per
-    // lane of warp 0, copied asynchronously one chunk ahead
+    // lane of warp 1 (warp 0 issues the MMAs), copied asynchronously one chunk ahead
     const size_t ntok = (size_t)gridDim.x * a.T;   // B * T * H beta values
     auto issue_gate = [&](int c) {
         uint32_t *dst = sGate + (c & 1) * 128;
@@ -327,12 +356,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         cp_async_commit();
     };
     if (tid == kTmaThread) issue_tma(0);
-    if (warp == 0) issue_gate(0);
+    if (warp == kGateWarp) issue_gate(0);
 
     bool out_pending = false;       // chunk whose outputs wait in TMEM for the write-out
     bool store_outstanding = false; // a TMA store may still be reading SM_OUT
-    bool tma_pending = true;        // a TMA load was issued and not yet waited for
-    int last_tma_c = 0;             // chunk of the most recent TMA load
+    int last_tma_c = 0;             // chunk of the most recent TMA load (TMA thread)
     bool s_outstanding = false;     // MMA group S (state update, E^T P^T) committed, not waited
     int cur_t0 = 0;                 // t0 of the chunk whose outputs are pending
     auto fail = [&]() {
@@ -342,6 +370,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
         if (!wait_cycles(bar, parity)) fail();
         tc_fence_after();
+    };
+    // (thread 0) wait for chunk c's tiles, then X = [Q; K] K^T into TM_X
+    auto issue_x = [&](int c) {
+        if (!wait_cycles(&bar_tma[c & 1], (c >> 1) & 1)) fail();
+        unsigned char *st = sm + (c & 1) * kStageBytes;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_bf16(tmem_base_s + TM_X, smem_desc_sw128(smem_u32(st + o), 16, 1024),
+                     smem_desc_sw128(smem_u32(st + OFF_K0 + o), 16, 1024), ID_KK_N64, ks > 0);
+        }
+        mma_commit(&bar_x);
     };
 
     // Output of the chunk at t0: o = G_r (Q S)^T + E^T P^T, staged row-major at SM_OUT in
@@ -394,21 +435,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         unsigned char *st = sm + s * kStageBytes;
         const int t0 = c * 64;
 
-        // ---- 1. this chunk's tiles; X = [Q; K] K^T
-        if (!wait_cycles(&bar_tma[s], (c >> 1) & 1)) fail();
-        tma_pending = false;
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_bf16(tmem_base_s + TM_X, smem_desc_sw128(smem_u32(st + o), 16, 1024),
-                         smem_desc_sw128(smem_u32(st + OFF_K0 + o), 16, 1024), ID_KK_N64, ks > 0);
-            }
-            mma_commit(&bar_x);
-        }
-        // ---- 2. cumulative log decay of this chunk (warp 0; its gates arrived by cp.async)
-        if (warp == 0) {
+        // ---- 1. X = [Q; K] K^T of this chunk (the first chunk's here; later ones are issued
+        //         right after the previous chunk's state update)
+        if (c == 0 && tid == 0) issue_x(0);
+        // ---- 2. cumulative log decay of this chunk (gate warp; its gates arrived by cp.async)
+        if (warp == kGateWarp) {
             cp_async_wait_all();
             __syncwarp();
             const uint32_t *gw = sGate + s * 128;
@@ -457,7 +488,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         if (out_pending) write_out(cur_t0);
         if (tid == kTmaThread && c + 1 < a.NC) {
             issue_tma(c + 1);
-            tma_pending = true;
             last_tma_c = c + 1;
         }
         // keep this chunk's exp(g_r) for its deferred write-out (write_out above ended with
@@ -477,7 +507,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             if (fac) {
                 const float er = sE[r];
 #pragma unroll
-                for (int u = 0; u < 32; ++u) dec[u] = er * sF[c0 + u];
+                for (int q = 0; q < 8; ++q) {
+                    const float4 f4 = *reinterpret_cast<const float4 *>(sF + c0 + 4 * q);
+                    dec[4 * q] = er * f4.x; dec[4 * q + 1] = er * f4.y;
+                    dec[4 * q + 2] = er * f4.z; dec[4 * q + 3] = er * f4.w;
+                }
             } else {
                 const float gr = sG[r];
 #pragma unroll
@@ -519,32 +553,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tc_fence_before();
         __syncthreads();
 
-        // ---- 5. T = (I + A)^-1 (fp32, [64][65] at SM_ST)
+        // ---- 5-6. T = (I + A)^-1 (fp32, [64][kTs] at SM_ST), with T diag(beta) and
+        //           T diag(beta G) in bf16 at SM_TB
         solve_unit_lower64(reinterpret_cast<const float *>(sm + SM_A),
-                           reinterpret_cast<float *>(sm + SM_ST), sM, tid);
-
-        // ---- 6. T diag(beta) and T diag(beta G) as bf16 K-major operands (64 x 64)
-        {
-            const float *sT = reinterpret_cast<const float *>(sm + SM_ST);
-            for (int task = tid; task < 512; task += kThreads) {
-                const int r = task >> 3, ch = task & 7;
-                uint32_t p1[4], p2[4];
-#pragma unroll
-                for (int u = 0; u < 8; u += 2) {
-                    const int s0 = 8 * ch + u;
-                    const float t0v = sT[r * 65 + s0] * sBeta[s0];
-                    const float t1v = sT[r * 65 + s0 + 1] * sBeta[s0 + 1];
-                    p1[u >> 1] = pack_bf16(t0v, t1v);
-                    p2[u >> 1] = pack_bf16(t0v * sGam[s0], t1v * sGam[s0 + 1]);
-                }
-                const uint32_t off = sw128_off(r, 8 * ch);
-                *reinterpret_cast<uint4 *>(sm + SM_TB + off) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-                *reinterpret_cast<uint4 *>(sm + SM_TB + 8192 + off) =
-                    make_uint4(p2[0], p2[1], p2[2], p2[3]);
-            }
-        }
-        fence_proxy_async();
-        __syncthreads();
+                           reinterpret_cast<float *>(sm + SM_ST), sM, sm + SM_TB, sBeta, sGam, tid);
 
         // ---- 7. U^T = V^T (T diag beta)^T,  W^T = K^T (T diag(beta G))^T
         if (tid == 0) {
@@ -673,6 +685,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                              smem_desc_sw128(smem_u32(sm + pb[part] + ks * 32), 16, 1024), ID_KK_N64,
                              (part | ks) != 0);
             mma_commit(&bar_s);
+            if (c + 1 < a.NC) issue_x(c + 1);
         }
         s_outstanding = true;
         out_pending = true;
@@ -687,7 +700,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     }
     if (abort_s) {
         // Drain this CTA's own asynchronous work (bounded) before TMEM is freed.
-        if (tid == kTmaThread && tma_pending)
+        if (tid == kTmaThread)   // the last load may still be in flight (bounded wait)
             wait_cycles(&bar_tma[last_tma_c & 1], (last_tma_c >> 1) & 1);
         if (tid == 0 && s_outstanding) wait_cycles(&bar_s, (a.NC - 1) & 1);
     } else if (a.final_state) {
@@ -700,7 +713,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             for (int u = 0; u < 32; ++u) a.final_state[((size_t)bh * 128 + i0 + u) * 128 + row] = v[u];
         }
     }
-    if (warp == 0) cp_async_wait_all();
+    if (warp == kGateWarp) cp_async_wait_all();
     if (tid == 0 && store_outstanding) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
