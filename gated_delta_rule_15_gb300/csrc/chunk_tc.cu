@@ -57,14 +57,15 @@ constexpr uint32_t OFF_K0 = 8192, OFF_V0 = 32768;
 constexpr uint32_t SM_W = 2 * kStageBytes;    // T diag beta (+G) for the U/W products, then
                                               // W 64 x 128 K-major (2 K-blocks of 8 KB), then
                                               // the low part of E^T
-constexpr uint32_t SM_ST = SM_W + 16384;      // S^T 128 x 128 K-major; fp32 T during the solve;
-                                              // after its MMA: low part of E^T diag(delta)
+constexpr uint32_t SM_ST = SM_W + 16384;      // S^T 128 x 128 K-major; fp32 T during the solve
 constexpr uint32_t SM_ET = SM_ST + 32768;     // E^T (high) 128 x 64
 constexpr uint32_t SM_ET2 = SM_ET + 16384;    // E^T diag(delta) (high); fp32 A during the solve
                                               // SM_ET..SM_ET2 + 16 KB: the output tile at the end
 constexpr uint32_t SM_P = SM_ET2 + 16384;     // P (high part) 64 x 64 K-major
 constexpr uint32_t SM_PLO = SM_P + 8192;      // P (low part)
-constexpr uint32_t SM_ETLO = SM_W, SM_ET2LO = SM_ST, SM_OUT = SM_ET;
+// The low part of E^T diag(delta) goes to the current stage's V tile, which is free from the
+// completion of the U/W products until the stage is reloaded after the state update.
+constexpr uint32_t SM_ETLO = SM_W, SM_OUT = SM_ET;
 constexpr uint32_t SM_SMALL = SM_PLO + 8192;  // per-token vectors and solve scratch
 constexpr uint32_t SM_A = SM_ET2;   // fp32 A during the solve
 constexpr uint32_t SM_TB = SM_W;    // T diag(beta), T diag(beta G) until the U/W products
@@ -140,16 +141,14 @@ __device__ __forceinline__ void warp_mm16(float (&acc)[2][4], FL L, FR R, int nk
                             to_tf32(R(kc + t4 + 4, 8 * nt + g)));
     }
 }
-// Writes sign * acc through st(r, n, v).
+// Writes sign * acc through st(r, n, v0, v1): elements (r, n) and (r, n + 1), n even.
 template <class FS>
 __device__ __forceinline__ void warp_store16(const float (&acc)[2][4], float sign, FS st, int g, int t4) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
         const int n = 8 * nt + 2 * t4;
-        st(g, n, sign * acc[nt][0]);
-        st(g, n + 1, sign * acc[nt][1]);
-        st(g + 8, n, sign * acc[nt][2]);
-        st(g + 8, n + 1, sign * acc[nt][3]);
+        st(g, n, sign * acc[nt][0], sign * acc[nt][1]);
+        st(g + 8, n, sign * acc[nt][2], sign * acc[nt][3]);
     }
 }
 
@@ -182,6 +181,14 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         const uint32_t off = sw128_off(r, s);
         *reinterpret_cast<__nv_bfloat16 *>(TB + off) = __float2bfloat16_rn(vb);
         *reinterpret_cast<__nv_bfloat16 *>(TB + 8192 + off) = __float2bfloat16_rn(vb * gam[s]);
+    };
+    // final elements (r, s) and (r, s + 1), s even: one 32-bit store per operand
+    auto fin2 = [&](int r, int s, float v0, float v1) {
+        *reinterpret_cast<float2 *>(T + r * kTs + s) = make_float2(v0, v1);
+        const float b0 = v0 * beta[s], b1 = v1 * beta[s + 1];
+        const uint32_t off = sw128_off(r, s);
+        *reinterpret_cast<uint32_t *>(TB + off) = pack_bf16(b0, b1);
+        *reinterpret_cast<uint32_t *>(TB + 8192 + off) = pack_bf16(b0 * gam[s], b1 * gam[s + 1]);
     };
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
     {
@@ -229,12 +236,14 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         warp_mm16(acc, [&](int r, int k) { return a(16 * i + r, 16 * j + k); },
                   [&](int k, int n) { return T[(16 * j + k) * kTs + 16 * j + n]; }, 1, g, t4);
-        warp_store16(acc, 1.f, [&](int r, int n, float v) { Ms[r * 16 + n] = v; }, g, t4);
+        warp_store16(acc, 1.f, [&](int r, int n, float v0, float v1) {
+            *reinterpret_cast<float2 *>(Ms + r * 16 + n) = make_float2(v0, v1); }, g, t4);
         __syncwarp();
         float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         warp_mm16(acc2, [&](int r, int k) { return T[(16 * i + r) * kTs + 16 * i + k]; },
                   [&](int k, int n) { return Ms[k * 16 + n]; }, 1, g, t4);
-        warp_store16(acc2, -1.f, [&](int r, int n, float v) { fin(16 * i + r, 16 * j + n, v); }, g, t4);
+        warp_store16(acc2, -1.f, [&](int r, int n, float v0, float v1) {
+            fin2(16 * i + r, 16 * j + n, v0, v1); }, g, t4);
     }
     __syncthreads();
     if (warp < 4) {   // M tile (rb, cb) = sum_{k = cb}^{1} A_{rb,k} T_{k,cb},  rb = 2 + w/2, cb = w%2
@@ -243,7 +252,8 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         warp_mm16(acc, [&](int r, int k) { return a(16 * rb + r, 16 * cb + k); },
                   [&](int k, int n) { return T[(16 * cb + k) * kTs + 16 * cb + n]; }, 2 - cb, g, t4);
         float *Mt = M + 256 * warp;
-        warp_store16(acc, 1.f, [&](int r, int n, float v) { Mt[r * 16 + n] = v; }, g, t4);
+        warp_store16(acc, 1.f, [&](int r, int n, float v0, float v1) {
+            *reinterpret_cast<float2 *>(Mt + r * 16 + n) = make_float2(v0, v1); }, g, t4);
     }
     __syncthreads();
     if (warp < 4) {   // T_{rb,cb} = -sum_{k = 2}^{rb} T_{rb,k} M_{k,cb}
@@ -252,7 +262,8 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         warp_mm16(acc, [&](int r, int k) { return T[(16 * rb + r) * kTs + 32 + k]; },
                   [&](int k, int n) { return M[256 * (((k >> 4) << 1) | cb) + (k & 15) * 16 + n]; },
                   rb - 1, g, t4);
-        warp_store16(acc, -1.f, [&](int r, int n, float v) { fin(16 * rb + r, 16 * cb + n, v); }, g, t4);
+        warp_store16(acc, -1.f, [&](int r, int n, float v0, float v1) {
+            fin2(16 * rb + r, 16 * cb + n, v0, v1); }, g, t4);
     }
     fence_proxy_async();   // the bf16 operands are read next by the tensor core
     __syncthreads();
@@ -266,7 +277,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     extern __shared__ unsigned char dsm_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
     // mbarriers: TMA stages, and one per MMA group (each completes once per chunk)
-    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_s;
+    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_q, bar_s;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s, factored_s;
 
@@ -296,6 +307,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         mbar_init(&bar_x, 1);
         mbar_init(&bar_uw, 1);
         mbar_init(&bar_d, 1);
+        mbar_init(&bar_q, 1);
         mbar_init(&bar_s, 1);
         abort_s = 0;
         fence_mbar_init();
@@ -621,18 +633,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                const uint64_t adesc = smem_desc_sw128(smem_u32(sm + SM_ST + o), 16, 1024);
-                mma_bf16(tmem_base_s + TM_D, adesc,
+                mma_bf16(tmem_base_s + TM_D, smem_desc_sw128(smem_u32(sm + SM_ST + o), 16, 1024),
                          smem_desc_sw128(smem_u32(sm + SM_W + (ks >> 2) * 8192 + (ks & 3) * 32), 16, 1024),
                          ID_KK_N64, ks > 0);
-                mma_bf16(tmem_base_s + TM_D + 64, adesc, smem_desc_sw128(smem_u32(st + o), 16, 1024),
-                         ID_KK_N64, ks > 0);
             }
-            mma_commit(&bar_d);
+            mma_commit(&bar_d);   // (W S)^T: needed by the E^T build
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+                mma_bf16(tmem_base_s + TM_D + 64, smem_desc_sw128(smem_u32(sm + SM_ST + o), 16, 1024),
+                         smem_desc_sw128(smem_u32(st + o), 16, 1024), ID_KK_N64, ks > 0);
+            }
+            mma_commit(&bar_q);   // (Q S)^T: needed by the write-out only
         }
         wait_bar(&bar_d, par);
 
-        // ---- 11. E^T = U^T - (W S)^T, and E^T diag(delta)  (bf16 high/low pairs)
+        // ---- 11. E^T = U^T - (W S)^T, and E^T diag(delta)  (bf16 high/low pairs); the (Q S)^T
+        //          half completes meanwhile and is read by the deferred write-out
         {
             float ws[32], uu[32];
             tmem_ld32(tm + TM_D + 32 * half, ws);
@@ -657,10 +674,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 *reinterpret_cast<uint4 *>(sm + SM_ET + off) = make_uint4(eh[0], eh[1], eh[2], eh[3]);
                 *reinterpret_cast<uint4 *>(sm + SM_ETLO + off) = make_uint4(el[0], el[1], el[2], el[3]);
                 *reinterpret_cast<uint4 *>(sm + SM_ET2 + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
-                *reinterpret_cast<uint4 *>(sm + SM_ET2LO + off) =
+                *reinterpret_cast<uint4 *>(st + OFF_V0 + off) =
                     make_uint4(dlo[0], dlo[1], dlo[2], dlo[3]);
             }
         }
+        wait_bar(&bar_q, par);
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
@@ -669,12 +687,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         //          while the next chunk starts, whose step 3 waits for it
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t e2[2] = {SM_ET2, SM_ET2LO};
+            unsigned char *e2[2] = {sm + SM_ET2, st + OFF_V0};
 #pragma unroll
             for (int part = 0; part < 2; ++part)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem_base_s + TM_S, smem_desc_sw128(smem_u32(sm + e2[part] + ks * 32), 16, 1024),
+                    mma_bf16(tmem_base_s + TM_S, smem_desc_sw128(smem_u32(e2[part] + ks * 32), 16, 1024),
                              smem_desc_sw128(smem_u32(st + OFF_K0 + ks * 2048), 16384, 1024), ID_KM_N128, 1);
             const uint32_t ea[3] = {SM_ET, SM_ET, SM_ETLO}, pb[3] = {SM_P, SM_PLO, SM_P};
 #pragma unroll
