@@ -56,10 +56,12 @@ inline ChunkWorkspace simt_workspace_carve(void *base, int64_t B, int64_t H, int
 int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStream_t stream);
 
 // Fused tensor-core path (chunk_tc.cu): bf16 inputs, dk = dv = 128, C = 64, scalar gate or
-// none, T > 0.  Needs no workspace.  `status_word` is the device status word of the
-// library (bounded waits record DR_ERR_TIMEOUT there).
+// none, T > 0.  Needs a workspace only when few long chains are split into segments
+// (chunk_tc_workspace_bytes).  `status_word` is the device status word of the library
+// (bounded waits record DR_ERR_TIMEOUT there).
 bool chunk_tc_supported(const ChunkProblem &p);
-int launch_chunk_tc(const ChunkProblem &p, int *status_word, cudaStream_t stream);
+size_t chunk_tc_workspace_bytes(const ChunkProblem &p);
+int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream);
 int launch_decode(int64_t BH, int dk, int dv, int in_bf16, int out_bf16, int gate,
                   const void *q, const void *k, const void *v, const float *la,
                   const void *beta, float *state, void *out, cudaStream_t s);

@@ -38,6 +38,7 @@
 // tcgen05.commit on an mbarrier.  Every wait is bounded by a cycle budget: on expiry the
 // kernel records DR_ERR_TIMEOUT in the status word, drains its own copies and MMAs (with
 // the same bound), frees TMEM and returns.
+#include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -88,6 +89,12 @@ struct TcArgs {
     float *final_state;
     int *status;
     int T, H, NC;
+    // Sequence segments (few long chains): role 0 runs whole sequences; role 1 runs each
+    // segment twice without outputs -- from S_0 = 0 (end state to ws_s0) and as the
+    // transition from S_0 = I with no value term (to ws_phi); role 2 reruns each segment
+    // from its true start state (ws_start) writing outputs.  [B*H][nseg][128][128] fp32.
+    int role, nseg, seg_len;
+    float *ws_phi, *ws_s0, *ws_start;
 };
 
 __device__ __forceinline__ bool wait_cycles(uint64_t *bar, uint32_t parity) {
@@ -284,7 +291,33 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
     const int row = 32 * quarter + lane;        // the TMEM lane this thread reads and writes
-    const int bh = blockIdx.x;
+    // this CTA's chain, token-chunk range, initial/final state and duties
+    int bh = blockIdx.x, c_begin = 0, c_end = a.NC;
+    const float *init_ptr = a.init_state ? a.init_state + (size_t)blockIdx.x * 16384 : nullptr;
+    float *fin_ptr = a.final_state ? a.final_state + (size_t)blockIdx.x * 16384 : nullptr;
+    bool init_identity = false, zero_u = false, outputs = true;
+    if (a.role != 0) {
+        const int idx = a.role == 1 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+        const int seg = idx % a.nseg;
+        bh = idx / a.nseg;
+        c_begin = seg * a.seg_len;
+        c_end = min(a.NC, c_begin + a.seg_len);
+        const size_t slot = ((size_t)bh * a.nseg + seg) * 16384;
+        if (a.role == 1) {
+            outputs = false;
+            init_ptr = nullptr;
+            if (blockIdx.x & 1) {   // transition: S_0 = I, no value term
+                init_identity = true;
+                zero_u = true;
+                fin_ptr = a.ws_phi + slot;
+            } else {
+                fin_ptr = a.ws_s0 + slot;
+            }
+        } else {
+            init_ptr = a.ws_start + slot;
+            fin_ptr = (seg == a.nseg - 1 && a.final_state) ? a.final_state + (size_t)bh * 16384 : nullptr;
+        }
+    }
     const int h = bh % a.H, b = bh / a.H;
     constexpr int kTmaThread = 224;              // lane 0 of warp 7 issues the TMA loads
     constexpr int kGateWarp = 1;                 // warp 1 scans the gates; thread 0 issues MMAs
@@ -328,14 +361,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             const int i0 = 64 * half + 32 * part;
 #pragma unroll
             for (int u = 0; u < 32; ++u)
-                v[u] = a.init_state ? a.init_state[((size_t)bh * 128 + i0 + u) * 128 + row] : 0.f;
+                v[u] = init_identity ? (i0 + u == row ? 1.f : 0.f)
+                                     : (init_ptr ? init_ptr[(size_t)(i0 + u) * 128 + row] : 0.f);
             tmem_st32(tm + TM_S + i0, v);
         }
         tmem_wait_st();
     }
 
-    auto issue_tma = [&](int c) {
-        const int s = c & 1;
+    // `it` counts this CTA's chunks (stage, barrier phases); `c` is the global chunk index
+    auto issue_tma = [&](int it, int c) {
+        const int s = it & 1;
         unsigned char *st = sm + s * kStageBytes;
         mbar_arrive_expect_tx(&bar_tma[s], kStageBytes);
         const int t0 = c * 64;
@@ -347,9 +382,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     };
     // beta (the aligned 32-bit word holding it) and log alpha of chunk c, two tokens per
     // lane of warp 1 (warp 0 issues the MMAs), copied asynchronously one chunk ahead
-    const size_t ntok = (size_t)gridDim.x * a.T;   // B * T * H beta values
-    auto issue_gate = [&](int c) {
-        uint32_t *dst = sGate + (c & 1) * 128;
+    const size_t ntok = (size_t)(gridDim.x / (a.role == 0 ? 1 : (a.role == 1 ? 2 * a.nseg : a.nseg))) * a.T;
+    auto issue_gate = [&](int it, int c) {
+        uint32_t *dst = sGate + (it & 1) * 128;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int r = 2 * lane + e, t = c * 64 + r;
@@ -367,12 +402,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
         cp_async_commit();
     };
-    if (tid == kTmaThread) issue_tma(0);
-    if (warp == kGateWarp) issue_gate(0);
+    const int n_it = c_end - c_begin;
+    if (tid == kTmaThread && n_it > 0) issue_tma(0, c_begin);
+    if (warp == kGateWarp && n_it > 0) issue_gate(0, c_begin);
 
     bool out_pending = false;       // chunk whose outputs wait in TMEM for the write-out
     bool store_outstanding = false; // a TMA store may still be reading SM_OUT
-    int last_tma_c = 0;             // chunk of the most recent TMA load (TMA thread)
+    int last_tma_it = 0;            // iteration of the most recent TMA load (TMA thread)
     bool s_outstanding = false;     // MMA group S (state update, E^T P^T) committed, not waited
     int cur_t0 = 0;                 // t0 of the chunk whose outputs are pending
     auto fail = [&]() {
@@ -384,9 +420,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tc_fence_after();
     };
     // (thread 0) wait for chunk c's tiles, then X = [Q; K] K^T into TM_X
-    auto issue_x = [&](int c) {
-        if (!wait_cycles(&bar_tma[c & 1], (c >> 1) & 1)) fail();
-        unsigned char *st = sm + (c & 1) * kStageBytes;
+    auto issue_x = [&](int it) {
+        if (!wait_cycles(&bar_tma[it & 1], (it >> 1) & 1)) fail();
+        unsigned char *st = sm + (it & 1) * kStageBytes;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
@@ -441,15 +477,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         if (kWideOut) __syncthreads();
     };
 
-    for (int c = 0; c < a.NC; ++c) {
-        const int s = c & 1;
-        const uint32_t par = c & 1;               // parity of this chunk's MMA barriers
+    for (int it = 0; it < n_it; ++it) {
+        const int c = c_begin + it;
+        const int s = it & 1;
+        const uint32_t par = it & 1;              // parity of this chunk's MMA barriers
         unsigned char *st = sm + s * kStageBytes;
         const int t0 = c * 64;
 
         // ---- 1. X = [Q; K] K^T of this chunk (the first chunk's here; later ones are issued
         //         right after the previous chunk's state update)
-        if (c == 0 && tid == 0) issue_x(0);
+        if (it == 0 && tid == 0) issue_x(0);
         // ---- 2. cumulative log decay of this chunk (gate warp; its gates arrived by cp.async)
         if (warp == kGateWarp) {
             cp_async_wait_all();
@@ -466,7 +503,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 l[e] = __uint_as_float(gw[64 + r]);
             }
             __syncwarp();
-            if (c + 1 < a.NC) issue_gate(c + 1);
+            if (it + 1 < n_it) issue_gate(it + 1, c + 1);
             float p = l[0] + l[1];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -497,10 +534,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
         __syncthreads();            // gate vectors published; previous chunk's MMAs done
         if (abort_s) break;
-        if (out_pending) write_out(cur_t0);
-        if (tid == kTmaThread && c + 1 < a.NC) {
-            issue_tma(c + 1);
-            last_tma_c = c + 1;
+        if (out_pending && outputs) write_out(cur_t0);
+        if (tid == kTmaThread && it + 1 < n_it) {
+            issue_tma(it + 1, c + 1);
+            last_tma_it = it + 1;
         }
         // keep this chunk's exp(g_r) for its deferred write-out (write_out above ended with
         // a barrier, so no thread still reads the previous values)
@@ -573,6 +610,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         // ---- 7. U^T = V^T (T diag beta)^T,  W^T = K^T (T diag(beta G))^T
         if (tid == 0) {
             tc_fence_after();
+            if (!zero_u)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 mma_bf16(tmem_base_s + TM_U, smem_desc_sw128(smem_u32(st + OFF_V0 + ks * 2048), 8192, 1024),
@@ -638,13 +676,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                          ID_KK_N64, ks > 0);
             }
             mma_commit(&bar_d);   // (W S)^T: needed by the E^T build
+            if (outputs) {
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_bf16(tmem_base_s + TM_D + 64, smem_desc_sw128(smem_u32(sm + SM_ST + o), 16, 1024),
-                         smem_desc_sw128(smem_u32(st + o), 16, 1024), ID_KK_N64, ks > 0);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_bf16(tmem_base_s + TM_D + 64, smem_desc_sw128(smem_u32(sm + SM_ST + o), 16, 1024),
+                             smem_desc_sw128(smem_u32(st + o), 16, 1024), ID_KK_N64, ks > 0);
+                }
+                mma_commit(&bar_q);   // (Q S)^T: needed by the write-out only
             }
-            mma_commit(&bar_q);   // (Q S)^T: needed by the write-out only
         }
         wait_bar(&bar_d, par);
 
@@ -655,6 +695,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             tmem_ld32(tm + TM_D + 32 * half, ws);
             tmem_ld32(tm + TM_U + 32 * half, uu);
             tmem_wait_ld();
+            if (zero_u)
+#pragma unroll
+                for (int u = 0; u < 32; ++u) uu[u] = 0.f;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 float e[8], ed[8];
@@ -678,7 +721,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     make_uint4(dlo[0], dlo[1], dlo[2], dlo[3]);
             }
         }
-        wait_bar(&bar_q, par);
+        if (outputs) wait_bar(&bar_q, par);
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
@@ -695,6 +738,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     mma_bf16(tmem_base_s + TM_S, smem_desc_sw128(smem_u32(e2[part] + ks * 32), 16, 1024),
                              smem_desc_sw128(smem_u32(st + OFF_K0 + ks * 2048), 16384, 1024), ID_KM_N128, 1);
             const uint32_t ea[3] = {SM_ET, SM_ET, SM_ETLO}, pb[3] = {SM_P, SM_PLO, SM_P};
+            if (outputs)
 #pragma unroll
             for (int part = 0; part < 3; ++part)
 #pragma unroll
@@ -703,7 +747,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                              smem_desc_sw128(smem_u32(sm + pb[part] + ks * 32), 16, 1024), ID_KK_N64,
                              (part | ks) != 0);
             mma_commit(&bar_s);
-            if (c + 1 < a.NC) issue_x(c + 1);
+            if (it + 1 < n_it) issue_x(it + 1);
         }
         s_outstanding = true;
         out_pending = true;
@@ -711,24 +755,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     }
 
     if (!abort_s && s_outstanding) {
-        wait_bar(&bar_s, (a.NC - 1) & 1);
+        wait_bar(&bar_s, (n_it - 1) & 1);
         s_outstanding = false;
         __syncthreads();
-        if (!abort_s && out_pending) write_out(cur_t0);
+        if (!abort_s && out_pending && outputs) write_out(cur_t0);
     }
     if (abort_s) {
         // Drain this CTA's own asynchronous work (bounded) before TMEM is freed.
         if (tid == kTmaThread)   // the last load may still be in flight (bounded wait)
-            wait_cycles(&bar_tma[last_tma_c & 1], (last_tma_c >> 1) & 1);
-        if (tid == 0 && s_outstanding) wait_cycles(&bar_s, (a.NC - 1) & 1);
-    } else if (a.final_state) {
+            wait_cycles(&bar_tma[last_tma_it & 1], (last_tma_it >> 1) & 1);
+        if (tid == 0 && s_outstanding) wait_cycles(&bar_s, (n_it - 1) & 1);
+    } else if (fin_ptr) {
         float v[32];
         for (int part = 0; part < 2; ++part) {
             const int i0 = 64 * half + 32 * part;
             tmem_ld32(tm + TM_S + i0, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int u = 0; u < 32; ++u) a.final_state[((size_t)bh * 128 + i0 + u) * 128 + row] = v[u];
+            for (int u = 0; u < 32; ++u) fin_ptr[(size_t)(i0 + u) * 128 + row] = v[u];
         }
     }
     if (warp == kGateWarp) cp_async_wait_all();
@@ -737,6 +781,39 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem_base_s, 512);
+}
+
+// Segment chaining (between the two segment passes): per chain, S_start(0) = S_0 and
+// S_start(p + 1) = Phi_p S_start(p) + S0_p, where Phi_p and S0_p are segment p's transition
+// and zero-start end state.  One CTA per (chain, block of 32 state columns), fp32.
+__global__ void __launch_bounds__(256) seg_combine_kernel(const float *__restrict__ init_state,
+                                                           const float *__restrict__ phi,
+                                                           const float *__restrict__ s0,
+                                                           float *__restrict__ start, int nseg) {
+    __shared__ float S[128][33];
+    const int cb = blockIdx.x & 3, bh = blockIdx.x >> 2;
+    const int tid = threadIdx.x, j = tid & 31, rg = tid >> 5;
+    const int col = 32 * cb + j;
+    for (int i = rg; i < 128; i += 8)
+        S[i][j] = init_state ? init_state[((size_t)bh * 128 + i) * 128 + col] : 0.f;
+    __syncthreads();
+    for (int p = 0; p < nseg; ++p) {
+        const size_t slot = ((size_t)bh * nseg + p) * 16384;
+        for (int i = rg; i < 128; i += 8) start[slot + i * 128 + col] = S[i][j];
+        if (p + 1 == nseg) break;
+        float acc[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc[m] = s0[slot + (size_t)(rg + 8 * m) * 128 + col];
+        for (int k = 0; k < 128; ++k) {
+            const float sk = S[k][j];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc[m] = fmaf(phi[slot + (size_t)(rg + 8 * m) * 128 + k], sk, acc[m]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < 16; ++m) S[rg + 8 * m][j] = acc[m];
+        __syncthreads();
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -788,20 +865,62 @@ bool chunk_tc_supported(const ChunkProblem &p) {
            (p.gate == 0 || p.gate == 1);
 }
 
-int launch_chunk_tc(const ChunkProblem &p, int *status_word, cudaStream_t stream) {
+// Few long chains leave most of the GPU's 152 SMs idle while each chain walks its chunks
+// one after another; such problems are split into `nseg` segments per chain (at least 16
+// chunks each) so that about 152 CTAs work at once.
+static constexpr int kGpuSms = 152;
+static void tc_segments(const ChunkProblem &p, int *nseg, int *seg_len) {
+    *nseg = 1;
+    *seg_len = p.NC;
+    const int64_t bh = p.B * p.H;
+    if (!chunk_tc_supported(p) || bh > kGpuSms / 2 || p.NC < 32) return;
+    int n = (int)std::min<int64_t>(p.NC / 16, kGpuSms / bh);
+    if (n < 2) return;
+    const int len = (p.NC + n - 1) / n;
+    *seg_len = len;
+    *nseg = (p.NC + len - 1) / len;
+}
+
+size_t chunk_tc_workspace_bytes(const ChunkProblem &p) {
+    int nseg, len;
+    tc_segments(p, &nseg, &len);
+    return nseg > 1 ? (size_t)3 * p.B * p.H * nseg * 16384 * sizeof(float) : 0;
+}
+
+int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream) {
     CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, p.q, p.B, p.T, p.H, false) || !make_map(&mk, p.k, p.B, p.T, p.H, false) ||
         !make_map(&mv, p.v, p.B, p.T, p.H, false) ||
         !make_map(&mo, p.out, p.B, p.T, p.H, !p.out_bf16))
         return kErrCuda;
     TcArgs ta{p.log_alpha, (const __nv_bfloat16 *)p.beta, p.init_state, p.final_state,
-              status_word, (int)p.T, (int)p.H, p.NC};
-    const unsigned grid = (unsigned)(p.B * p.H);
-    if (p.out_bf16)
-        return p.gate == 1 ? launch_t<__nv_bfloat16, 1>(mq, mk, mv, mo, ta, grid, stream)
-                           : launch_t<__nv_bfloat16, 0>(mq, mk, mv, mo, ta, grid, stream);
-    return p.gate == 1 ? launch_t<float, 1>(mq, mk, mv, mo, ta, grid, stream)
-                       : launch_t<float, 0>(mq, mk, mv, mo, ta, grid, stream);
+              status_word, (int)p.T, (int)p.H, p.NC, 0, 1, p.NC, nullptr, nullptr, nullptr};
+    auto launch = [&](const TcArgs &t, unsigned grid) {
+        if (p.out_bf16)
+            return p.gate == 1 ? launch_t<__nv_bfloat16, 1>(mq, mk, mv, mo, t, grid, stream)
+                               : launch_t<__nv_bfloat16, 0>(mq, mk, mv, mo, t, grid, stream);
+        return p.gate == 1 ? launch_t<float, 1>(mq, mk, mv, mo, t, grid, stream)
+                           : launch_t<float, 0>(mq, mk, mv, mo, t, grid, stream);
+    };
+    const unsigned bh = (unsigned)(p.B * p.H);
+    int nseg, seg_len;
+    tc_segments(p, &nseg, &seg_len);
+    if (nseg <= 1) return launch(ta, bh);
+    // segments: end states (two runs per segment), chaining, then outputs
+    float *ws = reinterpret_cast<float *>(workspace);
+    const size_t per = (size_t)bh * nseg * 16384;
+    ta.nseg = nseg;
+    ta.seg_len = seg_len;
+    ta.ws_phi = ws;
+    ta.ws_s0 = ws + per;
+    ta.ws_start = ws + 2 * per;
+    ta.role = 1;
+    int rc = launch(ta, bh * nseg * 2);
+    if (rc != kOk) return rc;
+    seg_combine_kernel<<<bh * 4, 256, 0, stream>>>(p.init_state, ta.ws_phi, ta.ws_s0, ta.ws_start, nseg);
+    if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+    ta.role = 2;
+    return launch(ta, bh * nseg);
 }
 
 }  // namespace dr

@@ -190,3 +190,34 @@ def test_tc_deterministic(dr):
 def test_tc_needs_no_workspace(dr):
     desc = dr.chunk_desc(8, 4096, 16, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_SCALAR, 64)
     assert dr.workspace_bytes(desc) == 0
+
+
+# ------------------------------------------------------------ segmented long sequences
+# Few chains with many chunks are split into segments (end states, chaining, outputs).
+@pytest.mark.parametrize("gate,T,la_range", [
+    ("scalar", 4096, (0.001, 0.1)),     # 2 chains x 64 chunks -> 4 segments of 16 chunks
+    ("none", 3000, (0.001, 0.1)),       # DeltaNet: transitions do not decay; ragged tail
+    ("scalar", 2500, (0.0, 0.02)),      # weak decay: the carried state matters across segments
+])
+def test_tc_segmented_long(dr, gate, T, la_range):
+    d = inputs.chunk_inputs(1, T, 2, 128, 128, gate=gate, dtype="bf16", init_state=True,
+                            seed=31, log_alpha_range=la_range)
+    desc = dr.chunk_desc(1, T, 2, 128, 128, dr.DR_BF16, dr.DR_BF16,
+                         inputs.GATE_CODE[gate], 64)
+    assert dr.workspace_bytes(desc) > 0          # the segmented path is taken
+    check(dr, d, "bf16")
+
+
+def test_tc_segmented_in_place_carry(dr):
+    """final_state == init_state on the segmented path."""
+    d = inputs.chunk_inputs(1, 2048, 2, 128, 128, gate="scalar", dtype="bf16",
+                            init_state=True, seed=32, log_alpha_range=(0.0, 0.02))
+    g = dev(d)
+    st = g["init_state"].clone()
+    out, fin = dr.chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], st,
+                            final_state=st)
+    torch.cuda.synchronize()
+    o_ref, f_ref = oracle.forward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                  d["init_state"])
+    assert_close(out, o_ref, "bf16", "out")
+    assert_close(st, f_ref, "bf16", "final_state")
