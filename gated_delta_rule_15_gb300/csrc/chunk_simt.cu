@@ -58,7 +58,83 @@ struct StateArgs {
 };
 
 size_t prep_smem_bytes(int dk) {
-    return sizeof(float) * (size_t)(3 * 64 * kLd + 64 * dk + 16 * dk + 2 * 64 * kLdA + 64 + 64);
+    return sizeof(float) * (size_t)(3 * 64 * kLd + 64 * dk + 16 * dk + 2 * 64 * kLdA + 64 + 64 + 1024);
+}
+
+// out(r, n) (r, n < 16) = sum_{k < 16 nk} L(r, k) R(k, n) by one warp in fp32; lane owns row
+// lane / 2 and columns 8 (lane % 2) .. + 7; result written through st(r, n, v).
+template <class FL, class FR, class FS>
+__device__ __forceinline__ void warp_tile16(FL L, FR R, int nk, FS st, int lane) {
+    const int r = lane >> 1, n0 = 8 * (lane & 1);
+    float acc[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+    for (int k = 0; k < 16 * nk; ++k) {
+        const float l = L(r, k);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[m] = fmaf(l, R(k, n0 + m), acc[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) st(r, n0 + m, acc[m]);
+}
+
+// T = (I + A)^{-1} for C = 64 in fp32 by 16 x 16 blocks (A, T: [64][kLdA]; M: 1024 floats):
+// the diagonal blocks by right-looking substitution (four threads per column, the pivot
+// value broadcast by a shuffle), then T_ij = -T_ii sum_{j <= k < i} A_ik T_kj: T_10 and
+// T_32, then the lower-left 32 x 32 quarter through M = A[32:64, 0:32] T[0:32, 0:32].
+// Only the lower triangle of T (diagonal included) is written.  All 256 threads; ends with a
+// barrier.
+__device__ __forceinline__ void solve64_blocked(const float *sA, float *sT, float *sM, int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+    {
+        const int o = 16 * (tid >> 6), c = (tid >> 2) & 15, part = tid & 3, owner = lane & ~3;
+        float ar[4][16];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int q = 0; q < 16; ++q) ar[m][q] = sA[(o + part + 4 * m) * kLdA + o + q];
+        float y[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) y[m] = (part + 4 * m == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < 15; ++s2) {
+            const float xs = __shfl_sync(0xffffffffu, y[s2 >> 2], owner | (s2 & 3));
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                if (part + 4 * m > s2) y[m] = fmaf(-ar[m][s2], xs, y[m]);
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) sT[(o + part + 4 * m) * kLdA + o + c] = y[m];
+    }
+    __syncthreads();
+    if (warp < 2) {
+        const int i = 2 * warp + 1, j = 2 * warp;
+        float *Ms = sM + 256 * warp;
+        warp_tile16([&](int r, int k) { return sA[(16 * i + r) * kLdA + 16 * j + k]; },
+                    [&](int k, int n) { return sT[(16 * j + k) * kLdA + 16 * j + n]; }, 1,
+                    [&](int r, int n, float v) { Ms[r * 16 + n] = v; }, lane);
+        __syncwarp();
+        warp_tile16([&](int r, int k) { return sT[(16 * i + r) * kLdA + 16 * i + k]; },
+                    [&](int k, int n) { return Ms[k * 16 + n]; }, 1,
+                    [&](int r, int n, float v) { sT[(16 * i + r) * kLdA + 16 * j + n] = -v; }, lane);
+    }
+    __syncthreads();
+    if (warp < 4) {   // M tile (rb, cb) = sum_{k = cb}^{1} A_{rb,k} T_{k,cb}
+        const int rb = 2 + (warp >> 1), cb = warp & 1;
+        float *Mt = sM + 256 * warp;
+        warp_tile16([&](int r, int k) { return sA[(16 * rb + r) * kLdA + 16 * cb + k]; },
+                    [&](int k, int n) { return sT[(16 * cb + k) * kLdA + 16 * cb + n]; }, 2 - cb,
+                    [&](int r, int n, float v) { Mt[r * 16 + n] = v; }, lane);
+    }
+    __syncthreads();
+    if (warp < 4) {   // T_{rb,cb} = -sum_{k = 2}^{rb} T_{rb,k} M_{k,cb}
+        const int rb = 2 + (warp >> 1), cb = warp & 1;
+        warp_tile16([&](int r, int k) { return sT[(16 * rb + r) * kLdA + 32 + k]; },
+                    [&](int k, int n) { return sM[256 * (((k >> 4) << 1) | cb) + (k & 15) * 16 + n]; },
+                    rb - 1,
+                    [&](int r, int n, float v) { sT[(16 * rb + r) * kLdA + 16 * cb + n] = -v; }, lane);
+    }
+    __syncthreads();
 }
 
 template <int DK, typename Tin>
@@ -73,6 +149,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
     float *sT = sA + 64 * kLdA;                    // [64][kLdA] T = (I + A)^-1
     float *sB = sT + 64 * kLdA;                    // [64] beta
     float *sg = sB + 64;                           // [64] cumulative log decay (scalar)
+    float *sM = sg + 64;                           // [1024] scratch of the blocked solve
 
     const Tin *q = (const Tin *)a.q, *k = (const Tin *)a.k, *v = (const Tin *)a.v;
     const Tin *beta = (const Tin *)a.beta;
@@ -89,10 +166,18 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
     // 1. beta and the cumulative log decay (padded rows: beta = 0, log a = 0).
     for (int r = tid; r < C; r += kThreads) sB[r] = r < Lc ? to_f32(beta[tok(r)]) : 0.f;
     if (gate == 2) {
+        // stage the chunk's log alpha rows (coalesced, all loads in flight), then scan
+        for (int idx = tid; idx < C * (DK / 4); idx += kThreads) {
+            const int r = idx / (DK / 4), c4 = 4 * (idx % (DK / 4));
+            *reinterpret_cast<float4 *>(sG + r * DK + c4) =
+                r < Lc ? *reinterpret_cast<const float4 *>(a.log_alpha + tok(r) * DK + c4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncthreads();
         for (int ch = tid; ch < DK; ch += kThreads) {
             float acc = 0.f;
             for (int r = 0; r < C; ++r) {
-                if (r < Lc) acc += a.log_alpha[tok(r) * DK + ch];
+                acc += sG[r * DK + ch];
                 sG[r * DK + ch] = acc;
             }
         }
@@ -203,9 +288,11 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
     }
     __syncthreads();
 
-    // 5. T = (I + A)^{-1} by forward substitution, column j by the 4 lanes tid/4 == j:
-    //    T_rj = delta_rj - sum_{j <= s < r} A_rs T_sj.
-    {
+    // 5. T = (I + A)^{-1}: blocked for C = 64; otherwise by forward substitution, column j
+    //    by the 4 lanes tid/4 == j: T_rj = delta_rj - sum_{j <= s < r} A_rs T_sj.
+    if (C == 64) {
+        solve64_blocked(sA, sT, sM, tid);
+    } else {
         const int j = tid >> 2, part = tid & 3;
         for (int r = part; r < C; r += 4)
             if (j < C) sT[r * kLdA + j] = (r == j) ? 1.f : 0.f;

@@ -1,0 +1,198 @@
+// tc_common.cuh -- device helpers shared by the tensor-core chunk kernels: bounded mbarrier
+// waits, bf16 packing (single and high/low pairs), warp-level TF32 16 x 16 products and the
+// blocked 64 x 64 unit-lower-triangular inverse.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "umma.cuh"
+
+namespace dr {
+namespace tc {
+
+using namespace umma;
+
+constexpr long long kWaitCycles = 2000000000LL;   // ~1 s at the loaded SM clock
+
+__device__ __forceinline__ bool wait_cycles(uint64_t *bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi); packs two such pairs.
+__device__ __forceinline__ void pack_hi_lo(float a, float b, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
+    __nv_bfloat162 h2;
+    h2.x = ha;
+    h2.y = hb;
+    hi = *reinterpret_cast<uint32_t *>(&h2);
+    lo = pack_bf16(a - __bfloat162float(ha), b - __bfloat162float(hb));
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+// d += a (16 x 8, row) * b (8 x 8, col), TF32 operands, fp32 accumulate (one warp).
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// acc (16 x 16, mma.sync C fragment) += L (16 x 16 nk) * R (16 nk x 16); one warp.
+// L(r, k) and R(k, n) return fp32 elements; operands are rounded to TF32.
+template <class FL, class FR>
+__device__ __forceinline__ void warp_mm16(float (&acc)[2][4], FL L, FR R, int nk, int g, int t4) {
+    for (int kt = 0; kt < 2 * nk; ++kt) {
+        const int kc = 8 * kt;
+        const uint32_t af[4] = {to_tf32(L(g, kc + t4)), to_tf32(L(g + 8, kc + t4)),
+                                to_tf32(L(g, kc + t4 + 4)), to_tf32(L(g + 8, kc + t4 + 4))};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+            mma_tf32_16x8x8(acc[nt], af, to_tf32(R(kc + t4, 8 * nt + g)),
+                            to_tf32(R(kc + t4 + 4, 8 * nt + g)));
+    }
+}
+// Writes sign * acc through st(r, n, v0, v1): elements (r, n) and (r, n + 1), n even.
+template <class FS>
+__device__ __forceinline__ void warp_store16(const float (&acc)[2][4], float sign, FS st, int g, int t4) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int n = 8 * nt + 2 * t4;
+        st(g, n, sign * acc[nt][0], sign * acc[nt][1]);
+        st(g + 8, n, sign * acc[nt][2], sign * acc[nt][3]);
+    }
+}
+
+constexpr int kTs = 68;   // row stride (floats) of the fp32 T matrix: 16-byte aligned rows
+
+// Element (r, s) of the fp32 A matrix: rows of 64, 16-byte groups XOR-swizzled by r % 16.
+__device__ __forceinline__ int a_index(int r, int s) {
+    return r * 64 + ((((s >> 2) ^ (r & 15)) << 2) | (s & 3));
+}
+
+// T = (I + A)^-1 for a strictly lower-triangular 64 x 64 A (fp32), T stored [64][kTs].
+//   1. the four diagonal 16 x 16 blocks by right-looking substitution, four threads per
+//      column (each owns four rows; the pivot row's value is broadcast by a shuffle);
+//   2. T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (two warps);
+//   3. lower-left 32 x 32 quarter: M = A[32:64, 0:32] T[0:32, 0:32], then
+//      T[32:64, 0:32] = -T[32:64, 32:64] M (four warps, one 16 x 16 tile each).
+// Each element is written, once final, also as T diag(beta) and T diag(beta G) in bf16
+// (128-byte-swizzled K-major 64 x 64 tiles at TB and TB + 8192): the U and W operands.
+// Products use TF32 mma.sync with fp32 accumulation.  M needs 1024 floats.  Called by all
+// 256 threads; starts after and ends with a barrier.
+__device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, float *M,
+                                                   unsigned char *TB, const float *beta,
+                                                   const float *gam, int tid) {
+    auto a = [&](int r, int s) { return A[a_index(r, s)]; };
+    // final element (r, s) of T: fp32 copy for the later levels, and the two bf16 MMA
+    // operands T diag(beta) (at TB) and T diag(beta G) (at TB + 8192)
+    auto fin = [&](int r, int s, float v) {
+        T[r * kTs + s] = v;
+        const float vb = v * beta[s];
+        const uint32_t off = sw128_off(r, s);
+        *reinterpret_cast<__nv_bfloat16 *>(TB + off) = __float2bfloat16_rn(vb);
+        *reinterpret_cast<__nv_bfloat16 *>(TB + 8192 + off) = __float2bfloat16_rn(vb * gam[s]);
+    };
+    // final elements (r, s) and (r, s + 1), s even: one 32-bit store per operand
+    auto fin2 = [&](int r, int s, float v0, float v1) {
+        *reinterpret_cast<float2 *>(T + r * kTs + s) = make_float2(v0, v1);
+        const float b0 = v0 * beta[s], b1 = v1 * beta[s + 1];
+        const uint32_t off = sw128_off(r, s);
+        *reinterpret_cast<uint32_t *>(TB + off) = pack_bf16(b0, b1);
+        *reinterpret_cast<uint32_t *>(TB + 8192 + off) = pack_bf16(b0 * gam[s], b1 * gam[s + 1]);
+    };
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+    {
+        const int o = 16 * (tid >> 6), c = (tid >> 2) & 15, part = tid & 3;
+        const int owner = lane & ~3;
+        // this thread's four rows of the diagonal block, o + part + 4m, columns o .. o + 15
+        float ar[4][16];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int r = o + part + 4 * m;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(A + a_index(r, o + 4 * q));
+                ar[m][4 * q] = v4.x; ar[m][4 * q + 1] = v4.y;
+                ar[m][4 * q + 2] = v4.z; ar[m][4 * q + 3] = v4.w;
+            }
+        }
+        float y[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) y[m] = (part + 4 * m == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < 15; ++s2) {
+            const float xs = __shfl_sync(0xffffffffu, y[s2 >> 2], owner | (s2 & 3));
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                if (part + 4 * m > s2) y[m] = fmaf(-ar[m][s2], xs, y[m]);
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) fin(o + part + 4 * m, o + c, y[m]);
+        // the six blocks above the diagonal are zero in the bf16 operands (the fp32 copy
+        // of those blocks is never read): (0,1) (0,2) (0,3) (1,2) (1,3) (2,3), 8 per task
+        for (int idx = tid; idx < 6 * 32; idx += 256) {
+            const int blk = idx >> 5, e = idx & 31;
+            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            const uint32_t off = sw128_off(16 * bi + (e >> 1), 16 * bj + 8 * (e & 1));
+            *reinterpret_cast<uint4 *>(TB + off) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(TB + 8192 + off) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    __syncthreads();
+    if (warp < 2) {
+        const int i = 2 * warp + 1, j = 2 * warp;
+        float *Ms = M + 256 * warp;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        warp_mm16(acc, [&](int r, int k) { return a(16 * i + r, 16 * j + k); },
+                  [&](int k, int n) { return T[(16 * j + k) * kTs + 16 * j + n]; }, 1, g, t4);
+        warp_store16(acc, 1.f, [&](int r, int n, float v0, float v1) {
+            *reinterpret_cast<float2 *>(Ms + r * 16 + n) = make_float2(v0, v1); }, g, t4);
+        __syncwarp();
+        float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        warp_mm16(acc2, [&](int r, int k) { return T[(16 * i + r) * kTs + 16 * i + k]; },
+                  [&](int k, int n) { return Ms[k * 16 + n]; }, 1, g, t4);
+        warp_store16(acc2, -1.f, [&](int r, int n, float v0, float v1) {
+            fin2(16 * i + r, 16 * j + n, v0, v1); }, g, t4);
+    }
+    __syncthreads();
+    if (warp < 4) {   // M tile (rb, cb) = sum_{k = cb}^{1} A_{rb,k} T_{k,cb},  rb = 2 + w/2, cb = w%2
+        const int rb = 2 + (warp >> 1), cb = warp & 1;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        warp_mm16(acc, [&](int r, int k) { return a(16 * rb + r, 16 * cb + k); },
+                  [&](int k, int n) { return T[(16 * cb + k) * kTs + 16 * cb + n]; }, 2 - cb, g, t4);
+        float *Mt = M + 256 * warp;
+        warp_store16(acc, 1.f, [&](int r, int n, float v0, float v1) {
+            *reinterpret_cast<float2 *>(Mt + r * 16 + n) = make_float2(v0, v1); }, g, t4);
+    }
+    __syncthreads();
+    if (warp < 4) {   // T_{rb,cb} = -sum_{k = 2}^{rb} T_{rb,k} M_{k,cb}
+        const int rb = 2 + (warp >> 1), cb = warp & 1;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        warp_mm16(acc, [&](int r, int k) { return T[(16 * rb + r) * kTs + 32 + k]; },
+                  [&](int k, int n) { return M[256 * (((k >> 4) << 1) | cb) + (k & 15) * 16 + n]; },
+                  rb - 1, g, t4);
+        warp_store16(acc, -1.f, [&](int r, int n, float v0, float v1) {
+            fin2(16 * rb + r, 16 * cb + n, v0, v1); }, g, t4);
+    }
+    fence_proxy_async();   // the bf16 operands are read next by the tensor core
+    __syncthreads();
+}
+
+}  // namespace tc
+}  // namespace dr
