@@ -62,6 +62,12 @@ int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStrea
 bool chunk_tc_supported(const ChunkProblem &p);
 size_t chunk_tc_workspace_bytes(const ChunkProblem &p);
 int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream);
+// Two-kernel tensor-core path for the per-channel gate (chunk_kda.cu): bf16 inputs,
+// dk = dv = 128, C = 64, T > 0.  Its workspace holds the per-chunk operands that the
+// prep kernel writes and the state kernel reads (chunk_kda_workspace_bytes).
+bool chunk_kda_supported(const ChunkProblem &p);
+size_t chunk_kda_workspace_bytes(const ChunkProblem &p);
+int launch_chunk_kda(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream);
 int launch_decode(int64_t BH, int dk, int dv, int in_bf16, int out_bf16, int gate,
                   const void *q, const void *k, const void *v, const float *la,
                   const void *beta, float *state, void *out, cudaStream_t s);

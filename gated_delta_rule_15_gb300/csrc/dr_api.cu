@@ -63,9 +63,12 @@ extern "C" int dr_chunk_fwd_workspace_bytes(const dr_chunk_desc *desc, size_t *b
     ChunkProblem p{};
     const int rc = check_chunk_desc(desc, &p);
     if (rc != kOk) return rc;
-    *bytes = chunk_tc_supported(p)
-                 ? chunk_tc_workspace_bytes(p)
-                 : sizeof(float) * simt_workspace_floats(p.B, p.H, p.NC, p.C, p.dk, p.dv);
+    if (chunk_tc_supported(p))
+        *bytes = chunk_tc_workspace_bytes(p);
+    else if (chunk_kda_supported(p))
+        *bytes = chunk_kda_workspace_bytes(p);
+    else
+        *bytes = sizeof(float) * simt_workspace_floats(p.B, p.H, p.NC, p.C, p.dk, p.dv);
     return kOk;
 }
 
@@ -97,6 +100,11 @@ extern "C" int dr_chunk_fwd(const dr_chunk_desc *desc, const void *q, const void
         int *status = device_status_ptr();
         if (!status) return kErrCuda;
         return launch_chunk_tc(p, workspace, status, (cudaStream_t)stream);
+    }
+    if (chunk_kda_supported(p)) {
+        int *status = device_status_ptr();
+        if (!status) return kErrCuda;
+        return launch_chunk_kda(p, workspace, status, (cudaStream_t)stream);
     }
     const ChunkWorkspace ws = simt_workspace_carve(workspace, p.B, p.H, p.NC, p.C, p.dk, p.dv);
     return launch_chunk_simt(p, ws, (cudaStream_t)stream);

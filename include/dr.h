@@ -138,10 +138,12 @@ int dr_recurrent_step(const dr_step_desc *desc,
  * DR_NOALLOC_SCRATCH_BYTES that libdr.so holds on every GPU it is loaded on until exit.
  *
  *   - Problems whose dr_chunk_fwd_workspace_bytes() exceeds DR_NOALLOC_SCRATCH_BYTES are
- *     rejected with DR_ERR_WORKSPACE before anything is enqueued.  The fused tensor-core
- *     path (bf16, dk = dv = 128, C = 64, scalar or no gate) needs none; the CUDA-core path
- *     (fp32 inputs, per-channel gate, other sizes) needs 147,968 bytes per (b, h, chunk)
- *     at dk = dv = 128, C = 64, so there B * H * ceil(T / 64) <= 453.
+ *     rejected with DR_ERR_WORKSPACE before anything is enqueued.  At bf16 inputs,
+ *     dk = dv = 128, C = 64: the fused tensor-core path (scalar or no gate) needs none
+ *     unless few long chains are split into segments; the per-channel gate needs 131,584
+ *     bytes per (b, h, chunk), so there B * H * ceil(T / 64) <= 510.  The CUDA-core path
+ *     (fp32 inputs, other sizes) needs 147,968 bytes per (b, h, chunk) at dk = dv = 128,
+ *     C = 64, so there B * H * ceil(T / 64) <= 453.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress
  *     with that device current); make that first call before any stream capture.
  *   - Every call shares the array.  Calls whose work overlaps on the GPU (other streams,

@@ -45,7 +45,7 @@ def test_version_and_strerror(dr):
 
 
 def _desc(dr, **kw):
-    # per-channel gate: the CUDA-core path, which needs a workspace
+    # per-channel gate: a two-kernel path, which needs a workspace
     d = dict(B=2, T=100, H=3, dk=128, dv=128, in_dtype=dr.DR_BF16, out_dtype=dr.DR_BF16,
              gate=dr.DR_GATE_CHANNEL, chunk=64)
     d.update(kw)

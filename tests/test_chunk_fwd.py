@@ -221,3 +221,79 @@ def test_tc_segmented_in_place_carry(dr):
                                   d["init_state"])
     assert_close(out, o_ref, "bf16", "out")
     assert_close(st, f_ref, "bf16", "final_state")
+
+
+# ------------------------------------------------------------ per-channel gate, tensor cores
+# bf16 inputs, d_k = d_v = 128, C = 64, per-channel gate: the prep + state kernel pair.
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 127, 129, 200])
+def test_kda_tc_edge_lengths(dr, T):
+    d = inputs.chunk_inputs(2, T, 3, 128, 128, gate="channel", dtype="bf16",
+                            init_state=True, seed=200 + T)
+    check(dr, d, "bf16")
+
+
+def test_kda_tc_many_heads(dr):
+    d = inputs.chunk_inputs(3, 333, 5, 128, 128, gate="channel", dtype="bf16",
+                            init_state=True, seed=8)
+    check(dr, d, "bf16")
+
+
+@pytest.mark.parametrize("la_range", [(0.0, 1.0), (0.0, 5.0)])
+def test_kda_tc_strong_decay(dr, la_range):
+    """Per-token log decays up to -5 per channel: a 16-token block can decay by e^-80."""
+    d = inputs.chunk_inputs(2, 300, 2, 128, 128, gate="channel", dtype="bf16",
+                            init_state=True, seed=15, log_alpha_range=la_range)
+    check(dr, d, "bf16")
+
+
+def test_kda_tc_extreme_decay_exact_diagonal(dr):
+    """log alpha ~ -U(0, 20): every 16-token block decays past exp(-64) in some channel, so
+    the diagonal blocks of the intra-chunk products are taken on the exact fallback."""
+    d = inputs.chunk_inputs(1, 256, 2, 128, 128, gate="channel", dtype="bf16",
+                            init_state=True, seed=16, log_alpha_range=(0.0, 20.0))
+    check(dr, d, "bf16", out_dtype=torch.float32)
+
+
+def test_kda_tc_mixed_decay(dr):
+    """Half of the channels barely decay, half decay steeply: the exact fallback runs for
+    the chunk while the slow channels still carry state across chunks."""
+    d = inputs.chunk_inputs(1, 320, 2, 128, 128, gate="channel", dtype="bf16",
+                            init_state=True, seed=17, log_alpha_range=(0.0, 0.01))
+    d["log_alpha"][..., 64:] *= 2000.0      # -U(0, 20) on channels 64..127
+    check(dr, d, "bf16", out_dtype=torch.float32)
+
+
+def test_kda_tc_fp32_output_strict(dr):
+    d = inputs.chunk_inputs(2, 500, 4, 128, 128, gate="channel", dtype="bf16",
+                            init_state=True, seed=18)
+    check(dr, d, "bf16", out_dtype=torch.float32)
+
+
+def test_kda_tc_deterministic(dr):
+    d = inputs.chunk_inputs(2, 300, 3, 128, 128, gate="channel", dtype="bf16", seed=19)
+    o1, f1 = run(dr, d)
+    o2, f2 = run(dr, d)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
+def test_kda_tc_in_place_carry(dr):
+    d = inputs.chunk_inputs(2, 190, 2, 128, 128, gate="channel", dtype="bf16",
+                            init_state=True, seed=20)
+    g = dev(d)
+    st = g["init_state"].clone()
+    out, _ = dr.chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], st,
+                          final_state=st)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    o_ref, f_ref = oracle.forward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                  d["init_state"])
+    assert_close(out, o_ref, "bf16", "out")
+    assert_close(st, f_ref, "bf16", "final_state")
+
+
+def test_kda_tc_workspace_bytes(dr):
+    # per (b, h, chunk): W 16 KiB, U 32 KiB, P pair 16 KiB, Q*G and K*G_C/G pairs 64 KiB,
+    # G_C 512 B
+    desc = dr.chunk_desc(4, 8192, 32, 128, 128, dr.DR_BF16, dr.DR_BF16,
+                         dr.DR_GATE_CHANNEL, 64)
+    assert dr.workspace_bytes(desc) == 4 * 32 * 128 * 131584

@@ -42,8 +42,8 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
     import gated_delta_rule_15_gb300.dr as dr
-    # The per-channel gate runs on the CUDA-core path, which needs 147,968 B of workspace
-    # per (b, h, chunk) at d = 128: 600 chunks of one head exceed 64 MiB.
+    # The per-channel gate (bf16, d = 128, C = 64) needs 131,584 B of workspace per
+    # (b, h, chunk): 600 chunks of one head exceed 64 MiB.
     T = 64 * 600
     desc = dr.chunk_desc(1, T, 1, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_CHANNEL, 64)
     assert dr.workspace_bytes(desc) > dr.NOALLOC_SCRATCH_BYTES
