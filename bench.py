@@ -63,6 +63,26 @@ def tc_path(w):
             and w.gate in ("none", "scalar") and w.T > 0)
 
 
+def kda_path(w):
+    """The prep + state tensor-core pair serves the same shapes with the per-channel gate."""
+    return (w.dtype == "bf16" and w.dk == 128 and w.dv == 128 and w.chunk == 64
+            and w.gate == "channel" and w.T > 0)
+
+
+def path_kernels(w):
+    """Kernels one dr_chunk_fwd call launches for workload w, in launch order (the segment
+    rule mirrors the library's: chains <= 76 with >= 32 chunks are split for 152 SMs)."""
+    if tc_path(w):
+        nc, bh = -(-w.T // w.chunk), w.B * w.H
+        if bh <= 76 and nc >= 32 and min(nc // 16, 152 // bh) >= 2:
+            return ["chunk_tc_kernel (segment end states)", "seg_combine_kernel",
+                    "chunk_tc_kernel (segment outputs)"]
+        return ["chunk_tc_kernel"]
+    if kda_path(w):
+        return ["kda_prep_kernel", "kda_state_kernel"]
+    return ["chunk_prep_kernel", "chunk_state_kernel"]
+
+
 # ------------------------------------------------------------------ algorithmic counts
 def chunk_bytes(w):
     """Each input read once, each output written once; a zero initial state is not read."""
@@ -301,8 +321,8 @@ def run_native(args):
     ach_gbs = byts / (ms * 1e-3) / 1e9
     e2e_ms, h2d, d2h = bench_chunk_e2e(w, r["host_inputs"], max(2, args.steps // 2),
                                        max(3, args.warmup), world)
-    on_tc = tc_path(w)
-    launches_per_call = 1 if on_tc else 2
+    kernels = path_kernels(w)
+    launches_per_call = len(kernels)
 
     extra = {}
     if not args.quick:
@@ -316,7 +336,8 @@ def run_native(args):
                 "gbs": bx / (rx["ms"] * 1e-3) / 1e9,
                 "hbm_frac": bx / (rx["ms"] * 1e-3) / 1e9 / hbm,
                 "tflops": fx / (rx["ms"] * 1e-3) / 1e12,
-                "tensor_frac": fx / (rx["ms"] * 1e-3) / 1e12 / tc}
+                "tensor_frac": fx / (rx["ms"] * 1e-3) / 1e12 / tc,
+                "kernels": path_kernels(wx)}
             del rx
     decode = {}
     for name in ("decode_scalar_B256_H32_d128", "decode_channel_B256_H32_d128"):
@@ -347,8 +368,7 @@ def run_native(args):
         "roofline": {"bound": "hbm", "achieved": ach_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": ach_gbs / hbm, "peak_source": pk_kind,
                      "traffic": (tr["bytes"] if tr and tr["src"] == src else None),
-                     "kernel": ("chunk_tc_kernel (fused tcgen05, one launch per call)" if on_tc else
-                                "chunk_prep_kernel + chunk_state_kernel"),
+                     "kernel": " + ".join(kernels),
                      "algorithmic_bytes": byts,
                      "tensor_tflops": flops / (ms * 1e-3) / 1e12,
                      "tensor_frac": flops / (ms * 1e-3) / 1e12 / tc},

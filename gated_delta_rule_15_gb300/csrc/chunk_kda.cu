@@ -69,18 +69,27 @@ KdaWorkspace kda_carve(void *base, int64_t nch) {
 }
 
 // ---------------------------------------------------------------- prep kernel layout
-constexpr uint32_t P1_Q = 0, P1_K = 16384, P1_V = 32768;   // 64 x 128 bf16 tiles, 2 K-blocks
-constexpr uint32_t P1_LA = 49152;    // log alpha, then g: 4 boxes [64][32] fp32 (no swizzle)
-constexpr uint32_t P1_OPS = 81920;   // round operands; after them A, T, T diag(beta), K*G
-constexpr uint32_t P1_LH = P1_OPS, P1_LL = P1_OPS + 32768;   // [L_Q kb0|L_K kb0|L_Q kb1|L_K kb1]
-constexpr uint32_t P1_RH = P1_OPS + 65536, P1_RL = P1_OPS + 69632;   // [R kb0 | R kb1], 2 KB each
-constexpr uint32_t P1_A = P1_OPS, P1_T = P1_OPS + 16384, P1_TB = P1_OPS + 34816,
-                   P1_KG = P1_OPS + 51200;
-constexpr uint32_t P1_SMALL = P1_OPS + 73728;   // beta[64], ones[64], solve scratch[1024]
-constexpr uint32_t P1_TOTAL = P1_SMALL + 8192;
-constexpr uint32_t P1_TM_X = 0, P1_TM_U = 64, P1_TM_W = 128;
+// Sized for two CTAs per SM (<= 113 KB each): the left factors of the intra-chunk products
+// live in tensor memory (A operand of tcgen05.mma), the right factors in shared memory.
+constexpr uint32_t P1_Q = 0, P1_K = 16384;    // 64 x 128 bf16 tiles, 2 K-blocks, 128B swizzle
+constexpr uint32_t P1_LA = 32768;             // log alpha -> g: 4 boxes [64][32] fp32, 128B swizzle
+constexpr uint32_t P1_V = 65536, P1_KG = 81920;
+constexpr uint32_t P1_R = 98304;              // right factors: high [kb][16][64], low at +4096
+constexpr uint32_t P1_SMALL = 106496;         // beta[64], solve scratch[1024]
+constexpr uint32_t P1_TOTAL = P1_SMALL + 256 + 4096 + 512;   // + G_C[128]
+// after the products: A over Q, T over K (and the first KB of g), T diag(beta) inside g,
+// the exact diagonal blocks over the right factors; staging of W and U at the end
+constexpr uint32_t P1_A = 0, P1_T = 16384, P1_TB = 34816, P1_XD = P1_R;
+constexpr uint32_t P1_WST = 0, P1_UST = 16384;
+// one-product chunks: the right factor's high half over V, its low half over K*G
+constexpr uint32_t P1_R1H = P1_V, P1_R1L = P1_KG;
+// tensor memory: X = [Q; K] R^T, the left factor's high and low halves; U^T, W^T afterwards
+constexpr uint32_t P1_TM_X = 0, P1_TM_LH = 64, P1_TM_LL = 128, P1_TM_U = 64, P1_TM_W = 128;
+static_assert(P1_T + 64 * kTs * 4 <= P1_TB && P1_TB + 8192 <= P1_V, "prep layout");
+static_assert(P1_UST + 32768 <= P1_V && P1_TOTAL + 1024 <= 113 * 1024, "prep layout");
 
 constexpr uint32_t ID_KK_N16 = idesc_bf16(128, 16, false, false);
+constexpr uint32_t ID_KK_N64 = idesc_bf16(128, 64, false, false);
 // Largest per-channel decay (natural log) inside one 16-token block that the tensor-core
 // products of the diagonal blocks take; beyond it the chunk recomputes those entries.
 constexpr float kDiagLimit = 64.f;
@@ -93,9 +102,10 @@ struct PrepArgs {
     int T, H, NC;
 };
 
-// Element (t, c) of the [64][128] fp32 tile loaded as four [64][32] boxes.
-__device__ __forceinline__ uint32_t la_off(int t, int c) {
-    return (uint32_t)((c >> 5) * 8192 + t * 128 + (c & 31) * 4);
+// Float index of element (t, c) of the [64][128] fp32 tile held as four 128-byte-swizzled
+// [64][32] boxes: 16-byte groups of a row permuted by t % 8.
+__device__ __forceinline__ int la_idx(int t, int c) {
+    return (c >> 5) * 2048 + t * 32 + ((((c & 31) >> 2) ^ (t & 7)) << 2) + (c & 3);
 }
 // Eight consecutive bf16 values (columns 8 c8 .. 8 c8 + 7) of row r of a swizzled tile.
 __device__ __forceinline__ void load8_bf16(const unsigned char *tile, int r, int c8, float (&v)[8]) {
@@ -108,24 +118,27 @@ __device__ __forceinline__ void load8_bf16(const unsigned char *tile, int r, int
         v[2 * i + 1] = f.y;
     }
 }
-__device__ __forceinline__ void load8_f32(const float *p, float (&v)[8]) {
-    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+// g at token t, channels c .. c + 7 (c a multiple of 8).
+__device__ __forceinline__ void load8_g(const float *LA, int t, int c, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4 *>(LA + la_idx(t, c));
+    const float4 b = *reinterpret_cast<const float4 *>(LA + la_idx(t, c + 4));
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tla,
+                const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
                 const PrepArgs a) {
     extern __shared__ unsigned char dsm_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
     __shared__ uint64_t bar_ld, bar_mma;
     __shared__ uint32_t tmem_base_s;
-    __shared__ int abort_s, diag_exact_s;
+    __shared__ int abort_s, diag_exact_s, four_rounds_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
-    const int row = 32 * quarter + lane;
+    const int row = 32 * quarter + lane;   // TMEM lane: row of [Q; K], or channel
     const int64_t n = blockIdx.x;
     const int c = (int)(n % a.NC);
     const int64_t bh = n / a.NC;
@@ -133,10 +146,15 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const int t0 = c * 64;
     const int Lc = min(64, a.T - t0);
     float *sBeta = reinterpret_cast<float *>(sm + P1_SMALL);
-    float *sOnes = sBeta + 64;
-    float *sM = sBeta + 128;
-    const float *LA = reinterpret_cast<const float *>(sm + P1_LA);
-    float *const Xd = reinterpret_cast<float *>(sm + P1_KG);   // exact diagonal blocks
+    float *sM = sBeta + 64;
+    float *sGamC = sM + 1024;   // G_C per channel
+    float *LA = reinterpret_cast<float *>(sm + P1_LA);
+    float *const Xd = reinterpret_cast<float *>(sm + P1_XD);   // exact diagonal blocks
+    const int t_row = row & 63, blk = t_row >> 4;   // this thread's row of [Q; K]: token, block
+    const bool qrow = quarter < 2;
+    const unsigned char *xt = sm + (qrow ? P1_Q : P1_K);
+    float *const sF = reinterpret_cast<float *>(sm + P1_V);        // [8][128] block factors
+    float *const sExpRef = sF + 8 * 128;                           // [4][128] exp(ref_i)
     bool diag_exact = false;
 
     if (tid == 0) {
@@ -144,6 +162,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         mbar_init(&bar_mma, 1);
         abort_s = 0;
         diag_exact_s = 0;
+        four_rounds_s = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -155,134 +174,291 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmb = tmem_base_s;
     const uint32_t tm = tmb + ((uint32_t)(32 * quarter) << 16);
+    uint32_t mma_phase = 0;
     auto fail = [&]() {
         abort_s = 1;
         atomicExch(a.status, kErrTimeout);
     };
 
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_ld, 49152 + 32768);
+        mbar_arrive_expect_tx(&bar_ld, 32768 + 32768);
         for (int kb = 0; kb < 2; ++kb) {
             tma_load_4d(sm + P1_Q + kb * 8192, &tq, &bar_ld, 64 * kb, h, t0, b);
             tma_load_4d(sm + P1_K + kb * 8192, &tk, &bar_ld, 64 * kb, h, t0, b);
-            tma_load_4d(sm + P1_V + kb * 8192, &tv, &bar_ld, 64 * kb, h, t0, b);
         }
         for (int bx = 0; bx < 4; ++bx)
             tma_load_4d(sm + P1_LA + bx * 8192, &tla, &bar_ld, 32 * bx, h, t0, b);
     }
-    if (tid < 64) {
+    if (tid < 64)
         sBeta[tid] = tid < Lc ? __bfloat162float(a.beta[((size_t)b * a.T + t0 + tid) * a.H + h]) : 0.f;
-        sOnes[tid] = 1.f;
-    }
     if (!wait_cycles(&bar_ld, 0)) fail();
     __syncthreads();
     if (abort_s) goto done;
 
-    // ---- cumulative log decay g (in place) and G_C = exp(g_63) per channel; flag the chunk
-    //      if some channel decays by more than kDiagLimit inside one 16-token block
+    // ---- cumulative log decay g (in place, one channel per thread, held in registers),
+    //      G_C = exp(g_63); flag the chunk if a channel decays by more than kDiagLimit
+    //      inside one 16-token block.  With ref_i = g at the last token of block i, the
+    //      per-channel factors exp(ref_i) and F_ij = exp(ref_i - ref_j) (i > j, both <= 1)
+    //      go to the V buffer, which is loaded only after the products.
     if (tid < 128) {
-        float *la = reinterpret_cast<float *>(sm + P1_LA);
-        float acc = 0.f;
-        bool steep = false;
-        for (int t = 0; t < 64; ++t) {
-            acc += la[la_off(t, tid) / 4];
-            la[la_off(t, tid) / 4] = acc;
-        }
+        float v[64];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            steep |= la[la_off(16 * j, tid) / 4] - la[la_off(16 * j + 15, tid) / 4] > kDiagLimit;
+        for (int t = 0; t < 64; ++t) v[t] = LA[la_idx(t, tid)];
+#pragma unroll
+        for (int t = 1; t < 64; ++t) v[t] += v[t - 1];
+#pragma unroll
+        for (int t = 0; t < 64; ++t) LA[la_idx(t, tid)] = v[t];
+        bool steep = false;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) steep |= v[16 * j] - v[16 * j + 15] > kDiagLimit;
         if (steep) diag_exact_s = 1;
-        a.ws.GAM[n * 128 + tid] = __expf(acc);
+        if (v[0] - v[63] > kDiagLimit) four_rounds_s = 1;
+        const float gc = __expf(v[63]);
+        a.ws.GAM[n * 128 + tid] = gc;
+        sGamC[tid] = gc;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sExpRef[i * 128 + tid] = __expf(v[16 * i + 15]);
+#pragma unroll
+        for (int i = 1; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < i; ++j)
+                sF[(i * (i - 1) / 2 + j) * 128 + tid] = __expf(v[16 * i + 15] - v[16 * j + 15]);
+        sF[6 * 128 + tid] = 1.f;   // same block
+        sF[7 * 128 + tid] = 0.f;   // row above the column block (entry masked)
     }
     __syncthreads();
+    diag_exact = diag_exact_s != 0;
 
-    // ---- X = [Q; K] K^T with per-channel decays, by column block j (tokens 16 j .. 16 j + 15),
-    //      against the reference g_ref = g at the block's last token: the right factor
-    //      k_s exp(g_ref - g_s) is <= |k_s|, the left factor exp(g_r - g_ref) is <= 1 below
-    //      the block and at most exp(kDiagLimit) inside it (clamped there; a flagged chunk
-    //      recomputes those entries below)
-    for (int j = 0; j < 4; ++j) {
-        const int ref = 16 * j + 15;
-        for (int task = tid; task < (64 - 16 * j) * 16; task += kThreads) {
-            const int r = 16 * j + (task >> 4), c8 = task & 15;
-            float q8[8], k8[8], g8[8], rf[8];
-            load8_bf16(sm + P1_Q, r, c8, q8);
-            load8_bf16(sm + P1_K, r, c8, k8);
-            load8_f32(LA + la_off(r, 8 * c8) / 4, g8);
-            load8_f32(LA + la_off(ref, 8 * c8) / 4, rf);
-            uint32_t qh[4], ql[4], kh[4], kl[4];
-#pragma unroll
-            for (int u = 0; u < 8; u += 2) {
-                const float f0 = __expf(fminf(g8[u] - rf[u], kDiagLimit));
-                const float f1 = __expf(fminf(g8[u + 1] - rf[u + 1], kDiagLimit));
-                pack_hi_lo(q8[u] * f0, q8[u + 1] * f1, qh[u >> 1], ql[u >> 1]);
-                pack_hi_lo(k8[u] * f0, k8[u + 1] * f1, kh[u >> 1], kl[u >> 1]);
-            }
-            const uint32_t off = (c8 >> 3) * 16384 + sw128_off(r, (8 * c8) & 63);
-            *reinterpret_cast<uint4 *>(sm + P1_LH + off) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
-            *reinterpret_cast<uint4 *>(sm + P1_LL + off) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
-            *reinterpret_cast<uint4 *>(sm + P1_LH + 8192 + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-            *reinterpret_cast<uint4 *>(sm + P1_LL + 8192 + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
-        }
+    if (!four_rounds_s) {
+        // ---- one product for the whole chunk against ref = g_63 (no channel decays by more
+        //      than kDiagLimit across the chunk): left factor xE_t = x_t exp(g_t - g_63) in
+        //      [|x|, |x| e^kDiagLimit] (tensor memory), right factor k_s exp(g_63 - g_s) =
+        //      (K*G_C/G)_s <= |k_s| (shared memory, and the workspace's pair).  Q rows also
+        //      write Q*G = xE G_C; K rows keep K*G = xE G_C for the W operand.
+        uint32_t kg_keep[32];
         {
-            const int rr = tid >> 4, c8 = tid & 15, s = 16 * j + rr;
-            float k8[8], g8[8], rf[8];
-            load8_bf16(sm + P1_K, s, c8, k8);
-            load8_f32(LA + la_off(s, 8 * c8) / 4, g8);
-            load8_f32(LA + la_off(ref, 8 * c8) / 4, rf);
-            uint32_t hi[4], lo[4];
+            const size_t go = ((size_t)n * 64 + t_row) * 128 + 64 * half;
 #pragma unroll
-            for (int u = 0; u < 8; u += 2)
-                pack_hi_lo(k8[u] * __expf(rf[u] - g8[u]), k8[u + 1] * __expf(rf[u + 1] - g8[u + 1]),
-                           hi[u >> 1], lo[u >> 1]);
-            const uint32_t off = (c8 >> 3) * 2048 + sw128_off(rr, (8 * c8) & 63);
-            *reinterpret_cast<uint4 *>(sm + P1_RH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(sm + P1_RL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            for (int p = 0; p < 2; ++p) {
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = 64 * half + 32 * p + 8 * i, w = 4 * (4 * p + i);
+                    float x8[8], g8[8], gl[8], e8[8];
+                    load8_bf16(xt, t_row, c >> 3, x8);
+                    load8_g(LA, t_row, c, g8);
+                    load8_g(LA, 63, c, gl);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) e8[u] = x8[u] * __expf(g8[u] - gl[u]);
+#pragma unroll
+                    for (int u = 0; u < 8; u += 2)
+                        pack_hi_lo(e8[u], e8[u + 1], hi[4 * i + (u >> 1)], lo[4 * i + (u >> 1)]);
+                    uint32_t oh[4], ol[4];
+                    if (qrow) {
+#pragma unroll
+                        for (int u = 0; u < 8; u += 2)
+                            pack_hi_lo(e8[u] * sGamC[c + u], e8[u + 1] * sGamC[c + u + 1], oh[u >> 1], ol[u >> 1]);
+                        *reinterpret_cast<uint4 *>(a.ws.QH + go + 32 * p + 8 * i) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+                        *reinterpret_cast<uint4 *>(a.ws.QL + go + 32 * p + 8 * i) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 8; u += 2) {
+                            kg_keep[w + (u >> 1)] = pack_bf16(e8[u] * sGamC[c + u], e8[u + 1] * sGamC[c + u + 1]);
+                            pack_hi_lo(x8[u] * __expf(gl[u] - g8[u]), x8[u + 1] * __expf(gl[u + 1] - g8[u + 1]),
+                                       oh[u >> 1], ol[u >> 1]);
+                        }
+                        const uint32_t so = (c >> 6) * 8192 + sw128_off(t_row, c & 63);
+                        *reinterpret_cast<uint4 *>(sm + P1_R1H + so) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+                        *reinterpret_cast<uint4 *>(sm + P1_R1L + so) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+                        *reinterpret_cast<uint4 *>(a.ws.KH + go + 32 * p + 8 * i) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+                        *reinterpret_cast<uint4 *>(a.ws.KL + go + 32 * p + 8 * i) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+                    }
+                }
+                tmem_st16u(tm + P1_TM_LH + 32 * half + 16 * p, hi);
+                tmem_st16u(tm + P1_TM_LL + 32 * half + 16 * p, lo);
+            }
+            tmem_wait_st();
         }
         fence_proxy_async();
+        tc_fence_before();
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t la_[3] = {P1_LH, P1_LH, P1_LL}, ra_[3] = {P1_RH, P1_RL, P1_RH};
 #pragma unroll
             for (int part = 0; part < 3; ++part)
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t kb = ks >> 2, kk = (ks & 3) * 32;
-                    mma_bf16(tmb + P1_TM_X + 16 * j,
-                             smem_desc_sw128(smem_u32(sm + la_[part] + kb * 16384 + kk), 16, 1024),
-                             smem_desc_sw128(smem_u32(sm + ra_[part] + kb * 2048 + kk), 16, 1024),
-                             ID_KK_N16, (part | ks) != 0);
-                }
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ts(tmb + P1_TM_X, tmb + (part == 2 ? P1_TM_LL : P1_TM_LH) + 8 * ks,
+                                smem_desc_sw128(smem_u32(sm + (part == 1 ? P1_R1L : P1_R1H) +
+                                                         (ks >> 2) * 8192 + (ks & 3) * 32), 16, 1024),
+                                ID_KK_N64, (part | ks) != 0);
             mma_commit(&bar_mma);
         }
-        if (!wait_cycles(&bar_mma, j & 1)) fail();
+        if (!wait_cycles(&bar_mma, mma_phase)) fail();
+        mma_phase ^= 1;
         tc_fence_after();
-        __syncthreads();
+        __syncthreads();   // the right factors are dead: K*G takes their place
+        if (!qrow) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int c = 64 * half + 8 * i;
+                *reinterpret_cast<uint4 *>(sm + P1_KG + (c >> 6) * 8192 + sw128_off(t_row, c & 63)) =
+                    make_uint4(kg_keep[4 * i], kg_keep[4 * i + 1], kg_keep[4 * i + 2], kg_keep[4 * i + 3]);
+            }
+        }
         if (abort_s) goto done;
+    } else {
+        // ---- per row (this thread: row t of Q or K, channels 64 half .. 64 half + 63):
+        //      xE_c = x_tc exp(g_tc - ref_i(t)) in [|x|, |x| e^kDiagLimit], kept in registers for
+        //      the products below; Q rows write Q*G = xE exp(ref_i) (pair) to the workspace, K rows
+        //      write K*G = xE exp(ref_i) (the W operand) and K*G_C/G = k exp(g_63 - g_t) (pair).
+        //      A flagged chunk takes every factor directly from its own exponent instead.
+        float xE[64];
+        {
+            const size_t go = ((size_t)n * 64 + t_row) * 128 + 64 * half;
+    #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int c = 64 * half + 8 * i;
+                float x8[8], g8[8], r8[8], e8[8];
+                load8_bf16(xt, t_row, c >> 3, x8);
+                load8_g(LA, t_row, c, g8);
+                load8_g(LA, 16 * blk + 15, c, r8);
+    #pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    xE[8 * i + u] = x8[u] * __expf(fminf(g8[u] - r8[u], kDiagLimit));
+                    e8[u] = diag_exact ? x8[u] * __expf(g8[u]) : xE[8 * i + u] * sExpRef[blk * 128 + c + u];
+                }
+                if (qrow) {
+                    uint32_t hi[4], lo[4];
+    #pragma unroll
+                    for (int u = 0; u < 8; u += 2) pack_hi_lo(e8[u], e8[u + 1], hi[u >> 1], lo[u >> 1]);
+                    *reinterpret_cast<uint4 *>(a.ws.QH + go + 8 * i) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(a.ws.QL + go + 8 * i) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                } else {
+                    float gl[8];
+                    load8_g(LA, 63, c, gl);
+                    uint32_t kg[4], hi[4], lo[4];
+    #pragma unroll
+                    for (int u = 0; u < 8; u += 2) {
+                        kg[u >> 1] = pack_bf16(e8[u], e8[u + 1]);
+                        pack_hi_lo(x8[u] * __expf(gl[u] - g8[u]), x8[u + 1] * __expf(gl[u + 1] - g8[u + 1]),
+                                   hi[u >> 1], lo[u >> 1]);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + P1_KG + (c >> 6) * 8192 + sw128_off(t_row, c & 63)) =
+                        make_uint4(kg[0], kg[1], kg[2], kg[3]);
+                    *reinterpret_cast<uint4 *>(a.ws.KH + go + 8 * i) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(a.ws.KL + go + 8 * i) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+        }
+
+        // ---- X = [Q; K] K^T with per-channel decays, by column block j (tokens 16 j .. 16 j + 15),
+        //      against ref_j: the right factor k_s exp(ref_j - g_s) (shared memory) is <= |k_s|;
+        //      the left factor x_t exp(g_t - ref_j) = xE_t F_{i(t) j} (tensor memory, one [Q; K]
+        //      row per lane, 64 channels per warp) is <= |x_t| below the block and at most
+        //      |x_t| e^kDiagLimit inside it (a flagged chunk clamps it there, takes it directly
+        //      from its exponent, and recomputes the diagonal blocks below).  Rows above the
+        //      block get zeros: their entries are masked.
+        for (int j = 0; j < 4; ++j) {
+            const int ref = 16 * j + 15;
+            {
+                const int rr = tid >> 4, c8 = tid & 15, s = 16 * j + rr;
+                float k8[8], g8[8], rf[8];
+                load8_bf16(sm + P1_K, s, c8, k8);
+                load8_g(LA, s, 8 * c8, g8);
+                load8_g(LA, ref, 8 * c8, rf);
+                uint32_t hi[4], lo[4];
+    #pragma unroll
+                for (int u = 0; u < 8; u += 2)
+                    pack_hi_lo(k8[u] * __expf(rf[u] - g8[u]), k8[u + 1] * __expf(rf[u + 1] - g8[u + 1]),
+                               hi[u >> 1], lo[u >> 1]);
+                const uint32_t off = (c8 >> 3) * 2048 + sw128_off(rr, (8 * c8) & 63);
+                *reinterpret_cast<uint4 *>(sm + P1_R + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(sm + P1_R + 4096 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            if ((quarter & 1) || j < 2) {   // some row of this warp is at or below the block
+                const int fr = blk < j ? 7 : (blk == j ? 6 : blk * (blk - 1) / 2 + j);
+                const float *Fr = sF + fr * 128;
+    #pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    uint32_t hi[16], lo[16];
+    #pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int cl = 32 * p + 8 * i, c = 64 * half + cl;
+                        float f8[8];
+                        if (!diag_exact) {
+                            const float4 f0 = *reinterpret_cast<const float4 *>(Fr + c);
+                            const float4 f1 = *reinterpret_cast<const float4 *>(Fr + c + 4);
+                            f8[0] = xE[cl] * f0.x;     f8[1] = xE[cl + 1] * f0.y;
+                            f8[2] = xE[cl + 2] * f0.z; f8[3] = xE[cl + 3] * f0.w;
+                            f8[4] = xE[cl + 4] * f1.x; f8[5] = xE[cl + 5] * f1.y;
+                            f8[6] = xE[cl + 6] * f1.z; f8[7] = xE[cl + 7] * f1.w;
+                        } else {
+                            float x8[8], g8[8], r8[8];
+                            load8_bf16(xt, t_row, c >> 3, x8);
+                            load8_g(LA, t_row, c, g8);
+                            load8_g(LA, ref, c, r8);
+    #pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                f8[u] = blk < j ? 0.f : x8[u] * __expf(fminf(g8[u] - r8[u], kDiagLimit));
+                        }
+    #pragma unroll
+                        for (int u = 0; u < 8; u += 2)
+                            pack_hi_lo(f8[u], f8[u + 1], hi[4 * i + (u >> 1)], lo[4 * i + (u >> 1)]);
+                    }
+                    tmem_st16u(tm + P1_TM_LH + 32 * half + 16 * p, hi);
+                    tmem_st16u(tm + P1_TM_LL + 32 * half + 16 * p, lo);
+                }
+                tmem_wait_st();
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after();
+    #pragma unroll
+                for (int part = 0; part < 3; ++part)
+    #pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ts(tmb + P1_TM_X + 16 * j, tmb + (part == 2 ? P1_TM_LL : P1_TM_LH) + 8 * ks,
+                                    smem_desc_sw128(smem_u32(sm + P1_R + (part == 1 ? 4096 : 0) +
+                                                             (ks >> 2) * 2048 + (ks & 3) * 32), 16, 1024),
+                                    ID_KK_N16, (part | ks) != 0);
+                mma_commit(&bar_mma);
+            }
+            if (!wait_cycles(&bar_mma, mma_phase)) fail();
+            mma_phase ^= 1;
+            tc_fence_after();
+            __syncthreads();
+            if (abort_s) goto done;
+        }
+    }
+    if (tid == 0) {   // the factors in the V buffer are dead: load V (U operand)
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&bar_ld, 16384);
+        for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + P1_V + kb * 8192, &tv, &bar_ld, 64 * kb, h, t0, b);
     }
 
     // ---- flagged chunk: entries of the four diagonal 16 x 16 blocks in fp32, one exponential
     //      per channel, into Xd[2][64][16] (rows of P, then rows of A before beta)
-    diag_exact = diag_exact_s != 0;
     if (diag_exact) {
         for (int task = tid; task < 2 * 64 * 16; task += kThreads) {
             const int part = task >> 10, r = (task >> 4) & 63, s = (r & ~15) + (task & 15);
-            const unsigned char *xt = sm + (part ? P1_K : P1_Q);
+            const unsigned char *xs = sm + (part ? P1_K : P1_Q);
             float acc = 0.f;
             if (s <= r)
                 for (int ch = 0; ch < 128; ++ch) {
                     const uint32_t o = (ch >> 6) * 8192;
                     const float xr = __bfloat162float(
-                        *reinterpret_cast<const __nv_bfloat16 *>(xt + o + sw128_off(r, ch & 63)));
+                        *reinterpret_cast<const __nv_bfloat16 *>(xs + o + sw128_off(r, ch & 63)));
                     const float ks = __bfloat162float(
                         *reinterpret_cast<const __nv_bfloat16 *>(sm + P1_K + o + sw128_off(s, ch & 63)));
-                    acc = fmaf(xr * ks, __expf(LA[la_off(r, ch) / 4] - LA[la_off(s, ch) / 4]), acc);
+                    acc = fmaf(xr * ks, __expf(LA[la_idx(r, ch)] - LA[la_idx(s, ch)]), acc);
                 }
             Xd[task] = acc;
         }
-        __syncthreads();
     }
+    __syncthreads();   // Q, K and g are dead from here on
 
     // ---- P (rows 0..63 of X) to the workspace as a bf16 pair; A (rows 64..127) in fp32
     {
@@ -328,41 +504,13 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tc_fence_before();
     __syncthreads();
 
-    // ---- T = (I + A)^-1 with T diag(beta) in bf16 (the second operand, T diag(beta)
-    //      diag(ones), is not used here)
-    solve_unit_lower64(reinterpret_cast<const float *>(sm + P1_A), reinterpret_cast<float *>(sm + P1_T),
-                       sM, sm + P1_TB, sBeta, sOnes, tid);
-
-    // ---- K*G (MMA operand), and Q*G, K*G_C/G (bf16 pairs) to the workspace
-    for (int task = tid; task < 64 * 16; task += kThreads) {
-        const int r = task >> 4, c8 = task & 15;
-        float q8[8], k8[8], g8[8], gl[8];
-        load8_bf16(sm + P1_Q, r, c8, q8);
-        load8_bf16(sm + P1_K, r, c8, k8);
-        load8_f32(LA + la_off(r, 8 * c8) / 4, g8);
-        load8_f32(LA + la_off(63, 8 * c8) / 4, gl);
-        uint32_t kg[4], qh[4], ql[4], dh[4], dl[4];
-#pragma unroll
-        for (int u = 0; u < 8; u += 2) {
-            const float e0 = __expf(g8[u]), e1 = __expf(g8[u + 1]);
-            kg[u >> 1] = pack_bf16(k8[u] * e0, k8[u + 1] * e1);
-            pack_hi_lo(q8[u] * e0, q8[u + 1] * e1, qh[u >> 1], ql[u >> 1]);
-            pack_hi_lo(k8[u] * __expf(gl[u] - g8[u]), k8[u + 1] * __expf(gl[u + 1] - g8[u + 1]),
-                       dh[u >> 1], dl[u >> 1]);
-        }
-        *reinterpret_cast<uint4 *>(sm + P1_KG + (c8 >> 3) * 8192 + sw128_off(r, (8 * c8) & 63)) =
-            make_uint4(kg[0], kg[1], kg[2], kg[3]);
-        const size_t go = ((size_t)n * 64 + r) * 128 + 8 * c8;
-        *reinterpret_cast<uint4 *>(a.ws.QH + go) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
-        *reinterpret_cast<uint4 *>(a.ws.QL + go) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
-        *reinterpret_cast<uint4 *>(a.ws.KH + go) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
-        *reinterpret_cast<uint4 *>(a.ws.KL + go) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
-    }
-    fence_proxy_async();
-    __syncthreads();
+    // ---- T = (I + A)^-1 and its bf16 operand T diag(beta)
+    solve_unit_lower64<false>(reinterpret_cast<const float *>(sm + P1_A), reinterpret_cast<float *>(sm + P1_T),
+                              sM, sm + P1_TB, sBeta, nullptr, tid);
 
     // ---- U^T = V^T (T diag beta)^T,  W^T = (K*G)^T (T diag beta)^T
     if (tid == 0) {
+        if (!wait_cycles(&bar_ld, 1)) fail();
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -374,20 +522,34 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                      smem_desc_sw128(smem_u32(sm + P1_TB + ks * 32), 16, 1024), ID_MK_N64, ks > 0);
         mma_commit(&bar_mma);
     }
-    if (!wait_cycles(&bar_mma, 0)) fail();   // fifth completion of bar_mma: parity 0
+    if (!wait_cycles(&bar_mma, mma_phase)) fail();
     tc_fence_after();
-    // W[r][i] and U[r][j] from the transposed TMEM tiles (lane = channel, column = token)
+    // ---- W (bf16) and U (fp32) staged row-major (lane = channel, column = token) and
+    //      written by TMA
     {
         float w[32], u32[32];
         tmem_ld32(tm + P1_TM_W + 32 * half, w);
         tmem_ld32(tm + P1_TM_U + 32 * half, u32);
         tmem_wait_ld();
+        const int j = row;
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
-            const size_t rr = (size_t)n * 64 + 32 * half + u;
-            a.ws.W[rr * 128 + row] = __float2bfloat16_rn(w[u]);
-            a.ws.U[rr * 128 + row] = u32[u];
+            const int r = 32 * half + u;
+            *reinterpret_cast<__nv_bfloat16 *>(sm + P1_WST + (j >> 6) * 8192 + sw128_off(r, j & 63)) =
+                __float2bfloat16_rn(w[u]);
+            *reinterpret_cast<float *>(sm + P1_UST + (j >> 5) * 8192 + r * 128 + (j & 31) * 4) = u32[u];
         }
+    }
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {
+        const int y = (int)(n * 64);
+        tma_store_2d(&mw, sm + P1_WST, 0, y);
+        tma_store_2d(&mw, sm + P1_WST + 8192, 64, y);
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx) tma_store_2d(&mu, sm + P1_UST + bx * 8192, 32 * bx, y);
+        bulk_commit();
+        bulk_wait_read_all();
     }
 done:
     tc_fence_before();
@@ -408,7 +570,6 @@ constexpr uint32_t S2_SMALL = 196608;                        // G_C of two chunk
 constexpr uint32_t S2_TOTAL = S2_SMALL + 1024;
 constexpr uint32_t S2_TM_S = 0, S2_TM_D = 128, S2_TM_PE = 256;
 
-constexpr uint32_t ID_KK_N64 = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_KM_N128 = idesc_bf16(128, 128, false, true);
 
 struct StateArgs {
@@ -734,7 +895,7 @@ int launch_chunk_kda(const ChunkProblem &p, void *workspace, int *status_word, c
     const KdaWorkspace ws = kda_carve(workspace, nch);
     CUtensorMap tq, tk, tv, tla, to;
     if (!map4(&tq, p.q, p.B, p.T, p.H, 2, true) || !map4(&tk, p.k, p.B, p.T, p.H, 2, true) ||
-        !map4(&tv, p.v, p.B, p.T, p.H, 2, true) || !map4(&tla, p.log_alpha, p.B, p.T, p.H, 4, false) ||
+        !map4(&tv, p.v, p.B, p.T, p.H, 2, true) || !map4(&tla, p.log_alpha, p.B, p.T, p.H, 4, true) ||
         !map4(&to, p.out, p.B, p.T, p.H, p.out_bf16 ? 2 : 4, true))
         return kErrCuda;
     CUtensorMap mw, mqh, mql, mkh, mkl, mph, mpl, mu;
@@ -749,7 +910,7 @@ int launch_chunk_kda(const ChunkProblem &p, void *workspace, int *status_word, c
     if (cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, s1) != cudaSuccess)
         return kErrCuda;
     PrepArgs pa{(const __nv_bfloat16 *)p.beta, ws, status_word, (int)p.T, (int)p.H, p.NC};
-    kda_prep_kernel<<<(unsigned)nch, kThreads, s1, stream>>>(tq, tk, tv, tla, pa);
+    kda_prep_kernel<<<(unsigned)nch, kThreads, s1, stream>>>(tq, tk, tv, tla, mw, mu, pa);
     if (cudaGetLastError() != cudaSuccess) return kErrCuda;
 
     StateArgs sa{p.init_state, p.final_state, ws.GAM, status_word, (int)p.T, (int)p.H, p.NC};

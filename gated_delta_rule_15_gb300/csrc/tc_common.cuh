@@ -29,12 +29,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi); packs two such pairs.
 __device__ __forceinline__ void pack_hi_lo(float a, float b, uint32_t &hi, uint32_t &lo) {
-    const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
-    __nv_bfloat162 h2;
-    h2.x = ha;
-    h2.y = hb;
-    hi = *reinterpret_cast<uint32_t *>(&h2);
-    lo = pack_bf16(a - __bfloat162float(ha), b - __bfloat162float(hb));
+    hi = pack_bf16(a, b);
+    lo = pack_bf16(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
 }
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
@@ -90,10 +86,11 @@ __device__ __forceinline__ int a_index(int r, int s) {
 //   2. T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (two warps);
 //   3. lower-left 32 x 32 quarter: M = A[32:64, 0:32] T[0:32, 0:32], then
 //      T[32:64, 0:32] = -T[32:64, 32:64] M (four warps, one 16 x 16 tile each).
-// Each element is written, once final, also as T diag(beta) and T diag(beta G) in bf16
-// (128-byte-swizzled K-major 64 x 64 tiles at TB and TB + 8192): the U and W operands.
-// Products use TF32 mma.sync with fp32 accumulation.  M needs 1024 floats.  Called by all
-// 256 threads; starts after and ends with a barrier.
+// Each element is written, once final, also as T diag(beta) in bf16 (a 128-byte-swizzled
+// K-major 64 x 64 tile at TB) and, with kPair, as T diag(beta G) at TB + 8192: the U and W
+// operands.  Products use TF32 mma.sync with fp32 accumulation.  M needs 1024 floats.
+// Called by all 256 threads; starts after and ends with a barrier.
+template <bool kPair = true>
 __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, float *M,
                                                    unsigned char *TB, const float *beta,
                                                    const float *gam, int tid) {
@@ -105,7 +102,8 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         const float vb = v * beta[s];
         const uint32_t off = sw128_off(r, s);
         *reinterpret_cast<__nv_bfloat16 *>(TB + off) = __float2bfloat16_rn(vb);
-        *reinterpret_cast<__nv_bfloat16 *>(TB + 8192 + off) = __float2bfloat16_rn(vb * gam[s]);
+        if constexpr (kPair)
+            *reinterpret_cast<__nv_bfloat16 *>(TB + 8192 + off) = __float2bfloat16_rn(vb * gam[s]);
     };
     // final elements (r, s) and (r, s + 1), s even: one 32-bit store per operand
     auto fin2 = [&](int r, int s, float v0, float v1) {
@@ -113,7 +111,8 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         const float b0 = v0 * beta[s], b1 = v1 * beta[s + 1];
         const uint32_t off = sw128_off(r, s);
         *reinterpret_cast<uint32_t *>(TB + off) = pack_bf16(b0, b1);
-        *reinterpret_cast<uint32_t *>(TB + 8192 + off) = pack_bf16(b0 * gam[s], b1 * gam[s + 1]);
+        if constexpr (kPair)
+            *reinterpret_cast<uint32_t *>(TB + 8192 + off) = pack_bf16(b0 * gam[s], b1 * gam[s + 1]);
     };
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
     {
@@ -151,7 +150,8 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
             const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
             const uint32_t off = sw128_off(16 * bi + (e >> 1), 16 * bj + 8 * (e & 1));
             *reinterpret_cast<uint4 *>(TB + off) = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4 *>(TB + 8192 + off) = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (kPair)
+                *reinterpret_cast<uint4 *>(TB + 8192 + off) = make_uint4(0u, 0u, 0u, 0u);
         }
     }
     __syncthreads();

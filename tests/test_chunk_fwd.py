@@ -238,9 +238,12 @@ def test_kda_tc_many_heads(dr):
     check(dr, d, "bf16")
 
 
-@pytest.mark.parametrize("la_range", [(0.0, 1.0), (0.0, 5.0)])
+@pytest.mark.parametrize("la_range", [(0.0, 1.0), (0.0, 3.0), (0.0, 5.0)])
 def test_kda_tc_strong_decay(dr, la_range):
-    """Per-token log decays up to -5 per channel: a 16-token block can decay by e^-80."""
+    """Per-token log decays up to -1, -3, -5 per channel.  Up to -1 a chunk decays by at
+    most e^-64 and takes one product against its last token; beyond, chunks take four
+    products against 16-token block ends, and at -5 a block can decay by e^-80 (exact
+    diagonal blocks)."""
     d = inputs.chunk_inputs(2, 300, 2, 128, 128, gate="channel", dtype="bf16",
                             init_state=True, seed=15, log_alpha_range=la_range)
     check(dr, d, "bf16")
