@@ -72,7 +72,7 @@ KdaWorkspace kda_carve(void *base, int64_t nch) {
 // Sized for two CTAs per SM (<= 113 KB each): the left factors of the intra-chunk products
 // live in tensor memory (A operand of tcgen05.mma), the right factors in shared memory.
 constexpr uint32_t P1_Q = 0, P1_K = 16384;    // 64 x 128 bf16 tiles, 2 K-blocks, 128B swizzle
-constexpr uint32_t P1_LA = 32768;             // log alpha -> g: 4 boxes [64][32] fp32, 128B swizzle
+constexpr uint32_t P1_LA = 32768;   // log alpha -> g log2(e): 4 boxes [64][32] fp32, 128B swizzle
 constexpr uint32_t P1_V = 65536, P1_KG = 81920;
 constexpr uint32_t P1_R = 98304;              // right factors: high [kb][16][64], low at +4096
 constexpr uint32_t P1_SMALL = 106496;         // beta[64], solve scratch[1024]
@@ -93,6 +93,15 @@ constexpr uint32_t ID_KK_N64 = idesc_bf16(128, 64, false, false);
 // Largest per-channel decay (natural log) inside one 16-token block that the tensor-core
 // products of the diagonal blocks take; beyond it the chunk recomputes those entries.
 constexpr float kDiagLimit = 64.f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kDiagLimit2 = kDiagLimit * kLog2e;   // the same bound in base-2 units
+
+// 2^x (PTX ex2.approx.ftz: relative error about 2^-22; results below 2^-126 flush to zero)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 constexpr uint32_t ID_MK_N64 = idesc_bf16(128, 64, true, false);
 
 struct PrepArgs {
@@ -195,7 +204,8 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     __syncthreads();
     if (abort_s) goto done;
 
-    // ---- cumulative log decay g (in place, one channel per thread, held in registers),
+    // ---- cumulative log decay g (in place, stored as g log2(e) so that every factor below
+    //      is one ex2; one channel per thread, held in registers),
     //      G_C = exp(g_63); flag the chunk if a channel decays by more than kDiagLimit
     //      inside one 16-token block.  With ref_i = g at the last token of block i, the
     //      per-channel factors exp(ref_i) and F_ij = exp(ref_i - ref_j) (i > j, both <= 1)
@@ -207,7 +217,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
         for (int t = 1; t < 64; ++t) v[t] += v[t - 1];
 #pragma unroll
-        for (int t = 0; t < 64; ++t) LA[la_idx(t, tid)] = v[t];
+        for (int t = 0; t < 64; ++t) LA[la_idx(t, tid)] = v[t] * kLog2e;   // g in base-2 units
         bool steep = false;
 #pragma unroll
         for (int j = 0; j < 4; ++j) steep |= v[16 * j] - v[16 * j + 15] > kDiagLimit;
@@ -249,7 +259,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     load8_g(LA, t_row, c, g8);
                     load8_g(LA, 63, c, gl);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) e8[u] = x8[u] * __expf(g8[u] - gl[u]);
+                    for (int u = 0; u < 8; ++u) e8[u] = x8[u] * ex2(g8[u] - gl[u]);
 #pragma unroll
                     for (int u = 0; u < 8; u += 2)
                         pack_hi_lo(e8[u], e8[u + 1], hi[4 * i + (u >> 1)], lo[4 * i + (u >> 1)]);
@@ -264,7 +274,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
                         for (int u = 0; u < 8; u += 2) {
                             kg_keep[w + (u >> 1)] = pack_bf16(e8[u] * sGamC[c + u], e8[u + 1] * sGamC[c + u + 1]);
-                            pack_hi_lo(x8[u] * __expf(gl[u] - g8[u]), x8[u + 1] * __expf(gl[u + 1] - g8[u + 1]),
+                            pack_hi_lo(x8[u] * ex2(gl[u] - g8[u]), x8[u + 1] * ex2(gl[u + 1] - g8[u + 1]),
                                        oh[u >> 1], ol[u >> 1]);
                         }
                         const uint32_t so = (c >> 6) * 8192 + sw128_off(t_row, c & 63);
@@ -325,8 +335,8 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 load8_g(LA, 16 * blk + 15, c, r8);
     #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    xE[8 * i + u] = x8[u] * __expf(fminf(g8[u] - r8[u], kDiagLimit));
-                    e8[u] = diag_exact ? x8[u] * __expf(g8[u]) : xE[8 * i + u] * sExpRef[blk * 128 + c + u];
+                    xE[8 * i + u] = x8[u] * ex2(fminf(g8[u] - r8[u], kDiagLimit2));
+                    e8[u] = diag_exact ? x8[u] * ex2(g8[u]) : xE[8 * i + u] * sExpRef[blk * 128 + c + u];
                 }
                 if (qrow) {
                     uint32_t hi[4], lo[4];
@@ -341,7 +351,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     #pragma unroll
                     for (int u = 0; u < 8; u += 2) {
                         kg[u >> 1] = pack_bf16(e8[u], e8[u + 1]);
-                        pack_hi_lo(x8[u] * __expf(gl[u] - g8[u]), x8[u + 1] * __expf(gl[u + 1] - g8[u + 1]),
+                        pack_hi_lo(x8[u] * ex2(gl[u] - g8[u]), x8[u + 1] * ex2(gl[u + 1] - g8[u + 1]),
                                    hi[u >> 1], lo[u >> 1]);
                     }
                     *reinterpret_cast<uint4 *>(sm + P1_KG + (c >> 6) * 8192 + sw128_off(t_row, c & 63)) =
@@ -370,7 +380,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 uint32_t hi[4], lo[4];
     #pragma unroll
                 for (int u = 0; u < 8; u += 2)
-                    pack_hi_lo(k8[u] * __expf(rf[u] - g8[u]), k8[u + 1] * __expf(rf[u + 1] - g8[u + 1]),
+                    pack_hi_lo(k8[u] * ex2(rf[u] - g8[u]), k8[u + 1] * ex2(rf[u + 1] - g8[u + 1]),
                                hi[u >> 1], lo[u >> 1]);
                 const uint32_t off = (c8 >> 3) * 2048 + sw128_off(rr, (8 * c8) & 63);
                 *reinterpret_cast<uint4 *>(sm + P1_R + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -400,7 +410,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                             load8_g(LA, ref, c, r8);
     #pragma unroll
                             for (int u = 0; u < 8; ++u)
-                                f8[u] = blk < j ? 0.f : x8[u] * __expf(fminf(g8[u] - r8[u], kDiagLimit));
+                                f8[u] = blk < j ? 0.f : x8[u] * ex2(fminf(g8[u] - r8[u], kDiagLimit2));
                         }
     #pragma unroll
                         for (int u = 0; u < 8; u += 2)
@@ -453,7 +463,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                         *reinterpret_cast<const __nv_bfloat16 *>(xs + o + sw128_off(r, ch & 63)));
                     const float ks = __bfloat162float(
                         *reinterpret_cast<const __nv_bfloat16 *>(sm + P1_K + o + sw128_off(s, ch & 63)));
-                    acc = fmaf(xr * ks, __expf(LA[la_idx(r, ch)] - LA[la_idx(s, ch)]), acc);
+                    acc = fmaf(xr * ks, ex2(LA[la_idx(r, ch)] - LA[la_idx(s, ch)]), acc);
                 }
             Xd[task] = acc;
         }
@@ -561,14 +571,15 @@ done:
 // ---------------------------------------------------------------- state kernel layout
 constexpr uint32_t S2_W = 0, S2_QH = 16384, S2_QL = 32768;   // K-major [64][128], 2 K-blocks
 constexpr uint32_t S2_KH = 49152, S2_KL = 65536;             // MN-major [64 tok][128 ch]
-constexpr uint32_t S2_PH = 81920, S2_PL = 90112;             // K-major [64][64]
-constexpr uint32_t S2_U = 98304;                             // [64][128] fp32, 4 boxes of 32
-constexpr uint32_t S2_ST = 131072;                           // S^T bf16 [128][128], 2 K-blocks
-constexpr uint32_t S2_EH = 163840, S2_EL = 180224;           // E^T bf16 pair [128][64]
-constexpr uint32_t S2_OUT = S2_EH;                           // output tile after the MMAs
-constexpr uint32_t S2_SMALL = 196608;                        // G_C of two chunks
+constexpr uint32_t S2_P = 81920;                             // 2 buffers of [P high | P low]
+constexpr uint32_t S2_U = 114688;                            // [64][128] fp32, 4 boxes of 32
+constexpr uint32_t S2_ST = 147456;                           // S^T bf16 [128][128]; output staging
+constexpr uint32_t S2_EH = 180224, S2_EL = 196608;           // E^T bf16 pair [128][64]
+constexpr uint32_t S2_SMALL = 212992;                        // G_C of two chunks
 constexpr uint32_t S2_TOTAL = S2_SMALL + 1024;
-constexpr uint32_t S2_TM_S = 0, S2_TM_D = 128, S2_TM_PE = 256;
+static_assert(S2_TOTAL + 1024 <= 227 * 1024, "state layout");
+// tensor memory: S^T, (W S)^T, then two buffers each of (Q*G S)^T and E^T P^T
+constexpr uint32_t S2_TM_S = 0, S2_TM_DW = 128, S2_TM_DQ = 192, S2_TM_PE = 320;
 
 constexpr uint32_t ID_KM_N128 = idesc_bf16(128, 128, false, true);
 
@@ -580,6 +591,16 @@ struct StateArgs {
     int T, H, NC;
 };
 
+// Per chunk c, in order (thread 0 issues the MMAs, thread 224 the TMA loads):
+//   1. S^T -> bf16 operand (ST), S^T <- S^T Diag(G_C)
+//   2. (W S)^T -> DW [bar_dw];  (Q*G S)^T -> DQ[c % 2] [bar_dq]
+//   3. refill W for c + 1; refill P for c + 1 (its buffer was read by chunk c - 1)
+//   4. E^T = U^T - (W S)^T as a bf16 pair; refill Q (once (Q*G S)^T is done) and U
+//   5. S^T += E^T (K*G_C/G) [bar_s];  E^T P^T -> PE[c % 2] [bar_pe]
+//   6. once DQ[c % 2] is done reading ST: output of chunk c - 1 = DQ + PE of its
+//      buffers, staged in ST and stored by TMA (overlaps the MMAs of step 5)
+//   7. wait for the state update; refill K
+// Every parity wait is placed where its barrier can be at most one phase ahead.
 template <typename Tout>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mqh,
@@ -589,8 +610,7 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
                  const __grid_constant__ CUtensorMap to, const StateArgs a) {
     extern __shared__ unsigned char dsm_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
-    // operand groups (each completes once per chunk): W + Q pair, U, K pair + P pair
-    __shared__ uint64_t bar_wq, bar_u, bar_kp, bar_d, bar_s;
+    __shared__ uint64_t bar_w, bar_q, bar_u, bar_k, bar_p[2], bar_dw, bar_dq, bar_s, bar_pe;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
 
@@ -603,11 +623,9 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
     float *sGam = reinterpret_cast<float *>(sm + S2_SMALL);   // [2][128]
 
     if (tid == 0) {
-        mbar_init(&bar_wq, 1);
-        mbar_init(&bar_u, 1);
-        mbar_init(&bar_kp, 1);
-        mbar_init(&bar_d, 1);
-        mbar_init(&bar_s, 1);
+        uint64_t *bars[] = {&bar_w, &bar_q, &bar_u, &bar_k, &bar_p[0], &bar_p[1],
+                            &bar_dw, &bar_dq, &bar_s, &bar_pe};
+        for (uint64_t *bb : bars) mbar_init(bb, 1);
         abort_s = 0;
         fence_mbar_init();
     }
@@ -642,45 +660,94 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
     }
 
     const int64_t n0 = (int64_t)bh * a.NC;   // first chunk of this chain in the workspace
-    auto load_wq = [&](int c) {
-        const int y = (int)((n0 + c) * 64);
-        mbar_arrive_expect_tx(&bar_wq, 3 * 16384);
+    auto rowc = [&](int c) { return (int)((n0 + c) * 64); };
+    auto load_w = [&](int c) {
+        mbar_arrive_expect_tx(&bar_w, 16384);
+        for (int kb = 0; kb < 2; ++kb) tma_load_2d(sm + S2_W + kb * 8192, &mw, &bar_w, 64 * kb, rowc(c));
+    };
+    auto load_q = [&](int c) {
+        mbar_arrive_expect_tx(&bar_q, 32768);
         for (int kb = 0; kb < 2; ++kb) {
-            tma_load_2d(sm + S2_W + kb * 8192, &mw, &bar_wq, 64 * kb, y);
-            tma_load_2d(sm + S2_QH + kb * 8192, &mqh, &bar_wq, 64 * kb, y);
-            tma_load_2d(sm + S2_QL + kb * 8192, &mql, &bar_wq, 64 * kb, y);
+            tma_load_2d(sm + S2_QH + kb * 8192, &mqh, &bar_q, 64 * kb, rowc(c));
+            tma_load_2d(sm + S2_QL + kb * 8192, &mql, &bar_q, 64 * kb, rowc(c));
         }
     };
     auto load_u = [&](int c) {
-        const int y = (int)((n0 + c) * 64);
         mbar_arrive_expect_tx(&bar_u, 32768);
-        for (int bx = 0; bx < 4; ++bx) tma_load_2d(sm + S2_U + bx * 8192, &mu, &bar_u, 32 * bx, y);
+        for (int bx = 0; bx < 4; ++bx) tma_load_2d(sm + S2_U + bx * 8192, &mu, &bar_u, 32 * bx, rowc(c));
     };
-    auto load_kp = [&](int c) {
-        const int y = (int)((n0 + c) * 64);
-        mbar_arrive_expect_tx(&bar_kp, 2 * 16384 + 2 * 8192);
+    auto load_k = [&](int c) {
+        mbar_arrive_expect_tx(&bar_k, 32768);
         for (int kb = 0; kb < 2; ++kb) {
-            tma_load_2d(sm + S2_KH + kb * 8192, &mkh, &bar_kp, 64 * kb, y);
-            tma_load_2d(sm + S2_KL + kb * 8192, &mkl, &bar_kp, 64 * kb, y);
+            tma_load_2d(sm + S2_KH + kb * 8192, &mkh, &bar_k, 64 * kb, rowc(c));
+            tma_load_2d(sm + S2_KL + kb * 8192, &mkl, &bar_k, 64 * kb, rowc(c));
         }
-        tma_load_2d(sm + S2_PH, &mph, &bar_kp, 0, y);
-        tma_load_2d(sm + S2_PL, &mpl, &bar_kp, 0, y);
+    };
+    auto load_p = [&](int c) {
+        uint64_t *bb = &bar_p[c & 1];
+        unsigned char *dst = sm + S2_P + (c & 1) * 16384;
+        mbar_arrive_expect_tx(bb, 16384);
+        tma_load_2d(dst, &mph, bb, 0, rowc(c));
+        tma_load_2d(dst + 8192, &mpl, bb, 0, rowc(c));
     };
     if (tid == kTmaThread && a.NC > 0) {
-        load_wq(0);
+        load_w(0);
+        load_q(0);
         load_u(0);
-        load_kp(0);
+        load_k(0);
+        load_p(0);
+        if (a.NC > 1) load_p(1);
     }
     if (tid < 128 && a.NC > 0) cp_async4(sGam + tid, a.gam + n0 * 128 + tid, 4);
     cp_async_commit();
 
-    bool store_outstanding = false;
+    bool store_outstanding = false;   // thread 0: a TMA store from ST may still be reading it
+    // output of chunk c from its DQ / PE buffers, staged in ST (free: see the callers)
+    auto emit = [&](int c) {
+        float o[32], pe[32];
+        tmem_ld32(tm + S2_TM_DQ + 64 * (c & 1) + 32 * half, o);
+        tmem_ld32(tm + S2_TM_PE + 64 * (c & 1) + 32 * half, pe);
+        tmem_wait_ld();
+        const int j = row;
+        if (sizeof(Tout) == 2) {
+            unsigned char *dst = sm + S2_ST + (j >> 6) * 8192;
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, j & 63)) =
+                    __float2bfloat16_rn(o[u] + pe[u]);
+        } else {
+            unsigned char *dst = sm + S2_ST + (j >> 5) * 8192;
+            const int cj = j & 31;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int r = 32 * half + u;
+                *reinterpret_cast<float *>(dst + r * 128 + ((((cj >> 2) ^ (r & 7)) & 7) << 4) +
+                                           ((cj & 3) << 2)) = o[u] + pe[u];
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
+#pragma unroll
+            for (int kb = 0; kb < kOutBoxes; ++kb)
+                tma_store_4d(&to, sm + S2_ST + kb * 8192, cols * kb, h, c * 64, b);
+            bulk_commit();
+            store_outstanding = true;
+        }
+    };
+
     for (int c = 0; c < a.NC; ++c) {
         const uint32_t par = c & 1;
-        const int t0 = c * 64;
-        // ---- S^T to bf16 (MMA operand); S^T <- S^T Diag(G_C)
+        // ---- 1. S^T to bf16 (ST, free once the previous output's store has read it);
+        //         S^T <- S^T Diag(G_C)
+        if (tid == 0 && store_outstanding) {
+            bulk_wait_read_all();
+            store_outstanding = false;
+        }
         cp_async_wait_all();
-        __syncthreads();   // G_C of this chunk visible
+        __syncthreads();   // G_C of this chunk visible; ST free
         if (tid < 128 && c + 1 < a.NC)   // prefetch the next chunk's G_C
             cp_async4(sGam + ((c + 1) & 1) * 128 + tid, a.gam + (n0 + c + 1) * 128 + tid, 4);
         cp_async_commit();
@@ -710,32 +777,46 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         __syncthreads();
         if (abort_s) break;
 
-        // ---- D = S^T [W; Q*G]^T  (the Q*G half as a high/low pair)
+        // ---- 2. (W S)^T, then (Q*G S)^T (a high/low pair) into this chunk's DQ buffer
         if (tid == 0) {
-            if (store_outstanding) {   // the previous output tile must have left S2_OUT
-                bulk_wait_read_all();
-                store_outstanding = false;
-            }
-            if (!wait_cycles(&bar_wq, par)) fail();
+            if (!wait_cycles(&bar_w, par)) fail();
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32, ob = (ks >> 2) * 8192 + (ks & 3) * 32;
-                const uint64_t ad = smem_desc_sw128(smem_u32(sm + S2_ST + o), 16, 1024);
-                mma_bf16(tmb + S2_TM_D, ad, smem_desc_sw128(smem_u32(sm + S2_W + ob), 16, 1024), ID_KK_N64, ks > 0);
-                mma_bf16(tmb + S2_TM_D + 64, ad, smem_desc_sw128(smem_u32(sm + S2_QH + ob), 16, 1024), ID_KK_N64, ks > 0);
-                mma_bf16(tmb + S2_TM_D + 64, ad, smem_desc_sw128(smem_u32(sm + S2_QL + ob), 16, 1024), ID_KK_N64, 1);
+                mma_bf16(tmb + S2_TM_DW, smem_desc_sw128(smem_u32(sm + S2_ST + o), 16, 1024),
+                         smem_desc_sw128(smem_u32(sm + S2_W + ob), 16, 1024), ID_KK_N64, ks > 0);
             }
-            mma_commit(&bar_d);
+            mma_commit(&bar_dw);
+            if (!wait_cycles(&bar_q, par)) fail();
+            tc_fence_after();
+            const uint32_t dq = tmb + S2_TM_DQ + 64 * par;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32, ob = (ks >> 2) * 8192 + (ks & 3) * 32;
+                const uint64_t ad = smem_desc_sw128(smem_u32(sm + S2_ST + o), 16, 1024);
+                mma_bf16(dq, ad, smem_desc_sw128(smem_u32(sm + S2_QH + ob), 16, 1024), ID_KK_N64, ks > 0);
+                mma_bf16(dq, ad, smem_desc_sw128(smem_u32(sm + S2_QL + ob), 16, 1024), ID_KK_N64, 1);
+            }
+            mma_commit(&bar_dq);
         }
-        wait_bar(&bar_d, par);
-        if (tid == kTmaThread && c + 1 < a.NC) load_wq(c + 1);   // W, Q*G buffers are free
+        wait_bar(&bar_dw, par);
+        // ---- 3. refills: W for c + 1; P for c + 1 into the buffer chunk c - 1 read
+        if (tid == kTmaThread && c + 1 < a.NC) {
+            load_w(c + 1);
+            if (c >= 1) {
+                if (!wait_cycles(&bar_pe, (c - 1) & 1)) fail();
+                load_p(c + 1);
+            }
+        }
 
-        // ---- E^T = U^T - (W S)^T as a bf16 pair (lane j = value channel, columns = tokens)
+        // ---- 4. E^T = U^T - (W S)^T as a bf16 pair (lane j = value channel, columns = tokens);
+        //         E^T P^T of chunk c - 1 must have read E first
+        if (c >= 1) wait_bar(&bar_pe, (c - 1) & 1);
         if (!wait_cycles(&bar_u, par)) fail();
         {
             float ws[32];
-            tmem_ld32(tm + S2_TM_D + 32 * half, ws);
+            tmem_ld32(tm + S2_TM_DW + 32 * half, ws);
             tmem_wait_ld();
             const float *U = reinterpret_cast<const float *>(sm + S2_U);
             const int j = row;
@@ -755,67 +836,58 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
                 *reinterpret_cast<uint4 *>(sm + S2_EL + off) = make_uint4(el[0], el[1], el[2], el[3]);
             }
         }
+        if (tid == kTmaThread && c + 1 < a.NC) {   // (Q*G S)^T was issued before (W S)^T completed
+            if (!wait_cycles(&bar_dq, par)) fail();
+            load_q(c + 1);
+        }
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
-        if (tid == kTmaThread && c + 1 < a.NC) load_u(c + 1);    // U buffer is free
+        if (tid == kTmaThread && c + 1 < a.NC) load_u(c + 1);   // U buffer is free
 
-        // ---- S^T += E^T (K*G_C/G);  PE = E^T P^T   (bf16 pairs: hi.hi + hi.lo + lo.hi)
+        // ---- 5. S^T += E^T (K*G_C/G) [bar_s];  E^T P^T -> PE[c % 2] [bar_pe]
+        //         (bf16 pairs: hi.hi + hi.lo + lo.hi)
         if (tid == 0) {
-            if (!wait_cycles(&bar_kp, par)) fail();
+            if (!wait_cycles(&bar_k, par)) fail();
+            if (!wait_cycles(&bar_p[par], (c >> 1) & 1)) fail();
             tc_fence_after();
+            const uint32_t pb = S2_P + par * 16384;
             const uint32_t ea[3] = {S2_EH, S2_EH, S2_EL}, kbuf[3] = {S2_KH, S2_KL, S2_KH},
-                           pbuf[3] = {S2_PH, S2_PL, S2_PH};
+                           pbuf[3] = {pb, pb + 8192, pb};
 #pragma unroll
             for (int part = 0; part < 3; ++part)
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t ad = smem_desc_sw128(smem_u32(sm + ea[part] + ks * 32), 16, 1024);
-                    mma_bf16(tmb + S2_TM_S, ad,
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmb + S2_TM_S, smem_desc_sw128(smem_u32(sm + ea[part] + ks * 32), 16, 1024),
                              smem_desc_sw128(smem_u32(sm + kbuf[part] + ks * 2048), 8192, 1024), ID_KM_N128, 1);
-                    mma_bf16(tmb + S2_TM_PE, ad, smem_desc_sw128(smem_u32(sm + pbuf[part] + ks * 32), 16, 1024),
-                             ID_KK_N64, (part | ks) != 0);
-                }
             mma_commit(&bar_s);
+            const uint32_t pe = tmb + S2_TM_PE + 64 * par;
+#pragma unroll
+            for (int part = 0; part < 3; ++part)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(pe, smem_desc_sw128(smem_u32(sm + ea[part] + ks * 32), 16, 1024),
+                             smem_desc_sw128(smem_u32(sm + pbuf[part] + ks * 32), 16, 1024), ID_KK_N64,
+                             (part | ks) != 0);
+            mma_commit(&bar_pe);
         }
-        wait_bar(&bar_s, par);
-        if (tid == kTmaThread && c + 1 < a.NC) load_kp(c + 1);   // K, P buffers are free
 
-        // ---- outputs o = (Q*G S)^T + E^T P^T, staged row-major and written by TMA
-        {
-            float o[32], pe[32];
-            tmem_ld32(tm + S2_TM_D + 64 + 32 * half, o);
-            tmem_ld32(tm + S2_TM_PE + 32 * half, pe);
-            tmem_wait_ld();
-            const int j = row;
-            if (sizeof(Tout) == 2) {
-                unsigned char *dst = sm + S2_OUT + (j >> 6) * 8192;
-#pragma unroll
-                for (int u = 0; u < 32; ++u)
-                    *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, j & 63)) =
-                        __float2bfloat16_rn(o[u] + pe[u]);
-            } else {
-                unsigned char *dst = sm + S2_OUT + (j >> 5) * 8192;
-                const int cj = j & 31;
-#pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int r = 32 * half + u;
-                    *reinterpret_cast<float *>(dst + r * 128 + ((((cj >> 2) ^ (r & 7)) & 7) << 4) +
-                                               ((cj & 3) << 2)) = o[u] + pe[u];
-                }
-            }
+        // ---- 6. once (Q*G S)^T has read ST: output of chunk c - 1
+        wait_bar(&bar_dq, par);
+        if (c >= 1) emit(c - 1);
+
+        // ---- 7. state update done; K buffer is free
+        wait_bar(&bar_s, par);
+        if (tid == kTmaThread && c + 1 < a.NC) load_k(c + 1);
+    }
+    if (!abort_s && a.NC > 0) {   // output of the last chunk
+        wait_bar(&bar_pe, (a.NC - 1) & 1);
+        if (tid == 0 && store_outstanding) {
+            bulk_wait_read_all();
+            store_outstanding = false;
         }
-        fence_proxy_async();
-        tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
-            constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
-#pragma unroll
-            for (int kb = 0; kb < kOutBoxes; ++kb)
-                tma_store_4d(&to, sm + S2_OUT + kb * 8192, cols * kb, h, t0, b);
-            bulk_commit();
-            store_outstanding = true;
-        }
+        emit(a.NC - 1);
     }
     if (!abort_s && a.final_state) {
         float v[32];
