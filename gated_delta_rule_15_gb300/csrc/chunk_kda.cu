@@ -81,15 +81,18 @@ constexpr uint32_t P1_TOTAL = P1_SMALL + 256 + 4096 + 512;   // + G_C[128]
 // the exact diagonal blocks over the right factors; staging of W and U at the end
 constexpr uint32_t P1_A = 0, P1_T = 16384, P1_TB = 34816, P1_XD = P1_R;
 constexpr uint32_t P1_WST = 0, P1_UST = 16384;
-// one-product chunks: the right factor's high half over V, its low half over K*G
-constexpr uint32_t P1_R1H = P1_V, P1_R1L = P1_KG;
-// tensor memory: X = [Q; K] R^T, the left factor's high and low halves; U^T, W^T afterwards
-constexpr uint32_t P1_TM_X = 0, P1_TM_LH = 64, P1_TM_LL = 128, P1_TM_U = 64, P1_TM_W = 128;
+// one-product chunks: the right factor as a 128-row B operand [R high; R low], K-block 0
+// over V and K-block 1 over K*G (16 KB apart)
+constexpr uint32_t P1_R1 = P1_V;
+// tensor memory: X = [Q; K] R^T (one product: [X_hh + X_lh | X_hl + X_ll], 128 columns; four
+// rounds: 64 columns), the left factor's high and low halves; U^T, W^T afterwards
+constexpr uint32_t P1_TM_X = 0, P1_TM_LH = 128, P1_TM_LL = 192, P1_TM_U = 128, P1_TM_W = 192;
 static_assert(P1_T + 64 * kTs * 4 <= P1_TB && P1_TB + 8192 <= P1_V, "prep layout");
 static_assert(P1_UST + 32768 <= P1_V && P1_TOTAL + 1024 <= 113 * 1024, "prep layout");
 
 constexpr uint32_t ID_KK_N16 = idesc_bf16(128, 16, false, false);
 constexpr uint32_t ID_KK_N64 = idesc_bf16(128, 64, false, false);
+constexpr uint32_t ID_KK_N128 = idesc_bf16(128, 128, false, false);
 // Largest per-channel decay (natural log) inside one 16-token block that the tensor-core
 // products of the diagonal blocks take; beyond it the chunk recomputes those entries.
 constexpr float kDiagLimit = 64.f;
@@ -184,6 +187,8 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const uint32_t tmb = tmem_base_s;
     const uint32_t tm = tmb + ((uint32_t)(32 * quarter) << 16);
     uint32_t mma_phase = 0;
+    // operand descriptors of the shared-memory base: K-major and MN-major (two 64-wide atoms)
+    const uint64_t dK0 = smem_desc_sw128(smem_u32(sm), 16, 1024), dM0 = smem_desc_sw128(smem_u32(sm), 8192, 1024);
     auto fail = [&]() {
         abort_s = 1;
         atomicExch(a.status, kErrTimeout);
@@ -277,9 +282,9 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                             pack_hi_lo(x8[u] * ex2(gl[u] - g8[u]), x8[u + 1] * ex2(gl[u + 1] - g8[u + 1]),
                                        oh[u >> 1], ol[u >> 1]);
                         }
-                        const uint32_t so = (c >> 6) * 8192 + sw128_off(t_row, c & 63);
-                        *reinterpret_cast<uint4 *>(sm + P1_R1H + so) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
-                        *reinterpret_cast<uint4 *>(sm + P1_R1L + so) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+                        const uint32_t so = (c >> 6) * 16384 + sw128_off(t_row, c & 63);
+                        *reinterpret_cast<uint4 *>(sm + P1_R1 + so) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+                        *reinterpret_cast<uint4 *>(sm + P1_R1 + 8192 + so) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
                         *reinterpret_cast<uint4 *>(a.ws.KH + go + 32 * p + 8 * i) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
                         *reinterpret_cast<uint4 *>(a.ws.KL + go + 32 * p + 8 * i) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
                     }
@@ -294,14 +299,14 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
+            // [L high; L low] x [R high; R low]^T: two N = 128 products into one accumulator
 #pragma unroll
-            for (int part = 0; part < 3; ++part)
+            for (int part = 0; part < 2; ++part)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ts(tmb + P1_TM_X, tmb + (part == 2 ? P1_TM_LL : P1_TM_LH) + 8 * ks,
-                                smem_desc_sw128(smem_u32(sm + (part == 1 ? P1_R1L : P1_R1H) +
-                                                         (ks >> 2) * 8192 + (ks & 3) * 32), 16, 1024),
-                                ID_KK_N64, (part | ks) != 0);
+                    mma_bf16_ts(tmb + P1_TM_X, tmb + (part ? P1_TM_LL : P1_TM_LH) + 8 * ks,
+                                desc_add(dK0, P1_R1 + (ks >> 2) * 16384 + (ks & 3) * 32), ID_KK_N128,
+                                (part | ks) != 0);
             mma_commit(&bar_mma);
         }
         if (!wait_cycles(&bar_mma, mma_phase)) fail();
@@ -431,8 +436,8 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
                         mma_bf16_ts(tmb + P1_TM_X + 16 * j, tmb + (part == 2 ? P1_TM_LL : P1_TM_LH) + 8 * ks,
-                                    smem_desc_sw128(smem_u32(sm + P1_R + (part == 1 ? 4096 : 0) +
-                                                             (ks >> 2) * 2048 + (ks & 3) * 32), 16, 1024),
+                                    desc_add(dK0, P1_R + (part == 1 ? 4096 : 0) +
+                                                             (ks >> 2) * 2048 + (ks & 3) * 32),
                                     ID_KK_N16, (part | ks) != 0);
                 mma_commit(&bar_mma);
             }
@@ -474,6 +479,13 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     {
         float x[32];
         tmem_ld32(tm + P1_TM_X + 32 * half, x);
+        if (!four_rounds_s) {   // one product: X = X_hh + X_lh + (X_hl + X_ll)
+            float x2[32];
+            tmem_ld32(tm + P1_TM_X + 64 + 32 * half, x2);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) x[u] += x2[u];
+        }
         tmem_wait_ld();
         const int c0 = 32 * half;
         if (diag_exact) {
@@ -524,12 +536,12 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmb + P1_TM_U, smem_desc_sw128(smem_u32(sm + P1_V + ks * 2048), 8192, 1024),
-                     smem_desc_sw128(smem_u32(sm + P1_TB + ks * 32), 16, 1024), ID_MK_N64, ks > 0);
+            mma_bf16(tmb + P1_TM_U, desc_add(dM0, P1_V + ks * 2048),
+                     desc_add(dK0, P1_TB + ks * 32), ID_MK_N64, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmb + P1_TM_W, smem_desc_sw128(smem_u32(sm + P1_KG + ks * 2048), 8192, 1024),
-                     smem_desc_sw128(smem_u32(sm + P1_TB + ks * 32), 16, 1024), ID_MK_N64, ks > 0);
+            mma_bf16(tmb + P1_TM_W, desc_add(dM0, P1_KG + ks * 2048),
+                     desc_add(dK0, P1_TB + ks * 32), ID_MK_N64, ks > 0);
         mma_commit(&bar_mma);
     }
     if (!wait_cycles(&bar_mma, mma_phase)) fail();
@@ -569,7 +581,9 @@ done:
 }
 
 // ---------------------------------------------------------------- state kernel layout
-constexpr uint32_t S2_W = 0, S2_QH = 16384, S2_QL = 32768;   // K-major [64][128], 2 K-blocks
+// [W; Q*G high; Q*G low] as one 192-row K-major B operand: per K-block of 64 channels
+// [W (8 KB) | QH (8 KB) | QL (8 KB)], the two K-blocks 24 KB apart
+constexpr uint32_t S2_WQ = 0, S2_WQ_KB = 24576;
 constexpr uint32_t S2_KH = 49152, S2_KL = 65536;             // MN-major [64 tok][128 ch]
 constexpr uint32_t S2_P = 81920;                             // 2 buffers of [P high | P low]
 constexpr uint32_t S2_U = 114688;                            // [64][128] fp32, 4 boxes of 32
@@ -578,10 +592,11 @@ constexpr uint32_t S2_EH = 180224, S2_EL = 196608;           // E^T bf16 pair [1
 constexpr uint32_t S2_SMALL = 212992;                        // G_C of two chunks
 constexpr uint32_t S2_TOTAL = S2_SMALL + 1024;
 static_assert(S2_TOTAL + 1024 <= 227 * 1024, "state layout");
-// tensor memory: S^T, (W S)^T, then two buffers each of (Q*G S)^T and E^T P^T
-constexpr uint32_t S2_TM_S = 0, S2_TM_DW = 128, S2_TM_DQ = 192, S2_TM_PE = 320;
+// tensor memory: S^T, then two buffers of [(W S)^T | (QH S)^T + E^T P^T | (QL S)^T]
+constexpr uint32_t S2_TM_S = 0, S2_TM_D = 128, S2_TM_DSTRIDE = 192;
 
 constexpr uint32_t ID_KM_N128 = idesc_bf16(128, 128, false, true);
+constexpr uint32_t ID_KK_N192 = idesc_bf16(128, 192, false, false);
 
 struct StateArgs {
     const float *init_state;
@@ -593,12 +608,12 @@ struct StateArgs {
 
 // Per chunk c, in order (thread 0 issues the MMAs, thread 224 the TMA loads):
 //   1. S^T -> bf16 operand (ST), S^T <- S^T Diag(G_C)
-//   2. (W S)^T -> DW [bar_dw];  (Q*G S)^T -> DQ[c % 2] [bar_dq]
-//   3. refill W for c + 1; refill P for c + 1 (its buffer was read by chunk c - 1)
-//   4. E^T = U^T - (W S)^T as a bf16 pair; refill Q (once (Q*G S)^T is done) and U
-//   5. S^T += E^T (K*G_C/G) [bar_s];  E^T P^T -> PE[c % 2] [bar_pe]
-//   6. once DQ[c % 2] is done reading ST: output of chunk c - 1 = DQ + PE of its
-//      buffers, staged in ST and stored by TMA (overlaps the MMAs of step 5)
+//   2. D[c % 2] = S^T [W; QH; QL]^T, one N = 192 product [bar_dw]
+//   3. refill W and Q for c + 1; refill P for c + 1 (its buffer was read by chunk c - 1)
+//   4. E^T = U^T - (W S)^T as a bf16 pair; refill U
+//   5. S^T += E^T (K*G_C/G) [bar_s];  E^T P^T accumulated onto (QH S)^T in D[c % 2] [bar_pe]
+//   6. output of chunk c - 1 = the sum of its D buffer's two (Q*G S)^T halves, staged in ST
+//      (free: D[c % 2] is done reading it) and stored by TMA (overlaps step 5's MMAs)
 //   7. wait for the state update; refill K
 // Every parity wait is placed where its barrier can be at most one phase ahead.
 template <typename Tout>
@@ -610,7 +625,7 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
                  const __grid_constant__ CUtensorMap to, const StateArgs a) {
     extern __shared__ unsigned char dsm_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
-    __shared__ uint64_t bar_w, bar_q, bar_u, bar_k, bar_p[2], bar_dw, bar_dq, bar_s, bar_pe;
+    __shared__ uint64_t bar_w, bar_q, bar_u, bar_k, bar_p[2], bar_dw, bar_s, bar_pe;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
 
@@ -624,7 +639,7 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
 
     if (tid == 0) {
         uint64_t *bars[] = {&bar_w, &bar_q, &bar_u, &bar_k, &bar_p[0], &bar_p[1],
-                            &bar_dw, &bar_dq, &bar_s, &bar_pe};
+                            &bar_dw, &bar_s, &bar_pe};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         abort_s = 0;
         fence_mbar_init();
@@ -638,6 +653,8 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
     tc_fence_after();
     const uint32_t tmb = tmem_base_s;
     const uint32_t tm = tmb + ((uint32_t)(32 * quarter) << 16);
+    // operand descriptors of the shared-memory base: K-major and MN-major (two 64-wide atoms)
+    const uint64_t dK0 = smem_desc_sw128(smem_u32(sm), 16, 1024), dM0 = smem_desc_sw128(smem_u32(sm), 8192, 1024);
     auto fail = [&]() {
         abort_s = 1;
         atomicExch(a.status, kErrTimeout);
@@ -663,13 +680,13 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
     auto rowc = [&](int c) { return (int)((n0 + c) * 64); };
     auto load_w = [&](int c) {
         mbar_arrive_expect_tx(&bar_w, 16384);
-        for (int kb = 0; kb < 2; ++kb) tma_load_2d(sm + S2_W + kb * 8192, &mw, &bar_w, 64 * kb, rowc(c));
+        for (int kb = 0; kb < 2; ++kb) tma_load_2d(sm + S2_WQ + kb * S2_WQ_KB, &mw, &bar_w, 64 * kb, rowc(c));
     };
     auto load_q = [&](int c) {
         mbar_arrive_expect_tx(&bar_q, 32768);
         for (int kb = 0; kb < 2; ++kb) {
-            tma_load_2d(sm + S2_QH + kb * 8192, &mqh, &bar_q, 64 * kb, rowc(c));
-            tma_load_2d(sm + S2_QL + kb * 8192, &mql, &bar_q, 64 * kb, rowc(c));
+            tma_load_2d(sm + S2_WQ + kb * S2_WQ_KB + 8192, &mqh, &bar_q, 64 * kb, rowc(c));
+            tma_load_2d(sm + S2_WQ + kb * S2_WQ_KB + 16384, &mql, &bar_q, 64 * kb, rowc(c));
         }
     };
     auto load_u = [&](int c) {
@@ -704,9 +721,9 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
     bool store_outstanding = false;   // thread 0: a TMA store from ST may still be reading it
     // output of chunk c from its DQ / PE buffers, staged in ST (free: see the callers)
     auto emit = [&](int c) {
-        float o[32], pe[32];
-        tmem_ld32(tm + S2_TM_DQ + 64 * (c & 1) + 32 * half, o);
-        tmem_ld32(tm + S2_TM_PE + 64 * (c & 1) + 32 * half, pe);
+        float o[32], pe[32];   // (QH S)^T + E^T P^T, and (QL S)^T
+        tmem_ld32(tm + S2_TM_D + S2_TM_DSTRIDE * (c & 1) + 64 + 32 * half, o);
+        tmem_ld32(tm + S2_TM_D + S2_TM_DSTRIDE * (c & 1) + 128 + 32 * half, pe);
         tmem_wait_ld();
         const int j = row;
         if (sizeof(Tout) == 2) {
@@ -777,33 +794,24 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         __syncthreads();
         if (abort_s) break;
 
-        // ---- 2. (W S)^T, then (Q*G S)^T (a high/low pair) into this chunk's DQ buffer
+        // ---- 2. D[c % 2] = S^T [W; QH; QL]^T in one N = 192 product
         if (tid == 0) {
             if (!wait_cycles(&bar_w, par)) fail();
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32, ob = (ks >> 2) * 8192 + (ks & 3) * 32;
-                mma_bf16(tmb + S2_TM_DW, smem_desc_sw128(smem_u32(sm + S2_ST + o), 16, 1024),
-                         smem_desc_sw128(smem_u32(sm + S2_W + ob), 16, 1024), ID_KK_N64, ks > 0);
-            }
-            mma_commit(&bar_dw);
             if (!wait_cycles(&bar_q, par)) fail();
             tc_fence_after();
-            const uint32_t dq = tmb + S2_TM_DQ + 64 * par;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32, ob = (ks >> 2) * 8192 + (ks & 3) * 32;
-                const uint64_t ad = smem_desc_sw128(smem_u32(sm + S2_ST + o), 16, 1024);
-                mma_bf16(dq, ad, smem_desc_sw128(smem_u32(sm + S2_QH + ob), 16, 1024), ID_KK_N64, ks > 0);
-                mma_bf16(dq, ad, smem_desc_sw128(smem_u32(sm + S2_QL + ob), 16, 1024), ID_KK_N64, 1);
+                const uint32_t kk = (ks & 3) * 32;
+                mma_bf16(tmb + S2_TM_D + S2_TM_DSTRIDE * par, desc_add(dK0, S2_ST + (ks >> 2) * 16384 + kk),
+                         desc_add(dK0, S2_WQ + (ks >> 2) * S2_WQ_KB + kk), ID_KK_N192, ks > 0);
             }
-            mma_commit(&bar_dq);
+            mma_commit(&bar_dw);
         }
         wait_bar(&bar_dw, par);
-        // ---- 3. refills: W for c + 1; P for c + 1 into the buffer chunk c - 1 read
+        // ---- 3. refills: W and Q for c + 1; P for c + 1 into the buffer chunk c - 1 read
         if (tid == kTmaThread && c + 1 < a.NC) {
             load_w(c + 1);
+            load_q(c + 1);
             if (c >= 1) {
                 if (!wait_cycles(&bar_pe, (c - 1) & 1)) fail();
                 load_p(c + 1);
@@ -816,7 +824,7 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         if (!wait_cycles(&bar_u, par)) fail();
         {
             float ws[32];
-            tmem_ld32(tm + S2_TM_DW + 32 * half, ws);
+            tmem_ld32(tm + S2_TM_D + S2_TM_DSTRIDE * par + 32 * half, ws);
             tmem_wait_ld();
             const float *U = reinterpret_cast<const float *>(sm + S2_U);
             const int j = row;
@@ -836,10 +844,6 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
                 *reinterpret_cast<uint4 *>(sm + S2_EL + off) = make_uint4(el[0], el[1], el[2], el[3]);
             }
         }
-        if (tid == kTmaThread && c + 1 < a.NC) {   // (Q*G S)^T was issued before (W S)^T completed
-            if (!wait_cycles(&bar_dq, par)) fail();
-            load_q(c + 1);
-        }
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
@@ -858,22 +862,20 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
             for (int part = 0; part < 3; ++part)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmb + S2_TM_S, smem_desc_sw128(smem_u32(sm + ea[part] + ks * 32), 16, 1024),
-                             smem_desc_sw128(smem_u32(sm + kbuf[part] + ks * 2048), 8192, 1024), ID_KM_N128, 1);
+                    mma_bf16(tmb + S2_TM_S, desc_add(dK0, ea[part] + ks * 32),
+                             desc_add(dM0, kbuf[part] + ks * 2048), ID_KM_N128, 1);
             mma_commit(&bar_s);
-            const uint32_t pe = tmb + S2_TM_PE + 64 * par;
+            const uint32_t pe = tmb + S2_TM_D + S2_TM_DSTRIDE * par + 64;   // onto (QH S)^T
 #pragma unroll
             for (int part = 0; part < 3; ++part)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(pe, smem_desc_sw128(smem_u32(sm + ea[part] + ks * 32), 16, 1024),
-                             smem_desc_sw128(smem_u32(sm + pbuf[part] + ks * 32), 16, 1024), ID_KK_N64,
-                             (part | ks) != 0);
+                    mma_bf16(pe, desc_add(dK0, ea[part] + ks * 32),
+                             desc_add(dK0, pbuf[part] + ks * 32), ID_KK_N64, 1);
             mma_commit(&bar_pe);
         }
 
-        // ---- 6. once (Q*G S)^T has read ST: output of chunk c - 1
-        wait_bar(&bar_dq, par);
+        // ---- 6. output of chunk c - 1 (ST is free: this chunk's D product has completed)
         if (c >= 1) emit(c - 1);
 
         // ---- 7. state update done; K buffer is free

@@ -53,14 +53,18 @@ namespace {
 using namespace umma;
 using namespace tc;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;                  // compute warps 0..7
+constexpr int kMmaWarp = 8;                    // warp 8 only issues the tcgen05 MMAs
+constexpr int kCtaThreads = kThreads + 32;
 constexpr uint32_t kStageBytes = 49152;
 // stage layout: [Q kb0 | K kb0 | Q kb1 | K kb1 | V kb0 | V kb1], 8 KB each (64 x 64 bf16)
 constexpr uint32_t OFF_K0 = 8192, OFF_V0 = 32768;
 constexpr uint32_t SM_W = 2 * kStageBytes;    // T diag beta (+G) for the U/W products, then
-                                              // W 64 x 128 K-major (2 K-blocks of 8 KB), then
-                                              // the low part of E^T
-constexpr uint32_t SM_ST = SM_W + 16384;      // S^T 128 x 128 K-major; fp32 T during the solve
+                                              // [W kb0 | Q kb0 | W kb1 | Q kb1]: the 128-row
+                                              // B operand [W; Q] of D (W 64 x 128 K-major and
+                                              // a copy of the chunk's Q), then the low part
+                                              // of E^T
+constexpr uint32_t SM_ST = SM_W + 32768;      // S^T 128 x 128 K-major; fp32 T during the solve
 constexpr uint32_t SM_ET = SM_ST + 32768;     // E^T (high) 128 x 64
 constexpr uint32_t SM_ET2 = SM_ET + 16384;    // E^T diag(delta) (high); fp32 A during the solve
                                               // SM_ET..SM_ET2 + 16 KB: the output tile at the end
@@ -73,6 +77,7 @@ constexpr uint32_t SM_SMALL = SM_PLO + 8192;  // per-token vectors and solve scr
 constexpr uint32_t SM_A = SM_ET2;   // fp32 A during the solve
 constexpr uint32_t SM_TB = SM_W;    // T diag(beta), T diag(beta G) until the U/W products
 constexpr uint32_t SM_TOTAL = SM_SMALL + 8192;
+static_assert(SM_TOTAL + 1024 <= 227 * 1024, "layout");
 constexpr uint32_t TM_S = 0, TM_D = 128, TM_X = 256, TM_U = 320, TM_W = 384, TM_PE = 448;
 // TM_D: [ (W S)^T | (Q S)^T ];  TM_X: [Q; K] K^T;  TM_PE: E^T P^T
 // Largest in-chunk log-decay span for which exp(g_r - g_s) is formed as a product of two
@@ -82,6 +87,7 @@ constexpr float kFactorSpan = 80.f;
 constexpr uint32_t ID_KK_N64 = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_MK_N64 = idesc_bf16(128, 64, true, false);
 constexpr uint32_t ID_KM_N128 = idesc_bf16(128, 128, false, true);
+constexpr uint32_t ID_KK_N128 = idesc_bf16(128, 128, false, false);
 
 struct TcArgs {
     const float *log_alpha;
@@ -99,14 +105,16 @@ struct TcArgs {
 };
 
 template <typename Tout, int GATE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kCtaThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
                 const TcArgs a) {
     extern __shared__ unsigned char dsm_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
-    // mbarriers: TMA stages, and one per MMA group (each completes once per chunk)
-    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_q, bar_s;
+    // mbarriers: TMA stages; per MMA group its completion (committed by the MMA warp) and,
+    // for the groups whose operands the compute warps write, "operands ready" (full_*,
+    // arrived by thread 0 after the compute warps' barrier).  Each completes once per chunk.
+    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_s, full_uw, full_d, full_s;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s, factored_s;
 
@@ -142,7 +150,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     }
     const int h = bh % a.H, b = bh / a.H;
     constexpr int kTmaThread = 224;              // lane 0 of warp 7 issues the TMA loads
-    constexpr int kGateWarp = 1;                 // warp 1 scans the gates; thread 0 issues MMAs
+    constexpr int kGateWarp = 1;                 // warp 1 scans the gates
     float *sG = reinterpret_cast<float *>(sm + SM_SMALL);   // g_r (cumulative log decay)
     float *sGam = sG + 64;     // exp(g_r)
     float *sDel = sG + 128;    // exp(g_63 - g_r)
@@ -162,8 +170,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         mbar_init(&bar_x, 1);
         mbar_init(&bar_uw, 1);
         mbar_init(&bar_d, 1);
-        mbar_init(&bar_q, 1);
         mbar_init(&bar_s, 1);
+        mbar_init(&full_uw, 1);
+        mbar_init(&full_d, 1);
+        mbar_init(&full_s, 1);
         abort_s = 0;
         fence_mbar_init();
     }
@@ -175,9 +185,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = tmem_base_s + ((uint32_t)(32 * quarter) << 16);   // + this warp's lanes
+    // operand descriptors of the shared-memory base: K-major, and MN-major with the two
+    // 64-wide atoms 8192 or 16384 bytes apart
+    const uint64_t dK0 = smem_desc_sw128(smem_u32(sm), 16, 1024);
+    const uint64_t dM8 = smem_desc_sw128(smem_u32(sm), 8192, 1024), dM16 = smem_desc_sw128(smem_u32(sm), 16384, 1024);
 
     // S^T[j][i] = S_0[i][j]: this thread owns j = row and i in [64 half, 64 half + 64).
-    {
+    if (warp < kMmaWarp) {
         float v[32];
         for (int part = 0; part < 2; ++part) {
             const int i0 = 64 * half + 32 * part;
@@ -241,7 +255,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         if (!wait_cycles(bar, parity)) fail();
         tc_fence_after();
     };
-    // (thread 0) wait for chunk c's tiles, then X = [Q; K] K^T into TM_X
+    // (MMA warp) wait for chunk c's tiles, then X = [Q; K] K^T into TM_X
     auto issue_x = [&](int it) {
         if (!wait_cycles(&bar_tma[it & 1], (it >> 1) & 1)) fail();
         unsigned char *st = sm + (it & 1) * kStageBytes;
@@ -249,8 +263,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_bf16(tmem_base_s + TM_X, smem_desc_sw128(smem_u32(st + o), 16, 1024),
-                     smem_desc_sw128(smem_u32(st + OFF_K0 + o), 16, 1024), ID_KK_N64, ks > 0);
+            mma_bf16(tmem_base_s + TM_X, desc_add(dK0, (uint32_t)((st + o) - sm)),
+                     desc_add(dK0, (uint32_t)((st + OFF_K0 + o) - sm)), ID_KK_N64, ks > 0);
         }
         mma_commit(&bar_x);
     };
@@ -283,7 +297,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        named_sync(1, kThreads);
         if (tid == 0) {
             constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
 #pragma unroll
@@ -296,8 +310,73 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 store_outstanding = false;
             }
         }
-        if (kWideOut) __syncthreads();
+        if (kWideOut) named_sync(1, kThreads);
     };
+
+    // ---------------- MMA warp: issues every tcgen05.mma group in chunk order, each once its
+    // operands are ready, and commits it to the barrier the compute warps wait on.
+    if (warp == kMmaWarp) {
+        if (lane == 0 && n_it > 0) {
+            uint64_t *last = &bar_x;   // most recent commit (drained on abort)
+            uint32_t last_par = 0;
+            issue_x(0);
+            for (int it = 0; it < n_it && !abort_s; ++it) {
+                const uint32_t par = it & 1;
+                unsigned char *st = sm + (it & 1) * kStageBytes;
+                // U^T = V^T (T diag beta)^T,  W^T = K^T (T diag(beta G))^T
+                if (!wait_cycles(&full_uw, par)) { fail(); break; }
+                tc_fence_after();
+                if (!zero_u)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem_base_s + TM_U, desc_add(dM8, (uint32_t)((st + OFF_V0 + ks * 2048) - sm)),
+                             desc_add(dK0, (uint32_t)(SM_TB + ks * 32)), ID_MK_N64, ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem_base_s + TM_W, desc_add(dM16, (uint32_t)((st + OFF_K0 + ks * 2048) - sm)),
+                             desc_add(dK0, (uint32_t)(SM_TB + 8192 + ks * 32)), ID_MK_N64, ks > 0);
+                mma_commit(&bar_uw);
+                last = &bar_uw; last_par = par;
+                // D = S^T [W; Q]^T in one N = 128 product: (W S)^T | (Q S)^T
+                if (!wait_cycles(&full_d, par)) { fail(); break; }
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_bf16(tmem_base_s + TM_D, desc_add(dK0, SM_ST + o), desc_add(dK0, SM_W + o),
+                             outputs ? ID_KK_N128 : ID_KK_N64, ks > 0);
+                }
+                mma_commit(&bar_d);
+                last = &bar_d; last_par = par;
+                // S^T += (E^T diag delta) K ;  PE = E^T P^T  (high/low pairs); then the next X
+                if (!wait_cycles(&full_s, par)) { fail(); break; }
+                tc_fence_after();
+                unsigned char *e2[2] = {sm + SM_ET2, st + OFF_V0};
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tmem_base_s + TM_S, desc_add(dK0, (uint32_t)((e2[part] + ks * 32) - sm)),
+                                 desc_add(dM16, (uint32_t)((st + OFF_K0 + ks * 2048) - sm)), ID_KM_N128, 1);
+                const uint32_t ea[3] = {SM_ET, SM_ET, SM_ETLO}, pb[3] = {SM_P, SM_PLO, SM_P};
+                if (outputs)
+#pragma unroll
+                for (int part = 0; part < 3; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tmem_base_s + TM_PE, desc_add(dK0, ea[part] + ks * 32),
+                                 desc_add(dK0, pb[part] + ks * 32), ID_KK_N64, (part | ks) != 0);
+                mma_commit(&bar_s);
+                last = &bar_s; last_par = par;
+                if (it + 1 < n_it) {
+                    issue_x(it + 1);
+                    last = &bar_x; last_par = (it + 1) & 1;
+                }
+            }
+            if (abort_s) wait_cycles(last, last_par);   // drain this warp's MMAs (bounded)
+        }
+        __syncwarp();
+    } else {
 
     for (int it = 0; it < n_it; ++it) {
         const int c = c_begin + it;
@@ -306,9 +385,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         unsigned char *st = sm + s * kStageBytes;
         const int t0 = c * 64;
 
-        // ---- 1. X = [Q; K] K^T of this chunk (the first chunk's here; later ones are issued
-        //         right after the previous chunk's state update)
-        if (it == 0 && tid == 0) issue_x(0);
+        // ---- 1. X = [Q; K] K^T of this chunk: issued by the MMA warp (the first chunk's at
+        //         once, later ones right after the previous chunk's state update)
         // ---- 2. cumulative log decay of this chunk (gate warp; its gates arrived by cp.async)
         if (warp == kGateWarp) {
             cp_async_wait_all();
@@ -354,7 +432,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             wait_bar(&bar_s, par ^ 1);
             s_outstanding = false;
         }
-        __syncthreads();            // gate vectors published; previous chunk's MMAs done
+        named_sync(1, kThreads);    // gate vectors published; previous chunk's MMAs done
         if (abort_s) break;
         if (out_pending && outputs) write_out(cur_t0);
         if (tid == kTmaThread && it + 1 < n_it) {
@@ -422,27 +500,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        named_sync(1, kThreads);
 
         // ---- 5-6. T = (I + A)^-1 (fp32, [64][kTs] at SM_ST), with T diag(beta) and
         //           T diag(beta G) in bf16 at SM_TB
         solve_unit_lower64(reinterpret_cast<const float *>(sm + SM_A),
                            reinterpret_cast<float *>(sm + SM_ST), sM, sm + SM_TB, sBeta, sGam, tid);
 
-        // ---- 7. U^T = V^T (T diag beta)^T,  W^T = K^T (T diag(beta G))^T
-        if (tid == 0) {
-            tc_fence_after();
-            if (!zero_u)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem_base_s + TM_U, smem_desc_sw128(smem_u32(st + OFF_V0 + ks * 2048), 8192, 1024),
-                         smem_desc_sw128(smem_u32(sm + SM_TB + ks * 32), 16, 1024), ID_MK_N64, ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem_base_s + TM_W, smem_desc_sw128(smem_u32(st + OFF_K0 + ks * 2048), 16384, 1024),
-                         smem_desc_sw128(smem_u32(sm + SM_TB + 8192 + ks * 32), 16, 1024), ID_MK_N64, ks > 0);
-            mma_commit(&bar_uw);
-        }
+        // ---- 7. U^T = V^T (T diag beta)^T,  W^T = K^T (T diag(beta G))^T (MMA warp)
+        if (tid == 0) mbar_arrive(&full_uw);
         // ---- 8. meanwhile: S^T to bf16 (MMA operand at SM_ST); S^T <- gamma S^T in TMEM
         {
             const float gamma = sGam[63];
@@ -465,53 +531,49 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             }
             tmem_wait_st();
         }
-        // ---- 9. W from W^T: lane i = key channel, columns = tokens r
+        // ---- 9. W from W^T (lane i = key channel, columns = tokens r) into the B operand
+        //         [W; Q] of D, and the chunk's Q tiles copied beside it
         wait_bar(&bar_uw, par);
         {
             float w[32];
             tmem_ld32(tm + TM_W + 32 * half, w);
             tmem_wait_ld();
             const int i = row, kb = i >> 6, ci = i & 63;
-            unsigned char *dst = sm + SM_W + kb * 8192;
+            unsigned char *dst = sm + SM_W + kb * 16384;
 #pragma unroll
             for (int u = 0; u < 32; ++u)
                 *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, ci)) =
                     __float2bfloat16_rn(w[u]);
+            if (outputs) {   // 16 KB of swizzled tiles: the copy keeps the pattern (1 KB aligned)
+                // the tiles arrived by TMA (seen so far by the MMA warp only); this stage's
+                // next load is issued after the next chunk's step 3
+                if (!wait_cycles(&bar_tma[it & 1], (it >> 1) & 1)) fail();
+                const uint4 *qs = reinterpret_cast<const uint4 *>(st);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = tid + 256 * k, kbq = e >> 9, off = e & 511;   // 512 x 16 B per kb
+                    reinterpret_cast<uint4 *>(sm + SM_W + kbq * 16384 + 8192)[off] = qs[kbq * 1024 + off];
+                }
+            }
         }
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        named_sync(1, kThreads);
         if (abort_s) break;
 
-        // ---- 10. D = S^T [W; Q]^T  (Q straight from the stage)
+        // ---- 10. D = S^T [W; Q]^T  (MMA warp)
         if (tid == 0) {
+            mbar_arrive(&full_d);
             if (store_outstanding) {   // the previous output tile must have left SM_OUT
                 bulk_wait_read_all();  // before E^T is written there
                 store_outstanding = false;
             }
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_bf16(tmem_base_s + TM_D, smem_desc_sw128(smem_u32(sm + SM_ST + o), 16, 1024),
-                         smem_desc_sw128(smem_u32(sm + SM_W + (ks >> 2) * 8192 + (ks & 3) * 32), 16, 1024),
-                         ID_KK_N64, ks > 0);
-            }
-            mma_commit(&bar_d);   // (W S)^T: needed by the E^T build
-            if (outputs) {
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_bf16(tmem_base_s + TM_D + 64, smem_desc_sw128(smem_u32(sm + SM_ST + o), 16, 1024),
-                             smem_desc_sw128(smem_u32(st + o), 16, 1024), ID_KK_N64, ks > 0);
-                }
-                mma_commit(&bar_q);   // (Q S)^T: needed by the write-out only
-            }
         }
+        named_sync(1, kThreads);
         wait_bar(&bar_d, par);
 
         // ---- 11. E^T = U^T - (W S)^T, and E^T diag(delta)  (bf16 high/low pairs); the (Q S)^T
-        //          half completes meanwhile and is read by the deferred write-out
+        //          half is read by the deferred write-out
         {
             float ws[32], uu[32];
             tmem_ld32(tm + TM_D + 32 * half, ws);
@@ -543,34 +605,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     make_uint4(dlo[0], dlo[1], dlo[2], dlo[3]);
             }
         }
-        if (outputs) wait_bar(&bar_q, par);
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        named_sync(1, kThreads);
 
-        // ---- 12. S^T += (E^T diag delta) K ;  PE = E^T P^T  (high/low pairs); completes
-        //          while the next chunk starts, whose step 3 waits for it
-        if (tid == 0) {
-            tc_fence_after();
-            unsigned char *e2[2] = {sm + SM_ET2, st + OFF_V0};
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem_base_s + TM_S, smem_desc_sw128(smem_u32(e2[part] + ks * 32), 16, 1024),
-                             smem_desc_sw128(smem_u32(st + OFF_K0 + ks * 2048), 16384, 1024), ID_KM_N128, 1);
-            const uint32_t ea[3] = {SM_ET, SM_ET, SM_ETLO}, pb[3] = {SM_P, SM_PLO, SM_P};
-            if (outputs)
-#pragma unroll
-            for (int part = 0; part < 3; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem_base_s + TM_PE, smem_desc_sw128(smem_u32(sm + ea[part] + ks * 32), 16, 1024),
-                             smem_desc_sw128(smem_u32(sm + pb[part] + ks * 32), 16, 1024), ID_KK_N64,
-                             (part | ks) != 0);
-            mma_commit(&bar_s);
-            if (it + 1 < n_it) issue_x(it + 1);
-        }
+        // ---- 12. S^T += (E^T diag delta) K ;  PE = E^T P^T  (high/low pairs; MMA warp, which
+        //          then issues the next chunk's X); completes while the next chunk starts,
+        //          whose step 3 waits for it
+        if (tid == 0) mbar_arrive(&full_s);
         s_outstanding = true;
         out_pending = true;
         cur_t0 = t0;
@@ -579,14 +621,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     if (!abort_s && s_outstanding) {
         wait_bar(&bar_s, (n_it - 1) & 1);
         s_outstanding = false;
-        __syncthreads();
+        named_sync(1, kThreads);
         if (!abort_s && out_pending && outputs) write_out(cur_t0);
     }
     if (abort_s) {
-        // Drain this CTA's own asynchronous work (bounded) before TMEM is freed.
+        // Drain this CTA's own asynchronous work (bounded) before TMEM is freed; the MMA
+        // warp drains its own MMAs.
         if (tid == kTmaThread)   // the last load may still be in flight (bounded wait)
             wait_cycles(&bar_tma[last_tma_it & 1], (last_tma_it >> 1) & 1);
-        if (tid == 0 && s_outstanding) wait_cycles(&bar_s, (n_it - 1) & 1);
     } else if (fin_ptr) {
         float v[32];
         for (int part = 0; part < 2; ++part) {
@@ -599,6 +641,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     }
     if (warp == kGateWarp) cp_async_wait_all();
     if (tid == 0 && store_outstanding) bulk_wait_all();
+    }   // compute warps
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -676,7 +719,7 @@ int launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv
     if (cudaFuncSetAttribute(chunk_tc_kernel<Tout, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
         return kErrCuda;
-    chunk_tc_kernel<Tout, GATE><<<grid, kThreads, smem, stream>>>(mq, mk, mv, mo, ta);
+    chunk_tc_kernel<Tout, GATE><<<grid, kCtaThreads, smem, stream>>>(mq, mk, mv, mo, ta);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 

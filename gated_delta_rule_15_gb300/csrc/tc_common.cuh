@@ -89,7 +89,8 @@ __device__ __forceinline__ int a_index(int r, int s) {
 // Each element is written, once final, also as T diag(beta) in bf16 (a 128-byte-swizzled
 // K-major 64 x 64 tile at TB) and, with kPair, as T diag(beta G) at TB + 8192: the U and W
 // operands.  Products use TF32 mma.sync with fp32 accumulation.  M needs 1024 floats.
-// Called by all 256 threads; starts after and ends with a barrier.
+// Called by 256 threads (the CTA's compute warps, which synchronise on named barrier 1);
+// starts after and ends with a barrier.
 template <bool kPair = true>
 __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, float *M,
                                                    unsigned char *TB, const float *beta,
@@ -154,7 +155,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
                 *reinterpret_cast<uint4 *>(TB + 8192 + off) = make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    __syncthreads();
+    named_sync(1, 256);
     if (warp < 2) {
         const int i = 2 * warp + 1, j = 2 * warp;
         float *Ms = M + 256 * warp;
@@ -170,7 +171,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         warp_store16(acc2, -1.f, [&](int r, int n, float v0, float v1) {
             fin2(16 * i + r, 16 * j + n, v0, v1); }, g, t4);
     }
-    __syncthreads();
+    named_sync(1, 256);
     if (warp < 4) {   // M tile (rb, cb) = sum_{k = cb}^{1} A_{rb,k} T_{k,cb},  rb = 2 + w/2, cb = w%2
         const int rb = 2 + (warp >> 1), cb = warp & 1;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -180,7 +181,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         warp_store16(acc, 1.f, [&](int r, int n, float v0, float v1) {
             *reinterpret_cast<float2 *>(Mt + r * 16 + n) = make_float2(v0, v1); }, g, t4);
     }
-    __syncthreads();
+    named_sync(1, 256);
     if (warp < 4) {   // T_{rb,cb} = -sum_{k = 2}^{rb} T_{rb,k} M_{k,cb}
         const int rb = 2 + (warp >> 1), cb = warp & 1;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -191,7 +192,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
             fin2(16 * rb + r, 16 * cb + n, v0, v1); }, g, t4);
     }
     fence_proxy_async();   // the bf16 operands are read next by the tensor core
-    __syncthreads();
+    named_sync(1, 256);
 }
 
 }  // namespace tc
