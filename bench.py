@@ -33,10 +33,11 @@ HEADLINE = "gdn_bf16_B8_H16_T4096_d128"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic per launch (read + write bytes) of the dominant kernel, from one ncu capture
-# (profiles/chunk_tc_kernel_gdn_B2_T16384_H16.md): that case has the headline's 524,288
-# head-tokens, and the kernel's traffic is proportional to head-tokens.  Valid only while
-# the kernel sources hash to `src`; otherwise the bench reports null.
-TRAFFIC = {"chunk_fwd": {"bytes": 405889536 + 115638784, "src": "222becd13a98e893"}}
+# (profiles/chunk_tc_kernel_gdn_B8_T2048_H16.md): that case is the headline's launch shape
+# (128 chains) with half its head-tokens, and the kernel's traffic is proportional to
+# head-tokens, so the figure is twice the captured one.  Valid only while the kernel
+# sources hash to `src`; otherwise the bench reports null.
+TRAFFIC = {"chunk_fwd": {"bytes": 2 * (203593984 + 50276608), "src": "9fb528ecf7d1b64e"}}
 
 
 def peaks():
