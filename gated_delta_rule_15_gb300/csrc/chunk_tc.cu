@@ -11,7 +11,7 @@
 //
 //   X   = [Q; K] K^T                     (128 x 64)  raw q.k and k.k products
 //   P   = tril(exp(g_r - g_s) Q K^T)     (64 x 64)   read matrix, diagonal included
-//   A   = stril(beta_r exp(g_r - g_s) K K^T),  T = (I + A)^-1   (fp32, blocked, see below)
+//   A   = stril(beta_r exp(g_r - g_s) K K^T),  T = (I + A)^-1   (fp32, blocked)
 //   U^T = V^T (T diag beta)^T            (128 x 64)  = (T diag(beta) V)^T
 //   W^T = K^T (T diag(beta G))^T         (128 x 64)  = (T diag(beta) (K*G))^T
 //   D   = S^T [W; Q]^T                   (128 x 128) = [(W S)^T | (Q S)^T]
@@ -22,22 +22,26 @@
 // Precision: P, E^T and E^T diag(delta) enter their products as a bf16 pair (high part and
 // the bf16 rounding of the remainder), so those products carry ~2^-16 relative error
 // instead of bf16's 2^-8; S^T, W and the T factors enter as single bf16 operands, Q exactly
-// (its decay G is applied to Q S in fp32).  A
-// rounding model of this arithmetic against the fp64 oracle puts the output error at
-// ~1e-2 x RMS (about 3e-2 without the pairs).
+// (its decay G is applied to Q S in fp32).  A rounding model of this arithmetic against the
+// fp64 oracle puts the output error at ~1e-2 x RMS (about 3e-2 without the pairs).
 //
-// One CTA per (b, h), 256 threads, the whole TMEM (512 columns): S^T [0,128), D [128,256),
-// X [256,320) (later E^T P^T), U^T [320,384), W^T [384,448).  T = (I + A)^-1 is built by
-// 16 x 16 blocks: the diagonal blocks by right-looking substitution (one thread per column),
-// the blocks below them by warp-level TF32 mma.sync chains, T_ij = -T_ii sum_k A_ik T_kj,
-// one warp per block column (no cross-warp dependence).  q, k, v tiles (64 tokens x 128, bf16) arrive
-// by TMA with 128-byte swizzle into a double-buffered stage; the next chunk's tiles load
-// while the current chunk computes.  Operands written by the CUDA cores (P, T diag beta,
-// W, Q*G, S^T, E^T) use the same swizzled K-major layout; V and K tiles also serve as
-// MN-major operands directly.  One thread issues the MMAs; completion is tracked with
-// tcgen05.commit on an mbarrier.  Every wait is bounded by a cycle budget: on expiry the
-// kernel records DR_ERR_TIMEOUT in the status word, drains its own copies and MMAs (with
-// the same bound), frees TMEM and returns.
+// One CTA per (b, h): eight compute warps and one warp that only issues the tcgen05 MMAs.
+// The chunk steps are software-pipelined across two chunks, so that the MMA groups of one
+// run while the CUDA cores work on the other.  In the iteration of chunk c the compute warps
+//   1. convert S^T to the bf16 operand of D and decay S^T in TMEM,
+//   2. write W (from TMEM) as the B operand of D            -> MMA warp: D(c)
+//   3. build the next chunk's A from its X (already in TMEM),
+//   4. build E^T and E^T diag(delta)                          -> MMA warp: state update,
+//                                                                E^T P^T (c)
+//   5. solve the next chunk's T = (I + A)^-1                  -> MMA warp: U/W(c+1)
+//   6. write chunk c's output and the next chunk's P          -> MMA warp: X(c+2),
+//                                                                stage of c takes c + 2
+// and the gate warp scans the gates two chunks ahead.  T = (I + A)^-1 is built by 16 x 16
+// blocks (tc_common.cuh).  q, k, v tiles (64 tokens x 128, bf16) arrive by TMA with 128-byte
+// swizzle into two stages; operands written by the CUDA cores use the same swizzled K-major
+// layout, and the V and K tiles also serve as MN-major operands directly.  Every wait is
+// bounded by a cycle budget: on expiry the kernel records DR_ERR_TIMEOUT in the status
+// word, drains its own copies and MMAs (with the same bound), frees TMEM and returns.
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -59,23 +63,22 @@ constexpr int kCtaThreads = kThreads + 32;
 constexpr uint32_t kStageBytes = 49152;
 // stage layout: [Q kb0 | K kb0 | Q kb1 | K kb1 | V kb0 | V kb1], 8 KB each (64 x 64 bf16)
 constexpr uint32_t OFF_K0 = 8192, OFF_V0 = 32768;
-constexpr uint32_t SM_W = 2 * kStageBytes;    // T diag beta (+G) for the U/W products, then
-                                              // [W kb0 | Q kb0 | W kb1 | Q kb1]: the 128-row
-                                              // B operand [W; Q] of D (W 64 x 128 K-major and
-                                              // a copy of the chunk's Q), then the low part
-                                              // of E^T
-constexpr uint32_t SM_ST = SM_W + 32768;      // S^T 128 x 128 K-major; fp32 T during the solve
-constexpr uint32_t SM_ET = SM_ST + 32768;     // E^T (high) 128 x 64
-constexpr uint32_t SM_ET2 = SM_ET + 16384;    // E^T diag(delta) (high); fp32 A during the solve
-                                              // SM_ET..SM_ET2 + 16 KB: the output tile at the end
-constexpr uint32_t SM_P = SM_ET2 + 16384;     // P (high part) 64 x 64 K-major
-constexpr uint32_t SM_PLO = SM_P + 8192;      // P (low part)
-// The low part of E^T diag(delta) goes to the current stage's V tile, which is free from the
-// completion of the U/W products until the stage is reloaded after the state update.
-constexpr uint32_t SM_ETLO = SM_W, SM_OUT = SM_ET;
-constexpr uint32_t SM_SMALL = SM_PLO + 8192;  // per-token vectors and solve scratch
-constexpr uint32_t SM_A = SM_ET2;   // fp32 A during the solve
-constexpr uint32_t SM_TB = SM_W;    // T diag(beta), T diag(beta G) until the U/W products
+// Beyond the two stages (lifetimes within the iteration of chunk c, steps as above):
+constexpr uint32_t SM_ST = 2 * kStageBytes;   // 32 KB: S^T bf16 128 x 128 K-major (steps 1 ->
+                                              // D(c)); then, from step 5, the next chunk's fp32
+                                              // T (16 KB, swizzled) and T diag beta | T diag
+                                              // beta G (16 KB, until U/W(c+1)); the output
+                                              // tile over T at step 6
+constexpr uint32_t SM_T = SM_ST, SM_TB = SM_ST + 16384, SM_OUT = SM_ST;
+constexpr uint32_t SM_W = SM_ST + 32768;      // W 64 x 128 K-major (step 2 -> D(c)), then E^T
+                                              // high 128 x 64 (step 4 -> E^T P^T)
+constexpr uint32_t SM_ELO = SM_W + 16384;     // E^T low
+constexpr uint32_t SM_ET2 = SM_ELO + 16384;   // E^T diag(delta) high (its low part goes to the
+                                              // stage's V tile, read by U/W(c) already)
+constexpr uint32_t SM_A = SM_ET2 + 16384;     // the next chunk's fp32 A (step 3 -> step 5)
+constexpr uint32_t SM_P = SM_A + 16384;       // the next chunk's P high | P low (step 6 ->
+                                              // its E^T P^T)
+constexpr uint32_t SM_SMALL = SM_P + 16384;   // gate vectors of two chunks, solve scratch
 constexpr uint32_t SM_TOTAL = SM_SMALL + 8192;
 static_assert(SM_TOTAL + 1024 <= 227 * 1024, "layout");
 constexpr uint32_t TM_S = 0, TM_D = 128, TM_X = 256, TM_U = 320, TM_W = 384, TM_PE = 448;
@@ -87,7 +90,6 @@ constexpr float kFactorSpan = 80.f;
 constexpr uint32_t ID_KK_N64 = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_MK_N64 = idesc_bf16(128, 64, true, false);
 constexpr uint32_t ID_KM_N128 = idesc_bf16(128, 128, false, true);
-constexpr uint32_t ID_KK_N128 = idesc_bf16(128, 128, false, false);
 
 struct TcArgs {
     const float *log_alpha;
@@ -114,9 +116,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     // mbarriers: TMA stages; per MMA group its completion (committed by the MMA warp) and,
     // for the groups whose operands the compute warps write, "operands ready" (full_*,
     // arrived by thread 0 after the compute warps' barrier).  Each completes once per chunk.
-    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_s, full_uw, full_d, full_s;
+    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_q, bar_s, bar_pe;
+    __shared__ uint64_t full_x, full_uw, full_d, full_s;
     __shared__ uint32_t tmem_base_s;
-    __shared__ int abort_s, factored_s;
+    __shared__ int abort_s, factored_s[2];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
@@ -149,31 +152,22 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
     }
     const int h = bh % a.H, b = bh / a.H;
+    const int n_it = c_end - c_begin;            // this CTA's chunks, indexed 0 .. n_it - 1
     constexpr int kTmaThread = 224;              // lane 0 of warp 7 issues the TMA loads
     constexpr int kGateWarp = 1;                 // warp 1 scans the gates
-    float *sG = reinterpret_cast<float *>(sm + SM_SMALL);   // g_r (cumulative log decay)
-    float *sGam = sG + 64;     // exp(g_r)
-    float *sDel = sG + 128;    // exp(g_63 - g_r)
-    float *sBeta = sG + 192;   // beta_r
-    float *sE = sG + 256;      // exp(g_r - g_31)
-    float *sF = sG + 320;      // exp(g_31 - g_r)
-    float *sM = sG + 384;      // 1024 floats of solve scratch
+    // gate vectors of two chunks (chunk `it` in set it % 2): g_r, exp(g_r), exp(g_63 - g_r),
+    // beta_r, and the factors exp(g_r - g_31), exp(g_31 - g_r)
+    float *sVec = reinterpret_cast<float *>(sm + SM_SMALL);   // [2][6][64]
+    auto vec = [&](int it, int k) { return sVec + (it & 1) * 384 + 64 * k; };
+    float *sM = sVec + 768;    // 1024 floats of solve scratch
     // raw gate words of two chunks: [slot][beta word | log alpha][64 tokens]
-    uint32_t *sGate = reinterpret_cast<uint32_t *>(sG + 1408);
-    float *sGamOut = sG + 1664;   // exp(g_r) of the chunk whose outputs are pending
+    uint32_t *sGate = reinterpret_cast<uint32_t *>(sVec + 1792);
     constexpr int kOutBoxes = sizeof(Tout) == 2 ? 2 : 4;   // 128-byte rows per output box
-    constexpr bool kWideOut = sizeof(Tout) == 4;           // fp32 tile covers SM_ET and SM_ET2
 
     if (tid == 0) {
-        mbar_init(&bar_tma[0], 1);
-        mbar_init(&bar_tma[1], 1);
-        mbar_init(&bar_x, 1);
-        mbar_init(&bar_uw, 1);
-        mbar_init(&bar_d, 1);
-        mbar_init(&bar_s, 1);
-        mbar_init(&full_uw, 1);
-        mbar_init(&full_d, 1);
-        mbar_init(&full_s, 1);
+        uint64_t *bars[] = {&bar_tma[0], &bar_tma[1], &bar_x, &bar_uw, &bar_d, &bar_q, &bar_s,
+                            &bar_pe, &full_x, &full_uw, &full_d, &full_s};
+        for (uint64_t *bb : bars) mbar_init(bb, 1);
         abort_s = 0;
         fence_mbar_init();
     }
@@ -184,14 +178,286 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tm = tmem_base_s + ((uint32_t)(32 * quarter) << 16);   // + this warp's lanes
+    const uint32_t tmb = tmem_base_s;
+    const uint32_t tm = tmb + ((uint32_t)(32 * quarter) << 16);   // + this warp's lanes
     // operand descriptors of the shared-memory base: K-major, and MN-major with the two
     // 64-wide atoms 8192 or 16384 bytes apart
     const uint64_t dK0 = smem_desc_sw128(smem_u32(sm), 16, 1024);
     const uint64_t dM8 = smem_desc_sw128(smem_u32(sm), 8192, 1024), dM16 = smem_desc_sw128(smem_u32(sm), 16384, 1024);
+    auto stage = [&](int it) { return sm + (it & 1) * kStageBytes; };
+    auto fail = [&]() {
+        abort_s = 1;
+        atomicExch(a.status, kErrTimeout);
+    };
+    auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
+        if (!wait_cycles(bar, parity)) fail();
+        tc_fence_after();
+    };
 
+    auto issue_tma = [&](int it) {   // chunk `it`'s q, k, v tiles into stage it % 2
+        const int s = it & 1;
+        unsigned char *st = stage(it);
+        mbar_arrive_expect_tx(&bar_tma[s], kStageBytes);
+        const int t0 = (c_begin + it) * 64;
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_4d(st + kb * 16384, &tq, &bar_tma[s], 64 * kb, h, t0, b);
+            tma_load_4d(st + kb * 16384 + OFF_K0, &tk, &bar_tma[s], 64 * kb, h, t0, b);
+            tma_load_4d(st + OFF_V0 + kb * 8192, &tv, &bar_tma[s], 64 * kb, h, t0, b);
+        }
+    };
+    // beta (the aligned 32-bit word holding it) and log alpha of chunk `it`, two tokens per
+    // lane of the gate warp, copied asynchronously two chunks ahead; one commit group per
+    // chunk (empty past the end), so that waiting for all but the newest group finds the
+    // chunk about to be scanned complete
+    const size_t ntok = (size_t)(gridDim.x / (a.role == 0 ? 1 : (a.role == 1 ? 2 * a.nseg : a.nseg))) * a.T;
+    auto issue_gate = [&](int it) {
+        if (it < n_it) {
+            uint32_t *dst = sGate + (it & 1) * 128;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = 2 * lane + e, t = (c_begin + it) * 64 + r;
+                const bool valid = t < a.T;
+                const size_t tok = valid ? ((size_t)b * a.T + t) * a.H + h : 0;
+                if (valid && tok + 1 == ntok && ((2 * tok) & 3) == 0) {
+                    // the 32-bit word would run past the end of beta: load this value alone
+                    dst[r] = (uint32_t)__bfloat16_as_ushort(a.beta[tok]);
+                } else {
+                    cp_async4(dst + r, reinterpret_cast<const char *>(a.beta) + ((2 * tok) & ~(size_t)3),
+                              valid ? 4 : 0);
+                }
+                cp_async4(dst + 64 + r, GATE == 1 ? (const void *)(a.log_alpha + tok) : (const void *)a.beta,
+                          (GATE == 1 && valid) ? 4 : 0);
+            }
+        }
+        cp_async_commit();
+    };
+    // (gate warp) chunk `it`'s cumulative log decay and factors into set it % 2; its raw
+    // gate slot then takes chunk it + 2
+    auto scan_gates = [&](int it) {
+        cp_async_wait_group1();
+        __syncwarp();
+        const uint32_t *gw = sGate + (it & 1) * 128;
+        const int t0 = (c_begin + it) * 64;
+        float l[2], bt[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 2 * lane + e, t = t0 + r;
+            const size_t tok = t < a.T ? ((size_t)b * a.T + t) * a.H + h : 0;
+            const uint32_t wd = gw[r];
+            const uint16_t hb = (uint16_t)(((2 * tok) & 2) ? (wd >> 16) : (wd & 0xffffu));
+            bt[e] = __bfloat162float(__ushort_as_bfloat16(hb));
+            l[e] = __uint_as_float(gw[64 + r]);
+        }
+        __syncwarp();
+        issue_gate(it + 2);
+        float p = l[0] + l[1];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, p, o);
+            if (lane >= o) p += y;
+        }
+        const float g1 = p, g0 = p - l[1];                     // g_{2l}, g_{2l+1}
+        const float glast = __shfl_sync(0xffffffffu, g1, 31);  // g_63
+        const float gmid = __shfl_sync(0xffffffffu, g1, 15);   // g_31
+        const float gfirst = __shfl_sync(0xffffffffu, g0, 0);  // g_0
+        const int r = 2 * lane;
+        float *sG = vec(it, 0), *sGam = vec(it, 1), *sDel = vec(it, 2), *sBeta = vec(it, 3),
+              *sE = vec(it, 4), *sF = vec(it, 5);
+        sG[r] = g0; sG[r + 1] = g1;
+        sBeta[r] = bt[0]; sBeta[r + 1] = bt[1];
+        sGam[r] = __expf(g0); sGam[r + 1] = __expf(g1);
+        sDel[r] = __expf(glast - g0); sDel[r + 1] = __expf(glast - g1);
+        const bool fac = gfirst - glast < kFactorSpan;
+        if (fac) {
+            sE[r] = __expf(g0 - gmid); sE[r + 1] = __expf(g1 - gmid);
+            sF[r] = __expf(gmid - g0); sF[r + 1] = __expf(gmid - g1);
+        }
+        if (lane == 0) factored_s[it & 1] = fac;
+    };
+    // (MMA warp) wait for chunk `it`'s tiles, then X = [Q; K] K^T into TM_X
+    auto issue_x = [&](int it) {
+        if (!wait_cycles(&bar_tma[it & 1], (it >> 1) & 1)) fail();
+        unsigned char *st = stage(it);
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_bf16(tmb + TM_X, desc_add(dK0, (uint32_t)((st + o) - sm)),
+                     desc_add(dK0, (uint32_t)((st + OFF_K0 + o) - sm)), ID_KK_N64, ks > 0);
+        }
+        mma_commit(&bar_x);
+    };
+    // (compute warps) rows of X for chunk `it` (whose X is in TMEM, gate set it % 2): the
+    // A rows (64..127, fp32, at SM_A; warps of lane quarters 2 and 3) or the P rows (0..63,
+    // bf16 high/low at SM_P; quarters 0 and 1)
+    auto build_pa = [&](int it, bool rows_a) {
+        if ((quarter >= 2) != rows_a) return;
+        float x[32];
+        tmem_ld32(tm + TM_X + 32 * half, x);
+        tmem_wait_ld();
+        const int c0 = 32 * half;
+        const int r = quarter < 2 ? row : row - 64;
+        const float *sG = vec(it, 0), *sBeta = vec(it, 3), *sE = vec(it, 4), *sF = vec(it, 5);
+        float dec[32];   // exp(g_r - g_s), s = c0 + u
+        if (factored_s[it & 1]) {
+            const float er = sE[r];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 f4 = *reinterpret_cast<const float4 *>(sF + c0 + 4 * q);
+                dec[4 * q] = er * f4.x; dec[4 * q + 1] = er * f4.y;
+                dec[4 * q + 2] = er * f4.z; dec[4 * q + 3] = er * f4.w;
+            }
+        } else {
+            const float gr = sG[r];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) dec[u] = __expf(fminf(gr - sG[c0 + u], 0.f));
+        }
+        if (!rows_a) {
+            uint32_t pk[16], pl[16];
+#pragma unroll
+            for (int u = 0; u < 32; u += 2) {
+                const int s0 = c0 + u;
+                const float p0 = s0 <= r ? dec[u] * x[u] : 0.f;
+                const float p1 = s0 + 1 <= r ? dec[u + 1] * x[u + 1] : 0.f;
+                pack_hi_lo(p0, p1, pk[u >> 1], pl[u >> 1]);
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const uint32_t off = sw128_off(r, c0 + 8 * q4);
+                *reinterpret_cast<uint4 *>(sm + SM_P + off) =
+                    make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                *reinterpret_cast<uint4 *>(sm + SM_P + 8192 + off) =
+                    make_uint4(pl[4 * q4], pl[4 * q4 + 1], pl[4 * q4 + 2], pl[4 * q4 + 3]);
+            }
+        } else {
+            const float br = sBeta[r];
+            float *sA = reinterpret_cast<float *>(sm + SM_A);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                float4 v4;
+                const int s0 = c0 + 4 * q4;
+                v4.x = s0 < r ? br * dec[4 * q4] * x[4 * q4] : 0.f;
+                v4.y = s0 + 1 < r ? br * dec[4 * q4 + 1] * x[4 * q4 + 1] : 0.f;
+                v4.z = s0 + 2 < r ? br * dec[4 * q4 + 2] * x[4 * q4 + 2] : 0.f;
+                v4.w = s0 + 3 < r ? br * dec[4 * q4 + 3] * x[4 * q4 + 3] : 0.f;
+                *reinterpret_cast<float4 *>(sA + a_index(r, s0)) = v4;
+            }
+        }
+    };
+    // (compute warps) T = (I + A)^-1 of chunk `it` (fp32, swizzled, over the S^T operand's
+    // first half) with T diag(beta) and T diag(beta G) in bf16 at SM_TB
+    auto solve = [&](int it) {
+        solve_unit_lower64<true, true>(reinterpret_cast<const float *>(sm + SM_A),
+                                       reinterpret_cast<float *>(sm + SM_T), sM, sm + SM_TB,
+                                       vec(it, 3), vec(it, 1), tid);
+    };
+
+    // prologue loads: stages 0 and 1, raw gates of chunks 0 and 1
+    if (tid == kTmaThread) {
+        if (n_it > 0) issue_tma(0);
+        if (n_it > 1) issue_tma(1);
+    }
+    if (warp == kGateWarp) {
+        issue_gate(0);
+        issue_gate(1);
+    }
+
+    // ---------------- MMA warp: issues every tcgen05.mma group, each once its operands are
+    // ready, in the order the compute warps produce them, and commits it to the barrier
+    // they wait on.  Chunk c's D, state update and E^T P^T; then chunk c + 1's U/W; then
+    // chunk c + 2's X.
+    if (warp == kMmaWarp) {
+        if (lane == 0 && n_it > 0) {
+            uint64_t *last = &bar_x;   // most recent commit (drained on abort)
+            uint32_t last_par = 0;
+            auto issue_uw = [&](int it) {   // U^T = V^T (T diag beta)^T, W^T = K^T (T diag(beta G))^T
+                unsigned char *st = stage(it);
+                if (!zero_u)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmb + TM_U, desc_add(dM8, (uint32_t)((st + OFF_V0 + ks * 2048) - sm)),
+                             desc_add(dK0, SM_TB + ks * 32), ID_MK_N64, ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmb + TM_W, desc_add(dM16, (uint32_t)((st + OFF_K0 + ks * 2048) - sm)),
+                             desc_add(dK0, SM_TB + 8192 + ks * 32), ID_MK_N64, ks > 0);
+                mma_commit(&bar_uw);
+            };
+            issue_x(0);
+            if (!wait_cycles(&full_uw, 0)) fail();
+            tc_fence_after();
+            issue_uw(0);
+            last = &bar_uw;
+            if (n_it > 1) {
+                if (!wait_cycles(&full_x, 0)) fail();
+                tc_fence_after();
+                issue_x(1);
+                last = &bar_x; last_par = 1;
+            }
+            for (int it = 0; it < n_it && !abort_s; ++it) {
+                const uint32_t par = it & 1;
+                unsigned char *st = stage(it);
+                // D = S^T [W; Q]^T: (W S)^T first (the E^T build waits for it), then (Q S)^T
+                if (!wait_cycles(&full_d, par)) { fail(); break; }
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_bf16(tmb + TM_D, desc_add(dK0, SM_ST + o),
+                             desc_add(dK0, SM_W + (ks >> 2) * 8192 + (ks & 3) * 32), ID_KK_N64, ks > 0);
+                }
+                mma_commit(&bar_d);
+                if (outputs)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16(tmb + TM_D + 64, desc_add(dK0, SM_ST + o),
+                                 desc_add(dK0, (uint32_t)((st + o) - sm)), ID_KK_N64, ks > 0);
+                    }
+                mma_commit(&bar_q);
+                last = &bar_q; last_par = par;
+                // S^T += (E^T diag delta) K, then PE = E^T P^T  (high/low pairs)
+                if (!wait_cycles(&full_s, par)) { fail(); break; }
+                tc_fence_after();
+                unsigned char *e2[2] = {sm + SM_ET2, st + OFF_V0};
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tmb + TM_S, desc_add(dK0, (uint32_t)((e2[part] + ks * 32) - sm)),
+                                 desc_add(dM16, (uint32_t)((st + OFF_K0 + ks * 2048) - sm)), ID_KM_N128, 1);
+                mma_commit(&bar_s);
+                const uint32_t ea[3] = {SM_W, SM_W, SM_ELO}, pb[3] = {SM_P, SM_P + 8192, SM_P};
+                if (outputs)
+#pragma unroll
+                    for (int part = 0; part < 3; ++part)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_bf16(tmb + TM_PE, desc_add(dK0, ea[part] + ks * 32),
+                                     desc_add(dK0, pb[part] + ks * 32), ID_KK_N64, (part | ks) != 0);
+                mma_commit(&bar_pe);
+                last = &bar_pe; last_par = par;
+                // the next chunk's U/W, then the chunk after's X
+                if (it + 1 < n_it) {
+                    if (!wait_cycles(&full_uw, (it + 1) & 1)) { fail(); break; }
+                    tc_fence_after();
+                    issue_uw(it + 1);
+                    last = &bar_uw; last_par = (it + 1) & 1;
+                }
+                if (it + 2 < n_it) {
+                    if (!wait_cycles(&full_x, (it + 1) & 1)) { fail(); break; }
+                    tc_fence_after();
+                    issue_x(it + 2);
+                    last = &bar_x; last_par = it & 1;
+                }
+            }
+            if (abort_s) wait_cycles(last, last_par);   // drain this warp's MMAs (bounded)
+        }
+        __syncwarp();
+    } else {
+    // ---------------- compute warps
     // S^T[j][i] = S_0[i][j]: this thread owns j = row and i in [64 half, 64 half + 64).
-    if (warp < kMmaWarp) {
+    {
         float v[32];
         for (int part = 0; part < 2; ++part) {
             const int i0 = 64 * half + 32 * part;
@@ -203,315 +469,41 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
         tmem_wait_st();
     }
-
-    // `it` counts this CTA's chunks (stage, barrier phases); `c` is the global chunk index
-    auto issue_tma = [&](int it, int c) {
-        const int s = it & 1;
-        unsigned char *st = sm + s * kStageBytes;
-        mbar_arrive_expect_tx(&bar_tma[s], kStageBytes);
-        const int t0 = c * 64;
-        for (int kb = 0; kb < 2; ++kb) {
-            tma_load_4d(st + kb * 16384, &tq, &bar_tma[s], 64 * kb, h, t0, b);
-            tma_load_4d(st + kb * 16384 + OFF_K0, &tk, &bar_tma[s], 64 * kb, h, t0, b);
-            tma_load_4d(st + OFF_V0 + kb * 8192, &tv, &bar_tma[s], 64 * kb, h, t0, b);
-        }
-    };
-    // beta (the aligned 32-bit word holding it) and log alpha of chunk c, two tokens per
-    // lane of warp 1 (warp 0 issues the MMAs), copied asynchronously one chunk ahead
-    const size_t ntok = (size_t)(gridDim.x / (a.role == 0 ? 1 : (a.role == 1 ? 2 * a.nseg : a.nseg))) * a.T;
-    auto issue_gate = [&](int it, int c) {
-        uint32_t *dst = sGate + (it & 1) * 128;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int r = 2 * lane + e, t = c * 64 + r;
-            const bool valid = t < a.T;
-            const size_t tok = valid ? ((size_t)b * a.T + t) * a.H + h : 0;
-            if (valid && tok + 1 == ntok && ((2 * tok) & 3) == 0) {
-                // the 32-bit word would run past the end of beta: load this value alone
-                dst[r] = (uint32_t)__bfloat16_as_ushort(a.beta[tok]);
-            } else {
-                cp_async4(dst + r, reinterpret_cast<const char *>(a.beta) + ((2 * tok) & ~(size_t)3),
-                          valid ? 4 : 0);
-            }
-            cp_async4(dst + 64 + r, GATE == 1 ? (const void *)(a.log_alpha + tok) : (const void *)a.beta,
-                      (GATE == 1 && valid) ? 4 : 0);
-        }
-        cp_async_commit();
-    };
-    const int n_it = c_end - c_begin;
-    if (tid == kTmaThread && n_it > 0) issue_tma(0, c_begin);
-    if (warp == kGateWarp && n_it > 0) issue_gate(0, c_begin);
-
-    bool out_pending = false;       // chunk whose outputs wait in TMEM for the write-out
-    bool store_outstanding = false; // a TMA store may still be reading SM_OUT
-    int last_tma_it = 0;            // iteration of the most recent TMA load (TMA thread)
-    bool s_outstanding = false;     // MMA group S (state update, E^T P^T) committed, not waited
-    int cur_t0 = 0;                 // t0 of the chunk whose outputs are pending
-    auto fail = [&]() {
-        abort_s = 1;
-        atomicExch(a.status, kErrTimeout);
-    };
-    auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
-        if (!wait_cycles(bar, parity)) fail();
-        tc_fence_after();
-    };
-    // (MMA warp) wait for chunk c's tiles, then X = [Q; K] K^T into TM_X
-    auto issue_x = [&](int it) {
-        if (!wait_cycles(&bar_tma[it & 1], (it >> 1) & 1)) fail();
-        unsigned char *st = sm + (it & 1) * kStageBytes;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_bf16(tmem_base_s + TM_X, desc_add(dK0, (uint32_t)((st + o) - sm)),
-                     desc_add(dK0, (uint32_t)((st + OFF_K0 + o) - sm)), ID_KK_N64, ks > 0);
-        }
-        mma_commit(&bar_x);
-    };
-
-    // Output of the chunk at t0: o = G_r (Q S)^T + E^T P^T, staged row-major at SM_OUT in
-    // 128-byte swizzled boxes and written by TMA (rows past T are skipped).  Needs group S.
-    auto write_out = [&](int t0) {
-        float o[32], pe[32];
-        tmem_ld32(tm + TM_D + 64 + 32 * half, o);
-        tmem_ld32(tm + TM_PE + 32 * half, pe);
-        tmem_wait_ld();
-#pragma unroll
-        for (int u = 0; u < 32; ++u) o[u] = fmaf(sGamOut[32 * half + u], o[u], pe[u]);
-        const int j = row;
-        if (sizeof(Tout) == 2) {
-            unsigned char *dst = sm + SM_OUT + (j >> 6) * 8192;
-#pragma unroll
-            for (int u = 0; u < 32; ++u)
-                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, j & 63)) =
-                    __float2bfloat16_rn(o[u]);
-        } else {
-            unsigned char *dst = sm + SM_OUT + (j >> 5) * 8192;
-            const int cj = j & 31;
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int r = 32 * half + u;
-                *reinterpret_cast<float *>(dst + r * 128 + ((((cj >> 2) ^ (r & 7)) & 7) << 4) +
-                                           ((cj & 3) << 2)) = o[u];
-            }
-        }
+    bool store_outstanding = false;   // thread 0: a TMA store may still be reading SM_OUT
+    if (n_it > 0) {
+        // prologue: chunk 0's gates, A and P, solve; chunk 1's gates
+        if (warp == kGateWarp) scan_gates(0);
+        named_sync(1, kThreads);
+        wait_bar(&bar_x, 0);
+        build_pa(0, true);
+        if (outputs) build_pa(0, false);
         fence_proxy_async();
         tc_fence_before();
         named_sync(1, kThreads);
-        if (tid == 0) {
-            constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
-#pragma unroll
-            for (int kb = 0; kb < kOutBoxes; ++kb)
-                tma_store_4d(&to, sm + SM_OUT + kb * 8192, cols * kb, h, t0, b);
-            bulk_commit();
-            store_outstanding = true;
-            if (kWideOut) {   // the fp32 tile also covers SM_A, written next by P/A
-                bulk_wait_read_all();
-                store_outstanding = false;
-            }
-        }
-        if (kWideOut) named_sync(1, kThreads);
-    };
-
-    // ---------------- MMA warp: issues every tcgen05.mma group in chunk order, each once its
-    // operands are ready, and commits it to the barrier the compute warps wait on.
-    if (warp == kMmaWarp) {
-        if (lane == 0 && n_it > 0) {
-            uint64_t *last = &bar_x;   // most recent commit (drained on abort)
-            uint32_t last_par = 0;
-            issue_x(0);
-            for (int it = 0; it < n_it && !abort_s; ++it) {
-                const uint32_t par = it & 1;
-                unsigned char *st = sm + (it & 1) * kStageBytes;
-                // U^T = V^T (T diag beta)^T,  W^T = K^T (T diag(beta G))^T
-                if (!wait_cycles(&full_uw, par)) { fail(); break; }
-                tc_fence_after();
-                if (!zero_u)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem_base_s + TM_U, desc_add(dM8, (uint32_t)((st + OFF_V0 + ks * 2048) - sm)),
-                             desc_add(dK0, (uint32_t)(SM_TB + ks * 32)), ID_MK_N64, ks > 0);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem_base_s + TM_W, desc_add(dM16, (uint32_t)((st + OFF_K0 + ks * 2048) - sm)),
-                             desc_add(dK0, (uint32_t)(SM_TB + 8192 + ks * 32)), ID_MK_N64, ks > 0);
-                mma_commit(&bar_uw);
-                last = &bar_uw; last_par = par;
-                // D = S^T [W; Q]^T in one N = 128 product: (W S)^T | (Q S)^T
-                if (!wait_cycles(&full_d, par)) { fail(); break; }
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_bf16(tmem_base_s + TM_D, desc_add(dK0, SM_ST + o), desc_add(dK0, SM_W + o),
-                             outputs ? ID_KK_N128 : ID_KK_N64, ks > 0);
-                }
-                mma_commit(&bar_d);
-                last = &bar_d; last_par = par;
-                // S^T += (E^T diag delta) K ;  PE = E^T P^T  (high/low pairs); then the next X
-                if (!wait_cycles(&full_s, par)) { fail(); break; }
-                tc_fence_after();
-                unsigned char *e2[2] = {sm + SM_ET2, st + OFF_V0};
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmem_base_s + TM_S, desc_add(dK0, (uint32_t)((e2[part] + ks * 32) - sm)),
-                                 desc_add(dM16, (uint32_t)((st + OFF_K0 + ks * 2048) - sm)), ID_KM_N128, 1);
-                const uint32_t ea[3] = {SM_ET, SM_ET, SM_ETLO}, pb[3] = {SM_P, SM_PLO, SM_P};
-                if (outputs)
-#pragma unroll
-                for (int part = 0; part < 3; ++part)
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmem_base_s + TM_PE, desc_add(dK0, ea[part] + ks * 32),
-                                 desc_add(dK0, pb[part] + ks * 32), ID_KK_N64, (part | ks) != 0);
-                mma_commit(&bar_s);
-                last = &bar_s; last_par = par;
-                if (it + 1 < n_it) {
-                    issue_x(it + 1);
-                    last = &bar_x; last_par = (it + 1) & 1;
-                }
-            }
-            if (abort_s) wait_cycles(last, last_par);   // drain this warp's MMAs (bounded)
-        }
-        __syncwarp();
-    } else {
+        if (tid == 0 && n_it > 1) mbar_arrive(&full_x);   // X(1) may overwrite TM_X
+        solve(0);
+        if (tid == 0) mbar_arrive(&full_uw);
+        if (warp == kGateWarp && n_it > 1) scan_gates(1);
+    }
 
     for (int it = 0; it < n_it; ++it) {
-        const int c = c_begin + it;
-        const int s = it & 1;
-        const uint32_t par = it & 1;              // parity of this chunk's MMA barriers
-        unsigned char *st = sm + s * kStageBytes;
-        const int t0 = c * 64;
+        const uint32_t par = it & 1;
+        unsigned char *st = stage(it);
+        const int t0 = (c_begin + it) * 64;
+        const bool next = it + 1 < n_it;
 
-        // ---- 1. X = [Q; K] K^T of this chunk: issued by the MMA warp (the first chunk's at
-        //         once, later ones right after the previous chunk's state update)
-        // ---- 2. cumulative log decay of this chunk (gate warp; its gates arrived by cp.async)
-        if (warp == kGateWarp) {
-            cp_async_wait_all();
-            __syncwarp();
-            const uint32_t *gw = sGate + s * 128;
-            float l[2], bt[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int r = 2 * lane + e, t = t0 + r;
-                const size_t tok = t < a.T ? ((size_t)b * a.T + t) * a.H + h : 0;
-                const uint32_t wd = gw[r];
-                const uint16_t hb = (uint16_t)(((2 * tok) & 2) ? (wd >> 16) : (wd & 0xffffu));
-                bt[e] = __bfloat162float(__ushort_as_bfloat16(hb));
-                l[e] = __uint_as_float(gw[64 + r]);
-            }
-            __syncwarp();
-            if (it + 1 < n_it) issue_gate(it + 1, c + 1);
-            float p = l[0] + l[1];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, p, o);
-                if (lane >= o) p += y;
-            }
-            const float g1 = p, g0 = p - l[1];                     // g_{2l}, g_{2l+1}
-            const float glast = __shfl_sync(0xffffffffu, g1, 31);  // g_63
-            const float gmid = __shfl_sync(0xffffffffu, g1, 15);   // g_31
-            const float gfirst = __shfl_sync(0xffffffffu, g0, 0);  // g_0
-            const int r = 2 * lane;
-            sG[r] = g0; sG[r + 1] = g1;
-            sBeta[r] = bt[0]; sBeta[r + 1] = bt[1];
-            sGam[r] = __expf(g0); sGam[r + 1] = __expf(g1);
-            sDel[r] = __expf(glast - g0); sDel[r + 1] = __expf(glast - g1);
-            const bool fac = gfirst - glast < kFactorSpan;
-            if (fac) {
-                sE[r] = __expf(g0 - gmid); sE[r + 1] = __expf(g1 - gmid);
-                sF[r] = __expf(gmid - g0); sF[r + 1] = __expf(gmid - g1);
-            }
-            if (lane == 0) factored_s = fac;
+        // ---- 1. S^T to bf16 (SM_ST) and S^T <- gamma S^T in TMEM: after the previous state
+        //         update, after this chunk's U/W products have read T diag beta (SM_TB), and
+        //         after the previous output tile's store has read SM_OUT
+        if (it >= 1) wait_bar(&bar_s, par ^ 1);
+        wait_bar(&bar_uw, par);
+        if (tid == 0 && store_outstanding) {
+            bulk_wait_read_all();
+            store_outstanding = false;
         }
-        // ---- 3. previous chunk: wait for its state update, write its outputs; then the
-        //         stage it used is free for the next chunk's tiles
-        if (s_outstanding) {
-            wait_bar(&bar_s, par ^ 1);
-            s_outstanding = false;
-        }
-        named_sync(1, kThreads);    // gate vectors published; previous chunk's MMAs done
-        if (abort_s) break;
-        if (out_pending && outputs) write_out(cur_t0);
-        if (tid == kTmaThread && it + 1 < n_it) {
-            issue_tma(it + 1, c + 1);
-            last_tma_it = it + 1;
-        }
-        // keep this chunk's exp(g_r) for its deferred write-out (write_out above ended with
-        // a barrier, so no thread still reads the previous values)
-        if (tid < 64) sGamOut[tid] = sGam[tid];
-
-        // ---- 4. P (rows 0..63 of X, bf16 high/low) and A (rows 64..127 of X, fp32)
-        wait_bar(&bar_x, par);
-        {
-            float x[32];
-            tmem_ld32(tm + TM_X + 32 * half, x);
-            tmem_wait_ld();
-            const int c0 = 32 * half;
-            const bool fac = factored_s;
-            const int r = quarter < 2 ? row : row - 64;
-            float dec[32];   // exp(g_r - g_s), s = c0 + u
-            if (fac) {
-                const float er = sE[r];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 f4 = *reinterpret_cast<const float4 *>(sF + c0 + 4 * q);
-                    dec[4 * q] = er * f4.x; dec[4 * q + 1] = er * f4.y;
-                    dec[4 * q + 2] = er * f4.z; dec[4 * q + 3] = er * f4.w;
-                }
-            } else {
-                const float gr = sG[r];
-#pragma unroll
-                for (int u = 0; u < 32; ++u) dec[u] = __expf(fminf(gr - sG[c0 + u], 0.f));
-            }
-            if (quarter < 2) {
-                uint32_t pk[16], pl[16];
-#pragma unroll
-                for (int u = 0; u < 32; u += 2) {
-                    const int s0 = c0 + u;
-                    const float p0 = s0 <= r ? dec[u] * x[u] : 0.f;
-                    const float p1 = s0 + 1 <= r ? dec[u + 1] * x[u + 1] : 0.f;
-                    pack_hi_lo(p0, p1, pk[u >> 1], pl[u >> 1]);
-                }
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const uint32_t off = sw128_off(r, c0 + 8 * q4);
-                    *reinterpret_cast<uint4 *>(sm + SM_P + off) =
-                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-                    *reinterpret_cast<uint4 *>(sm + SM_PLO + off) =
-                        make_uint4(pl[4 * q4], pl[4 * q4 + 1], pl[4 * q4 + 2], pl[4 * q4 + 3]);
-                }
-            } else {
-                const float br = sBeta[r];
-                float *sA = reinterpret_cast<float *>(sm + SM_A);
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    float4 v4;
-                    const int s0 = c0 + 4 * q4;
-                    v4.x = s0 < r ? br * dec[4 * q4] * x[4 * q4] : 0.f;
-                    v4.y = s0 + 1 < r ? br * dec[4 * q4 + 1] * x[4 * q4 + 1] : 0.f;
-                    v4.z = s0 + 2 < r ? br * dec[4 * q4 + 2] * x[4 * q4 + 2] : 0.f;
-                    v4.w = s0 + 3 < r ? br * dec[4 * q4 + 3] * x[4 * q4 + 3] : 0.f;
-                    *reinterpret_cast<float4 *>(sA + a_index(r, s0)) = v4;
-                }
-            }
-        }
-        fence_proxy_async();
-        tc_fence_before();
         named_sync(1, kThreads);
-
-        // ---- 5-6. T = (I + A)^-1 (fp32, [64][kTs] at SM_ST), with T diag(beta) and
-        //           T diag(beta G) in bf16 at SM_TB
-        solve_unit_lower64(reinterpret_cast<const float *>(sm + SM_A),
-                           reinterpret_cast<float *>(sm + SM_ST), sM, sm + SM_TB, sBeta, sGam, tid);
-
-        // ---- 7. U^T = V^T (T diag beta)^T,  W^T = K^T (T diag(beta G))^T (MMA warp)
-        if (tid == 0) mbar_arrive(&full_uw);
-        // ---- 8. meanwhile: S^T to bf16 (MMA operand at SM_ST); S^T <- gamma S^T in TMEM
         {
-            const float gamma = sGam[63];
+            const float gamma = vec(it, 1)[63];
             float v[32];
             unsigned char *dst = sm + SM_ST + half * 16384;
             for (int part = 0; part < 2; ++part) {
@@ -531,50 +523,34 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             }
             tmem_wait_st();
         }
-        // ---- 9. W from W^T (lane i = key channel, columns = tokens r) into the B operand
-        //         [W; Q] of D, and the chunk's Q tiles copied beside it
-        wait_bar(&bar_uw, par);
+        // ---- 2. W from W^T (lane i = key channel, columns = tokens r) into SM_W
         {
             float w[32];
             tmem_ld32(tm + TM_W + 32 * half, w);
             tmem_wait_ld();
             const int i = row, kb = i >> 6, ci = i & 63;
-            unsigned char *dst = sm + SM_W + kb * 16384;
+            unsigned char *dst = sm + SM_W + kb * 8192;
 #pragma unroll
             for (int u = 0; u < 32; ++u)
                 *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, ci)) =
                     __float2bfloat16_rn(w[u]);
-            if (outputs) {   // 16 KB of swizzled tiles: the copy keeps the pattern (1 KB aligned)
-                // the tiles arrived by TMA (seen so far by the MMA warp only); this stage's
-                // next load is issued after the next chunk's step 3
-                if (!wait_cycles(&bar_tma[it & 1], (it >> 1) & 1)) fail();
-                const uint4 *qs = reinterpret_cast<const uint4 *>(st);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int e = tid + 256 * k, kbq = e >> 9, off = e & 511;   // 512 x 16 B per kb
-                    reinterpret_cast<uint4 *>(sm + SM_W + kbq * 16384 + 8192)[off] = qs[kbq * 1024 + off];
-                }
-            }
         }
         fence_proxy_async();
         tc_fence_before();
         named_sync(1, kThreads);
         if (abort_s) break;
+        if (tid == 0) mbar_arrive(&full_d);   // D = S^T [W; Q]^T (MMA warp)
 
-        // ---- 10. D = S^T [W; Q]^T  (MMA warp)
-        if (tid == 0) {
-            mbar_arrive(&full_d);
-            if (store_outstanding) {   // the previous output tile must have left SM_OUT
-                bulk_wait_read_all();  // before E^T is written there
-                store_outstanding = false;
-            }
+        // ---- 3. A of the next chunk (its X arrived meanwhile)
+        if (next) {
+            wait_bar(&bar_x, (it + 1) & 1);
+            build_pa(it + 1, true);
         }
-        named_sync(1, kThreads);
-        wait_bar(&bar_d, par);
 
-        // ---- 11. E^T = U^T - (W S)^T, and E^T diag(delta)  (bf16 high/low pairs); the (Q S)^T
-        //          half is read by the deferred write-out
+        // ---- 4. E^T = U^T - (W S)^T, and E^T diag(delta)  (bf16 high/low pairs)
+        wait_bar(&bar_d, par);
         {
+            const float *sDel = vec(it, 2);
             float ws[32], uu[32];
             tmem_ld32(tm + TM_D + 32 * half, ws);
             tmem_ld32(tm + TM_U + 32 * half, uu);
@@ -598,46 +574,91 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     pack_hi_lo(e[2 * u], e[2 * u + 1], eh[u], el[u]);
                     pack_hi_lo(ed[2 * u], ed[2 * u + 1], dh[u], dlo[u]);
                 }
-                *reinterpret_cast<uint4 *>(sm + SM_ET + off) = make_uint4(eh[0], eh[1], eh[2], eh[3]);
-                *reinterpret_cast<uint4 *>(sm + SM_ETLO + off) = make_uint4(el[0], el[1], el[2], el[3]);
+                *reinterpret_cast<uint4 *>(sm + SM_W + off) = make_uint4(eh[0], eh[1], eh[2], eh[3]);
+                *reinterpret_cast<uint4 *>(sm + SM_ELO + off) = make_uint4(el[0], el[1], el[2], el[3]);
                 *reinterpret_cast<uint4 *>(sm + SM_ET2 + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
-                *reinterpret_cast<uint4 *>(st + OFF_V0 + off) =
-                    make_uint4(dlo[0], dlo[1], dlo[2], dlo[3]);
+                *reinterpret_cast<uint4 *>(st + OFF_V0 + off) = make_uint4(dlo[0], dlo[1], dlo[2], dlo[3]);
             }
         }
         fence_proxy_async();
         tc_fence_before();
         named_sync(1, kThreads);
+        if (tid == 0) mbar_arrive(&full_s);   // state update, E^T P^T (MMA warp)
 
-        // ---- 12. S^T += (E^T diag delta) K ;  PE = E^T P^T  (high/low pairs; MMA warp, which
-        //          then issues the next chunk's X); completes while the next chunk starts,
-        //          whose step 3 waits for it
-        if (tid == 0) mbar_arrive(&full_s);
-        s_outstanding = true;
-        out_pending = true;
-        cur_t0 = t0;
-    }
-
-    if (!abort_s && s_outstanding) {
-        wait_bar(&bar_s, (n_it - 1) & 1);
-        s_outstanding = false;
-        named_sync(1, kThreads);
-        if (!abort_s && out_pending && outputs) write_out(cur_t0);
-    }
-    if (abort_s) {
-        // Drain this CTA's own asynchronous work (bounded) before TMEM is freed; the MMA
-        // warp drains its own MMAs.
-        if (tid == kTmaThread)   // the last load may still be in flight (bounded wait)
-            wait_cycles(&bar_tma[last_tma_it & 1], (last_tma_it >> 1) & 1);
-    } else if (fin_ptr) {
-        float v[32];
-        for (int part = 0; part < 2; ++part) {
-            const int i0 = 64 * half + 32 * part;
-            tmem_ld32(tm + TM_S + i0, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int u = 0; u < 32; ++u) fin_ptr[(size_t)(i0 + u) * 128 + row] = v[u];
+        // ---- 5. the next chunk's solve; its T goes over S^T, which (Q S)^T must have read
+        if (next) {
+            wait_bar(&bar_q, par);
+            solve(it + 1);
+            if (tid == 0) mbar_arrive(&full_uw);   // the next chunk's U/W (MMA warp)
         }
+
+        // ---- 6. this chunk's output o = G_r (Q S)^T + E^T P^T, staged at SM_OUT and written by
+        //         TMA; the next chunk's P (E^T P^T has read SM_P); the stage takes chunk it + 2
+        wait_bar(&bar_pe, par);
+        if (outputs) {
+            float o[32], pe[32];
+            tmem_ld32(tm + TM_D + 64 + 32 * half, o);
+            tmem_ld32(tm + TM_PE + 32 * half, pe);
+            tmem_wait_ld();
+            const float *sGam = vec(it, 1);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) o[u] = fmaf(sGam[32 * half + u], o[u], pe[u]);
+            const int j = row;
+            if (sizeof(Tout) == 2) {
+                unsigned char *dst = sm + SM_OUT + (j >> 6) * 8192;
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, j & 63)) =
+                        __float2bfloat16_rn(o[u]);
+            } else {
+                // fp32: 32 KB, over S^T's second half too, which the next chunk's U/W products
+                // read as T diag beta: they must have completed
+                if (next) wait_bar(&bar_uw, (it + 1) & 1);
+                unsigned char *dst = sm + SM_OUT + (j >> 5) * 8192;
+                const int cj = j & 31;
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int r = 32 * half + u;
+                    *reinterpret_cast<float *>(dst + r * 128 + ((((cj >> 2) ^ (r & 7)) & 7) << 4) +
+                                               ((cj & 3) << 2)) = o[u];
+                }
+            }
+            if (next) build_pa(it + 1, false);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        named_sync(1, kThreads);
+        if (tid == 0) {
+            if (outputs) {
+                constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
+#pragma unroll
+                for (int kb = 0; kb < kOutBoxes; ++kb)
+                    tma_store_4d(&to, sm + SM_OUT + kb * 8192, cols * kb, h, t0, b);
+                bulk_commit();
+                store_outstanding = true;
+            }
+            if (it + 2 < n_it) mbar_arrive(&full_x);   // the chunk after next's X (MMA warp)
+        }
+        if (tid == kTmaThread && it + 2 < n_it) issue_tma(it + 2);
+        // ---- 7. gates of the chunk after next (into this chunk's set, now free)
+        if (warp == kGateWarp && it + 2 < n_it) scan_gates(it + 2);
+    }
+
+    if (!abort_s && n_it > 0) {
+        wait_bar(&bar_s, (n_it - 1) & 1);
+        if (fin_ptr) {
+            float v[32];
+            for (int part = 0; part < 2; ++part) {
+                const int i0 = 64 * half + 32 * part;
+                tmem_ld32(tm + TM_S + i0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 32; ++u) fin_ptr[(size_t)(i0 + u) * 128 + row] = v[u];
+            }
+        }
+    } else if (abort_s && tid == kTmaThread) {
+        // the stage loads this thread issued may still be in flight (bounded waits)
+        for (int i = 0; i < min(n_it, 2); ++i) wait_cycles(&bar_tma[i], 0);
     }
     if (warp == kGateWarp) cp_async_wait_all();
     if (tid == 0 && store_outstanding) bulk_wait_all();
@@ -645,7 +666,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem_base_s, 512);
+    if (warp == 0) tmem_dealloc(tmb, 512);
 }
 
 // Segment chaining (between the two segment passes): per chain, S_start(0) = S_0 and

@@ -73,14 +73,21 @@ __device__ __forceinline__ void warp_store16(const float (&acc)[2][4], float sig
     }
 }
 
-constexpr int kTs = 68;   // row stride (floats) of the fp32 T matrix: 16-byte aligned rows
+constexpr int kTs = 68;   // row stride (floats) of the padded fp32 T matrix: 16-byte aligned rows
+
+// Element (r, s) of the fp32 T matrix: padded rows of kTs floats (kSwizzledT false), or dense
+// rows of 64 with 16-byte groups XOR-swizzled by r % 16 (16 KB; pairs and quads stay whole).
+template <bool kSwizzledT>
+__device__ __forceinline__ int t_index(int r, int s) {
+    return kSwizzledT ? r * 64 + (s ^ ((r & 15) << 2)) : r * kTs + s;
+}
 
 // Element (r, s) of the fp32 A matrix: rows of 64, 16-byte groups XOR-swizzled by r % 16.
 __device__ __forceinline__ int a_index(int r, int s) {
     return r * 64 + ((((s >> 2) ^ (r & 15)) << 2) | (s & 3));
 }
 
-// T = (I + A)^-1 for a strictly lower-triangular 64 x 64 A (fp32), T stored [64][kTs].
+// T = (I + A)^-1 for a strictly lower-triangular 64 x 64 A (fp32), T stored as t_index says.
 //   1. the four diagonal 16 x 16 blocks by right-looking substitution, four threads per
 //      column (each owns four rows; the pivot row's value is broadcast by a shuffle);
 //   2. T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (two warps);
@@ -91,7 +98,7 @@ __device__ __forceinline__ int a_index(int r, int s) {
 // operands.  Products use TF32 mma.sync with fp32 accumulation.  M needs 1024 floats.
 // Called by 256 threads (the CTA's compute warps, which synchronise on named barrier 1);
 // starts after and ends with a barrier.
-template <bool kPair = true>
+template <bool kPair = true, bool kSwizzledT = false>
 __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, float *M,
                                                    unsigned char *TB, const float *beta,
                                                    const float *gam, int tid) {
@@ -99,7 +106,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
     // final element (r, s) of T: fp32 copy for the later levels, and the two bf16 MMA
     // operands T diag(beta) (at TB) and T diag(beta G) (at TB + 8192)
     auto fin = [&](int r, int s, float v) {
-        T[r * kTs + s] = v;
+        T[t_index<kSwizzledT>(r, s)] = v;
         const float vb = v * beta[s];
         const uint32_t off = sw128_off(r, s);
         *reinterpret_cast<__nv_bfloat16 *>(TB + off) = __float2bfloat16_rn(vb);
@@ -108,7 +115,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
     };
     // final elements (r, s) and (r, s + 1), s even: one 32-bit store per operand
     auto fin2 = [&](int r, int s, float v0, float v1) {
-        *reinterpret_cast<float2 *>(T + r * kTs + s) = make_float2(v0, v1);
+        *reinterpret_cast<float2 *>(T + t_index<kSwizzledT>(r, s)) = make_float2(v0, v1);
         const float b0 = v0 * beta[s], b1 = v1 * beta[s + 1];
         const uint32_t off = sw128_off(r, s);
         *reinterpret_cast<uint32_t *>(TB + off) = pack_bf16(b0, b1);
@@ -161,12 +168,12 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         float *Ms = M + 256 * warp;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         warp_mm16(acc, [&](int r, int k) { return a(16 * i + r, 16 * j + k); },
-                  [&](int k, int n) { return T[(16 * j + k) * kTs + 16 * j + n]; }, 1, g, t4);
+                  [&](int k, int n) { return T[t_index<kSwizzledT>(16 * j + k, 16 * j + n)]; }, 1, g, t4);
         warp_store16(acc, 1.f, [&](int r, int n, float v0, float v1) {
             *reinterpret_cast<float2 *>(Ms + r * 16 + n) = make_float2(v0, v1); }, g, t4);
         __syncwarp();
         float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_mm16(acc2, [&](int r, int k) { return T[(16 * i + r) * kTs + 16 * i + k]; },
+        warp_mm16(acc2, [&](int r, int k) { return T[t_index<kSwizzledT>(16 * i + r, 16 * i + k)]; },
                   [&](int k, int n) { return Ms[k * 16 + n]; }, 1, g, t4);
         warp_store16(acc2, -1.f, [&](int r, int n, float v0, float v1) {
             fin2(16 * i + r, 16 * j + n, v0, v1); }, g, t4);
@@ -176,7 +183,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         const int rb = 2 + (warp >> 1), cb = warp & 1;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         warp_mm16(acc, [&](int r, int k) { return a(16 * rb + r, 16 * cb + k); },
-                  [&](int k, int n) { return T[(16 * cb + k) * kTs + 16 * cb + n]; }, 2 - cb, g, t4);
+                  [&](int k, int n) { return T[t_index<kSwizzledT>(16 * cb + k, 16 * cb + n)]; }, 2 - cb, g, t4);
         float *Mt = M + 256 * warp;
         warp_store16(acc, 1.f, [&](int r, int n, float v0, float v1) {
             *reinterpret_cast<float2 *>(Mt + r * 16 + n) = make_float2(v0, v1); }, g, t4);
@@ -185,7 +192,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
     if (warp < 4) {   // T_{rb,cb} = -sum_{k = 2}^{rb} T_{rb,k} M_{k,cb}
         const int rb = 2 + (warp >> 1), cb = warp & 1;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_mm16(acc, [&](int r, int k) { return T[(16 * rb + r) * kTs + 32 + k]; },
+        warp_mm16(acc, [&](int r, int k) { return T[t_index<kSwizzledT>(16 * rb + r, 32 + k)]; },
                   [&](int k, int n) { return M[256 * (((k >> 4) << 1) | cb) + (k & 15) * 16 + n]; },
                   rb - 1, g, t4);
         warp_store16(acc, -1.f, [&](int r, int n, float v0, float v1) {

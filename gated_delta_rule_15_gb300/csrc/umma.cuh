@@ -104,6 +104,10 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t s
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
+// Wait until at most one committed cp.async group of this thread is still pending.
+__device__ __forceinline__ void cp_async_wait_group1() {
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
