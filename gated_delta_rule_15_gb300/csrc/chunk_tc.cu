@@ -67,13 +67,13 @@ constexpr uint32_t OFF_K0 = 8192, OFF_V0 = 32768;
 constexpr uint32_t SM_ST = 2 * kStageBytes;   // 32 KB: S^T bf16 128 x 128 K-major (steps 1 ->
                                               // D(c)); then, from step 5, the next chunk's fp32
                                               // T (16 KB, swizzled) and T diag beta | T diag
-                                              // beta G (16 KB, until U/W(c+1)); the output
-                                              // tile over T at step 6
-constexpr uint32_t SM_T = SM_ST, SM_TB = SM_ST + 16384, SM_OUT = SM_ST;
-constexpr uint32_t SM_W = SM_ST + 32768;      // W 64 x 128 K-major (step 2 -> D(c)), then E^T
-                                              // high 128 x 64 (step 4 -> E^T P^T)
-constexpr uint32_t SM_ELO = SM_W + 16384;     // E^T low
-constexpr uint32_t SM_ET2 = SM_ELO + 16384;   // E^T diag(delta) high (its low part goes to the
+                                              // beta G (16 KB, until U/W(c+1))
+constexpr uint32_t SM_T = SM_ST, SM_TB = SM_ST + 16384;
+constexpr uint32_t SM_WQ = SM_ST + 32768;     // 32 KB: [W kb0 | Q kb0 | W kb1 | Q kb1], the
+                                              // 128-row B operand [W; Q] of D (W from TMEM, Q
+                                              // copied from the stage; step 2 -> D(c)); then
+                                              // E^T high | E^T low (step 4 -> E^T P^T)
+constexpr uint32_t SM_ET2 = SM_WQ + 32768;    // E^T diag(delta) high (its low part goes to the
                                               // stage's V tile, read by U/W(c) already)
 constexpr uint32_t SM_A = SM_ET2 + 16384;     // the next chunk's fp32 A (step 3 -> step 5)
 constexpr uint32_t SM_P = SM_A + 16384;       // the next chunk's P high | P low (step 6 ->
@@ -90,6 +90,7 @@ constexpr float kFactorSpan = 80.f;
 constexpr uint32_t ID_KK_N64 = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_MK_N64 = idesc_bf16(128, 64, true, false);
 constexpr uint32_t ID_KM_N128 = idesc_bf16(128, 128, false, true);
+constexpr uint32_t ID_KK_N128 = idesc_bf16(128, 128, false, false);
 
 struct TcArgs {
     const float *log_alpha;
@@ -116,7 +117,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     // mbarriers: TMA stages; per MMA group its completion (committed by the MMA warp) and,
     // for the groups whose operands the compute warps write, "operands ready" (full_*,
     // arrived by thread 0 after the compute warps' barrier).  Each completes once per chunk.
-    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_q, bar_s, bar_pe;
+    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_s, bar_pe;
     __shared__ uint64_t full_x, full_uw, full_d, full_s;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s, factored_s[2];
@@ -165,8 +166,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     constexpr int kOutBoxes = sizeof(Tout) == 2 ? 2 : 4;   // 128-byte rows per output box
 
     if (tid == 0) {
-        uint64_t *bars[] = {&bar_tma[0], &bar_tma[1], &bar_x, &bar_uw, &bar_d, &bar_q, &bar_s,
-                            &bar_pe, &full_x, &full_uw, &full_d, &full_s};
+        uint64_t *bars[] = {&bar_tma[0], &bar_tma[1], &bar_x, &bar_uw, &bar_d, &bar_s, &bar_pe,
+                            &full_x, &full_uw, &full_d, &full_s};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         abort_s = 0;
         fence_mbar_init();
@@ -290,12 +291,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     // (compute warps) rows of X for chunk `it` (whose X is in TMEM, gate set it % 2): the
     // A rows (64..127, fp32, at SM_A; warps of lane quarters 2 and 3) or the P rows (0..63,
     // bf16 high/low at SM_P; quarters 0 and 1)
-    auto build_pa = [&](int it, bool rows_a) {
+    auto build_pa = [&](int it, bool rows_a, int col_half) {
         if ((quarter >= 2) != rows_a) return;
         float x[32];
-        tmem_ld32(tm + TM_X + 32 * half, x);
+        tmem_ld32(tm + TM_X + 32 * col_half, x);
         tmem_wait_ld();
-        const int c0 = 32 * half;
+        const int c0 = 32 * col_half;
         const int r = quarter < 2 ? row : row - 64;
         const float *sG = vec(it, 0), *sBeta = vec(it, 3), *sE = vec(it, 4), *sF = vec(it, 5);
         float dec[32];   // exp(g_r - g_s), s = c0 + u
@@ -397,25 +398,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             for (int it = 0; it < n_it && !abort_s; ++it) {
                 const uint32_t par = it & 1;
                 unsigned char *st = stage(it);
-                // D = S^T [W; Q]^T: (W S)^T first (the E^T build waits for it), then (Q S)^T
+                // D = S^T [W; Q]^T = [(W S)^T | (Q S)^T], one N = 128 product (N = 64 without
+                // outputs)
                 if (!wait_cycles(&full_d, par)) { fail(); break; }
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_bf16(tmb + TM_D, desc_add(dK0, SM_ST + o),
-                             desc_add(dK0, SM_W + (ks >> 2) * 8192 + (ks & 3) * 32), ID_KK_N64, ks > 0);
+                    mma_bf16(tmb + TM_D, desc_add(dK0, SM_ST + o), desc_add(dK0, SM_WQ + o),
+                             outputs ? ID_KK_N128 : ID_KK_N64, ks > 0);
                 }
                 mma_commit(&bar_d);
-                if (outputs)
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16(tmb + TM_D + 64, desc_add(dK0, SM_ST + o),
-                                 desc_add(dK0, (uint32_t)((st + o) - sm)), ID_KK_N64, ks > 0);
-                    }
-                mma_commit(&bar_q);
-                last = &bar_q; last_par = par;
+                last = &bar_d; last_par = par;
                 // S^T += (E^T diag delta) K, then PE = E^T P^T  (high/low pairs)
                 if (!wait_cycles(&full_s, par)) { fail(); break; }
                 tc_fence_after();
@@ -427,7 +421,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                         mma_bf16(tmb + TM_S, desc_add(dK0, (uint32_t)((e2[part] + ks * 32) - sm)),
                                  desc_add(dM16, (uint32_t)((st + OFF_K0 + ks * 2048) - sm)), ID_KM_N128, 1);
                 mma_commit(&bar_s);
-                const uint32_t ea[3] = {SM_W, SM_W, SM_ELO}, pb[3] = {SM_P, SM_P + 8192, SM_P};
+                const uint32_t ea[3] = {SM_WQ, SM_WQ, SM_WQ + 16384}, pb[3] = {SM_P, SM_P + 8192, SM_P};
                 if (outputs)
 #pragma unroll
                     for (int part = 0; part < 3; ++part)
@@ -469,14 +463,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
         tmem_wait_st();
     }
-    bool store_outstanding = false;   // thread 0: a TMA store may still be reading SM_OUT
     if (n_it > 0) {
         // prologue: chunk 0's gates, A and P, solve; chunk 1's gates
         if (warp == kGateWarp) scan_gates(0);
         named_sync(1, kThreads);
         wait_bar(&bar_x, 0);
-        build_pa(0, true);
-        if (outputs) build_pa(0, false);
+        build_pa(0, true, half);
+        if (outputs) build_pa(0, false, half);
         fence_proxy_async();
         tc_fence_before();
         named_sync(1, kThreads);
@@ -493,15 +486,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const bool next = it + 1 < n_it;
 
         // ---- 1. S^T to bf16 (SM_ST) and S^T <- gamma S^T in TMEM: after the previous state
-        //         update, after this chunk's U/W products have read T diag beta (SM_TB), and
-        //         after the previous output tile's store has read SM_OUT
+        //         update, and after this chunk's U/W products have read T diag beta (SM_TB)
         if (it >= 1) wait_bar(&bar_s, par ^ 1);
         wait_bar(&bar_uw, par);
-        if (tid == 0 && store_outstanding) {
-            bulk_wait_read_all();
-            store_outstanding = false;
-        }
-        named_sync(1, kThreads);
         {
             const float gamma = vec(it, 1)[63];
             float v[32];
@@ -523,17 +510,28 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             }
             tmem_wait_st();
         }
-        // ---- 2. W from W^T (lane i = key channel, columns = tokens r) into SM_W
+        // ---- 2. W from W^T (lane i = key channel, columns = tokens r) and the chunk's Q tiles
+        //         (arrived by TMA, seen so far by the MMA warp only; this stage's next load is
+        //         issued at step 6) into the B operand [W; Q] of D
         {
             float w[32];
             tmem_ld32(tm + TM_W + 32 * half, w);
             tmem_wait_ld();
             const int i = row, kb = i >> 6, ci = i & 63;
-            unsigned char *dst = sm + SM_W + kb * 8192;
+            unsigned char *dst = sm + SM_WQ + kb * 16384;
 #pragma unroll
             for (int u = 0; u < 32; ++u)
                 *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, ci)) =
                     __float2bfloat16_rn(w[u]);
+            if (outputs) {   // 1 KB-aligned 8 KB tiles: a plain copy keeps the swizzle
+                if (!wait_cycles(&bar_tma[it & 1], (it >> 1) & 1)) fail();
+                const uint4 *qs = reinterpret_cast<const uint4 *>(st);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = tid + kThreads * k, kbq = e >> 9, off = e & 511;   // 512 x 16 B per tile
+                    reinterpret_cast<uint4 *>(sm + SM_WQ + kbq * 16384 + 8192)[off] = qs[kbq * 1024 + off];
+                }
+            }
         }
         fence_proxy_async();
         tc_fence_before();
@@ -544,7 +542,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         // ---- 3. A of the next chunk (its X arrived meanwhile)
         if (next) {
             wait_bar(&bar_x, (it + 1) & 1);
-            build_pa(it + 1, true);
+            build_pa(it + 1, true, half);
         }
 
         // ---- 4. E^T = U^T - (W S)^T, and E^T diag(delta)  (bf16 high/low pairs)
@@ -574,8 +572,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     pack_hi_lo(e[2 * u], e[2 * u + 1], eh[u], el[u]);
                     pack_hi_lo(ed[2 * u], ed[2 * u + 1], dh[u], dlo[u]);
                 }
-                *reinterpret_cast<uint4 *>(sm + SM_W + off) = make_uint4(eh[0], eh[1], eh[2], eh[3]);
-                *reinterpret_cast<uint4 *>(sm + SM_ELO + off) = make_uint4(el[0], el[1], el[2], el[3]);
+                *reinterpret_cast<uint4 *>(sm + SM_WQ + off) = make_uint4(eh[0], eh[1], eh[2], eh[3]);
+                *reinterpret_cast<uint4 *>(sm + SM_WQ + 16384 + off) = make_uint4(el[0], el[1], el[2], el[3]);
                 *reinterpret_cast<uint4 *>(sm + SM_ET2 + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
                 *reinterpret_cast<uint4 *>(st + OFF_V0 + off) = make_uint4(dlo[0], dlo[1], dlo[2], dlo[3]);
             }
@@ -585,59 +583,74 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         named_sync(1, kThreads);
         if (tid == 0) mbar_arrive(&full_s);   // state update, E^T P^T (MMA warp)
 
-        // ---- 5. the next chunk's solve; its T goes over S^T, which (Q S)^T must have read
+        // ---- 5. the next chunk's solve (its T goes over S^T, which D has read): the diagonal
+        //         blocks on all warps, then the merges on warps 0..3 while warps 4..7 write
+        //         this chunk's output o = G_r (Q S)^T + E^T P^T (staged in the stage's Q and K
+        //         tiles, dead once E^T P^T is done) and the next chunk's P (E^T P^T has read
+        //         SM_P)
+        const SolveOut<true, true> sout{reinterpret_cast<float *>(sm + SM_T), sm + SM_TB, vec(it + 1, 3),
+                                        vec(it + 1, 1)};
         if (next) {
-            wait_bar(&bar_q, par);
-            solve(it + 1);
-            if (tid == 0) mbar_arrive(&full_uw);   // the next chunk's U/W (MMA warp)
+            solve_diag64(reinterpret_cast<const float *>(sm + SM_A), sout, tid);
+            named_sync(1, kThreads);
         }
-
-        // ---- 6. this chunk's output o = G_r (Q S)^T + E^T P^T, staged at SM_OUT and written by
-        //         TMA; the next chunk's P (E^T P^T has read SM_P); the stage takes chunk it + 2
-        wait_bar(&bar_pe, par);
-        if (outputs) {
-            float o[32], pe[32];
-            tmem_ld32(tm + TM_D + 64 + 32 * half, o);
-            tmem_ld32(tm + TM_PE + 32 * half, pe);
-            tmem_wait_ld();
-            const float *sGam = vec(it, 1);
+        if (warp < 4) {
+            if (next) solve_merge64(reinterpret_cast<const float *>(sm + SM_A), sout, sM, tid, 2);
+        } else {
+            wait_bar(&bar_pe, par);
+            if (outputs) {
+                const int j = row;   // value channel; all 64 tokens of this lane
+                const float *sGam = vec(it, 1);
 #pragma unroll
-            for (int u = 0; u < 32; ++u) o[u] = fmaf(sGam[32 * half + u], o[u], pe[u]);
-            const int j = row;
-            if (sizeof(Tout) == 2) {
-                unsigned char *dst = sm + SM_OUT + (j >> 6) * 8192;
+                for (int hh = 0; hh < 2; ++hh) {
+                    float o[32], pe[32];
+                    tmem_ld32(tm + TM_D + 64 + 32 * hh, o);
+                    tmem_ld32(tm + TM_PE + 32 * hh, pe);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int u = 0; u < 32; ++u)
-                    *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, j & 63)) =
-                        __float2bfloat16_rn(o[u]);
-            } else {
-                // fp32: 32 KB, over S^T's second half too, which the next chunk's U/W products
-                // read as T diag beta: they must have completed
-                if (next) wait_bar(&bar_uw, (it + 1) & 1);
-                unsigned char *dst = sm + SM_OUT + (j >> 5) * 8192;
-                const int cj = j & 31;
+                    for (int u = 0; u < 32; ++u) o[u] = fmaf(sGam[32 * hh + u], o[u], pe[u]);
+                    if (sizeof(Tout) == 2) {
+                        unsigned char *dst = st + (j >> 6) * 16384;
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int r = 32 * half + u;
-                    *reinterpret_cast<float *>(dst + r * 128 + ((((cj >> 2) ^ (r & 7)) & 7) << 4) +
-                                               ((cj & 3) << 2)) = o[u];
+                        for (int u = 0; u < 32; ++u)
+                            *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * hh + u, j & 63)) =
+                                __float2bfloat16_rn(o[u]);
+                    } else {
+                        unsigned char *dst = st + (j >> 5) * 8192;
+                        const int cj = j & 31;
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) {
+                            const int r = 32 * hh + u;
+                            *reinterpret_cast<float *>(dst + r * 128 + ((((cj >> 2) ^ (r & 7)) & 7) << 4) +
+                                                       ((cj & 3) << 2)) = o[u];
+                        }
+                    }
+                }
+                if (next) {   // P rows: lanes 0..63 (warps 4 and 5), both column halves
+                    build_pa(it + 1, false, 0);
+                    build_pa(it + 1, false, 1);
+                }
+                fence_proxy_async();
+                named_sync(3, 128);
+                if (tid == kTmaThread) {
+                    constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
+                    constexpr uint32_t box = sizeof(Tout) == 2 ? 16384 : 8192;
+#pragma unroll
+                    for (int kb = 0; kb < kOutBoxes; ++kb)
+                        tma_store_4d(&to, st + kb * box, cols * kb, h, t0, b);
+                    bulk_commit();
+                    bulk_wait_read_all();   // the stage is reloaded next
                 }
             }
-            if (next) build_pa(it + 1, false);
         }
-        fence_proxy_async();
         tc_fence_before();
         named_sync(1, kThreads);
+
+        // ---- 6. hand-offs: the next chunk's U/W and the chunk after next's X (MMA warp); the
+        //         stage of this chunk takes the chunk after next
         if (tid == 0) {
-            if (outputs) {
-                constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
-#pragma unroll
-                for (int kb = 0; kb < kOutBoxes; ++kb)
-                    tma_store_4d(&to, sm + SM_OUT + kb * 8192, cols * kb, h, t0, b);
-                bulk_commit();
-                store_outstanding = true;
-            }
-            if (it + 2 < n_it) mbar_arrive(&full_x);   // the chunk after next's X (MMA warp)
+            if (next) mbar_arrive(&full_uw);
+            if (it + 2 < n_it) mbar_arrive(&full_x);
         }
         if (tid == kTmaThread && it + 2 < n_it) issue_tma(it + 2);
         // ---- 7. gates of the chunk after next (into this chunk's set, now free)
@@ -661,7 +674,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         for (int i = 0; i < min(n_it, 2); ++i) wait_cycles(&bar_tma[i], 0);
     }
     if (warp == kGateWarp) cp_async_wait_all();
-    if (tid == 0 && store_outstanding) bulk_wait_all();
+    if (tid == kTmaThread) bulk_wait_all();   // the output stores' global writes
     }   // compute warps
     tc_fence_before();
     __syncthreads();

@@ -96,73 +96,86 @@ __device__ __forceinline__ int a_index(int r, int s) {
 // Each element is written, once final, also as T diag(beta) in bf16 (a 128-byte-swizzled
 // K-major 64 x 64 tile at TB) and, with kPair, as T diag(beta G) at TB + 8192: the U and W
 // operands.  Products use TF32 mma.sync with fp32 accumulation.  M needs 1024 floats.
-// Called by 256 threads (the CTA's compute warps, which synchronise on named barrier 1);
-// starts after and ends with a barrier.
-template <bool kPair = true, bool kSwizzledT = false>
-__device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, float *M,
-                                                   unsigned char *TB, const float *beta,
-                                                   const float *gam, int tid) {
-    auto a = [&](int r, int s) { return A[a_index(r, s)]; };
-    // final element (r, s) of T: fp32 copy for the later levels, and the two bf16 MMA
-    // operands T diag(beta) (at TB) and T diag(beta G) (at TB + 8192)
-    auto fin = [&](int r, int s, float v) {
+// Step 1 is solve_diag64 (256 threads); steps 2 and 3 are solve_merge64 (warps 0..3 only,
+// synchronising on their own named barrier), so that warps 4..7 are free meanwhile.
+template <bool kPair, bool kSwizzledT>
+struct SolveOut {
+    float *T;
+    unsigned char *TB;
+    const float *beta, *gam;
+    // final element (r, s) of T: fp32 copy for the later levels, and the bf16 MMA operands
+    __device__ __forceinline__ void fin(int r, int s, float v) const {
         T[t_index<kSwizzledT>(r, s)] = v;
         const float vb = v * beta[s];
         const uint32_t off = sw128_off(r, s);
         *reinterpret_cast<__nv_bfloat16 *>(TB + off) = __float2bfloat16_rn(vb);
         if constexpr (kPair)
             *reinterpret_cast<__nv_bfloat16 *>(TB + 8192 + off) = __float2bfloat16_rn(vb * gam[s]);
-    };
+    }
     // final elements (r, s) and (r, s + 1), s even: one 32-bit store per operand
-    auto fin2 = [&](int r, int s, float v0, float v1) {
+    __device__ __forceinline__ void fin2(int r, int s, float v0, float v1) const {
         *reinterpret_cast<float2 *>(T + t_index<kSwizzledT>(r, s)) = make_float2(v0, v1);
         const float b0 = v0 * beta[s], b1 = v1 * beta[s + 1];
         const uint32_t off = sw128_off(r, s);
         *reinterpret_cast<uint32_t *>(TB + off) = pack_bf16(b0, b1);
         if constexpr (kPair)
             *reinterpret_cast<uint32_t *>(TB + 8192 + off) = pack_bf16(b0 * gam[s], b1 * gam[s + 1]);
-    };
-    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-    {
-        const int o = 16 * (tid >> 6), c = (tid >> 2) & 15, part = tid & 3;
-        const int owner = lane & ~3;
-        // this thread's four rows of the diagonal block, o + part + 4m, columns o .. o + 15
-        float ar[4][16];
+    }
+};
+
+// Step 1 (256 threads, tid 0..255): the diagonal blocks and the zero blocks of the operands.
+template <bool kPair, bool kSwizzledT>
+__device__ __forceinline__ void solve_diag64(const float *A, const SolveOut<kPair, kSwizzledT> &out,
+                                             int tid) {
+    const int lane = tid & 31;
+    const int o = 16 * (tid >> 6), c = (tid >> 2) & 15, part = tid & 3;
+    const int owner = lane & ~3;
+    // this thread's four rows of the diagonal block, o + part + 4m, columns o .. o + 15
+    float ar[4][16];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int r = o + part + 4 * m;
+    for (int m = 0; m < 4; ++m) {
+        const int r = o + part + 4 * m;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(A + a_index(r, o + 4 * q));
-                ar[m][4 * q] = v4.x; ar[m][4 * q + 1] = v4.y;
-                ar[m][4 * q + 2] = v4.z; ar[m][4 * q + 3] = v4.w;
-            }
-        }
-        float y[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) y[m] = (part + 4 * m == c) ? 1.f : 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < 15; ++s2) {
-            const float xs = __shfl_sync(0xffffffffu, y[s2 >> 2], owner | (s2 & 3));
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-                if (part + 4 * m > s2) y[m] = fmaf(-ar[m][s2], xs, y[m]);
-        }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) fin(o + part + 4 * m, o + c, y[m]);
-        // the six blocks above the diagonal are zero in the bf16 operands (the fp32 copy
-        // of those blocks is never read): (0,1) (0,2) (0,3) (1,2) (1,3) (2,3), 8 per task
-        for (int idx = tid; idx < 6 * 32; idx += 256) {
-            const int blk = idx >> 5, e = idx & 31;
-            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            const uint32_t off = sw128_off(16 * bi + (e >> 1), 16 * bj + 8 * (e & 1));
-            *reinterpret_cast<uint4 *>(TB + off) = make_uint4(0u, 0u, 0u, 0u);
-            if constexpr (kPair)
-                *reinterpret_cast<uint4 *>(TB + 8192 + off) = make_uint4(0u, 0u, 0u, 0u);
+        for (int q = 0; q < 4; ++q) {
+            const float4 v4 = *reinterpret_cast<const float4 *>(A + a_index(r, o + 4 * q));
+            ar[m][4 * q] = v4.x; ar[m][4 * q + 1] = v4.y;
+            ar[m][4 * q + 2] = v4.z; ar[m][4 * q + 3] = v4.w;
         }
     }
-    named_sync(1, 256);
+    float y[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) y[m] = (part + 4 * m == c) ? 1.f : 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < 15; ++s2) {
+        const float xs = __shfl_sync(0xffffffffu, y[s2 >> 2], owner | (s2 & 3));
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            if (part + 4 * m > s2) y[m] = fmaf(-ar[m][s2], xs, y[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) out.fin(o + part + 4 * m, o + c, y[m]);
+    // the six blocks above the diagonal are zero in the bf16 operands (the fp32 copy of
+    // those blocks is never read): (0,1) (0,2) (0,3) (1,2) (1,3) (2,3), 8 per task
+    if (tid < 6 * 32) {
+        const int blk = tid >> 5, e = tid & 31;
+        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        const uint32_t off = sw128_off(16 * bi + (e >> 1), 16 * bj + 8 * (e & 1));
+        *reinterpret_cast<uint4 *>(out.TB + off) = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (kPair)
+            *reinterpret_cast<uint4 *>(out.TB + 8192 + off) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async();   // these operand entries are read by the tensor core later
+}
+
+// Steps 2 and 3 (warps 0..3, tid 0..127; starts after a barrier that follows step 1 and
+// ends with the operands' proxy fence, without a final barrier).
+template <bool kPair, bool kSwizzledT>
+__device__ __forceinline__ void solve_merge64(const float *A, const SolveOut<kPair, kSwizzledT> &out,
+                                              float *M, int tid, uint32_t bar_id) {
+    const float *T = out.T;
+    auto a = [&](int r, int s) { return A[a_index(r, s)]; };
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
     if (warp < 2) {
         const int i = 2 * warp + 1, j = 2 * warp;
         float *Ms = M + 256 * warp;
@@ -176,10 +189,10 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         warp_mm16(acc2, [&](int r, int k) { return T[t_index<kSwizzledT>(16 * i + r, 16 * i + k)]; },
                   [&](int k, int n) { return Ms[k * 16 + n]; }, 1, g, t4);
         warp_store16(acc2, -1.f, [&](int r, int n, float v0, float v1) {
-            fin2(16 * i + r, 16 * j + n, v0, v1); }, g, t4);
+            out.fin2(16 * i + r, 16 * j + n, v0, v1); }, g, t4);
     }
-    named_sync(1, 256);
-    if (warp < 4) {   // M tile (rb, cb) = sum_{k = cb}^{1} A_{rb,k} T_{k,cb},  rb = 2 + w/2, cb = w%2
+    named_sync(bar_id, 128);
+    {   // M tile (rb, cb) = sum_{k = cb}^{1} A_{rb,k} T_{k,cb},  rb = 2 + w/2, cb = w%2
         const int rb = 2 + (warp >> 1), cb = warp & 1;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         warp_mm16(acc, [&](int r, int k) { return a(16 * rb + r, 16 * cb + k); },
@@ -188,17 +201,29 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
         warp_store16(acc, 1.f, [&](int r, int n, float v0, float v1) {
             *reinterpret_cast<float2 *>(Mt + r * 16 + n) = make_float2(v0, v1); }, g, t4);
     }
-    named_sync(1, 256);
-    if (warp < 4) {   // T_{rb,cb} = -sum_{k = 2}^{rb} T_{rb,k} M_{k,cb}
+    named_sync(bar_id, 128);
+    {   // T_{rb,cb} = -sum_{k = 2}^{rb} T_{rb,k} M_{k,cb}
         const int rb = 2 + (warp >> 1), cb = warp & 1;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         warp_mm16(acc, [&](int r, int k) { return T[t_index<kSwizzledT>(16 * rb + r, 32 + k)]; },
                   [&](int k, int n) { return M[256 * (((k >> 4) << 1) | cb) + (k & 15) * 16 + n]; },
                   rb - 1, g, t4);
         warp_store16(acc, -1.f, [&](int r, int n, float v0, float v1) {
-            fin2(16 * rb + r, 16 * cb + n, v0, v1); }, g, t4);
+            out.fin2(16 * rb + r, 16 * cb + n, v0, v1); }, g, t4);
     }
     fence_proxy_async();   // the bf16 operands are read next by the tensor core
+}
+
+// The whole solve by 256 threads (the CTA's compute warps, which synchronise on named
+// barriers 1 (all) and 2 (warps 0..3)); starts after and ends with a barrier.
+template <bool kPair = true, bool kSwizzledT = false>
+__device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, float *M,
+                                                   unsigned char *TB, const float *beta,
+                                                   const float *gam, int tid) {
+    const SolveOut<kPair, kSwizzledT> out{T, TB, beta, gam};
+    solve_diag64(A, out, tid);
+    named_sync(1, 256);
+    if (tid < 128) solve_merge64(A, out, M, tid, 2);
     named_sync(1, 256);
 }
 
