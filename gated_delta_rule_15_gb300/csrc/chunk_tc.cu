@@ -69,10 +69,9 @@ constexpr uint32_t SM_ST = 2 * kStageBytes;   // 32 KB: S^T bf16 128 x 128 K-maj
                                               // T (16 KB, swizzled) and T diag beta | T diag
                                               // beta G (16 KB, until U/W(c+1))
 constexpr uint32_t SM_T = SM_ST, SM_TB = SM_ST + 16384;
-constexpr uint32_t SM_WQ = SM_ST + 32768;     // 32 KB: [W kb0 | Q kb0 | W kb1 | Q kb1], the
-                                              // 128-row B operand [W; Q] of D (W from TMEM, Q
-                                              // copied from the stage; step 2 -> D(c)); then
-                                              // E^T high | E^T low (step 4 -> E^T P^T)
+constexpr uint32_t SM_WQ = SM_ST + 32768;     // 32 KB: W^T 128 x 64 (MN-major B operand of
+                                              // (W S)^T; step 2 -> D(c)); then E^T high |
+                                              // E^T low (step 4 -> E^T P^T)
 constexpr uint32_t SM_ET2 = SM_WQ + 32768;    // E^T diag(delta) high (its low part goes to the
                                               // stage's V tile, read by U/W(c) already)
 constexpr uint32_t SM_A = SM_ET2 + 16384;     // the next chunk's fp32 A (step 3 -> step 5)
@@ -90,7 +89,7 @@ constexpr float kFactorSpan = 80.f;
 constexpr uint32_t ID_KK_N64 = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_MK_N64 = idesc_bf16(128, 64, true, false);
 constexpr uint32_t ID_KM_N128 = idesc_bf16(128, 128, false, true);
-constexpr uint32_t ID_KK_N128 = idesc_bf16(128, 128, false, false);
+constexpr uint32_t ID_KM_N64 = idesc_bf16(128, 64, false, true);
 
 struct TcArgs {
     const float *log_alpha;
@@ -117,7 +116,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     // mbarriers: TMA stages; per MMA group its completion (committed by the MMA warp) and,
     // for the groups whose operands the compute warps write, "operands ready" (full_*,
     // arrived by thread 0 after the compute warps' barrier).  Each completes once per chunk.
-    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_s, bar_pe;
+    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_q, bar_s, bar_pe;
     __shared__ uint64_t full_x, full_uw, full_d, full_s;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s, factored_s[2];
@@ -166,8 +165,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     constexpr int kOutBoxes = sizeof(Tout) == 2 ? 2 : 4;   // 128-byte rows per output box
 
     if (tid == 0) {
-        uint64_t *bars[] = {&bar_tma[0], &bar_tma[1], &bar_x, &bar_uw, &bar_d, &bar_s, &bar_pe,
-                            &full_x, &full_uw, &full_d, &full_s};
+        uint64_t *bars[] = {&bar_tma[0], &bar_tma[1], &bar_x, &bar_uw, &bar_d, &bar_q, &bar_s,
+                            &bar_pe, &full_x, &full_uw, &full_d, &full_s};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         abort_s = 0;
         fence_mbar_init();
@@ -398,18 +397,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             for (int it = 0; it < n_it && !abort_s; ++it) {
                 const uint32_t par = it & 1;
                 unsigned char *st = stage(it);
-                // D = S^T [W; Q]^T = [(W S)^T | (Q S)^T], one N = 128 product (N = 64 without
-                // outputs)
+                // D = S^T [W; Q]^T: (W S)^T first (W^T MN-major; the E^T build waits for it),
+                // then (Q S)^T (Q straight from the stage)
                 if (!wait_cycles(&full_d, par)) { fail(); break; }
                 tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_bf16(tmb + TM_D, desc_add(dK0, SM_ST + o), desc_add(dK0, SM_WQ + o),
-                             outputs ? ID_KK_N128 : ID_KK_N64, ks > 0);
-                }
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tmb + TM_D, desc_add(dK0, SM_ST + (ks >> 2) * 16384 + (ks & 3) * 32),
+                             desc_add(dM8, SM_WQ + ks * 2048), ID_KM_N64, ks > 0);
                 mma_commit(&bar_d);
-                last = &bar_d; last_par = par;
+                if (outputs)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16(tmb + TM_D + 64, desc_add(dK0, SM_ST + o),
+                                 desc_add(dK0, (uint32_t)((st + o) - sm)), ID_KK_N64, ks > 0);
+                    }
+                mma_commit(&bar_q);
+                last = &bar_q; last_par = par;
                 // S^T += (E^T diag delta) K, then PE = E^T P^T  (high/low pairs)
                 if (!wait_cycles(&full_s, par)) { fail(); break; }
                 tc_fence_after();
@@ -510,27 +515,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             }
             tmem_wait_st();
         }
-        // ---- 2. W from W^T (lane i = key channel, columns = tokens r) and the chunk's Q tiles
-        //         (arrived by TMA, seen so far by the MMA warp only; this stage's next load is
-        //         issued at step 6) into the B operand [W; Q] of D
+        // ---- 2. W^T (lane i = key channel, columns = tokens r) as the MN-major B operand of
+        //         (W S)^T: this lane's row of 64 tokens, 16 bytes at a time
         {
             float w[32];
             tmem_ld32(tm + TM_W + 32 * half, w);
             tmem_wait_ld();
-            const int i = row, kb = i >> 6, ci = i & 63;
-            unsigned char *dst = sm + SM_WQ + kb * 16384;
 #pragma unroll
-            for (int u = 0; u < 32; ++u)
-                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, ci)) =
-                    __float2bfloat16_rn(w[u]);
-            if (outputs) {   // 1 KB-aligned 8 KB tiles: a plain copy keeps the swizzle
-                if (!wait_cycles(&bar_tma[it & 1], (it >> 1) & 1)) fail();
-                const uint4 *qs = reinterpret_cast<const uint4 *>(st);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int e = tid + kThreads * k, kbq = e >> 9, off = e & 511;   // 512 x 16 B per tile
-                    reinterpret_cast<uint4 *>(sm + SM_WQ + kbq * 16384 + 8192)[off] = qs[kbq * 1024 + off];
-                }
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float *f = w + 8 * q4;
+                *reinterpret_cast<uint4 *>(sm + SM_WQ + sw128_off(row, 32 * half + 8 * q4)) =
+                    make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                               pack_bf16(f[6], f[7]));
             }
         }
         fence_proxy_async();
@@ -583,7 +579,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         named_sync(1, kThreads);
         if (tid == 0) mbar_arrive(&full_s);   // state update, E^T P^T (MMA warp)
 
-        // ---- 5. the next chunk's solve (its T goes over S^T, which D has read): the diagonal
+        // ---- 5. the next chunk's solve (its T goes over S^T, which D must have read): the diagonal
         //         blocks on all warps, then the merges on warps 0..3 while warps 4..7 write
         //         this chunk's output o = G_r (Q S)^T + E^T P^T (staged in the stage's Q and K
         //         tiles, dead once E^T P^T is done) and the next chunk's P (E^T P^T has read
@@ -591,6 +587,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const SolveOut<true, true> sout{reinterpret_cast<float *>(sm + SM_T), sm + SM_TB, vec(it + 1, 3),
                                         vec(it + 1, 1)};
         if (next) {
+            wait_bar(&bar_q, par);
             solve_diag64(reinterpret_cast<const float *>(sm + SM_A), sout, tid);
             named_sync(1, kThreads);
         }
