@@ -340,6 +340,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 v4.y = s0 + 1 < r ? br * dec[4 * q4 + 1] * x[4 * q4 + 1] : 0.f;
                 v4.z = s0 + 2 < r ? br * dec[4 * q4 + 2] * x[4 * q4 + 2] : 0.f;
                 v4.w = s0 + 3 < r ? br * dec[4 * q4 + 3] * x[4 * q4 + 3] : 0.f;
+                if ((s0 >> 4) != (r >> 4)) {   // off-diagonal blocks: read only as TF32 operands
+                    v4.x = round_tf32(v4.x); v4.y = round_tf32(v4.y);
+                    v4.z = round_tf32(v4.z); v4.w = round_tf32(v4.w);
+                }
                 *reinterpret_cast<float4 *>(sA + a_index(r, s0)) = v4;
             }
         }
@@ -584,7 +588,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         //         this chunk's output o = G_r (Q S)^T + E^T P^T (staged in the stage's Q and K
         //         tiles, dead once E^T P^T is done) and the next chunk's P (E^T P^T has read
         //         SM_P)
-        const SolveOut<true, true> sout{reinterpret_cast<float *>(sm + SM_T), sm + SM_TB, vec(it + 1, 3),
+        const SolveOut<true, true, true> sout{reinterpret_cast<float *>(sm + SM_T), sm + SM_TB, vec(it + 1, 3),
                                         vec(it + 1, 1)};
         if (next) {
             wait_bar(&bar_q, par);

@@ -48,18 +48,35 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// fp32 element as a TF32 operand: rounded here (kCvt), or already rounded when stored
+template <bool kCvt>
+__device__ __forceinline__ uint32_t tf32_op(float x) { return kCvt ? to_tf32(x) : __float_as_uint(x); }
+// x rounded to TF32 (its low 13 mantissa bits cleared), as a float
+__device__ __forceinline__ float round_tf32(float x) { return __uint_as_float(to_tf32(x)); }
+
 // acc (16 x 16, mma.sync C fragment) += L (16 x 16 nk) * R (16 nk x 16); one warp.
-// L(r, k) and R(k, n) return fp32 elements; operands are rounded to TF32.
-template <class FL, class FR>
+// L(r, k) and R(k, n) return fp32 elements, rounded to TF32 here unless kCvt is false
+// (then they must have been stored rounded).
+template <bool kCvt = true, class FL, class FR>
 __device__ __forceinline__ void warp_mm16(float (&acc)[2][4], FL L, FR R, int nk, int g, int t4) {
     for (int kt = 0; kt < 2 * nk; ++kt) {
         const int kc = 8 * kt;
-        const uint32_t af[4] = {to_tf32(L(g, kc + t4)), to_tf32(L(g + 8, kc + t4)),
-                                to_tf32(L(g, kc + t4 + 4)), to_tf32(L(g + 8, kc + t4 + 4))};
+        const uint32_t af[4] = {tf32_op<kCvt>(L(g, kc + t4)), tf32_op<kCvt>(L(g + 8, kc + t4)),
+                                tf32_op<kCvt>(L(g, kc + t4 + 4)), tf32_op<kCvt>(L(g + 8, kc + t4 + 4))};
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
-            mma_tf32_16x8x8(acc[nt], af, to_tf32(R(kc + t4, 8 * nt + g)),
-                            to_tf32(R(kc + t4 + 4, 8 * nt + g)));
+            mma_tf32_16x8x8(acc[nt], af, tf32_op<kCvt>(R(kc + t4, 8 * nt + g)),
+                            tf32_op<kCvt>(R(kc + t4 + 4, 8 * nt + g)));
+    }
+}
+// acc (16 x 8) += L (16 x 16 nk) * R (16 nk x 8); one warp, one n-tile.
+template <bool kCvt = true, class FL, class FR>
+__device__ __forceinline__ void warp_mm16x8(float (&acc)[4], FL L, FR R, int nk, int g, int t4) {
+    for (int kt = 0; kt < 2 * nk; ++kt) {
+        const int kc = 8 * kt;
+        const uint32_t af[4] = {tf32_op<kCvt>(L(g, kc + t4)), tf32_op<kCvt>(L(g + 8, kc + t4)),
+                                tf32_op<kCvt>(L(g, kc + t4 + 4)), tf32_op<kCvt>(L(g + 8, kc + t4 + 4))};
+        mma_tf32_16x8x8(acc, af, tf32_op<kCvt>(R(kc + t4, g)), tf32_op<kCvt>(R(kc + t4 + 4, g)));
     }
 }
 // Writes sign * acc through st(r, n, v0, v1): elements (r, n) and (r, n + 1), n even.
@@ -98,14 +115,14 @@ __device__ __forceinline__ int a_index(int r, int s) {
 // operands.  Products use TF32 mma.sync with fp32 accumulation.  M needs 1024 floats.
 // Step 1 is solve_diag64 (256 threads); steps 2 and 3 are solve_merge64 (warps 0..3 only,
 // synchronising on their own named barrier), so that warps 4..7 are free meanwhile.
-template <bool kPair, bool kSwizzledT>
+template <bool kPair, bool kSwizzledT, bool kPreRound = false>
 struct SolveOut {
     float *T;
     unsigned char *TB;
     const float *beta, *gam;
     // final element (r, s) of T: fp32 copy for the later levels, and the bf16 MMA operands
     __device__ __forceinline__ void fin(int r, int s, float v) const {
-        T[t_index<kSwizzledT>(r, s)] = v;
+        T[t_index<kSwizzledT>(r, s)] = kPreRound ? round_tf32(v) : v;
         const float vb = v * beta[s];
         const uint32_t off = sw128_off(r, s);
         *reinterpret_cast<__nv_bfloat16 *>(TB + off) = __float2bfloat16_rn(vb);
@@ -114,7 +131,8 @@ struct SolveOut {
     }
     // final elements (r, s) and (r, s + 1), s even: one 32-bit store per operand
     __device__ __forceinline__ void fin2(int r, int s, float v0, float v1) const {
-        *reinterpret_cast<float2 *>(T + t_index<kSwizzledT>(r, s)) = make_float2(v0, v1);
+        *reinterpret_cast<float2 *>(T + t_index<kSwizzledT>(r, s)) =
+            kPreRound ? make_float2(round_tf32(v0), round_tf32(v1)) : make_float2(v0, v1);
         const float b0 = v0 * beta[s], b1 = v1 * beta[s + 1];
         const uint32_t off = sw128_off(r, s);
         *reinterpret_cast<uint32_t *>(TB + off) = pack_bf16(b0, b1);
@@ -124,9 +142,9 @@ struct SolveOut {
 };
 
 // Step 1 (256 threads, tid 0..255): the diagonal blocks and the zero blocks of the operands.
-template <bool kPair, bool kSwizzledT>
-__device__ __forceinline__ void solve_diag64(const float *A, const SolveOut<kPair, kSwizzledT> &out,
-                                             int tid) {
+template <bool kPair, bool kSwizzledT, bool kPreRound>
+__device__ __forceinline__ void solve_diag64(const float *A,
+                                             const SolveOut<kPair, kSwizzledT, kPreRound> &out, int tid) {
     const int lane = tid & 31;
     const int o = 16 * (tid >> 6), c = (tid >> 2) & 15, part = tid & 3;
     const int owner = lane & ~3;
@@ -169,25 +187,48 @@ __device__ __forceinline__ void solve_diag64(const float *A, const SolveOut<kPai
 }
 
 // Steps 2 and 3 (warps 0..3, tid 0..127; starts after a barrier that follows step 1 and
-// ends with the operands' proxy fence, without a final barrier).
-template <bool kPair, bool kSwizzledT>
-__device__ __forceinline__ void solve_merge64(const float *A, const SolveOut<kPair, kSwizzledT> &out,
+// ends with the operands' proxy fence, without a final barrier).  With kPreRound, T, M and
+// the off-diagonal blocks of A hold TF32-rounded values (the products take them as they are;
+// the result is the same as rounding at each load), and level 2 runs on four warps, one
+// 8-column half of a block each (the second product needs only its own half of the first).
+template <bool kPair, bool kSwizzledT, bool kPreRound>
+__device__ __forceinline__ void solve_merge64(const float *A,
+                                              const SolveOut<kPair, kSwizzledT, kPreRound> &out,
                                               float *M, int tid, uint32_t bar_id) {
+    constexpr bool kCvt = !kPreRound;
     const float *T = out.T;
     auto a = [&](int r, int s) { return A[a_index(r, s)]; };
+    auto tt = [&](int r, int s) { return T[t_index<kSwizzledT>(r, s)]; };
+    auto rnd = [&](float x) { return kPreRound ? round_tf32(x) : x; };
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-    if (warp < 2) {
+    if constexpr (kPreRound) {
+        // T_10 (warps 0, 1) and T_32 (warps 2, 3), columns 8 nh .. 8 nh + 7
+        const int bp = warp >> 1, nh = warp & 1, i = 2 * bp + 1, j = 2 * bp;
+        float *Ms = M + 256 * bp;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_mm16x8<false>(acc, [&](int r, int k) { return a(16 * i + r, 16 * j + k); },
+                           [&](int k, int n) { return tt(16 * j + k, 16 * j + 8 * nh + n); }, 1, g, t4);
+        const int n0 = 8 * nh + 2 * t4;
+        *reinterpret_cast<float2 *>(Ms + g * 16 + n0) = make_float2(rnd(acc[0]), rnd(acc[1]));
+        *reinterpret_cast<float2 *>(Ms + (g + 8) * 16 + n0) = make_float2(rnd(acc[2]), rnd(acc[3]));
+        __syncwarp();
+        float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_mm16x8<false>(acc2, [&](int r, int k) { return tt(16 * i + r, 16 * i + k); },
+                           [&](int k, int n) { return Ms[k * 16 + 8 * nh + n]; }, 1, g, t4);
+        out.fin2(16 * i + g, 16 * j + n0, -acc2[0], -acc2[1]);
+        out.fin2(16 * i + g + 8, 16 * j + n0, -acc2[2], -acc2[3]);
+    } else if (warp < 2) {
         const int i = 2 * warp + 1, j = 2 * warp;
         float *Ms = M + 256 * warp;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_mm16(acc, [&](int r, int k) { return a(16 * i + r, 16 * j + k); },
-                  [&](int k, int n) { return T[t_index<kSwizzledT>(16 * j + k, 16 * j + n)]; }, 1, g, t4);
+        warp_mm16<kCvt>(acc, [&](int r, int k) { return a(16 * i + r, 16 * j + k); },
+                        [&](int k, int n) { return tt(16 * j + k, 16 * j + n); }, 1, g, t4);
         warp_store16(acc, 1.f, [&](int r, int n, float v0, float v1) {
             *reinterpret_cast<float2 *>(Ms + r * 16 + n) = make_float2(v0, v1); }, g, t4);
         __syncwarp();
         float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_mm16(acc2, [&](int r, int k) { return T[t_index<kSwizzledT>(16 * i + r, 16 * i + k)]; },
-                  [&](int k, int n) { return Ms[k * 16 + n]; }, 1, g, t4);
+        warp_mm16<kCvt>(acc2, [&](int r, int k) { return tt(16 * i + r, 16 * i + k); },
+                        [&](int k, int n) { return Ms[k * 16 + n]; }, 1, g, t4);
         warp_store16(acc2, -1.f, [&](int r, int n, float v0, float v1) {
             out.fin2(16 * i + r, 16 * j + n, v0, v1); }, g, t4);
     }
@@ -195,19 +236,19 @@ __device__ __forceinline__ void solve_merge64(const float *A, const SolveOut<kPa
     {   // M tile (rb, cb) = sum_{k = cb}^{1} A_{rb,k} T_{k,cb},  rb = 2 + w/2, cb = w%2
         const int rb = 2 + (warp >> 1), cb = warp & 1;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_mm16(acc, [&](int r, int k) { return a(16 * rb + r, 16 * cb + k); },
-                  [&](int k, int n) { return T[t_index<kSwizzledT>(16 * cb + k, 16 * cb + n)]; }, 2 - cb, g, t4);
+        warp_mm16<kCvt>(acc, [&](int r, int k) { return a(16 * rb + r, 16 * cb + k); },
+                        [&](int k, int n) { return tt(16 * cb + k, 16 * cb + n); }, 2 - cb, g, t4);
         float *Mt = M + 256 * warp;
         warp_store16(acc, 1.f, [&](int r, int n, float v0, float v1) {
-            *reinterpret_cast<float2 *>(Mt + r * 16 + n) = make_float2(v0, v1); }, g, t4);
+            *reinterpret_cast<float2 *>(Mt + r * 16 + n) = make_float2(rnd(v0), rnd(v1)); }, g, t4);
     }
     named_sync(bar_id, 128);
     {   // T_{rb,cb} = -sum_{k = 2}^{rb} T_{rb,k} M_{k,cb}
         const int rb = 2 + (warp >> 1), cb = warp & 1;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_mm16(acc, [&](int r, int k) { return T[t_index<kSwizzledT>(16 * rb + r, 32 + k)]; },
-                  [&](int k, int n) { return M[256 * (((k >> 4) << 1) | cb) + (k & 15) * 16 + n]; },
-                  rb - 1, g, t4);
+        warp_mm16<kCvt>(acc, [&](int r, int k) { return tt(16 * rb + r, 32 + k); },
+                        [&](int k, int n) { return M[256 * (((k >> 4) << 1) | cb) + (k & 15) * 16 + n]; },
+                        rb - 1, g, t4);
         warp_store16(acc, -1.f, [&](int r, int n, float v0, float v1) {
             out.fin2(16 * rb + r, 16 * cb + n, v0, v1); }, g, t4);
     }
