@@ -37,7 +37,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (128 chains) with half its head-tokens, and the kernel's traffic is proportional to
 # head-tokens, so the figure is twice the captured one.  Valid only while the kernel
 # sources hash to `src`; otherwise the bench reports null.
-TRAFFIC = {"chunk_fwd": {"bytes": 2 * (203593984 + 50276608), "src": "9fb528ecf7d1b64e"}}
+TRAFFIC = {"chunk_fwd": {"bytes": 2 * (203113472 + 50139648), "src": "c67fd0fdf39dca5f"}}
 
 
 def peaks():
