@@ -162,3 +162,62 @@ def step(q, k, v, log_alpha, beta, state, *, nthreads: int | None = None):
     if rc != 0:
         raise RuntimeError(f"oracle_step returned {rc}")
     return out, st
+
+
+# ---------------------------------------------------------------- neighbouring steps
+# The steps either side of the recurrence, for the library's fused entry points: q and k
+# L2-normalised per (b, t, h) vector (the workloads' recipe normalises them), beta taken as
+# the sigmoid of logits, and the output gate of the page "linear-attention gated-deltanet
+# guide" (section 4: a gate with a SiLU activation on what is read out), out = o * silu(z).
+# The pages print no epsilon for the normalisation; the reading is x / sqrt(|x|^2 + eps)
+# with eps = 1e-6.
+L2NORM_EPS = 1e-6
+
+
+def l2_normalize(x) -> np.ndarray:
+    """x / sqrt(|x|^2 + L2NORM_EPS) along the last axis, in float64."""
+    x = to_f64(x)
+    return x / np.sqrt((x * x).sum(axis=-1, keepdims=True) + L2NORM_EPS)
+
+
+def sigmoid(x) -> np.ndarray:
+    """1 / (1 + exp(-x)) in float64, without overflow for large |x|."""
+    x = to_f64(x)
+    e = np.exp(-np.abs(x))
+    return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def silu(x) -> np.ndarray:
+    """x * sigmoid(x) in float64."""
+    x = to_f64(x)
+    return x * sigmoid(x)
+
+
+def forward_fused(q, k, v, log_alpha, beta, init_state=None, *, qk_l2norm=False,
+                  beta_sigmoid=False, z=None, **kw):
+    """``forward`` with the neighbouring steps: q, k normalised first (qk_l2norm), beta
+    given as logits (beta_sigmoid), and the output multiplied by silu(z) (z given, in the
+    output's layout).  The final state is that of ``forward`` on the prepared inputs."""
+    q, k, beta = to_f64(q), to_f64(k), to_f64(beta)
+    if qk_l2norm:
+        q, k = l2_normalize(q), l2_normalize(k)
+    if beta_sigmoid:
+        beta = sigmoid(beta)
+    out, final = forward(q, k, v, log_alpha, beta, init_state, **kw)
+    if z is not None:
+        out = out * silu(z)
+    return out, final
+
+
+def step_fused(q, k, v, log_alpha, beta, state, *, qk_l2norm=False, beta_sigmoid=False,
+               z=None, **kw):
+    """``step`` with the same neighbouring steps as ``forward_fused``."""
+    q, k, beta = to_f64(q), to_f64(k), to_f64(beta)
+    if qk_l2norm:
+        q, k = l2_normalize(q), l2_normalize(k)
+    if beta_sigmoid:
+        beta = sigmoid(beta)
+    out, st = step(q, k, v, log_alpha, beta, state, **kw)
+    if z is not None:
+        out = out * silu(z)
+    return out, st

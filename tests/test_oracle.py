@@ -435,3 +435,112 @@ def test_planted_mistake_is_caught(mistake):
         if not err <= max(tol, 1e-12):
             failed.append(name)
     assert failed, f"no pin caught the planted mistake {mistake}"
+
+
+# ------------------------------------------------------------ neighbouring steps
+# Pins of the fused entry points' reference: each ties one neighbouring step to a fact
+# that does not restate its formula.
+def _raw_problem(seed, gate="scalar", T=20):
+    rng = np.random.default_rng(seed)
+    B, H, dk, dv = 1, 2, 8, 6
+    q = rng.standard_normal((B, T, H, dk))
+    k = rng.standard_normal((B, T, H, dk))
+    v = rng.standard_normal((B, T, H, dv))
+    b = rng.standard_normal((B, T, H))
+    la = -rng.uniform(0.0, 0.3, (B, T, H) if gate == "scalar" else (B, T, H, dk))
+    s0 = rng.standard_normal((B, H, dk, dv)) * 0.1
+    z = rng.standard_normal((B, T, H, dv))
+    return q, k, v, la, b, s0, z
+
+
+@pytest.mark.parametrize("gate", ["scalar", "channel"])
+def test_l2norm_scale_invariance(gate):
+    """Normalised keys and queries do not depend on the scale of the raw vectors (up to the
+    epsilon's relative effect, eps / (2 |x|^2) < 1e-6 here; a missing normalisation would
+    move the results by O(1))."""
+    q, k, v, la, b, s0, _ = _raw_problem(1, gate)
+    rng = np.random.default_rng(2)
+    cq = rng.uniform(0.5, 4.0, q.shape[:3] + (1,))
+    ck = rng.uniform(0.5, 4.0, k.shape[:3] + (1,))
+    o1, f1 = oracle.forward_fused(q, k, v, la, oracle.sigmoid(b), s0, qk_l2norm=True)
+    o2, f2 = oracle.forward_fused(q * cq, k * ck, v, la, oracle.sigmoid(b), s0, qk_l2norm=True)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-5)
+    np.testing.assert_allclose(f1, f2, rtol=0, atol=1e-5)
+
+
+def test_l2norm_leaves_unit_vectors():
+    """Unit vectors are (up to eps) left alone: normalised inputs give the plain forward."""
+    q, k, v, la, b, s0, _ = _raw_problem(3)
+    qu = q / np.linalg.norm(q, axis=-1, keepdims=True)
+    ku = k / np.linalg.norm(k, axis=-1, keepdims=True)
+    bb = oracle.sigmoid(b)
+    o1, f1 = oracle.forward_fused(qu, ku, v, la, bb, s0, qk_l2norm=True)
+    o2, f2 = oracle.forward(qu, ku, v, la, bb, s0)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-5)
+    np.testing.assert_allclose(f1, f2, rtol=0, atol=1e-5)
+
+
+def test_beta_logits_limits():
+    """Logits of -40, 0, +40 act as beta = 0, 1/2, 1 (no write, half write, full write)."""
+    q, k, v, la, _, s0, _ = _raw_problem(4)
+    for logit, beta in [(-40.0, 0.0), (0.0, 0.5), (40.0, 1.0)]:
+        bl = np.full(q.shape[:3], logit)
+        o1, f1 = oracle.forward_fused(q, k, v, la, bl, s0, beta_sigmoid=True)
+        o2, f2 = oracle.forward(q, k, v, la, np.full(q.shape[:3], beta), s0)
+        np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(f1, f2, rtol=0, atol=1e-12)
+
+
+def test_output_gate_identities():
+    """z = 0 closes the gate exactly; out(z) - out(-z) = o * z (an odd-part identity of
+    x * sigmoid(x)); a large z passes o * z; the state is never gated."""
+    q, k, v, la, b, s0, z = _raw_problem(5)
+    bb = oracle.sigmoid(b)
+    o, f = oracle.forward(q, k, v, la, bb, s0)
+    o0, f0 = oracle.forward_fused(q, k, v, la, bb, s0, z=np.zeros_like(z))
+    assert np.all(o0 == 0.0) and np.array_equal(f0, f)
+    op, _ = oracle.forward_fused(q, k, v, la, bb, s0, z=z)
+    om, _ = oracle.forward_fused(q, k, v, la, bb, s0, z=-z)
+    np.testing.assert_allclose(op - om, o * z, rtol=0, atol=1e-12)
+    ob, _ = oracle.forward_fused(q, k, v, la, bb, s0, z=np.full_like(z, 40.0))
+    np.testing.assert_allclose(ob, o * 40.0, rtol=1e-12, atol=1e-12)
+
+
+def test_step_fused_is_one_token_forward_fused():
+    q, k, v, la, b, s0, z = _raw_problem(6, "channel", T=1)
+    o1, f1 = oracle.forward_fused(q, k, v, la, b, s0, qk_l2norm=True, beta_sigmoid=True, z=z)
+    o2, f2 = oracle.step_fused(q[:, 0], k[:, 0], v[:, 0], la[:, 0], b[:, 0], s0,
+                               qk_l2norm=True, beta_sigmoid=True, z=z[:, 0])
+    np.testing.assert_allclose(o1[:, 0], o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(f1, f2, rtol=0, atol=1e-13)
+
+
+def _fused_with_mistake(mistake):
+    """A copy of oracle.forward_fused with one plausible mistake planted."""
+    def f(q, k, v, la, b, s0, *, qk_l2norm=False, beta_sigmoid=False, z=None):
+        q, k, b = oracle.to_f64(q), oracle.to_f64(k), oracle.to_f64(b)
+        if qk_l2norm:
+            q = oracle.l2_normalize(q)
+            if mistake != "normalise_q_only":
+                k = oracle.l2_normalize(k)
+        if beta_sigmoid:
+            b = oracle.sigmoid(-b) if mistake == "sigmoid_sign" else oracle.sigmoid(b)
+        out, fin = oracle.forward(q, k, v, la, b, s0)
+        if z is not None:
+            out = out * (oracle.sigmoid(z) if mistake == "gate_sigmoid" else oracle.silu(z))
+        return out, fin
+    return f
+
+
+@pytest.mark.parametrize("mistake", ["normalise_q_only", "sigmoid_sign", "gate_sigmoid"])
+def test_fused_pins_catch_planted_mistake(mistake, monkeypatch):
+    monkeypatch.setattr(oracle, "forward_fused", _fused_with_mistake(mistake))
+    pins = [lambda: test_l2norm_scale_invariance("scalar"), test_beta_logits_limits,
+            test_output_gate_identities]
+    failed = 0
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed >= 1, f"no pin caught {mistake}"
