@@ -28,6 +28,13 @@
 // chunk, TMA-loads the stored operands: D = S^T [W; Q*G]^T, E^T = U^T - (W S)^T,
 // S^T <- S^T Diag(G_C) + E^T (K*G_C/G), O^T = (Q*G S)^T + E^T P^T, with the operand
 // buffers of the next chunk refilled as soon as each is consumed.
+//
+// Fused neighbours (DR_FUSE_* of include/dr.h; page "linear-attention gated-deltanet
+// guide", section 4): the prep kernel computes 1 / |q_r| and 1 / |k_r| from the bf16 tiles
+// (threads 128..255, while threads 0..127 scan the gates) and scales every q and k value
+// as it converts it to fp32, so all the stored operands are those of the normalised rows;
+// it takes beta = sigmoid(logit).  The state kernel multiplies each output by silu(z), z's
+// tile arriving by TMA one chunk ahead.
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -76,7 +83,7 @@ constexpr uint32_t P1_LA = 32768;   // log alpha -> g log2(e): 4 boxes [64][32] 
 constexpr uint32_t P1_V = 65536, P1_KG = 81920;
 constexpr uint32_t P1_R = 98304;              // right factors: high [kb][16][64], low at +4096
 constexpr uint32_t P1_SMALL = 106496;         // beta[64], solve scratch[1024]
-constexpr uint32_t P1_TOTAL = P1_SMALL + 256 + 4096 + 512;   // + G_C[128]
+constexpr uint32_t P1_TOTAL = P1_SMALL + 256 + 4096 + 512 + 512;   // + G_C[128], row norms[128]
 // after the products: A over Q, T over K (and the first KB of g), T diag(beta) inside g,
 // the exact diagonal blocks over the right factors; staging of W and U at the end
 constexpr uint32_t P1_A = 0, P1_T = 16384, P1_TB = 34816, P1_XD = P1_R;
@@ -112,6 +119,7 @@ struct PrepArgs {
     KdaWorkspace ws;
     int *status;
     int T, H, NC;
+    uint32_t fuse;   // DR_FUSE_* bits
 };
 
 // Float index of element (t, c) of the [64][128] fp32 tile held as four 128-byte-swizzled
@@ -160,6 +168,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     float *sBeta = reinterpret_cast<float *>(sm + P1_SMALL);
     float *sM = sBeta + 64;
     float *sGamC = sM + 1024;   // G_C per channel
+    float *sInv = sGamC + 128;  // 1 / |x| of the rows of [Q; K] (1 unless normalised)
     float *LA = reinterpret_cast<float *>(sm + P1_LA);
     float *const Xd = reinterpret_cast<float *>(sm + P1_XD);   // exact diagonal blocks
     const int t_row = row & 63, blk = t_row >> 4;   // this thread's row of [Q; K]: token, block
@@ -168,6 +177,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     float *const sF = reinterpret_cast<float *>(sm + P1_V);        // [8][128] block factors
     float *const sExpRef = sF + 8 * 128;                           // [4][128] exp(ref_i)
     bool diag_exact = false;
+    float rinv = 1.f;   // 1 / |x| of this thread's row of [Q; K] (after the norms)
 
     if (tid == 0) {
         mbar_init(&bar_ld, 1);
@@ -203,8 +213,11 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         for (int bx = 0; bx < 4; ++bx)
             tma_load_4d(sm + P1_LA + bx * 8192, &tla, &bar_ld, 32 * bx, h, t0, b);
     }
-    if (tid < 64)
-        sBeta[tid] = tid < Lc ? __bfloat162float(a.beta[((size_t)b * a.T + t0 + tid) * a.H + h]) : 0.f;
+    if (tid < 64) {
+        float bt = tid < Lc ? __bfloat162float(a.beta[((size_t)b * a.T + t0 + tid) * a.H + h]) : 0.f;
+        if ((a.fuse & kFuseSigmoid) && tid < Lc) bt = sigmoid_f(bt);
+        sBeta[tid] = bt;
+    }
     if (!wait_cycles(&bar_ld, 0)) fail();
     __syncthreads();
     if (abort_s) goto done;
@@ -240,9 +253,34 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 sF[(i * (i - 1) / 2 + j) * 128 + tid] = __expf(v[16 * i + 15] - v[16 * j + 15]);
         sF[6 * 128 + tid] = 1.f;   // same block
         sF[7 * 128 + tid] = 0.f;   // row above the column block (entry masked)
+    } else {
+        // row norms of [Q; K] (thread 128 + i: row i; a quarter-warp's 16-byte loads of one
+        // logical group fall in eight different bank groups)
+        const int i = tid - 128;
+        float inv = 1.f;
+        if (a.fuse & kFuseL2) {
+            const unsigned char *src = sm + (i < 64 ? P1_Q : P1_K) + (i & 63) * 128;
+            float ss = 0.f;
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(src + kb * 8192 + 16 * (j ^ (i & 7)));
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+                        ss = fmaf(f.x, f.x, ss);
+                        ss = fmaf(f.y, f.y, ss);
+                    }
+                }
+            inv = rsqrtf(ss + kL2NormEps);
+        }
+        sInv[i] = inv;
     }
     __syncthreads();
     diag_exact = diag_exact_s != 0;
+    rinv = sInv[row];
 
     if (!four_rounds_s) {
         // ---- one product for the whole chunk against ref = g_63 (no channel decays by more
@@ -261,6 +299,8 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     const int c = 64 * half + 32 * p + 8 * i, w = 4 * (4 * p + i);
                     float x8[8], g8[8], gl[8], e8[8];
                     load8_bf16(xt, t_row, c >> 3, x8);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) x8[u] *= rinv;
                     load8_g(LA, t_row, c, g8);
                     load8_g(LA, 63, c, gl);
 #pragma unroll
@@ -336,6 +376,8 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 const int c = 64 * half + 8 * i;
                 float x8[8], g8[8], r8[8], e8[8];
                 load8_bf16(xt, t_row, c >> 3, x8);
+    #pragma unroll
+                for (int u = 0; u < 8; ++u) x8[u] *= rinv;
                 load8_g(LA, t_row, c, g8);
                 load8_g(LA, 16 * blk + 15, c, r8);
     #pragma unroll
@@ -380,6 +422,9 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 const int rr = tid >> 4, c8 = tid & 15, s = 16 * j + rr;
                 float k8[8], g8[8], rf[8];
                 load8_bf16(sm + P1_K, s, c8, k8);
+                const float ks = sInv[64 + s];
+    #pragma unroll
+                for (int u = 0; u < 8; ++u) k8[u] *= ks;
                 load8_g(LA, s, 8 * c8, g8);
                 load8_g(LA, ref, 8 * c8, rf);
                 uint32_t hi[4], lo[4];
@@ -411,6 +456,8 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                         } else {
                             float x8[8], g8[8], r8[8];
                             load8_bf16(xt, t_row, c >> 3, x8);
+    #pragma unroll
+                            for (int u = 0; u < 8; ++u) x8[u] *= rinv;
                             load8_g(LA, t_row, c, g8);
                             load8_g(LA, ref, c, r8);
     #pragma unroll
@@ -470,7 +517,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                         *reinterpret_cast<const __nv_bfloat16 *>(sm + P1_K + o + sw128_off(s, ch & 63)));
                     acc = fmaf(xr * ks, ex2(LA[la_idx(r, ch)] - LA[la_idx(s, ch)]), acc);
                 }
-            Xd[task] = acc;
+            Xd[task] = acc * sInv[part * 64 + r] * sInv[64 + s];
         }
     }
     __syncthreads();   // Q, K and g are dead from here on
@@ -591,7 +638,9 @@ constexpr uint32_t S2_ST = 147456;                           // S^T bf16 [128][1
 constexpr uint32_t S2_EH = 180224, S2_EL = 196608;           // E^T bf16 pair [128][64]
 constexpr uint32_t S2_SMALL = 212992;                        // G_C of two chunks
 constexpr uint32_t S2_TOTAL = S2_SMALL + 1024;
-static_assert(S2_TOTAL + 1024 <= 227 * 1024, "state layout");
+constexpr uint32_t S2_Z = S2_TOTAL;                          // output gate: z tile [64][128] bf16
+constexpr uint32_t S2_TOTAL_Z = S2_Z + 16384;
+static_assert(S2_TOTAL_Z + 1024 <= 227 * 1024, "state layout");
 // tensor memory: S^T, then two buffers of [(W S)^T | (QH S)^T + E^T P^T | (QL S)^T]
 constexpr uint32_t S2_TM_S = 0, S2_TM_D = 128, S2_TM_DSTRIDE = 192;
 
@@ -604,6 +653,7 @@ struct StateArgs {
     const float *gam;
     int *status;
     int T, H, NC;
+    bool zgate;   // multiply the outputs by silu(z)
 };
 
 // Per chunk c, in order (thread 0 issues the MMAs, thread 224 the TMA loads):
@@ -622,10 +672,11 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
                  const __grid_constant__ CUtensorMap mql, const __grid_constant__ CUtensorMap mkh,
                  const __grid_constant__ CUtensorMap mkl, const __grid_constant__ CUtensorMap mph,
                  const __grid_constant__ CUtensorMap mpl, const __grid_constant__ CUtensorMap mu,
-                 const __grid_constant__ CUtensorMap to, const StateArgs a) {
+                 const __grid_constant__ CUtensorMap to, const __grid_constant__ CUtensorMap tz,
+                 const StateArgs a) {
     extern __shared__ unsigned char dsm_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
-    __shared__ uint64_t bar_w, bar_q, bar_u, bar_k, bar_p[2], bar_dw, bar_s, bar_pe;
+    __shared__ uint64_t bar_w, bar_q, bar_u, bar_k, bar_p[2], bar_dw, bar_s, bar_pe, bar_z;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
 
@@ -639,7 +690,7 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
 
     if (tid == 0) {
         uint64_t *bars[] = {&bar_w, &bar_q, &bar_u, &bar_k, &bar_p[0], &bar_p[1],
-                            &bar_dw, &bar_s, &bar_pe};
+                            &bar_dw, &bar_s, &bar_pe, &bar_z};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         abort_s = 0;
         fence_mbar_init();
@@ -678,11 +729,21 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
 
     const int64_t n0 = (int64_t)bh * a.NC;   // first chunk of this chain in the workspace
     auto rowc = [&](int c) { return (int)((n0 + c) * 64); };
+    // (TMA thread) loads issued per barrier: w, q, u, k, p[0], p[1], z -- on an abort it
+    // waits (bounded) for the last phase of each
+    int issued[7] = {0, 0, 0, 0, 0, 0, 0};
+    auto load_z = [&](int c) {
+        ++issued[6];
+        mbar_arrive_expect_tx(&bar_z, 16384);
+        for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + S2_Z + kb * 8192, &tz, &bar_z, 64 * kb, h, c * 64, b);
+    };
     auto load_w = [&](int c) {
+        ++issued[0];
         mbar_arrive_expect_tx(&bar_w, 16384);
         for (int kb = 0; kb < 2; ++kb) tma_load_2d(sm + S2_WQ + kb * S2_WQ_KB, &mw, &bar_w, 64 * kb, rowc(c));
     };
     auto load_q = [&](int c) {
+        ++issued[1];
         mbar_arrive_expect_tx(&bar_q, 32768);
         for (int kb = 0; kb < 2; ++kb) {
             tma_load_2d(sm + S2_WQ + kb * S2_WQ_KB + 8192, &mqh, &bar_q, 64 * kb, rowc(c));
@@ -690,10 +751,12 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         }
     };
     auto load_u = [&](int c) {
+        ++issued[2];
         mbar_arrive_expect_tx(&bar_u, 32768);
         for (int bx = 0; bx < 4; ++bx) tma_load_2d(sm + S2_U + bx * 8192, &mu, &bar_u, 32 * bx, rowc(c));
     };
     auto load_k = [&](int c) {
+        ++issued[3];
         mbar_arrive_expect_tx(&bar_k, 32768);
         for (int kb = 0; kb < 2; ++kb) {
             tma_load_2d(sm + S2_KH + kb * 8192, &mkh, &bar_k, 64 * kb, rowc(c));
@@ -702,6 +765,7 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
     };
     auto load_p = [&](int c) {
         uint64_t *bb = &bar_p[c & 1];
+        ++issued[4 + (c & 1)];
         unsigned char *dst = sm + S2_P + (c & 1) * 16384;
         mbar_arrive_expect_tx(bb, 16384);
         tma_load_2d(dst, &mph, bb, 0, rowc(c));
@@ -714,6 +778,7 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         load_k(0);
         load_p(0);
         if (a.NC > 1) load_p(1);
+        if (a.zgate) load_z(0);
     }
     if (tid < 128 && a.NC > 0) cp_async4(sGam + tid, a.gam + n0 * 128 + tid, 4);
     cp_async_commit();
@@ -726,12 +791,22 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         tmem_ld32(tm + S2_TM_D + S2_TM_DSTRIDE * (c & 1) + 128 + 32 * half, pe);
         tmem_wait_ld();
         const int j = row;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) o[u] += pe[u];
+        if (a.zgate) {
+            if (!wait_cycles(&bar_z, c & 1)) fail();
+            const unsigned char *zt = sm + S2_Z + (j >> 6) * 8192;
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                o[u] *= silu_f(__bfloat162float(
+                    *reinterpret_cast<const __nv_bfloat16 *>(zt + sw128_off(32 * half + u, j & 63))));
+        }
         if (sizeof(Tout) == 2) {
             unsigned char *dst = sm + S2_ST + (j >> 6) * 8192;
 #pragma unroll
             for (int u = 0; u < 32; ++u)
                 *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * half + u, j & 63)) =
-                    __float2bfloat16_rn(o[u] + pe[u]);
+                    __float2bfloat16_rn(o[u]);
         } else {
             unsigned char *dst = sm + S2_ST + (j >> 5) * 8192;
             const int cj = j & 31;
@@ -739,12 +814,13 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
             for (int u = 0; u < 32; ++u) {
                 const int r = 32 * half + u;
                 *reinterpret_cast<float *>(dst + r * 128 + ((((cj >> 2) ^ (r & 7)) & 7) << 4) +
-                                           ((cj & 3) << 2)) = o[u] + pe[u];
+                                           ((cj & 3) << 2)) = o[u];
             }
         }
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
+        if (tid == kTmaThread && a.zgate && c + 1 < a.NC) load_z(c + 1);   // the z tile is read
         if (tid == 0) {
             constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
 #pragma unroll
@@ -903,6 +979,11 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
     }
     cp_async_wait_all();
     if (tid == 0 && store_outstanding) bulk_wait_all();
+    if (abort_s && tid == kTmaThread) {
+        uint64_t *lbars[7] = {&bar_w, &bar_q, &bar_u, &bar_k, &bar_p[0], &bar_p[1], &bar_z};
+        for (int i = 0; i < 7; ++i)
+            if (issued[i] > 0) wait_cycles(lbars[i], (uint32_t)(issued[i] - 1) & 1);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -967,10 +1048,12 @@ size_t chunk_kda_workspace_bytes(const ChunkProblem &p) {
 int launch_chunk_kda(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream) {
     const int64_t nch = p.B * p.H * p.NC;
     const KdaWorkspace ws = kda_carve(workspace, nch);
-    CUtensorMap tq, tk, tv, tla, to;
+    CUtensorMap tq, tk, tv, tla, to, tz;
+    const bool zgate = (p.fuse & kFuseGate) != 0;
     if (!map4(&tq, p.q, p.B, p.T, p.H, 2, true) || !map4(&tk, p.k, p.B, p.T, p.H, 2, true) ||
         !map4(&tv, p.v, p.B, p.T, p.H, 2, true) || !map4(&tla, p.log_alpha, p.B, p.T, p.H, 4, true) ||
-        !map4(&to, p.out, p.B, p.T, p.H, p.out_bf16 ? 2 : 4, true))
+        !map4(&to, p.out, p.B, p.T, p.H, p.out_bf16 ? 2 : 4, true) ||
+        !map4(&tz, zgate ? p.z : p.q, p.B, p.T, p.H, 2, true))   // (unused unless gated)
         return kErrCuda;
     CUtensorMap mw, mqh, mql, mkh, mkl, mph, mpl, mu;
     const int64_t rows = nch * 64;
@@ -980,25 +1063,26 @@ int launch_chunk_kda(const ChunkProblem &p, void *workspace, int *status_word, c
         !map2(&mpl, ws.PL, rows, 64, 2, true) || !map2(&mu, ws.U, rows, 128, 4, false))
         return kErrCuda;
 
-    const int s1 = (int)P1_TOTAL + 1024, s2 = (int)S2_TOTAL + 1024;
+    const int s1 = (int)P1_TOTAL + 1024, s2 = (int)(zgate ? S2_TOTAL_Z : S2_TOTAL) + 1024;
+    const int s2max = (int)S2_TOTAL_Z + 1024;
     if (cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, s1) != cudaSuccess)
         return kErrCuda;
-    PrepArgs pa{(const __nv_bfloat16 *)p.beta, ws, status_word, (int)p.T, (int)p.H, p.NC};
+    PrepArgs pa{(const __nv_bfloat16 *)p.beta, ws, status_word, (int)p.T, (int)p.H, p.NC, p.fuse};
     kda_prep_kernel<<<(unsigned)nch, kThreads, s1, stream>>>(tq, tk, tv, tla, mw, mu, pa);
     if (cudaGetLastError() != cudaSuccess) return kErrCuda;
 
-    StateArgs sa{p.init_state, p.final_state, ws.GAM, status_word, (int)p.T, (int)p.H, p.NC};
+    StateArgs sa{p.init_state, p.final_state, ws.GAM, status_word, (int)p.T, (int)p.H, p.NC, zgate};
     const unsigned grid = (unsigned)(p.B * p.H);
     if (p.out_bf16) {
         if (cudaFuncSetAttribute(kda_state_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 s2) != cudaSuccess)
+                                 s2max) != cudaSuccess)
             return kErrCuda;
-        kda_state_kernel<__nv_bfloat16><<<grid, kThreads, s2, stream>>>(mw, mqh, mql, mkh, mkl, mph, mpl, mu, to, sa);
+        kda_state_kernel<__nv_bfloat16><<<grid, kThreads, s2, stream>>>(mw, mqh, mql, mkh, mkl, mph, mpl, mu, to, tz, sa);
     } else {
-        if (cudaFuncSetAttribute(kda_state_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, s2) !=
+        if (cudaFuncSetAttribute(kda_state_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, s2max) !=
             cudaSuccess)
             return kErrCuda;
-        kda_state_kernel<float><<<grid, kThreads, s2, stream>>>(mw, mqh, mql, mkh, mkl, mph, mpl, mu, to, sa);
+        kda_state_kernel<float><<<grid, kThreads, s2, stream>>>(mw, mqh, mql, mkh, mkl, mph, mpl, mu, to, tz, sa);
     }
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }

@@ -18,7 +18,14 @@ struct ChunkProblem {
     int64_t B, T, H;
     int dk, dv, C, NC, gate;
     bool in_bf16, out_bf16;
+    // fused neighbours (DR_FUSE_* bits of include/dr.h) and the output gate's input
+    // [B, T, H, dv] in the input dtype (NULL unless the output gate is fused)
+    uint32_t fuse;
+    const void *z;
 };
+
+// DR_FUSE_* bits (include/dr.h)
+constexpr uint32_t kFuseL2 = 1, kFuseSigmoid = 2, kFuseGate = 4;
 
 // fp32 intermediates of the two-kernel CUDA-core path, one slab per (b, h, chunk) n:
 //   W  [n][C][dk]   T diag(beta) (K*G)
@@ -69,7 +76,7 @@ bool chunk_kda_supported(const ChunkProblem &p);
 size_t chunk_kda_workspace_bytes(const ChunkProblem &p);
 int launch_chunk_kda(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream);
 int launch_decode(int64_t BH, int dk, int dv, int in_bf16, int out_bf16, int gate,
-                  const void *q, const void *k, const void *v, const float *la,
-                  const void *beta, float *state, void *out, cudaStream_t s);
+                  uint32_t fuse, const void *q, const void *k, const void *v, const float *la,
+                  const void *beta, const void *z, float *state, void *out, cudaStream_t s);
 
 }  // namespace dr

@@ -27,6 +27,10 @@
 // one holding s (s <= p < r):  exp(g_r - ref_i) * exp(ref_i - ref_j) * exp(ref_j - g_s),
 // ref_j = g_{16 j - 1} (0 for j = 0), so no product divides by a tiny cumulative decay
 // (the log-space, two-level chunking remedy named on the "Transformer notes (5)" page).
+//
+// Fused neighbours (DR_FUSE_* of include/dr.h): the prep kernel takes beta = sigmoid(logit)
+// and divides each q and k row by its norm as soon as the rows are in shared memory (fp32);
+// the state kernel multiplies each output by silu(z).
 #include "common.cuh"
 #include "chunk_layout.h"
 
@@ -45,6 +49,7 @@ struct PrepArgs {
     const void *beta;
     int64_t B, T, H;
     int dv, C, NC, gate;
+    uint32_t fuse;
     ChunkWorkspace ws;
 };
 
@@ -52,13 +57,15 @@ struct StateArgs {
     const float *init_state;
     void *out;
     float *final_state;
+    const void *z;   // output gate input (in_bf16 ? bf16 : fp32), NULL when not fused
+    bool z_bf16;
     int64_t B, T, H;
     int dv, C, NC;
     ChunkWorkspace ws;
 };
 
 size_t prep_smem_bytes(int dk) {
-    return sizeof(float) * (size_t)(3 * 64 * kLd + 64 * dk + 16 * dk + 2 * 64 * kLdA + 64 + 64 + 1024);
+    return sizeof(float) * (size_t)(3 * 64 * kLd + 64 * dk + 16 * dk + 2 * 64 * kLdA + 64 + 64 + 1024 + 64);
 }
 
 // out(r, n) (r, n < 16) = sum_{k < 16 nk} L(r, k) R(k, n) by one warp in fp32; lane owns row
@@ -150,6 +157,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
     float *sB = sT + 64 * kLdA;                    // [64] beta
     float *sg = sB + 64;                           // [64] cumulative log decay (scalar)
     float *sM = sg + 64;                           // [1024] scratch of the blocked solve
+    float *sNk = sM + 1024;                        // [64] 1 / |k_r| (1 unless normalised)
 
     const Tin *q = (const Tin *)a.q, *k = (const Tin *)a.k, *v = (const Tin *)a.v;
     const Tin *beta = (const Tin *)a.beta;
@@ -164,7 +172,12 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
     auto tok = [&](int r) -> int64_t { return (b * a.T + t0 + r) * a.H + h; };
 
     // 1. beta and the cumulative log decay (padded rows: beta = 0, log a = 0).
-    for (int r = tid; r < C; r += kThreads) sB[r] = r < Lc ? to_f32(beta[tok(r)]) : 0.f;
+    const bool l2 = (a.fuse & kFuseL2) != 0;
+    for (int r = tid; r < C; r += kThreads) {
+        float br = r < Lc ? to_f32(beta[tok(r)]) : 0.f;
+        if ((a.fuse & kFuseSigmoid) && r < Lc) br = sigmoid_f(br);
+        sB[r] = br;
+    }
     if (gate == 2) {
         // stage the chunk's log alpha rows (coalesced, all loads in flight), then scan
         for (int idx = tid; idx < C * (DK / 4); idx += kThreads) {
@@ -200,6 +213,31 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
         *reinterpret_cast<float4 *>(sQ + r * kLd + c4) = qq;
     }
     __syncthreads();
+    //    L2-normalised rows: four threads per row, each a quarter of the channels.
+    {
+        const int r = tid >> 2, part = tid & 3;
+        float nk = 1.f;
+        if (l2) {
+            float sk2 = 0.f, sq2 = 0.f;
+            for (int ch = part * (DK / 4); ch < (part + 1) * (DK / 4); ++ch) {
+                sk2 = fmaf(sK[r * kLd + ch], sK[r * kLd + ch], sk2);
+                sq2 = fmaf(sQ[r * kLd + ch], sQ[r * kLd + ch], sq2);
+            }
+            sk2 += __shfl_xor_sync(0xffffffffu, sk2, 1);
+            sq2 += __shfl_xor_sync(0xffffffffu, sq2, 1);
+            sk2 += __shfl_xor_sync(0xffffffffu, sk2, 2);
+            sq2 += __shfl_xor_sync(0xffffffffu, sq2, 2);
+            nk = rsqrtf(sk2 + kL2NormEps);
+            const float nq = rsqrtf(sq2 + kL2NormEps);
+            if (r < C)
+                for (int ch = part * (DK / 4); ch < (part + 1) * (DK / 4); ++ch) {
+                    sK[r * kLd + ch] *= nk;
+                    sQ[r * kLd + ch] *= nq;
+                }
+        }
+        if (part == 0 && r < C) sNk[r] = nk;
+        if (l2) __syncthreads();
+    }
 
     auto G = [&](int r, int ch) -> float { return gate == 2 ? sG[r * DK + ch] : sg[r]; };
 
@@ -310,7 +348,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
     // 6. W = T diag(b) (K*G):  rows b_s k_s exp(g_s) (exponent <= 0), k reloaded raw.
     for (int idx = tid; idx < C * DK; idx += kThreads) {
         const int s = idx / DK, ch = idx % DK;
-        sR[s * kLd + ch] = s < Lc ? sB[s] * to_f32(k[tok(s) * DK + ch]) * expf(G(s, ch)) : 0.f;
+        sR[s * kLd + ch] = s < Lc ? sB[s] * sNk[s] * to_f32(k[tok(s) * DK + ch]) * expf(G(s, ch)) : 0.f;
     }
     __syncthreads();
     for (int idx = tid; idx < C * DK; idx += kThreads) {
@@ -419,7 +457,13 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(StateArgs a) {
             if (r < C) {
                 float acc = o[m];
                 for (int s = 0; s <= r; ++s) acc += sP[r * kLdA + s] * sE[s * kDvt + j];
-                if (r < Lc) out[((b * a.T + t0 + r) * a.H + h) * dv + col] = from_f32<Tout>(acc);
+                if (r < Lc) {
+                    const int64_t oi = ((b * a.T + t0 + r) * a.H + h) * dv + col;
+                    if (a.z)
+                        acc *= silu_f(a.z_bf16 ? to_f32(((const __nv_bfloat16 *)a.z)[oi])
+                                               : ((const float *)a.z)[oi]);
+                    out[oi] = from_f32<Tout>(acc);
+                }
             }
         }
         // S <- Diag(G_C) S + (K*G_C/G)^T E.
@@ -454,8 +498,9 @@ int launch_simt_t(const PrepArgs &pa, const StateArgs &sa, cudaStream_t stream) 
 }  // namespace
 
 int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStream_t stream) {
-    PrepArgs pa{p.q, p.k, p.v, p.log_alpha, p.beta, p.B, p.T, p.H, p.dv, p.C, p.NC, p.gate, ws};
-    StateArgs sa{p.init_state, p.out, p.final_state, p.B, p.T, p.H, p.dv, p.C, p.NC, ws};
+    PrepArgs pa{p.q, p.k, p.v, p.log_alpha, p.beta, p.B, p.T, p.H, p.dv, p.C, p.NC, p.gate, p.fuse, ws};
+    StateArgs sa{p.init_state, p.out, p.final_state, (p.fuse & kFuseGate) ? p.z : nullptr, p.in_bf16,
+                 p.B, p.T, p.H, p.dv, p.C, p.NC, ws};
     using bf = __nv_bfloat16;
     const bool ib = p.in_bf16, ob = p.out_bf16;
     if (p.dk == 128) {

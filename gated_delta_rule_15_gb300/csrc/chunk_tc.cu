@@ -42,6 +42,18 @@
 // layout, and the V and K tiles also serve as MN-major operands directly.  Every wait is
 // bounded by a cycle budget: on expiry the kernel records DR_ERR_TIMEOUT in the status
 // word, drains its own copies and MMAs (with the same bound), frees TMEM and returns.
+//
+// Fused neighbours (DR_FUSE_* of include/dr.h: L2-normalised q and k, beta from logits, the
+// SiLU output gate of the Gated DeltaNet layer, page "linear-attention gated-deltanet
+// guide", section 4).  Every product above is bilinear in the rows of Q and K, so with
+// nq_r = 1 / |q_r| and nk_r = 1 / |k_r| (computed from the bf16 tiles in shared memory, two
+// threads per row) the normalisation folds into scalings the kernel already applies in
+// fp32 and the tiles stay as loaded: X's entries get nq_r nk_s or nk_r nk_s in the P and A
+// builds, T diag(beta G) becomes T diag(beta G nk), diag(delta) becomes diag(delta nk) and
+// the output's G_r becomes G_r nq_r.  The gate warp takes beta = sigmoid(logit); the output
+// warps multiply by silu(z).  z's tile is prefetched into L2 with the chunk's q, k, v and
+// copied by TMA into the stage's V slot as soon as the state update has read that slot
+// (the MMA warp waits for it), which is before the output step needs it.
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -79,7 +91,12 @@ constexpr uint32_t SM_P = SM_A + 16384;       // the next chunk's P high | P low
                                               // its E^T P^T)
 constexpr uint32_t SM_SMALL = SM_P + 16384;   // gate vectors of two chunks, solve scratch
 constexpr uint32_t SM_TOTAL = SM_SMALL + 8192;
-static_assert(SM_TOTAL + 1024 <= 227 * 1024, "layout");
+// fused neighbours only: norm vectors of two chunks [2][5][64] (nq, nk, G nk, delta nk,
+// G nq)
+constexpr uint32_t SM_NRM = SM_TOTAL;
+constexpr uint32_t SM_TOTAL_FUSED = SM_NRM + 2560;
+static_assert(SM_TOTAL_FUSED + 1024 <= 227 * 1024, "layout");
+enum { NV_NQ = 0, NV_NK = 1, NV_GK = 2, NV_DK = 3, NV_GQ = 4 };
 constexpr uint32_t TM_S = 0, TM_D = 128, TM_X = 256, TM_U = 320, TM_W = 384, TM_PE = 448;
 // TM_D: [ (W S)^T | (Q S)^T ];  TM_X: [Q; K] K^T;  TM_PE: E^T P^T
 // Largest in-chunk log-decay span for which exp(g_r - g_s) is formed as a product of two
@@ -98,6 +115,7 @@ struct TcArgs {
     float *final_state;
     int *status;
     int T, H, NC;
+    uint32_t fuse;   // DR_FUSE_* bits
     // Sequence segments (few long chains): role 0 runs whole sequences; role 1 runs each
     // segment twice without outputs -- from S_0 = 0 (end state to ws_s0) and as the
     // transition from S_0 = I with no value term (to ws_phi); role 2 reruns each segment
@@ -110,14 +128,14 @@ template <typename Tout, int GATE>
 __global__ void __launch_bounds__(kCtaThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
-                const TcArgs a) {
+                const __grid_constant__ CUtensorMap tz, const TcArgs a) {
     extern __shared__ unsigned char dsm_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
     // mbarriers: TMA stages; per MMA group its completion (committed by the MMA warp) and,
     // for the groups whose operands the compute warps write, "operands ready" (full_*,
     // arrived by thread 0 after the compute warps' barrier).  Each completes once per chunk.
     __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_q, bar_s, bar_pe;
-    __shared__ uint64_t full_x, full_uw, full_d, full_s;
+    __shared__ uint64_t full_x, full_uw, full_d, full_s, bar_z;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s, factored_s[2];
 
@@ -163,10 +181,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     // raw gate words of two chunks: [slot][beta word | log alpha][64 tokens]
     uint32_t *sGate = reinterpret_cast<uint32_t *>(sVec + 1792);
     constexpr int kOutBoxes = sizeof(Tout) == 2 ? 2 : 4;   // 128-byte rows per output box
+    const bool l2 = (a.fuse & kFuseL2) != 0;
+    const bool zgate = (a.fuse & kFuseGate) != 0 && outputs;
+    // norm vectors of chunk `it` (set it % 2)
+    auto nvec = [&](int it, int k) { return reinterpret_cast<float *>(sm + SM_NRM) + (it & 1) * 320 + 64 * k; };
 
     if (tid == 0) {
         uint64_t *bars[] = {&bar_tma[0], &bar_tma[1], &bar_x, &bar_uw, &bar_d, &bar_q, &bar_s,
-                            &bar_pe, &full_x, &full_uw, &full_d, &full_s};
+                            &bar_pe, &full_x, &full_uw, &full_d, &full_s, &bar_z};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         abort_s = 0;
         fence_mbar_init();
@@ -203,7 +225,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             tma_load_4d(st + kb * 16384, &tq, &bar_tma[s], 64 * kb, h, t0, b);
             tma_load_4d(st + kb * 16384 + OFF_K0, &tk, &bar_tma[s], 64 * kb, h, t0, b);
             tma_load_4d(st + OFF_V0 + kb * 8192, &tv, &bar_tma[s], 64 * kb, h, t0, b);
+            if (zgate) tma_prefetch_4d(&tz, 64 * kb, h, t0, b);
         }
+    };
+    auto issue_z = [&](int it) {   // (MMA warp) chunk `it`'s output gate input into its V slot
+        mbar_arrive_expect_tx(&bar_z, 16384);
+        const int t0 = (c_begin + it) * 64;
+        for (int kb = 0; kb < 2; ++kb)
+            tma_load_4d(stage(it) + OFF_V0 + kb * 8192, &tz, &bar_z, 64 * kb, h, t0, b);
     };
     // beta (the aligned 32-bit word holding it) and log alpha of chunk `it`, two tokens per
     // lane of the gate warp, copied asynchronously two chunks ahead; one commit group per
@@ -246,6 +275,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             const uint32_t wd = gw[r];
             const uint16_t hb = (uint16_t)(((2 * tok) & 2) ? (wd >> 16) : (wd & 0xffffu));
             bt[e] = __bfloat162float(__ushort_as_bfloat16(hb));
+            if (a.fuse & kFuseSigmoid) bt[e] = t < a.T ? sigmoid_f(bt[e]) : 0.f;
             l[e] = __uint_as_float(gw[64 + r]);
         }
         __syncwarp();
@@ -274,6 +304,41 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
         if (lane == 0) factored_s[it & 1] = fac;
     };
+    // (compute warps, fused L2 norm) wait for chunk `it`'s tiles, then 1 / |q_r| and
+    // 1 / |k_r| and their products with the chunk's gate vectors into norm set it % 2.  Row
+    // 128-byte halves: thread (row tid / 2, K-block tid % 2), the K-block 1 thread starting
+    // four 16-byte groups further so that each quarter-warp's loads hit eight bank groups.
+    auto norms = [&](int it) {
+        wait_bar(&bar_tma[it & 1], (it >> 1) & 1);
+        const int rq = tid >> 1, kb = tid & 1, r = rq & 63;
+        const unsigned char *src = stage(it) + (rq < 64 ? 0 : OFF_K0) + kb * 16384 + r * 128;
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int cg = ((j + 4 * kb) & 7) ^ (r & 7);
+            const uint4 u = *reinterpret_cast<const uint4 *>(src + 16 * cg);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+                ss = fmaf(f.x, f.x, ss);
+                ss = fmaf(f.y, f.y, ss);
+            }
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        const float inv = rsqrtf(ss + kL2NormEps);
+        if (kb == 0) {
+            const float gr = vec(it, 1)[r];
+            if (rq < 64) {
+                nvec(it, NV_NQ)[r] = inv;
+                nvec(it, NV_GQ)[r] = gr * inv;
+            } else {
+                nvec(it, NV_NK)[r] = inv;
+                nvec(it, NV_GK)[r] = gr * inv;
+                nvec(it, NV_DK)[r] = vec(it, 2)[r] * inv;
+            }
+        }
+    };
     // (MMA warp) wait for chunk `it`'s tiles, then X = [Q; K] K^T into TM_X
     auto issue_x = [&](int it) {
         if (!wait_cycles(&bar_tma[it & 1], (it >> 1) & 1)) fail();
@@ -298,6 +363,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const int c0 = 32 * col_half;
         const int r = quarter < 2 ? row : row - 64;
         const float *sG = vec(it, 0), *sBeta = vec(it, 3), *sE = vec(it, 4), *sF = vec(it, 5);
+        if (l2) {   // x_rs nq_r nk_s (P rows) or nk_r nk_s (A rows)
+            const float *nk = nvec(it, NV_NK);
+            const float rs = rows_a ? nk[r] : nvec(it, NV_NQ)[r];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 n4 = *reinterpret_cast<const float4 *>(nk + c0 + 4 * q);
+                x[4 * q] *= rs * n4.x; x[4 * q + 1] *= rs * n4.y;
+                x[4 * q + 2] *= rs * n4.z; x[4 * q + 3] *= rs * n4.w;
+            }
+        }
         float dec[32];   // exp(g_r - g_s), s = c0 + u
         if (factored_s[it & 1]) {
             const float er = sE[r];
@@ -353,7 +428,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     auto solve = [&](int it) {
         solve_unit_lower64<true, true>(reinterpret_cast<const float *>(sm + SM_A),
                                        reinterpret_cast<float *>(sm + SM_T), sM, sm + SM_TB,
-                                       vec(it, 3), vec(it, 1), tid);
+                                       vec(it, 3), l2 ? nvec(it, NV_GK) : vec(it, 1), tid);
     };
 
     // prologue loads: stages 0 and 1, raw gates of chunks 0 and 1
@@ -440,6 +515,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                                      desc_add(dK0, pb[part] + ks * 32), ID_KK_N64, (part | ks) != 0);
                 mma_commit(&bar_pe);
                 last = &bar_pe; last_par = par;
+                if (zgate) {   // the V slot is dead once the state update has read it
+                    if (!wait_cycles(&bar_s, par)) { fail(); break; }
+                    issue_z(it);
+                    last = &bar_z; last_par = par;
+                }
                 // the next chunk's U/W, then the chunk after's X
                 if (it + 1 < n_it) {
                     if (!wait_cycles(&full_uw, (it + 1) & 1)) { fail(); break; }
@@ -454,7 +534,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     last = &bar_x; last_par = it & 1;
                 }
             }
-            if (abort_s) wait_cycles(last, last_par);   // drain this warp's MMAs (bounded)
+            if (abort_s) {   // drain this warp's MMAs and copies (bounded)
+                wait_cycles(last, last_par);
+                if (last == &bar_z) wait_cycles(&bar_pe, last_par);
+            }
         }
         __syncwarp();
     } else {
@@ -476,6 +559,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         // prologue: chunk 0's gates, A and P, solve; chunk 1's gates
         if (warp == kGateWarp) scan_gates(0);
         named_sync(1, kThreads);
+        if (l2) {
+            norms(0);
+            named_sync(1, kThreads);
+        }
         wait_bar(&bar_x, 0);
         build_pa(0, true, half);
         if (outputs) build_pa(0, false, half);
@@ -541,6 +628,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
         // ---- 3. A of the next chunk (its X arrived meanwhile)
         if (next) {
+            if (l2) {
+                norms(it + 1);
+                named_sync(1, kThreads);
+            }
             wait_bar(&bar_x, (it + 1) & 1);
             build_pa(it + 1, true, half);
         }
@@ -548,7 +639,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         // ---- 4. E^T = U^T - (W S)^T, and E^T diag(delta)  (bf16 high/low pairs)
         wait_bar(&bar_d, par);
         {
-            const float *sDel = vec(it, 2);
+            const float *sDel = l2 ? nvec(it, NV_DK) : vec(it, 2);
             float ws[32], uu[32];
             tmem_ld32(tm + TM_D + 32 * half, ws);
             tmem_ld32(tm + TM_U + 32 * half, uu);
@@ -589,7 +680,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         //         tiles, dead once E^T P^T is done) and the next chunk's P (E^T P^T has read
         //         SM_P)
         const SolveOut<true, true, true> sout{reinterpret_cast<float *>(sm + SM_T), sm + SM_TB, vec(it + 1, 3),
-                                        vec(it + 1, 1)};
+                                              l2 ? nvec(it + 1, NV_GK) : vec(it + 1, 1)};
         if (next) {
             wait_bar(&bar_q, par);
             solve_diag64(reinterpret_cast<const float *>(sm + SM_A), sout, tid);
@@ -601,7 +692,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             wait_bar(&bar_pe, par);
             if (outputs) {
                 const int j = row;   // value channel; all 64 tokens of this lane
-                const float *sGam = vec(it, 1);
+                const float *sGam = l2 ? nvec(it, NV_GQ) : vec(it, 1);
+                if (zgate) wait_bar(&bar_z, it & 1);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     float o[32], pe[32];
@@ -610,6 +702,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     tmem_wait_ld();
 #pragma unroll
                     for (int u = 0; u < 32; ++u) o[u] = fmaf(sGam[32 * hh + u], o[u], pe[u]);
+                    if (zgate) {
+                        const unsigned char *zt = st + OFF_V0 + (j >> 6) * 8192;
+#pragma unroll
+                        for (int u = 0; u < 32; ++u)
+                            o[u] *= silu_f(__bfloat162float(
+                                *reinterpret_cast<const __nv_bfloat16 *>(zt + sw128_off(32 * hh + u, j & 63))));
+                    }
                     if (sizeof(Tout) == 2) {
                         unsigned char *dst = st + (j >> 6) * 16384;
 #pragma unroll
@@ -749,12 +848,13 @@ bool make_map(CUtensorMap *m, const void *base, int64_t B, int64_t T, int64_t H,
 
 template <typename Tout, int GATE>
 int launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-             const CUtensorMap &mo, const TcArgs &ta, unsigned grid, cudaStream_t stream) {
-    const int smem = (int)SM_TOTAL + 1024;
+             const CUtensorMap &mo, const CUtensorMap &mz, const TcArgs &ta, unsigned grid,
+             cudaStream_t stream) {
+    const int smem = (int)(ta.fuse ? SM_TOTAL_FUSED : SM_TOTAL) + 1024;
     if (cudaFuncSetAttribute(chunk_tc_kernel<Tout, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
+                             (int)SM_TOTAL_FUSED + 1024) != cudaSuccess)
         return kErrCuda;
-    chunk_tc_kernel<Tout, GATE><<<grid, kCtaThreads, smem, stream>>>(mq, mk, mv, mo, ta);
+    chunk_tc_kernel<Tout, GATE><<<grid, kCtaThreads, smem, stream>>>(mq, mk, mv, mo, mz, ta);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
@@ -788,19 +888,21 @@ size_t chunk_tc_workspace_bytes(const ChunkProblem &p) {
 }
 
 int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream) {
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv, mo, mz;
+    const bool zgate = (p.fuse & kFuseGate) != 0;
     if (!make_map(&mq, p.q, p.B, p.T, p.H, false) || !make_map(&mk, p.k, p.B, p.T, p.H, false) ||
         !make_map(&mv, p.v, p.B, p.T, p.H, false) ||
-        !make_map(&mo, p.out, p.B, p.T, p.H, !p.out_bf16))
+        !make_map(&mo, p.out, p.B, p.T, p.H, !p.out_bf16) ||
+        !make_map(&mz, zgate ? p.z : p.q, p.B, p.T, p.H, false))   // (unused unless gated)
         return kErrCuda;
     TcArgs ta{p.log_alpha, (const __nv_bfloat16 *)p.beta, p.init_state, p.final_state,
-              status_word, (int)p.T, (int)p.H, p.NC, 0, 1, p.NC, nullptr, nullptr, nullptr};
+              status_word, (int)p.T, (int)p.H, p.NC, p.fuse, 0, 1, p.NC, nullptr, nullptr, nullptr};
     auto launch = [&](const TcArgs &t, unsigned grid) {
         if (p.out_bf16)
-            return p.gate == 1 ? launch_t<__nv_bfloat16, 1>(mq, mk, mv, mo, t, grid, stream)
-                               : launch_t<__nv_bfloat16, 0>(mq, mk, mv, mo, t, grid, stream);
-        return p.gate == 1 ? launch_t<float, 1>(mq, mk, mv, mo, t, grid, stream)
-                           : launch_t<float, 0>(mq, mk, mv, mo, t, grid, stream);
+            return p.gate == 1 ? launch_t<__nv_bfloat16, 1>(mq, mk, mv, mo, mz, t, grid, stream)
+                               : launch_t<__nv_bfloat16, 0>(mq, mk, mv, mo, mz, t, grid, stream);
+        return p.gate == 1 ? launch_t<float, 1>(mq, mk, mv, mo, mz, t, grid, stream)
+                           : launch_t<float, 0>(mq, mk, mv, mo, mz, t, grid, stream);
     };
     const unsigned bh = (unsigned)(p.B * p.H);
     int nseg, seg_len;

@@ -41,6 +41,18 @@ __device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 v) {
     *reinterpret_cast<uint2 *>(p) = u;
 }
 
+// Neighbours of the operation that the kernels fuse (DR_FUSE_* of include/dr.h).
+// L2-normalisation epsilon under the square root (DR_L2NORM_EPS).
+constexpr float kL2NormEps = 1e-6f;
+// 1 / (1 + exp(-x)), without overflow for either sign of x (exp of a non-positive value).
+__device__ __forceinline__ float sigmoid_f(float x) {
+    const float e = expf(-fabsf(x));
+    const float r = __frcp_rn(1.f + e);
+    return x >= 0.f ? r : e * r;
+}
+// x sigmoid(x)
+__device__ __forceinline__ float silu_f(float x) { return x * sigmoid_f(x); }
+
 // Library status codes (mirrors include/dr.h).
 enum : int {
     kOk = 0, kErrInvalid = -1, kErrUnsupported = -2, kErrCuda = -3, kErrTimeout = -4,

@@ -72,22 +72,35 @@ extern "C" int dr_chunk_fwd_workspace_bytes(const dr_chunk_desc *desc, size_t *b
     return kOk;
 }
 
-extern "C" int dr_chunk_fwd(const dr_chunk_desc *desc, const void *q, const void *k,
-                            const void *v, const float *log_alpha, const void *beta,
-                            const float *init_state, void *out, float *final_state,
-                            void *workspace, size_t workspace_bytes, dr_stream_t stream) {
+// Whether byte ranges [a, a + na) and [b, b + nb) overlap.
+static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const char *a0 = (const char *)a, *b0 = (const char *)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+extern "C" int dr_chunk_fwd_ex(const dr_chunk_desc *desc, uint32_t fuse, const void *q,
+                               const void *k, const void *v, const float *log_alpha,
+                               const void *beta, const void *z, const float *init_state,
+                               void *out, float *final_state, void *workspace,
+                               size_t workspace_bytes, dr_stream_t stream) {
     ChunkProblem p{};
     int rc = check_chunk_desc(desc, &p);
     if (rc != kOk) return rc;
+    if (fuse & ~DR_FUSE_ALL) return kErrInvalid;
+    if (!(fuse & kFuseGate)) z = nullptr;
     if (p.T > 0 && (!q || !k || !v || !beta || !out)) return kErrInvalid;
     if (p.gate != DR_GATE_NONE && p.T > 0 && !log_alpha) return kErrInvalid;
-    const void *ptrs[] = {q, k, v, log_alpha, beta, init_state, out, final_state, workspace};
+    if ((fuse & kFuseGate) && p.T > 0 && !z) return kErrInvalid;
+    const void *ptrs[] = {q, k, v, log_alpha, beta, z, init_state, out, final_state, workspace};
     for (const void *ptr : ptrs)
         if (ptr && !aligned16(ptr)) return kErrInvalid;
     if (final_state && init_state && final_state != init_state) {
         const size_t sb = sizeof(float) * (size_t)(p.B * p.H * p.dk * p.dv);
-        const char *a0 = (const char *)init_state, *b0 = (const char *)final_state;
-        if (a0 < b0 + sb && b0 < a0 + sb) return kErrInvalid;   // partial overlap
+        if (overlaps(init_state, sb, final_state, sb)) return kErrInvalid;   // partial overlap
+    }
+    if (z && p.T > 0) {
+        const size_t n = (size_t)(p.B * p.T * p.H * p.dv);
+        if (overlaps(z, n * (p.in_bf16 ? 2 : 4), out, n * (p.out_bf16 ? 2 : 4))) return kErrInvalid;
     }
     size_t need = 0;
     dr_chunk_fwd_workspace_bytes(desc, &need);
@@ -95,6 +108,7 @@ extern "C" int dr_chunk_fwd(const dr_chunk_desc *desc, const void *q, const void
 
     p.q = q; p.k = k; p.v = v; p.log_alpha = p.gate == DR_GATE_NONE ? nullptr : log_alpha;
     p.beta = beta; p.init_state = init_state; p.out = out; p.final_state = final_state;
+    p.fuse = fuse; p.z = z;
     if (p.NC == 0 && !final_state) return kOk;
     if (chunk_tc_supported(p)) {
         int *status = device_status_ptr();
@@ -110,28 +124,49 @@ extern "C" int dr_chunk_fwd(const dr_chunk_desc *desc, const void *q, const void
     return launch_chunk_simt(p, ws, (cudaStream_t)stream);
 }
 
-extern "C" int dr_recurrent_step(const dr_step_desc *d, const void *q, const void *k,
-                                 const void *v, const float *log_alpha, const void *beta,
-                                 float *state, void *out, dr_stream_t stream) {
+extern "C" int dr_chunk_fwd(const dr_chunk_desc *desc, const void *q, const void *k,
+                            const void *v, const float *log_alpha, const void *beta,
+                            const float *init_state, void *out, float *final_state,
+                            void *workspace, size_t workspace_bytes, dr_stream_t stream) {
+    return dr_chunk_fwd_ex(desc, 0u, q, k, v, log_alpha, beta, nullptr, init_state, out,
+                           final_state, workspace, workspace_bytes, stream);
+}
+
+extern "C" int dr_recurrent_step_ex(const dr_step_desc *d, uint32_t fuse, const void *q,
+                                    const void *k, const void *v, const float *log_alpha,
+                                    const void *beta, const void *z, float *state, void *out,
+                                    dr_stream_t stream) {
     if (!d) return kErrInvalid;
     if (d->B < 1 || d->H < 1 || d->dk < 1 || d->dv < 1 || d->reserved != 0) return kErrInvalid;
     if (!dtype_ok(d->in_dtype) || !dtype_ok(d->out_dtype)) return kErrInvalid;
     if (d->gate < DR_GATE_NONE || d->gate > DR_GATE_CHANNEL) return kErrInvalid;
+    if (fuse & ~DR_FUSE_ALL) return kErrInvalid;
     if (!dim_ok(d->dk) || !dim_ok(d->dv)) return kErrUnsupported;
     if (d->B * d->H > 0x7fffffffLL) return kErrUnsupported;
+    if (!(fuse & kFuseGate)) z = nullptr;
     if (!q || !k || !v || !beta || !state || !out) return kErrInvalid;
     if (d->gate != DR_GATE_NONE && !log_alpha) return kErrInvalid;
-    const void *ptrs[] = {q, k, v, log_alpha, beta, state, out};
+    if ((fuse & kFuseGate) && !z) return kErrInvalid;
+    const void *ptrs[] = {q, k, v, log_alpha, beta, z, state, out};
     for (const void *ptr : ptrs)
         if (ptr && !aligned16(ptr)) return kErrInvalid;
     const size_t sb = sizeof(float) * (size_t)(d->B * d->H * d->dk * d->dv);
     const size_t ob = (size_t)(d->B * d->H * d->dv) * (d->out_dtype == DR_BF16 ? 2 : 4);
-    const char *s0 = (const char *)state, *o0 = (const char *)out;
-    if (s0 < o0 + ob && o0 < s0 + sb) return kErrInvalid;
+    if (overlaps(state, sb, out, ob)) return kErrInvalid;
+    if (z) {
+        const size_t zb = (size_t)(d->B * d->H * d->dv) * (d->in_dtype == DR_BF16 ? 2 : 4);
+        if (overlaps(z, zb, state, sb) || overlaps(z, zb, out, ob)) return kErrInvalid;
+    }
     return launch_decode(d->B * d->H, (int)d->dk, (int)d->dv, d->in_dtype == DR_BF16,
-                         d->out_dtype == DR_BF16, d->gate, q, k, v,
-                         d->gate == DR_GATE_NONE ? nullptr : log_alpha, beta, state, out,
+                         d->out_dtype == DR_BF16, d->gate, fuse, q, k, v,
+                         d->gate == DR_GATE_NONE ? nullptr : log_alpha, beta, z, state, out,
                          (cudaStream_t)stream);
+}
+
+extern "C" int dr_recurrent_step(const dr_step_desc *d, const void *q, const void *k,
+                                 const void *v, const float *log_alpha, const void *beta,
+                                 float *state, void *out, dr_stream_t stream) {
+    return dr_recurrent_step_ex(d, 0u, q, k, v, log_alpha, beta, nullptr, state, out, stream);
 }
 
 extern "C" int dr_get_device_status(dr_stream_t stream) {

@@ -66,6 +66,12 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_
           "r"(c0), "r"(c1), "r"(c2), "r"(c3) : "memory");
 }
 
+// Prefetch of a tensor-map box into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_4d(const void *tmap, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+                 ::"l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_t *bar, int c0, int c1) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"

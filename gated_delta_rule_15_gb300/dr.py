@@ -28,11 +28,14 @@ DR_F32, DR_BF16 = 0, 1
 DR_GATE_NONE, DR_GATE_SCALAR, DR_GATE_CHANNEL = 0, 1, 2
 DR_OK, DR_ERR_INVALID, DR_ERR_UNSUPPORTED, DR_ERR_CUDA, DR_ERR_TIMEOUT, DR_ERR_WORKSPACE = \
     0, -1, -2, -3, -4, -5
+# fused neighbours (flags of dr_chunk_fwd_ex / dr_recurrent_step_ex)
+DR_FUSE_QK_L2NORM, DR_FUSE_BETA_SIGMOID, DR_FUSE_OUT_SILU_GATE = 1, 2, 4
+L2NORM_EPS = 1e-6   # DR_L2NORM_EPS
 
 # Symbols of include/dr.h (checked by tests/test_abi.py against the header).
 EXPORTED = ("dr_version", "dr_chunk_fwd_workspace_bytes", "dr_chunk_fwd",
             "dr_recurrent_step", "dr_get_device_status", "dr_strerror",
-            "dr_chunk_fwd_noalloc")
+            "dr_chunk_fwd_noalloc", "dr_chunk_fwd_ex", "dr_recurrent_step_ex")
 
 
 class ChunkDesc(ctypes.Structure):
@@ -61,6 +64,12 @@ _lib.dr_chunk_fwd.restype = ctypes.c_int
 _lib.dr_recurrent_step.argtypes = [ctypes.POINTER(StepDesc), _vp, _vp, _vp, _vp, _vp, _vp,
                                    _vp, _vp]
 _lib.dr_recurrent_step.restype = ctypes.c_int
+_lib.dr_chunk_fwd_ex.argtypes = [ctypes.POINTER(ChunkDesc), ctypes.c_uint32, _vp, _vp, _vp, _vp,
+                                 _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.dr_chunk_fwd_ex.restype = ctypes.c_int
+_lib.dr_recurrent_step_ex.argtypes = [ctypes.POINTER(StepDesc), ctypes.c_uint32, _vp, _vp, _vp,
+                                      _vp, _vp, _vp, _vp, _vp, _vp]
+_lib.dr_recurrent_step_ex.restype = ctypes.c_int
 _lib.dr_get_device_status.argtypes = [_vp]
 _lib.dr_get_device_status.restype = ctypes.c_int
 _lib.dr_strerror.argtypes = [ctypes.c_int]
@@ -119,6 +128,12 @@ def _check_dev(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
+def fuse_flags(qk_l2norm: bool = False, beta_sigmoid: bool = False, z=None) -> int:
+    """DR_FUSE_* bits for the fused neighbours requested."""
+    return ((DR_FUSE_QK_L2NORM if qk_l2norm else 0) | (DR_FUSE_BETA_SIGMOID if beta_sigmoid else 0)
+            | (DR_FUSE_OUT_SILU_GATE if z is not None else 0))
+
+
 def chunk_desc(B, T, H, dk, dv, in_dtype, out_dtype, gate, chunk=64) -> ChunkDesc:
     return ChunkDesc(B, T, H, dk, dv, in_dtype, out_dtype, gate, chunk)
 
@@ -133,15 +148,19 @@ def workspace_bytes(desc: ChunkDesc) -> int:
 
 def chunk_fwd(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
               out_dtype=None, return_final_state: bool = True, out=None,
-              final_state=None, workspace=None, stream=None):
-    """Chunkwise forward (dr_chunk_fwd) on device tensors.
+              final_state=None, workspace=None, stream=None, qk_l2norm: bool = False,
+              beta_sigmoid: bool = False, z=None):
+    """Chunkwise forward (dr_chunk_fwd, or dr_chunk_fwd_ex with fused neighbours) on
+    device tensors.
 
     q, k [B,T,H,dk]; v [B,T,H,dv]; beta [B,T,H] (q's dtype); log_alpha None, fp32
     [B,T,H] or [B,T,H,dk]; init_state None or fp32 [B,H,dk,dv].  Returns
     (out [B,T,H,dv], final_state [B,H,dk,dv] fp32 or None).  ``final_state`` may be the
-    ``init_state`` tensor for an in-place carry.
+    ``init_state`` tensor for an in-place carry.  Fused neighbours: ``qk_l2norm`` divides
+    q and k rows by their norms, ``beta_sigmoid`` reads beta as logits, ``z``
+    ([B,T,H,dv], q's dtype) gates the output by silu(z).
     """
-    _check_dev(q, k, v, log_alpha, beta, init_state, out, final_state, workspace)
+    _check_dev(q, k, v, log_alpha, beta, init_state, out, final_state, workspace, z)
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
@@ -154,6 +173,9 @@ def chunk_fwd(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
     if init_state is not None and (init_state.dtype != torch.float32
                                    or tuple(init_state.shape) != (B, H, dk, dv)):
         raise ValueError("init_state must be float32 [B,H,dk,dv]")
+    if z is not None and (z.dtype != q.dtype or tuple(z.shape) != (B, T, H, dv)):
+        raise ValueError("z must have q's dtype and shape [B,T,H,dv]")
+    fuse = fuse_flags(qk_l2norm, beta_sigmoid, z)
     gate = _gate_of(log_alpha, (B, T, H), dk)
     odt = _DT[out_dtype or q.dtype]
     desc = chunk_desc(B, T, H, dk, dv, _DT[q.dtype], odt, gate, chunk)
@@ -165,6 +187,14 @@ def chunk_fwd(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if fuse:
+        rc = _lib.dr_chunk_fwd_ex(ctypes.byref(desc), fuse, _ptr(q), _ptr(k), _ptr(v),
+                                  _ptr(log_alpha), _ptr(beta), _ptr(z), _ptr(init_state),
+                                  _ptr(out), _ptr(final_state), _ptr(workspace), wbytes,
+                                  _stream_handle(stream))
+        if rc != DR_OK:
+            raise DrError(rc, "dr_chunk_fwd_ex")
+        return out, final_state
     rc = _lib.dr_chunk_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
                            _ptr(beta), _ptr(init_state), _ptr(out), _ptr(final_state),
                            _ptr(workspace), wbytes, _stream_handle(stream))
@@ -193,11 +223,12 @@ def chunk_fwd_noalloc(q, k, v, log_alpha, beta, init_state, out, final_state, *,
 
 
 def recurrent_step(q, k, v, log_alpha, beta, state, *, out=None, out_dtype=None,
-                   stream=None):
-    """One decode step (dr_recurrent_step); ``state`` [B,H,dk,dv] fp32 is updated in
+                   stream=None, qk_l2norm: bool = False, beta_sigmoid: bool = False, z=None):
+    """One decode step (dr_recurrent_step, or dr_recurrent_step_ex with fused neighbours,
+    flags as for chunk_fwd; z [B,H,dv]); ``state`` [B,H,dk,dv] fp32 is updated in
     place.  q, k [B,H,dk]; v [B,H,dv]; beta [B,H]; log_alpha None, [B,H] or [B,H,dk].
     Returns out [B,H,dv]."""
-    _check_dev(q, k, v, log_alpha, beta, state, out)
+    _check_dev(q, k, v, log_alpha, beta, state, out, z)
     B, H, dk = q.shape
     dv = v.shape[-1]
     if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
@@ -206,11 +237,21 @@ def recurrent_step(q, k, v, log_alpha, beta, state, *, out=None, out_dtype=None,
         raise ValueError("state must be float32 [B,H,dk,dv]")
     if log_alpha is not None and log_alpha.dtype != torch.float32:
         raise ValueError("log_alpha must be float32")
+    if z is not None and (z.dtype != q.dtype or tuple(z.shape) != (B, H, dv)):
+        raise ValueError("z must have q's dtype and shape [B,H,dv]")
+    fuse = fuse_flags(qk_l2norm, beta_sigmoid, z)
     gate = _gate_of(log_alpha, (B, H), dk)
     odt = _DT[out_dtype or q.dtype]
     desc = StepDesc(B, H, dk, dv, _DT[q.dtype], odt, gate, 0)
     if out is None:
         out = torch.empty((B, H, dv), dtype=_TORCH_DT[odt], device=q.device)
+    if fuse:
+        rc = _lib.dr_recurrent_step_ex(ctypes.byref(desc), fuse, _ptr(q), _ptr(k), _ptr(v),
+                                       _ptr(log_alpha), _ptr(beta), _ptr(z), _ptr(state),
+                                       _ptr(out), _stream_handle(stream))
+        if rc != DR_OK:
+            raise DrError(rc, "dr_recurrent_step_ex")
+        return out
     rc = _lib.dr_recurrent_step(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v),
                                 _ptr(log_alpha), _ptr(beta), _ptr(state), _ptr(out),
                                 _stream_handle(stream))

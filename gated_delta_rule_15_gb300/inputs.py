@@ -12,6 +12,11 @@ Recipe (one CPU torch.Generator seeded once per workload, draws in this order, f
 Then q <- q/|q|, k <- k/|k| per (b, t, h) in fp32, beta = sigmoid(logits), and q, k, v,
 beta are cast to the storage dtype (round to nearest even); log alpha and the state stay
 fp32.
+
+Raw inputs for the fused neighbours (`raw=True`): the same draws, then z ~ N(0, 1)
+[B,T,H,dv]; q, k are stored unnormalised (scaled by a per-token factor ~ U(0.25, 4), drawn
+after z, so that the norms vary), beta keeps its logits, and z is stored in the storage
+dtype.  The normalisation, the sigmoid and the output gate are then the library's work.
 """
 from __future__ import annotations
 
@@ -87,10 +92,11 @@ def _log_alpha(g, shape, lo, hi):
 
 
 def chunk_inputs(B, T, H, dk, dv, *, gate="scalar", dtype="bf16", init_state=False,
-                 seed=0, log_alpha_range=(0.001, 0.1), unit_keys=True):
+                 seed=0, log_alpha_range=(0.001, 0.1), unit_keys=True, raw=False):
     """Draw one chunk-forward problem on the CPU.  Returns a dict with q, k, v
     ([B,T,H,d], storage dtype), beta ([B,T,H], storage dtype), log_alpha (fp32 or
-    None) and init_state (fp32 [B,H,dk,dv] or None)."""
+    None) and init_state (fp32 [B,H,dk,dv] or None); with `raw`, also z ([B,T,H,dv],
+    storage dtype), and q, k, beta as described in the module's recipe."""
     if gate not in GATES:
         raise ValueError(gate)
     g = torch.Generator().manual_seed(seed)
@@ -106,11 +112,20 @@ def chunk_inputs(B, T, H, dk, dv, *, gate="scalar", dtype="bf16", init_state=Fal
     else:
         la = None
     s0 = 0.02 * torch.randn((B, H, dk, dv), generator=g) if init_state else None
+    dt = DTYPES[dtype]
+    if raw:
+        z = torch.randn((B, T, H, dv), generator=g)
+        q = q * (0.25 + 3.75 * torch.rand((B, T, H, 1), generator=g))
+        k = k * (0.25 + 3.75 * torch.rand((B, T, H, 1), generator=g))
+        return {"q": q.to(dt).contiguous(), "k": k.to(dt).contiguous(),
+                "v": v.to(dt).contiguous(), "beta": bl.to(dt).contiguous(),
+                "log_alpha": None if la is None else la.contiguous(),
+                "init_state": None if s0 is None else s0.contiguous(),
+                "z": z.to(dt).contiguous()}
     if unit_keys:
         q = q / q.norm(dim=-1, keepdim=True)
         k = k / k.norm(dim=-1, keepdim=True)
     beta = torch.sigmoid(bl)
-    dt = DTYPES[dtype]
     return {"q": q.to(dt).contiguous(), "k": k.to(dt).contiguous(),
             "v": v.to(dt).contiguous(), "beta": beta.to(dt).contiguous(),
             "log_alpha": None if la is None else la.contiguous(),
@@ -124,12 +139,13 @@ def workload_inputs(w: ChunkWorkload, seed=0):
 
 
 def decode_inputs(B, H, dk, dv, steps, *, gate="scalar", dtype="bf16", seed=0,
-                  log_alpha_range=(0.001, 0.1)):
+                  log_alpha_range=(0.001, 0.1), raw=False):
     """Draw `steps` single-token decode inputs and the initial state.  q, k [steps,B,H,dk],
     v [steps,B,H,dv], beta [steps,B,H], log_alpha [steps,B,H] or [steps,B,H,dk] (None
-    without a gate), state [B,H,dk,dv] fp32 ~ N(0, 0.02^2)."""
+    without a gate), state [B,H,dk,dv] fp32 ~ N(0, 0.02^2); with `raw`, z [steps,B,H,dv]
+    and raw q, k, beta as for chunk_inputs."""
     d = chunk_inputs(steps, B, H, dk, dv, gate=gate, dtype=dtype, init_state=False,
-                     seed=seed, log_alpha_range=log_alpha_range)
+                     seed=seed, log_alpha_range=log_alpha_range, raw=raw)
     g = torch.Generator().manual_seed(seed + 1)
     state = 0.02 * torch.randn((B, H, dk, dv), generator=g)
     d["state"] = state.contiguous()

@@ -26,6 +26,8 @@ def main():
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--H", type=int, default=None)
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--fused", action="store_true",
+                    help="raw inputs with every fused neighbour (L2 norm, sigmoid, SiLU gate)")
     args = ap.parse_args()
 
     import torch
@@ -37,14 +39,19 @@ def main():
         w = inputs.WORKLOADS[args.workload or "gdn_bf16_B8_H16_T4096_d128"]
         w = dataclasses.replace(w, **{k: getattr(args, k) for k in ("B", "T", "H")
                                       if getattr(args, k) is not None})
-        d = inputs.workload_inputs(w)
+        d = inputs.chunk_inputs(w.B, w.T, w.H, w.dk, w.dv, gate=w.gate, dtype=w.dtype,
+                                init_state=w.init_state, log_alpha_range=w.log_alpha_range,
+                                raw=args.fused)
         g = {k: (None if t is None else t.cuda()) for k, t in d.items()}
+        fz = dict(qk_l2norm=True, beta_sigmoid=True, z=g["z"]) if args.fused else {}
         run = lambda: dr.chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"],
-                                   g["init_state"], chunk=w.chunk)
+                                   g["init_state"], chunk=w.chunk, **fz)
     else:
         w = inputs.DECODE_WORKLOADS[args.workload or "decode_scalar_B256_H32_d128"]
         w = dataclasses.replace(w, **({"B": args.B} if args.B else {}))
-        s = inputs.decode_workload_inputs(w, steps=max(1, args.iters))
+        s = inputs.decode_inputs(w.B, w.H, w.dk, w.dv, max(1, args.iters), gate=w.gate,
+                                 dtype=w.dtype, log_alpha_range=w.log_alpha_range,
+                                 raw=args.fused)
         st = s["state"].cuda()
         g = {k: (None if t is None else t.cuda()) for k, t in s.items() if k != "state"}
         i = [0]
@@ -53,7 +60,8 @@ def main():
             t = i[0] % g["q"].shape[0]
             i[0] += 1
             la = None if g["log_alpha"] is None else g["log_alpha"][t]
-            dr.recurrent_step(g["q"][t], g["k"][t], g["v"][t], la, g["beta"][t], st)
+            fz = dict(qk_l2norm=True, beta_sigmoid=True, z=g["z"][t]) if args.fused else {}
+            dr.recurrent_step(g["q"][t], g["k"][t], g["v"][t], la, g["beta"][t], st, **fz)
     run()
     torch.cuda.synchronize()
     e0.record()
@@ -61,7 +69,8 @@ def main():
         run()
     e1.record()
     torch.cuda.synchronize()
-    print(f"{w.name} {dataclasses.asdict(w)}: {e0.elapsed_time(e1) / args.iters:.4f} ms/launch")
+    tag = " fused" if args.fused else ""
+    print(f"{w.name}{tag} {dataclasses.asdict(w)}: {e0.elapsed_time(e1) / args.iters:.4f} ms/launch")
 
 
 if __name__ == "__main__":

@@ -25,7 +25,8 @@
  *   - Token-major layouts, the layout a projection GEMM writes:
  *       q, k        [B, T, H, dk]    in_dtype
  *       v           [B, T, H, dv]    in_dtype
- *       beta        [B, T, H]        in_dtype, values in [0, 1]
+ *       beta        [B, T, H]        in_dtype, values in [0, 1] (logits under
+ *                                    DR_FUSE_BETA_SIGMOID)
  *       log_alpha   [B, T, H] (DR_GATE_SCALAR) or [B, T, H, dk] (DR_GATE_CHANNEL), fp32,
  *                   values <= 0; NULL for DR_GATE_NONE
  *       out         [B, T, H, dv]    out_dtype
@@ -83,6 +84,24 @@ typedef struct {
     int32_t reserved;         /* must be 0                                              */
 } dr_step_desc;
 
+/*
+ * Fused neighbours of the operation: the steps on either side of it in a Gated DeltaNet
+ * layer (page "linear-attention gated-deltanet guide", section 4: the write gate beta, the
+ * read-out gated by SiLU; q and k enter L2-normalised), applied inside the kernels of
+ * dr_chunk_fwd_ex and dr_recurrent_step_ex, with no extra pass over memory.  OR-ed into
+ * their `fuse` argument:
+ *   DR_FUSE_QK_L2NORM      every q and k row (dk values) is divided by
+ *                          sqrt(sum of squares + DR_L2NORM_EPS), in fp32, before use
+ *   DR_FUSE_BETA_SIGMOID   `beta` holds logits (any finite value, in_dtype); the kernels
+ *                          use beta = 1 / (1 + exp(-logit))
+ *   DR_FUSE_OUT_SILU_GATE  out = o * z * sigmoid(z), elementwise, with `z` laid out as
+ *                          out ([B, T, H, dv], or [B, H, dv] for a step) in in_dtype
+ * The state (init_state, final_state, the decode state) is never gated: only `out` is.
+ */
+enum { DR_FUSE_QK_L2NORM = 1, DR_FUSE_BETA_SIGMOID = 2, DR_FUSE_OUT_SILU_GATE = 4 };
+#define DR_FUSE_ALL 7u
+#define DR_L2NORM_EPS 1e-6f
+
 /* Library version, (major << 16) | minor. */
 int dr_version(void);
 
@@ -113,6 +132,20 @@ int dr_chunk_fwd(const dr_chunk_desc *desc,
                  void *workspace, size_t workspace_bytes, dr_stream_t stream);
 
 /*
+ * dr_chunk_fwd with fused neighbours: `fuse` is an OR of DR_FUSE_* (0 makes the call
+ * identical to dr_chunk_fwd); `z` is the output gate's input, [B, T, H, dv] in_dtype, read
+ * only, required (non-NULL, 16-byte aligned, not overlapping `out`) when DR_FUSE_OUT_SILU_GATE
+ * is set and ignored otherwise.  Every configuration dr_chunk_fwd accepts takes every flag; the workspace size
+ * does not depend on them.  Returns the statuses of dr_chunk_fwd; DR_ERR_INVALID also for
+ * bits outside DR_FUSE_ALL or a missing z.
+ */
+int dr_chunk_fwd_ex(const dr_chunk_desc *desc, uint32_t fuse,
+                    const void *q, const void *k, const void *v,
+                    const float *log_alpha, const void *beta, const void *z,
+                    const float *init_state, void *out, float *final_state,
+                    void *workspace, size_t workspace_bytes, dr_stream_t stream);
+
+/*
  * One decode step for B x H chains, one token each (the loop body of the recurrence
  * once).  Streams the fp32 state through HBM once: it is read, decayed, updated and
  * written back in place.
@@ -127,6 +160,16 @@ int dr_recurrent_step(const dr_step_desc *desc,
                       const void *q, const void *k, const void *v,
                       const float *log_alpha, const void *beta,
                       float *state, void *out, dr_stream_t stream);
+
+/*
+ * dr_recurrent_step with fused neighbours (flags as for dr_chunk_fwd_ex); `z` is
+ * [B, H, dv] in_dtype, required when DR_FUSE_OUT_SILU_GATE is set, and must not overlap
+ * `state` or `out`.  Returns the statuses of dr_recurrent_step.
+ */
+int dr_recurrent_step_ex(const dr_step_desc *desc, uint32_t fuse,
+                         const void *q, const void *k, const void *v,
+                         const float *log_alpha, const void *beta, const void *z,
+                         float *state, void *out, dr_stream_t stream);
 
 /*
  * dr_chunk_fwd without a caller-provided workspace.  The pages have no counterpart of

@@ -205,7 +205,7 @@ def forward_fused(q, k, v, log_alpha, beta, init_state=None, *, qk_l2norm=False,
         beta = sigmoid(beta)
     out, final = forward(q, k, v, log_alpha, beta, init_state, **kw)
     if z is not None:
-        out = out * silu(z)
+        out = out * silu(to_f64(z))
     return out, final
 
 
@@ -219,5 +219,5 @@ def step_fused(q, k, v, log_alpha, beta, state, *, qk_l2norm=False, beta_sigmoid
         beta = sigmoid(beta)
     out, st = step(q, k, v, log_alpha, beta, state, **kw)
     if z is not None:
-        out = out * silu(z)
+        out = out * silu(to_f64(z))
     return out, st

@@ -116,6 +116,31 @@ def test_recurrent_step_host_side_errors(dr):
     assert call(d3) == dr.DR_ERR_INVALID
 
 
+@no_gpu_only
+def test_fused_entry_points_host_side_errors(dr):
+    lib = dr.lib()
+    d = _desc(dr)
+    fake = ctypes.c_void_p(1 << 20)
+    far = lambda n: ctypes.c_void_p(n << 32)   # disjoint fake buffers, never dereferenced
+    names = ("q", "k", "v", "la", "beta", "z", "s0", "out", "fin", "ws")
+    args = lambda **o: [o.get(n, fake if n not in ("z", "out") else far(names.index(n)))
+                        for n in names]
+    call = lambda fuse, a: lib.dr_chunk_fwd_ex(ctypes.byref(d), fuse, *a, 1 << 40, None)
+    assert call(8, args()) == dr.DR_ERR_INVALID                        # unknown bit
+    assert call(dr.DR_FUSE_OUT_SILU_GATE, args(z=None)) == dr.DR_ERR_INVALID
+    assert call(dr.DR_FUSE_OUT_SILU_GATE, args(z=ctypes.c_void_p((2 << 32) + 8))) \
+        == dr.DR_ERR_INVALID                                           # misaligned z
+    assert call(dr.DR_FUSE_OUT_SILU_GATE, args(z=far(7))) == dr.DR_ERR_INVALID  # z overlaps out
+    assert call(dr.DR_FUSE_QK_L2NORM, args(q=None)) == dr.DR_ERR_INVALID
+    sd = dr.StepDesc(4, 2, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_CHANNEL, 0)
+    step = lambda fuse, **o: lib.dr_recurrent_step_ex(
+        ctypes.byref(sd), fuse, *[o.get(n, fake) for n in ("q", "k", "v", "la", "beta")],
+        o.get("z", far(3)), far(1), far(2), None)
+    assert step(16) == dr.DR_ERR_INVALID
+    assert step(dr.DR_FUSE_OUT_SILU_GATE, z=None) == dr.DR_ERR_INVALID
+    assert step(dr.DR_FUSE_OUT_SILU_GATE, z=far(1)) == dr.DR_ERR_INVALID   # z overlaps state
+
+
 def test_python_binding_rejects_host_tensors(dr):
     import torch
     x = torch.zeros(1, 4, 1, 64)
