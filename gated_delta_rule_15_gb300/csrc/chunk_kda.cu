@@ -33,8 +33,8 @@
 // guide", section 4): the prep kernel computes 1 / |q_r| and 1 / |k_r| from the bf16 tiles
 // (threads 128..255, while threads 0..127 scan the gates) and scales every q and k value
 // as it converts it to fp32, so all the stored operands are those of the normalised rows;
-// it takes beta = sigmoid(logit).  The state kernel multiplies each output by silu(z), z's
-// tile arriving by TMA one chunk ahead.
+// it takes beta = sigmoid(logit) rounded to bf16 (beta's storage dtype).  The state kernel
+// multiplies each output by silu(z), z's tile arriving by TMA one chunk ahead.
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -215,7 +215,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     }
     if (tid < 64) {
         float bt = tid < Lc ? __bfloat162float(a.beta[((size_t)b * a.T + t0 + tid) * a.H + h]) : 0.f;
-        if ((a.fuse & kFuseSigmoid) && tid < Lc) bt = sigmoid_f(bt);
+        if ((a.fuse & kFuseSigmoid) && tid < Lc) bt = round_bf16(sigmoid_f(bt));
         sBeta[tid] = bt;
     }
     if (!wait_cycles(&bar_ld, 0)) fail();
@@ -798,7 +798,7 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
             const unsigned char *zt = sm + S2_Z + (j >> 6) * 8192;
 #pragma unroll
             for (int u = 0; u < 32; ++u)
-                o[u] *= silu_f(__bfloat162float(
+                o[u] *= silu_tanh(__bfloat162float(
                     *reinterpret_cast<const __nv_bfloat16 *>(zt + sw128_off(32 * half + u, j & 63))));
         }
         if (sizeof(Tout) == 2) {

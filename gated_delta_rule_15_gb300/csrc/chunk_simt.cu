@@ -29,8 +29,8 @@
 // (the log-space, two-level chunking remedy named on the "Transformer notes (5)" page).
 //
 // Fused neighbours (DR_FUSE_* of include/dr.h): the prep kernel takes beta = sigmoid(logit)
-// and divides each q and k row by its norm as soon as the rows are in shared memory (fp32);
-// the state kernel multiplies each output by silu(z).
+// (stored in beta's dtype) and divides each q and k row by its norm as soon as the rows are
+// in shared memory (fp32); the state kernel multiplies each output by silu(z).
 #include "common.cuh"
 #include "chunk_layout.h"
 
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
     const bool l2 = (a.fuse & kFuseL2) != 0;
     for (int r = tid; r < C; r += kThreads) {
         float br = r < Lc ? to_f32(beta[tok(r)]) : 0.f;
-        if ((a.fuse & kFuseSigmoid) && r < Lc) br = sigmoid_f(br);
+        if ((a.fuse & kFuseSigmoid) && r < Lc) br = to_f32(from_f32<Tin>(sigmoid_f(br)));
         sB[r] = br;
     }
     if (gate == 2) {

@@ -50,8 +50,9 @@
 // threads per row) the normalisation folds into scalings the kernel already applies in
 // fp32 and the tiles stay as loaded: X's entries get nq_r nk_s or nk_r nk_s in the P and A
 // builds, T diag(beta G) becomes T diag(beta G nk), diag(delta) becomes diag(delta nk) and
-// the output's G_r becomes G_r nq_r.  The gate warp takes beta = sigmoid(logit); the output
-// warps multiply by silu(z).  z's tile is prefetched into L2 with the chunk's q, k, v and
+// the output's G_r becomes G_r nq_r.  The gate warp takes beta = sigmoid(logit) rounded to
+// bf16, beta's storage dtype (so that, as for a stored beta, the diagonal of the U operand
+// T diag(beta) is exact).  The output warps multiply by silu(z).  z's tile is prefetched into L2 with the chunk's q, k, v and
 // copied by TMA into the stage's V slot as soon as the state update has read that slot
 // (the MMA warp waits for it), which is before the output step needs it.
 #include <algorithm>
@@ -275,7 +276,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             const uint32_t wd = gw[r];
             const uint16_t hb = (uint16_t)(((2 * tok) & 2) ? (wd >> 16) : (wd & 0xffffu));
             bt[e] = __bfloat162float(__ushort_as_bfloat16(hb));
-            if (a.fuse & kFuseSigmoid) bt[e] = t < a.T ? sigmoid_f(bt[e]) : 0.f;
+            if (a.fuse & kFuseSigmoid) bt[e] = t < a.T ? round_bf16(sigmoid_f(bt[e])) : 0.f;
             l[e] = __uint_as_float(gw[64 + r]);
         }
         __syncwarp();
@@ -706,7 +707,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                         const unsigned char *zt = st + OFF_V0 + (j >> 6) * 8192;
 #pragma unroll
                         for (int u = 0; u < 32; ++u)
-                            o[u] *= silu_f(__bfloat162float(
+                            o[u] *= silu_tanh(__bfloat162float(
                                 *reinterpret_cast<const __nv_bfloat16 *>(zt + sw128_off(32 * hh + u, j & 63))));
                     }
                     if (sizeof(Tout) == 2) {

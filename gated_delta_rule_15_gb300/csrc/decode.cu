@@ -23,7 +23,8 @@
 // guide", section 4), all on values the kernel already holds: with the raw q, k and
 // nq = 1 / |q|, nk = 1 / |k| (each warp reduces the two sums of squares itself),
 // p_j = nk sum_i alpha_i k_i S_ij, r_j = nq sum_i alpha_i q_i S_ij, q.k scaled by nq nk,
-// and the write k_i (nk e_j); beta = sigmoid(logit); out_j = o_j silu(z_j).
+// and the write k_i (nk e_j); beta = sigmoid(logit) stored in beta's dtype; out_j = o_j
+// silu(z_j).
 #include "chunk_layout.h"
 #include "common.cuh"
 
@@ -60,7 +61,7 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         sa[i] = a;
     }
     float bt = to_f32(beta[bh]);
-    if (fuse & kFuseSigmoid) bt = sigmoid_f(bt);
+    if (fuse & kFuseSigmoid) bt = to_f32(from_f32<Tin>(sigmoid_f(bt)));   // stored as beta
     const float4 vv = load4(v + (size_t)bh * DV + col);
     float4 zz = make_float4(0.f, 0.f, 0.f, 0.f);
     if ((fuse & kFuseGate) && rr == 0) zz = load4(z + (size_t)bh * DV + col);

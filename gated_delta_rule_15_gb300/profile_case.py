@@ -18,6 +18,20 @@ import sys
 sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 
 
+def with_raw(make, fl):
+    """Prepared inputs, with the raw q, k / beta logits / z of the same draw for the
+    fused neighbours in `fl`."""
+    d = make(False)
+    if fl:
+        raw = make(True)
+        if "l2" in fl:
+            d["q"], d["k"] = raw["q"], raw["k"]
+        if "sigmoid" in fl:
+            d["beta"] = raw["beta"]
+        d["z"] = raw["z"]
+    return d
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--what", choices=["chunk", "decode"], required=True)
@@ -26,32 +40,38 @@ def main():
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--H", type=int, default=None)
     ap.add_argument("--iters", type=int, default=3)
-    ap.add_argument("--fused", action="store_true",
-                    help="raw inputs with every fused neighbour (L2 norm, sigmoid, SiLU gate)")
+    ap.add_argument("--fused", nargs="?", const="l2,sigmoid,silu", default="",
+                    help="raw inputs with the fused neighbours listed (default: all of "
+                         "l2, sigmoid, silu)")
     args = ap.parse_args()
 
     import torch
     from gated_delta_rule_15_gb300 import dr, inputs
 
     torch.cuda.set_device(0)
+    fl = set(filter(None, args.fused.split(",")))
+    if fl - {"l2", "sigmoid", "silu"}:
+        ap.error(f"unknown fused neighbours {fl}")
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if args.what == "chunk":
         w = inputs.WORKLOADS[args.workload or "gdn_bf16_B8_H16_T4096_d128"]
         w = dataclasses.replace(w, **{k: getattr(args, k) for k in ("B", "T", "H")
                                       if getattr(args, k) is not None})
-        d = inputs.chunk_inputs(w.B, w.T, w.H, w.dk, w.dv, gate=w.gate, dtype=w.dtype,
-                                init_state=w.init_state, log_alpha_range=w.log_alpha_range,
-                                raw=args.fused)
+        mk = lambda raw: inputs.chunk_inputs(w.B, w.T, w.H, w.dk, w.dv, gate=w.gate,
+                                             dtype=w.dtype, init_state=w.init_state,
+                                             log_alpha_range=w.log_alpha_range, raw=raw)
+        d = with_raw(mk, fl)
         g = {k: (None if t is None else t.cuda()) for k, t in d.items()}
-        fz = dict(qk_l2norm=True, beta_sigmoid=True, z=g["z"]) if args.fused else {}
+        fz = dict(qk_l2norm="l2" in fl, beta_sigmoid="sigmoid" in fl,
+                  z=g["z"] if "silu" in fl else None) if fl else {}
         run = lambda: dr.chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"],
                                    g["init_state"], chunk=w.chunk, **fz)
     else:
         w = inputs.DECODE_WORKLOADS[args.workload or "decode_scalar_B256_H32_d128"]
         w = dataclasses.replace(w, **({"B": args.B} if args.B else {}))
-        s = inputs.decode_inputs(w.B, w.H, w.dk, w.dv, max(1, args.iters), gate=w.gate,
-                                 dtype=w.dtype, log_alpha_range=w.log_alpha_range,
-                                 raw=args.fused)
+        s = with_raw(lambda raw: inputs.decode_inputs(
+            w.B, w.H, w.dk, w.dv, max(1, args.iters), gate=w.gate, dtype=w.dtype,
+            log_alpha_range=w.log_alpha_range, raw=raw), fl)
         st = s["state"].cuda()
         g = {k: (None if t is None else t.cuda()) for k, t in s.items() if k != "state"}
         i = [0]
@@ -60,7 +80,8 @@ def main():
             t = i[0] % g["q"].shape[0]
             i[0] += 1
             la = None if g["log_alpha"] is None else g["log_alpha"][t]
-            fz = dict(qk_l2norm=True, beta_sigmoid=True, z=g["z"][t]) if args.fused else {}
+            fz = dict(qk_l2norm="l2" in fl, beta_sigmoid="sigmoid" in fl,
+                      z=g["z"][t] if "silu" in fl else None) if fl else {}
             dr.recurrent_step(g["q"][t], g["k"][t], g["v"][t], la, g["beta"][t], st, **fz)
     run()
     torch.cuda.synchronize()
@@ -69,7 +90,7 @@ def main():
         run()
     e1.record()
     torch.cuda.synchronize()
-    tag = " fused" if args.fused else ""
+    tag = f" fused[{args.fused}]" if fl else ""
     print(f"{w.name}{tag} {dataclasses.asdict(w)}: {e0.elapsed_time(e1) / args.iters:.4f} ms/launch")
 
 

@@ -93,7 +93,8 @@ typedef struct {
  *   DR_FUSE_QK_L2NORM      every q and k row (dk values) is divided by
  *                          sqrt(sum of squares + DR_L2NORM_EPS), in fp32, before use
  *   DR_FUSE_BETA_SIGMOID   `beta` holds logits (any finite value, in_dtype); the kernels
- *                          use beta = 1 / (1 + exp(-logit))
+ *                          use beta = 1 / (1 + exp(-logit)) rounded to in_dtype, the
+ *                          value a beta stored before the call would hold
  *   DR_FUSE_OUT_SILU_GATE  out = o * z * sigmoid(z), elementwise, with `z` laid out as
  *                          out ([B, T, H, dv], or [B, H, dv] for a step) in in_dtype
  * The state (init_state, final_state, the decode state) is never gated: only `out` is.

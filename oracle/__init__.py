@@ -170,8 +170,26 @@ def step(q, k, v, log_alpha, beta, state, *, nthreads: int | None = None):
 # the sigmoid of logits, and the output gate of the page "linear-attention gated-deltanet
 # guide" (section 4: a gate with a SiLU activation on what is read out), out = o * silu(z).
 # The pages print no epsilon for the normalisation; the reading is x / sqrt(|x|^2 + eps)
-# with eps = 1e-6.
+# with eps = 1e-6.  Nor do they fix the precision of beta: the reading is that the sigmoid
+# is stored in beta's own dtype, as a beta computed before the call would be (for bf16
+# logits, the sigmoid rounded to nearest-even bf16).
 L2NORM_EPS = 1e-6
+
+
+def round_bf16(x) -> np.ndarray:
+    """float64 values rounded to the nearest bfloat16 (8 significant bits), ties to even,
+    for normal bf16 magnitudes (|x| >= 2^-126) and zero."""
+    x = to_f64(x)
+    m, e = np.frexp(x)                  # x = m 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)   # np.round: half to even
+
+
+def _is_bf16(x) -> bool:
+    try:
+        import torch
+        return isinstance(x, torch.Tensor) and x.dtype == torch.bfloat16
+    except ImportError:
+        return False
 
 
 def l2_normalize(x) -> np.ndarray:
@@ -196,13 +214,15 @@ def silu(x) -> np.ndarray:
 def forward_fused(q, k, v, log_alpha, beta, init_state=None, *, qk_l2norm=False,
                   beta_sigmoid=False, z=None, **kw):
     """``forward`` with the neighbouring steps: q, k normalised first (qk_l2norm), beta
-    given as logits (beta_sigmoid), and the output multiplied by silu(z) (z given, in the
-    output's layout).  The final state is that of ``forward`` on the prepared inputs."""
+    given as logits (beta_sigmoid; the sigmoid stored in the logits' dtype), and the output
+    multiplied by silu(z) (z given, in the output's layout).  The final state is that of
+    ``forward`` on the prepared inputs."""
+    bf16_beta = _is_bf16(beta)
     q, k, beta = to_f64(q), to_f64(k), to_f64(beta)
     if qk_l2norm:
         q, k = l2_normalize(q), l2_normalize(k)
     if beta_sigmoid:
-        beta = sigmoid(beta)
+        beta = round_bf16(sigmoid(beta)) if bf16_beta else sigmoid(beta)
     out, final = forward(q, k, v, log_alpha, beta, init_state, **kw)
     if z is not None:
         out = out * silu(to_f64(z))
@@ -212,11 +232,12 @@ def forward_fused(q, k, v, log_alpha, beta, init_state=None, *, qk_l2norm=False,
 def step_fused(q, k, v, log_alpha, beta, state, *, qk_l2norm=False, beta_sigmoid=False,
                z=None, **kw):
     """``step`` with the same neighbouring steps as ``forward_fused``."""
+    bf16_beta = _is_bf16(beta)
     q, k, beta = to_f64(q), to_f64(k), to_f64(beta)
     if qk_l2norm:
         q, k = l2_normalize(q), l2_normalize(k)
     if beta_sigmoid:
-        beta = sigmoid(beta)
+        beta = round_bf16(sigmoid(beta)) if bf16_beta else sigmoid(beta)
     out, st = step(q, k, v, log_alpha, beta, state, **kw)
     if z is not None:
         out = out * silu(to_f64(z))

@@ -9,6 +9,9 @@ bf16 adds a representation error of at most half a bf16 ulp of the value, which 
 exceed 2e-2 * RMS when the outputs are heavy-tailed (max/RMS ~ 8).  So for a bf16 result
 each element's deviation is first reduced by half a bf16 ulp of max(|x_gpu|, |x_oracle|)
 (clamped at zero); fp32-stored results get no allowance.
+
+Reading for the fused SiLU output gate (out = o * silu(z)): the bound is the operation's,
+carried through the elementwise gate (err_gated).
 """
 import numpy as np
 import torch
@@ -48,4 +51,36 @@ def err(gpu, ref, dtype):
 def assert_close(gpu, ref, dtype, what=""):
     e, tol = err(gpu, ref, dtype)
     assert e <= tol, f"{what}: error {e:.3e} > {tol:.1e}"
+    return e
+
+
+def err_gated(gpu, ref_ungated, gate, dtype):
+    """Error of a gated output out = o * gate (gate = silu(z), fp64) against the oracle's
+    ungated o.  The output gate is an elementwise scaling of the operation's result, so the
+    operation's bound carries over element by element: |out_gpu - o_ref gate| <= tol *
+    scale * |gate| (+ half a bf16 ulp of the stored value), scale = 1 (fp32 inputs) or
+    RMS(o_ref) (bf16 inputs).  Returns (max of the scaled deviation, tolerance)."""
+    stored_bf16 = isinstance(gpu, torch.Tensor) and gpu.dtype == torch.bfloat16
+    g = to_np(gpu)
+    o = np.asarray(ref_ungated, dtype=np.float64)
+    gt = np.asarray(gate, dtype=np.float64)
+    r = o * gt
+    assert g.shape == r.shape, (g.shape, r.shape)
+    if not np.isfinite(g).all():
+        return np.inf, 0.0
+    if g.size == 0:
+        return 0.0, (TOL_F32_ABS if dtype == "f32" else TOL_BF16_REL)
+    dev = np.abs(g - r)
+    if stored_bf16:
+        dev = np.maximum(dev - half_ulp_bf16(np.maximum(np.abs(g), np.abs(r))), 0.0)
+    dev = dev / np.maximum(np.abs(gt), 1e-30)
+    if dtype == "f32":
+        return dev.max(), TOL_F32_ABS
+    rms = np.sqrt((o ** 2).mean())
+    return dev.max() / max(rms, 1e-30), TOL_BF16_REL
+
+
+def assert_close_gated(gpu, ref_ungated, gate, dtype, what=""):
+    e, tol = err_gated(gpu, ref_ungated, gate, dtype)
+    assert e <= tol, f"{what}: gated error {e:.3e} > {tol:.1e}"
     return e

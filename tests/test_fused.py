@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from gated_delta_rule_15_gb300 import inputs
-from parity import assert_close
+from parity import assert_close, assert_close_gated
 
 pytestmark = pytest.mark.gpu
 
@@ -27,17 +27,17 @@ def dr():
 
 
 def problem(B, T, H, dk, dv, flags, **kw):
-    """Raw inputs for the requested neighbours.  Without the normalisation the keys are
-    drawn unit (raw keys of norm ~ sqrt(dk) would make the rule diverge), with the
-    beta logits and z of the same draws."""
+    """Inputs for the requested neighbours: the raw q, k (normalisation fused), beta
+    logits (sigmoid fused) and z (gate fused) of one draw, the prepared values of the same
+    draw otherwise (raw keys of norm ~ sqrt(dk), or logits used as beta, make the rule
+    diverge)."""
     l2, sig, gz = flags
     raw = inputs.chunk_inputs(B, T, H, dk, dv, raw=True, **kw)
+    d = inputs.chunk_inputs(B, T, H, dk, dv, **kw)
     if l2:
-        d = raw
-    else:
-        d = inputs.chunk_inputs(B, T, H, dk, dv, **kw)
-        if sig:
-            d["beta"] = raw["beta"]
+        d["q"], d["k"] = raw["q"], raw["k"]
+    if sig:
+        d["beta"] = raw["beta"]
     d["z"] = raw["z"] if gz else None
     return d
 
@@ -52,14 +52,21 @@ def run(dr, d, flags, **kw):
     return out, fin
 
 
+def assert_out(out, o_ungated, z, dtype, what="out"):
+    """The output against the oracle: directly, or through the gate's elementwise bound
+    when the SiLU gate is fused."""
+    if z is None:
+        return assert_close(out, o_ungated, dtype, what)
+    return assert_close_gated(out, o_ungated, oracle.silu(oracle.to_f64(z)), dtype, what)
+
+
 def check(dr, d, flags, dtype, **kw):
     l2, sig, _ = flags
     out, fin = run(dr, d, flags, **kw)
     o_ref, f_ref = oracle.forward_fused(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
-                                        d["init_state"], qk_l2norm=l2, beta_sigmoid=sig,
-                                        z=d["z"])
+                                        d["init_state"], qk_l2norm=l2, beta_sigmoid=sig)
     if d["q"].shape[1]:
-        assert_close(out, o_ref, dtype, "out")
+        assert_out(out, o_ref, d["z"], dtype)
     assert_close(fin, f_ref, dtype, "final_state")
 
 
@@ -147,7 +154,9 @@ def test_decode_steps(dr, flags, gate, dtype, dk, dv):
     l2, sig, gz = flags
     steps = 8
     raw = inputs.decode_inputs(5, 3, dk, dv, steps, gate=gate, dtype=dtype, seed=4, raw=True)
-    s = raw if l2 else inputs.decode_inputs(5, 3, dk, dv, steps, gate=gate, dtype=dtype, seed=4)
+    s = inputs.decode_inputs(5, 3, dk, dv, steps, gate=gate, dtype=dtype, seed=4)
+    if l2:
+        s["q"], s["k"] = raw["q"], raw["k"]
     beta = raw["beta"] if sig else s["beta"]
     z = raw["z"] if gz else None
     st = s["state"].cuda()
@@ -159,9 +168,8 @@ def test_decode_steps(dr, flags, gate, dtype, dk, dv):
                               qk_l2norm=l2, beta_sigmoid=sig,
                               z=None if z is None else z[t].cuda())
         o_ref, ref = oracle.step_fused(s["q"][t], s["k"][t], s["v"][t], la, beta[t], ref,
-                                       qk_l2norm=l2, beta_sigmoid=sig,
-                                       z=None if z is None else z[t])
-        assert_close(o, o_ref, dtype, f"out step {t}")
+                                       qk_l2norm=l2, beta_sigmoid=sig)
+        assert_out(o, o_ref, None if z is None else z[t], dtype, f"out step {t}")
     assert_close(st, ref, dtype, "state")
     assert dr.device_status() == 0
 
@@ -180,6 +188,6 @@ def test_decode_continues_fused_prefill(dr):
                           st, z=g["z"][:, 96].contiguous(), **kw)
     torch.cuda.synchronize()
     o_ref, f_ref = oracle.forward_fused(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
-                                        d["init_state"], z=d["z"], **kw)
-    assert_close(o, o_ref[:, 96], "bf16", "out")
+                                        d["init_state"], **kw)
+    assert_out(o, o_ref[:, 96], d["z"][:, 96], "bf16")
     assert_close(st, f_ref, "bf16", "state")

@@ -544,3 +544,31 @@ def test_fused_pins_catch_planted_mistake(mistake, monkeypatch):
         except AssertionError:
             failed += 1
     assert failed >= 1, f"no pin caught {mistake}"
+
+
+def test_round_bf16_matches_torch_on_fp32_values():
+    """On fp32 values (no double rounding) the oracle's bf16 rounding is torch's cast."""
+    import torch
+    x = (torch.randn(200000) * torch.exp(torch.randn(200000) * 5)).float()
+    x = torch.cat([x, torch.tensor([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8)])])
+    ref = x.to(torch.bfloat16).double().numpy()
+    assert np.array_equal(oracle.round_bf16(x.double().numpy()), ref)
+
+
+def test_sigmoid_of_bf16_logits_is_stored_in_bf16():
+    """Reading: a beta computed from bf16 logits is the bf16-stored sigmoid (ties to even),
+    and that rounding changes the result (it is not a no-op)."""
+    import torch
+    q, k, v, la, b, s0, _ = _raw_problem(5, "scalar")
+    qn, kn = oracle.l2_normalize(q), oracle.l2_normalize(k)
+    bl = torch.from_numpy(b).to(torch.bfloat16)
+    o1, f1 = oracle.forward_fused(qn, kn, v, la, bl, s0, beta_sigmoid=True)
+    br = oracle.round_bf16(oracle.sigmoid(bl))
+    o2, f2 = oracle.forward(qn, kn, v, la, br, s0)
+    assert np.array_equal(o1, o2) and np.array_equal(f1, f2)
+    o3, _ = oracle.forward(qn, kn, v, la, oracle.sigmoid(bl), s0)
+    assert np.abs(o3 - o1).max() > 1e-6
+    # fp32 / fp64 logits keep the unrounded sigmoid
+    o4, _ = oracle.forward_fused(qn, kn, v, la, b, s0, beta_sigmoid=True)
+    o5, _ = oracle.forward(qn, kn, v, la, oracle.sigmoid(b), s0)
+    assert np.array_equal(o4, o5)

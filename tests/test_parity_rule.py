@@ -31,3 +31,23 @@ def test_rounded_exact_result_passes_and_perturbed_fails():
 def test_nonfinite_fails():
     e, _ = err(torch.tensor([1.0, float("nan")]), np.array([1.0, 1.0]), "f32")
     assert e == np.inf
+
+
+def test_gated_rule_carries_the_bound_through_the_gate():
+    """A deviation within the operation's bound, scaled by the gate, passes; a wrong gate
+    (sigmoid for silu) or an ungated output fails."""
+    import oracle
+    from parity import err_gated
+    rng = np.random.default_rng(1)
+    o = rng.standard_normal((32, 128))
+    z = rng.standard_normal((32, 128))
+    gate = oracle.silu(z)
+    rms = np.sqrt((o ** 2).mean())
+    # within the bound: deviation 1e-2 RMS before the gate
+    g = torch.from_numpy((o + 1e-2 * rms * rng.uniform(-1, 1, o.shape)) * gate).float()
+    e, tol = err_gated(g, o, gate, "bf16")
+    assert e <= tol
+    e, _ = err_gated(torch.from_numpy(o * oracle.sigmoid(z)).float(), o, gate, "bf16")
+    assert e > tol
+    e, _ = err_gated(torch.from_numpy(o).float(), o, gate, "bf16")
+    assert e > tol
