@@ -45,16 +45,22 @@
 //
 // Fused neighbours (DR_FUSE_* of include/dr.h: L2-normalised q and k, beta from logits, the
 // SiLU output gate of the Gated DeltaNet layer, page "linear-attention gated-deltanet
-// guide", section 4).  Every product above is bilinear in the rows of Q and K, so with
-// nq_r = 1 / |q_r| and nk_r = 1 / |k_r| (computed from the bf16 tiles in shared memory, two
-// threads per row) the normalisation folds into scalings the kernel already applies in
-// fp32 and the tiles stay as loaded: X's entries get nq_r nk_s or nk_r nk_s in the P and A
-// builds, T diag(beta G) becomes T diag(beta G nk), diag(delta) becomes diag(delta nk) and
-// the output's G_r becomes G_r nq_r.  The gate warp takes beta = sigmoid(logit) rounded to
-// bf16, beta's storage dtype (so that, as for a stored beta, the diagonal of the U operand
-// T diag(beta) is exact).  The output warps multiply by silu(z).  z's tile is prefetched into L2 with the chunk's q, k, v and
-// copied by TMA into the stage's V slot as soon as the state update has read that slot
-// (the MMA warp waits for it), which is before the output step needs it.
+// guide", section 4).  With N = diag(nk), nk_r = 1 / |k_r|, and nq_r = 1 / |q_r|, every
+// product is bilinear in the rows of Q and K, so the tiles stay as loaded and the norms
+// enter scalings the kernel applies in fp32 anyway: P_rs gets nq_r nk_s, the state update's
+// diag(delta) becomes diag(delta nk), the output's G_r becomes G_r nq_r, and the U and W
+// operands are T diag(beta) and T diag(beta G nk).  Only A_rs = beta_r nk_r nk_s (...) would
+// need every norm while A is built; the kernel builds instead the similar B = N A N^-1,
+// B_rs = beta_r nk_r^2 (...), whose row r needs only |k_r| (summed by the row's own
+// thread), solves T_B = (I + B)^-1 and writes the operands of T = N^-1 T_B N:
+// (T diag beta)_rs = |k_r| T_B,rs nk_s beta_s.  So no extra barrier is needed; the four
+// warps that build no A rows compute the norm vectors meanwhile.  The diagonal of the U
+// operand stays exact: T_rr = 1 and the gate warp takes beta = sigmoid(logit) rounded to
+// bf16, beta's storage dtype, as a stored beta would be.  The output warps multiply by
+// silu(z).  z's tile is prefetched into L2 with the chunk's q, k, v and copied by TMA into
+// the stage's Q tiles as soon as (Q S)^T has read them (the MMA warp waits for it), two MMA
+// groups before the output step needs it; the output is then staged in the V slot (and the
+// K tiles for fp32).
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -92,12 +98,12 @@ constexpr uint32_t SM_P = SM_A + 16384;       // the next chunk's P high | P low
                                               // its E^T P^T)
 constexpr uint32_t SM_SMALL = SM_P + 16384;   // gate vectors of two chunks, solve scratch
 constexpr uint32_t SM_TOTAL = SM_SMALL + 8192;
-// fused neighbours only: norm vectors of two chunks [2][5][64] (nq, nk, G nk, delta nk,
-// G nq)
+// fused neighbours only: norm vectors of two chunks [2][7][64]: nq, nk, G nq, beta nk,
+// G nk, |k| (1 / nk) and delta nk
 constexpr uint32_t SM_NRM = SM_TOTAL;
-constexpr uint32_t SM_TOTAL_FUSED = SM_NRM + 2560;
+constexpr uint32_t SM_TOTAL_FUSED = SM_NRM + 3584;
 static_assert(SM_TOTAL_FUSED + 1024 <= 227 * 1024, "layout");
-enum { NV_NQ = 0, NV_NK = 1, NV_GK = 2, NV_DK = 3, NV_GQ = 4 };
+enum { NV_NQ = 0, NV_NK = 1, NV_GQ = 2, NV_BK = 3, NV_GK = 4, NV_RK = 5, NV_DK = 6 };
 constexpr uint32_t TM_S = 0, TM_D = 128, TM_X = 256, TM_U = 320, TM_W = 384, TM_PE = 448;
 // TM_D: [ (W S)^T | (Q S)^T ];  TM_X: [Q; K] K^T;  TM_PE: E^T P^T
 // Largest in-chunk log-decay span for which exp(g_r - g_s) is formed as a product of two
@@ -125,7 +131,9 @@ struct TcArgs {
     float *ws_phi, *ws_s0, *ws_start;
 };
 
-template <typename Tout, int GATE>
+// FUSED: the fused neighbours' code is compiled in (each still switched by a.fuse); the
+// plain instantiation carries none of it.
+template <typename Tout, int GATE, bool FUSED>
 __global__ void __launch_bounds__(kCtaThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -182,10 +190,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     // raw gate words of two chunks: [slot][beta word | log alpha][64 tokens]
     uint32_t *sGate = reinterpret_cast<uint32_t *>(sVec + 1792);
     constexpr int kOutBoxes = sizeof(Tout) == 2 ? 2 : 4;   // 128-byte rows per output box
-    const bool l2 = (a.fuse & kFuseL2) != 0;
-    const bool zgate = (a.fuse & kFuseGate) != 0 && outputs;
+    const bool l2 = FUSED && (a.fuse & kFuseL2) != 0;
+    const bool zgate = FUSED && (a.fuse & kFuseGate) != 0 && outputs;
     // norm vectors of chunk `it` (set it % 2)
-    auto nvec = [&](int it, int k) { return reinterpret_cast<float *>(sm + SM_NRM) + (it & 1) * 320 + 64 * k; };
+    auto nvec = [&](int it, int k) { return reinterpret_cast<float *>(sm + SM_NRM) + (it & 1) * 448 + 64 * k; };
 
     if (tid == 0) {
         uint64_t *bars[] = {&bar_tma[0], &bar_tma[1], &bar_x, &bar_uw, &bar_d, &bar_q, &bar_s,
@@ -229,11 +237,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             if (zgate) tma_prefetch_4d(&tz, 64 * kb, h, t0, b);
         }
     };
-    auto issue_z = [&](int it) {   // (MMA warp) chunk `it`'s output gate input into its V slot
+    // (MMA warp) chunk `it`'s output gate input into its stage's Q tiles (dead once (Q S)^T
+    // has read them)
+    auto issue_z = [&](int it) {
         mbar_arrive_expect_tx(&bar_z, 16384);
         const int t0 = (c_begin + it) * 64;
         for (int kb = 0; kb < 2; ++kb)
-            tma_load_4d(stage(it) + OFF_V0 + kb * 8192, &tz, &bar_z, 64 * kb, h, t0, b);
+            tma_load_4d(stage(it) + kb * 16384, &tz, &bar_z, 64 * kb, h, t0, b);
+    };
+    // byte offset in the stage of output box kb: the Q tiles (bf16) or the Q and K tiles
+    // (fp32); with the gate, whose z holds the Q tiles, the V slot (bf16) or the K tiles and
+    // the V slot (fp32) -- all dead once E^T P^T has completed
+    auto obox = [&](int kb) -> uint32_t {
+        if (!zgate) return (uint32_t)kb * (sizeof(Tout) == 2 ? 16384u : 8192u);
+        if (sizeof(Tout) == 2) return OFF_V0 + 8192u * kb;
+        return kb < 2 ? OFF_K0 + 16384u * kb : OFF_V0 + 8192u * (kb - 2);
     };
     // beta (the aligned 32-bit word holding it) and log alpha of chunk `it`, two tokens per
     // lane of the gate warp, copied asynchronously two chunks ahead; one commit group per
@@ -276,7 +294,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             const uint32_t wd = gw[r];
             const uint16_t hb = (uint16_t)(((2 * tok) & 2) ? (wd >> 16) : (wd & 0xffffu));
             bt[e] = __bfloat162float(__ushort_as_bfloat16(hb));
-            if (a.fuse & kFuseSigmoid) bt[e] = t < a.T ? round_bf16(sigmoid_f(bt[e])) : 0.f;
+            if (FUSED && (a.fuse & kFuseSigmoid)) bt[e] = t < a.T ? round_bf16(sigmoid_f(bt[e])) : 0.f;
             l[e] = __uint_as_float(gw[64 + r]);
         }
         __syncwarp();
@@ -305,39 +323,44 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
         if (lane == 0) factored_s[it & 1] = fac;
     };
-    // (compute warps, fused L2 norm) wait for chunk `it`'s tiles, then 1 / |q_r| and
-    // 1 / |k_r| and their products with the chunk's gate vectors into norm set it % 2.  Row
-    // 128-byte halves: thread (row tid / 2, K-block tid % 2), the K-block 1 thread starting
-    // four 16-byte groups further so that each quarter-warp's loads hit eight bank groups.
-    auto norms = [&](int it) {
+    // (fused L2 norm) 1 / sqrt(|x|^2 + eps) of row r of chunk `it`'s Q (rows_k false) or K
+    // tile, after waiting for the tiles: the row's 128 values are 128 bytes of each K-block
+    // tile (a quarter-warp's 16-byte loads of consecutive rows hit eight bank groups)
+    auto inv_norm = [&](int it, bool rows_k, int r) {
         wait_bar(&bar_tma[it & 1], (it >> 1) & 1);
-        const int rq = tid >> 1, kb = tid & 1, r = rq & 63;
-        const unsigned char *src = stage(it) + (rq < 64 ? 0 : OFF_K0) + kb * 16384 + r * 128;
+        const unsigned char *src = stage(it) + (rows_k ? OFF_K0 : 0) + r * 128;
         float ss = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int cg = ((j + 4 * kb) & 7) ^ (r & 7);
-            const uint4 u = *reinterpret_cast<const uint4 *>(src + 16 * cg);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll 4
+            for (int j = 0; j < 8; ++j) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(src + kb * 16384 + 16 * (j ^ (r & 7)));
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
-                ss = fmaf(f.x, f.x, ss);
-                ss = fmaf(f.y, f.y, ss);
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+                    ss = fmaf(f.x, f.x, ss);
+                    ss = fmaf(f.y, f.y, ss);
+                }
             }
-        }
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        const float inv = rsqrtf(ss + kL2NormEps);
-        if (kb == 0) {
-            const float gr = vec(it, 1)[r];
-            if (rq < 64) {
-                nvec(it, NV_NQ)[r] = inv;
-                nvec(it, NV_GQ)[r] = gr * inv;
-            } else {
-                nvec(it, NV_NK)[r] = inv;
-                nvec(it, NV_GK)[r] = gr * inv;
-                nvec(it, NV_DK)[r] = vec(it, 2)[r] * inv;
-            }
+        return rsqrtf(ss + kL2NormEps);
+    };
+    // (the four warps that build no A rows: quarters 0 and 1) chunk `it`'s norm vectors, one
+    // row of Q or K per thread
+    auto norm_vecs = [&](int it) {
+        const int i = 64 * half + row;   // 0..127: Q rows, then K rows
+        const int r = i & 63;
+        const float inv = inv_norm(it, i >= 64, r);
+        const float gr = vec(it, 1)[r];
+        if (i < 64) {
+            nvec(it, NV_NQ)[r] = inv;
+            nvec(it, NV_GQ)[r] = gr * inv;
+        } else {
+            nvec(it, NV_NK)[r] = inv;
+            nvec(it, NV_BK)[r] = vec(it, 3)[r] * inv;
+            nvec(it, NV_GK)[r] = gr * inv;
+            nvec(it, NV_RK)[r] = 1.f / inv;
+            nvec(it, NV_DK)[r] = vec(it, 2)[r] * inv;
         }
     };
     // (MMA warp) wait for chunk `it`'s tiles, then X = [Q; K] K^T into TM_X
@@ -358,22 +381,28 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     // bf16 high/low at SM_P; quarters 0 and 1)
     auto build_pa = [&](int it, bool rows_a, int col_half) {
         if ((quarter >= 2) != rows_a) return;
+        const int r = quarter < 2 ? row : row - 64;
+        float nk2 = 1.f;   // A rows of B (fused norm): nk_r^2, summed before X is held
+        if (l2 && rows_a) {
+            const float nk = inv_norm(it, true, r);
+            nk2 = nk * nk;
+        }
         float x[32];
         tmem_ld32(tm + TM_X + 32 * col_half, x);
         tmem_wait_ld();
         const int c0 = 32 * col_half;
-        const int r = quarter < 2 ? row : row - 64;
         const float *sG = vec(it, 0), *sBeta = vec(it, 3), *sE = vec(it, 4), *sF = vec(it, 5);
-        if (l2) {   // x_rs nq_r nk_s (P rows) or nk_r nk_s (A rows)
+        if (l2 && !rows_a) {   // P_rs nq_r nk_s
             const float *nk = nvec(it, NV_NK);
-            const float rs = rows_a ? nk[r] : nvec(it, NV_NQ)[r];
+            const float nq = nvec(it, NV_NQ)[r];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const float4 n4 = *reinterpret_cast<const float4 *>(nk + c0 + 4 * q);
-                x[4 * q] *= rs * n4.x; x[4 * q + 1] *= rs * n4.y;
-                x[4 * q + 2] *= rs * n4.z; x[4 * q + 3] *= rs * n4.w;
+                x[4 * q] *= nq * n4.x; x[4 * q + 1] *= nq * n4.y;
+                x[4 * q + 2] *= nq * n4.z; x[4 * q + 3] *= nq * n4.w;
             }
         }
+
         float dec[32];   // exp(g_r - g_s), s = c0 + u
         if (factored_s[it & 1]) {
             const float er = sE[r];
@@ -406,7 +435,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     make_uint4(pl[4 * q4], pl[4 * q4 + 1], pl[4 * q4 + 2], pl[4 * q4 + 3]);
             }
         } else {
-            const float br = sBeta[r];
+            const float br = sBeta[r] * nk2;   // B_rs = beta_r nk_r^2 ... with the fused norm
             float *sA = reinterpret_cast<float *>(sm + SM_A);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
@@ -425,11 +454,30 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
     };
     // (compute warps) T = (I + A)^-1 of chunk `it` (fp32, swizzled, over the S^T operand's
-    // first half) with T diag(beta) and T diag(beta G) in bf16 at SM_TB
-    auto solve = [&](int it) {
-        solve_unit_lower64<true, true>(reinterpret_cast<const float *>(sm + SM_A),
-                                       reinterpret_cast<float *>(sm + SM_T), sM, sm + SM_TB,
-                                       vec(it, 3), l2 ? nvec(it, NV_GK) : vec(it, 1), tid);
+    // first half) with T diag(beta) and T diag(beta G) in bf16 at SM_TB; with the fused
+    // norm, the operands of N^-1 (I + B)^-1 N
+    const float *sA_c = reinterpret_cast<const float *>(sm + SM_A);
+    auto solve_out = [&](int it) {
+        return SolveOut<true, true, true>{reinterpret_cast<float *>(sm + SM_T), sm + SM_TB, vec(it, 3),
+                                          vec(it, 1), nullptr};
+    };
+    auto solve_out_l2 = [&](int it) {
+        return SolveOut<true, true, true, true>{reinterpret_cast<float *>(sm + SM_T), sm + SM_TB,
+                                                nvec(it, NV_BK), nvec(it, NV_GK), nvec(it, NV_RK)};
+    };
+    auto solve_diag = [&](int it) {
+        if (l2) solve_diag64(sA_c, solve_out_l2(it), tid);
+        else solve_diag64(sA_c, solve_out(it), tid);
+    };
+    auto solve_merge = [&](int it) {   // warps 0..3
+        if (l2) solve_merge64(sA_c, solve_out_l2(it), sM, tid, 2);
+        else solve_merge64(sA_c, solve_out(it), sM, tid, 2);
+    };
+    auto solve = [&](int it) {   // all compute warps; starts after and ends with a barrier
+        solve_diag(it);
+        named_sync(1, kThreads);
+        if (warp < 4) solve_merge(it);
+        named_sync(1, kThreads);
     };
 
     // prologue loads: stages 0 and 1, raw gates of chunks 0 and 1
@@ -450,6 +498,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         if (lane == 0 && n_it > 0) {
             uint64_t *last = &bar_x;   // most recent commit (drained on abort)
             uint32_t last_par = 0;
+            int z_last = -1;           // chunk of the most recent z copy
             auto issue_uw = [&](int it) {   // U^T = V^T (T diag beta)^T, W^T = K^T (T diag(beta G))^T
                 unsigned char *st = stage(it);
                 if (!zero_u)
@@ -495,6 +544,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     }
                 mma_commit(&bar_q);
                 last = &bar_q; last_par = par;
+                if (zgate) {   // the Q tiles are dead once (Q S)^T has read them
+                    if (!wait_cycles(&bar_q, par)) { fail(); break; }
+                    issue_z(it);
+                    z_last = it;
+                }
                 // S^T += (E^T diag delta) K, then PE = E^T P^T  (high/low pairs)
                 if (!wait_cycles(&full_s, par)) { fail(); break; }
                 tc_fence_after();
@@ -516,11 +570,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                                      desc_add(dK0, pb[part] + ks * 32), ID_KK_N64, (part | ks) != 0);
                 mma_commit(&bar_pe);
                 last = &bar_pe; last_par = par;
-                if (zgate) {   // the V slot is dead once the state update has read it
-                    if (!wait_cycles(&bar_s, par)) { fail(); break; }
-                    issue_z(it);
-                    last = &bar_z; last_par = par;
-                }
                 // the next chunk's U/W, then the chunk after's X
                 if (it + 1 < n_it) {
                     if (!wait_cycles(&full_uw, (it + 1) & 1)) { fail(); break; }
@@ -537,7 +586,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             }
             if (abort_s) {   // drain this warp's MMAs and copies (bounded)
                 wait_cycles(last, last_par);
-                if (last == &bar_z) wait_cycles(&bar_pe, last_par);
+                if (z_last >= 0) wait_cycles(&bar_z, (uint32_t)z_last & 1);
             }
         }
         __syncwarp();
@@ -560,8 +609,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         // prologue: chunk 0's gates, A and P, solve; chunk 1's gates
         if (warp == kGateWarp) scan_gates(0);
         named_sync(1, kThreads);
-        if (l2) {
-            norms(0);
+        if (l2) {   // the P build reads every norm
+            if (quarter < 2) norm_vecs(0);
             named_sync(1, kThreads);
         }
         wait_bar(&bar_x, 0);
@@ -629,10 +678,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
         // ---- 3. A of the next chunk (its X arrived meanwhile)
         if (next) {
-            if (l2) {
-                norms(it + 1);
-                named_sync(1, kThreads);
-            }
+            if (l2 && quarter < 2) norm_vecs(it + 1);   // read from step 5 on
             wait_bar(&bar_x, (it + 1) & 1);
             build_pa(it + 1, true, half);
         }
@@ -680,15 +726,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         //         this chunk's output o = G_r (Q S)^T + E^T P^T (staged in the stage's Q and K
         //         tiles, dead once E^T P^T is done) and the next chunk's P (E^T P^T has read
         //         SM_P)
-        const SolveOut<true, true, true> sout{reinterpret_cast<float *>(sm + SM_T), sm + SM_TB, vec(it + 1, 3),
-                                              l2 ? nvec(it + 1, NV_GK) : vec(it + 1, 1)};
         if (next) {
             wait_bar(&bar_q, par);
-            solve_diag64(reinterpret_cast<const float *>(sm + SM_A), sout, tid);
+            solve_diag(it + 1);
             named_sync(1, kThreads);
         }
         if (warp < 4) {
-            if (next) solve_merge64(reinterpret_cast<const float *>(sm + SM_A), sout, sM, tid, 2);
+            if (next) solve_merge(it + 1);
         } else {
             wait_bar(&bar_pe, par);
             if (outputs) {
@@ -704,20 +748,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
                     for (int u = 0; u < 32; ++u) o[u] = fmaf(sGam[32 * hh + u], o[u], pe[u]);
                     if (zgate) {
-                        const unsigned char *zt = st + OFF_V0 + (j >> 6) * 8192;
+                        const unsigned char *zt = st + (j >> 6) * 16384;
 #pragma unroll
                         for (int u = 0; u < 32; ++u)
                             o[u] *= silu_tanh(__bfloat162float(
                                 *reinterpret_cast<const __nv_bfloat16 *>(zt + sw128_off(32 * hh + u, j & 63))));
                     }
                     if (sizeof(Tout) == 2) {
-                        unsigned char *dst = st + (j >> 6) * 16384;
+                        unsigned char *dst = st + obox(j >> 6);
 #pragma unroll
                         for (int u = 0; u < 32; ++u)
                             *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * hh + u, j & 63)) =
                                 __float2bfloat16_rn(o[u]);
                     } else {
-                        unsigned char *dst = st + (j >> 5) * 8192;
+                        unsigned char *dst = st + obox(j >> 5);
                         const int cj = j & 31;
 #pragma unroll
                         for (int u = 0; u < 32; ++u) {
@@ -735,10 +779,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 named_sync(3, 128);
                 if (tid == kTmaThread) {
                     constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
-                    constexpr uint32_t box = sizeof(Tout) == 2 ? 16384 : 8192;
 #pragma unroll
                     for (int kb = 0; kb < kOutBoxes; ++kb)
-                        tma_store_4d(&to, st + kb * box, cols * kb, h, t0, b);
+                        tma_store_4d(&to, st + obox(kb), cols * kb, h, t0, b);
                     bulk_commit();
                     bulk_wait_read_all();   // the stage is reloaded next
                 }
@@ -847,16 +890,24 @@ bool make_map(CUtensorMap *m, const void *base, int64_t B, int64_t T, int64_t H,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <typename Tout, int GATE, bool FUSED>
+int launch_f(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+             const CUtensorMap &mo, const CUtensorMap &mz, const TcArgs &ta, unsigned grid,
+             cudaStream_t stream) {
+    const int smem = (int)(FUSED ? SM_TOTAL_FUSED : SM_TOTAL) + 1024;
+    if (cudaFuncSetAttribute(chunk_tc_kernel<Tout, GATE, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+        return kErrCuda;
+    chunk_tc_kernel<Tout, GATE, FUSED><<<grid, kCtaThreads, smem, stream>>>(mq, mk, mv, mo, mz, ta);
+    return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+}
+
 template <typename Tout, int GATE>
 int launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
              const CUtensorMap &mo, const CUtensorMap &mz, const TcArgs &ta, unsigned grid,
              cudaStream_t stream) {
-    const int smem = (int)(ta.fuse ? SM_TOTAL_FUSED : SM_TOTAL) + 1024;
-    if (cudaFuncSetAttribute(chunk_tc_kernel<Tout, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SM_TOTAL_FUSED + 1024) != cudaSuccess)
-        return kErrCuda;
-    chunk_tc_kernel<Tout, GATE><<<grid, kCtaThreads, smem, stream>>>(mq, mk, mv, mo, mz, ta);
-    return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+    return ta.fuse ? launch_f<Tout, GATE, true>(mq, mk, mv, mo, mz, ta, grid, stream)
+                   : launch_f<Tout, GATE, false>(mq, mk, mv, mo, mz, ta, grid, stream);
 }
 
 }  // namespace

@@ -112,18 +112,20 @@ __device__ __forceinline__ int a_index(int r, int s) {
 //      T[32:64, 0:32] = -T[32:64, 32:64] M (four warps, one 16 x 16 tile each).
 // Each element is written, once final, also as T diag(beta) in bf16 (a 128-byte-swizzled
 // K-major 64 x 64 tile at TB) and, with kPair, as T diag(beta G) at TB + 8192: the U and W
-// operands.  Products use TF32 mma.sync with fp32 accumulation.  M needs 1024 floats.
+// operands.  With kRow the operands are diag(rowf) T diag(beta) and diag(rowf) T diag(beta G)
+// (a similarity of T, the fp32 copy staying T).  Products use TF32 mma.sync with fp32 accumulation.  M needs 1024 floats.
 // Step 1 is solve_diag64 (256 threads); steps 2 and 3 are solve_merge64 (warps 0..3 only,
 // synchronising on their own named barrier), so that warps 4..7 are free meanwhile.
-template <bool kPair, bool kSwizzledT, bool kPreRound = false>
+template <bool kPair, bool kSwizzledT, bool kPreRound = false, bool kRow = false>
 struct SolveOut {
     float *T;
     unsigned char *TB;
     const float *beta, *gam;
+    const float *rowf;   // kRow only
     // final element (r, s) of T: fp32 copy for the later levels, and the bf16 MMA operands
     __device__ __forceinline__ void fin(int r, int s, float v) const {
         T[t_index<kSwizzledT>(r, s)] = kPreRound ? round_tf32(v) : v;
-        const float vb = v * beta[s];
+        const float vb = kRow ? v * beta[s] * rowf[r] : v * beta[s];
         const uint32_t off = sw128_off(r, s);
         *reinterpret_cast<__nv_bfloat16 *>(TB + off) = __float2bfloat16_rn(vb);
         if constexpr (kPair)
@@ -133,7 +135,12 @@ struct SolveOut {
     __device__ __forceinline__ void fin2(int r, int s, float v0, float v1) const {
         *reinterpret_cast<float2 *>(T + t_index<kSwizzledT>(r, s)) =
             kPreRound ? make_float2(round_tf32(v0), round_tf32(v1)) : make_float2(v0, v1);
-        const float b0 = v0 * beta[s], b1 = v1 * beta[s + 1];
+        float b0 = v0 * beta[s], b1 = v1 * beta[s + 1];
+        if constexpr (kRow) {
+            const float f = rowf[r];
+            b0 *= f;
+            b1 *= f;
+        }
         const uint32_t off = sw128_off(r, s);
         *reinterpret_cast<uint32_t *>(TB + off) = pack_bf16(b0, b1);
         if constexpr (kPair)
@@ -142,9 +149,10 @@ struct SolveOut {
 };
 
 // Step 1 (256 threads, tid 0..255): the diagonal blocks and the zero blocks of the operands.
-template <bool kPair, bool kSwizzledT, bool kPreRound>
+template <bool kPair, bool kSwizzledT, bool kPreRound, bool kRow>
 __device__ __forceinline__ void solve_diag64(const float *A,
-                                             const SolveOut<kPair, kSwizzledT, kPreRound> &out, int tid) {
+                                             const SolveOut<kPair, kSwizzledT, kPreRound, kRow> &out,
+                                             int tid) {
     const int lane = tid & 31;
     const int o = 16 * (tid >> 6), c = (tid >> 2) & 15, part = tid & 3;
     const int owner = lane & ~3;
@@ -191,9 +199,9 @@ __device__ __forceinline__ void solve_diag64(const float *A,
 // the off-diagonal blocks of A hold TF32-rounded values (the products take them as they are;
 // the result is the same as rounding at each load), and level 2 runs on four warps, one
 // 8-column half of a block each (the second product needs only its own half of the first).
-template <bool kPair, bool kSwizzledT, bool kPreRound>
+template <bool kPair, bool kSwizzledT, bool kPreRound, bool kRow>
 __device__ __forceinline__ void solve_merge64(const float *A,
-                                              const SolveOut<kPair, kSwizzledT, kPreRound> &out,
+                                              const SolveOut<kPair, kSwizzledT, kPreRound, kRow> &out,
                                               float *M, int tid, uint32_t bar_id) {
     constexpr bool kCvt = !kPreRound;
     const float *T = out.T;
@@ -261,7 +269,7 @@ template <bool kPair = true, bool kSwizzledT = false>
 __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, float *M,
                                                    unsigned char *TB, const float *beta,
                                                    const float *gam, int tid) {
-    const SolveOut<kPair, kSwizzledT> out{T, TB, beta, gam};
+    const SolveOut<kPair, kSwizzledT> out{T, TB, beta, gam, nullptr};
     solve_diag64(A, out, tid);
     named_sync(1, 256);
     if (tid < 128) solve_merge64(A, out, M, tid, 2);
