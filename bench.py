@@ -49,10 +49,15 @@ def peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
+# Sources of the headline kernel (chunk_tc_kernel): the traffic figure below was captured
+# from these; it is reported only while they are unchanged.
+HEADLINE_SOURCES = ("chunk_tc.cu", "tc_common.cuh", "umma.cuh", "common.cuh", "chunk_layout.h")
+
+
 def csrc_hash():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "gated_delta_rule_15_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
+    for name in HEADLINE_SOURCES:
         with open(os.path.join(d, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]

@@ -242,3 +242,76 @@ def step_fused(q, k, v, log_alpha, beta, state, *, qk_l2norm=False, beta_sigmoid
     if z is not None:
         out = out * silu(to_f64(z))
     return out, st
+
+
+# ---------------------------------------------------------------- backward
+# Reverse mode of the token loop of ``forward`` (the recurrence of the page "NLP: linear
+# attention summary", KDA section, in the order of the `gated_delta_rule` loop of the page
+# "linear-attention gated-deltanet guide", section 4): with the loss
+#     L = sum(d_out * out) + sum(d_final * final_state),
+# the step S' = Diag(a_t) S_{t-1}, p = S'^T k_t, e = beta_t (v_t - p), S_t = S' + k_t e^T,
+# o_t = S_t^T q_t is differentiated line by line, last token first.  States are recomputed
+# from checkpoints every `block` tokens.  Pinned by central differences of ``forward``.
+def backward(q, k, v, log_alpha, beta, init_state, d_out, d_final=None, *, block: int = 64):
+    """Gradients of L with respect to every input, in float64:
+    (dq [B,T,H,dk], dk [B,T,H,dk], dv [B,T,H,dv], dlog_alpha (shape of log_alpha, or None),
+    dbeta [B,T,H], dinit [B,H,dk,dv])."""
+    q, k, v, beta = to_f64(q), to_f64(k), to_f64(v), to_f64(beta)
+    la, s0, do = to_f64(log_alpha), to_f64(init_state), to_f64(d_out)
+    dfin = to_f64(d_final)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    gate = _gate_of(la, (B, T, H), dk)
+    # [B,H,T,...] views; a = alpha per key channel
+    qt, kt, vt, dot = (np.moveaxis(x, 2, 1) for x in (q, k, v, do))
+    bt = np.moveaxis(beta, 2, 1)
+    if gate == GATE_NONE:
+        a = np.ones((B, H, T, dk))
+    elif gate == GATE_SCALAR:
+        a = np.repeat(np.exp(np.moveaxis(la, 2, 1))[..., None], dk, axis=-1)
+    else:
+        a = np.exp(np.moveaxis(la, 2, 1))
+
+    def step_fwd(S, t):
+        Sd = a[:, :, t, :, None] * S
+        p = np.einsum("bhij,bhi->bhj", Sd, kt[:, :, t])
+        e = bt[:, :, t, None] * (vt[:, :, t] - p)
+        return Sd, p, e, Sd + kt[:, :, t, :, None] * e[:, :, None, :]
+
+    S = np.zeros((B, H, dk, dv)) if s0 is None else s0.copy()
+    ckpt = {}
+    for t in range(T):
+        if t % block == 0:
+            ckpt[t] = S.copy()
+        S = step_fwd(S, t)[3]
+    dS = np.zeros((B, H, dk, dv)) if dfin is None else dfin.copy()
+    gq, gk, gv = np.zeros_like(qt), np.zeros_like(kt), np.zeros_like(vt)
+    gb = np.zeros_like(bt)
+    gla = np.zeros((B, H, T, dk))      # d log alpha per key channel
+    for t0 in reversed(range(0, T, block)):
+        t1 = min(T, t0 + block)
+        prev = [ckpt[t0]]               # state before each step of the block
+        for t in range(t0, t1 - 1):
+            prev.append(step_fwd(prev[-1], t)[3])
+        for t in reversed(range(t0, t1)):
+            Sd, p, e, St = step_fwd(prev[t - t0], t)
+            dS = dS + qt[:, :, t, :, None] * dot[:, :, t, None, :]        # o_t = S_t^T q_t
+            gq[:, :, t] = np.einsum("bhij,bhj->bhi", St, dot[:, :, t])
+            de = np.einsum("bhij,bhi->bhj", dS, kt[:, :, t])          # through S_t = S' + k e^T
+            gk[:, :, t] = np.einsum("bhij,bhj->bhi", dS, e)
+            dSd = dS.copy()
+            gv[:, :, t] = bt[:, :, t, None] * de                       # e = beta (v - p)
+            gb[:, :, t] = (de * (vt[:, :, t] - p)).sum(-1)
+            dp = -bt[:, :, t, None] * de
+            dSd = dSd + kt[:, :, t, :, None] * dp[:, :, None, :]       # p = S'^T k
+            gk[:, :, t] += np.einsum("bhij,bhj->bhi", Sd, dp)
+            gla[:, :, t] = (dSd * Sd).sum(-1)                          # S' = Diag(a) S
+            dS = a[:, :, t, :, None] * dSd
+    back = lambda x: np.ascontiguousarray(np.moveaxis(x, 1, 2))
+    if gate == GATE_NONE:
+        dla = None
+    elif gate == GATE_SCALAR:
+        dla = back(gla.sum(-1))
+    else:
+        dla = back(gla)
+    return back(gq), back(gk), back(gv), dla, back(gb), dS

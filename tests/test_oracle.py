@@ -572,3 +572,68 @@ def test_sigmoid_of_bf16_logits_is_stored_in_bf16():
     o4, _ = oracle.forward_fused(qn, kn, v, la, b, s0, beta_sigmoid=True)
     o5, _ = oracle.forward(qn, kn, v, la, oracle.sigmoid(b), s0)
     assert np.array_equal(o4, o5)
+
+
+def _bwd_problem(seed, gate, B=1, T=7, H=2, dk=5, dv=4):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, T, H, dk))
+    k = rng.standard_normal((B, T, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, H, dv))
+    b = rng.uniform(0.1, 0.9, (B, T, H))
+    la = None if gate == "none" else -rng.uniform(0.0, 0.5, (B, T, H) if gate == "scalar"
+                                                  else (B, T, H, dk))
+    s0 = rng.standard_normal((B, H, dk, dv)) * 0.3
+    do = rng.standard_normal((B, T, H, dv))
+    dfin = rng.standard_normal((B, H, dk, dv))
+    return q, k, v, la, b, s0, do, dfin
+
+
+@pytest.mark.parametrize("gate", ["none", "scalar", "channel"])
+def test_backward_matches_central_differences(gate):
+    """Every gradient of L = <d_out, out> + <d_final, final> equals the central difference
+    of the (pinned) forward, element by element, on a tiny problem."""
+    q, k, v, la, b, s0, do, dfin = _bwd_problem(3, gate)
+    grads = oracle.backward(q, k, v, la, b, s0, do, dfin)
+    names = ["q", "k", "v", "la", "b", "s0"]
+    args = [q, k, v, la, b, s0]
+
+    def loss(a):
+        o, f = oracle.forward(*a)
+        return float((do * o).sum() + (dfin * f).sum())
+
+    h = 1e-6
+    for idx, (name, x, g) in enumerate(zip(names, args, grads)):
+        if x is None:
+            assert g is None
+            continue
+        assert g.shape == x.shape, name
+        fd = np.zeros_like(x)
+        for e in range(x.size):
+            xp, xm = x.copy(), x.copy()
+            xp.flat[e] += h
+            xm.flat[e] -= h
+            ap, am = list(args), list(args)
+            ap[idx], am[idx] = xp, xm
+            fd.flat[e] = (loss(ap) - loss(am)) / (2 * h)
+        scale = max(1.0, np.abs(fd).max())
+        np.testing.assert_allclose(g, fd, rtol=0, atol=1e-7 * scale, err_msg=name)
+
+
+def test_backward_checkpoint_interval_is_invisible():
+    """Recomputing states from checkpoints every 3 tokens gives the same gradients bit for
+    bit as one checkpoint."""
+    q, k, v, la, b, s0, do, dfin = _bwd_problem(4, "channel", T=11)
+    g1 = oracle.backward(q, k, v, la, b, s0, do, dfin, block=3)
+    g2 = oracle.backward(q, k, v, la, b, s0, do, dfin, block=64)
+    for a, c in zip(g1, g2):
+        assert np.array_equal(a, c)
+
+
+def test_backward_without_final_gradient_or_state():
+    """d_final = None is a zero final-state gradient, init_state = None a zero state."""
+    q, k, v, la, b, s0, do, dfin = _bwd_problem(5, "scalar")
+    g1 = oracle.backward(q, k, v, la, b, None, do, None)
+    g2 = oracle.backward(q, k, v, la, b, np.zeros_like(s0), do, np.zeros_like(dfin))
+    for a, c in zip(g1, g2):
+        assert np.array_equal(a, c)
