@@ -1,0 +1,521 @@
+// chunk_bwd.cu -- backward of the chunkwise forward on the fp32 CUDA cores: the gradients of
+// L = <d_out, out> + <d_final, final_state> with respect to q, k, v, log alpha, beta and the
+// initial state.
+//
+// The pages ask for chunkwise kernels for training (page "linear-attention gated-deltanet
+// guide", section 5) and print no backward; this one differentiates the chunk form of
+// chunk_simt.cu.  Per chunk, started from S0, with g_r the cumulative log decay, G = exp(g),
+// gamma = G at the chunk's last token and the pair factor D_rs = exp(g_r - g_s) (s <= r, per
+// key channel, <= 1):
+//
+//   A_rs = b_r sum_i k_ri k_si D_rs,i (s < r),  T = (I + A)^-1,  R = diag(b) (V - (K*G) S0),
+//   E = T R,  P_rs = sum_i q_ri k_si D_rs,i (s <= r),  O = (Q*G) S0 + P E,
+//   S_C = Diag(gamma) S0 + Kd^T E,  Kd_r = k_r * exp(g_C - g_r).
+//
+// Given dO and dS_C:
+//   dE = P^T dO + Kd dS_C,   dR = T^T dE,   dP = tril(dO E^T),   dA = -stril(dR E^T)
+//   dS0 = Diag(gamma) dS_C + (Q*G)^T dO - W^T dE          (W = T diag(b) (K*G))
+//   dv_r = b_r dR_r,   db_r = dR_r . (v_r - ((K*G) S0)_r) + sum_{s<r} dA_rs A_rs / b_r
+//   and dq, dk, dg from the products holding q, k and g (chunk_grad_kernel, phase by phase);
+//   d log alpha_t = sum_{r >= t} dg_r, the last token's dg also taking the terms of gamma.
+//
+// Three steps after the CUDA-core forward has recomputed W, U, Q*G, Kd, P, gamma, T and the
+// state at every chunk's start (the checkpoints):
+//   chunk_dstate_kernel  one CTA per (b, h, 32 state columns), chunks in reverse: stores
+//                        dS_C of every chunk and returns dS0 of the first;
+//   chunk_grad_kernel    one CTA per (b, h, chunk), all chunks in parallel: every gradient
+//                        of the chunk's tokens.
+#include "chunk_layout.h"
+#include "common.cuh"
+
+namespace dr {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kLdA = 65;   // padded row stride of [64][64] tiles
+constexpr int kDvt = 32;   // state columns per CTA of the reverse pass
+
+// Workspace of the backward, in floats, after the forward's slabs: T [n][C][C], checkpoints
+// [n][dk][dv], dS_C [n][dk][dv].
+struct BwdWorkspace {
+    ChunkWorkspace fw;
+    float *T, *ckpt, *dsc;
+};
+
+size_t bwd_floats(const ChunkProblem &p) {
+    const int64_t n = p.B * p.H * p.NC;
+    return simt_workspace_floats(p.B, p.H, p.NC, p.C, p.dk, p.dv) +
+           (size_t)(n * ((int64_t)p.C * p.C + 2 * (int64_t)p.dk * p.dv));
+}
+
+BwdWorkspace bwd_carve(void *base, const ChunkProblem &p) {
+    BwdWorkspace w;
+    w.fw = simt_workspace_carve(base, p.B, p.H, p.NC, p.C, p.dk, p.dv);
+    const int64_t n = p.B * p.H * p.NC;
+    float *f = (float *)base + simt_workspace_floats(p.B, p.H, p.NC, p.C, p.dk, p.dv);
+    w.T = f;     f += n * p.C * p.C;
+    w.ckpt = f;  f += n * (int64_t)p.dk * p.dv;
+    w.dsc = f;
+    return w;
+}
+
+struct DStateArgs {
+    const void *d_out;
+    const float *d_final;
+    float *d_init;
+    BwdWorkspace ws;
+    int64_t B, T, H;
+    int dv, C, NC;
+};
+
+size_t dstate_smem_bytes(int dk) {
+    return sizeof(float) * (size_t)(dk * kDvt + 3 * 64 * (dk + 4) + 2 * 64 * kDvt + 64 * kLdA + dk);
+}
+
+// Reverse state-gradient pass: dS starts as d_final; for each chunk, last first, it is
+// stored as that chunk's dS_C, then  dE = P^T dO + Kd dS,  dS <- Diag(gamma) dS + (Q*G)^T dO
+// - W^T dE.  Column j of dS only meets column j of dO, so a CTA owns 32 columns.
+template <int DK, typename Tg>
+__global__ void __launch_bounds__(kThreads) chunk_dstate_kernel(DStateArgs a) {
+    constexpr int LD = DK + 4;
+    extern __shared__ float4 smem4[];
+    float *sDS = reinterpret_cast<float *>(smem4);  // [DK][32]
+    float *sW = sDS + DK * kDvt;                    // [64][LD]
+    float *sQg = sW + 64 * LD;                      // [64][LD]
+    float *sKd = sQg + 64 * LD;                     // [64][LD]
+    float *sDO = sKd + 64 * LD;                     // [64][32]
+    float *sDE = sDO + 64 * kDvt;                   // [64][32]
+    float *sP = sDE + 64 * kDvt;                    // [64][kLdA]
+    float *sGam = sP + 64 * kLdA;                   // [DK]
+
+    const int tiles = a.dv / kDvt;
+    const int jt = blockIdx.x % tiles;
+    const int64_t bh = blockIdx.x / tiles;
+    const int64_t h = bh % a.H, b = bh / a.H;
+    const int C = a.C, NC = a.NC, dv = a.dv, tid = threadIdx.x;
+    const int j = tid & 31, rg = tid >> 5;
+    const int col = jt * kDvt + j;
+    const Tg *dout = (const Tg *)a.d_out;
+
+    for (int i = rg; i < DK; i += 8)
+        sDS[i * kDvt + j] = a.d_final ? a.d_final[(bh * DK + i) * dv + col] : 0.f;
+
+    for (int c = NC - 1; c >= 0; --c) {
+        const int64_t n = bh * NC + c;
+        const int64_t t0 = (int64_t)c * C;
+        const int Lc = (int)(a.T - t0 < (int64_t)C ? a.T - t0 : (int64_t)C);
+        const float *W = a.ws.fw.W + n * (int64_t)C * DK;
+        const float *Qg = a.ws.fw.Qg + n * (int64_t)C * DK;
+        const float *Kd = a.ws.fw.Kd + n * (int64_t)C * DK;
+        const float *P = a.ws.fw.P + n * (int64_t)C * C;
+        __syncthreads();   // the previous chunk's readers are done
+        for (int idx = tid; idx < C * (DK / 4); idx += kThreads) {
+            const int r = idx / (DK / 4), c4 = 4 * (idx % (DK / 4));
+            *reinterpret_cast<float4 *>(sW + r * LD + c4) = load4(W + r * DK + c4);
+            *reinterpret_cast<float4 *>(sQg + r * LD + c4) = load4(Qg + r * DK + c4);
+            *reinterpret_cast<float4 *>(sKd + r * LD + c4) = load4(Kd + r * DK + c4);
+        }
+        for (int idx = tid; idx < C * kDvt; idx += kThreads) {
+            const int r = idx / kDvt, jj = idx % kDvt;
+            sDO[idx] = r < Lc ? to_f32(dout[((b * a.T + t0 + r) * a.H + h) * dv + jt * kDvt + jj]) : 0.f;
+        }
+        for (int idx = tid; idx < C * C; idx += kThreads) sP[(idx / C) * kLdA + idx % C] = P[idx];
+        for (int i = tid; i < DK; i += kThreads) sGam[i] = a.ws.fw.gam[n * DK + i];
+        for (int i = rg; i < DK; i += 8) a.ws.dsc[(n * DK + i) * dv + col] = sDS[i * kDvt + j];
+        __syncthreads();
+        // dE = P^T dO + Kd dS  (rows r = rg + 8m)
+        for (int r = rg; r < C; r += 8) {
+            float acc = 0.f;
+            for (int s = r; s < C; ++s) acc = fmaf(sP[s * kLdA + r], sDO[s * kDvt + j], acc);
+            for (int i = 0; i < DK; ++i) acc = fmaf(sKd[r * LD + i], sDS[i * kDvt + j], acc);
+            sDE[r * kDvt + j] = acc;
+        }
+        __syncthreads();
+        // dS <- Diag(gamma) dS + (Q*G)^T dO - W^T dE  (rows i = rg + 8m; own entries only)
+        for (int i = rg; i < DK; i += 8) {
+            float acc = sGam[i] * sDS[i * kDvt + j];
+            for (int r = 0; r < C; ++r)
+                acc = fmaf(sQg[r * LD + i], sDO[r * kDvt + j], fmaf(-sW[r * LD + i], sDE[r * kDvt + j], acc));
+            sDS[i * kDvt + j] = acc;
+        }
+    }
+    if (a.d_init) {
+        __syncthreads();
+        for (int i = rg; i < DK; i += 8) a.d_init[(bh * DK + i) * dv + col] = sDS[i * kDvt + j];
+    }
+}
+
+struct GradArgs {
+    const void *q, *k, *v;
+    const float *log_alpha;
+    const void *beta;
+    const void *d_out;
+    BwdWorkspace ws;
+    void *dq, *dk, *dv;
+    float *d_log_alpha;
+    void *d_beta;
+    int64_t B, T, H;
+    int dv_, C, NC, gate;
+};
+
+size_t grad_smem_bytes(int dk, int dv) {
+    const int ldw = (dk > dv ? dk : dv) + 4;
+    return sizeof(float) * (size_t)(3 * 64 * (dk + 4) + 2 * 64 * ldw + 2 * 64 * kLdA + 64 + dk + 64);
+}
+
+// Every gradient of one chunk's tokens.  Thread (row r = tid / 4, part = tid % 4) owns key
+// channels i = part + 4m and value columns j = part + 4m of row r; its dq, dk and dg entries
+// accumulate in registers over the phases:
+//   0. q, k, beta, g (cumulative, per channel; a scalar gate is broadcast), T, P, dO;
+//   1. E = U - W S0;  dO S0^T  -> dq, dg;
+//   2. dE = P^T dO + Kd dS_C;  dP = tril(dO E^T) (over P);
+//   3. dR = T^T dE (over dE);
+//   4. dA = -stril(dR E^T) (over T);  dv = b dR;  db, part 1;  dR S0^T -> dk, dg;
+//      E dS_C^T -> dk, dg and the last token's dg;
+//   5. the pair products of P and A -> dq, dk, dg, db part 2;
+//   6. db, dq, dk out; dg summed from the last token back -> d log alpha.
+template <int DK, typename Tin, typename Tg>
+__global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
+    constexpr int LDK = DK + 4;
+    constexpr int NI = DK / 4;   // key channels per thread
+    extern __shared__ float4 smem4[];
+    const int dv = a.dv_;
+    const int ldw = (DK > dv ? DK : dv) + 4;
+    float *sQ = reinterpret_cast<float *>(smem4);  // [64][LDK] q (then dg)
+    float *sK = sQ + 64 * LDK;                     // [64][LDK] k
+    float *sG = sK + 64 * LDK;                     // [64][LDK] g per channel
+    float *sE = sG + 64 * LDK;                     // [64][ldw] E
+    float *sX = sE + 64 * ldw;                     // [64][ldw] dO -> dE -> dR -> E dS_C^T terms
+    float *sT = sX + 64 * ldw;                     // [64][kLdA] T -> dA
+    float *sP = sT + 64 * kLdA;                    // [64][kLdA] P -> dP
+    float *sB = sP + 64 * kLdA;                    // [64] beta
+    float *sDgC = sB + 64;                         // [DK] d g of the last token (gamma terms)
+    float *sRed = sDgC + DK;                       // [64] row sums
+
+    const Tin *q = (const Tin *)a.q, *k = (const Tin *)a.k, *v = (const Tin *)a.v;
+    const Tin *beta = (const Tin *)a.beta;
+    const Tg *dout = (const Tg *)a.d_out;
+    const int C = a.C, NC = a.NC, tid = threadIdx.x;
+    const int64_t n = blockIdx.x;
+    const int c = (int)(n % NC);
+    const int64_t bh = n / NC;
+    const int64_t h = bh % a.H, b = bh / a.H;
+    const int64_t t0 = (int64_t)c * C;
+    const int Lc = (int)(a.T - t0 < (int64_t)C ? a.T - t0 : (int64_t)C);
+    auto tok = [&](int r) -> int64_t { return (b * a.T + t0 + r) * a.H + h; };
+    const float *S0 = a.ws.ckpt + n * (int64_t)DK * dv;
+    const float *dSC = a.ws.dsc + n * (int64_t)DK * dv;
+    const float *Wn = a.ws.fw.W + n * (int64_t)C * DK;
+    const float *Un = a.ws.fw.U + n * (int64_t)C * dv;
+    const float *Kdn = a.ws.fw.Kd + n * (int64_t)C * DK;
+    const int r = tid >> 2, part = tid & 3;
+    const bool row_ok = r < C;
+
+    // ---- 0. inputs (rows past the sequence: zero, log alpha 0)
+    for (int idx = tid; idx < C * DK; idx += kThreads) {
+        const int rr = idx / DK, i = idx % DK;
+        const bool ok = rr < Lc;
+        sQ[rr * LDK + i] = ok ? to_f32(q[tok(rr) * DK + i]) : 0.f;
+        sK[rr * LDK + i] = ok ? to_f32(k[tok(rr) * DK + i]) : 0.f;
+        float la = 0.f;
+        if (ok && a.gate == 2) la = a.log_alpha[tok(rr) * DK + i];
+        if (ok && a.gate == 1) la = a.log_alpha[tok(rr)];
+        sG[rr * LDK + i] = la;
+    }
+    for (int rr = tid; rr < C; rr += kThreads) sB[rr] = rr < Lc ? to_f32(beta[tok(rr)]) : 0.f;
+    for (int idx = tid; idx < C * C; idx += kThreads) {
+        sT[(idx / C) * kLdA + idx % C] = a.ws.T[n * (int64_t)C * C + idx];
+        sP[(idx / C) * kLdA + idx % C] = a.ws.fw.P[n * (int64_t)C * C + idx];
+    }
+    for (int idx = tid; idx < C * dv; idx += kThreads) {
+        const int rr = idx / dv, j = idx % dv;
+        sX[rr * ldw + j] = rr < Lc ? to_f32(dout[tok(rr) * dv + j]) : 0.f;
+    }
+    for (int i = tid; i < DK; i += kThreads) sDgC[i] = 0.f;
+    __syncthreads();
+    for (int i = tid; i < DK; i += kThreads) {   // cumulative log decay down each channel
+        float acc = 0.f;
+        for (int rr = 0; rr < C; ++rr) {
+            acc += sG[rr * LDK + i];
+            sG[rr * LDK + i] = acc;
+        }
+    }
+    __syncthreads();
+
+    float aq[NI], ak[NI], ag[NI];
+#pragma unroll
+    for (int m = 0; m < NI; ++m) { aq[m] = 0.f; ak[m] = 0.f; ag[m] = 0.f; }
+
+    // ---- 1. E = U - W S0 (row r, columns part + 4m); dq, dg from (dO S0^T)_ri
+    if (row_ok) {
+        for (int j = part; j < dv; j += 4) {
+            float acc = Un[r * dv + j];
+            for (int i = 0; i < DK; ++i) acc = fmaf(-Wn[r * DK + i], S0[i * dv + j], acc);
+            sE[r * ldw + j] = acc;
+        }
+#pragma unroll
+        for (int m = 0; m < NI; ++m) {
+            const int i = part + 4 * m;
+            float acc = 0.f;
+            for (int j = 0; j < dv; j += 4) {
+                const float4 s4 = load4(S0 + i * dv + j);
+                acc = fmaf(sX[r * ldw + j], s4.x, acc);
+                acc = fmaf(sX[r * ldw + j + 1], s4.y, acc);
+                acc = fmaf(sX[r * ldw + j + 2], s4.z, acc);
+                acc = fmaf(sX[r * ldw + j + 3], s4.w, acc);
+            }
+            const float e = __expf(sG[r * LDK + i]);
+            aq[m] = fmaf(e, acc, aq[m]);
+            ag[m] = fmaf(sQ[r * LDK + i] * e, acc, ag[m]);
+        }
+    }
+    __syncthreads();
+
+    // ---- 2. dE = P^T dO + Kd dS_C (registers), dP = tril(dO E^T) over P, then dE over dO
+    constexpr int NJ = 32;   // value columns per thread (dv <= 128)
+    float x[NJ];
+#pragma unroll
+    for (int m = 0; m < NJ; ++m) x[m] = 0.f;
+    if (row_ok) {
+#pragma unroll
+        for (int m = 0; m < NJ; ++m) {
+            const int j = part + 4 * m;
+            if (j < dv) {
+                float acc = 0.f;
+                for (int s = r; s < C; ++s) acc = fmaf(sP[s * kLdA + r], sX[s * ldw + j], acc);
+                for (int i = 0; i < DK; ++i) acc = fmaf(Kdn[r * DK + i], dSC[i * dv + j], acc);
+                x[m] = acc;
+            }
+        }
+    }
+    __syncthreads();
+    if (row_ok)
+        for (int s = part; s < C; s += 4) {
+            float acc = 0.f;
+            if (s <= r)
+                for (int j = 0; j < dv; ++j) acc = fmaf(sX[r * ldw + j], sE[s * ldw + j], acc);
+            sP[r * kLdA + s] = acc;
+        }
+    __syncthreads();
+    if (row_ok)
+#pragma unroll
+        for (int m = 0; m < NJ; ++m)
+            if (part + 4 * m < dv) sX[r * ldw + part + 4 * m] = x[m];
+    __syncthreads();
+
+    // ---- 3. dR = T^T dE, over dE
+    if (row_ok) {
+#pragma unroll
+        for (int m = 0; m < NJ; ++m) {
+            const int j = part + 4 * m;
+            if (j < dv) {
+                float acc = 0.f;
+                for (int s = r; s < C; ++s) acc = fmaf(sT[s * kLdA + r], sX[s * ldw + j], acc);
+                x[m] = acc;
+            }
+        }
+    }
+    __syncthreads();
+    if (row_ok)
+#pragma unroll
+        for (int m = 0; m < NJ; ++m)
+            if (part + 4 * m < dv) sX[r * ldw + part + 4 * m] = x[m];
+    __syncthreads();
+
+    // ---- 4. dA over T; dv; db part 1; (dR S0^T) -> dk, dg
+    const float br = row_ok ? sB[r] : 0.f;
+    float db = 0.f;
+    if (row_ok) {
+        for (int s = part; s < C; s += 4) {
+            float acc = 0.f;
+            if (s < r)
+                for (int j = 0; j < dv; ++j) acc = fmaf(sX[r * ldw + j], sE[s * ldw + j], acc);
+            sT[r * kLdA + s] = -acc;
+        }
+        Tin *gv = (Tin *)a.dv;
+        for (int j = part; j < dv; j += 4) {
+            const float dr = sX[r * ldw + j];
+            if (r < Lc) gv[tok(r) * dv + j] = from_f32<Tin>(br * dr);
+            float kgs = 0.f;   // ((K*G) S0)_rj
+            for (int i = 0; i < DK; ++i) kgs = fmaf(sK[r * LDK + i] * __expf(sG[r * LDK + i]), S0[i * dv + j], kgs);
+            const float u0 = (r < Lc ? to_f32(v[tok(r) * dv + j]) : 0.f) - kgs;
+            db = fmaf(dr, u0, db);
+        }
+#pragma unroll
+        for (int m = 0; m < NI; ++m) {
+            const int i = part + 4 * m;
+            float acc = 0.f;
+            for (int j = 0; j < dv; j += 4) {
+                const float4 s4 = load4(S0 + i * dv + j);
+                acc = fmaf(sX[r * ldw + j], s4.x, acc);
+                acc = fmaf(sX[r * ldw + j + 1], s4.y, acc);
+                acc = fmaf(sX[r * ldw + j + 2], s4.z, acc);
+                acc = fmaf(sX[r * ldw + j + 3], s4.w, acc);
+            }
+            const float w = br * __expf(sG[r * LDK + i]) * acc;
+            ak[m] -= w;
+            ag[m] = fmaf(-w, sK[r * LDK + i], ag[m]);
+        }
+    }
+    __syncthreads();   // dR is dead: sX takes the terms of the last token's dg
+
+    // ---- 4b. Y = E dS_C^T -> dk, dg; Y k exp(g_C - g) -> sX for the last token's dg
+    if (row_ok) {
+#pragma unroll
+        for (int m = 0; m < NI; ++m) {
+            const int i = part + 4 * m;
+            float y = 0.f;
+            for (int j = 0; j < dv; j += 4) {
+                const float4 d4 = load4(dSC + i * dv + j);
+                y = fmaf(sE[r * ldw + j], d4.x, y);
+                y = fmaf(sE[r * ldw + j + 1], d4.y, y);
+                y = fmaf(sE[r * ldw + j + 2], d4.z, y);
+                y = fmaf(sE[r * ldw + j + 3], d4.w, y);
+            }
+            const float f = __expf(sG[(C - 1) * LDK + i] - sG[r * LDK + i]);
+            const float z = y * sK[r * LDK + i] * f;
+            ak[m] = fmaf(y, f, ak[m]);
+            ag[m] -= z;
+            sX[r * ldw + i] = z;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < DK; i += kThreads) {   // d g_C,i = sum_r z_ri + sum_j dS_C,ij gamma_i S0_ij
+        float acc = 0.f;
+        for (int rr = 0; rr < C; ++rr) acc += sX[rr * ldw + i];
+        const float gi = __expf(sG[(C - 1) * LDK + i]);
+        for (int j = 0; j < dv; ++j) acc = fmaf(dSC[i * dv + j] * gi, S0[i * dv + j], acc);
+        sDgC[i] = acc;
+    }
+
+    // ---- 5. pair products: P_rs = sum_i q_ri k_si D_rs,i (s <= r) and A_rs = b_r sum_i
+    //         k_ri k_si D_rs,i (s < r), D = exp(g_r - g_s) <= 1; row r as the row, then as
+    //         the column
+    float db2 = 0.f;
+    if (row_ok) {
+        for (int s = 0; s <= r; ++s) {
+            const float dp = sP[r * kLdA + s];
+            const float da = s < r ? sT[r * kLdA + s] : 0.f;
+#pragma unroll
+            for (int m = 0; m < NI; ++m) {
+                const int i = part + 4 * m;
+                const float kd = sK[s * LDK + i] * __expf(sG[r * LDK + i] - sG[s * LDK + i]);
+                const float kr = sK[r * LDK + i];
+                const float tq = dp * kd, ta = da * br * kd;
+                aq[m] += tq;
+                ak[m] += ta;
+                ag[m] = fmaf(sQ[r * LDK + i], tq, fmaf(kr, ta, ag[m]));
+                db2 = fmaf(da * kr, kd, db2);
+            }
+        }
+        for (int s2 = r; s2 < C; ++s2) {
+            const float dp = sP[s2 * kLdA + r];
+            const float da = s2 > r ? sT[s2 * kLdA + r] * sB[s2] : 0.f;
+#pragma unroll
+            for (int m = 0; m < NI; ++m) {
+                const int i = part + 4 * m;
+                const float d = __expf(sG[s2 * LDK + i] - sG[r * LDK + i]);
+                const float t = (dp * sQ[s2 * LDK + i] + da * sK[s2 * LDK + i]) * d;
+                ak[m] += t;
+                ag[m] = fmaf(-sK[r * LDK + i], t, ag[m]);
+            }
+        }
+    }
+    db += db2;
+    db += __shfl_xor_sync(0xffffffffu, db, 1);
+    db += __shfl_xor_sync(0xffffffffu, db, 2);
+
+    // ---- 6. outputs; d log alpha_t = sum_{r >= t} dg_r (+ the last token's gamma terms)
+    if (row_ok && r < Lc) {
+        Tin *gq = (Tin *)a.dq, *gk = (Tin *)a.dk;
+        if (part == 0) ((Tin *)a.d_beta)[tok(r)] = from_f32<Tin>(db);
+#pragma unroll
+        for (int m = 0; m < NI; ++m) {
+            gq[tok(r) * DK + part + 4 * m] = from_f32<Tin>(aq[m]);
+            gk[tok(r) * DK + part + 4 * m] = from_f32<Tin>(ak[m]);
+        }
+    }
+    if (a.gate == 0) return;
+    __syncthreads();   // sQ is dead
+    if (row_ok)
+#pragma unroll
+        for (int m = 0; m < NI; ++m) sQ[r * LDK + part + 4 * m] = ag[m];
+    __syncthreads();
+    if (a.gate == 2) {
+        for (int i = tid; i < DK; i += kThreads) {
+            float run = sDgC[i];
+            for (int rr = C - 1; rr >= 0; --rr) {
+                run += sQ[rr * LDK + i];
+                if (rr < Lc) a.d_log_alpha[tok(rr) * DK + i] = run;
+            }
+        }
+    } else {
+        for (int rr = tid; rr < C; rr += kThreads) {
+            float acc = 0.f;
+            for (int i = 0; i < DK; ++i) acc += sQ[rr * LDK + i];
+            sRed[rr] = acc;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float run = 0.f;
+            for (int i = 0; i < DK; ++i) run += sDgC[i];
+            for (int rr = C - 1; rr >= 0; --rr) {
+                run += sRed[rr];
+                if (rr < Lc) a.d_log_alpha[tok(rr)] = run;
+            }
+        }
+    }
+}
+
+template <int DK, typename Tin, typename Tg>
+int launch_bwd_t(const DStateArgs &da, const GradArgs &ga, int64_t nstate, int64_t ngrad,
+                 cudaStream_t stream) {
+    const size_t ds = dstate_smem_bytes(DK), gs = grad_smem_bytes(DK, ga.dv_);
+    if (cudaFuncSetAttribute(chunk_dstate_kernel<DK, Tg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ds) != cudaSuccess ||
+        cudaFuncSetAttribute(chunk_grad_kernel<DK, Tin, Tg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gs) != cudaSuccess)
+        return kErrCuda;
+    chunk_dstate_kernel<DK, Tg><<<(unsigned)nstate, kThreads, ds, stream>>>(da);
+    if (ngrad > 0) chunk_grad_kernel<DK, Tin, Tg><<<(unsigned)ngrad, kThreads, gs, stream>>>(ga);
+    return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(const ChunkProblem &p) { return sizeof(float) * bwd_floats(p); }
+
+int launch_chunk_bwd(const ChunkProblem &p, const BwdIo &g, void *workspace, cudaStream_t stream) {
+    const BwdWorkspace ws = bwd_carve(workspace, p);
+    if (p.NC > 0) {
+        // the forward's per-chunk operands, T and the chunk-start states, without outputs
+        ChunkProblem f = p;
+        f.out = nullptr;
+        f.final_state = nullptr;
+        f.fuse = 0;
+        f.z = nullptr;
+        const int rc = launch_chunk_simt(f, ws.fw, stream, ws.T, ws.ckpt);
+        if (rc != kOk) return rc;
+    }
+    DStateArgs da{g.d_out, g.d_final, g.d_init, ws, p.B, p.T, p.H, p.dv, p.C, p.NC};
+    GradArgs ga{p.q, p.k, p.v, p.log_alpha, p.beta, g.d_out, ws, g.dq, g.dk, g.dv, g.d_log_alpha,
+                g.d_beta, p.B, p.T, p.H, p.dv, p.C, p.NC, p.gate};
+    const int64_t nstate = p.B * p.H * (p.dv / kDvt), ngrad = p.B * p.H * p.NC;
+    using bf = __nv_bfloat16;
+    const bool ib = p.in_bf16, ob = p.out_bf16;
+    if (p.dk == 128) {
+        if (ib && ob) return launch_bwd_t<128, bf, bf>(da, ga, nstate, ngrad, stream);
+        if (ib) return launch_bwd_t<128, bf, float>(da, ga, nstate, ngrad, stream);
+        if (ob) return launch_bwd_t<128, float, bf>(da, ga, nstate, ngrad, stream);
+        return launch_bwd_t<128, float, float>(da, ga, nstate, ngrad, stream);
+    }
+    if (p.dk == 64) {
+        if (ib && ob) return launch_bwd_t<64, bf, bf>(da, ga, nstate, ngrad, stream);
+        if (ib) return launch_bwd_t<64, bf, float>(da, ga, nstate, ngrad, stream);
+        if (ob) return launch_bwd_t<64, float, bf>(da, ga, nstate, ngrad, stream);
+        return launch_bwd_t<64, float, float>(da, ga, nstate, ngrad, stream);
+    }
+    return kErrUnsupported;
+}
+
+}  // namespace dr

@@ -60,7 +60,22 @@ inline ChunkWorkspace simt_workspace_carve(void *base, int64_t B, int64_t H, int
     return w;
 }
 
-int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStream_t stream);
+// CUDA-core path (chunk_simt.cu).  For the backward, `T_out` ([n][C][C]) and `ckpt`
+// ([n][dk][dv], the state at each chunk's start) are also written; `p.out` may then be NULL.
+int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStream_t stream,
+                      float *T_out = nullptr, float *ckpt = nullptr);
+// Backward of the chunk forward on the CUDA cores (chunk_bwd.cu): gradients of
+// <d_out, out> + <d_final, final_state>.  Workspace: bwd_workspace_bytes(p).
+struct BwdIo {
+    const void *d_out;          // [B,T,H,dv] out dtype
+    const float *d_final;       // [B,H,dk,dv] or NULL (zero)
+    void *dq, *dk, *dv;         // in dtype
+    float *d_log_alpha;         // shape of log_alpha (NULL iff no gate)
+    void *d_beta;               // [B,T,H] in dtype
+    float *d_init;              // [B,H,dk,dv] or NULL (not returned)
+};
+size_t bwd_workspace_bytes(const ChunkProblem &p);
+int launch_chunk_bwd(const ChunkProblem &p, const BwdIo &g, void *workspace, cudaStream_t stream);
 
 // Fused tensor-core path (chunk_tc.cu): bf16 inputs, dk = dv = 128, C = 64, scalar gate or
 // none, T > 0.  Needs a workspace only when few long chains are split into segments

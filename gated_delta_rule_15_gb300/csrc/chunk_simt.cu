@@ -51,6 +51,7 @@ struct PrepArgs {
     int dv, C, NC, gate;
     uint32_t fuse;
     ChunkWorkspace ws;
+    float *T_out;    // backward only: T = (I + A)^-1 per chunk, [n][C][C] (NULL otherwise)
 };
 
 struct StateArgs {
@@ -62,6 +63,8 @@ struct StateArgs {
     int64_t B, T, H;
     int dv, C, NC;
     ChunkWorkspace ws;
+    float *ckpt;     // backward only: the state at each chunk's start, [n][dk][dv] (NULL
+                     // otherwise); with it, `out` may be NULL (no outputs written)
 };
 
 size_t prep_smem_bytes(int dk) {
@@ -345,6 +348,13 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
             __syncwarp();
         }
     }
+    if (a.T_out) {   // T for the backward (lower triangle, diagonal included)
+        __syncthreads();
+        for (int idx = tid; idx < C * C; idx += kThreads) {
+            const int r = idx / C, s2 = idx % C;
+            a.T_out[n * (int64_t)C * C + idx] = s2 <= r ? sT[r * kLdA + s2] : 0.f;
+        }
+    }
     // 6. W = T diag(b) (K*G):  rows b_s k_s exp(g_s) (exponent <= 0), k reloaded raw.
     for (int idx = tid; idx < C * DK; idx += kThreads) {
         const int s = idx / DK, ch = idx % DK;
@@ -424,6 +434,8 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(StateArgs a) {
             sU[idx] = U[(idx / kDvt) * dv + jt * kDvt + idx % kDvt];
         for (int idx = tid; idx < C * C; idx += kThreads) sP[(idx / C) * kLdA + idx % C] = P[idx];
         for (int i = tid; i < DK; i += kThreads) sGam[i] = a.ws.gam[n * DK + i];
+        if (a.ckpt)   // the state at this chunk's start (sS is final after the barrier above)
+            for (int i = rg; i < DK; i += 8) a.ckpt[(n * DK + i) * dv + col] = sS[i * kDvt + j];
         __syncthreads();
 
         // E = U - W S and the inter-chunk read (Q*G) S, rows r = rg + 8m.
@@ -457,7 +469,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(StateArgs a) {
             if (r < C) {
                 float acc = o[m];
                 for (int s = 0; s <= r; ++s) acc += sP[r * kLdA + s] * sE[s * kDvt + j];
-                if (r < Lc) {
+                if (r < Lc && out) {
                     const int64_t oi = ((b * a.T + t0 + r) * a.H + h) * dv + col;
                     if (a.z)
                         acc *= silu_f(a.z_bf16 ? to_f32(((const __nv_bfloat16 *)a.z)[oi])
@@ -497,10 +509,12 @@ int launch_simt_t(const PrepArgs &pa, const StateArgs &sa, cudaStream_t stream) 
 
 }  // namespace
 
-int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStream_t stream) {
-    PrepArgs pa{p.q, p.k, p.v, p.log_alpha, p.beta, p.B, p.T, p.H, p.dv, p.C, p.NC, p.gate, p.fuse, ws};
+int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStream_t stream,
+                      float *T_out, float *ckpt) {
+    PrepArgs pa{p.q, p.k, p.v, p.log_alpha, p.beta, p.B, p.T, p.H, p.dv, p.C, p.NC, p.gate, p.fuse, ws,
+                T_out};
     StateArgs sa{p.init_state, p.out, p.final_state, (p.fuse & kFuseGate) ? p.z : nullptr, p.in_bf16,
-                 p.B, p.T, p.H, p.dv, p.C, p.NC, ws};
+                 p.B, p.T, p.H, p.dv, p.C, p.NC, ws, ckpt};
     using bf = __nv_bfloat16;
     const bool ib = p.in_bf16, ob = p.out_bf16;
     if (p.dk == 128) {

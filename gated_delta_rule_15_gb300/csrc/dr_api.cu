@@ -124,6 +124,41 @@ extern "C" int dr_chunk_fwd_ex(const dr_chunk_desc *desc, uint32_t fuse, const v
     return launch_chunk_simt(p, ws, (cudaStream_t)stream);
 }
 
+extern "C" int dr_chunk_bwd_workspace_bytes(const dr_chunk_desc *desc, size_t *bytes) {
+    if (!bytes) return kErrInvalid;
+    ChunkProblem p{};
+    const int rc = check_chunk_desc(desc, &p);
+    if (rc != kOk) return rc;
+    *bytes = bwd_workspace_bytes(p);
+    return kOk;
+}
+
+extern "C" int dr_chunk_bwd(const dr_chunk_desc *desc, const void *q, const void *k,
+                            const void *v, const float *log_alpha, const void *beta,
+                            const float *init_state, const void *d_out,
+                            const float *d_final_state, void *dq, void *dk, void *dv,
+                            float *d_log_alpha, void *d_beta, float *d_init_state,
+                            void *workspace, size_t workspace_bytes, dr_stream_t stream) {
+    ChunkProblem p{};
+    const int rc = check_chunk_desc(desc, &p);
+    if (rc != kOk) return rc;
+    if (p.T > 0 && (!q || !k || !v || !beta || !d_out || !dq || !dk || !dv || !d_beta))
+        return kErrInvalid;
+    if (p.gate != DR_GATE_NONE && p.T > 0 && (!log_alpha || !d_log_alpha)) return kErrInvalid;
+    if (p.gate == DR_GATE_NONE && d_log_alpha) return kErrInvalid;
+    const void *ptrs[] = {q, k, v, log_alpha, beta, init_state, d_out, d_final_state, dq, dk, dv,
+                          d_log_alpha, d_beta, d_init_state, workspace};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return kErrInvalid;
+    const size_t need = bwd_workspace_bytes(p);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return kErrWorkspace;
+    if (p.NC == 0 && !d_init_state) return kOk;
+    p.q = q; p.k = k; p.v = v; p.log_alpha = p.gate == DR_GATE_NONE ? nullptr : log_alpha;
+    p.beta = beta; p.init_state = init_state; p.out = nullptr; p.final_state = nullptr;
+    const BwdIo g{d_out, d_final_state, dq, dk, dv, d_log_alpha, d_beta, d_init_state};
+    return launch_chunk_bwd(p, g, workspace, (cudaStream_t)stream);
+}
+
 extern "C" int dr_chunk_fwd(const dr_chunk_desc *desc, const void *q, const void *k,
                             const void *v, const float *log_alpha, const void *beta,
                             const float *init_state, void *out, float *final_state,

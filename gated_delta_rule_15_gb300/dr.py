@@ -35,7 +35,8 @@ L2NORM_EPS = 1e-6   # DR_L2NORM_EPS
 # Symbols of include/dr.h (checked by tests/test_abi.py against the header).
 EXPORTED = ("dr_version", "dr_chunk_fwd_workspace_bytes", "dr_chunk_fwd",
             "dr_recurrent_step", "dr_get_device_status", "dr_strerror",
-            "dr_chunk_fwd_noalloc", "dr_chunk_fwd_ex", "dr_recurrent_step_ex")
+            "dr_chunk_fwd_noalloc", "dr_chunk_fwd_ex", "dr_recurrent_step_ex",
+            "dr_chunk_bwd_workspace_bytes", "dr_chunk_bwd")
 
 
 class ChunkDesc(ctypes.Structure):
@@ -70,6 +71,11 @@ _lib.dr_chunk_fwd_ex.restype = ctypes.c_int
 _lib.dr_recurrent_step_ex.argtypes = [ctypes.POINTER(StepDesc), ctypes.c_uint32, _vp, _vp, _vp,
                                       _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.dr_recurrent_step_ex.restype = ctypes.c_int
+_lib.dr_chunk_bwd_workspace_bytes.argtypes = [ctypes.POINTER(ChunkDesc),
+                                              ctypes.POINTER(ctypes.c_size_t)]
+_lib.dr_chunk_bwd_workspace_bytes.restype = ctypes.c_int
+_lib.dr_chunk_bwd.argtypes = [ctypes.POINTER(ChunkDesc)] + [_vp] * 15 + [ctypes.c_size_t, _vp]
+_lib.dr_chunk_bwd.restype = ctypes.c_int
 _lib.dr_get_device_status.argtypes = [_vp]
 _lib.dr_get_device_status.restype = ctypes.c_int
 _lib.dr_strerror.argtypes = [ctypes.c_int]
@@ -201,6 +207,52 @@ def chunk_fwd(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
     if rc != DR_OK:
         raise DrError(rc, "dr_chunk_fwd")
     return out, final_state
+
+
+def bwd_workspace_bytes(desc: ChunkDesc) -> int:
+    n = ctypes.c_size_t(0)
+    rc = _lib.dr_chunk_bwd_workspace_bytes(ctypes.byref(desc), ctypes.byref(n))
+    if rc != DR_OK:
+        raise DrError(rc, "dr_chunk_bwd_workspace_bytes")
+    return n.value
+
+
+def chunk_bwd(q, k, v, log_alpha, beta, init_state, d_out, d_final_state=None, *,
+              chunk: int = 64, return_d_init: bool = True, workspace=None, stream=None):
+    """Backward of chunk_fwd (dr_chunk_bwd): gradients of <d_out, out> +
+    <d_final_state, final_state>.  Inputs as for chunk_fwd; d_out [B,T,H,dv] in the
+    forward output's dtype; d_final_state None or fp32 [B,H,dk,dv].  Returns (dq, dk, dv,
+    d_log_alpha, d_beta, d_init_state): the first three and d_beta in the inputs' dtype,
+    d_log_alpha fp32 with log_alpha's shape (None without a gate), d_init_state fp32
+    [B,H,dk,dv] (None unless return_d_init)."""
+    _check_dev(q, k, v, log_alpha, beta, init_state, d_out, d_final_state, workspace)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
+        raise ValueError("q, k, v, beta must share one dtype (float32 or bfloat16)")
+    if d_out.dtype not in _DT or tuple(d_out.shape) != (B, T, H, dv):
+        raise ValueError("d_out must be float32 or bfloat16 [B,T,H,dv]")
+    for t in (init_state, d_final_state):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != (B, H, dk, dv)):
+            raise ValueError("states must be float32 [B,H,dk,dv]")
+    gate = _gate_of(log_alpha, (B, T, H), dk)
+    desc = chunk_desc(B, T, H, dk, dv, _DT[q.dtype], _DT[d_out.dtype], gate, chunk)
+    dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dla = None if log_alpha is None else torch.empty_like(log_alpha)
+    dbeta = torch.empty_like(beta)
+    dinit = (torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+             if return_d_init else None)
+    need = bwd_workspace_bytes(desc)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _lib.dr_chunk_bwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                           _ptr(beta), _ptr(init_state), _ptr(d_out), _ptr(d_final_state),
+                           _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dla), _ptr(dbeta), _ptr(dinit),
+                           _ptr(workspace), wbytes, _stream_handle(stream))
+    if rc != DR_OK:
+        raise DrError(rc, "dr_chunk_bwd")
+    return dq, dk_, dv_, dla, dbeta, dinit
 
 
 def chunk_fwd_noalloc(q, k, v, log_alpha, beta, init_state, out, final_state, *,

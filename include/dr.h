@@ -163,6 +163,40 @@ int dr_recurrent_step(const dr_step_desc *desc,
                       float *state, void *out, dr_stream_t stream);
 
 /*
+ * Backward of dr_chunk_fwd (training): the gradients of
+ *     L = <d_out, out> + <d_final_state, final_state>
+ * with respect to every input, for the same descriptor (any gate, dk, dv in {64, 128},
+ * chunk 16, 32 or 64, fp32 or bf16), computed chunkwise on the CUDA cores in fp32: the
+ * forward's per-chunk operands and chunk-start states are recomputed into the workspace, a
+ * reverse pass carries the state gradient from the last chunk to the first, and every
+ * chunk's token gradients follow in parallel.  The pages ask for chunkwise kernels for
+ * training (page "linear-attention gated-deltanet guide", section 5) without printing a
+ * backward; this is the derivative of the chunk form.
+ *
+ *   inputs         as for dr_chunk_fwd (q, k, v, log_alpha, beta, init_state)
+ *   d_out          [B, T, H, dv] out_dtype
+ *   d_final_state  NULL (zero) or [B, H, dk, dv] fp32
+ *   dq, dk         [B, T, H, dk] in_dtype (written)
+ *   dv             [B, T, H, dv] in_dtype (written)
+ *   d_log_alpha    log_alpha's shape, fp32 (written); NULL exactly when gate is NONE
+ *   d_beta         [B, T, H] in_dtype (written)
+ *   d_init_state   NULL (not returned) or [B, H, dk, dv] fp32 (written)
+ *   workspace      at least dr_chunk_bwd_workspace_bytes() (295,424 bytes per
+ *                  (b, h, chunk) at dk = dv = 128, C = 64); contents on entry ignored
+ * Written buffers must not overlap each other or any input.  The fused-neighbour flags
+ * are not taken here.  Returns DR_OK, DR_ERR_INVALID, DR_ERR_UNSUPPORTED,
+ * DR_ERR_WORKSPACE or DR_ERR_CUDA.
+ */
+int dr_chunk_bwd_workspace_bytes(const dr_chunk_desc *desc, size_t *bytes);
+int dr_chunk_bwd(const dr_chunk_desc *desc,
+                 const void *q, const void *k, const void *v,
+                 const float *log_alpha, const void *beta, const float *init_state,
+                 const void *d_out, const float *d_final_state,
+                 void *dq, void *dk, void *dv, float *d_log_alpha, void *d_beta,
+                 float *d_init_state, void *workspace, size_t workspace_bytes,
+                 dr_stream_t stream);
+
+/*
  * dr_recurrent_step with fused neighbours (flags as for dr_chunk_fwd_ex); `z` is
  * [B, H, dv] in_dtype, required when DR_FUSE_OUT_SILU_GATE is set, and must not overlap
  * `state` or `out`.  Returns the statuses of dr_recurrent_step.

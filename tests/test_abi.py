@@ -146,3 +146,24 @@ def test_python_binding_rejects_host_tensors(dr):
     x = torch.zeros(1, 4, 1, 64)
     with pytest.raises(ValueError):
         dr.chunk_fwd(x, x, x, None, torch.zeros(1, 4, 1))
+
+
+@no_gpu_only
+def test_chunk_bwd_host_side_errors(dr):
+    lib = dr.lib()
+    d = _desc(dr)   # per-channel gate
+    names = ("q", "k", "v", "la", "beta", "s0", "do", "dfin", "dq", "dk", "dv", "dla", "db",
+             "dinit", "ws")
+    far = lambda n: ctypes.c_void_p((n + 1) << 32)
+    args = lambda **o: [o.get(n, far(i)) for i, n in enumerate(names)]
+    call = lambda a, wb=1 << 40: lib.dr_chunk_bwd(ctypes.byref(d), *a, wb, None)
+    n = ctypes.c_size_t(0)
+    assert lib.dr_chunk_bwd_workspace_bytes(ctypes.byref(d), ctypes.byref(n)) == 0
+    assert n.value > dr.workspace_bytes(d)
+    assert call(args(dq=None)) == dr.DR_ERR_INVALID
+    assert call(args(dla=None)) == dr.DR_ERR_INVALID            # a gate needs d_log_alpha
+    assert call(args(do=ctypes.c_void_p((3 << 32) + 8))) == dr.DR_ERR_INVALID
+    assert call(args(ws=None)) == dr.DR_ERR_WORKSPACE
+    assert call(args(), wb=n.value - 16) == dr.DR_ERR_WORKSPACE
+    d0 = _desc(dr, gate=dr.DR_GATE_NONE)
+    assert lib.dr_chunk_bwd(ctypes.byref(d0), *args(), 1 << 40, None) == dr.DR_ERR_INVALID
