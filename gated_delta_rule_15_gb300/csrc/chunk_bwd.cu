@@ -34,6 +34,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kLdA = 65;   // padded row stride of [64][64] tiles
 constexpr int kDvt = 32;   // state columns per CTA of the reverse pass
+constexpr int kSlice = 32; // rows of a [dk][dv] state matrix staged at a time
 
 // Workspace of the backward, in floats, after the forward's slabs: T [n][C][C], checkpoints
 // [n][dk][dv], dS_C [n][dk][dv].
@@ -160,7 +161,8 @@ struct GradArgs {
 
 size_t grad_smem_bytes(int dk, int dv) {
     const int ldw = (dk > dv ? dk : dv) + 4;
-    return sizeof(float) * (size_t)(3 * 64 * (dk + 4) + 2 * 64 * ldw + 2 * 64 * kLdA + 64 + dk + 64);
+    return sizeof(float) * (size_t)(3 * 64 * (dk + 4) + 2 * 64 * ldw + 2 * 64 * kLdA + 64 + dk + 64 +
+                                    kSlice * (dv + 4));
 }
 
 // Every gradient of one chunk's tokens.  Thread (row r = tid / 4, part = tid % 4) owns key
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
     float *sB = sP + 64 * kLdA;                    // [64] beta
     float *sDgC = sB + 64;                         // [DK] d g of the last token (gamma terms)
     float *sRed = sDgC + DK;                       // [64] row sums
+    float *sS = sRed + 64;                         // [kSlice][dv + 4] rows of S0 or dS_C
 
     const Tin *q = (const Tin *)a.q, *k = (const Tin *)a.k, *v = (const Tin *)a.v;
     const Tin *beta = (const Tin *)a.beta;
@@ -210,6 +213,16 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
     const float *Kdn = a.ws.fw.Kd + n * (int64_t)C * DK;
     const int r = tid >> 2, part = tid & 3;
     const bool row_ok = r < C;
+    const int lds = dv + 4;
+    // rows i0 .. i0 + kSlice - 1 of a [DK][dv] matrix into sS (all threads; barriers around)
+    auto stage = [&](const float *M, int i0) {
+        __syncthreads();
+        for (int idx = tid; idx < kSlice * (dv / 4); idx += kThreads) {
+            const int ii = idx / (dv / 4), j4 = 4 * (idx % (dv / 4));
+            *reinterpret_cast<float4 *>(sS + ii * lds + j4) = load4(M + (i0 + ii) * dv + j4);
+        }
+        __syncthreads();
+    };
 
     // ---- 0. inputs (rows past the sequence: zero, log alpha 0)
     for (int idx = tid; idx < C * DK; idx += kThreads) {
@@ -246,46 +259,56 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
 #pragma unroll
     for (int m = 0; m < NI; ++m) { aq[m] = 0.f; ak[m] = 0.f; ag[m] = 0.f; }
 
-    // ---- 1. E = U - W S0 (row r, columns part + 4m); dq, dg from (dO S0^T)_ri
-    if (row_ok) {
-        for (int j = part; j < dv; j += 4) {
-            float acc = Un[r * dv + j];
-            for (int i = 0; i < DK; ++i) acc = fmaf(-Wn[r * DK + i], S0[i * dv + j], acc);
-            sE[r * ldw + j] = acc;
+    // ---- 1. E = U - W S0 (row r, columns part + 4m); dq, dg from (dO S0^T)_ri; S0 staged
+    //         by slices of kSlice rows
+    constexpr int NJ = 32;   // value columns per thread (dv <= 128)
+    float x[NJ];
+#pragma unroll
+    for (int m = 0; m < NJ; ++m) x[m] = (row_ok && part + 4 * m < dv) ? Un[r * dv + part + 4 * m] : 0.f;
+    for (int i0 = 0; i0 < DK; i0 += kSlice) {
+        stage(S0, i0);
+        if (!row_ok) continue;
+        for (int ii = 0; ii < kSlice; ++ii) {
+            const float w = Wn[r * DK + i0 + ii];
+#pragma unroll
+            for (int m = 0; m < NJ; ++m)
+                if (part + 4 * m < dv) x[m] = fmaf(-w, sS[ii * lds + part + 4 * m], x[m]);
         }
 #pragma unroll
         for (int m = 0; m < NI; ++m) {
             const int i = part + 4 * m;
+            if (i < i0 || i >= i0 + kSlice) continue;
             float acc = 0.f;
-            for (int j = 0; j < dv; j += 4) {
-                const float4 s4 = load4(S0 + i * dv + j);
-                acc = fmaf(sX[r * ldw + j], s4.x, acc);
-                acc = fmaf(sX[r * ldw + j + 1], s4.y, acc);
-                acc = fmaf(sX[r * ldw + j + 2], s4.z, acc);
-                acc = fmaf(sX[r * ldw + j + 3], s4.w, acc);
-            }
+            for (int j = 0; j < dv; ++j) acc = fmaf(sX[r * ldw + j], sS[(i - i0) * lds + j], acc);
             const float e = __expf(sG[r * LDK + i]);
             aq[m] = fmaf(e, acc, aq[m]);
             ag[m] = fmaf(sQ[r * LDK + i] * e, acc, ag[m]);
         }
     }
+    if (row_ok)
+#pragma unroll
+        for (int m = 0; m < NJ; ++m)
+            if (part + 4 * m < dv) sE[r * ldw + part + 4 * m] = x[m];
     __syncthreads();
 
-    // ---- 2. dE = P^T dO + Kd dS_C (registers), dP = tril(dO E^T) over P, then dE over dO
-    constexpr int NJ = 32;   // value columns per thread (dv <= 128)
-    float x[NJ];
+    // ---- 2. dE = P^T dO + Kd dS_C (registers; dS_C by slices), dP = tril(dO E^T) over P,
+    //         then dE over dO
 #pragma unroll
-    for (int m = 0; m < NJ; ++m) x[m] = 0.f;
-    if (row_ok) {
+    for (int m = 0; m < NJ; ++m) {
+        const int j = part + 4 * m;
+        float acc = 0.f;
+        if (row_ok && j < dv)
+            for (int s = r; s < C; ++s) acc = fmaf(sP[s * kLdA + r], sX[s * ldw + j], acc);
+        x[m] = acc;
+    }
+    for (int i0 = 0; i0 < DK; i0 += kSlice) {
+        stage(dSC, i0);
+        if (!row_ok) continue;
+        for (int ii = 0; ii < kSlice; ++ii) {
+            const float kd = Kdn[r * DK + i0 + ii];
 #pragma unroll
-        for (int m = 0; m < NJ; ++m) {
-            const int j = part + 4 * m;
-            if (j < dv) {
-                float acc = 0.f;
-                for (int s = r; s < C; ++s) acc = fmaf(sP[s * kLdA + r], sX[s * ldw + j], acc);
-                for (int i = 0; i < DK; ++i) acc = fmaf(Kdn[r * DK + i], dSC[i * dv + j], acc);
-                x[m] = acc;
-            }
+            for (int m = 0; m < NJ; ++m)
+                if (part + 4 * m < dv) x[m] = fmaf(kd, sS[ii * lds + part + 4 * m], x[m]);
         }
     }
     __syncthreads();
@@ -322,7 +345,7 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
             if (part + 4 * m < dv) sX[r * ldw + part + 4 * m] = x[m];
     __syncthreads();
 
-    // ---- 4. dA over T; dv; db part 1; (dR S0^T) -> dk, dg
+    // ---- 4. dA over T; dv; db part 1 (with (K*G) S0); (dR S0^T) -> dk, dg; S0 by slices
     const float br = row_ok ? sB[r] : 0.f;
     float db = 0.f;
     if (row_ok) {
@@ -332,46 +355,54 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
                 for (int j = 0; j < dv; ++j) acc = fmaf(sX[r * ldw + j], sE[s * ldw + j], acc);
             sT[r * kLdA + s] = -acc;
         }
-        Tin *gv = (Tin *)a.dv;
-        for (int j = part; j < dv; j += 4) {
-            const float dr = sX[r * ldw + j];
-            if (r < Lc) gv[tok(r) * dv + j] = from_f32<Tin>(br * dr);
-            float kgs = 0.f;   // ((K*G) S0)_rj
-            for (int i = 0; i < DK; ++i) kgs = fmaf(sK[r * LDK + i] * __expf(sG[r * LDK + i]), S0[i * dv + j], kgs);
-            const float u0 = (r < Lc ? to_f32(v[tok(r) * dv + j]) : 0.f) - kgs;
-            db = fmaf(dr, u0, db);
+        if (r < Lc) {
+            Tin *gv = (Tin *)a.dv;
+            for (int j = part; j < dv; j += 4) gv[tok(r) * dv + j] = from_f32<Tin>(br * sX[r * ldw + j]);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < NJ; ++m) x[m] = 0.f;   // ((K*G) S0)_rj
+    for (int i0 = 0; i0 < DK; i0 += kSlice) {
+        stage(S0, i0);
+        if (!row_ok) continue;
+        for (int ii = 0; ii < kSlice; ++ii) {
+            const float kg = sK[r * LDK + i0 + ii] * __expf(sG[r * LDK + i0 + ii]);
+#pragma unroll
+            for (int m = 0; m < NJ; ++m)
+                if (part + 4 * m < dv) x[m] = fmaf(kg, sS[ii * lds + part + 4 * m], x[m]);
         }
 #pragma unroll
         for (int m = 0; m < NI; ++m) {
             const int i = part + 4 * m;
+            if (i < i0 || i >= i0 + kSlice) continue;
             float acc = 0.f;
-            for (int j = 0; j < dv; j += 4) {
-                const float4 s4 = load4(S0 + i * dv + j);
-                acc = fmaf(sX[r * ldw + j], s4.x, acc);
-                acc = fmaf(sX[r * ldw + j + 1], s4.y, acc);
-                acc = fmaf(sX[r * ldw + j + 2], s4.z, acc);
-                acc = fmaf(sX[r * ldw + j + 3], s4.w, acc);
-            }
+            for (int j = 0; j < dv; ++j) acc = fmaf(sX[r * ldw + j], sS[(i - i0) * lds + j], acc);
             const float w = br * __expf(sG[r * LDK + i]) * acc;
             ak[m] -= w;
             ag[m] = fmaf(-w, sK[r * LDK + i], ag[m]);
         }
     }
-    __syncthreads();   // dR is dead: sX takes the terms of the last token's dg
+    if (row_ok)
+#pragma unroll
+        for (int m = 0; m < NJ; ++m) {
+            const int j = part + 4 * m;
+            if (j < dv) {
+                const float u0 = (r < Lc ? to_f32(v[tok(r) * dv + j]) : 0.f) - x[m];
+                db = fmaf(sX[r * ldw + j], u0, db);
+            }
+        }
 
-    // ---- 4b. Y = E dS_C^T -> dk, dg; Y k exp(g_C - g) -> sX for the last token's dg
-    if (row_ok) {
+    // ---- 4b. Y = E dS_C^T -> dk, dg; Y k exp(g_C - g) -> sX (dR is dead after the first
+    //          staging barrier) for the last token's dg; dS_C by slices
+    for (int i0 = 0; i0 < DK; i0 += kSlice) {
+        stage(dSC, i0);
+        if (!row_ok) continue;
 #pragma unroll
         for (int m = 0; m < NI; ++m) {
             const int i = part + 4 * m;
+            if (i < i0 || i >= i0 + kSlice) continue;
             float y = 0.f;
-            for (int j = 0; j < dv; j += 4) {
-                const float4 d4 = load4(dSC + i * dv + j);
-                y = fmaf(sE[r * ldw + j], d4.x, y);
-                y = fmaf(sE[r * ldw + j + 1], d4.y, y);
-                y = fmaf(sE[r * ldw + j + 2], d4.z, y);
-                y = fmaf(sE[r * ldw + j + 3], d4.w, y);
-            }
+            for (int j = 0; j < dv; ++j) y = fmaf(sE[r * ldw + j], sS[(i - i0) * lds + j], y);
             const float f = __expf(sG[(C - 1) * LDK + i] - sG[r * LDK + i]);
             const float z = y * sK[r * LDK + i] * f;
             ak[m] = fmaf(y, f, ak[m]);

@@ -34,7 +34,7 @@ def with_raw(make, fl):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--what", choices=["chunk", "decode"], required=True)
+    ap.add_argument("--what", choices=["chunk", "bwd", "decode"], required=True)
     ap.add_argument("--workload", default=None)
     ap.add_argument("--B", type=int, default=None)
     ap.add_argument("--T", type=int, default=None)
@@ -53,7 +53,20 @@ def main():
     if fl - {"l2", "sigmoid", "silu"}:
         ap.error(f"unknown fused neighbours {fl}")
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if args.what == "chunk":
+    if args.what == "bwd":
+        w = inputs.WORKLOADS[args.workload or "gdn_bf16_B8_H16_T4096_d128"]
+        w = dataclasses.replace(w, **{k: getattr(args, k) for k in ("B", "T", "H")
+                                      if getattr(args, k) is not None})
+        d = inputs.workload_inputs(w)
+        g = {k: (None if t is None else t.cuda()) for k, t in d.items()}
+        gen = torch.Generator().manual_seed(1)
+        dout = torch.randn((w.B, w.T, w.H, w.dv), generator=gen).to(g["q"].dtype).cuda()
+        dB = dr.chunk_desc(w.B, w.T, w.H, w.dk, w.dv, dr._DT[g["q"].dtype], dr._DT[dout.dtype],
+                           inputs.GATE_CODE[w.gate], w.chunk)
+        ws = torch.empty(dr.bwd_workspace_bytes(dB), dtype=torch.uint8, device="cuda")
+        run = lambda: dr.chunk_bwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"],
+                                   g["init_state"], dout, None, chunk=w.chunk, workspace=ws)
+    elif args.what == "chunk":
         w = inputs.WORKLOADS[args.workload or "gdn_bf16_B8_H16_T4096_d128"]
         w = dataclasses.replace(w, **{k: getattr(args, k) for k in ("B", "T", "H")
                                       if getattr(args, k) is not None})
