@@ -37,7 +37,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (128 chains) with half its head-tokens, and the kernel's traffic is proportional to
 # head-tokens, so the figure is twice the captured one.  Valid only while the kernel
 # sources hash to `src`; otherwise the bench reports null.
-TRAFFIC = {"chunk_fwd": {"bytes": 2 * (203113472 + 50139648), "src": "c67fd0fdf39dca5f"}}
+TRAFFIC = {"chunk_fwd": {"bytes": 2 * (203059968 + 49612288), "src": "3ba1a054781b013e"}}
 
 
 def peaks():
@@ -260,6 +260,40 @@ def bench_chunk_e2e(w, d, steps, warmup, world):
     return ms, runner.h2d_bytes, runner.d2h_bytes
 
 
+def bench_bwd(w, steps, warmup, world):
+    """dr_chunk_bwd on the workload (d_out ~ N(0, 1) in the output dtype, no final-state
+    gradient): ms per call."""
+    import torch
+    from gated_delta_rule_15_gb300 import dr, inputs
+    d = inputs.workload_inputs(w)
+    g = {k: (None if t is None else t.cuda()) for k, t in d.items()}
+    gen = torch.Generator().manual_seed(1)
+    dout = torch.randn((w.B, w.T, w.H, w.dv), generator=gen).to(g["q"].dtype).cuda()
+    desc = dr.chunk_desc(w.B, w.T, w.H, w.dk, w.dv, dr._DT[g["q"].dtype], dr._DT[dout.dtype],
+                         inputs.GATE_CODE[w.gate], w.chunk)
+    ws = torch.empty(dr.bwd_workspace_bytes(desc), dtype=torch.uint8, device="cuda")
+    call = lambda: dr.chunk_bwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"],
+                                g["init_state"], dout, None, chunk=w.chunk, workspace=ws)
+    ms, _ = time_calls(call, steps, warmup, world)
+    return ms
+
+
+def bench_fused(w, steps, warmup, world):
+    """dr_chunk_fwd_ex with every fused neighbour (raw q, k, beta logits, SiLU gate z):
+    ms per call."""
+    import torch
+    from gated_delta_rule_15_gb300 import dr, inputs
+    d = inputs.chunk_inputs(w.B, w.T, w.H, w.dk, w.dv, gate=w.gate, dtype=w.dtype,
+                            init_state=w.init_state, log_alpha_range=w.log_alpha_range, raw=True)
+    g = {k: (None if t is None else t.cuda()) for k, t in d.items()}
+    out = torch.empty((w.B, w.T, w.H, w.dv), dtype=g["q"].dtype, device="cuda")
+    call = lambda: dr.chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"],
+                                g["init_state"], chunk=w.chunk, out=out, qk_l2norm=True,
+                                beta_sigmoid=True, z=g["z"])
+    ms, _ = time_calls(call, steps, warmup, world)
+    return ms
+
+
 def bench_decode(w, steps, warmup, world):
     import torch
     from gated_delta_rule_15_gb300 import dr, inputs
@@ -332,6 +366,16 @@ def run_native(args):
 
     extra = {}
     if not args.quick:
+        fms = bench_fused(w, max(2, args.steps // 3), 3, world)
+        extra["fused_neighbours_" + w.name] = {
+            "what": "dr_chunk_fwd_ex: q/k L2 norm, beta = sigmoid(logit), SiLU output gate",
+            "ms_per_call": round(fms, 4), "tokens_per_s": w.B * w.T / (fms * 1e-3),
+            "vs_plain": round(fms / ms, 3)}
+        bms = bench_bwd(w, 2, 3, world)
+        extra["backward_" + w.name] = {
+            "what": "dr_chunk_bwd (CUDA cores, fp32): every input gradient",
+            "ms_per_call": round(bms, 3), "tokens_per_s": w.B * w.T / (bms * 1e-3),
+            "vs_forward": round(bms / ms, 1)}
         for name in ("kda_bf16_B4_H32_T8192_d128", "gdn_bf16_B1_H16_T65536_d128_init"):
             wx = inputs.WORKLOADS[name]
             rx = bench_chunk(wx, max(2, args.steps // 3), 3, world)
