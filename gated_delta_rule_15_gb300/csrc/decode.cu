@@ -30,12 +30,15 @@
 
 namespace dr {
 
-template <int DK, int DV, int GATE, typename Tin, typename Tout>
+// FUSED: the fused neighbours' code is compiled in (each switched by `fuse_flags`); the
+// plain instantiation carries none of it.
+template <int DK, int DV, int GATE, bool FUSED, typename Tin, typename Tout>
 __global__ void __launch_bounds__(DV * 2)
 decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    const Tin *__restrict__ v, const float *__restrict__ log_alpha,
-                   const Tin *__restrict__ beta, const Tin *__restrict__ z, uint32_t fuse,
+                   const Tin *__restrict__ beta, const Tin *__restrict__ z, uint32_t fuse_flags,
                    float *__restrict__ state, Tout *__restrict__ out) {
+    const uint32_t fuse = FUSED ? fuse_flags : 0u;
     constexpr int NT = DV * 2;     // threads: DV/16 warps
     constexpr int RPL = DK / 8;    // rows per lane
     const int bh = blockIdx.x;
@@ -149,9 +152,14 @@ struct DecodeIo {
 
 template <int DK, int DV, int GATE, typename Tin, typename Tout>
 static int launch_decode_t(int64_t BH, const DecodeIo &io, cudaStream_t stream) {
-    decode_step_kernel<DK, DV, GATE, Tin, Tout><<<(unsigned)BH, DV * 2, 0, stream>>>(
-        (const Tin *)io.q, (const Tin *)io.k, (const Tin *)io.v, io.la, (const Tin *)io.beta,
-        (const Tin *)io.z, io.fuse, io.state, (Tout *)io.out);
+    if (io.fuse)
+        decode_step_kernel<DK, DV, GATE, true, Tin, Tout><<<(unsigned)BH, DV * 2, 0, stream>>>(
+            (const Tin *)io.q, (const Tin *)io.k, (const Tin *)io.v, io.la, (const Tin *)io.beta,
+            (const Tin *)io.z, io.fuse, io.state, (Tout *)io.out);
+    else
+        decode_step_kernel<DK, DV, GATE, false, Tin, Tout><<<(unsigned)BH, DV * 2, 0, stream>>>(
+            (const Tin *)io.q, (const Tin *)io.k, (const Tin *)io.v, io.la, (const Tin *)io.beta,
+            nullptr, 0u, io.state, (Tout *)io.out);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
