@@ -35,6 +35,25 @@ constexpr int kThreads = 256;
 constexpr int kLdA = 65;   // padded row stride of [64][64] tiles
 constexpr int kDvt = 32;   // state columns per CTA of the reverse pass
 constexpr int kSlice = 32; // rows of a [dk][dv] state matrix staged at a time
+constexpr int kGThreads = 512;   // per-chunk gradient kernel: 8 threads per token row
+constexpr int kParts = 8;
+
+// a . b over n floats (n a multiple of 8, both 16-byte aligned, shared memory): float4 loads
+// into four independent partial sums
+__device__ __forceinline__ float dotv(const float *a, const float *b, int n) {
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+    for (int j = 0; j < n; j += 8) {
+        const float4 x0 = *reinterpret_cast<const float4 *>(a + j);
+        const float4 y0 = *reinterpret_cast<const float4 *>(b + j);
+        const float4 x1 = *reinterpret_cast<const float4 *>(a + j + 4);
+        const float4 y1 = *reinterpret_cast<const float4 *>(b + j + 4);
+        s0.x = fmaf(x0.x, y0.x, s0.x); s0.y = fmaf(x0.y, y0.y, s0.y);
+        s0.z = fmaf(x0.z, y0.z, s0.z); s0.w = fmaf(x0.w, y0.w, s0.w);
+        s1.x = fmaf(x1.x, y1.x, s1.x); s1.y = fmaf(x1.y, y1.y, s1.y);
+        s1.z = fmaf(x1.z, y1.z, s1.z); s1.w = fmaf(x1.w, y1.w, s1.w);
+    }
+    return ((s0.x + s1.x) + (s0.y + s1.y)) + ((s0.z + s1.z) + (s0.w + s1.w));
+}
 
 // Workspace of the backward, in floats, after the forward's slabs: T [n][C][C], checkpoints
 // [n][dk][dv], dS_C [n][dk][dv].
@@ -124,20 +143,48 @@ __global__ void __launch_bounds__(kThreads) chunk_dstate_kernel(DStateArgs a) {
         for (int i = tid; i < DK; i += kThreads) sGam[i] = a.ws.fw.gam[n * DK + i];
         for (int i = rg; i < DK; i += 8) a.ws.dsc[(n * DK + i) * dv + col] = sDS[i * kDvt + j];
         __syncthreads();
-        // dE = P^T dO + Kd dS  (rows r = rg + 8m)
-        for (int r = rg; r < C; r += 8) {
-            float acc = 0.f;
-            for (int s = r; s < C; ++s) acc = fmaf(sP[s * kLdA + r], sDO[s * kDvt + j], acc);
-            for (int i = 0; i < DK; ++i) acc = fmaf(sKd[r * LD + i], sDS[i * kDvt + j], acc);
-            sDE[r * kDvt + j] = acc;
+        // dE = P^T dO + Kd dS  (rows r = rg + 8m: eight independent sums per thread)
+        {
+            float e[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) e[m] = 0.f;
+            for (int s = 0; s < C; ++s) {
+                const float d = sDO[s * kDvt + j];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int r = rg + 8 * m;
+                    if (r < C && s >= r) e[m] = fmaf(sP[s * kLdA + r], d, e[m]);
+                }
+            }
+            for (int i = 0; i < DK; ++i) {
+                const float d = sDS[i * kDvt + j];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int r = rg + 8 * m;
+                    if (r < C) e[m] = fmaf(sKd[r * LD + i], d, e[m]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+                if (rg + 8 * m < C) sDE[(rg + 8 * m) * kDvt + j] = e[m];
         }
         __syncthreads();
         // dS <- Diag(gamma) dS + (Q*G)^T dO - W^T dE  (rows i = rg + 8m; own entries only)
-        for (int i = rg; i < DK; i += 8) {
-            float acc = sGam[i] * sDS[i * kDvt + j];
-            for (int r = 0; r < C; ++r)
-                acc = fmaf(sQg[r * LD + i], sDO[r * kDvt + j], fmaf(-sW[r * LD + i], sDE[r * kDvt + j], acc));
-            sDS[i * kDvt + j] = acc;
+        {
+            constexpr int NR = DK / 8;
+            float acc[NR];
+#pragma unroll
+            for (int m = 0; m < NR; ++m) acc[m] = sGam[rg + 8 * m] * sDS[(rg + 8 * m) * kDvt + j];
+            for (int r = 0; r < C; ++r) {
+                const float d = sDO[r * kDvt + j], de = sDE[r * kDvt + j];
+#pragma unroll
+                for (int m = 0; m < NR; ++m) {
+                    const int i = rg + 8 * m;
+                    acc[m] = fmaf(sQg[r * LD + i], d, fmaf(-sW[r * LD + i], de, acc[m]));
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < NR; ++m) sDS[(rg + 8 * m) * kDvt + j] = acc[m];
         }
     }
     if (a.d_init) {
@@ -161,12 +208,12 @@ struct GradArgs {
 
 size_t grad_smem_bytes(int dk, int dv) {
     const int ldw = (dk > dv ? dk : dv) + 4;
-    return sizeof(float) * (size_t)(3 * 64 * (dk + 4) + 2 * 64 * ldw + 2 * 64 * kLdA + 64 + dk + 64 +
+    return sizeof(float) * (size_t)(3 * 64 * (dk + 8) + 2 * 64 * ldw + 2 * 64 * kLdA + 64 + dk + 64 +
                                     kSlice * (dv + 4));
 }
 
-// Every gradient of one chunk's tokens.  Thread (row r = tid / 4, part = tid % 4) owns key
-// channels i = part + 4m and value columns j = part + 4m of row r; its dq, dk and dg entries
+// Every gradient of one chunk's tokens.  Thread (row r = tid / 8, part = tid % 8) owns key
+// channels i = part + 8m and value columns j = part + 8m of row r; its dq, dk and dg entries
 // accumulate in registers over the phases:
 //   0. q, k, beta, g (cumulative, per channel; a scalar gate is broadcast), T, P, dO;
 //   1. E = U - W S0;  dO S0^T  -> dq, dg;
@@ -177,9 +224,9 @@ size_t grad_smem_bytes(int dk, int dv) {
 //   5. the pair products of P and A -> dq, dk, dg, db part 2;
 //   6. db, dq, dk out; dg summed from the last token back -> d log alpha.
 template <int DK, typename Tin, typename Tg>
-__global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
-    constexpr int LDK = DK + 4;
-    constexpr int NI = DK / 4;   // key channels per thread
+__global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
+    constexpr int LDK = DK + 8;
+    constexpr int NI = DK / kParts;   // key channels per thread
     extern __shared__ float4 smem4[];
     const int dv = a.dv_;
     const int ldw = (DK > dv ? DK : dv) + 4;
@@ -211,13 +258,13 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
     const float *Wn = a.ws.fw.W + n * (int64_t)C * DK;
     const float *Un = a.ws.fw.U + n * (int64_t)C * dv;
     const float *Kdn = a.ws.fw.Kd + n * (int64_t)C * DK;
-    const int r = tid >> 2, part = tid & 3;
+    const int r = tid / kParts, part = tid % kParts;
     const bool row_ok = r < C;
     const int lds = dv + 4;
     // rows i0 .. i0 + kSlice - 1 of a [DK][dv] matrix into sS (all threads; barriers around)
     auto stage = [&](const float *M, int i0) {
         __syncthreads();
-        for (int idx = tid; idx < kSlice * (dv / 4); idx += kThreads) {
+        for (int idx = tid; idx < kSlice * (dv / 4); idx += kGThreads) {
             const int ii = idx / (dv / 4), j4 = 4 * (idx % (dv / 4));
             *reinterpret_cast<float4 *>(sS + ii * lds + j4) = load4(M + (i0 + ii) * dv + j4);
         }
@@ -225,7 +272,7 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
     };
 
     // ---- 0. inputs (rows past the sequence: zero, log alpha 0)
-    for (int idx = tid; idx < C * DK; idx += kThreads) {
+    for (int idx = tid; idx < C * DK; idx += kGThreads) {
         const int rr = idx / DK, i = idx % DK;
         const bool ok = rr < Lc;
         sQ[rr * LDK + i] = ok ? to_f32(q[tok(rr) * DK + i]) : 0.f;
@@ -235,18 +282,18 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
         if (ok && a.gate == 1) la = a.log_alpha[tok(rr)];
         sG[rr * LDK + i] = la;
     }
-    for (int rr = tid; rr < C; rr += kThreads) sB[rr] = rr < Lc ? to_f32(beta[tok(rr)]) : 0.f;
-    for (int idx = tid; idx < C * C; idx += kThreads) {
+    for (int rr = tid; rr < C; rr += kGThreads) sB[rr] = rr < Lc ? to_f32(beta[tok(rr)]) : 0.f;
+    for (int idx = tid; idx < C * C; idx += kGThreads) {
         sT[(idx / C) * kLdA + idx % C] = a.ws.T[n * (int64_t)C * C + idx];
         sP[(idx / C) * kLdA + idx % C] = a.ws.fw.P[n * (int64_t)C * C + idx];
     }
-    for (int idx = tid; idx < C * dv; idx += kThreads) {
+    for (int idx = tid; idx < C * dv; idx += kGThreads) {
         const int rr = idx / dv, j = idx % dv;
         sX[rr * ldw + j] = rr < Lc ? to_f32(dout[tok(rr) * dv + j]) : 0.f;
     }
-    for (int i = tid; i < DK; i += kThreads) sDgC[i] = 0.f;
+    for (int i = tid; i < DK; i += kGThreads) sDgC[i] = 0.f;
     __syncthreads();
-    for (int i = tid; i < DK; i += kThreads) {   // cumulative log decay down each channel
+    for (int i = tid; i < DK; i += kGThreads) {   // cumulative log decay down each channel
         float acc = 0.f;
         for (int rr = 0; rr < C; ++rr) {
             acc += sG[rr * LDK + i];
@@ -259,12 +306,12 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
 #pragma unroll
     for (int m = 0; m < NI; ++m) { aq[m] = 0.f; ak[m] = 0.f; ag[m] = 0.f; }
 
-    // ---- 1. E = U - W S0 (row r, columns part + 4m); dq, dg from (dO S0^T)_ri; S0 staged
+    // ---- 1. E = U - W S0 (row r, columns part + 8m); dq, dg from (dO S0^T)_ri; S0 staged
     //         by slices of kSlice rows
-    constexpr int NJ = 32;   // value columns per thread (dv <= 128)
+    constexpr int NJ = 128 / kParts;   // value columns per thread (dv <= 128)
     float x[NJ];
 #pragma unroll
-    for (int m = 0; m < NJ; ++m) x[m] = (row_ok && part + 4 * m < dv) ? Un[r * dv + part + 4 * m] : 0.f;
+    for (int m = 0; m < NJ; ++m) x[m] = (row_ok && part + kParts * m < dv) ? Un[r * dv + part + kParts * m] : 0.f;
     for (int i0 = 0; i0 < DK; i0 += kSlice) {
         stage(S0, i0);
         if (!row_ok) continue;
@@ -272,14 +319,13 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
             const float w = Wn[r * DK + i0 + ii];
 #pragma unroll
             for (int m = 0; m < NJ; ++m)
-                if (part + 4 * m < dv) x[m] = fmaf(-w, sS[ii * lds + part + 4 * m], x[m]);
+                if (part + kParts * m < dv) x[m] = fmaf(-w, sS[ii * lds + part + kParts * m], x[m]);
         }
 #pragma unroll
         for (int m = 0; m < NI; ++m) {
-            const int i = part + 4 * m;
+            const int i = part + kParts * m;
             if (i < i0 || i >= i0 + kSlice) continue;
-            float acc = 0.f;
-            for (int j = 0; j < dv; ++j) acc = fmaf(sX[r * ldw + j], sS[(i - i0) * lds + j], acc);
+            const float acc = dotv(sX + r * ldw, sS + (i - i0) * lds, dv);
             const float e = __expf(sG[r * LDK + i]);
             aq[m] = fmaf(e, acc, aq[m]);
             ag[m] = fmaf(sQ[r * LDK + i] * e, acc, ag[m]);
@@ -288,19 +334,20 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
     if (row_ok)
 #pragma unroll
         for (int m = 0; m < NJ; ++m)
-            if (part + 4 * m < dv) sE[r * ldw + part + 4 * m] = x[m];
+            if (part + kParts * m < dv) sE[r * ldw + part + kParts * m] = x[m];
     __syncthreads();
 
     // ---- 2. dE = P^T dO + Kd dS_C (registers; dS_C by slices), dP = tril(dO E^T) over P,
     //         then dE over dO
 #pragma unroll
-    for (int m = 0; m < NJ; ++m) {
-        const int j = part + 4 * m;
-        float acc = 0.f;
-        if (row_ok && j < dv)
-            for (int s = r; s < C; ++s) acc = fmaf(sP[s * kLdA + r], sX[s * ldw + j], acc);
-        x[m] = acc;
-    }
+    for (int m = 0; m < NJ; ++m) x[m] = 0.f;
+    if (row_ok)
+        for (int s = r; s < C; ++s) {
+            const float pv = sP[s * kLdA + r];
+#pragma unroll
+            for (int m = 0; m < NJ; ++m)
+                if (part + kParts * m < dv) x[m] = fmaf(pv, sX[s * ldw + part + kParts * m], x[m]);
+        }
     for (int i0 = 0; i0 < DK; i0 += kSlice) {
         stage(dSC, i0);
         if (!row_ok) continue;
@@ -308,56 +355,46 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
             const float kd = Kdn[r * DK + i0 + ii];
 #pragma unroll
             for (int m = 0; m < NJ; ++m)
-                if (part + 4 * m < dv) x[m] = fmaf(kd, sS[ii * lds + part + 4 * m], x[m]);
+                if (part + kParts * m < dv) x[m] = fmaf(kd, sS[ii * lds + part + kParts * m], x[m]);
         }
     }
     __syncthreads();
     if (row_ok)
-        for (int s = part; s < C; s += 4) {
-            float acc = 0.f;
-            if (s <= r)
-                for (int j = 0; j < dv; ++j) acc = fmaf(sX[r * ldw + j], sE[s * ldw + j], acc);
-            sP[r * kLdA + s] = acc;
-        }
+        for (int s = part; s < C; s += kParts)
+            sP[r * kLdA + s] = s <= r ? dotv(sX + r * ldw, sE + s * ldw, dv) : 0.f;
     __syncthreads();
     if (row_ok)
 #pragma unroll
         for (int m = 0; m < NJ; ++m)
-            if (part + 4 * m < dv) sX[r * ldw + part + 4 * m] = x[m];
+            if (part + kParts * m < dv) sX[r * ldw + part + kParts * m] = x[m];
     __syncthreads();
 
     // ---- 3. dR = T^T dE, over dE
-    if (row_ok) {
 #pragma unroll
-        for (int m = 0; m < NJ; ++m) {
-            const int j = part + 4 * m;
-            if (j < dv) {
-                float acc = 0.f;
-                for (int s = r; s < C; ++s) acc = fmaf(sT[s * kLdA + r], sX[s * ldw + j], acc);
-                x[m] = acc;
-            }
+    for (int m = 0; m < NJ; ++m) x[m] = 0.f;
+    if (row_ok)
+        for (int s = r; s < C; ++s) {
+            const float tv = sT[s * kLdA + r];
+#pragma unroll
+            for (int m = 0; m < NJ; ++m)
+                if (part + kParts * m < dv) x[m] = fmaf(tv, sX[s * ldw + part + kParts * m], x[m]);
         }
-    }
     __syncthreads();
     if (row_ok)
 #pragma unroll
         for (int m = 0; m < NJ; ++m)
-            if (part + 4 * m < dv) sX[r * ldw + part + 4 * m] = x[m];
+            if (part + kParts * m < dv) sX[r * ldw + part + kParts * m] = x[m];
     __syncthreads();
 
     // ---- 4. dA over T; dv; db part 1 (with (K*G) S0); (dR S0^T) -> dk, dg; S0 by slices
     const float br = row_ok ? sB[r] : 0.f;
     float db = 0.f;
     if (row_ok) {
-        for (int s = part; s < C; s += 4) {
-            float acc = 0.f;
-            if (s < r)
-                for (int j = 0; j < dv; ++j) acc = fmaf(sX[r * ldw + j], sE[s * ldw + j], acc);
-            sT[r * kLdA + s] = -acc;
-        }
+        for (int s = part; s < C; s += kParts)
+            sT[r * kLdA + s] = s < r ? -dotv(sX + r * ldw, sE + s * ldw, dv) : 0.f;
         if (r < Lc) {
             Tin *gv = (Tin *)a.dv;
-            for (int j = part; j < dv; j += 4) gv[tok(r) * dv + j] = from_f32<Tin>(br * sX[r * ldw + j]);
+            for (int j = part; j < dv; j += kParts) gv[tok(r) * dv + j] = from_f32<Tin>(br * sX[r * ldw + j]);
         }
     }
 #pragma unroll
@@ -369,14 +406,13 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
             const float kg = sK[r * LDK + i0 + ii] * __expf(sG[r * LDK + i0 + ii]);
 #pragma unroll
             for (int m = 0; m < NJ; ++m)
-                if (part + 4 * m < dv) x[m] = fmaf(kg, sS[ii * lds + part + 4 * m], x[m]);
+                if (part + kParts * m < dv) x[m] = fmaf(kg, sS[ii * lds + part + kParts * m], x[m]);
         }
 #pragma unroll
         for (int m = 0; m < NI; ++m) {
-            const int i = part + 4 * m;
+            const int i = part + kParts * m;
             if (i < i0 || i >= i0 + kSlice) continue;
-            float acc = 0.f;
-            for (int j = 0; j < dv; ++j) acc = fmaf(sX[r * ldw + j], sS[(i - i0) * lds + j], acc);
+            const float acc = dotv(sX + r * ldw, sS + (i - i0) * lds, dv);
             const float w = br * __expf(sG[r * LDK + i]) * acc;
             ak[m] -= w;
             ag[m] = fmaf(-w, sK[r * LDK + i], ag[m]);
@@ -385,7 +421,7 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
     if (row_ok)
 #pragma unroll
         for (int m = 0; m < NJ; ++m) {
-            const int j = part + 4 * m;
+            const int j = part + kParts * m;
             if (j < dv) {
                 const float u0 = (r < Lc ? to_f32(v[tok(r) * dv + j]) : 0.f) - x[m];
                 db = fmaf(sX[r * ldw + j], u0, db);
@@ -399,10 +435,9 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
         if (!row_ok) continue;
 #pragma unroll
         for (int m = 0; m < NI; ++m) {
-            const int i = part + 4 * m;
+            const int i = part + kParts * m;
             if (i < i0 || i >= i0 + kSlice) continue;
-            float y = 0.f;
-            for (int j = 0; j < dv; ++j) y = fmaf(sE[r * ldw + j], sS[(i - i0) * lds + j], y);
+            const float y = dotv(sE + r * ldw, sS + (i - i0) * lds, dv);
             const float f = __expf(sG[(C - 1) * LDK + i] - sG[r * LDK + i]);
             const float z = y * sK[r * LDK + i] * f;
             ak[m] = fmaf(y, f, ak[m]);
@@ -411,7 +446,7 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
         }
     }
     __syncthreads();
-    for (int i = tid; i < DK; i += kThreads) {   // d g_C,i = sum_r z_ri + sum_j dS_C,ij gamma_i S0_ij
+    for (int i = tid; i < DK; i += kGThreads) {   // d g_C,i = sum_r z_ri + sum_j dS_C,ij gamma_i S0_ij
         float acc = 0.f;
         for (int rr = 0; rr < C; ++rr) acc += sX[rr * ldw + i];
         const float gi = __expf(sG[(C - 1) * LDK + i]);
@@ -429,7 +464,7 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
             const float da = s < r ? sT[r * kLdA + s] : 0.f;
 #pragma unroll
             for (int m = 0; m < NI; ++m) {
-                const int i = part + 4 * m;
+                const int i = part + kParts * m;
                 const float kd = sK[s * LDK + i] * __expf(sG[r * LDK + i] - sG[s * LDK + i]);
                 const float kr = sK[r * LDK + i];
                 const float tq = dp * kd, ta = da * br * kd;
@@ -444,7 +479,7 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
             const float da = s2 > r ? sT[s2 * kLdA + r] * sB[s2] : 0.f;
 #pragma unroll
             for (int m = 0; m < NI; ++m) {
-                const int i = part + 4 * m;
+                const int i = part + kParts * m;
                 const float d = __expf(sG[s2 * LDK + i] - sG[r * LDK + i]);
                 const float t = (dp * sQ[s2 * LDK + i] + da * sK[s2 * LDK + i]) * d;
                 ak[m] += t;
@@ -455,6 +490,7 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
     db += db2;
     db += __shfl_xor_sync(0xffffffffu, db, 1);
     db += __shfl_xor_sync(0xffffffffu, db, 2);
+    db += __shfl_xor_sync(0xffffffffu, db, 4);
 
     // ---- 6. outputs; d log alpha_t = sum_{r >= t} dg_r (+ the last token's gamma terms)
     if (row_ok && r < Lc) {
@@ -462,18 +498,18 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
         if (part == 0) ((Tin *)a.d_beta)[tok(r)] = from_f32<Tin>(db);
 #pragma unroll
         for (int m = 0; m < NI; ++m) {
-            gq[tok(r) * DK + part + 4 * m] = from_f32<Tin>(aq[m]);
-            gk[tok(r) * DK + part + 4 * m] = from_f32<Tin>(ak[m]);
+            gq[tok(r) * DK + part + kParts * m] = from_f32<Tin>(aq[m]);
+            gk[tok(r) * DK + part + kParts * m] = from_f32<Tin>(ak[m]);
         }
     }
     if (a.gate == 0) return;
     __syncthreads();   // sQ is dead
     if (row_ok)
 #pragma unroll
-        for (int m = 0; m < NI; ++m) sQ[r * LDK + part + 4 * m] = ag[m];
+        for (int m = 0; m < NI; ++m) sQ[r * LDK + part + kParts * m] = ag[m];
     __syncthreads();
     if (a.gate == 2) {
-        for (int i = tid; i < DK; i += kThreads) {
+        for (int i = tid; i < DK; i += kGThreads) {
             float run = sDgC[i];
             for (int rr = C - 1; rr >= 0; --rr) {
                 run += sQ[rr * LDK + i];
@@ -481,7 +517,7 @@ __global__ void __launch_bounds__(kThreads) chunk_grad_kernel(GradArgs a) {
             }
         }
     } else {
-        for (int rr = tid; rr < C; rr += kThreads) {
+        for (int rr = tid; rr < C; rr += kGThreads) {
             float acc = 0.f;
             for (int i = 0; i < DK; ++i) acc += sQ[rr * LDK + i];
             sRed[rr] = acc;
@@ -508,7 +544,7 @@ int launch_bwd_t(const DStateArgs &da, const GradArgs &ga, int64_t nstate, int64
                              (int)gs) != cudaSuccess)
         return kErrCuda;
     chunk_dstate_kernel<DK, Tg><<<(unsigned)nstate, kThreads, ds, stream>>>(da);
-    if (ngrad > 0) chunk_grad_kernel<DK, Tin, Tg><<<(unsigned)ngrad, kThreads, gs, stream>>>(ga);
+    if (ngrad > 0) chunk_grad_kernel<DK, Tin, Tg><<<(unsigned)ngrad, kGThreads, gs, stream>>>(ga);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 

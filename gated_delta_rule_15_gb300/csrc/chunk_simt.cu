@@ -462,14 +462,23 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(StateArgs a) {
             if (r < C) sE[r * kDvt + j] = sU[r * kDvt + j] - e[m];
         }
         __syncthreads();
-        // O = (Q*G) S + P E  (P lower triangular, diagonal included).
+        // O = (Q*G) S + P E  (P lower triangular, diagonal included): eight rows at once;
+        // skipped when the outputs are not wanted (the backward's recompute)
+        if (out) {
+#pragma unroll 4
+            for (int s = 0; s < C; ++s) {
+                const float es = sE[s * kDvt + j];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const int r = rg + 8 * m;
-            if (r < C) {
-                float acc = o[m];
-                for (int s = 0; s <= r; ++s) acc += sP[r * kLdA + s] * sE[s * kDvt + j];
-                if (r < Lc && out) {
+                for (int m = 0; m < 8; ++m) {
+                    const int r = rg + 8 * m;
+                    if (r < C && s <= r) o[m] = fmaf(sP[r * kLdA + s], es, o[m]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int r = rg + 8 * m;
+                if (r < Lc) {
+                    float acc = o[m];
                     const int64_t oi = ((b * a.T + t0 + r) * a.H + h) * dv + col;
                     if (a.z)
                         acc *= silu_f(a.z_bf16 ? to_f32(((const __nv_bfloat16 *)a.z)[oi])
@@ -478,11 +487,19 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(StateArgs a) {
                 }
             }
         }
-        // S <- Diag(G_C) S + (K*G_C/G)^T E.
-        for (int i = rg; i < DK; i += 8) {
-            float acc = sGam[i] * sS[i * kDvt + j];
-            for (int r = 0; r < C; ++r) acc += sKd[r * LD + i] * sE[r * kDvt + j];
-            sS[i * kDvt + j] = acc;
+        // S <- Diag(G_C) S + (K*G_C/G)^T E: DK / 8 independent sums per thread
+        {
+            constexpr int NR = DK / 8;
+            float acc[NR];
+#pragma unroll
+            for (int m = 0; m < NR; ++m) acc[m] = sGam[rg + 8 * m] * sS[(rg + 8 * m) * kDvt + j];
+            for (int r = 0; r < C; ++r) {
+                const float e = sE[r * kDvt + j];
+#pragma unroll
+                for (int m = 0; m < NR; ++m) acc[m] = fmaf(sKd[r * LD + rg + 8 * m], e, acc[m]);
+            }
+#pragma unroll
+            for (int m = 0; m < NR; ++m) sS[(rg + 8 * m) * kDvt + j] = acc[m];
         }
     }
     if (a.final_state) {
