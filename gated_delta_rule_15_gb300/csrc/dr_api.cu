@@ -4,6 +4,7 @@
 #include "../../include/dr.h"
 #include "chunk_layout.h"
 #include "common.cuh"
+#include "umma.cuh"
 
 namespace dr {
 
@@ -23,6 +24,22 @@ int *device_status_ptr() {
         addr[dev] = (int *)p;
     }
     return addr[dev];
+}
+
+// dr_selftest_bounded_wait's kernel: one thread waits, with the chunk kernels' bounded loop
+// (try_wait until a clock64 budget is spent), on an mbarrier that nothing completes; on
+// expiry it records DR_ERR_TIMEOUT in the status word, as an expired wait in a chunk
+// kernel does, and returns.
+__global__ void bounded_wait_kernel(long long budget, int *status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    umma::mbar_init(&bar, 1);
+    umma::fence_mbar_init();
+    const long long t0 = clock64();
+    bool done = false;
+    while (!(done = umma::mbar_try_wait(&bar, 0)))
+        if (clock64() - t0 > budget) break;
+    if (!done) atomicExch(status, kErrTimeout);
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -202,6 +219,14 @@ extern "C" int dr_recurrent_step(const dr_step_desc *d, const void *q, const voi
                                  const void *v, const float *log_alpha, const void *beta,
                                  float *state, void *out, dr_stream_t stream) {
     return dr_recurrent_step_ex(d, 0u, q, k, v, log_alpha, beta, nullptr, state, out, stream);
+}
+
+extern "C" int dr_selftest_bounded_wait(long long cycles, dr_stream_t stream) {
+    if (cycles < 1 || cycles > 4000000000LL) return kErrInvalid;
+    int *status = device_status_ptr();
+    if (!status) return kErrCuda;
+    bounded_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(cycles, status);
+    return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
 extern "C" int dr_get_device_status(dr_stream_t stream) {

@@ -36,7 +36,7 @@ L2NORM_EPS = 1e-6   # DR_L2NORM_EPS
 EXPORTED = ("dr_version", "dr_chunk_fwd_workspace_bytes", "dr_chunk_fwd",
             "dr_recurrent_step", "dr_get_device_status", "dr_strerror",
             "dr_chunk_fwd_noalloc", "dr_chunk_fwd_ex", "dr_recurrent_step_ex",
-            "dr_chunk_bwd_workspace_bytes", "dr_chunk_bwd")
+            "dr_chunk_bwd_workspace_bytes", "dr_chunk_bwd", "dr_selftest_bounded_wait")
 
 
 class ChunkDesc(ctypes.Structure):
@@ -76,6 +76,8 @@ _lib.dr_chunk_bwd_workspace_bytes.argtypes = [ctypes.POINTER(ChunkDesc),
 _lib.dr_chunk_bwd_workspace_bytes.restype = ctypes.c_int
 _lib.dr_chunk_bwd.argtypes = [ctypes.POINTER(ChunkDesc)] + [_vp] * 15 + [ctypes.c_size_t, _vp]
 _lib.dr_chunk_bwd.restype = ctypes.c_int
+_lib.dr_selftest_bounded_wait.argtypes = [ctypes.c_longlong, _vp]
+_lib.dr_selftest_bounded_wait.restype = ctypes.c_int
 _lib.dr_get_device_status.argtypes = [_vp]
 _lib.dr_get_device_status.restype = ctypes.c_int
 _lib.dr_strerror.argtypes = [ctypes.c_int]
@@ -310,6 +312,12 @@ def recurrent_step(q, k, v, log_alpha, beta, state, *, out=None, out_dtype=None,
     if rc != DR_OK:
         raise DrError(rc, "dr_recurrent_step")
     return out
+
+
+def selftest_bounded_wait(cycles: int = 2_000_000, stream=None) -> int:
+    """dr_selftest_bounded_wait: a wait that runs out on purpose (no fault); the next
+    device_status() returns DR_ERR_TIMEOUT.  Returns the enqueue status."""
+    return _lib.dr_selftest_bounded_wait(int(cycles), _stream_handle(stream))
 
 
 def device_status(stream=None) -> int:

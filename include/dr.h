@@ -242,6 +242,13 @@ int dr_chunk_fwd_noalloc(const dr_chunk_desc *desc,
    DR_ERR_CUDA if the synchronisation itself failed. */
 int dr_get_device_status(dr_stream_t stream);
 
+/* Self-test of failure detection, with no GPU fault: launches one kernel whose thread waits
+   on a barrier that nothing completes, with the chunk kernels' bounded-wait loop and a
+   budget of `cycles` SM clock cycles (1 .. 4e9); on expiry it records DR_ERR_TIMEOUT in
+   the status word that dr_get_device_status returns, and exits.  Returns DR_OK once
+   enqueued, DR_ERR_INVALID for a budget out of range, DR_ERR_CUDA on a launch failure. */
+int dr_selftest_bounded_wait(long long cycles, dr_stream_t stream);
+
 /* Static, human-readable text of a status code (never NULL). */
 const char *dr_strerror(int status);
 

@@ -167,3 +167,9 @@ def test_chunk_bwd_host_side_errors(dr):
     assert call(args(), wb=n.value - 16) == dr.DR_ERR_WORKSPACE
     d0 = _desc(dr, gate=dr.DR_GATE_NONE)
     assert lib.dr_chunk_bwd(ctypes.byref(d0), *args(), 1 << 40, None) == dr.DR_ERR_INVALID
+
+
+def test_selftest_budget_checked_on_host(dr):
+    lib = dr.lib()
+    assert lib.dr_selftest_bounded_wait(0, None) == dr.DR_ERR_INVALID
+    assert lib.dr_selftest_bounded_wait(5_000_000_000, None) == dr.DR_ERR_INVALID
