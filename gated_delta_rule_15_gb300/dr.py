@@ -36,7 +36,8 @@ L2NORM_EPS = 1e-6   # DR_L2NORM_EPS
 EXPORTED = ("dr_version", "dr_chunk_fwd_workspace_bytes", "dr_chunk_fwd",
             "dr_recurrent_step", "dr_get_device_status", "dr_strerror",
             "dr_chunk_fwd_noalloc", "dr_chunk_fwd_ex", "dr_recurrent_step_ex",
-            "dr_chunk_bwd_workspace_bytes", "dr_chunk_bwd", "dr_selftest_bounded_wait")
+            "dr_chunk_bwd_workspace_bytes", "dr_chunk_bwd", "dr_selftest_bounded_wait",
+            "dr_chunk_fwd_host_dev_bytes", "dr_chunk_fwd_host")
 
 
 class ChunkDesc(ctypes.Structure):
@@ -76,6 +77,12 @@ _lib.dr_chunk_bwd_workspace_bytes.argtypes = [ctypes.POINTER(ChunkDesc),
 _lib.dr_chunk_bwd_workspace_bytes.restype = ctypes.c_int
 _lib.dr_chunk_bwd.argtypes = [ctypes.POINTER(ChunkDesc)] + [_vp] * 15 + [ctypes.c_size_t, _vp]
 _lib.dr_chunk_bwd.restype = ctypes.c_int
+_lib.dr_chunk_fwd_host_dev_bytes.argtypes = [ctypes.POINTER(ChunkDesc), ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
+_lib.dr_chunk_fwd_host_dev_bytes.restype = ctypes.c_int
+_lib.dr_chunk_fwd_host.argtypes = [ctypes.POINTER(ChunkDesc), ctypes.c_int] + [_vp] * 9 + \
+    [ctypes.c_size_t, _vp]
+_lib.dr_chunk_fwd_host.restype = ctypes.c_int
 _lib.dr_selftest_bounded_wait.argtypes = [ctypes.c_longlong, _vp]
 _lib.dr_selftest_bounded_wait.restype = ctypes.c_int
 _lib.dr_get_device_status.argtypes = [_vp]
@@ -326,52 +333,60 @@ def device_status(stream=None) -> int:
 
 
 class HostChunkRunner:
-    """End-to-end chunk forward for callers holding HOST buffers.
+    """End-to-end chunk forward for callers holding HOST buffers, through dr_chunk_fwd_host.
 
-    Owns device staging buffers and pinned host result buffers for one problem shape.
-    Each call copies the inputs host -> device on the current stream, runs dr_chunk_fwd,
-    copies out and final_state device -> host, and synchronises.  Returns the pinned host
-    result tensors (reused across calls)."""
+    Owns the device staging buffer and pinned host result buffers for one problem shape.
+    Each call enqueues, behind the current stream, the host -> device copies of the inputs,
+    the forward and the device -> host copies of out and final_state, the batch split into
+    `pieces` groups of rows so that copies and kernels overlap; with `sync` it waits for
+    the stream.  Returns the pinned host result tensors (reused across calls).  The host
+    inputs should be pinned."""
 
-    def __init__(self, like: dict, *, chunk: int = 64, out_dtype=None, device="cuda"):
-        def mk(t):
-            return None if t is None else torch.empty(t.shape, dtype=t.dtype, device=device)
-        self.dev = {k_: mk(t) for k_, t in like.items()}
+    def __init__(self, like: dict, *, chunk: int = 64, out_dtype=None, pieces: int = 8,
+                 device="cuda"):
         q, v = like["q"], like["v"]
         B, T, H, dk = q.shape
         dv = v.shape[-1]
         odt = out_dtype or q.dtype
-        self.out = torch.empty((B, T, H, dv), dtype=odt, device=device)
-        self.fin = torch.empty((B, H, dk, dv), dtype=torch.float32, device=device)
-        self.out_h = torch.empty(self.out.shape, dtype=odt, pin_memory=True)
-        self.fin_h = torch.empty(self.fin.shape, dtype=torch.float32, pin_memory=True)
-        self.chunk = chunk
+        self.pieces = pieces
+        self.out_h = torch.empty((B, T, H, dv), dtype=odt, pin_memory=True)
+        self.fin_h = torch.empty((B, H, dk, dv), dtype=torch.float32, pin_memory=True)
         gate = _gate_of(like["log_alpha"], (B, T, H), dk)
-        desc = chunk_desc(B, T, H, dk, dv, _DT[q.dtype], _DT[odt], gate, chunk)
-        n = workspace_bytes(desc)
-        self.ws = torch.empty(n, dtype=torch.uint8, device=device) if n else None
+        self.desc = chunk_desc(B, T, H, dk, dv, _DT[q.dtype], _DT[odt], gate, chunk)
+        self.with_init = like.get("init_state") is not None
+        n = ctypes.c_size_t(0)
+        rc = _lib.dr_chunk_fwd_host_dev_bytes(ctypes.byref(self.desc), pieces, int(self.with_init),
+                                              1, ctypes.byref(n))
+        if rc != DR_OK:
+            raise DrError(rc, "dr_chunk_fwd_host_dev_bytes")
+        self.dev = torch.empty(n.value + 256, dtype=torch.uint8, device=device)
+        self.dev_off = (-self.dev.data_ptr()) % 256     # 256-byte aligned start
+        self.dev_bytes = n.value
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in like.values()
                              if t is not None)
         self.d2h_bytes = (self.out_h.numel() * self.out_h.element_size()
                           + self.fin_h.numel() * self.fin_h.element_size())
 
     def __call__(self, host: dict, sync: bool = True):
-        for k_, t in host.items():
-            if t is not None:
-                self.dev[k_].copy_(t, non_blocking=True)
-        g = self.dev
-        chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g.get("init_state"),
-                  chunk=self.chunk, out=self.out, final_state=self.fin, workspace=self.ws)
-        self.out_h.copy_(self.out, non_blocking=True)
-        self.fin_h.copy_(self.fin, non_blocking=True)
+        for t in host.values():
+            if t is not None and t.is_cuda:
+                raise ValueError("HostChunkRunner takes host tensors")
+        rc = _lib.dr_chunk_fwd_host(
+            ctypes.byref(self.desc), self.pieces, _ptr(host["q"]), _ptr(host["k"]), _ptr(host["v"]),
+            _ptr(host["log_alpha"]), _ptr(host["beta"]), _ptr(host.get("init_state")),
+            _ptr(self.out_h), _ptr(self.fin_h),
+            ctypes.c_void_p(self.dev.data_ptr() + self.dev_off), self.dev_bytes,
+            _stream_handle(None))
+        if rc != DR_OK:
+            raise DrError(rc, "dr_chunk_fwd_host")
         if sync:
             torch.cuda.current_stream().synchronize()
         return self.out_h, self.fin_h
 
 
 def chunk_fwd_host(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
-                   out_dtype=None):
+                   out_dtype=None, pieces: int = 8):
     """One-shot end-to-end call for host tensors (see HostChunkRunner)."""
     like = {"q": q, "k": k, "v": v, "log_alpha": log_alpha, "beta": beta,
             "init_state": init_state}
-    return HostChunkRunner(like, chunk=chunk, out_dtype=out_dtype)(like)
+    return HostChunkRunner(like, chunk=chunk, out_dtype=out_dtype, pieces=pieces)(like)
