@@ -105,3 +105,36 @@ def test_zero_length_returns_final_gradient(dr):
 def test_longer_sequence_bf16(dr):
     # 32 chunks: the reverse state-gradient pass carries dS through every chunk
     check(dr, grads_problem(1, 2048, 2, 128, 128, gate="scalar", dtype="bf16", seed=5), "bf16")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,nsample", [("gdn_bf16_B8_H16_T4096_d128", 2),
+                                          ("kda_bf16_B4_H32_T8192_d128", 1)])
+def test_full_size_sampled_chains(dr, name, nsample):
+    """The backward of the full workload, in the configuration the benchmark times; the
+    oracle's reverse mode recomputes a sample of whole (b, h) chains."""
+    import numpy as np
+    w = inputs.WORKLOADS[name]
+    d = inputs.workload_inputs(w)
+    g = torch.Generator().manual_seed(1)
+    d_out = torch.randn((w.B, w.T, w.H, w.dv), generator=g).to(inputs.DTYPES[w.dtype])
+    dev = {k: (None if v is None else v.cuda()) for k, v in d.items()}
+    got = dr.chunk_bwd(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"],
+                       dev["init_state"], d_out.cuda(), None, chunk=w.chunk)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    got = [None if t is None else t.cpu() for t in got]
+    rng = np.random.default_rng(0)
+    for c in rng.choice(w.B * w.H, size=nsample, replace=False):
+        b, h = int(c) // w.H, int(c) % w.H
+        pick = lambda t: None if t is None else t[b:b + 1, :, h:h + 1].contiguous()
+        s0 = None if d["init_state"] is None else d["init_state"][b:b + 1, h:h + 1]
+        ref = oracle.backward(pick(d["q"]), pick(d["k"]), pick(d["v"]), pick(d["log_alpha"]),
+                              pick(d["beta"]), s0, pick(d_out), None)
+        names = ("dq", "dk", "dv", "dlog_alpha", "dbeta")
+        for name_, gt, r in zip(names, got, ref):
+            if r is None:
+                continue
+            assert_grad(pick(gt), r, "f32" if name_ == "dlog_alpha" else w.dtype,
+                        f"{name_} chain {(b, h)}")
+        assert_grad(got[5][b:b + 1, h:h + 1], ref[5], "f32", f"dinit chain {(b, h)}")

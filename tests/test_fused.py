@@ -191,3 +191,22 @@ def test_decode_continues_fused_prefill(dr):
                                         d["init_state"], **kw)
     assert_out(o, o_ref[:, 96], d["z"][:, 96], "bf16")
     assert_close(st, f_ref, "bf16", "state")
+
+
+@pytest.mark.slow
+def test_full_size_sampled_chains_all_flags(dr):
+    """Every neighbour fused on the headline workload at full size (B8 H16 T4096), in the
+    configuration the benchmark times; the oracle recomputes a sample of whole chains."""
+    w = inputs.WORKLOADS["gdn_bf16_B8_H16_T4096_d128"]
+    d = problem(w.B, w.T, w.H, w.dk, w.dv, FLAGS[-1], gate=w.gate, dtype=w.dtype, seed=0)
+    out, fin = run(dr, d, FLAGS[-1])
+    out, fin = out.cpu(), fin.cpu()
+    rng = np.random.default_rng(1)
+    for c in rng.choice(w.B * w.H, size=3, replace=False):
+        b, h = int(c) // w.H, int(c) % w.H
+        pick = lambda t: None if t is None else t[b:b + 1, :, h:h + 1].contiguous()
+        o_ref, f_ref = oracle.forward_fused(pick(d["q"]), pick(d["k"]), pick(d["v"]),
+                                            pick(d["log_alpha"]), pick(d["beta"]), None,
+                                            qk_l2norm=True, beta_sigmoid=True)
+        assert_out(out[b:b + 1, :, h:h + 1], o_ref, pick(d["z"]), "bf16", f"out chain {(b, h)}")
+        assert_close(fin[b:b + 1, h:h + 1], f_ref, "bf16", f"state chain {(b, h)}")
