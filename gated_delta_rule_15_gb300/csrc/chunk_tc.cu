@@ -828,34 +828,40 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
 // Segment chaining (between the two segment passes): per chain, S_start(0) = S_0 and
 // S_start(p + 1) = Phi_p S_start(p) + S0_p, where Phi_p and S0_p are segment p's transition
-// and zero-start end state.  One CTA per (chain, block of 32 state columns), fp32.
+// and zero-start end state.  One CTA per (chain, block of 32 state columns), fp32; each
+// Phi_p is staged in shared memory (64 KB, coalesced) before its product.
+constexpr int kCombineSmem = 128 * 128 * 4;
 __global__ void __launch_bounds__(256) seg_combine_kernel(const float *__restrict__ init_state,
                                                            const float *__restrict__ phi,
                                                            const float *__restrict__ s0,
                                                            float *__restrict__ start, int nseg) {
     __shared__ float S[128][33];
+    extern __shared__ float4 phi_s4[];
+    const float *phi_s = reinterpret_cast<const float *>(phi_s4);   // [128][128]
     const int cb = blockIdx.x & 3, bh = blockIdx.x >> 2;
     const int tid = threadIdx.x, j = tid & 31, rg = tid >> 5;
     const int col = 32 * cb + j;
     for (int i = rg; i < 128; i += 8)
         S[i][j] = init_state ? init_state[((size_t)bh * 128 + i) * 128 + col] : 0.f;
-    __syncthreads();
     for (int p = 0; p < nseg; ++p) {
         const size_t slot = ((size_t)bh * nseg + p) * 16384;
+        __syncthreads();   // S is complete; the previous Phi's readers are done
         for (int i = rg; i < 128; i += 8) start[slot + i * 128 + col] = S[i][j];
         if (p + 1 == nseg) break;
+        for (int idx = tid; idx < 4096; idx += 256)
+            phi_s4[idx] = reinterpret_cast<const float4 *>(phi + slot)[idx];
         float acc[16];
 #pragma unroll
         for (int m = 0; m < 16; ++m) acc[m] = s0[slot + (size_t)(rg + 8 * m) * 128 + col];
+        __syncthreads();
         for (int k = 0; k < 128; ++k) {
             const float sk = S[k][j];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) acc[m] = fmaf(phi[slot + (size_t)(rg + 8 * m) * 128 + k], sk, acc[m]);
+            for (int m = 0; m < 16; ++m) acc[m] = fmaf(phi_s[(rg + 8 * m) * 128 + k], sk, acc[m]);
         }
         __syncthreads();
 #pragma unroll
         for (int m = 0; m < 16; ++m) S[rg + 8 * m][j] = acc[m];
-        __syncthreads();
     }
 }
 
@@ -971,7 +977,11 @@ int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cu
     ta.role = 1;
     int rc = launch(ta, bh * nseg * 2);
     if (rc != kOk) return rc;
-    seg_combine_kernel<<<bh * 4, 256, 0, stream>>>(p.init_state, ta.ws_phi, ta.ws_s0, ta.ws_start, nseg);
+    if (cudaFuncSetAttribute(seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCombineSmem) !=
+        cudaSuccess)
+        return kErrCuda;
+    seg_combine_kernel<<<bh * 4, 256, kCombineSmem, stream>>>(p.init_state, ta.ws_phi, ta.ws_s0, ta.ws_start,
+                                                              nseg);
     if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     ta.role = 2;
     return launch(ta, bh * nseg);
