@@ -458,7 +458,37 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     //         k_ri k_si D_rs,i (s < r), D = exp(g_r - g_s) <= 1; row r as the row, then as
     //         the column
     float db2 = 0.f;
-    if (row_ok) {
+    if (row_ok && a.gate != 2) {   // scalar gate or none: D_rs is one number per (r, s)
+        const float gr = sG[r * LDK];
+        for (int s = 0; s <= r; ++s) {
+            const float d = __expf(gr - sG[s * LDK]);
+            const float cp = sP[r * kLdA + s] * d;
+            const float da = s < r ? sT[r * kLdA + s] * d : 0.f, ca = da * br;
+            float kk = 0.f;
+#pragma unroll
+            for (int m = 0; m < NI; ++m) {
+                const int i = part + kParts * m;
+                const float ks = sK[s * LDK + i], kr = sK[r * LDK + i];
+                aq[m] = fmaf(cp, ks, aq[m]);
+                ak[m] = fmaf(ca, ks, ak[m]);
+                ag[m] = fmaf(ks, fmaf(cp, sQ[r * LDK + i], ca * kr), ag[m]);
+                kk = fmaf(kr, ks, kk);
+            }
+            db2 = fmaf(da, kk, db2);
+        }
+        for (int s2 = r; s2 < C; ++s2) {
+            const float d = __expf(sG[s2 * LDK] - gr);
+            const float c1 = sP[s2 * kLdA + r] * d;
+            const float c2 = s2 > r ? sT[s2 * kLdA + r] * sB[s2] * d : 0.f;
+#pragma unroll
+            for (int m = 0; m < NI; ++m) {
+                const int i = part + kParts * m;
+                const float t = fmaf(c1, sQ[s2 * LDK + i], c2 * sK[s2 * LDK + i]);
+                ak[m] += t;
+                ag[m] = fmaf(-sK[r * LDK + i], t, ag[m]);
+            }
+        }
+    } else if (row_ok) {
         for (int s = 0; s <= r; ++s) {
             const float dp = sP[r * kLdA + s];
             const float da = s < r ? sT[r * kLdA + s] : 0.f;
