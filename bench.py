@@ -174,13 +174,25 @@ def dist_setup():
 
 
 def max_over_ranks(x, world):
+    """The largest of every rank's x (a time: the slowest rank sets the job's)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(rank):
+    """Each rank draws its own batch (weak scaling over independent batches)."""
+    return 1000 * rank
+
+
+def job_throughput(units_per_rank, ms_max, world):
+    """Units all ranks processed per second, over the slowest rank's time."""
+    return world * units_per_rank / (ms_max * 1e-3)
 
 
 def barrier(world):
@@ -228,10 +240,10 @@ def time_calls(fn, steps, warmup, world, sampler_index=None, soak_s=1.0):
     return max_over_ranks(ms, world), (sampler.summary() if sampler else None)
 
 
-def bench_chunk(w, steps, warmup, world, sample_clocks=None):
+def bench_chunk(w, steps, warmup, world, sample_clocks=None, seed=0):
     import torch
     from gated_delta_rule_15_gb300 import dr, inputs
-    d = inputs.workload_inputs(w)
+    d = inputs.workload_inputs(w, seed=seed)
     g = {k: (None if t is None else t.cuda()) for k, t in d.items()}
     B, T, H = w.B, w.T, w.H
     out = torch.empty((B, T, H, w.dv), dtype=g["q"].dtype, device="cuda")
@@ -354,10 +366,10 @@ def run_native(args):
     hbm, tc = pk["hbm_gbs"], pk["bf16_tflops"]
 
     w = inputs.WORKLOADS[HEADLINE]
-    r = bench_chunk(w, args.steps, args.warmup, world, sample_clocks=local)
+    r = bench_chunk(w, args.steps, args.warmup, world, sample_clocks=local, seed=rank_seed(rank))
     ms = r["ms"]
     tokens = w.B * w.T
-    value = world * tokens / (ms * 1e-3)
+    value = job_throughput(tokens, ms, world)
     byts, flops = chunk_bytes(w), chunk_flops(w)
     ach_gbs = byts / (ms * 1e-3) / 1e9
     e2e_ms, h2d, d2h = bench_chunk_e2e(w, r["host_inputs"], max(2, args.steps // 2),
@@ -424,7 +436,7 @@ def run_native(args):
                      "tensor_tflops": flops / (ms * 1e-3) / 1e12,
                      "tensor_frac": flops / (ms * 1e-3) / 1e12 / tc},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(tokens, e2e_ms, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_call * args.steps,
