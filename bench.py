@@ -264,7 +264,7 @@ def bench_chunk(w, steps, warmup, world, sample_clocks=None, seed=0):
 def bench_chunk_e2e(w, d, steps, warmup, world):
     """Same metric through the C-ABI call for host buffers (dr_chunk_fwd_host): per step
     the H2D copies of the inputs from pinned memory, the forward and the D2H copies of out
-    and final_state, the batch in 8 pieces so that copies and kernels overlap."""
+    and final_state, the sequence in 4 time pieces so that copies and kernels overlap."""
     import torch
     from gated_delta_rule_15_gb300 import dr
     host = {k: (None if t is None else t.pin_memory()) for k, t in d.items()}

@@ -77,8 +77,8 @@ _lib.dr_chunk_bwd_workspace_bytes.argtypes = [ctypes.POINTER(ChunkDesc),
 _lib.dr_chunk_bwd_workspace_bytes.restype = ctypes.c_int
 _lib.dr_chunk_bwd.argtypes = [ctypes.POINTER(ChunkDesc)] + [_vp] * 15 + [ctypes.c_size_t, _vp]
 _lib.dr_chunk_bwd.restype = ctypes.c_int
-_lib.dr_chunk_fwd_host_dev_bytes.argtypes = [ctypes.POINTER(ChunkDesc), ctypes.c_int, ctypes.c_int,
-                                             ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
+_lib.dr_chunk_fwd_host_dev_bytes.argtypes = [ctypes.POINTER(ChunkDesc), ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_size_t)]
 _lib.dr_chunk_fwd_host_dev_bytes.restype = ctypes.c_int
 _lib.dr_chunk_fwd_host.argtypes = [ctypes.POINTER(ChunkDesc), ctypes.c_int] + [_vp] * 9 + \
     [ctypes.c_size_t, _vp]
@@ -337,12 +337,12 @@ class HostChunkRunner:
 
     Owns the device staging buffer and pinned host result buffers for one problem shape.
     Each call enqueues, behind the current stream, the host -> device copies of the inputs,
-    the forward and the device -> host copies of out and final_state, the batch split into
-    `pieces` groups of rows so that copies and kernels overlap; with `sync` it waits for
+    the forward and the device -> host copies of out and final_state, the sequence split
+    into `pieces` time ranges so that copies and kernels overlap; with `sync` it waits for
     the stream.  Returns the pinned host result tensors (reused across calls).  The host
     inputs should be pinned."""
 
-    def __init__(self, like: dict, *, chunk: int = 64, out_dtype=None, pieces: int = 8,
+    def __init__(self, like: dict, *, chunk: int = 64, out_dtype=None, pieces: int = 4,
                  device="cuda"):
         q, v = like["q"], like["v"]
         B, T, H, dk = q.shape
@@ -355,8 +355,7 @@ class HostChunkRunner:
         self.desc = chunk_desc(B, T, H, dk, dv, _DT[q.dtype], _DT[odt], gate, chunk)
         self.with_init = like.get("init_state") is not None
         n = ctypes.c_size_t(0)
-        rc = _lib.dr_chunk_fwd_host_dev_bytes(ctypes.byref(self.desc), pieces, int(self.with_init),
-                                              1, ctypes.byref(n))
+        rc = _lib.dr_chunk_fwd_host_dev_bytes(ctypes.byref(self.desc), pieces, ctypes.byref(n))
         if rc != DR_OK:
             raise DrError(rc, "dr_chunk_fwd_host_dev_bytes")
         self.dev = torch.empty(n.value + 256, dtype=torch.uint8, device=device)
@@ -385,7 +384,7 @@ class HostChunkRunner:
 
 
 def chunk_fwd_host(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
-                   out_dtype=None, pieces: int = 8):
+                   out_dtype=None, pieces: int = 4):
     """One-shot end-to-end call for host tensors (see HostChunkRunner)."""
     like = {"q": q, "k": k, "v": v, "log_alpha": log_alpha, "beta": beta,
             "init_state": init_state}

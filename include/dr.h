@@ -138,17 +138,18 @@ int dr_chunk_fwd(const dr_chunk_desc *desc,
  * out and final_state (NULL = not returned).  The call copies the inputs host -> device,
  * runs the forward and copies the results device -> host, all enqueued behind `stream`
  * (the results are in place once `stream` has completed; the host buffers must not be
- * touched before).  The batch is split into `pieces` groups of batch rows (1 .. 16, at most
- * B): one piece's copies overlap another's kernels and the two copy directions overlap each
- * other.  Host buffers should be page-locked (cudaHostAlloc / pinned) for the copies to be
- * asynchronous.  `dev` is a device buffer of at least dr_chunk_fwd_host_dev_bytes() bytes,
- * 256-byte aligned, holding the staging copies and the workspace; it must not be used by
- * other work until `stream` completes.  Streams and events are created for the call and
- * released behind its work.  Returns the statuses of dr_chunk_fwd (DR_ERR_WORKSPACE for a
- * missing or short `dev`); on DR_ERR_CUDA part of the work may have been enqueued.
+ * touched before).  The sequence is split into `pieces` time ranges of whole chunks (1 ..
+ * 16, at most the number of chunks), the state carried from one to the next on the device:
+ * one piece's kernels overlap the next piece's input copies and the previous piece's output
+ * copies (the two directions also overlap each other).  Host buffers should be page-locked
+ * (cudaHostAlloc / pinned) for the copies to be asynchronous.  `dev` is a device buffer of
+ * at least dr_chunk_fwd_host_dev_bytes() bytes, 256-byte aligned, holding the staging
+ * copies, the state and the workspace; it must not be used by other work until `stream`
+ * completes.  Streams and events are created for the call and released behind its work.
+ * Returns the statuses of dr_chunk_fwd (DR_ERR_WORKSPACE for a missing or short `dev`); on
+ * DR_ERR_CUDA part of the work may have been enqueued.
  */
-int dr_chunk_fwd_host_dev_bytes(const dr_chunk_desc *desc, int pieces, int with_init_state,
-                                int with_final_state, size_t *bytes);
+int dr_chunk_fwd_host_dev_bytes(const dr_chunk_desc *desc, int pieces, size_t *bytes);
 int dr_chunk_fwd_host(const dr_chunk_desc *desc, int pieces,
                       const void *q, const void *k, const void *v,
                       const float *log_alpha, const void *beta,

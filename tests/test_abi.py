@@ -179,10 +179,10 @@ def test_host_entry_point_checks(dr):
     lib = dr.lib()
     d = _desc(dr)
     n = ctypes.c_size_t(0)
-    assert lib.dr_chunk_fwd_host_dev_bytes(ctypes.byref(d), 4, 1, 1, ctypes.byref(n)) == 0
-    staging = 2 * 100 * 3 * (3 * 128 * 2 + 2 + 128 * 4 + 128 * 2) + 2 * 2 * 3 * 128 * 128 * 4
+    assert lib.dr_chunk_fwd_host_dev_bytes(ctypes.byref(d), 4, ctypes.byref(n)) == 0
+    staging = 2 * 100 * 3 * (3 * 128 * 2 + 2 + 128 * 4 + 128 * 2) + 2 * 3 * 128 * 128 * 4
     assert n.value >= staging + dr.workspace_bytes(d)
-    assert lib.dr_chunk_fwd_host_dev_bytes(ctypes.byref(d), 0, 1, 1, ctypes.byref(n)) == dr.DR_ERR_INVALID
+    assert lib.dr_chunk_fwd_host_dev_bytes(ctypes.byref(d), 0, ctypes.byref(n)) == dr.DR_ERR_INVALID
     fake = ctypes.c_void_p(1 << 20)
     call = lambda pieces, dev, nbytes: lib.dr_chunk_fwd_host(
         ctypes.byref(d), pieces, fake, fake, fake, fake, fake, None, fake, None, dev, nbytes, None)

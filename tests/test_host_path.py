@@ -1,10 +1,13 @@
-"""dr_chunk_fwd_host (host buffers in, host buffers out, the batch split into pieces whose
-copies and kernels overlap) against the device entry point: the same results bit for bit,
-since every (b, h) chain runs the same kernel code whichever piece holds it."""
+"""dr_chunk_fwd_host (host buffers in, host buffers out, the sequence split into time pieces
+whose copies and kernels overlap, the state carried on the device) against the device entry
+point.  The pieces are whole chunks and every kernel carries the state between chunks in
+fp32, as it is carried between pieces, so the results are the same bit for bit."""
 import pytest
 import torch
 
+import oracle
 from gated_delta_rule_15_gb300 import inputs
+from parity import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -27,7 +30,12 @@ def test_host_path_equals_device_path(dr, pieces, gate, dtype, dk, init):
     host = {k: (None if v is None else v.pin_memory()) for k, v in d.items()}
     out_h, fin_h = dr.HostChunkRunner(host, pieces=pieces)(host)
     assert dr.device_status() == 0
+    # whole chunks per piece, the state carried in fp32 as inside one call: the same bits
     assert torch.equal(out_h, out_d.cpu()) and torch.equal(fin_h, fin_d.cpu())
+    o_ref, f_ref = oracle.forward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                  d["init_state"])
+    assert_close(out_h, o_ref, dtype, "out")
+    assert_close(fin_h, f_ref, dtype, "final_state")
 
 
 def test_host_path_runs_repeatedly(dr):
