@@ -19,8 +19,9 @@
 //   and dq, dk, dg from the products holding q, k and g (chunk_grad_kernel, phase by phase);
 //   d log alpha_t = sum_{r >= t} dg_r, the last token's dg also taking the terms of gamma.
 //
-// Three steps after the CUDA-core forward has recomputed W, U, Q*G, Kd, P, gamma, T and the
-// state at every chunk's start (the checkpoints):
+// Three steps after the CUDA-core forward has recomputed W, U, Q*G, Kd, P, gamma and T, and
+// a forward pass (the tensor-core kernel where it serves the problem, else the CUDA-core
+// state pass) the state at every chunk's start (the checkpoints):
 //   chunk_dstate_kernel  one CTA per (b, h, 32 state columns), chunks in reverse: stores
 //                        dS_C of every chunk and returns dS0 of the first;
 //   chunk_grad_kernel    one CTA per (b, h, chunk), all chunks in parallel: every gradient
@@ -60,12 +61,19 @@ __device__ __forceinline__ float dotv(const float *a, const float *b, int n) {
 struct BwdWorkspace {
     ChunkWorkspace fw;
     float *T, *ckpt, *dsc;
+    float *tc;   // the tensor-core forward's workspace (checkpoint recompute)
 };
+
+// The tensor-core forward's own workspace (segments of few long chains) when it writes the
+// checkpoints, in floats.
+size_t tc_ws_floats(const ChunkProblem &p) {
+    return chunk_tc_supported(p) ? (chunk_tc_workspace_bytes(p) + 3) / 4 : 0;
+}
 
 size_t bwd_floats(const ChunkProblem &p) {
     const int64_t n = p.B * p.H * p.NC;
     return simt_workspace_floats(p.B, p.H, p.NC, p.C, p.dk, p.dv) +
-           (size_t)(n * ((int64_t)p.C * p.C + 2 * (int64_t)p.dk * p.dv));
+           (size_t)(n * ((int64_t)p.C * p.C + 2 * (int64_t)p.dk * p.dv)) + tc_ws_floats(p);
 }
 
 BwdWorkspace bwd_carve(void *base, const ChunkProblem &p) {
@@ -75,7 +83,8 @@ BwdWorkspace bwd_carve(void *base, const ChunkProblem &p) {
     float *f = (float *)base + simt_workspace_floats(p.B, p.H, p.NC, p.C, p.dk, p.dv);
     w.T = f;     f += n * p.C * p.C;
     w.ckpt = f;  f += n * (int64_t)p.dk * p.dv;
-    w.dsc = f;
+    w.dsc = f;   f += n * (int64_t)p.dk * p.dv;
+    w.tc = f;
     return w;
 }
 
@@ -582,17 +591,24 @@ int launch_bwd_t(const DStateArgs &da, const GradArgs &ga, int64_t nstate, int64
 
 size_t bwd_workspace_bytes(const ChunkProblem &p) { return sizeof(float) * bwd_floats(p); }
 
-int launch_chunk_bwd(const ChunkProblem &p, const BwdIo &g, void *workspace, cudaStream_t stream) {
+int launch_chunk_bwd(const ChunkProblem &p, const BwdIo &g, void *workspace, int *status_word,
+                     cudaStream_t stream) {
     const BwdWorkspace ws = bwd_carve(workspace, p);
     if (p.NC > 0) {
-        // the forward's per-chunk operands, T and the chunk-start states, without outputs
+        // the forward's per-chunk operands and T (CUDA cores), and the chunk-start states,
+        // without outputs: from the tensor-core forward where it serves the problem
         ChunkProblem f = p;
         f.out = nullptr;
         f.final_state = nullptr;
         f.fuse = 0;
         f.z = nullptr;
-        const int rc = launch_chunk_simt(f, ws.fw, stream, ws.T, ws.ckpt);
+        const bool tc = chunk_tc_supported(f);
+        int rc = launch_chunk_simt(f, ws.fw, stream, ws.T, tc ? nullptr : ws.ckpt, tc);
         if (rc != kOk) return rc;
+        if (tc) {
+            rc = launch_chunk_tc(f, ws.tc, status_word, stream, ws.ckpt);
+            if (rc != kOk) return rc;
+        }
     }
     DStateArgs da{g.d_out, g.d_final, g.d_init, ws, p.B, p.T, p.H, p.dv, p.C, p.NC};
     GradArgs ga{p.q, p.k, p.v, p.log_alpha, p.beta, g.d_out, ws, g.dq, g.dk, g.dv, g.d_log_alpha,

@@ -63,7 +63,7 @@ inline ChunkWorkspace simt_workspace_carve(void *base, int64_t B, int64_t H, int
 // CUDA-core path (chunk_simt.cu).  For the backward, `T_out` ([n][C][C]) and `ckpt`
 // ([n][dk][dv], the state at each chunk's start) are also written; `p.out` may then be NULL.
 int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStream_t stream,
-                      float *T_out = nullptr, float *ckpt = nullptr);
+                      float *T_out = nullptr, float *ckpt = nullptr, bool prep_only = false);
 // Backward of the chunk forward on the CUDA cores (chunk_bwd.cu): gradients of
 // <d_out, out> + <d_final, final_state>.  Workspace: bwd_workspace_bytes(p).
 struct BwdIo {
@@ -75,7 +75,8 @@ struct BwdIo {
     float *d_init;              // [B,H,dk,dv] or NULL (not returned)
 };
 size_t bwd_workspace_bytes(const ChunkProblem &p);
-int launch_chunk_bwd(const ChunkProblem &p, const BwdIo &g, void *workspace, cudaStream_t stream);
+int launch_chunk_bwd(const ChunkProblem &p, const BwdIo &g, void *workspace, int *status_word,
+                     cudaStream_t stream);
 
 // Fused tensor-core path (chunk_tc.cu): bf16 inputs, dk = dv = 128, C = 64, scalar gate or
 // none, T > 0.  Needs a workspace only when few long chains are split into segments
@@ -83,7 +84,10 @@ int launch_chunk_bwd(const ChunkProblem &p, const BwdIo &g, void *workspace, cud
 // (bounded waits record DR_ERR_TIMEOUT there).
 bool chunk_tc_supported(const ChunkProblem &p);
 size_t chunk_tc_workspace_bytes(const ChunkProblem &p);
-int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream);
+// With `ckpt` ([B*H][NC][dk][dv] fp32), it writes the state at every chunk's start instead of
+// the outputs (the backward's recompute).
+int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream,
+                    float *ckpt = nullptr);
 // Two-kernel tensor-core path for the per-channel gate (chunk_kda.cu): bf16 inputs,
 // dk = dv = 128, C = 64, T > 0.  Its workspace holds the per-chunk operands that the
 // prep kernel writes and the state kernel reads (chunk_kda_workspace_bytes).

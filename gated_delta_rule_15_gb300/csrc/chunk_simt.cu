@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(StateArgs a) {
 }
 
 template <int DK, typename Tin, typename Tout>
-int launch_simt_t(const PrepArgs &pa, const StateArgs &sa, cudaStream_t stream) {
+int launch_simt_t(const PrepArgs &pa, const StateArgs &sa, cudaStream_t stream, bool prep_only) {
     const size_t ps = prep_smem_bytes(DK), ss = state_smem_bytes(DK);
     if (cudaFuncSetAttribute(chunk_prep_kernel<DK, Tin>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps) != cudaSuccess)
@@ -520,14 +520,14 @@ int launch_simt_t(const PrepArgs &pa, const StateArgs &sa, cudaStream_t stream) 
     const int64_t nprep = pa.B * pa.H * pa.NC;
     const int64_t nstate = sa.B * sa.H * (sa.dv / kDvt);
     if (nprep > 0) chunk_prep_kernel<DK, Tin><<<(unsigned)nprep, kThreads, ps, stream>>>(pa);
-    chunk_state_kernel<DK, Tout><<<(unsigned)nstate, kThreads, ss, stream>>>(sa);
+    if (!prep_only) chunk_state_kernel<DK, Tout><<<(unsigned)nstate, kThreads, ss, stream>>>(sa);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
 }  // namespace
 
 int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStream_t stream,
-                      float *T_out, float *ckpt) {
+                      float *T_out, float *ckpt, bool prep_only) {
     PrepArgs pa{p.q, p.k, p.v, p.log_alpha, p.beta, p.B, p.T, p.H, p.dv, p.C, p.NC, p.gate, p.fuse, ws,
                 T_out};
     StateArgs sa{p.init_state, p.out, p.final_state, (p.fuse & kFuseGate) ? p.z : nullptr, p.in_bf16,
@@ -535,16 +535,16 @@ int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStrea
     using bf = __nv_bfloat16;
     const bool ib = p.in_bf16, ob = p.out_bf16;
     if (p.dk == 128) {
-        if (ib && ob) return launch_simt_t<128, bf, bf>(pa, sa, stream);
-        if (ib) return launch_simt_t<128, bf, float>(pa, sa, stream);
-        if (ob) return launch_simt_t<128, float, bf>(pa, sa, stream);
-        return launch_simt_t<128, float, float>(pa, sa, stream);
+        if (ib && ob) return launch_simt_t<128, bf, bf>(pa, sa, stream, prep_only);
+        if (ib) return launch_simt_t<128, bf, float>(pa, sa, stream, prep_only);
+        if (ob) return launch_simt_t<128, float, bf>(pa, sa, stream, prep_only);
+        return launch_simt_t<128, float, float>(pa, sa, stream, prep_only);
     }
     if (p.dk == 64) {
-        if (ib && ob) return launch_simt_t<64, bf, bf>(pa, sa, stream);
-        if (ib) return launch_simt_t<64, bf, float>(pa, sa, stream);
-        if (ob) return launch_simt_t<64, float, bf>(pa, sa, stream);
-        return launch_simt_t<64, float, float>(pa, sa, stream);
+        if (ib && ob) return launch_simt_t<64, bf, bf>(pa, sa, stream, prep_only);
+        if (ib) return launch_simt_t<64, bf, float>(pa, sa, stream, prep_only);
+        if (ob) return launch_simt_t<64, float, bf>(pa, sa, stream, prep_only);
+        return launch_simt_t<64, float, float>(pa, sa, stream, prep_only);
     }
     return kErrUnsupported;
 }

@@ -129,6 +129,9 @@ struct TcArgs {
     // from its true start state (ws_start) writing outputs.  [B*H][nseg][128][128] fp32.
     int role, nseg, seg_len;
     float *ws_phi, *ws_s0, *ws_start;
+    // (fused instantiation) the state at every chunk's start, [B*H][NC][dk][dv] fp32, for
+    // the backward's recompute: written by roles 0 and 2, which then write no outputs
+    float *ckpt;
 };
 
 // FUSED: the fused neighbours' code is compiled in (each still switched by a.fuse); the
@@ -155,7 +158,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     int bh = blockIdx.x, c_begin = 0, c_end = a.NC;
     const float *init_ptr = a.init_state ? a.init_state + (size_t)blockIdx.x * 16384 : nullptr;
     float *fin_ptr = a.final_state ? a.final_state + (size_t)blockIdx.x * 16384 : nullptr;
-    bool init_identity = false, zero_u = false, outputs = true;
+    bool init_identity = false, zero_u = false, outputs = !(FUSED && a.ckpt);
     if (a.role != 0) {
         const int idx = a.role == 1 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
         const int seg = idx % a.nseg;
@@ -166,7 +169,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         if (a.role == 1) {
             outputs = false;
             init_ptr = nullptr;
-            if (blockIdx.x & 1) {   // transition: S_0 = I, no value term
+            if (blockIdx.x & 1) {   // transition: S_0 = I, no value term (no checkpoints)
                 init_identity = true;
                 zero_u = true;
                 fin_ptr = a.ws_phi + slot;
@@ -643,6 +646,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 const int i0 = 64 * half + 32 * part;
                 tmem_ld32(tm + TM_S + i0, v);
                 tmem_wait_ld();
+                if (FUSED && a.ckpt && a.role != 1) {   // S[i][j] at this chunk's start
+                    float *ck = a.ckpt + ((size_t)bh * a.NC + c_begin + it) * 16384 + (size_t)i0 * 128 + row;
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) ck[(size_t)u * 128] = v[u];
+                }
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const float *f = v + 8 * q4;
@@ -912,8 +920,8 @@ template <typename Tout, int GATE>
 int launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
              const CUtensorMap &mo, const CUtensorMap &mz, const TcArgs &ta, unsigned grid,
              cudaStream_t stream) {
-    return ta.fuse ? launch_f<Tout, GATE, true>(mq, mk, mv, mo, mz, ta, grid, stream)
-                   : launch_f<Tout, GATE, false>(mq, mk, mv, mo, mz, ta, grid, stream);
+    return (ta.fuse || ta.ckpt) ? launch_f<Tout, GATE, true>(mq, mk, mv, mo, mz, ta, grid, stream)
+                                : launch_f<Tout, GATE, false>(mq, mk, mv, mo, mz, ta, grid, stream);
 }
 
 }  // namespace
@@ -945,16 +953,17 @@ size_t chunk_tc_workspace_bytes(const ChunkProblem &p) {
     return nseg > 1 ? (size_t)3 * p.B * p.H * nseg * 16384 * sizeof(float) : 0;
 }
 
-int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream) {
+int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream,
+                    float *ckpt) {
     CUtensorMap mq, mk, mv, mo, mz;
     const bool zgate = (p.fuse & kFuseGate) != 0;
     if (!make_map(&mq, p.q, p.B, p.T, p.H, false) || !make_map(&mk, p.k, p.B, p.T, p.H, false) ||
         !make_map(&mv, p.v, p.B, p.T, p.H, false) ||
-        !make_map(&mo, p.out, p.B, p.T, p.H, !p.out_bf16) ||
+        !make_map(&mo, p.out ? p.out : p.q, p.B, p.T, p.H, p.out ? !p.out_bf16 : false) ||
         !make_map(&mz, zgate ? p.z : p.q, p.B, p.T, p.H, false))   // (unused unless gated)
         return kErrCuda;
     TcArgs ta{p.log_alpha, (const __nv_bfloat16 *)p.beta, p.init_state, p.final_state,
-              status_word, (int)p.T, (int)p.H, p.NC, p.fuse, 0, 1, p.NC, nullptr, nullptr, nullptr};
+              status_word, (int)p.T, (int)p.H, p.NC, p.fuse, 0, 1, p.NC, nullptr, nullptr, nullptr, ckpt};
     auto launch = [&](const TcArgs &t, unsigned grid) {
         if (p.out_bf16)
             return p.gate == 1 ? launch_t<__nv_bfloat16, 1>(mq, mk, mv, mo, mz, t, grid, stream)

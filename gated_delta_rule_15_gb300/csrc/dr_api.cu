@@ -173,7 +173,9 @@ extern "C" int dr_chunk_bwd(const dr_chunk_desc *desc, const void *q, const void
     p.q = q; p.k = k; p.v = v; p.log_alpha = p.gate == DR_GATE_NONE ? nullptr : log_alpha;
     p.beta = beta; p.init_state = init_state; p.out = nullptr; p.final_state = nullptr;
     const BwdIo g{d_out, d_final_state, dq, dk, dv, d_log_alpha, d_beta, d_init_state};
-    return launch_chunk_bwd(p, g, workspace, (cudaStream_t)stream);
+    int *status = device_status_ptr();
+    if (!status) return kErrCuda;
+    return launch_chunk_bwd(p, g, workspace, status, (cudaStream_t)stream);
 }
 
 extern "C" int dr_chunk_fwd(const dr_chunk_desc *desc, const void *q, const void *k,
