@@ -34,6 +34,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kLdA = 65;   // padded row stride of [64][64] tiles
+constexpr int kLdP = 68;   // row stride of the reverse pass's P tile (16-byte rows)
 constexpr int kDvt = 32;   // state columns per CTA of the reverse pass
 constexpr int kSlice = 32; // rows of a [dk][dv] state matrix staged at a time
 constexpr int kGThreads = 512;   // per-chunk gradient kernel: 8 threads per token row
@@ -54,6 +55,19 @@ __device__ __forceinline__ float dotv(const float *a, const float *b, int n) {
         s1.z = fmaf(x1.z, y1.z, s1.z); s1.w = fmaf(x1.w, y1.w, s1.w);
     }
     return ((s0.x + s1.x) + (s0.y + s1.y)) + ((s0.z + s1.z) + (s0.w + s1.w));
+}
+
+// 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned)
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_all;" ::: "memory");
+}
+// Prefetch of `bytes` (a multiple of 16, 16-byte-aligned address) into L2, no completion
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Workspace of the backward, in floats, after the forward's slabs: T [n][C][C], checkpoints
@@ -98,12 +112,15 @@ struct DStateArgs {
 };
 
 size_t dstate_smem_bytes(int dk) {
-    return sizeof(float) * (size_t)(dk * kDvt + 3 * 64 * (dk + 4) + 2 * 64 * kDvt + 64 * kLdA + dk);
+    return sizeof(float) * (size_t)(dk * kDvt + 3 * 64 * (dk + 4) + 2 * 64 * kDvt + 64 * kLdP + dk);
 }
 
 // Reverse state-gradient pass: dS starts as d_final; for each chunk, last first, it is
 // stored as that chunk's dS_C, then  dE = P^T dO + Kd dS,  dS <- Diag(gamma) dS + (Q*G)^T dO
-// - W^T dE.  Column j of dS only meets column j of dO, so a CTA owns 32 columns.
+// - W^T dE.  Column j of dS only meets column j of dO, so a CTA owns 32 columns.  A chunk's
+// operands arrive by 16-byte asynchronous copies behind one wait, and the next chunk's are
+// prefetched into L2 meanwhile: one CTA fits an SM, so the chain of chunks is otherwise
+// paced by global-load latency.
 template <int DK, typename Tg>
 __global__ void __launch_bounds__(kThreads) chunk_dstate_kernel(DStateArgs a) {
     constexpr int LD = DK + 4;
@@ -114,8 +131,8 @@ __global__ void __launch_bounds__(kThreads) chunk_dstate_kernel(DStateArgs a) {
     float *sKd = sQg + 64 * LD;                     // [64][LD]
     float *sDO = sKd + 64 * LD;                     // [64][32]
     float *sDE = sDO + 64 * kDvt;                   // [64][32]
-    float *sP = sDE + 64 * kDvt;                    // [64][kLdA]
-    float *sGam = sP + 64 * kLdA;                   // [DK]
+    float *sP = sDE + 64 * kDvt;                    // [64][kLdP]
+    float *sGam = sP + 64 * kLdP;                   // [DK]
 
     const int tiles = a.dv / kDvt;
     const int jt = blockIdx.x % tiles;
@@ -137,63 +154,101 @@ __global__ void __launch_bounds__(kThreads) chunk_dstate_kernel(DStateArgs a) {
         const float *Qg = a.ws.fw.Qg + n * (int64_t)C * DK;
         const float *Kd = a.ws.fw.Kd + n * (int64_t)C * DK;
         const float *P = a.ws.fw.P + n * (int64_t)C * C;
+        const float *gam = a.ws.fw.gam + n * DK;
         __syncthreads();   // the previous chunk's readers are done
         for (int idx = tid; idx < C * (DK / 4); idx += kThreads) {
             const int r = idx / (DK / 4), c4 = 4 * (idx % (DK / 4));
-            *reinterpret_cast<float4 *>(sW + r * LD + c4) = load4(W + r * DK + c4);
-            *reinterpret_cast<float4 *>(sQg + r * LD + c4) = load4(Qg + r * DK + c4);
-            *reinterpret_cast<float4 *>(sKd + r * LD + c4) = load4(Kd + r * DK + c4);
+            cp_async16(sW + r * LD + c4, W + r * DK + c4);
+            cp_async16(sQg + r * LD + c4, Qg + r * DK + c4);
+            cp_async16(sKd + r * LD + c4, Kd + r * DK + c4);
         }
-        for (int idx = tid; idx < C * kDvt; idx += kThreads) {
-            const int r = idx / kDvt, jj = idx % kDvt;
-            sDO[idx] = r < Lc ? to_f32(dout[((b * a.T + t0 + r) * a.H + h) * dv + jt * kDvt + jj]) : 0.f;
+        for (int idx = tid; idx < C * (C / 4); idx += kThreads) {
+            const int r = idx / (C / 4), c4 = 4 * (idx % (C / 4));
+            cp_async16(sP + r * kLdP + c4, P + r * C + c4);
         }
-        for (int idx = tid; idx < C * C; idx += kThreads) sP[(idx / C) * kLdA + idx % C] = P[idx];
-        for (int i = tid; i < DK; i += kThreads) sGam[i] = a.ws.fw.gam[n * DK + i];
+        for (int idx = tid; idx < DK / 4; idx += kThreads) cp_async16(sGam + 4 * idx, gam + 4 * idx);
+        {   // dO's 32 columns: every load of this thread issued before its stores
+            float dov[8];   // C * kDvt / kThreads = C / 8 <= 8
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = tid + u * kThreads, r = idx / kDvt, jj = idx % kDvt;
+                dov[u] = (idx < C * kDvt && r < Lc)
+                             ? to_f32(dout[((b * a.T + t0 + r) * a.H + h) * dv + jt * kDvt + jj]) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (tid + u * kThreads < C * kDvt) sDO[tid + u * kThreads] = dov[u];
+        }
         for (int i = rg; i < DK; i += 8) a.ws.dsc[(n * DK + i) * dv + col] = sDS[i * kDvt + j];
+        cp_async_commit_wait_all();
         __syncthreads();
-        // dE = P^T dO + Kd dS  (rows r = rg + 8m: eight independent sums per thread)
+        if (c > 0) {   // the next chunk's operands into L2 while this one computes
+            if (tid == 0) {
+                prefetch_l2(W - C * DK, (uint32_t)(C * DK * 4));
+                prefetch_l2(Qg - C * DK, (uint32_t)(C * DK * 4));
+                prefetch_l2(Kd - C * DK, (uint32_t)(C * DK * 4));
+                prefetch_l2(P - C * C, (uint32_t)(C * C * 4));
+            } else if (tid > 32 && tid <= 32 + C && t0 - C + (tid - 33) < a.T) {
+                const int r = tid - 33;   // dO rows of the next chunk (this CTA's 64 bytes)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(dout + ((b * a.T + t0 - C + r) * a.H + h) * dv +
+                                                               jt * kDvt));
+            }
+        }
+        // dE = P^T dO + Kd dS: warp rg owns rows 8 rg .. 8 rg + 7 (eight independent sums
+        // per thread), so that one float4 broadcast load serves four rows.  P is lower
+        // triangular (zeros stored above the diagonal): rows r >= 8 rg need s >= 8 rg only.
         {
+            const int r0 = 8 * rg;
             float e[8];
 #pragma unroll
             for (int m = 0; m < 8; ++m) e[m] = 0.f;
-            for (int s = 0; s < C; ++s) {
-                const float d = sDO[s * kDvt + j];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int r = rg + 8 * m;
-                    if (r < C && s >= r) e[m] = fmaf(sP[s * kLdA + r], d, e[m]);
+            if (r0 < C) {
+                for (int s = r0; s < C; ++s) {
+                    const float d = sDO[s * kDvt + j];
+                    const float4 p0 = *reinterpret_cast<const float4 *>(sP + s * kLdP + r0);
+                    const float4 p1 = *reinterpret_cast<const float4 *>(sP + s * kLdP + r0 + 4);
+                    e[0] = fmaf(p0.x, d, e[0]); e[1] = fmaf(p0.y, d, e[1]);
+                    e[2] = fmaf(p0.z, d, e[2]); e[3] = fmaf(p0.w, d, e[3]);
+                    e[4] = fmaf(p1.x, d, e[4]); e[5] = fmaf(p1.y, d, e[5]);
+                    e[6] = fmaf(p1.z, d, e[6]); e[7] = fmaf(p1.w, d, e[7]);
                 }
-            }
-            for (int i = 0; i < DK; ++i) {
-                const float d = sDS[i * kDvt + j];
+                for (int i = 0; i < DK; i += 4) {
+                    const float d0 = sDS[i * kDvt + j], d1 = sDS[(i + 1) * kDvt + j];
+                    const float d2 = sDS[(i + 2) * kDvt + j], d3 = sDS[(i + 3) * kDvt + j];
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int r = rg + 8 * m;
-                    if (r < C) e[m] = fmaf(sKd[r * LD + i], d, e[m]);
+                    for (int m = 0; m < 8; ++m) {
+                        const float4 kd = *reinterpret_cast<const float4 *>(sKd + (r0 + m) * LD + i);
+                        e[m] = fmaf(kd.x, d0, fmaf(kd.y, d1, fmaf(kd.z, d2, fmaf(kd.w, d3, e[m]))));
+                    }
                 }
-            }
 #pragma unroll
-            for (int m = 0; m < 8; ++m)
-                if (rg + 8 * m < C) sDE[(rg + 8 * m) * kDvt + j] = e[m];
+                for (int m = 0; m < 8; ++m)
+                    if (r0 + m < C) sDE[(r0 + m) * kDvt + j] = e[m];
+            }
         }
         __syncthreads();
-        // dS <- Diag(gamma) dS + (Q*G)^T dO - W^T dE  (rows i = rg + 8m; own entries only)
+        // dS <- Diag(gamma) dS + (Q*G)^T dO - W^T dE: warp rg owns the NR contiguous rows
+        // i = NR rg .. NR rg + NR - 1 of column j (own entries only), float4 broadcasts
         {
             constexpr int NR = DK / 8;
+            const int i0 = NR * rg;
             float acc[NR];
 #pragma unroll
-            for (int m = 0; m < NR; ++m) acc[m] = sGam[rg + 8 * m] * sDS[(rg + 8 * m) * kDvt + j];
+            for (int m = 0; m < NR; ++m) acc[m] = sGam[i0 + m] * sDS[(i0 + m) * kDvt + j];
             for (int r = 0; r < C; ++r) {
                 const float d = sDO[r * kDvt + j], de = sDE[r * kDvt + j];
 #pragma unroll
-                for (int m = 0; m < NR; ++m) {
-                    const int i = rg + 8 * m;
-                    acc[m] = fmaf(sQg[r * LD + i], d, fmaf(-sW[r * LD + i], de, acc[m]));
+                for (int q = 0; q < NR; q += 4) {
+                    const float4 qg = *reinterpret_cast<const float4 *>(sQg + r * LD + i0 + q);
+                    const float4 w = *reinterpret_cast<const float4 *>(sW + r * LD + i0 + q);
+                    acc[q] = fmaf(qg.x, d, fmaf(-w.x, de, acc[q]));
+                    acc[q + 1] = fmaf(qg.y, d, fmaf(-w.y, de, acc[q + 1]));
+                    acc[q + 2] = fmaf(qg.z, d, fmaf(-w.z, de, acc[q + 2]));
+                    acc[q + 3] = fmaf(qg.w, d, fmaf(-w.w, de, acc[q + 3]));
                 }
             }
 #pragma unroll
-            for (int m = 0; m < NR; ++m) sDS[(rg + 8 * m) * kDvt + j] = acc[m];
+            for (int m = 0; m < NR; ++m) sDS[(i0 + m) * kDvt + j] = acc[m];
         }
     }
     if (a.d_init) {
