@@ -28,6 +28,7 @@
 //                        of the chunk's tokens.
 #include "chunk_layout.h"
 #include "common.cuh"
+#include "tc_common.cuh"
 
 namespace dr {
 namespace {
@@ -39,23 +40,7 @@ constexpr int kDvt = 32;   // state columns per CTA of the reverse pass
 constexpr int kSlice = 32; // rows of a [dk][dv] state matrix staged at a time
 constexpr int kGThreads = 512;   // per-chunk gradient kernel: 8 threads per token row
 constexpr int kParts = 8;
-
-// a . b over n floats (n a multiple of 8, both 16-byte aligned, shared memory): float4 loads
-// into four independent partial sums
-__device__ __forceinline__ float dotv(const float *a, const float *b, int n) {
-    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-    for (int j = 0; j < n; j += 8) {
-        const float4 x0 = *reinterpret_cast<const float4 *>(a + j);
-        const float4 y0 = *reinterpret_cast<const float4 *>(b + j);
-        const float4 x1 = *reinterpret_cast<const float4 *>(a + j + 4);
-        const float4 y1 = *reinterpret_cast<const float4 *>(b + j + 4);
-        s0.x = fmaf(x0.x, y0.x, s0.x); s0.y = fmaf(x0.y, y0.y, s0.y);
-        s0.z = fmaf(x0.z, y0.z, s0.z); s0.w = fmaf(x0.w, y0.w, s0.w);
-        s1.x = fmaf(x1.x, y1.x, s1.x); s1.y = fmaf(x1.y, y1.y, s1.y);
-        s1.z = fmaf(x1.z, y1.z, s1.z); s1.w = fmaf(x1.w, y1.w, s1.w);
-    }
-    return ((s0.x + s1.x) + (s0.y + s1.y)) + ((s0.z + s1.z) + (s0.w + s1.w));
-}
+constexpr int kLdM = kSlice + 4;   // row stride of the gradient kernel's product slices
 
 // 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned)
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
@@ -68,6 +53,47 @@ __device__ __forceinline__ void cp_async_commit_wait_all() {
 // Prefetch of `bytes` (a multiple of 16, 16-byte-aligned address) into L2, no completion
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// out(r, n) = sum_{k < K} A[r][k] B[n][k] for r < R, n < N (R, N multiples of 16 and 8, K of
+// 8): fp32 rows in shared memory, A row r at A + r lda, B row n at B + n ldb.  Each warp of
+// the CTA takes 16 x 8 tiles (the mma.sync fragment shapes) in turn; a tile skipped by
+// `skip(r0, n0)` is not computed.  Three TF32 products of split operands (x = hi + lo, hi
+// and lo TF32: hi.hi + hi.lo + lo.hi) give about fp32 accuracy, the dropped lo.lo term
+// being ~2^-22 of the product.  st(r, n, v) receives each element once.
+template <class FSkip, class FS>
+__device__ __forceinline__ void rows_dot_rows(const float *A, int lda, const float *B, int ldb, int R, int N,
+                                              int K, int warp, int nwarps, int lane, FSkip skip, FS st) {
+    const int g = lane >> 2, t4 = lane & 3;
+    const int nrb = R / 16, ntiles = nrb * (N / 8);
+    for (int tile = warp; tile < ntiles; tile += nwarps) {
+        const int r0 = 16 * (tile % nrb), n0 = 8 * (tile / nrb);
+        if (skip(r0, n0)) continue;
+        const float *a = A + (r0 + g) * lda + t4, *b = B + (n0 + g) * ldb + t4;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k0 = 0; k0 < K; k0 += 8) {
+            const float av[4] = {a[k0], a[8 * lda + k0], a[k0 + 4], a[8 * lda + k0 + 4]};
+            const float bv[2] = {b[k0], b[k0 + 4]};
+            uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                ah[u] = tc::to_tf32(av[u]);
+                al[u] = tc::to_tf32(av[u] - __uint_as_float(ah[u]));
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                bh[u] = tc::to_tf32(bv[u]);
+                bl[u] = tc::to_tf32(bv[u] - __uint_as_float(bh[u]));
+            }
+            tc::mma_tf32_16x8x8(acc, al, bh[0], bh[1]);
+            tc::mma_tf32_16x8x8(acc, ah, bl[0], bl[1]);
+            tc::mma_tf32_16x8x8(acc, ah, bh[0], bh[1]);
+        }
+        st(r0 + g, n0 + 2 * t4, acc[0]);
+        st(r0 + g, n0 + 2 * t4 + 1, acc[1]);
+        st(r0 + g + 8, n0 + 2 * t4, acc[2]);
+        st(r0 + g + 8, n0 + 2 * t4 + 1, acc[3]);
+    }
 }
 
 // Workspace of the backward, in floats, after the forward's slabs: T [n][C][C], checkpoints
@@ -273,7 +299,7 @@ struct GradArgs {
 size_t grad_smem_bytes(int dk, int dv) {
     const int ldw = (dk > dv ? dk : dv) + 4;
     return sizeof(float) * (size_t)(3 * 64 * (dk + 8) + 2 * 64 * ldw + 2 * 64 * kLdA + 64 + dk + 64 +
-                                    kSlice * (dv + 4));
+                                    kSlice * (dv + 4) + 64 * kLdM);
 }
 
 // Every gradient of one chunk's tokens.  Thread (row r = tid / 8, part = tid % 8) owns key
@@ -305,6 +331,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     float *sDgC = sB + 64;                         // [DK] d g of the last token (gamma terms)
     float *sRed = sDgC + DK;                       // [64] row sums
     float *sS = sRed + 64;                         // [kSlice][dv + 4] rows of S0 or dS_C
+    float *sM = sS + kSlice * (dv + 4);            // [64][kLdM] a product against a staged slice
 
     const Tin *q = (const Tin *)a.q, *k = (const Tin *)a.k, *v = (const Tin *)a.v;
     const Tin *beta = (const Tin *)a.beta;
@@ -325,6 +352,16 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     const int r = tid / kParts, part = tid % kParts;
     const bool row_ok = r < C;
     const int lds = dv + 4;
+    const int warp = tid >> 5, lane = tid & 31;
+    constexpr int kWarps = kGThreads / 32;
+    auto none = [](int, int) { return false; };
+    // sM[r][n] = X_r . S_n over the staged slice (rows r < C of X, row stride ldx); ends
+    // with a barrier
+    auto slice_products = [&](const float *X, int ldx) {
+        rows_dot_rows(X, ldx, sS, lds, C, kSlice, dv, warp, kWarps, lane, none,
+                      [&](int rr, int nn, float v) { sM[rr * kLdM + nn] = v; });
+        __syncthreads();
+    };
     // rows i0 .. i0 + kSlice - 1 of a [DK][dv] matrix into sS (all threads; barriers around)
     auto stage = [&](const float *M, int i0) {
         __syncthreads();
@@ -378,6 +415,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     for (int m = 0; m < NJ; ++m) x[m] = (row_ok && part + kParts * m < dv) ? Un[r * dv + part + kParts * m] : 0.f;
     for (int i0 = 0; i0 < DK; i0 += kSlice) {
         stage(S0, i0);
+        slice_products(sX, ldw);   // (dO S0^T) over the slice
         if (!row_ok) continue;
         for (int ii = 0; ii < kSlice; ++ii) {
             const float w = Wn[r * DK + i0 + ii];
@@ -389,7 +427,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         for (int m = 0; m < NI; ++m) {
             const int i = part + kParts * m;
             if (i < i0 || i >= i0 + kSlice) continue;
-            const float acc = dotv(sX + r * ldw, sS + (i - i0) * lds, dv);
+            const float acc = sM[r * kLdM + i - i0];
             const float e = __expf(sG[r * LDK + i]);
             aq[m] = fmaf(e, acc, aq[m]);
             ag[m] = fmaf(sQ[r * LDK + i] * e, acc, ag[m]);
@@ -423,9 +461,13 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         }
     }
     __syncthreads();
-    if (row_ok)
-        for (int s = part; s < C; s += kParts)
-            sP[r * kLdA + s] = s <= r ? dotv(sX + r * ldw, sE + s * ldw, dv) : 0.f;
+    rows_dot_rows(sX, ldw, sE, ldw, C, C, dv, warp, kWarps, lane,
+                  [](int r0, int n0) { return n0 > r0 + 15; },   // tiles above the diagonal
+                  [&](int rr, int nn, float v) { sP[rr * kLdA + nn] = nn <= rr ? v : 0.f; });
+    for (int idx = tid; idx < C * C; idx += kGThreads) {          // their zeros
+        const int rr = idx / C, nn = idx % C;
+        if ((nn & ~7) > (rr | 15)) sP[rr * kLdA + nn] = 0.f;
+    }
     __syncthreads();
     if (row_ok)
 #pragma unroll
@@ -453,9 +495,14 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     // ---- 4. dA over T; dv; db part 1 (with (K*G) S0); (dR S0^T) -> dk, dg; S0 by slices
     const float br = row_ok ? sB[r] : 0.f;
     float db = 0.f;
+    rows_dot_rows(sX, ldw, sE, ldw, C, C, dv, warp, kWarps, lane,
+                  [](int r0, int n0) { return n0 > r0 + 15; },
+                  [&](int rr, int nn, float v) { sT[rr * kLdA + nn] = nn < rr ? -v : 0.f; });
+    for (int idx = tid; idx < C * C; idx += kGThreads) {
+        const int rr = idx / C, nn = idx % C;
+        if ((nn & ~7) > (rr | 15)) sT[rr * kLdA + nn] = 0.f;
+    }
     if (row_ok) {
-        for (int s = part; s < C; s += kParts)
-            sT[r * kLdA + s] = s < r ? -dotv(sX + r * ldw, sE + s * ldw, dv) : 0.f;
         if (r < Lc) {
             Tin *gv = (Tin *)a.dv;
             for (int j = part; j < dv; j += kParts) gv[tok(r) * dv + j] = from_f32<Tin>(br * sX[r * ldw + j]);
@@ -465,6 +512,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     for (int m = 0; m < NJ; ++m) x[m] = 0.f;   // ((K*G) S0)_rj
     for (int i0 = 0; i0 < DK; i0 += kSlice) {
         stage(S0, i0);
+        slice_products(sX, ldw);   // (dR S0^T) over the slice
         if (!row_ok) continue;
         for (int ii = 0; ii < kSlice; ++ii) {
             const float kg = sK[r * LDK + i0 + ii] * __expf(sG[r * LDK + i0 + ii]);
@@ -476,7 +524,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         for (int m = 0; m < NI; ++m) {
             const int i = part + kParts * m;
             if (i < i0 || i >= i0 + kSlice) continue;
-            const float acc = dotv(sX + r * ldw, sS + (i - i0) * lds, dv);
+            const float acc = sM[r * kLdM + i - i0];
             const float w = br * __expf(sG[r * LDK + i]) * acc;
             ak[m] -= w;
             ag[m] = fmaf(-w, sK[r * LDK + i], ag[m]);
@@ -496,12 +544,13 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     //          staging barrier) for the last token's dg; dS_C by slices
     for (int i0 = 0; i0 < DK; i0 += kSlice) {
         stage(dSC, i0);
+        slice_products(sE, ldw);   // (E dS_C^T) over the slice
         if (!row_ok) continue;
 #pragma unroll
         for (int m = 0; m < NI; ++m) {
             const int i = part + kParts * m;
             if (i < i0 || i >= i0 + kSlice) continue;
-            const float y = dotv(sE + r * ldw, sS + (i - i0) * lds, dv);
+            const float y = sM[r * kLdM + i - i0];
             const float f = __expf(sG[(C - 1) * LDK + i] - sG[r * LDK + i]);
             const float z = y * sK[r * LDK + i] * f;
             ak[m] = fmaf(y, f, ak[m]);
