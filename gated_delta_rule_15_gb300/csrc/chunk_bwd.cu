@@ -96,6 +96,38 @@ __device__ __forceinline__ void rows_dot_rows(const float *A, int lda, const flo
     }
 }
 
+// acc[t] (t < nt: the 16 x 8 C fragments at rows r0 .. r0 + 15, columns n0 + 8t ..) +=
+// sum_{k < K} A(r, k) B(k, n), K a multiple of 8; A(r, k) and B(k, n) return fp32 elements.
+// The same split-TF32 products as rows_dot_rows; one warp.
+template <class FA, class FB>
+__device__ __forceinline__ void rows_times_cols(float (&acc)[4][4], int nt, FA A, FB B, int r0, int n0, int K,
+                                                int g, int t4) {
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        const float av[4] = {A(r0 + g, k0 + t4), A(r0 + g + 8, k0 + t4), A(r0 + g, k0 + t4 + 4),
+                             A(r0 + g + 8, k0 + t4 + 4)};
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            ah[u] = tc::to_tf32(av[u]);
+            al[u] = tc::to_tf32(av[u] - __uint_as_float(ah[u]));
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            if (t >= nt) break;
+            const float bv[2] = {B(k0 + t4, n0 + 8 * t + g), B(k0 + t4 + 4, n0 + 8 * t + g)};
+            uint32_t bh[2], bl[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                bh[u] = tc::to_tf32(bv[u]);
+                bl[u] = tc::to_tf32(bv[u] - __uint_as_float(bh[u]));
+            }
+            tc::mma_tf32_16x8x8(acc[t], al, bh[0], bh[1]);
+            tc::mma_tf32_16x8x8(acc[t], ah, bl[0], bl[1]);
+            tc::mma_tf32_16x8x8(acc[t], ah, bh[0], bh[1]);
+        }
+    }
+}
+
 // Workspace of the backward, in floats, after the forward's slabs: T [n][C][C], checkpoints
 // [n][dk][dv], dS_C [n][dk][dv].
 struct BwdWorkspace {
@@ -357,6 +389,21 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     auto none = [](int, int) { return false; };
     // sM[r][n] = X_r . S_n over the staged slice (rows r < C of X, row stride ldx); ends
     // with a barrier
+    // [C][dv] products (E, dE, dR, (K*G) S0): warp w owns rows 16 (w % 4) .. + 15 and the
+    // dv / 4 columns from (w / 4) dv / 4, as nt tiles of 8; the fragment element (u of tile
+    // t) is row orow(u), column ocol(t, u)
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int orb = 16 * (warp & 3), ocn = (warp >> 2) * (dv / 4), ont = dv / 32;
+    const bool own = orb < C;
+    auto orow = [&](int u) { return orb + g8 + 8 * (u >> 1); };
+    auto ocol = [&](int t, int u) { return ocn + 8 * t + 2 * t4 + (u & 1); };
+    float acc[4][4];
+    auto acc_zero = [&]() {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc[t][u] = 0.f;
+    };
     auto slice_products = [&](const float *X, int ldx) {
         rows_dot_rows(X, ldx, sS, lds, C, kSlice, dv, warp, kWarps, lane, none,
                       [&](int rr, int nn, float v) { sM[rr * kLdM + nn] = v; });
@@ -393,6 +440,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         sX[rr * ldw + j] = rr < Lc ? to_f32(dout[tok(rr) * dv + j]) : 0.f;
     }
     for (int i = tid; i < DK; i += kGThreads) sDgC[i] = 0.f;
+    for (int rr = tid; rr < 64; rr += kGThreads) sRed[rr] = 0.f;   // db terms of phase 4
     __syncthreads();
     for (int i = tid; i < DK; i += kGThreads) {   // cumulative log decay down each channel
         float acc = 0.f;
@@ -407,22 +455,16 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
 #pragma unroll
     for (int m = 0; m < NI; ++m) { aq[m] = 0.f; ak[m] = 0.f; ag[m] = 0.f; }
 
-    // ---- 1. E = U - W S0 (row r, columns part + 8m); dq, dg from (dO S0^T)_ri; S0 staged
-    //         by slices of kSlice rows
-    constexpr int NJ = 128 / kParts;   // value columns per thread (dv <= 128)
-    float x[NJ];
-#pragma unroll
-    for (int m = 0; m < NJ; ++m) x[m] = (row_ok && part + kParts * m < dv) ? Un[r * dv + part + kParts * m] : 0.f;
+    // ---- 1. E = U - W S0 (tiles, W read from the workspace); dq, dg from (dO S0^T)_ri;
+    //         S0 staged by slices of kSlice rows
+    acc_zero();
     for (int i0 = 0; i0 < DK; i0 += kSlice) {
         stage(S0, i0);
         slice_products(sX, ldw);   // (dO S0^T) over the slice
+        if (own)
+            rows_times_cols(acc, ont, [&](int rr, int kk) { return Wn[rr * DK + i0 + kk]; },
+                            [&](int kk, int nn) { return sS[kk * lds + nn]; }, orb, ocn, kSlice, g8, t4);
         if (!row_ok) continue;
-        for (int ii = 0; ii < kSlice; ++ii) {
-            const float w = Wn[r * DK + i0 + ii];
-#pragma unroll
-            for (int m = 0; m < NJ; ++m)
-                if (part + kParts * m < dv) x[m] = fmaf(-w, sS[ii * lds + part + kParts * m], x[m]);
-        }
 #pragma unroll
         for (int m = 0; m < NI; ++m) {
             const int i = part + kParts * m;
@@ -433,32 +475,25 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
             ag[m] = fmaf(sQ[r * LDK + i] * e, acc, ag[m]);
         }
     }
-    if (row_ok)
+    if (own)
 #pragma unroll
-        for (int m = 0; m < NJ; ++m)
-            if (part + kParts * m < dv) sE[r * ldw + part + kParts * m] = x[m];
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (t < ont) sE[orow(u) * ldw + ocol(t, u)] = Un[orow(u) * dv + ocol(t, u)] - acc[t][u];
     __syncthreads();
 
-    // ---- 2. dE = P^T dO + Kd dS_C (registers; dS_C by slices), dP = tril(dO E^T) over P,
-    //         then dE over dO
-#pragma unroll
-    for (int m = 0; m < NJ; ++m) x[m] = 0.f;
-    if (row_ok)
-        for (int s = r; s < C; ++s) {
-            const float pv = sP[s * kLdA + r];
-#pragma unroll
-            for (int m = 0; m < NJ; ++m)
-                if (part + kParts * m < dv) x[m] = fmaf(pv, sX[s * ldw + part + kParts * m], x[m]);
-        }
+    // ---- 2. dE = P^T dO + Kd dS_C (tiles; P lower triangular, dS_C by slices), dP =
+    //         tril(dO E^T) over P, then dE over dO
+    acc_zero();
+    if (own)
+        rows_times_cols(acc, ont, [&](int rr, int kk) { return sP[kk * kLdA + rr]; },
+                        [&](int kk, int nn) { return sX[kk * ldw + nn]; }, orb, ocn, C, g8, t4);
     for (int i0 = 0; i0 < DK; i0 += kSlice) {
         stage(dSC, i0);
-        if (!row_ok) continue;
-        for (int ii = 0; ii < kSlice; ++ii) {
-            const float kd = Kdn[r * DK + i0 + ii];
-#pragma unroll
-            for (int m = 0; m < NJ; ++m)
-                if (part + kParts * m < dv) x[m] = fmaf(kd, sS[ii * lds + part + kParts * m], x[m]);
-        }
+        if (own)
+            rows_times_cols(acc, ont, [&](int rr, int kk) { return Kdn[rr * DK + i0 + kk]; },
+                            [&](int kk, int nn) { return sS[kk * lds + nn]; }, orb, ocn, kSlice, g8, t4);
     }
     __syncthreads();
     rows_dot_rows(sX, ldw, sE, ldw, C, C, dv, warp, kWarps, lane,
@@ -469,27 +504,24 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         if ((nn & ~7) > (rr | 15)) sP[rr * kLdA + nn] = 0.f;
     }
     __syncthreads();
-    if (row_ok)
+    auto acc_to_x = [&]() {   // the tiles over sX (rows < C)
+        if (own)
 #pragma unroll
-        for (int m = 0; m < NJ; ++m)
-            if (part + kParts * m < dv) sX[r * ldw + part + kParts * m] = x[m];
+            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (t < ont) sX[orow(u) * ldw + ocol(t, u)] = acc[t][u];
+    };
+    acc_to_x();
     __syncthreads();
 
-    // ---- 3. dR = T^T dE, over dE
-#pragma unroll
-    for (int m = 0; m < NJ; ++m) x[m] = 0.f;
-    if (row_ok)
-        for (int s = r; s < C; ++s) {
-            const float tv = sT[s * kLdA + r];
-#pragma unroll
-            for (int m = 0; m < NJ; ++m)
-                if (part + kParts * m < dv) x[m] = fmaf(tv, sX[s * ldw + part + kParts * m], x[m]);
-        }
+    // ---- 3. dR = T^T dE (T lower triangular), over dE
+    acc_zero();
+    if (own)
+        rows_times_cols(acc, ont, [&](int rr, int kk) { return sT[kk * kLdA + rr]; },
+                        [&](int kk, int nn) { return sX[kk * ldw + nn]; }, orb, ocn, C, g8, t4);
     __syncthreads();
-    if (row_ok)
-#pragma unroll
-        for (int m = 0; m < NJ; ++m)
-            if (part + kParts * m < dv) sX[r * ldw + part + kParts * m] = x[m];
+    acc_to_x();
     __syncthreads();
 
     // ---- 4. dA over T; dv; db part 1 (with (K*G) S0); (dR S0^T) -> dk, dg; S0 by slices
@@ -508,18 +540,15 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
             for (int j = part; j < dv; j += kParts) gv[tok(r) * dv + j] = from_f32<Tin>(br * sX[r * ldw + j]);
         }
     }
-#pragma unroll
-    for (int m = 0; m < NJ; ++m) x[m] = 0.f;   // ((K*G) S0)_rj
+    acc_zero();   // ((K*G) S0)_rj
     for (int i0 = 0; i0 < DK; i0 += kSlice) {
         stage(S0, i0);
         slice_products(sX, ldw);   // (dR S0^T) over the slice
+        if (own)
+            rows_times_cols(acc, ont,
+                            [&](int rr, int kk) { return sK[rr * LDK + i0 + kk] * __expf(sG[rr * LDK + i0 + kk]); },
+                            [&](int kk, int nn) { return sS[kk * lds + nn]; }, orb, ocn, kSlice, g8, t4);
         if (!row_ok) continue;
-        for (int ii = 0; ii < kSlice; ++ii) {
-            const float kg = sK[r * LDK + i0 + ii] * __expf(sG[r * LDK + i0 + ii]);
-#pragma unroll
-            for (int m = 0; m < NJ; ++m)
-                if (part + kParts * m < dv) x[m] = fmaf(kg, sS[ii * lds + part + kParts * m], x[m]);
-        }
 #pragma unroll
         for (int m = 0; m < NI; ++m) {
             const int i = part + kParts * m;
@@ -530,15 +559,28 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
             ag[m] = fmaf(-w, sK[r * LDK + i], ag[m]);
         }
     }
-    if (row_ok)
+    if (own) {   // db_r, part 1: sum_j dR_rj (v_rj - ((K*G) S0)_rj), into sRed[r]
+        float d2[2] = {0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < NJ; ++m) {
-            const int j = part + kParts * m;
-            if (j < dv) {
-                const float u0 = (r < Lc ? to_f32(v[tok(r) * dv + j]) : 0.f) - x[m];
-                db = fmaf(sX[r * ldw + j], u0, db);
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int rr = orow(u), j = ocol(t, u);
+                if (t < ont) {
+                    const float u0 = (rr < Lc ? to_f32(v[tok(rr) * dv + j]) : 0.f) - acc[t][u];
+                    d2[u >> 1] = fmaf(sX[rr * ldw + j], u0, d2[u >> 1]);
+                }
             }
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            d2[h2] += __shfl_xor_sync(0xffffffffu, d2[h2], 1);
+            d2[h2] += __shfl_xor_sync(0xffffffffu, d2[h2], 2);
         }
+        if (t4 == 0) {
+            atomicAdd(&sRed[orb + g8], d2[0]);
+            atomicAdd(&sRed[orb + g8 + 8], d2[1]);
+        }
+    }
 
     // ---- 4b. Y = E dS_C^T -> dk, dg; Y k exp(g_C - g) -> sX (dR is dead after the first
     //          staging barrier) for the last token's dg; dS_C by slices
@@ -559,12 +601,23 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         }
     }
     __syncthreads();
-    for (int i = tid; i < DK; i += kGThreads) {   // d g_C,i = sum_r z_ri + sum_j dS_C,ij gamma_i S0_ij
+    {   // d g_C,i = sum_r z_ri + gamma_i sum_j dS_C,ij S0_ij: four threads per key channel
+        const int i = tid >> 2, q4 = tid & 3;
         float acc = 0.f;
-        for (int rr = 0; rr < C; ++rr) acc += sX[rr * ldw + i];
-        const float gi = __expf(sG[(C - 1) * LDK + i]);
-        for (int j = 0; j < dv; ++j) acc = fmaf(dSC[i * dv + j] * gi, S0[i * dv + j], acc);
-        sDgC[i] = acc;
+        if (i < DK) {
+            for (int rr = q4; rr < C; rr += 4) acc += sX[rr * ldw + i];
+            const float4 *a4 = reinterpret_cast<const float4 *>(dSC + i * dv);
+            const float4 *b4 = reinterpret_cast<const float4 *>(S0 + i * dv);
+            float sd = 0.f;
+            for (int j4 = q4; j4 < dv / 4; j4 += 4) {
+                const float4 x = a4[j4], y = b4[j4];
+                sd = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, sd))));
+            }
+            acc = fmaf(sd, __expf(sG[(C - 1) * LDK + i]), acc);
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        if (i < DK && q4 == 0) sDgC[i] = acc;
     }
 
     // ---- 5. pair products: P_rs = sum_i q_ri k_si D_rs,i (s <= r) and A_rs = b_r sum_i
@@ -631,6 +684,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         }
     }
     db += db2;
+    if (row_ok && part == 0) db += sRed[r];   // complete since the staging barriers of 4b
     db += __shfl_xor_sync(0xffffffffu, db, 1);
     db += __shfl_xor_sync(0xffffffffu, db, 2);
     db += __shfl_xor_sync(0xffffffffu, db, 4);
