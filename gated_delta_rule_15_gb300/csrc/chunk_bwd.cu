@@ -55,79 +55,6 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// out(r, n) = sum_{k < K} A[r][k] B[n][k] for r < R, n < N (R, N multiples of 16 and 8, K of
-// 8): fp32 rows in shared memory, A row r at A + r lda, B row n at B + n ldb.  Each warp of
-// the CTA takes 16 x 8 tiles (the mma.sync fragment shapes) in turn; a tile skipped by
-// `skip(r0, n0)` is not computed.  Three TF32 products of split operands (x = hi + lo, hi
-// and lo TF32: hi.hi + hi.lo + lo.hi) give about fp32 accuracy, the dropped lo.lo term
-// being ~2^-22 of the product.  st(r, n, v) receives each element once.
-template <class FSkip, class FS>
-__device__ __forceinline__ void rows_dot_rows(const float *A, int lda, const float *B, int ldb, int R, int N,
-                                              int K, int warp, int nwarps, int lane, FSkip skip, FS st) {
-    const int g = lane >> 2, t4 = lane & 3;
-    const int nrb = R / 16, ntiles = nrb * (N / 8);
-    for (int tile = warp; tile < ntiles; tile += nwarps) {
-        const int r0 = 16 * (tile % nrb), n0 = 8 * (tile / nrb);
-        if (skip(r0, n0)) continue;
-        const float *a = A + (r0 + g) * lda + t4, *b = B + (n0 + g) * ldb + t4;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int k0 = 0; k0 < K; k0 += 8) {
-            const float av[4] = {a[k0], a[8 * lda + k0], a[k0 + 4], a[8 * lda + k0 + 4]};
-            const float bv[2] = {b[k0], b[k0 + 4]};
-            uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                ah[u] = tc::to_tf32(av[u]);
-                al[u] = tc::to_tf32(av[u] - __uint_as_float(ah[u]));
-            }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                bh[u] = tc::to_tf32(bv[u]);
-                bl[u] = tc::to_tf32(bv[u] - __uint_as_float(bh[u]));
-            }
-            tc::mma_tf32_16x8x8(acc, al, bh[0], bh[1]);
-            tc::mma_tf32_16x8x8(acc, ah, bl[0], bl[1]);
-            tc::mma_tf32_16x8x8(acc, ah, bh[0], bh[1]);
-        }
-        st(r0 + g, n0 + 2 * t4, acc[0]);
-        st(r0 + g, n0 + 2 * t4 + 1, acc[1]);
-        st(r0 + g + 8, n0 + 2 * t4, acc[2]);
-        st(r0 + g + 8, n0 + 2 * t4 + 1, acc[3]);
-    }
-}
-
-// acc[t] (t < nt: the 16 x 8 C fragments at rows r0 .. r0 + 15, columns n0 + 8t ..) +=
-// sum_{k < K} A(r, k) B(k, n), K a multiple of 8; A(r, k) and B(k, n) return fp32 elements.
-// The same split-TF32 products as rows_dot_rows; one warp.
-template <class FA, class FB>
-__device__ __forceinline__ void rows_times_cols(float (&acc)[4][4], int nt, FA A, FB B, int r0, int n0, int K,
-                                                int g, int t4) {
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        const float av[4] = {A(r0 + g, k0 + t4), A(r0 + g + 8, k0 + t4), A(r0 + g, k0 + t4 + 4),
-                             A(r0 + g + 8, k0 + t4 + 4)};
-        uint32_t ah[4], al[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            ah[u] = tc::to_tf32(av[u]);
-            al[u] = tc::to_tf32(av[u] - __uint_as_float(ah[u]));
-        }
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            if (t >= nt) break;
-            const float bv[2] = {B(k0 + t4, n0 + 8 * t + g), B(k0 + t4 + 4, n0 + 8 * t + g)};
-            uint32_t bh[2], bl[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                bh[u] = tc::to_tf32(bv[u]);
-                bl[u] = tc::to_tf32(bv[u] - __uint_as_float(bh[u]));
-            }
-            tc::mma_tf32_16x8x8(acc[t], al, bh[0], bh[1]);
-            tc::mma_tf32_16x8x8(acc[t], ah, bl[0], bl[1]);
-            tc::mma_tf32_16x8x8(acc[t], ah, bh[0], bh[1]);
-        }
-    }
-}
-
 // Workspace of the backward, in floats, after the forward's slabs: T [n][C][C], checkpoints
 // [n][dk][dv], dS_C [n][dk][dv].
 struct BwdWorkspace {
@@ -405,7 +332,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
             for (int u = 0; u < 4; ++u) acc[t][u] = 0.f;
     };
     auto slice_products = [&](const float *X, int ldx) {
-        rows_dot_rows(X, ldx, sS, lds, C, kSlice, dv, warp, kWarps, lane, none,
+        tc::rows_dot_rows(X, ldx, sS, lds, C, kSlice, dv, warp, kWarps, lane, none,
                       [&](int rr, int nn, float v) { sM[rr * kLdM + nn] = v; });
         __syncthreads();
     };
@@ -462,7 +389,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         stage(S0, i0);
         slice_products(sX, ldw);   // (dO S0^T) over the slice
         if (own)
-            rows_times_cols(acc, ont, [&](int rr, int kk) { return Wn[rr * DK + i0 + kk]; },
+            tc::rows_times_cols(acc, ont, [&](int rr, int kk) { return Wn[rr * DK + i0 + kk]; },
                             [&](int kk, int nn) { return sS[kk * lds + nn]; }, orb, ocn, kSlice, g8, t4);
         if (!row_ok) continue;
 #pragma unroll
@@ -487,16 +414,16 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     //         tril(dO E^T) over P, then dE over dO
     acc_zero();
     if (own)
-        rows_times_cols(acc, ont, [&](int rr, int kk) { return sP[kk * kLdA + rr]; },
+        tc::rows_times_cols(acc, ont, [&](int rr, int kk) { return sP[kk * kLdA + rr]; },
                         [&](int kk, int nn) { return sX[kk * ldw + nn]; }, orb, ocn, C, g8, t4);
     for (int i0 = 0; i0 < DK; i0 += kSlice) {
         stage(dSC, i0);
         if (own)
-            rows_times_cols(acc, ont, [&](int rr, int kk) { return Kdn[rr * DK + i0 + kk]; },
+            tc::rows_times_cols(acc, ont, [&](int rr, int kk) { return Kdn[rr * DK + i0 + kk]; },
                             [&](int kk, int nn) { return sS[kk * lds + nn]; }, orb, ocn, kSlice, g8, t4);
     }
     __syncthreads();
-    rows_dot_rows(sX, ldw, sE, ldw, C, C, dv, warp, kWarps, lane,
+    tc::rows_dot_rows(sX, ldw, sE, ldw, C, C, dv, warp, kWarps, lane,
                   [](int r0, int n0) { return n0 > r0 + 15; },   // tiles above the diagonal
                   [&](int rr, int nn, float v) { sP[rr * kLdA + nn] = nn <= rr ? v : 0.f; });
     for (int idx = tid; idx < C * C; idx += kGThreads) {          // their zeros
@@ -518,7 +445,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     // ---- 3. dR = T^T dE (T lower triangular), over dE
     acc_zero();
     if (own)
-        rows_times_cols(acc, ont, [&](int rr, int kk) { return sT[kk * kLdA + rr]; },
+        tc::rows_times_cols(acc, ont, [&](int rr, int kk) { return sT[kk * kLdA + rr]; },
                         [&](int kk, int nn) { return sX[kk * ldw + nn]; }, orb, ocn, C, g8, t4);
     __syncthreads();
     acc_to_x();
@@ -527,7 +454,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     // ---- 4. dA over T; dv; db part 1 (with (K*G) S0); (dR S0^T) -> dk, dg; S0 by slices
     const float br = row_ok ? sB[r] : 0.f;
     float db = 0.f;
-    rows_dot_rows(sX, ldw, sE, ldw, C, C, dv, warp, kWarps, lane,
+    tc::rows_dot_rows(sX, ldw, sE, ldw, C, C, dv, warp, kWarps, lane,
                   [](int r0, int n0) { return n0 > r0 + 15; },
                   [&](int rr, int nn, float v) { sT[rr * kLdA + nn] = nn < rr ? -v : 0.f; });
     for (int idx = tid; idx < C * C; idx += kGThreads) {
@@ -545,7 +472,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         stage(S0, i0);
         slice_products(sX, ldw);   // (dR S0^T) over the slice
         if (own)
-            rows_times_cols(acc, ont,
+            tc::rows_times_cols(acc, ont,
                             [&](int rr, int kk) { return sK[rr * LDK + i0 + kk] * __expf(sG[rr * LDK + i0 + kk]); },
                             [&](int kk, int nn) { return sS[kk * lds + nn]; }, orb, ocn, kSlice, g8, t4);
         if (!row_ok) continue;

@@ -33,6 +33,7 @@
 // in shared memory (fp32); the state kernel multiplies each output by silu(z).
 #include "common.cuh"
 #include "chunk_layout.h"
+#include "tc_common.cuh"
 
 namespace dr {
 
@@ -277,16 +278,36 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
         }
         __syncthreads();
     }
-    {
+    const int64_t pofs = n * (int64_t)C * C;
+    const int warp = tid >> 5, lane = tid & 31;
+    if (gate != 2) {
+        // X = K K^T and Q K^T on the lower tiles (split-TF32 warp tiles, about fp32
+        // accuracy), then the decay exp(g_r - g_s) (exponent <= 0) and beta_r
+        auto upper = [](int r0, int n0) { return n0 > r0 + 15; };
+        tc::rows_dot_rows(sK, kLd, sK, kLd, C, C, DK, warp, kThreads / 32, lane, upper,
+                          [&](int r, int s2, float v) {
+                              sA[r * kLdA + s2] = s2 < r ? sB[r] * v * expf(sg[r] - sg[s2]) : 0.f;
+                          });
+        tc::rows_dot_rows(sQ, kLd, sK, kLd, C, C, DK, warp, kThreads / 32, lane, upper,
+                          [&](int r, int s2, float v) {
+                              a.ws.P[pofs + r * C + s2] = s2 <= r ? v * expf(sg[r] - sg[s2]) : 0.f;
+                          });
+        for (int idx = tid; idx < C * C; idx += kThreads) {   // the skipped tiles: zeros
+            const int r = idx / C, s2 = idx % C;
+            if ((s2 & ~7) > (r | 15)) {
+                sA[r * kLdA + s2] = 0.f;
+                a.ws.P[pofs + idx] = 0.f;   // zero above the diagonal
+            }
+        }
+    } else {
         const int r = tid >> 2;
-        const int64_t pofs = n * (int64_t)C * C;
         for (int m = 0; m < 16; ++m) {
             const int s = (tid & 3) + 4 * m;
             if (r >= C || s >= C) continue;
             float ak = 0.f, aq = 0.f;
             if (s <= r) {
                 const float *lk = sK + r * kLd, *lq = sQ + r * kLd;
-                if (gate == 2) {
+                {   // per-channel gate: factors around the sub-chunk references
                     const float *rs = sR + s * kLd;
                     const int i = r / kSub, j = s / kSub;
                     if (i == j) {
@@ -309,18 +330,6 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
                             aq += y.x * zw.x + y.y * zw.y + y.z * zw.z + y.w * zw.w;
                         }
                     }
-                } else {
-                    const float *rs = sK + s * kLd;
-                    for (int ch = 0; ch < DK; ch += 4) {
-                        const float4 x = *reinterpret_cast<const float4 *>(lk + ch);
-                        const float4 y = *reinterpret_cast<const float4 *>(lq + ch);
-                        const float4 z = *reinterpret_cast<const float4 *>(rs + ch);
-                        ak += x.x * z.x + x.y * z.y + x.z * z.z + x.w * z.w;
-                        aq += y.x * z.x + y.y * z.y + y.z * z.z + y.w * z.w;
-                    }
-                    const float sc = expf(sg[r] - sg[s]);   // exponent <= 0
-                    ak *= sc;
-                    aq *= sc;
                 }
             }
             sA[r * kLdA + s] = (s < r) ? sB[r] * ak : 0.f;
@@ -361,12 +370,27 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
         sR[s * kLd + ch] = s < Lc ? sB[s] * sNk[s] * to_f32(k[tok(s) * DK + ch]) * expf(G(s, ch)) : 0.f;
     }
     __syncthreads();
-    for (int idx = tid; idx < C * DK; idx += kThreads) {
-        const int r = idx / DK, ch = idx % DK;
-        float acc = 0.f;
-        for (int s = 0; s <= r; ++s) acc += sT[r * kLdA + s] * sR[s * kLd + ch];
-        a.ws.W[wofs + idx] = acc;
-    }
+    // the [C][N] product T (lower triangular, as stored: entries above the diagonal are
+    // not read) times sR, written to `dst` with row stride N: warp tiles of 16 rows x
+    // N / (8 warps / (C / 16)) columns
+    auto t_times_r = [&](int N, float *dst) {
+        const int rbs = C / 16, groups = (kThreads / 32) / rbs, ncol = N / groups;
+        const int r0 = 16 * (warp % rbs), n0 = (warp / rbs) * ncol, g8 = lane >> 2, t4 = lane & 3;
+        float acc[8][4];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc[t][u] = 0.f;
+        tc::rows_times_cols(acc, ncol / 8, [&](int rr, int kk) { return kk <= rr ? sT[rr * kLdA + kk] : 0.f; },
+                            [&](int kk, int nn) { return sR[kk * kLd + nn]; }, r0, n0, C, g8, t4);
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+            if (8 * t < ncol)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    dst[(r0 + g8 + 8 * (u >> 1)) * N + n0 + 8 * t + 2 * t4 + (u & 1)] = acc[t][u];
+    };
+    t_times_r(DK, a.ws.W + wofs);
     __syncthreads();
     //    U = T diag(b) V.
     for (int idx = tid; idx < C * dv; idx += kThreads) {
@@ -375,12 +399,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
     }
     __syncthreads();
     const int64_t uofs = n * (int64_t)C * dv;
-    for (int idx = tid; idx < C * dv; idx += kThreads) {
-        const int r = idx / dv, j = idx % dv;
-        float acc = 0.f;
-        for (int s = 0; s <= r; ++s) acc += sT[r * kLdA + s] * sR[s * kLd + j];
-        a.ws.U[uofs + idx] = acc;
-    }
+    t_times_r(dv, a.ws.U + uofs);
 }
 
 constexpr int kDvt = 32;   // state columns per CTA of the state pass
