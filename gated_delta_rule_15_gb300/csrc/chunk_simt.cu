@@ -198,12 +198,18 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
                 sG[r * DK + ch] = acc;
             }
         }
-    } else if (tid == 0) {
-        float acc = 0.f;
-        for (int r = 0; r < C; ++r) {
-            if (gate == 1 && r < Lc) acc += a.log_alpha[tok(r)];
-            sg[r] = acc;
+    } else if (tid < 32) {   // scalar gate: warp 0, two tokens per lane, one scan
+        const int lane = tid, r = 2 * lane;
+        const float l0 = (gate == 1 && r < Lc) ? a.log_alpha[tok(r)] : 0.f;
+        const float l1 = (gate == 1 && r + 1 < Lc) ? a.log_alpha[tok(r + 1)] : 0.f;
+        float p = l0 + l1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, p, o);
+            if (lane >= o) p += y;
         }
+        if (r < C) sg[r] = p - l1;
+        if (r + 1 < C) sg[r + 1] = p;
     }
     // 2. k and q rows as fp32.
     for (int idx = tid; idx < C * (DK / 4); idx += kThreads) {
@@ -364,10 +370,26 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
             a.T_out[n * (int64_t)C * C + idx] = s2 <= r ? sT[r * kLdA + s2] : 0.f;
         }
     }
-    // 6. W = T diag(b) (K*G):  rows b_s k_s exp(g_s) (exponent <= 0), k reloaded raw.
-    for (int idx = tid; idx < C * DK; idx += kThreads) {
-        const int s = idx / DK, ch = idx % DK;
-        sR[s * kLd + ch] = s < Lc ? sB[s] * sNk[s] * to_f32(k[tok(s) * DK + ch]) * expf(G(s, ch)) : 0.f;
+    // 6. W = T diag(b) (K*G):  rows b_s k_s exp(g_s) (exponent <= 0), four channels per
+    //    step; k as held (scalar gate or none) or reloaded raw (the per-channel gate has
+    //    rescaled sK)
+#pragma unroll 4
+    for (int idx = tid; idx < C * (DK / 4); idx += kThreads) {
+        const int s = idx / (DK / 4), c4 = 4 * (idx % (DK / 4));
+        float4 kk = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s < Lc) {
+            if (gate == 2) {
+                kk = load4(k + tok(s) * DK + c4);
+                const float f = sNk[s];
+                kk = make_float4(kk.x * f, kk.y * f, kk.z * f, kk.w * f);
+            } else {
+                kk = *reinterpret_cast<const float4 *>(sK + s * kLd + c4);
+            }
+        }
+        const float b = sB[s];
+        *reinterpret_cast<float4 *>(sR + s * kLd + c4) =
+            make_float4(b * kk.x * expf(G(s, c4)), b * kk.y * expf(G(s, c4 + 1)),
+                        b * kk.z * expf(G(s, c4 + 2)), b * kk.w * expf(G(s, c4 + 3)));
     }
     __syncthreads();
     // the [C][N] product T (lower triangular, as stored: entries above the diagonal are
@@ -393,9 +415,12 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
     t_times_r(DK, a.ws.W + wofs);
     __syncthreads();
     //    U = T diag(b) V.
-    for (int idx = tid; idx < C * dv; idx += kThreads) {
-        const int s = idx / dv, j = idx % dv;
-        sR[s * kLd + j] = s < Lc ? sB[s] * to_f32(v[tok(s) * dv + j]) : 0.f;
+#pragma unroll 4
+    for (int idx = tid; idx < C * (dv / 4); idx += kThreads) {
+        const int s = idx / (dv / 4), j4 = 4 * (idx % (dv / 4));
+        float4 vv = s < Lc ? load4(v + tok(s) * dv + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float b = sB[s];
+        *reinterpret_cast<float4 *>(sR + s * kLd + j4) = make_float4(b * vv.x, b * vv.y, b * vv.z, b * vv.w);
     }
     __syncthreads();
     const int64_t uofs = n * (int64_t)C * dv;
