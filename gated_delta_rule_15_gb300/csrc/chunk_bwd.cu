@@ -347,24 +347,37 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     };
 
     // ---- 0. inputs (rows past the sequence: zero, log alpha 0)
-    for (int idx = tid; idx < C * DK; idx += kGThreads) {
-        const int rr = idx / DK, i = idx % DK;
+    //      (four elements per load, several loads in flight per thread)
+#pragma unroll 4
+    for (int idx = tid; idx < C * (DK / 4); idx += kGThreads) {
+        const int rr = idx / (DK / 4), i4 = 4 * (idx % (DK / 4));
         const bool ok = rr < Lc;
-        sQ[rr * LDK + i] = ok ? to_f32(q[tok(rr) * DK + i]) : 0.f;
-        sK[rr * LDK + i] = ok ? to_f32(k[tok(rr) * DK + i]) : 0.f;
-        float la = 0.f;
-        if (ok && a.gate == 2) la = a.log_alpha[tok(rr) * DK + i];
-        if (ok && a.gate == 1) la = a.log_alpha[tok(rr)];
-        sG[rr * LDK + i] = la;
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(sQ + rr * LDK + i4) = ok ? load4(q + tok(rr) * DK + i4) : z4;
+        *reinterpret_cast<float4 *>(sK + rr * LDK + i4) = ok ? load4(k + tok(rr) * DK + i4) : z4;
+        float4 la = z4;
+        if (ok && a.gate == 2) la = *reinterpret_cast<const float4 *>(a.log_alpha + tok(rr) * DK + i4);
+        if (ok && a.gate == 1) {
+            const float l = a.log_alpha[tok(rr)];
+            la = make_float4(l, l, l, l);
+        }
+        *reinterpret_cast<float4 *>(sG + rr * LDK + i4) = la;
     }
     for (int rr = tid; rr < C; rr += kGThreads) sB[rr] = rr < Lc ? to_f32(beta[tok(rr)]) : 0.f;
-    for (int idx = tid; idx < C * C; idx += kGThreads) {
-        sT[(idx / C) * kLdA + idx % C] = a.ws.T[n * (int64_t)C * C + idx];
-        sP[(idx / C) * kLdA + idx % C] = a.ws.fw.P[n * (int64_t)C * C + idx];
+#pragma unroll 2
+    for (int idx = tid; idx < C * C / 4; idx += kGThreads) {
+        const int rr = (4 * idx) / C, c0 = (4 * idx) % C;
+        const float4 t4v = *reinterpret_cast<const float4 *>(a.ws.T + n * (int64_t)C * C + 4 * idx);
+        const float4 p4v = *reinterpret_cast<const float4 *>(a.ws.fw.P + n * (int64_t)C * C + 4 * idx);
+        float *tr = sT + rr * kLdA + c0, *pr = sP + rr * kLdA + c0;
+        tr[0] = t4v.x; tr[1] = t4v.y; tr[2] = t4v.z; tr[3] = t4v.w;
+        pr[0] = p4v.x; pr[1] = p4v.y; pr[2] = p4v.z; pr[3] = p4v.w;
     }
-    for (int idx = tid; idx < C * dv; idx += kGThreads) {
-        const int rr = idx / dv, j = idx % dv;
-        sX[rr * ldw + j] = rr < Lc ? to_f32(dout[tok(rr) * dv + j]) : 0.f;
+#pragma unroll 4
+    for (int idx = tid; idx < C * (dv / 4); idx += kGThreads) {
+        const int rr = idx / (dv / 4), j4 = 4 * (idx % (dv / 4));
+        *reinterpret_cast<float4 *>(sX + rr * ldw + j4) =
+            rr < Lc ? load4(dout + tok(rr) * dv + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     for (int i = tid; i < DK; i += kGThreads) sDgC[i] = 0.f;
     for (int rr = tid; rr < 64; rr += kGThreads) sRed[rr] = 0.f;   // db terms of phase 4
