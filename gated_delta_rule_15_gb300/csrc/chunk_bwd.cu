@@ -564,36 +564,99 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     //         k_ri k_si D_rs,i (s < r), D = exp(g_r - g_s) <= 1; row r as the row, then as
     //         the column
     float db2 = 0.f;
-    if (row_ok && a.gate != 2) {   // scalar gate or none: D_rs is one number per (r, s)
-        const float gr = sG[r * LDK];
-        for (int s = 0; s <= r; ++s) {
-            const float d = __expf(gr - sG[s * LDK]);
-            const float cp = sP[r * kLdA + s] * d;
-            const float da = s < r ? sT[r * kLdA + s] * d : 0.f, ca = da * br;
-            float kk = 0.f;
+    if (a.gate != 2) {
+        // Scalar gate or none: D_rs is one number per (r, s), so with Pd = dP * D and Ad =
+        // dA * D (in place over dP and dA) the pair terms are three [C][DK] products,
+        //   dq += Pd K,   dk += diag(b) Ad K + Pd^T Q + (diag(b) Ad)^T K,
+        //   dg += Q * (Pd K) + diag(b) K * (Ad K) - K * (Pd^T Q + (diag(b) Ad)^T K),
+        //   db_r += sum_i k_ri (Ad K)_ri,
+        // as split-TF32 tiles.  The accumulators go through shared memory (dq over E, dk over
+        // the z values, dg over g, whose column 0 is kept in sM first).
+        __syncthreads();   // the z values in sX have been read
+        if (tid < C) sM[tid] = sG[tid * LDK];
+        __syncthreads();
+        if (row_ok)
 #pragma unroll
             for (int m = 0; m < NI; ++m) {
                 const int i = part + kParts * m;
-                const float ks = sK[s * LDK + i], kr = sK[r * LDK + i];
-                aq[m] = fmaf(cp, ks, aq[m]);
-                ak[m] = fmaf(ca, ks, ak[m]);
-                ag[m] = fmaf(ks, fmaf(cp, sQ[r * LDK + i], ca * kr), ag[m]);
-                kk = fmaf(kr, ks, kk);
+                sE[r * ldw + i] = aq[m];
+                sX[r * ldw + i] = ak[m];
+                sG[r * LDK + i] = ag[m];
             }
-            db2 = fmaf(da, kk, db2);
+        for (int idx = tid; idx < C * C; idx += kGThreads) {
+            const int rr = idx / C, ss = idx % C;
+            const float d = ss <= rr ? __expf(sM[rr] - sM[ss]) : 0.f;   // exponent <= 0
+            sP[rr * kLdA + ss] *= d;
+            sT[rr * kLdA + ss] *= d;
         }
-        for (int s2 = r; s2 < C; ++s2) {
-            const float d = __expf(sG[s2 * LDK] - gr);
-            const float c1 = sP[s2 * kLdA + r] * d;
-            const float c2 = s2 > r ? sT[s2 * kLdA + r] * sB[s2] * d : 0.f;
+        __syncthreads();
+        if (own) {
+            const int kcn = (warp >> 2) * (DK / 4), knt = DK / 32;
+            auto kcol = [&](int t, int u) { return kcn + 8 * t + 2 * t4 + (u & 1); };
+            auto Kat = [&](int kk, int nn) { return sK[kk * LDK + nn]; };
+            // Pd K
+            acc_zero();
+            tc::rows_times_cols(acc, knt, [&](int rr, int kk) { return sP[rr * kLdA + kk]; }, Kat, orb, kcn, C,
+                                g8, t4);
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (t < knt) {
+                        const int rr = orow(u), i = kcol(t, u);
+                        sE[rr * ldw + i] += acc[t][u];
+                        sG[rr * LDK + i] = fmaf(sQ[rr * LDK + i], acc[t][u], sG[rr * LDK + i]);
+                    }
+            // Ad K
+            acc_zero();
+            tc::rows_times_cols(acc, knt, [&](int rr, int kk) { return sT[rr * kLdA + kk]; }, Kat, orb, kcn, C,
+                                g8, t4);
+            float d2[2] = {0.f, 0.f};
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (t < knt) {
+                        const int rr = orow(u), i = kcol(t, u);
+                        const float kri = sK[rr * LDK + i], bm = sB[rr] * acc[t][u];
+                        sX[rr * ldw + i] += bm;
+                        sG[rr * LDK + i] = fmaf(kri, bm, sG[rr * LDK + i]);
+                        d2[u >> 1] = fmaf(kri, acc[t][u], d2[u >> 1]);
+                    }
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                d2[h2] += __shfl_xor_sync(0xffffffffu, d2[h2], 1);
+                d2[h2] += __shfl_xor_sync(0xffffffffu, d2[h2], 2);
+            }
+            if (t4 == 0) {
+                atomicAdd(&sRed[orb + g8], d2[0]);
+                atomicAdd(&sRed[orb + g8 + 8], d2[1]);
+            }
+            // Pd^T Q + (diag(b) Ad)^T K
+            acc_zero();
+            tc::rows_times_cols(acc, knt, [&](int rr, int kk) { return sP[kk * kLdA + rr]; },
+                                [&](int kk, int nn) { return sQ[kk * LDK + nn]; }, orb, kcn, C, g8, t4);
+            tc::rows_times_cols(acc, knt, [&](int rr, int kk) { return sB[kk] * sT[kk * kLdA + rr]; }, Kat, orb,
+                                kcn, C, g8, t4);
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (t < knt) {
+                        const int rr = orow(u), i = kcol(t, u);
+                        sX[rr * ldw + i] += acc[t][u];
+                        sG[rr * LDK + i] = fmaf(-sK[rr * LDK + i], acc[t][u], sG[rr * LDK + i]);
+                    }
+        }
+        __syncthreads();
+        if (row_ok)
 #pragma unroll
             for (int m = 0; m < NI; ++m) {
                 const int i = part + kParts * m;
-                const float t = fmaf(c1, sQ[s2 * LDK + i], c2 * sK[s2 * LDK + i]);
-                ak[m] += t;
-                ag[m] = fmaf(-sK[r * LDK + i], t, ag[m]);
+                aq[m] = sE[r * ldw + i];
+                ak[m] = sX[r * ldw + i];
+                ag[m] = sG[r * LDK + i];
             }
-        }
     } else if (row_ok) {
         for (int s = 0; s <= r; ++s) {
             const float dp = sP[r * kLdA + s];
