@@ -274,6 +274,9 @@ size_t grad_smem_bytes(int dk, int dv) {
 //   6. db, dq, dk out; dg summed from the last token back -> d log alpha.
 template <int DK, typename Tin, typename Tg>
 __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
+    // fp32 inputs: products at fp32 accuracy (three split-TF32 products); bf16 inputs, whose
+    // results are held to the bf16 bound: one TF32 product (~2^-11 relative)
+    constexpr bool kSplit = sizeof(Tin) == 4;
     constexpr int LDK = DK + 8;
     constexpr int NI = DK / kParts;   // key channels per thread
     extern __shared__ float4 smem4[];
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
             for (int u = 0; u < 4; ++u) acc[t][u] = 0.f;
     };
     auto slice_products = [&](const float *X, int ldx) {
-        tc::rows_dot_rows(X, ldx, sS, lds, C, kSlice, dv, warp, kWarps, lane, none,
+        tc::rows_dot_rows<kSplit>(X, ldx, sS, lds, C, kSlice, dv, warp, kWarps, lane, none,
                       [&](int rr, int nn, float v) { sM[rr * kLdM + nn] = v; });
         __syncthreads();
     };
@@ -402,7 +405,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         stage(S0, i0);
         slice_products(sX, ldw);   // (dO S0^T) over the slice
         if (own)
-            tc::rows_times_cols(acc, ont, [&](int rr, int kk) { return Wn[rr * DK + i0 + kk]; },
+            tc::rows_times_cols<kSplit>(acc, ont, [&](int rr, int kk) { return Wn[rr * DK + i0 + kk]; },
                             [&](int kk, int nn) { return sS[kk * lds + nn]; }, orb, ocn, kSlice, g8, t4);
         if (!row_ok) continue;
 #pragma unroll
@@ -427,16 +430,16 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     //         tril(dO E^T) over P, then dE over dO
     acc_zero();
     if (own)
-        tc::rows_times_cols(acc, ont, [&](int rr, int kk) { return sP[kk * kLdA + rr]; },
+        tc::rows_times_cols<kSplit>(acc, ont, [&](int rr, int kk) { return sP[kk * kLdA + rr]; },
                         [&](int kk, int nn) { return sX[kk * ldw + nn]; }, orb, ocn, C, g8, t4);
     for (int i0 = 0; i0 < DK; i0 += kSlice) {
         stage(dSC, i0);
         if (own)
-            tc::rows_times_cols(acc, ont, [&](int rr, int kk) { return Kdn[rr * DK + i0 + kk]; },
+            tc::rows_times_cols<kSplit>(acc, ont, [&](int rr, int kk) { return Kdn[rr * DK + i0 + kk]; },
                             [&](int kk, int nn) { return sS[kk * lds + nn]; }, orb, ocn, kSlice, g8, t4);
     }
     __syncthreads();
-    tc::rows_dot_rows(sX, ldw, sE, ldw, C, C, dv, warp, kWarps, lane,
+    tc::rows_dot_rows<kSplit>(sX, ldw, sE, ldw, C, C, dv, warp, kWarps, lane,
                   [](int r0, int n0) { return n0 > r0 + 15; },   // tiles above the diagonal
                   [&](int rr, int nn, float v) { sP[rr * kLdA + nn] = nn <= rr ? v : 0.f; });
     for (int idx = tid; idx < C * C; idx += kGThreads) {          // their zeros
@@ -458,7 +461,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     // ---- 3. dR = T^T dE (T lower triangular), over dE
     acc_zero();
     if (own)
-        tc::rows_times_cols(acc, ont, [&](int rr, int kk) { return sT[kk * kLdA + rr]; },
+        tc::rows_times_cols<kSplit>(acc, ont, [&](int rr, int kk) { return sT[kk * kLdA + rr]; },
                         [&](int kk, int nn) { return sX[kk * ldw + nn]; }, orb, ocn, C, g8, t4);
     __syncthreads();
     acc_to_x();
@@ -467,7 +470,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     // ---- 4. dA over T; dv; db part 1 (with (K*G) S0); (dR S0^T) -> dk, dg; S0 by slices
     const float br = row_ok ? sB[r] : 0.f;
     float db = 0.f;
-    tc::rows_dot_rows(sX, ldw, sE, ldw, C, C, dv, warp, kWarps, lane,
+    tc::rows_dot_rows<kSplit>(sX, ldw, sE, ldw, C, C, dv, warp, kWarps, lane,
                   [](int r0, int n0) { return n0 > r0 + 15; },
                   [&](int rr, int nn, float v) { sT[rr * kLdA + nn] = nn < rr ? -v : 0.f; });
     for (int idx = tid; idx < C * C; idx += kGThreads) {
@@ -485,7 +488,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         stage(S0, i0);
         slice_products(sX, ldw);   // (dR S0^T) over the slice
         if (own)
-            tc::rows_times_cols(acc, ont,
+            tc::rows_times_cols<kSplit>(acc, ont,
                             [&](int rr, int kk) { return sK[rr * LDK + i0 + kk] * __expf(sG[rr * LDK + i0 + kk]); },
                             [&](int kk, int nn) { return sS[kk * lds + nn]; }, orb, ocn, kSlice, g8, t4);
         if (!row_ok) continue;
@@ -596,7 +599,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
             auto Kat = [&](int kk, int nn) { return sK[kk * LDK + nn]; };
             // Pd K
             acc_zero();
-            tc::rows_times_cols(acc, knt, [&](int rr, int kk) { return sP[rr * kLdA + kk]; }, Kat, orb, kcn, C,
+            tc::rows_times_cols<kSplit>(acc, knt, [&](int rr, int kk) { return sP[rr * kLdA + kk]; }, Kat, orb, kcn, C,
                                 g8, t4);
 #pragma unroll
             for (int t = 0; t < 4; ++t)
@@ -609,7 +612,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
                     }
             // Ad K
             acc_zero();
-            tc::rows_times_cols(acc, knt, [&](int rr, int kk) { return sT[rr * kLdA + kk]; }, Kat, orb, kcn, C,
+            tc::rows_times_cols<kSplit>(acc, knt, [&](int rr, int kk) { return sT[rr * kLdA + kk]; }, Kat, orb, kcn, C,
                                 g8, t4);
             float d2[2] = {0.f, 0.f};
 #pragma unroll
@@ -634,9 +637,9 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
             }
             // Pd^T Q + (diag(b) Ad)^T K
             acc_zero();
-            tc::rows_times_cols(acc, knt, [&](int rr, int kk) { return sP[kk * kLdA + rr]; },
+            tc::rows_times_cols<kSplit>(acc, knt, [&](int rr, int kk) { return sP[kk * kLdA + rr]; },
                                 [&](int kk, int nn) { return sQ[kk * LDK + nn]; }, orb, kcn, C, g8, t4);
-            tc::rows_times_cols(acc, knt, [&](int rr, int kk) { return sB[kk] * sT[kk * kLdA + rr]; }, Kat, orb,
+            tc::rows_times_cols<kSplit>(acc, knt, [&](int rr, int kk) { return sB[kk] * sT[kk * kLdA + rr]; }, Kat, orb,
                                 kcn, C, g8, t4);
 #pragma unroll
             for (int t = 0; t < 4; ++t)

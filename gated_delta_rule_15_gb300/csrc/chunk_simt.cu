@@ -150,6 +150,9 @@ __device__ __forceinline__ void solve64_blocked(const float *sA, float *sT, floa
 
 template <int DK, typename Tin>
 __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
+    // fp32 inputs: products at fp32 accuracy (three split-TF32 products); bf16 inputs, whose
+    // results are held to the bf16 bound: one TF32 product (~2^-11 relative)
+    constexpr bool kSplit = sizeof(Tin) == 4;
     extern __shared__ float4 smem4[];
     float *sK = reinterpret_cast<float *>(smem4);  // k, then left factor of A
     float *sQ = sK + 64 * kLd;                     // q, then left factor of P
@@ -290,11 +293,11 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
         // X = K K^T and Q K^T on the lower tiles (split-TF32 warp tiles, about fp32
         // accuracy), then the decay exp(g_r - g_s) (exponent <= 0) and beta_r
         auto upper = [](int r0, int n0) { return n0 > r0 + 15; };
-        tc::rows_dot_rows(sK, kLd, sK, kLd, C, C, DK, warp, kThreads / 32, lane, upper,
+        tc::rows_dot_rows<kSplit>(sK, kLd, sK, kLd, C, C, DK, warp, kThreads / 32, lane, upper,
                           [&](int r, int s2, float v) {
                               sA[r * kLdA + s2] = s2 < r ? sB[r] * v * expf(sg[r] - sg[s2]) : 0.f;
                           });
-        tc::rows_dot_rows(sQ, kLd, sK, kLd, C, C, DK, warp, kThreads / 32, lane, upper,
+        tc::rows_dot_rows<kSplit>(sQ, kLd, sK, kLd, C, C, DK, warp, kThreads / 32, lane, upper,
                           [&](int r, int s2, float v) {
                               a.ws.P[pofs + r * C + s2] = s2 <= r ? v * expf(sg[r] - sg[s2]) : 0.f;
                           });
@@ -403,7 +406,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
         for (int t = 0; t < 8; ++t)
 #pragma unroll
             for (int u = 0; u < 4; ++u) acc[t][u] = 0.f;
-        tc::rows_times_cols(acc, ncol / 8, [&](int rr, int kk) { return kk <= rr ? sT[rr * kLdA + kk] : 0.f; },
+        tc::rows_times_cols<kSplit>(acc, ncol / 8, [&](int rr, int kk) { return kk <= rr ? sT[rr * kLdA + kk] : 0.f; },
                             [&](int kk, int nn) { return sR[kk * kLd + nn]; }, r0, n0, C, g8, t4);
 #pragma unroll
         for (int t = 0; t < 8; ++t)

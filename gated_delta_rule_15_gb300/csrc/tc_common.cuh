@@ -279,10 +279,11 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, float *T, flo
 // out(r, n) = sum_{k < K} A[r][k] B[n][k] for r < R, n < N (R, N multiples of 16 and 8, K of
 // 8): fp32 rows in shared memory, A row r at A + r lda, B row n at B + n ldb.  Each warp of
 // the CTA takes 16 x 8 tiles (the mma.sync fragment shapes) in turn; a tile skipped by
-// `skip(r0, n0)` is not computed.  Three TF32 products of split operands (x = hi + lo, hi
-// and lo TF32: hi.hi + hi.lo + lo.hi) give about fp32 accuracy, the dropped lo.lo term
-// being ~2^-22 of the product.  st(r, n, v) receives each element once.
-template <class FSkip, class FS>
+// `skip(r0, n0)` is not computed.  kSplit: three TF32 products of split operands (x = hi + lo,
+// hi and lo TF32: hi.hi + hi.lo + lo.hi) give about fp32 accuracy, the dropped lo.lo term
+// being ~2^-22 of the product; otherwise one product of the TF32-rounded operands (~2^-11
+// relative).  st(r, n, v) receives each element once.
+template <bool kSplit, class FSkip, class FS>
 __device__ __forceinline__ void rows_dot_rows(const float *A, int lda, const float *B, int ldb, int R, int N,
                                               int K, int warp, int nwarps, int lane, FSkip skip, FS st) {
     const int g = lane >> 2, t4 = lane & 3;
@@ -295,19 +296,20 @@ __device__ __forceinline__ void rows_dot_rows(const float *A, int lda, const flo
         for (int k0 = 0; k0 < K; k0 += 8) {
             const float av[4] = {a[k0], a[8 * lda + k0], a[k0 + 4], a[8 * lda + k0 + 4]};
             const float bv[2] = {b[k0], b[k0 + 4]};
-            uint32_t ah[4], al[4], bh[2], bl[2];
+            uint32_t ah[4], bh[2];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                ah[u] = to_tf32(av[u]);
-                al[u] = to_tf32(av[u] - __uint_as_float(ah[u]));
-            }
+            for (int u = 0; u < 4; ++u) ah[u] = to_tf32(av[u]);
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                bh[u] = to_tf32(bv[u]);
-                bl[u] = to_tf32(bv[u] - __uint_as_float(bh[u]));
+            for (int u = 0; u < 2; ++u) bh[u] = to_tf32(bv[u]);
+            if constexpr (kSplit) {
+                uint32_t al[4], bl[2];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) al[u] = to_tf32(av[u] - __uint_as_float(ah[u]));
+#pragma unroll
+                for (int u = 0; u < 2; ++u) bl[u] = to_tf32(bv[u] - __uint_as_float(bh[u]));
+                mma_tf32_16x8x8(acc, al, bh[0], bh[1]);
+                mma_tf32_16x8x8(acc, ah, bl[0], bl[1]);
             }
-            mma_tf32_16x8x8(acc, al, bh[0], bh[1]);
-            mma_tf32_16x8x8(acc, ah, bl[0], bl[1]);
             mma_tf32_16x8x8(acc, ah, bh[0], bh[1]);
         }
         st(r0 + g, n0 + 2 * t4, acc[0]);
@@ -319,8 +321,8 @@ __device__ __forceinline__ void rows_dot_rows(const float *A, int lda, const flo
 
 // acc[t] (t < nt <= NT: the 16 x 8 C fragments at rows r0 .. r0 + 15, columns n0 + 8t ..)
 // += sum_{k < K} A(r, k) B(k, n), K a multiple of 8; A(r, k) and B(k, n) return fp32
-// elements.  The same split-TF32 products as rows_dot_rows; one warp.
-template <int NT, class FA, class FB>
+// elements.  The same TF32 products as rows_dot_rows (kSplit as there); one warp.
+template <bool kSplit, int NT, class FA, class FB>
 __device__ __forceinline__ void rows_times_cols(float (&acc)[NT][4], int nt, FA A, FB B, int r0, int n0, int K,
                                                 int g, int t4) {
     for (int k0 = 0; k0 < K; k0 += 8) {
@@ -330,20 +332,22 @@ __device__ __forceinline__ void rows_times_cols(float (&acc)[NT][4], int nt, FA 
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             ah[u] = to_tf32(av[u]);
-            al[u] = to_tf32(av[u] - __uint_as_float(ah[u]));
+            if constexpr (kSplit) al[u] = to_tf32(av[u] - __uint_as_float(ah[u]));
         }
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             if (t >= nt) break;
             const float bv[2] = {B(k0 + t4, n0 + 8 * t + g), B(k0 + t4 + 4, n0 + 8 * t + g)};
-            uint32_t bh[2], bl[2];
+            uint32_t bh[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                bh[u] = to_tf32(bv[u]);
-                bl[u] = to_tf32(bv[u] - __uint_as_float(bh[u]));
+            for (int u = 0; u < 2; ++u) bh[u] = to_tf32(bv[u]);
+            if constexpr (kSplit) {
+                uint32_t bl[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) bl[u] = to_tf32(bv[u] - __uint_as_float(bh[u]));
+                mma_tf32_16x8x8(acc[t], al, bh[0], bh[1]);
+                mma_tf32_16x8x8(acc[t], ah, bl[0], bl[1]);
             }
-            mma_tf32_16x8x8(acc[t], al, bh[0], bh[1]);
-            mma_tf32_16x8x8(acc[t], ah, bl[0], bl[1]);
             mma_tf32_16x8x8(acc[t], ah, bh[0], bh[1]);
         }
     }
