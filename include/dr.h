@@ -190,10 +190,14 @@ int dr_recurrent_step(const dr_step_desc *desc,
  * Backward of dr_chunk_fwd (training): the gradients of
  *     L = <d_out, out> + <d_final_state, final_state>
  * with respect to every input, for the same descriptor (any gate, dk, dv in {64, 128},
- * chunk 16, 32 or 64, fp32 or bf16), computed chunkwise on the CUDA cores in fp32: the
- * forward's per-chunk operands and chunk-start states are recomputed into the workspace, a
- * reverse pass carries the state gradient from the last chunk to the first, and every
- * chunk's token gradients follow in parallel.  The pages ask for chunkwise kernels for
+ * chunk 16, 32 or 64, fp32 or bf16), computed chunkwise with fp32 sums: the forward's
+ * per-chunk operands and chunk-start states are recomputed into the workspace, a reverse
+ * pass carries the state gradient from the last chunk to the first, and every chunk's
+ * token gradients follow in parallel.  Products of rows run on the tensor cores as TF32
+ * tiles, split into three products (fp32 accuracy) for fp32 inputs and single products
+ * for bf16 inputs; the chunk-start states of bf16 problems that the tensor-core forward
+ * serves come from it (bf16 operands).  Accuracy: fp32 inputs within 1e-4 of the exact
+ * gradients (unit-scale values), bf16 inputs within the forward's bf16 bound.  The pages ask for chunkwise kernels for
  * training (page "linear-attention gated-deltanet guide", section 5) without printing a
  * backward; this is the derivative of the chunk form.
  *
