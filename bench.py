@@ -386,7 +386,7 @@ def run_native(args):
             "vs_plain": round(fms / ms, 3)}
         bms = bench_bwd(w, 2, 3, world)
         extra["backward_" + w.name] = {
-            "what": "dr_chunk_bwd (CUDA cores, fp32): every input gradient",
+            "what": "dr_chunk_bwd (fp32 sums, TF32 tensor-core tiles): every input gradient",
             "ms_per_call": round(bms, 3), "tokens_per_s": w.B * w.T / (bms * 1e-3),
             "vs_forward": round(bms / ms, 1)}
         for name in ("kda_bf16_B4_H32_T8192_d128", "gdn_bf16_B1_H16_T65536_d128_init"):
