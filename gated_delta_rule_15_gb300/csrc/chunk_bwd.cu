@@ -37,6 +37,8 @@ constexpr int kThreads = 256;
 constexpr int kLdA = 65;   // padded row stride of [64][64] tiles
 constexpr int kLdP = 68;   // row stride of the reverse pass's P tile (16-byte rows)
 constexpr int kDvt = 32;   // state columns per CTA of the reverse pass
+constexpr int kLdC = kDvt + 8;   // row stride of the reverse pass's 32-column tiles (conflict-free
+                                 // tensor-core fragments)
 constexpr int kSlice = 32; // rows of a [dk][dv] state matrix staged at a time
 constexpr int kGThreads = 512;   // per-chunk gradient kernel: 8 threads per token row
 constexpr int kParts = 8;
@@ -97,7 +99,7 @@ struct DStateArgs {
 };
 
 size_t dstate_smem_bytes(int dk) {
-    return sizeof(float) * (size_t)(dk * kDvt + 3 * 64 * (dk + 4) + 2 * 64 * kDvt + 64 * kLdP + dk);
+    return sizeof(float) * (size_t)(dk * kLdC + 3 * 64 * (dk + 4) + 2 * 64 * kLdC + 64 * kLdP + dk);
 }
 
 // Reverse state-gradient pass: dS starts as d_final; for each chunk, last first, it is
@@ -105,18 +107,19 @@ size_t dstate_smem_bytes(int dk) {
 // - W^T dE.  Column j of dS only meets column j of dO, so a CTA owns 32 columns.  A chunk's
 // operands arrive by 16-byte asynchronous copies behind one wait, and the next chunk's are
 // prefetched into L2 meanwhile: one CTA fits an SM, so the chain of chunks is otherwise
-// paced by global-load latency.
-template <int DK, typename Tg>
+// paced by global-load latency.  Both products run as TF32 warp tiles (kSplit: three split
+// products at fp32 accuracy, for fp32 inputs).
+template <int DK, typename Tg, bool kSplit>
 __global__ void __launch_bounds__(kThreads) chunk_dstate_kernel(DStateArgs a) {
     constexpr int LD = DK + 4;
     extern __shared__ float4 smem4[];
-    float *sDS = reinterpret_cast<float *>(smem4);  // [DK][32]
-    float *sW = sDS + DK * kDvt;                    // [64][LD]
+    float *sDS = reinterpret_cast<float *>(smem4);  // [DK][kLdC]
+    float *sW = sDS + DK * kLdC;                    // [64][LD]
     float *sQg = sW + 64 * LD;                      // [64][LD]
     float *sKd = sQg + 64 * LD;                     // [64][LD]
-    float *sDO = sKd + 64 * LD;                     // [64][32]
-    float *sDE = sDO + 64 * kDvt;                   // [64][32]
-    float *sP = sDE + 64 * kDvt;                    // [64][kLdP]
+    float *sDO = sKd + 64 * LD;                     // [64][kLdC]
+    float *sDE = sDO + 64 * kLdC;                   // [64][kLdC]
+    float *sP = sDE + 64 * kLdC;                    // [64][kLdP]
     float *sGam = sP + 64 * kLdP;                   // [DK]
 
     const int tiles = a.dv / kDvt;
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) chunk_dstate_kernel(DStateArgs a) {
     const Tg *dout = (const Tg *)a.d_out;
 
     for (int i = rg; i < DK; i += 8)
-        sDS[i * kDvt + j] = a.d_final ? a.d_final[(bh * DK + i) * dv + col] : 0.f;
+        sDS[i * kLdC + j] = a.d_final ? a.d_final[(bh * DK + i) * dv + col] : 0.f;
 
     for (int c = NC - 1; c >= 0; --c) {
         const int64_t n = bh * NC + c;
@@ -162,9 +165,9 @@ __global__ void __launch_bounds__(kThreads) chunk_dstate_kernel(DStateArgs a) {
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                if (tid + u * kThreads < C * kDvt) sDO[tid + u * kThreads] = dov[u];
+                if (tid + u * kThreads < C * kDvt) sDO[((tid + u * kThreads) / kDvt) * kLdC + (tid + u * kThreads) % kDvt] = dov[u];
         }
-        for (int i = rg; i < DK; i += 8) a.ws.dsc[(n * DK + i) * dv + col] = sDS[i * kDvt + j];
+        for (int i = rg; i < DK; i += 8) a.ws.dsc[(n * DK + i) * dv + col] = sDS[i * kLdC + j];
         cp_async_commit_wait_all();
         __syncthreads();
         if (c > 0) {   // the next chunk's operands into L2 while this one computes
@@ -179,66 +182,54 @@ __global__ void __launch_bounds__(kThreads) chunk_dstate_kernel(DStateArgs a) {
                                                                jt * kDvt));
             }
         }
-        // dE = P^T dO + Kd dS: warp rg owns rows 8 rg .. 8 rg + 7 (eight independent sums
-        // per thread), so that one float4 broadcast load serves four rows.  P is lower
-        // triangular (zeros stored above the diagonal): rows r >= 8 rg need s >= 8 rg only.
+        // dE [C][32] = P^T dO + Kd dS (P lower triangular): warp w, rows 16 (w % 4) ..,
+        // columns 16 (w / 4) .. (two tiles of 8)
+        const int g8 = j >> 2, t4 = j & 3;
         {
-            const int r0 = 8 * rg;
-            float e[8];
-#pragma unroll
-            for (int m = 0; m < 8; ++m) e[m] = 0.f;
+            const int r0 = 16 * (rg & 3), n0 = 16 * (rg >> 2);
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             if (r0 < C) {
-                for (int s = r0; s < C; ++s) {
-                    const float d = sDO[s * kDvt + j];
-                    const float4 p0 = *reinterpret_cast<const float4 *>(sP + s * kLdP + r0);
-                    const float4 p1 = *reinterpret_cast<const float4 *>(sP + s * kLdP + r0 + 4);
-                    e[0] = fmaf(p0.x, d, e[0]); e[1] = fmaf(p0.y, d, e[1]);
-                    e[2] = fmaf(p0.z, d, e[2]); e[3] = fmaf(p0.w, d, e[3]);
-                    e[4] = fmaf(p1.x, d, e[4]); e[5] = fmaf(p1.y, d, e[5]);
-                    e[6] = fmaf(p1.z, d, e[6]); e[7] = fmaf(p1.w, d, e[7]);
-                }
-                for (int i = 0; i < DK; i += 4) {
-                    const float d0 = sDS[i * kDvt + j], d1 = sDS[(i + 1) * kDvt + j];
-                    const float d2 = sDS[(i + 2) * kDvt + j], d3 = sDS[(i + 3) * kDvt + j];
+                tc::rows_times_cols<kSplit>(acc, 2, [&](int rr, int kk) { return sP[kk * kLdP + rr]; },
+                                            [&](int kk, int nn) { return sDO[kk * kLdC + nn]; }, r0, n0, C, g8, t4);
+                tc::rows_times_cols<kSplit>(acc, 2, [&](int rr, int kk) { return sKd[rr * LD + kk]; },
+                                            [&](int kk, int nn) { return sDS[kk * kLdC + nn]; }, r0, n0, DK, g8, t4);
 #pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        const float4 kd = *reinterpret_cast<const float4 *>(sKd + (r0 + m) * LD + i);
-                        e[m] = fmaf(kd.x, d0, fmaf(kd.y, d1, fmaf(kd.z, d2, fmaf(kd.w, d3, e[m]))));
-                    }
-                }
+                for (int t = 0; t < 2; ++t)
 #pragma unroll
-                for (int m = 0; m < 8; ++m)
-                    if (r0 + m < C) sDE[(r0 + m) * kDvt + j] = e[m];
+                    for (int u = 0; u < 4; ++u)
+                        sDE[(r0 + g8 + 8 * (u >> 1)) * kLdC + n0 + 8 * t + 2 * t4 + (u & 1)] = acc[t][u];
             }
         }
         __syncthreads();
-        // dS <- Diag(gamma) dS + (Q*G)^T dO - W^T dE: warp rg owns the NR contiguous rows
-        // i = NR rg .. NR rg + NR - 1 of column j (own entries only), float4 broadcasts
+        // dS <- Diag(gamma) dS + (Q*G)^T dO - W^T dE  [DK][32]: warp w owns rows DK/8 w ..
+        // (tiles of 16 rows x 8 columns; its own entries only, in place)
         {
-            constexpr int NR = DK / 8;
-            const int i0 = NR * rg;
-            float acc[NR];
+            constexpr int RB = DK / 16;   // row blocks: one or two per warp (DK = 64, 128)
+            for (int rb = rg; rb < RB; rb += 8) {
+                const int i0 = 16 * rb;
+                float acc[4][4];
 #pragma unroll
-            for (int m = 0; m < NR; ++m) acc[m] = sGam[i0 + m] * sDS[(i0 + m) * kDvt + j];
-            for (int r = 0; r < C; ++r) {
-                const float d = sDO[r * kDvt + j], de = sDE[r * kDvt + j];
+                for (int t = 0; t < 4; ++t)
 #pragma unroll
-                for (int q = 0; q < NR; q += 4) {
-                    const float4 qg = *reinterpret_cast<const float4 *>(sQg + r * LD + i0 + q);
-                    const float4 w = *reinterpret_cast<const float4 *>(sW + r * LD + i0 + q);
-                    acc[q] = fmaf(qg.x, d, fmaf(-w.x, de, acc[q]));
-                    acc[q + 1] = fmaf(qg.y, d, fmaf(-w.y, de, acc[q + 1]));
-                    acc[q + 2] = fmaf(qg.z, d, fmaf(-w.z, de, acc[q + 2]));
-                    acc[q + 3] = fmaf(qg.w, d, fmaf(-w.w, de, acc[q + 3]));
-                }
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = i0 + g8 + 8 * (u >> 1), jj = 8 * t + 2 * t4 + (u & 1);
+                        acc[t][u] = sGam[i] * sDS[i * kLdC + jj];
+                    }
+                tc::rows_times_cols<kSplit>(acc, 4, [&](int ii, int kk) { return sQg[kk * LD + ii]; },
+                                            [&](int kk, int nn) { return sDO[kk * kLdC + nn]; }, i0, 0, C, g8, t4);
+                tc::rows_times_cols<kSplit>(acc, 4, [&](int ii, int kk) { return -sW[kk * LD + ii]; },
+                                            [&](int kk, int nn) { return sDE[kk * kLdC + nn]; }, i0, 0, C, g8, t4);
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        sDS[(i0 + g8 + 8 * (u >> 1)) * kLdC + 8 * t + 2 * t4 + (u & 1)] = acc[t][u];
             }
-#pragma unroll
-            for (int m = 0; m < NR; ++m) sDS[(i0 + m) * kDvt + j] = acc[m];
         }
     }
     if (a.d_init) {
         __syncthreads();
-        for (int i = rg; i < DK; i += 8) a.d_init[(bh * DK + i) * dv + col] = sDS[i * kDvt + j];
+        for (int i = rg; i < DK; i += 8) a.d_init[(bh * DK + i) * dv + col] = sDS[i * kLdC + j];
     }
 }
 
@@ -741,12 +732,13 @@ template <int DK, typename Tin, typename Tg>
 int launch_bwd_t(const DStateArgs &da, const GradArgs &ga, int64_t nstate, int64_t ngrad,
                  cudaStream_t stream) {
     const size_t ds = dstate_smem_bytes(DK), gs = grad_smem_bytes(DK, ga.dv_);
-    if (cudaFuncSetAttribute(chunk_dstate_kernel<DK, Tg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    constexpr bool kSplit = sizeof(Tin) == 4;
+    if (cudaFuncSetAttribute(chunk_dstate_kernel<DK, Tg, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)ds) != cudaSuccess ||
         cudaFuncSetAttribute(chunk_grad_kernel<DK, Tin, Tg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)gs) != cudaSuccess)
         return kErrCuda;
-    chunk_dstate_kernel<DK, Tg><<<(unsigned)nstate, kThreads, ds, stream>>>(da);
+    chunk_dstate_kernel<DK, Tg, kSplit><<<(unsigned)nstate, kThreads, ds, stream>>>(da);
     if (ngrad > 0) chunk_grad_kernel<DK, Tin, Tg><<<(unsigned)ngrad, kGThreads, gs, stream>>>(ga);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
