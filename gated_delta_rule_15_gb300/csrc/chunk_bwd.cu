@@ -301,7 +301,6 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     const float *dSC = a.ws.dsc + n * (int64_t)DK * dv;
     const float *Wn = a.ws.fw.W + n * (int64_t)C * DK;
     const float *Un = a.ws.fw.U + n * (int64_t)C * dv;
-    const float *Kdn = a.ws.fw.Kd + n * (int64_t)C * DK;
     const int r = tid / kParts, part = tid % kParts;
     const bool row_ok = r < C;
     const int lds = dv + 4;
@@ -340,6 +339,15 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         __syncthreads();
     };
 
+    // the chunk's S0 and dS_C (staged later by slices), U (phase 1) and v rows (phase 4)
+    // into L2
+    if (tid == 0) {
+        prefetch_l2(S0, (uint32_t)(DK * dv * 4));
+        prefetch_l2(dSC, (uint32_t)(DK * dv * 4));
+        prefetch_l2(Un, (uint32_t)(C * dv * 4));
+    } else if (tid >= 32 && tid < 32 + Lc) {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(v + tok(tid - 32) * dv));
+    }
     // ---- 0. inputs (rows past the sequence: zero, log alpha 0)
     //      (four elements per load, several loads in flight per thread)
 #pragma unroll 4
@@ -392,11 +400,16 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     // ---- 1. E = U - W S0 (tiles, W read from the workspace); dq, dg from (dO S0^T)_ri;
     //         S0 staged by slices of kSlice rows
     acc_zero();
+    for (int idx = tid; idx < C * (DK / 4); idx += kGThreads) {   // W over sE until E is formed
+        const int rr = idx / (DK / 4), c4 = 4 * (idx % (DK / 4));
+        cp_async16(sE + rr * ldw + c4, Wn + rr * DK + c4);
+    }
+    cp_async_commit_wait_all();
     for (int i0 = 0; i0 < DK; i0 += kSlice) {
         stage(S0, i0);
         slice_products(sX, ldw);   // (dO S0^T) over the slice
         if (own)
-            tc::rows_times_cols<kSplit>(acc, ont, [&](int rr, int kk) { return Wn[rr * DK + i0 + kk]; },
+            tc::rows_times_cols<kSplit>(acc, ont, [&](int rr, int kk) { return sE[rr * ldw + i0 + kk]; },
                             [&](int kk, int nn) { return sS[kk * lds + nn]; }, orb, ocn, kSlice, g8, t4);
         if (!row_ok) continue;
 #pragma unroll
@@ -409,6 +422,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
             ag[m] = fmaf(sQ[r * LDK + i] * e, acc, ag[m]);
         }
     }
+    __syncthreads();   // every tile has read W
     if (own)
 #pragma unroll
         for (int t = 0; t < 4; ++t)
@@ -426,7 +440,9 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     for (int i0 = 0; i0 < DK; i0 += kSlice) {
         stage(dSC, i0);
         if (own)
-            tc::rows_times_cols<kSplit>(acc, ont, [&](int rr, int kk) { return Kdn[rr * DK + i0 + kk]; },
+            tc::rows_times_cols<kSplit>(acc, ont, [&](int rr, int kk) {   // Kd = k exp(g_C - g)
+                                    const int i = i0 + kk;
+                                    return sK[rr * LDK + i] * __expf(sG[(C - 1) * LDK + i] - sG[rr * LDK + i]); },
                             [&](int kk, int nn) { return sS[kk * lds + nn]; }, orb, ocn, kSlice, g8, t4);
     }
     __syncthreads();
