@@ -36,8 +36,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kLdA = 65;   // padded row stride of [64][64] tiles
 constexpr int kLdP = 68;   // row stride of the reverse pass's P tile (16-byte rows)
-constexpr int kDvt = 32;   // state columns per CTA of the reverse pass
-constexpr int kLdC = kDvt + 8;   // row stride of the reverse pass's 32-column tiles (conflict-free
+constexpr int kDvt = 64;   // state columns per CTA of the reverse pass
+constexpr int kLdC = kDvt + 8;   // row stride of the reverse pass's column tiles (conflict-free
                                  // tensor-core fragments)
 constexpr int kSlice = 32; // rows of a [dk][dv] state matrix staged at a time
 constexpr int kGThreads = 512;   // per-chunk gradient kernel: 8 threads per token row
@@ -104,7 +104,9 @@ size_t dstate_smem_bytes(int dk) {
 
 // Reverse state-gradient pass: dS starts as d_final; for each chunk, last first, it is
 // stored as that chunk's dS_C, then  dE = P^T dO + Kd dS,  dS <- Diag(gamma) dS + (Q*G)^T dO
-// - W^T dE.  Column j of dS only meets column j of dO, so a CTA owns 32 columns.  A chunk's
+// - W^T dE.  Column j of dS only meets column j of dO, so a CTA owns 64 columns (every
+// (b, h) in at most two rounds of CTAs over the GPU, each reading the chunk's operands
+// once for its 64 columns).  A chunk's
 // operands arrive by 16-byte asynchronous copies behind one wait, and the next chunk's are
 // prefetched into L2 meanwhile: one CTA fits an SM, so the chain of chunks is otherwise
 // paced by global-load latency.  Both products run as TF32 warp tiles (kSplit: three split
@@ -132,7 +134,8 @@ __global__ void __launch_bounds__(kThreads) chunk_dstate_kernel(DStateArgs a) {
     const Tg *dout = (const Tg *)a.d_out;
 
     for (int i = rg; i < DK; i += 8)
-        sDS[i * kLdC + j] = a.d_final ? a.d_final[(bh * DK + i) * dv + col] : 0.f;
+        for (int jj = j; jj < kDvt; jj += 32)
+            sDS[i * kLdC + jj] = a.d_final ? a.d_final[(bh * DK + i) * dv + col + jj - j] : 0.f;
 
     for (int c = NC - 1; c >= 0; --c) {
         const int64_t n = bh * NC + c;
@@ -155,19 +158,21 @@ __global__ void __launch_bounds__(kThreads) chunk_dstate_kernel(DStateArgs a) {
             cp_async16(sP + r * kLdP + c4, P + r * C + c4);
         }
         for (int idx = tid; idx < DK / 4; idx += kThreads) cp_async16(sGam + 4 * idx, gam + 4 * idx);
-        {   // dO's 32 columns: every load of this thread issued before its stores
-            float dov[8];   // C * kDvt / kThreads = C / 8 <= 8
+        {   // dO's kDvt columns: every load of this thread issued before its stores
+            constexpr int kPer = 64 * kDvt / kThreads;   // >= C * kDvt / kThreads
+            float dov[kPer];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < kPer; ++u) {
                 const int idx = tid + u * kThreads, r = idx / kDvt, jj = idx % kDvt;
                 dov[u] = (idx < C * kDvt && r < Lc)
                              ? to_f32(dout[((b * a.T + t0 + r) * a.H + h) * dv + jt * kDvt + jj]) : 0.f;
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < kPer; ++u)
                 if (tid + u * kThreads < C * kDvt) sDO[((tid + u * kThreads) / kDvt) * kLdC + (tid + u * kThreads) % kDvt] = dov[u];
         }
-        for (int i = rg; i < DK; i += 8) a.ws.dsc[(n * DK + i) * dv + col] = sDS[i * kLdC + j];
+        for (int i = rg; i < DK; i += 8)
+            for (int jj = j; jj < kDvt; jj += 32) a.ws.dsc[(n * DK + i) * dv + col + jj - j] = sDS[i * kLdC + jj];
         cp_async_commit_wait_all();
         __syncthreads();
         if (c > 0) {   // the next chunk's operands into L2 while this one computes
@@ -177,59 +182,65 @@ __global__ void __launch_bounds__(kThreads) chunk_dstate_kernel(DStateArgs a) {
                 prefetch_l2(Kd - C * DK, (uint32_t)(C * DK * 4));
                 prefetch_l2(P - C * C, (uint32_t)(C * C * 4));
             } else if (tid > 32 && tid <= 32 + C && t0 - C + (tid - 33) < a.T) {
-                const int r = tid - 33;   // dO rows of the next chunk (this CTA's 64 bytes)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(dout + ((b * a.T + t0 - C + r) * a.H + h) * dv +
-                                                               jt * kDvt));
+                const int r = tid - 33;   // dO rows of the next chunk (this CTA's columns)
+                const Tg *row = dout + ((b * a.T + t0 - C + r) * a.H + h) * dv + jt * kDvt;
+                for (int e = 0; e < kDvt; e += 128 / (int)sizeof(Tg))
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(row + e));
             }
         }
-        // dE [C][32] = P^T dO + Kd dS (P lower triangular): warp w, rows 16 (w % 4) ..,
-        // columns 16 (w / 4) .. (two tiles of 8)
+        // dE [C][kDvt] = P^T dO + Kd dS (P lower triangular): warp w, rows 16 (w % 4) ..,
+        // columns kDvt/2 (w / 4) .. (four tiles of 8)
         const int g8 = j >> 2, t4 = j & 3;
         {
-            const int r0 = 16 * (rg & 3), n0 = 16 * (rg >> 2);
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            constexpr int NT = kDvt / 16;
+            const int r0 = 16 * (rg & 3), n0 = (kDvt / 2) * (rg >> 2);
+            float acc[NT][4];
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) acc[t][u] = 0.f;
             if (r0 < C) {
-                tc::rows_times_cols<kSplit>(acc, 2, [&](int rr, int kk) { return sP[kk * kLdP + rr]; },
+                tc::rows_times_cols<kSplit>(acc, NT, [&](int rr, int kk) { return sP[kk * kLdP + rr]; },
                                             [&](int kk, int nn) { return sDO[kk * kLdC + nn]; }, r0, n0, C, g8, t4);
-                tc::rows_times_cols<kSplit>(acc, 2, [&](int rr, int kk) { return sKd[rr * LD + kk]; },
+                tc::rows_times_cols<kSplit>(acc, NT, [&](int rr, int kk) { return sKd[rr * LD + kk]; },
                                             [&](int kk, int nn) { return sDS[kk * kLdC + nn]; }, r0, n0, DK, g8, t4);
 #pragma unroll
-                for (int t = 0; t < 2; ++t)
+                for (int t = 0; t < NT; ++t)
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
                         sDE[(r0 + g8 + 8 * (u >> 1)) * kLdC + n0 + 8 * t + 2 * t4 + (u & 1)] = acc[t][u];
             }
         }
         __syncthreads();
-        // dS <- Diag(gamma) dS + (Q*G)^T dO - W^T dE  [DK][32]: warp w owns rows DK/8 w ..
-        // (tiles of 16 rows x 8 columns; its own entries only, in place)
+        // dS <- Diag(gamma) dS + (Q*G)^T dO - W^T dE  [DK][kDvt] (its own entries only, in
+        // place): DK = 128, warp w owns row block w and all 8 column tiles; DK = 64, row block
+        // w % 4 and the column half w / 4
         {
-            constexpr int RB = DK / 16;   // row blocks: one or two per warp (DK = 64, 128)
-            for (int rb = rg; rb < RB; rb += 8) {
-                const int i0 = 16 * rb;
-                float acc[4][4];
+            constexpr int RB = DK / 16, NTS = RB * (kDvt / 8) / 8;   // tiles per warp
+            const int i0 = 16 * (rg % RB), n0 = 8 * NTS * (rg / RB);
+            float acc[NTS][4];
 #pragma unroll
-                for (int t = 0; t < 4; ++t)
+            for (int t = 0; t < NTS; ++t)
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int i = i0 + g8 + 8 * (u >> 1), jj = 8 * t + 2 * t4 + (u & 1);
-                        acc[t][u] = sGam[i] * sDS[i * kLdC + jj];
-                    }
-                tc::rows_times_cols<kSplit>(acc, 4, [&](int ii, int kk) { return sQg[kk * LD + ii]; },
-                                            [&](int kk, int nn) { return sDO[kk * kLdC + nn]; }, i0, 0, C, g8, t4);
-                tc::rows_times_cols<kSplit>(acc, 4, [&](int ii, int kk) { return -sW[kk * LD + ii]; },
-                                            [&](int kk, int nn) { return sDE[kk * kLdC + nn]; }, i0, 0, C, g8, t4);
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + g8 + 8 * (u >> 1), jj = n0 + 8 * t + 2 * t4 + (u & 1);
+                    acc[t][u] = sGam[i] * sDS[i * kLdC + jj];
+                }
+            tc::rows_times_cols<kSplit>(acc, NTS, [&](int ii, int kk) { return sQg[kk * LD + ii]; },
+                                        [&](int kk, int nn) { return sDO[kk * kLdC + nn]; }, i0, n0, C, g8, t4);
+            tc::rows_times_cols<kSplit>(acc, NTS, [&](int ii, int kk) { return -sW[kk * LD + ii]; },
+                                        [&](int kk, int nn) { return sDE[kk * kLdC + nn]; }, i0, n0, C, g8, t4);
 #pragma unroll
-                for (int t = 0; t < 4; ++t)
+            for (int t = 0; t < NTS; ++t)
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        sDS[(i0 + g8 + 8 * (u >> 1)) * kLdC + 8 * t + 2 * t4 + (u & 1)] = acc[t][u];
-            }
+                for (int u = 0; u < 4; ++u)
+                    sDS[(i0 + g8 + 8 * (u >> 1)) * kLdC + n0 + 8 * t + 2 * t4 + (u & 1)] = acc[t][u];
         }
     }
     if (a.d_init) {
         __syncthreads();
-        for (int i = rg; i < DK; i += 8) a.d_init[(bh * DK + i) * dv + col] = sDS[i * kLdC + j];
+        for (int i = rg; i < DK; i += 8)
+            for (int jj = j; jj < kDvt; jj += 32) a.d_init[(bh * DK + i) * dv + col + jj - j] = sDS[i * kLdC + jj];
     }
 }
 
