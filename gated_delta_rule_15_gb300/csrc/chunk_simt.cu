@@ -68,8 +68,12 @@ struct StateArgs {
                      // otherwise); with it, `out` may be NULL (no outputs written)
 };
 
-size_t prep_smem_bytes(int dk) {
-    return sizeof(float) * (size_t)(3 * 64 * kLd + 64 * dk + 16 * dk + 2 * 64 * kLdA + 64 + 64 + 1024 + 64);
+// The per-channel gate needs its [64][dk] cumulative decays, the sub-chunk pair factors and
+// a separate right-factor tile; the scalar gate and no gate take the right factors over q's
+// tile (dead once P is formed), which lets two CTAs share an SM.
+size_t prep_smem_bytes(int dk, int gate) {
+    const size_t tiles = gate == 2 ? 3 * 64 * kLd + 64 * dk + 16 * dk : 2 * 64 * kLd;
+    return sizeof(float) * (tiles + 2 * 64 * kLdA + 64 + 64 + 1024 + 64);
 }
 
 // out(r, n) (r, n < 16) = sum_{k < 16 nk} L(r, k) R(k, n) by one warp in fp32; lane owns row
@@ -154,12 +158,13 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
     // results are held to the bf16 bound: one TF32 product (~2^-11 relative)
     constexpr bool kSplit = sizeof(Tin) == 4;
     extern __shared__ float4 smem4[];
+    const bool chan = a.gate == 2;
     float *sK = reinterpret_cast<float *>(smem4);  // k, then left factor of A
     float *sQ = sK + 64 * kLd;                     // q, then left factor of P
-    float *sR = sQ + 64 * kLd;                     // right factor, then b*K*G, then b*V
+    float *sR = chan ? sQ + 64 * kLd : sQ;         // right factor, then b*K*G, then b*V
     float *sG = sR + 64 * kLd;                     // [64][DK] cumulative log decay (channel)
     float *sF = sG + 64 * DK;                      // [16][DK] sub-chunk pair factors
-    float *sA = sF + 16 * DK;                      // [64][kLdA] A
+    float *sA = chan ? sF + 16 * DK : sQ + 64 * kLd;   // [64][kLdA] A
     float *sT = sA + 64 * kLdA;                    // [64][kLdA] T = (I + A)^-1
     float *sB = sT + 64 * kLdA;                    // [64] beta
     float *sg = sB + 64;                           // [64] cumulative log decay (scalar)
@@ -557,9 +562,11 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(StateArgs a) {
 
 template <int DK, typename Tin, typename Tout>
 int launch_simt_t(const PrepArgs &pa, const StateArgs &sa, cudaStream_t stream, bool prep_only) {
-    const size_t ps = prep_smem_bytes(DK), ss = state_smem_bytes(DK);
-    if (cudaFuncSetAttribute(chunk_prep_kernel<DK, Tin>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps) != cudaSuccess)
+    const size_t ps = prep_smem_bytes(DK, pa.gate), ss = state_smem_bytes(DK);
+    if (cudaFuncSetAttribute(chunk_prep_kernel<DK, Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)prep_smem_bytes(DK, 2)) != cudaSuccess ||
+        cudaFuncSetAttribute(chunk_prep_kernel<DK, Tin>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             100) != cudaSuccess)
         return kErrCuda;
     if (cudaFuncSetAttribute(chunk_state_kernel<DK, Tout>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss) != cudaSuccess)
