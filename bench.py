@@ -37,7 +37,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (128 chains) with half its head-tokens, and the kernel's traffic is proportional to
 # head-tokens, so the figure is twice the captured one.  Valid only while the kernel
 # sources hash to `src`; otherwise the bench reports null.
-TRAFFIC = {"chunk_fwd": {"bytes": 2 * (203065856 + 49730048), "src": "fa6cf1e75d2a8e78"}}
+TRAFFIC = {"chunk_fwd": {"bytes": 2 * (203061504 + 49720576), "src": "30e4fda208944912"}}
 
 
 def peaks():

@@ -134,13 +134,16 @@ struct TcArgs {
     float *ckpt;
 };
 
-// FUSED: the fused neighbours' code is compiled in (each still switched by a.fuse); the
-// plain instantiation carries none of it.
-template <typename Tout, int GATE, bool FUSED>
+// MODE 0: plain.  MODE 1 (FUSED): the fused neighbours' code is compiled in (each still
+// switched by a.fuse).  MODE 2 (CKPT): no outputs; the state at every chunk's start goes to
+// a.ckpt (the backward's recompute).  Each instantiation carries only its own code, which
+// keeps the register pressure of the others down.
+template <typename Tout, int GATE, int MODE>
 __global__ void __launch_bounds__(kCtaThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
                 const __grid_constant__ CUtensorMap tz, const TcArgs a) {
+    constexpr bool FUSED = MODE == 1, CKPT = MODE == 2;
     extern __shared__ unsigned char dsm_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
     // mbarriers: TMA stages; per MMA group its completion (committed by the MMA warp) and,
@@ -158,7 +161,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     int bh = blockIdx.x, c_begin = 0, c_end = a.NC;
     const float *init_ptr = a.init_state ? a.init_state + (size_t)blockIdx.x * 16384 : nullptr;
     float *fin_ptr = a.final_state ? a.final_state + (size_t)blockIdx.x * 16384 : nullptr;
-    bool init_identity = false, zero_u = false, outputs = !(FUSED && a.ckpt);
+    bool init_identity = false, zero_u = false, outputs = !CKPT;
     if (a.role != 0) {
         const int idx = a.role == 1 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
         const int seg = idx % a.nseg;
@@ -646,7 +649,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 const int i0 = 64 * half + 32 * part;
                 tmem_ld32(tm + TM_S + i0, v);
                 tmem_wait_ld();
-                if (FUSED && a.ckpt && a.role != 1) {   // S[i][j] at this chunk's start
+                if (CKPT && a.role != 1) {   // S[i][j] at this chunk's start
                     float *ck = a.ckpt + ((size_t)bh * a.NC + c_begin + it) * 16384 + (size_t)i0 * 128 + row;
 #pragma unroll
                     for (int u = 0; u < 32; ++u) ck[(size_t)u * 128] = v[u];
@@ -904,15 +907,15 @@ bool make_map(CUtensorMap *m, const void *base, int64_t B, int64_t T, int64_t H,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Tout, int GATE, bool FUSED>
+template <typename Tout, int GATE, int MODE>
 int launch_f(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
              const CUtensorMap &mo, const CUtensorMap &mz, const TcArgs &ta, unsigned grid,
              cudaStream_t stream) {
-    const int smem = (int)(FUSED ? SM_TOTAL_FUSED : SM_TOTAL) + 1024;
-    if (cudaFuncSetAttribute(chunk_tc_kernel<Tout, GATE, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const int smem = (int)(MODE == 1 ? SM_TOTAL_FUSED : SM_TOTAL) + 1024;
+    if (cudaFuncSetAttribute(chunk_tc_kernel<Tout, GATE, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
         return kErrCuda;
-    chunk_tc_kernel<Tout, GATE, FUSED><<<grid, kCtaThreads, smem, stream>>>(mq, mk, mv, mo, mz, ta);
+    chunk_tc_kernel<Tout, GATE, MODE><<<grid, kCtaThreads, smem, stream>>>(mq, mk, mv, mo, mz, ta);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
@@ -920,8 +923,9 @@ template <typename Tout, int GATE>
 int launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
              const CUtensorMap &mo, const CUtensorMap &mz, const TcArgs &ta, unsigned grid,
              cudaStream_t stream) {
-    return (ta.fuse || ta.ckpt) ? launch_f<Tout, GATE, true>(mq, mk, mv, mo, mz, ta, grid, stream)
-                                : launch_f<Tout, GATE, false>(mq, mk, mv, mo, mz, ta, grid, stream);
+    if (ta.ckpt) return launch_f<Tout, GATE, 2>(mq, mk, mv, mo, mz, ta, grid, stream);
+    return ta.fuse ? launch_f<Tout, GATE, 1>(mq, mk, mv, mo, mz, ta, grid, stream)
+                   : launch_f<Tout, GATE, 0>(mq, mk, mv, mo, mz, ta, grid, stream);
 }
 
 }  // namespace
