@@ -341,12 +341,32 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
         __syncthreads();
     };
     // rows i0 .. i0 + kSlice - 1 of a [DK][dv] matrix into sS (all threads; barriers around)
-    auto stage = [&](const float *M, int i0) {
-        __syncthreads();
-        for (int idx = tid; idx < kSlice * (dv / 4); idx += kGThreads) {
-            const int ii = idx / (dv / 4), j4 = 4 * (idx % (dv / 4));
-            *reinterpret_cast<float4 *>(sS + ii * lds + j4) = load4(M + (i0 + ii) * dv + j4);
+    // The stages follow one fixed sequence: the slices of S0, of dS_C, of S0, of dS_C (phases
+    // 1, 2, 4, 4b).  Each stage stores the slice that the previous one loaded into registers
+    // and starts the loads of the next, which run while this slice is computed on.
+    const int nsl = DK / kSlice, nstages = 4 * nsl;
+    constexpr int kPf = kSlice * 128 / 4 / kGThreads;   // float4 per thread per slice (dv <= 128)
+    float4 pf[kPf];
+    int sn = 0;
+    auto load_slice = [&](int k) {
+        const float *M = ((k / nsl) & 1) ? dSC : S0;
+        const int i0 = (k % nsl) * kSlice;
+#pragma unroll
+        for (int u = 0; u < kPf; ++u) {
+            const int idx = tid + u * kGThreads, ii = idx / (dv / 4), j4 = 4 * (idx % (dv / 4));
+            if (idx < kSlice * (dv / 4)) pf[u] = load4(M + (i0 + ii) * dv + j4);
         }
+    };
+    auto stage = [&](const float *M, int i0) {   // (M, i0): the sequence's next slice
+        (void)M;
+        (void)i0;
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kPf; ++u) {
+            const int idx = tid + u * kGThreads, ii = idx / (dv / 4), j4 = 4 * (idx % (dv / 4));
+            if (idx < kSlice * (dv / 4)) *reinterpret_cast<float4 *>(sS + ii * lds + j4) = pf[u];
+        }
+        if (++sn < nstages) load_slice(sn);
         __syncthreads();
     };
 
@@ -359,6 +379,7 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
     } else if (tid >= 32 && tid < 32 + Lc) {
         asm volatile("prefetch.global.L2 [%0];" ::"l"(v + tok(tid - 32) * dv));
     }
+    load_slice(0);
     // ---- 0. inputs (rows past the sequence: zero, log alpha 0)
     //      (four elements per load, several loads in flight per thread)
 #pragma unroll 4
@@ -738,19 +759,32 @@ __global__ void __launch_bounds__(kGThreads) chunk_grad_kernel(GradArgs a) {
             }
         }
     } else {
-        for (int rr = tid; rr < C; rr += kGThreads) {
+        {   // row sums of dg: eight threads per row
+            const int rr = tid >> 3, p8 = tid & 7;
             float acc = 0.f;
-            for (int i = 0; i < DK; ++i) acc += sQ[rr * LDK + i];
-            sRed[rr] = acc;
+            if (rr < C)
+                for (int i = p8; i < DK; i += 8) acc += sQ[rr * LDK + i];
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+            if (rr < C && p8 == 0) sRed[rr] = acc;
         }
         __syncthreads();
-        if (tid == 0) {
-            float run = 0.f;
-            for (int i = 0; i < DK; ++i) run += sDgC[i];
-            for (int rr = C - 1; rr >= 0; --rr) {
-                run += sRed[rr];
-                if (rr < Lc) a.d_log_alpha[tok(rr)] = run;
+        if (warp == 0) {   // d log alpha_t = sum_i dg_C,i + sum_{r >= t} (row sum)_r: one warp
+            float tg = 0.f;
+            for (int i = lane; i < DK; i += 32) tg += sDgC[i];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) tg += __shfl_xor_sync(0xffffffffu, tg, o);
+            const int r0 = 2 * lane;   // rows r0, r0 + 1 (C <= 64)
+            const float v0 = r0 < C ? sRed[r0] : 0.f, v1 = r0 + 1 < C ? sRed[r0 + 1] : 0.f;
+            float suf = v0 + v1;   // suffix sums over lanes >= this one
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_down_sync(0xffffffffu, suf, o);
+                if (lane + o < 32) suf += y;
             }
+            if (r0 < Lc) a.d_log_alpha[tok(r0)] = tg + suf;
+            if (r0 + 1 < Lc) a.d_log_alpha[tok(r0 + 1)] = tg + suf - v0;
         }
     }
 }
