@@ -262,11 +262,25 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(PrepArgs a) {
     // 3. G_C, K*G_C/G and Q*G to the workspace.
     const int64_t wofs = n * (int64_t)C * DK;
     for (int ch = tid; ch < DK; ch += kThreads) a.ws.gam[n * DK + ch] = expf(G(C - 1, ch));
-    for (int idx = tid; idx < C * DK; idx += kThreads) {
-        const int r = idx / DK, ch = idx % DK;
-        const float gr = G(r, ch);
-        a.ws.Kd[wofs + idx] = sK[r * kLd + ch] * expf(G(C - 1, ch) - gr);
-        a.ws.Qg[wofs + idx] = sQ[r * kLd + ch] * expf(gr);
+    if (gate == 2) {
+        for (int idx = tid; idx < C * DK; idx += kThreads) {
+            const int r = idx / DK, ch = idx % DK;
+            const float gr = G(r, ch);
+            a.ws.Kd[wofs + idx] = sK[r * kLd + ch] * expf(G(C - 1, ch) - gr);
+            a.ws.Qg[wofs + idx] = sQ[r * kLd + ch] * expf(gr);
+        }
+    } else {   // one decay per row: two exponentials per row, four channels per store
+#pragma unroll 4
+        for (int idx = tid; idx < C * (DK / 4); idx += kThreads) {
+            const int r = idx / (DK / 4), c4 = 4 * (idx % (DK / 4));
+            const float fk = expf(sg[C - 1] - sg[r]), fq = expf(sg[r]);
+            const float4 kk = *reinterpret_cast<const float4 *>(sK + r * kLd + c4);
+            const float4 qq = *reinterpret_cast<const float4 *>(sQ + r * kLd + c4);
+            *reinterpret_cast<float4 *>(a.ws.Kd + wofs + r * DK + c4) =
+                make_float4(kk.x * fk, kk.y * fk, kk.z * fk, kk.w * fk);
+            *reinterpret_cast<float4 *>(a.ws.Qg + wofs + r * DK + c4) =
+                make_float4(qq.x * fq, qq.y * fq, qq.z * fq, qq.w * fq);
+        }
     }
     __syncthreads();
 
