@@ -1,6 +1,7 @@
-// chunk_bwd.cu -- backward of the chunkwise forward on the fp32 CUDA cores: the gradients of
+// chunk_bwd.cu -- backward of the chunkwise forward: the gradients of
 // L = <d_out, out> + <d_final, final_state> with respect to q, k, v, log alpha, beta and the
-// initial state.
+// initial state, with fp32 sums and every contraction as a TF32 warp tile (tc_common.cuh:
+// three split products at fp32 accuracy for fp32 inputs, one for bf16 inputs).
 //
 // The pages ask for chunkwise kernels for training (page "linear-attention gated-deltanet
 // guide", section 5) and print no backward; this one differentiates the chunk form of
@@ -22,7 +23,7 @@
 // Three steps after the CUDA-core forward has recomputed W, U, Q*G, Kd, P, gamma and T, and
 // a forward pass (the tensor-core kernel where it serves the problem, else the CUDA-core
 // state pass) the state at every chunk's start (the checkpoints):
-//   chunk_dstate_kernel  one CTA per (b, h, 32 state columns), chunks in reverse: stores
+//   chunk_dstate_kernel  one CTA per (b, h, 64 state columns), chunks in reverse: stores
 //                        dS_C of every chunk and returns dS0 of the first;
 //   chunk_grad_kernel    one CTA per (b, h, chunk), all chunks in parallel: every gradient
 //                        of the chunk's tokens.
