@@ -1,4 +1,5 @@
-// chunk_simt.cu -- chunkwise forward of the gated delta rule on the fp32 CUDA cores.
+// chunk_simt.cu -- chunkwise forward of the gated delta rule with fp32 sums: the path for every
+// configuration the tensor-core kernels do not take, and the backward's operand recompute.
 //
 // Chunk form (derived from the recurrence S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} +
 // b_t k_t v_t^T, o_t = S_t^T q_t of the page "NLP: linear attention summary", KDA section;
@@ -17,7 +18,11 @@
 // Two kernels:
 //   chunk_prep_kernel   one CTA per (b, h, chunk), all chunks in parallel: cumulative log
 //                       decay, A and P, the forward substitution for T, W and U; writes
-//                       W, U, P, Q*G, K*G_C/G and G_C to the workspace (fp32).
+//                       W, U, P, Q*G, K*G_C/G and G_C to the workspace (fp32).  For the
+//                       scalar gate and no gate, A, P, W and U are TF32 warp tiles
+//                       (tc_common.cuh: three split products at fp32 accuracy for fp32
+//                       inputs, one for bf16 inputs); the per-channel gate's A and P stay
+//                       per-thread fp32 dot products around the sub-chunk references.
 //   chunk_state_kernel  one CTA per (b, h, 32 state columns), sequential over chunks:
 //                       E = U - W S, O = (Q*G) S + P E, S <- Diag(G_C) S + (K*G_C/G)^T E.
 //
