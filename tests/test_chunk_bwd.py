@@ -1,7 +1,7 @@
 """GPU parity of dr_chunk_bwd (the backward of the chunk forward) against the fp64 oracle's
 reverse mode of the token loop, through the C ABI.
 
-Tolerance (the pages and the task fix none for gradients): fp32 inputs, max|g - g_ref| <=
+Tolerance (the pages fix none for gradients): fp32 inputs, max|g - g_ref| <=
 1e-4 max(1, RMS(g_ref)) per gradient (the forward's absolute bound for unit-scale values,
 scaled with gradients that sum many unit-scale terms); bf16 inputs, the forward's rule
 (max-abs/RMS <= 2e-2, half a bf16 ulp allowed on bf16-stored gradients)."""
