@@ -31,11 +31,14 @@ sys.path.insert(0, ROOT)
 METRIC = "tokens/s gated-delta chunk fwd (T=4096,H=16,d=128) & decode GB/s; % roofline"
 HEADLINE = "gdn_bf16_B8_H16_T4096_d128"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300 HBM3e datasheet bandwidth (GB/s): reported beside the measured-copy fraction, since
+# a streaming in-place kernel can move bytes slightly faster than the copy that measured
+# the peak.
+HBM_NOMINAL_GBS = 7900.0
 
 # DRAM traffic per launch (read + write bytes) of the dominant kernel, from one ncu capture
-# (profiles/chunk_tc_kernel_gdn_B8_T2048_H16.md): that case is the headline's launch shape
-# (128 chains) with half its head-tokens, and the kernel's traffic is proportional to
-# head-tokens, so the figure is twice the captured one.  Valid only while the kernel
+# of the headline's launch shape (128 chains) at half its head-tokens (B8 H16 T2048); the
+# kernel's traffic is proportional to head-tokens, so the figure is twice the captured one.  Valid only while the kernel
 # sources hash to `src`; otherwise the bench reports null.
 TRAFFIC = {"chunk_fwd": {"bytes": 2 * (203061504 + 49720576), "src": "30e4fda208944912"}}
 
@@ -410,6 +413,7 @@ def run_native(args):
         decode[name] = {"ms_per_step": round(dms, 5), "steps": wd.steps,
                         "gbs": db / (dms * 1e-3) / 1e9,
                         "hbm_frac": db / (dms * 1e-3) / 1e9 / hbm,
+                        "hbm_frac_nominal": db / (dms * 1e-3) / 1e9 / HBM_NOMINAL_GBS,
                         "tokens_per_s": wd.B / (dms * 1e-3),
                         "bytes_per_step": db}
 
@@ -451,35 +455,43 @@ def run_native(args):
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
     """The oracle as it stands, timed on this host's cores, on the native arm's workload,
-    metric and unit; each step is a bounded sample (2 whole (b, h) chains x T tokens)."""
+    metric and unit.  Each step is a bounded sample: one batch row of the workload (H whole
+    (b, h) chains x T tokens), the rows taken in turn, so that the oracle's tasks (one per
+    chain) cover the host's cores."""
     world, rank, _ = dist_setup()
     if rank != 0:
         return
     import oracle
     from gated_delta_rule_15_gb300 import inputs
     w = inputs.WORKLOADS[HEADLINE]
-    d = inputs.chunk_inputs(1, w.T, 2, w.dk, w.dv, gate=w.gate, dtype=w.dtype,
-                            init_state=w.init_state, seed=0)
+    d = inputs.workload_inputs(w)
     cores = oracle.default_threads()
-    run = lambda: oracle.forward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
-                                 d["init_state"], nthreads=cores)
+    rows = [0]
+
+    def run():
+        b = rows[0] % w.B
+        rows[0] += 1
+        pick = lambda t: None if t is None else t[b:b + 1]
+        s0 = None if d["init_state"] is None else d["init_state"][b:b + 1]
+        oracle.forward(pick(d["q"]), pick(d["k"]), pick(d["v"]), pick(d["log_alpha"]),
+                       pick(d["beta"]), s0, nthreads=cores)
+
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         run()
     dt = (time.perf_counter() - t0) / args.steps
-    ht = w.T * 2
-    value = ht / w.H / dt
+    value = w.T / dt          # tokens (of H heads each) per second
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (same recipe as the native arm)",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-                   "gate": w.gate, "sample_per_step": f"2 (b,h) chains x {w.T} tokens"},
+                   "gate": w.gate, "sample_per_step": f"1 batch row = {w.H} (b,h) chains x {w.T} tokens"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"2 whole (b,h) chains x T={w.T} of {w.name} per step"},
+                         "sample": f"one batch row ({w.H} whole (b,h) chains x T={w.T}) of {w.name} per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,

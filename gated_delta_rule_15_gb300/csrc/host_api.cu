@@ -177,6 +177,14 @@ extern "C" int dr_chunk_fwd_host(const dr_chunk_desc *desc, int pieces, const vo
     if (ok && final_state)
         ok = cudaMemcpyAsync(final_state, state, st_bytes, cudaMemcpyDeviceToHost, s_out) == cudaSuccess;
     if (ok) ok = cudaEventRecord(e_done, s_out) == cudaSuccess && cudaStreamWaitEvent(main, e_done, 0) == cudaSuccess;
+    if (!ok) {
+        // part of the work may be enqueued: `main` still waits for all of it, so that a
+        // caller who synchronises `stream` after the error may free or reuse the buffers
+        // (a stream whose event cannot be recorded is synchronised instead)
+        for (cudaStream_t s : {s_in, s_comp, s_out})
+            if (cudaEventRecord(e_done, s) != cudaSuccess || cudaStreamWaitEvent(main, e_done, 0) != cudaSuccess)
+                cudaStreamSynchronize(s);
+    }
     cleanup();
     if (!ok) return rc != kOk ? rc : kErrCuda;
     return kOk;

@@ -147,7 +147,7 @@ int dr_chunk_fwd(const dr_chunk_desc *desc,
  * copies, the state and the workspace; it must not be used by other work until `stream`
  * completes.  Streams and events are created for the call and released behind its work.
  * Returns the statuses of dr_chunk_fwd (DR_ERR_WORKSPACE for a missing or short `dev`); on
- * DR_ERR_CUDA part of the work may have been enqueued.
+ * DR_ERR_CUDA part of the work may have been enqueued; `stream` then still waits for all of it.
  */
 int dr_chunk_fwd_host_dev_bytes(const dr_chunk_desc *desc, int pieces, size_t *bytes);
 int dr_chunk_fwd_host(const dr_chunk_desc *desc, int pieces,

@@ -1,7 +1,7 @@
 """Run one kernel of the library a few times on a chosen workload, for profilers.
 
-    python -m gated_delta_rule_15_gb300.profile_case --what decode --B 128 --iters 3
-    python -m gated_delta_rule_15_gb300.profile_case --what chunk \
+    python profile_case.py --what decode --B 128 --iters 3
+    python profile_case.py --what chunk \
         --workload gdn_bf16_B8_H16_T4096_d128 --B 2 --iters 3
 
 Sizes default to the named workload; --B / --T / --H shrink it (keep inputs larger than
@@ -15,7 +15,7 @@ import dataclasses
 import os
 import sys
 
-sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
 
 
 def with_raw(make, fl):

@@ -19,6 +19,14 @@ import torch
 TOL_F32_ABS = 1e-4
 TOL_BF16_REL = 2e-2
 
+# Measured errors of the full-size cases, printed at the end of the session (conftest) and
+# written as JSON lines to $DR_ERROR_LOG when that is set.
+ERROR_LOG = []
+
+
+def record(case, what, **values):
+    ERROR_LOG.append({"case": case, "what": what, **{k: float(v) for k, v in values.items()}})
+
 
 def to_np(x):
     return x.detach().to("cpu", torch.float64).numpy() if isinstance(x, torch.Tensor) else x
@@ -46,6 +54,15 @@ def err(gpu, ref, dtype):
         return dev.max(), TOL_F32_ABS
     rms = np.sqrt((r ** 2).mean())
     return dev.max() / max(rms, 1e-30), TOL_BF16_REL
+
+
+def plain_err(gpu, ref):
+    """max |x_gpu - x_oracle| / RMS(x_oracle) with no representation allowance."""
+    g, r = to_np(gpu), np.asarray(ref, dtype=np.float64)
+    if g.size == 0:
+        return 0.0
+    rms = np.sqrt((r ** 2).mean())
+    return np.abs(g - r).max() / max(rms, 1e-30)
 
 
 def assert_close(gpu, ref, dtype, what=""):

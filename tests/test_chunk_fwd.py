@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from gated_delta_rule_15_gb300 import inputs
-from parity import assert_close
+from parity import assert_close, plain_err, record
 
 pytestmark = pytest.mark.gpu
 
@@ -132,24 +132,34 @@ def sampled_chains(w, n, seed=0):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("name,nsample", [
     ("gdn_bf16_B8_H16_T4096_d128", 6),
     ("kda_bf16_B4_H32_T8192_d128", 4),
     ("gdn_bf16_B1_H16_T65536_d128_init", 2)])
-def test_full_size_sampled_chains(dr, name, nsample):
+def test_full_size_sampled_chains(dr, name, nsample, out_dtype):
     """The workload at full size, in the launch configuration the benchmark times; the
-    oracle recomputes a sample of whole (b, h) chains."""
+    oracle recomputes a sample of whole (b, h) chains.  With an fp32-stored output the
+    plain rule applies (max |gpu - oracle| <= 2e-2 RMS, no representation allowance); with
+    the default bf16 output the allowance of half a bf16 ulp applies, and the plain error
+    is recorded beside it."""
     w = inputs.WORKLOADS[name]
     d = inputs.workload_inputs(w)
-    out, fin = run(dr, d, chunk=w.chunk)
+    odt = torch.float32 if out_dtype == "f32" else None
+    out, fin = run(dr, d, chunk=w.chunk, out_dtype=odt)
     out_h, fin_h = out.cpu(), fin.cpu()
+    worst = {"out": 0.0, "out_plain": 0.0, "state": 0.0}
     for b, h in sampled_chains(w, nsample):
         pick = lambda t: None if t is None else t[b:b + 1, :, h:h + 1].contiguous()
         s0 = None if d["init_state"] is None else d["init_state"][b:b + 1, h:h + 1]
         o_ref, f_ref = oracle.forward(pick(d["q"]), pick(d["k"]), pick(d["v"]),
                                       pick(d["log_alpha"]), pick(d["beta"]), s0)
-        assert_close(out_h[b:b + 1, :, h:h + 1], o_ref, "bf16", f"out chain {(b, h)}")
-        assert_close(fin_h[b:b + 1, h:h + 1], f_ref, "bf16", f"state chain {(b, h)}")
+        o_gpu = out_h[b:b + 1, :, h:h + 1]
+        worst["out"] = max(worst["out"], assert_close(o_gpu, o_ref, "bf16", f"out chain {(b, h)}"))
+        worst["out_plain"] = max(worst["out_plain"], plain_err(o_gpu, o_ref))
+        worst["state"] = max(worst["state"],
+                             assert_close(fin_h[b:b + 1, h:h + 1], f_ref, "bf16", f"state chain {(b, h)}"))
+    record(name, f"chunk_fwd out={out_dtype}", **worst)
 
 
 # ------------------------------------------------------------ tensor-core path

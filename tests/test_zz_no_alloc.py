@@ -36,8 +36,15 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
                              init_state=True, seed=41)
     d2 = inputs.chunk_inputs(3, 190, 2, 128, 128, gate="scalar", dtype="f32",
                              init_state=False, seed=42)
+    # Few long chains of the scalar gate take the segment-parallel form, whose segment
+    # states also live in the scratch; it runs third, on what the two calls before left.
+    d3 = inputs.chunk_inputs(1, 4096, 2, 128, 128, gate="scalar", dtype="bf16",
+                             init_state=True, seed=43)
+    desc3 = dr.chunk_desc(1, 4096, 2, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_SCALAR, 64)
+    assert dr.workspace_bytes(desc3) > 0
     _run_both(dr, d1, "bf16")
     _run_both(dr, d2, "f32")
+    _run_both(dr, d3, "bf16")
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
