@@ -69,7 +69,7 @@ struct BwdWorkspace {
 // The tensor-core forward's own workspace (segments of few long chains) when it writes the
 // checkpoints, in floats.
 size_t tc_ws_floats(const ChunkProblem &p) {
-    return chunk_tc_supported(p) ? (chunk_tc_workspace_bytes(p) + 3) / 4 : 0;
+    return chunk_tc_supported(p) ? (chunk_tc_workspace_bytes(p, true) + 3) / 4 : 0;
 }
 
 size_t bwd_floats(const ChunkProblem &p) {
@@ -824,7 +824,7 @@ int launch_chunk_bwd(const ChunkProblem &p, const BwdIo &g, void *workspace, int
         int rc = launch_chunk_simt(f, ws.fw, stream, ws.T, tc ? nullptr : ws.ckpt, tc);
         if (rc != kOk) return rc;
         if (tc) {
-            rc = launch_chunk_tc(f, ws.tc, status_word, stream, ws.ckpt);
+            rc = launch_chunk_tc(f, ws.tc, tc_ws_floats(f) * sizeof(float), status_word, stream, ws.ckpt);
             if (rc != kOk) return rc;
         }
     }

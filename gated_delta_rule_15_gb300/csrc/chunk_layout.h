@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/dr.h"
+
 namespace dr {
 
 // A validated chunk-forward problem (all pointers are device pointers).
@@ -78,16 +80,22 @@ size_t bwd_workspace_bytes(const ChunkProblem &p);
 int launch_chunk_bwd(const ChunkProblem &p, const BwdIo &g, void *workspace, int *status_word,
                      cudaStream_t stream);
 
-// Fused tensor-core path (chunk_tc.cu): bf16 inputs, dk = dv = 128, C = 64, scalar gate or
-// none, T > 0.  Needs a workspace only when few long chains are split into segments
-// (chunk_tc_workspace_bytes).  `status_word` is the device status word of the library
-// (bounded waits record DR_ERR_TIMEOUT there).
+// Tensor-core path for bf16 inputs, dk = dv = 128, C = 64, scalar gate or none, T > 0
+// (chunk_tc.cu, gdn_chain.cu).  With a workspace of chunk_tc_workspace_bytes(p) (every
+// chunk's 16 KB T operands, plus the segments' states when few long chains are split) the
+// plain forward runs as two kernels (chunk-parallel solve, then the chains); with at least
+// chunk_tc_workspace_bytes(p, true) (the segments' states only) a single kernel solves inside
+// each chain, which also serves the fused neighbours and the backward's checkpoints.
+// `status_word` is the device status word of the library (bounded waits record
+// DR_ERR_TIMEOUT there).
 bool chunk_tc_supported(const ChunkProblem &p);
-size_t chunk_tc_workspace_bytes(const ChunkProblem &p);
+size_t chunk_tc_workspace_bytes(const ChunkProblem &p, bool least = false);
 // With `ckpt` ([B*H][NC][dk][dv] fp32), it writes the state at every chunk's start instead of
 // the outputs (the backward's recompute).
-int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream,
-                    float *ckpt = nullptr);
+int launch_chunk_tc(const ChunkProblem &p, void *workspace, size_t workspace_bytes, int *status_word,
+                    cudaStream_t stream, float *ckpt = nullptr);
+// The least workspace dr_chunk_fwd accepts for *desc (dr_api.cu).
+int chunk_fwd_least_workspace(const dr_chunk_desc *desc, size_t *bytes);
 // Two-kernel tensor-core path for the per-channel gate (chunk_kda.cu): bf16 inputs,
 // dk = dv = 128, C = 64, T > 0.  Its workspace holds the per-chunk operands that the
 // prep kernel writes and the state kernel reads (chunk_kda_workspace_bytes).

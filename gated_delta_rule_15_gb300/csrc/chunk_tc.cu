@@ -930,6 +930,19 @@ int launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv
 
 }  // namespace
 
+bool tc_make_map(CUtensorMap *m, const void *base, int64_t B, int64_t T, int64_t H, bool fp32) {
+    return make_map(m, base, B, T, H, fp32);
+}
+
+int tc_launch_seg_combine(const float *init_state, const float *phi, const float *s0, float *start,
+                          unsigned chains, int nseg, cudaStream_t stream) {
+    if (cudaFuncSetAttribute(seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCombineSmem) !=
+        cudaSuccess)
+        return kErrCuda;
+    seg_combine_kernel<<<chains * 4, 256, kCombineSmem, stream>>>(init_state, phi, s0, start, nseg);
+    return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+}
+
 bool chunk_tc_supported(const ChunkProblem &p) {
     return p.in_bf16 && p.dk == 128 && p.dv == 128 && p.C == 64 && p.T > 0 &&
            (p.gate == 0 || p.gate == 1);
@@ -939,7 +952,7 @@ bool chunk_tc_supported(const ChunkProblem &p) {
 // one after another; such problems are split into `nseg` segments per chain (at least 16
 // chunks each) so that about 152 CTAs work at once.
 static constexpr int kGpuSms = 152;
-static void tc_segments(const ChunkProblem &p, int *nseg, int *seg_len) {
+void tc_segment_split(const ChunkProblem &p, int *nseg, int *seg_len) {
     *nseg = 1;
     *seg_len = p.NC;
     const int64_t bh = p.B * p.H;
@@ -951,14 +964,23 @@ static void tc_segments(const ChunkProblem &p, int *nseg, int *seg_len) {
     *nseg = (p.NC + len - 1) / len;
 }
 
-size_t chunk_tc_workspace_bytes(const ChunkProblem &p) {
+size_t gdn_split_workspace_bytes(const ChunkProblem &p);
+int launch_gdn_split(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream);
+
+// The two-kernel path (gdn_chain.cu) takes the plain forward when the workspace holds every
+// chunk's T operands; the single kernel below (the solve inside the chain) needs only the
+// segments' states, and serves the fused neighbours and the backward's checkpoints.
+size_t chunk_tc_workspace_bytes(const ChunkProblem &p, bool least) {
+    if (!least) return gdn_split_workspace_bytes(p);
     int nseg, len;
-    tc_segments(p, &nseg, &len);
+    tc_segment_split(p, &nseg, &len);
     return nseg > 1 ? (size_t)3 * p.B * p.H * nseg * 16384 * sizeof(float) : 0;
 }
 
-int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream,
-                    float *ckpt) {
+int launch_chunk_tc(const ChunkProblem &p, void *workspace, size_t workspace_bytes, int *status_word,
+                    cudaStream_t stream, float *ckpt) {
+    if (!ckpt && !p.fuse && workspace && workspace_bytes >= gdn_split_workspace_bytes(p))
+        return launch_gdn_split(p, workspace, status_word, stream);
     CUtensorMap mq, mk, mv, mo, mz;
     const bool zgate = (p.fuse & kFuseGate) != 0;
     if (!make_map(&mq, p.q, p.B, p.T, p.H, false) || !make_map(&mk, p.k, p.B, p.T, p.H, false) ||
@@ -977,7 +999,7 @@ int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cu
     };
     const unsigned bh = (unsigned)(p.B * p.H);
     int nseg, seg_len;
-    tc_segments(p, &nseg, &seg_len);
+    tc_segment_split(p, &nseg, &seg_len);
     if (nseg <= 1) return launch(ta, bh);
     // segments: end states (two runs per segment), chaining, then outputs
     float *ws = reinterpret_cast<float *>(workspace);
@@ -990,12 +1012,8 @@ int launch_chunk_tc(const ChunkProblem &p, void *workspace, int *status_word, cu
     ta.role = 1;
     int rc = launch(ta, bh * nseg * 2);
     if (rc != kOk) return rc;
-    if (cudaFuncSetAttribute(seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCombineSmem) !=
-        cudaSuccess)
-        return kErrCuda;
-    seg_combine_kernel<<<bh * 4, 256, kCombineSmem, stream>>>(p.init_state, ta.ws_phi, ta.ws_s0, ta.ws_start,
-                                                              nseg);
-    if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+    rc = tc_launch_seg_combine(p.init_state, ta.ws_phi, ta.ws_s0, ta.ws_start, bh, nseg, stream);
+    if (rc != kOk) return rc;
     ta.role = 2;
     return launch(ta, bh * nseg);
 }

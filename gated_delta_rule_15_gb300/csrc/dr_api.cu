@@ -89,6 +89,24 @@ extern "C" int dr_chunk_fwd_workspace_bytes(const dr_chunk_desc *desc, size_t *b
     return kOk;
 }
 
+namespace dr {
+int chunk_fwd_least_workspace(const dr_chunk_desc *desc, size_t *bytes) {
+    if (!bytes) return kErrInvalid;
+    ChunkProblem p{};
+    const int rc = check_chunk_desc(desc, &p);
+    if (rc != kOk) return rc;
+    if (chunk_tc_supported(p)) {
+        *bytes = chunk_tc_workspace_bytes(p, true);
+        return kOk;
+    }
+    return dr_chunk_fwd_workspace_bytes(desc, bytes);
+}
+}  // namespace dr
+
+extern "C" int dr_chunk_fwd_min_workspace_bytes(const dr_chunk_desc *desc, size_t *bytes) {
+    return chunk_fwd_least_workspace(desc, bytes);
+}
+
 // Whether byte ranges [a, a + na) and [b, b + nb) overlap.
 static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     const char *a0 = (const char *)a, *b0 = (const char *)b;
@@ -120,7 +138,7 @@ extern "C" int dr_chunk_fwd_ex(const dr_chunk_desc *desc, uint32_t fuse, const v
         if (overlaps(z, n * (p.in_bf16 ? 2 : 4), out, n * (p.out_bf16 ? 2 : 4))) return kErrInvalid;
     }
     size_t need = 0;
-    dr_chunk_fwd_workspace_bytes(desc, &need);
+    chunk_fwd_least_workspace(desc, &need);
     if (need > 0 && p.NC > 0 && (!workspace || workspace_bytes < need)) return kErrWorkspace;
 
     p.q = q; p.k = k; p.v = v; p.log_alpha = p.gate == DR_GATE_NONE ? nullptr : log_alpha;
@@ -130,7 +148,7 @@ extern "C" int dr_chunk_fwd_ex(const dr_chunk_desc *desc, uint32_t fuse, const v
     if (chunk_tc_supported(p)) {
         int *status = device_status_ptr();
         if (!status) return kErrCuda;
-        return launch_chunk_tc(p, workspace, status, (cudaStream_t)stream);
+        return launch_chunk_tc(p, workspace, workspace ? workspace_bytes : 0, status, (cudaStream_t)stream);
     }
     if (chunk_kda_supported(p)) {
         int *status = device_status_ptr();

@@ -1,0 +1,778 @@
+// gdn_chain.cu -- chunkwise forward of the gated delta rule as two tensor-core kernels: a
+// chunk-parallel prep kernel and a per-chain kernel whose per-chunk products are a few wide
+// tcgen05 MMAs.  bf16 inputs, d_k = d_v = 128, chunk C = 64, scalar gate or no gate.
+//
+// The chunk form is the one of chunk_simt.cu and chunk_tc.cu (derived from the recurrence of
+// the page "NLP: linear attention summary", KDA section, in the order of the
+// `gated_delta_rule` loop of the page "linear-attention gated-deltanet guide", section 4;
+// chunks are processed in parallel inside and carried sequentially between them, page
+// "Transformer notes (5): linear attention optimisations", paragraph on chunked
+// computation).  Per chunk, with g the cumulative log decay, G = exp(g), gamma = G_63 and
+// delta_r = exp(g_63 - g_r):
+//
+//   A   = stril(beta_r exp(g_r - g_s) K K^T),  T = (I + A)^-1          (prep kernel)
+//   U^T = V^T (T diag beta)^T,   W^T = K^T (T diag(beta G))^T
+//   [(W S)^T | (Q S)^T] = S^T [W; Q]^T                                  (one N = 128 product)
+//   E^T = U^T - (W S)^T
+//   [O^T | S^T] <- [G (Q S)^T | gamma S^T] + E^T [P; Kt^T]^T             (one N = 192 product)
+//   with P = tril(exp(g_r - g_s) Q K^T) and Kt = diag(delta) K.
+//
+// The only step that depends on the previous chunk is the state: S^T -> [W S, Q S] -> E ->
+// S^T.  The triangular solve T = (I + A)^-1 depends on the chunk's own k, beta and gates
+// only, so gdn_prep_kernel forms it for every chunk at once (one CTA per chunk) and writes
+// the two bf16 operands T diag(beta) | T diag(beta G) (16 KB per chunk, already in the
+// swizzled layout of the tensor core's B operand) to the workspace.  gdn_chain_kernel then
+// walks each chain's chunks with nine or ten warps, each group with one duty:
+//
+//   warp 0       TMA: each chunk's q, k tiles (two stages) and its v tile and T operands
+//   warp 1       issues every tcgen05.mma and commits it to an mbarrier
+//   warp 2       the gates: beta and log alpha by cp.async, cumulative decays per chunk
+//   warps 3..6   the state: S^T -> bf16 (an A operand in tensor memory) and S^T <- gamma S^T,
+//                P from X = [Q; K] K^T, E^T = U^T - (W S)^T (fp32, in tensor memory: the
+//                tf32 A operand of the state update) and G (Q S)^T
+//   warps 7..10  W^T (tensor memory) -> W (bf16, the B operand of the next product), Kt^T
+//                (tf32) from the k tile, and the chunk's output (TMA store)
+//
+// Precision: S and W enter (W S, Q S) as bf16 (Q exactly), the state update and the output's
+// intra-chunk term take E, P and Kt as tf32 (10 explicit mantissa bits); T's operands are
+// bf16, as in chunk_tc.cu.  Every wait is bounded by a cycle budget: on expiry the kernel
+// records DR_ERR_TIMEOUT in the status word, stops, drains its own copies and MMAs with the
+// same bound, frees tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "chunk_layout.h"
+#include "common.cuh"
+#include "tc_common.cuh"
+#include "umma.cuh"
+
+namespace dr {
+
+// chunk_tc.cu: the tensor map of a [B, T, H, 128] tensor (64-token boxes, 128-byte swizzle),
+// the segment split of few long chains, and the segment chaining kernel's launch.
+bool tc_make_map(CUtensorMap *m, const void *base, int64_t B, int64_t T, int64_t H, bool fp32);
+void tc_segment_split(const ChunkProblem &p, int *nseg, int *seg_len);
+int tc_launch_seg_combine(const float *init_state, const float *phi, const float *s0, float *start,
+                          unsigned chains, int nseg, cudaStream_t stream);
+
+namespace {
+
+using namespace umma;
+using namespace tc;
+
+// Largest in-chunk log-decay span for which exp(g_r - g_s) is formed as a product of two
+// exponentials around the chunk's middle token (both factors stay within fp32 range).
+constexpr float kSpan = 80.f;
+
+// ============================================================ prep kernel
+// One CTA of four warps per (chain, chunk), all independent.  X = K K^T on the lower 16 x 16
+// blocks (mma.sync, bf16 in, fp32 out; warp w takes row block w), A_rs = beta_r exp(g_r - g_s)
+// X_rs for s < r (off-diagonal blocks TF32-rounded), then the blocked solve of tc_common.cuh,
+// which writes T diag(beta) | T diag(beta G) in bf16; the 16 KB image is copied to the
+// workspace.  Tokens past T are zero rows of K with beta = 0 (T is then the identity there),
+// as the chain kernel's loads make them.
+constexpr int kPrepThreads = 128;
+constexpr int kLdK = 136;                          // K tile row pitch (bf16): conflict-free fragments
+constexpr uint32_t PR_K = 0;                       // K tile [64][136] bf16; then fp32 T (swizzled)
+constexpr uint32_t PR_A = 64 * kLdK * 2;           // fp32 A (a_index)
+constexpr uint32_t PR_TB = PR_A + 16384;           // the operand image
+constexpr uint32_t PR_M = PR_TB + 16384;           // solve scratch
+constexpr uint32_t PR_V = PR_M + 4096;             // g, G, beta, exp(g - g_31), exp(g_31 - g)
+constexpr uint32_t PR_TOTAL = PR_V + 5 * 256;
+static_assert(PR_A >= 16384, "T fits over the K tile");
+
+template <int GATE>
+__global__ void __launch_bounds__(kPrepThreads, 4)
+gdn_prep_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ beta,
+                const float *__restrict__ log_alpha, unsigned char *__restrict__ tops, int T, int H, int NC) {
+    extern __shared__ float4 prep_sm4[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(prep_sm4);
+    __shared__ int fac_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = (int)(blockIdx.x % (unsigned)NC), bh = (int)(blockIdx.x / (unsigned)NC);
+    const int h = bh % H, b = bh / H, t0 = c * 64;
+    __nv_bfloat16 *sK = reinterpret_cast<__nv_bfloat16 *>(sm + PR_K);
+    float *sA = reinterpret_cast<float *>(sm + PR_A);
+    float *sV = reinterpret_cast<float *>(sm + PR_V);
+    float *sG = sV, *sGam = sV + 64, *sBeta = sV + 128, *sE = sV + 192, *sF = sV + 256;
+
+    // the K tile: 64 rows of 256 bytes, rows past T zero
+    for (int i = tid; i < 64 * 16; i += kPrepThreads) {
+        const int r = i >> 4, q = i & 15, t = t0 + r;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (t < T) v = *reinterpret_cast<const uint4 *>(k + (((size_t)b * T + t) * H + h) * 128 + 8 * q);
+        *reinterpret_cast<uint4 *>(sK + r * kLdK + 8 * q) = v;
+    }
+    if (warp == 0) {   // the chunk's gates, two tokens per lane
+        float l[2], bt[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = t0 + 2 * lane + e;
+            const size_t tok = ((size_t)b * T + t) * H + h;
+            bt[e] = t < T ? __bfloat162float(beta[tok]) : 0.f;
+            l[e] = (GATE == 1 && t < T) ? log_alpha[tok] : 0.f;
+        }
+        float p = l[0] + l[1];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, p, o);
+            if (lane >= o) p += y;
+        }
+        const float g1 = p, g0 = p - l[1];
+        const float glast = __shfl_sync(0xffffffffu, g1, 31);
+        const float gmid = __shfl_sync(0xffffffffu, g1, 15);
+        const float gfirst = __shfl_sync(0xffffffffu, g0, 0);
+        const int r = 2 * lane;
+        sG[r] = g0; sG[r + 1] = g1;
+        sBeta[r] = bt[0]; sBeta[r + 1] = bt[1];
+        sGam[r] = __expf(g0); sGam[r + 1] = __expf(g1);
+        const bool fac = gfirst - glast < kSpan;
+        if (fac) {
+            sE[r] = __expf(g0 - gmid); sE[r + 1] = __expf(g1 - gmid);
+            sF[r] = __expf(gmid - g0); sF[r + 1] = __expf(gmid - g1);
+        }
+        if (lane == 0) fac_s = fac;
+    }
+    __syncthreads();
+
+    // X on the lower blocks and A from it: warp w owns rows 16 w .. 16 w + 15
+    {
+        const int g = lane >> 2, t4 = lane & 3, r0 = 16 * warp;
+        const bool fac = fac_s != 0;
+        auto ld = [&](int r, int col) { return *reinterpret_cast<const uint32_t *>(sK + r * kLdK + col); };
+        for (int cb = 0; cb <= warp; ++cb) {
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kk = 0; kk < 128; kk += 16) {
+                const uint32_t af[4] = {ld(r0 + g, kk + 2 * t4), ld(r0 + g + 8, kk + 2 * t4),
+                                        ld(r0 + g, kk + 8 + 2 * t4), ld(r0 + g + 8, kk + 8 + 2 * t4)};
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int sr = 16 * cb + 8 * nt + g;
+                    mma_bf16_16x8x16(acc[nt], af, ld(sr, kk + 2 * t4), ld(sr, kk + 8 + 2 * t4));
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int r = r0 + g + 8 * hf, s0 = 16 * cb + 8 * nt + 2 * t4;
+                    float v[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int s = s0 + e;
+                        const float dec = fac ? sE[r] * sF[s] : __expf(fminf(sG[r] - sG[s], 0.f));
+                        v[e] = s < r ? sBeta[r] * dec * acc[nt][2 * hf + e] : 0.f;
+                        if (cb != warp) v[e] = round_tf32(v[e]);
+                    }
+                    *reinterpret_cast<float2 *>(sA + a_index(r, s0)) = make_float2(v[0], v[1]);
+                }
+        }
+    }
+    __syncthreads();   // the K tile is dead: T goes over it
+
+    const SolveOut<true, true, true> out{reinterpret_cast<float *>(sm + PR_K), sm + PR_TB, sBeta, sGam, nullptr};
+    solve_diag64(sA, out, tid);          // diagonal blocks 0, 1 (and operand zero blocks)
+    solve_diag64(sA, out, tid + 128);    // diagonal blocks 2, 3
+    __syncthreads();
+    solve_merge64(sA, out, reinterpret_cast<float *>(sm + PR_M), tid, 1);
+    __syncthreads();
+    uint4 *dst = reinterpret_cast<uint4 *>(tops + ((size_t)bh * NC + c) * 16384);
+    const uint4 *src = reinterpret_cast<const uint4 *>(sm + PR_TB);
+#pragma unroll
+    for (int i = tid; i < 1024; i += kPrepThreads) dst[i] = src[i];
+}
+
+// ============================================================ chain kernel
+constexpr int kChainThreads = 352;             // 11 warps
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpGate = 2, kWarpS0 = 3, kWarpO0 = 7;
+// shared memory (offsets from the 1024-byte-aligned base)
+constexpr uint32_t C_STAGE = 49152;            // one q/k stage: two K-blocks of [W | Q | K]
+constexpr uint32_t C_KB = 24576;               // one K-block (64 of the 128 key channels)
+constexpr uint32_t C_OFF_Q = 8192, C_OFF_K = 16384;
+constexpr uint32_t C_VT = 2 * C_STAGE;         // v tile (two 64-channel halves) and T operands
+constexpr uint32_t C_TB = C_VT + 16384;        // T diag(beta) | T diag(beta G) (bf16, 8 KB each)
+constexpr uint32_t C_BU = C_VT + 32768;        // tf32 [P; Kt^T]: two K-blocks of 32 tokens
+constexpr uint32_t C_BU_KB = 24576;            // 192 rows x 128 bytes
+constexpr uint32_t C_OUT = C_BU + 2 * C_BU_KB; // output staging (bf16: 2 boxes, fp32: 4 boxes)
+constexpr uint32_t C_SMALL = C_OUT + 32768;    // gate vectors [2][6][64] and raw gates [2][128]
+constexpr uint32_t C_TOTAL = C_SMALL + 4096;
+static_assert(C_TOTAL + 1024 <= 227 * 1024, "layout");
+// tensor memory columns
+constexpr uint32_t TM_WE = 0;     // (W S)^T, then E^T (fp32)
+constexpr uint32_t TM_QO = 64;    // (Q S)^T, then G (Q S)^T, then O^T
+constexpr uint32_t TM_S = 128;    // S^T (fp32)
+constexpr uint32_t TM_SB = 256;   // S^T as bf16 pairs (the A operand of [W S | Q S])
+constexpr uint32_t TM_X = 320;    // [Q; K] K^T
+constexpr uint32_t TM_W = 384;    // W^T
+constexpr uint32_t TM_U = 448;    // U^T
+// gate vector slots of one set
+enum { GV_G = 0, GV_GAM = 1, GV_DEL = 2, GV_BETA = 3, GV_E = 4, GV_F = 5 };
+
+constexpr uint32_t ID_X = idesc_bf16(128, 64, false, false);
+constexpr uint32_t ID_UW = idesc_bf16(128, 64, true, false);
+constexpr uint32_t ID_D = idesc_bf16(128, 128, false, false);
+constexpr uint32_t ID_UPD = idesc_tf32(128, 192);
+constexpr uint32_t ID_UPD_S = idesc_tf32(128, 128);
+
+struct ChainArgs {
+    const float *log_alpha;
+    const __nv_bfloat16 *beta;
+    const float *init_state;
+    float *final_state;
+    const unsigned char *tops;   // [B*H][NC][16384]: T diag(beta) | T diag(beta G) per chunk
+    int *status;
+    int B, T, H, NC;
+    // Sequence segments (few long chains), as in chunk_tc.cu: role 0 runs whole sequences;
+    // role 1 runs each segment twice without outputs -- from S_0 = 0 (end state to ws_s0)
+    // and as the transition from S_0 = I with no value term (to ws_phi); role 2 reruns each
+    // segment from its true start state (ws_start) writing outputs.
+    int role, nseg, seg_len;
+    float *ws_phi, *ws_s0, *ws_start;
+};
+
+// byte offset of fp32 element (row, k), k < 32, in a 128-byte-swizzled K-major tf32 tile
+__device__ __forceinline__ uint32_t sw128_off32(uint32_t row, uint32_t k) {
+    return row * 128u + ((((k >> 2) ^ (row & 7u)) & 7u) << 4) + ((k & 3u) << 2);
+}
+
+template <typename Tout, int GATE>
+__global__ void __launch_bounds__(kChainThreads, 1)
+gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                 const ChainArgs a) {
+    extern __shared__ unsigned char dsm_raw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
+    // Completed by TMA transactions or tcgen05.commit (count 1) ...
+    __shared__ uint64_t qkw_full[2], vt_full, x_done, uw_done, d_done, u_done;
+    // ... or by every thread of a group (stage_free: the commit of [W S | Q S] and warps
+    // 7..10 after Kt^T; gset_free: warps 3..10 after their last use of a gate set).
+    __shared__ uint64_t sb_ready, p_ready, e_ready, w_ready, kt_ready, o_read;
+    __shared__ uint64_t stage_free[2], g_ready[2], gset_free[2];
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s, fac_s[2];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = 32 * (warp & 3) + lane;   // the TMEM lane this thread reads and writes
+    // this CTA's chain, chunk range, initial/final state and duties
+    int bh = blockIdx.x, c_begin = 0, c_end = a.NC;
+    const float *init_ptr = a.init_state ? a.init_state + (size_t)blockIdx.x * 16384 : nullptr;
+    float *fin_ptr = a.final_state ? a.final_state + (size_t)blockIdx.x * 16384 : nullptr;
+    bool init_identity = false, zero_u = false, outputs = true;
+    if (a.role != 0) {
+        const int idx = a.role == 1 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+        const int seg = idx % a.nseg;
+        bh = idx / a.nseg;
+        c_begin = seg * a.seg_len;
+        c_end = min(a.NC, c_begin + a.seg_len);
+        const size_t slot = ((size_t)bh * a.nseg + seg) * 16384;
+        if (a.role == 1) {
+            outputs = false;
+            init_ptr = nullptr;
+            if (blockIdx.x & 1) {   // transition: S_0 = I, no value term
+                init_identity = true;
+                zero_u = true;
+                fin_ptr = a.ws_phi + slot;
+            } else {
+                fin_ptr = a.ws_s0 + slot;
+            }
+        } else {
+            init_ptr = a.ws_start + slot;
+            fin_ptr = (seg == a.nseg - 1 && a.final_state) ? a.final_state + (size_t)bh * 16384 : nullptr;
+        }
+    }
+    const int h = bh % a.H, b = bh / a.H;
+    const int n_it = c_end - c_begin;
+
+    float *sVec = reinterpret_cast<float *>(sm + C_SMALL);   // [2][6][64]
+    auto vec = [&](int it, int k) { return sVec + (it & 1) * 384 + 64 * k; };
+    uint32_t *sGate = reinterpret_cast<uint32_t *>(sm + C_SMALL + 3072);   // [2][beta word | log alpha][64]
+
+    if (tid == 0) {
+        uint64_t *ones[] = {&qkw_full[0], &qkw_full[1], &vt_full, &x_done, &uw_done, &d_done, &u_done};
+        for (uint64_t *bb : ones) mbar_init(bb, 1);
+        uint64_t *groups[] = {&sb_ready, &p_ready, &e_ready, &w_ready, &kt_ready, &o_read};
+        for (uint64_t *bb : groups) mbar_init(bb, 128);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&stage_free[s], 129);
+            mbar_init(&g_ready[s], 32);
+            mbar_init(&gset_free[s], 256);
+        }
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_s, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmb = tmem_base_s;
+    const uint32_t tm = tmb + ((uint32_t)(32 * (warp & 3)) << 16);   // + this warp's lanes
+    const uint64_t dK0 = smem_desc_sw128(smem_u32(sm), 16, 1024);
+    const uint64_t dMv = smem_desc_sw128(smem_u32(sm), 8192, 1024);    // MN-major, v halves
+    const uint64_t dMk = smem_desc_sw128(smem_u32(sm), C_KB, 1024);    // MN-major, k halves
+    auto stage = [&](int it) { return sm + (it & 1) * C_STAGE; };
+    volatile int *abort_v = &abort_s;
+    auto fail = [&]() {
+        *abort_v = 1;
+        atomicExch(a.status, kErrTimeout);
+    };
+    // bounded wait; false (and nothing further to do) once the CTA has failed
+    auto wait_bar = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (*abort_v) return false;
+        if (!wait_cycles(bar, parity)) {
+            fail();
+            return false;
+        }
+        tc_fence_after();
+        return true;
+    };
+
+    if (warp == kWarpTma) {
+        // ---------------- TMA: q, k of chunk it into stage it % 2 once the chunk two back has
+        // left it; v and T operands of chunk it once U/W(it - 1) have read the previous ones
+        if (lane == 0) {
+            int q_last[2] = {-1, -1}, v_last = -1;
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it & 1, t0 = (c_begin + it) * 64;
+                if (it >= 2 && !wait_bar(&stage_free[s], ((it - 2) >> 1) & 1)) break;
+                unsigned char *st = stage(it);
+                mbar_arrive_expect_tx(&qkw_full[s], 32768);
+                for (int kb = 0; kb < 2; ++kb) {
+                    tma_load_4d(st + kb * C_KB + C_OFF_Q, &tq, &qkw_full[s], 64 * kb, h, t0, b);
+                    tma_load_4d(st + kb * C_KB + C_OFF_K, &tk, &qkw_full[s], 64 * kb, h, t0, b);
+                }
+                q_last[s] = it;
+                if (it >= 1 && !wait_bar(&uw_done, (it - 1) & 1)) break;
+                mbar_arrive_expect_tx(&vt_full, zero_u ? 16384 : 32768);
+                if (!zero_u)
+                    for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + C_VT + kb * 8192, &tv, &vt_full, 64 * kb, h, t0, b);
+                bulk_load(sm + C_TB, a.tops + ((size_t)bh * a.NC + c_begin + it) * 16384, 16384, &vt_full);
+                v_last = it;
+            }
+            if (*abort_v) {   // loads this thread issued may still be in flight (bounded waits)
+                for (int s = 0; s < 2; ++s)
+                    if (q_last[s] >= 0) wait_cycles(&qkw_full[s], (q_last[s] >> 1) & 1);
+                if (v_last >= 0) wait_cycles(&vt_full, v_last & 1);
+            }
+        }
+    } else if (warp == kWarpMma) {
+        // ---------------- MMA issue: per chunk [W S | Q S](it), X(it + 1), the state update and
+        // output product (it), then U/W(it + 1)
+        if (lane == 0 && n_it > 0) {
+            uint64_t *last = nullptr;
+            uint32_t last_par = 0;
+            auto issue_x = [&](int it) {   // X = [Q; K] K^T (rows 0..63: Q K^T)
+                unsigned char *st = stage(it);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t o = (uint32_t)((st - sm) + (ks >> 2) * C_KB + (ks & 3) * 32);
+                    mma_bf16(tmb + TM_X, desc_add(dK0, o + C_OFF_Q), desc_add(dK0, o + C_OFF_K), ID_X, ks > 0);
+                }
+                mma_commit(&x_done);
+                last = &x_done; last_par = it & 1;
+            };
+            auto issue_uw = [&](int it) {  // U^T = V^T (T diag beta)^T, W^T = K^T (T diag(beta G))^T
+                const uint32_t sk = (uint32_t)(stage(it) - sm) + C_OFF_K;
+                if (!zero_u)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tmb + TM_U, desc_add(dMv, C_VT + ks * 2048), desc_add(dK0, C_TB + ks * 32), ID_UW,
+                                 ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmb + TM_W, desc_add(dMk, sk + ks * 2048), desc_add(dK0, C_TB + 8192 + ks * 32), ID_UW,
+                             ks > 0);
+                mma_commit(&uw_done);
+                last = &uw_done; last_par = it & 1;
+            };
+            bool ok = true;
+            if (outputs) {
+                ok = wait_bar(&qkw_full[0], 0);
+                if (ok) issue_x(0);
+            }
+            ok = ok && wait_bar(&vt_full, 0);
+            if (ok) issue_uw(0);
+            for (int it = 0; ok && it < n_it; ++it) {
+                const uint32_t par = it & 1;
+                const int s = it & 1;
+                const bool next = it + 1 < n_it;
+                // [W S | Q S](it): A = S^T (bf16 pairs in tensor memory), B = [W; Q] (stage)
+                if (!wait_bar(&sb_ready, par) || !wait_bar(&w_ready, par)) break;
+                if (outputs && it >= 1 && !wait_bar(&o_read, par ^ 1)) break;
+                const uint32_t sw = (uint32_t)(stage(it) - sm);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ts(tmb + TM_WE, tmb + TM_SB + 8 * ks,
+                                desc_add(dK0, sw + (ks >> 2) * C_KB + (ks & 3) * 32), ID_D, ks > 0);
+                mma_commit(&d_done);
+                mma_commit(&stage_free[s]);
+                last = &d_done; last_par = par;
+                // X(it + 1) once P(it) has been read out of TM_X
+                if (outputs && next) {
+                    if (!wait_bar(&qkw_full[(it + 1) & 1], ((it + 1) >> 1) & 1) || !wait_bar(&p_ready, par)) break;
+                    issue_x(it + 1);
+                }
+                // [O^T | S^T] += E^T [P; Kt^T]^T  (tf32; E^T from tensor memory)
+                if (!wait_bar(&e_ready, par) || !wait_bar(&kt_ready, par)) break;
+                if (outputs && !wait_bar(&p_ready, par)) break;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_tf32_ts(tmb + (outputs ? TM_QO : TM_S), tmb + TM_WE + 8 * ks,
+                                desc_add(dK0, C_BU + (outputs ? 0u : 8192u) + (ks >> 2) * C_BU_KB + (ks & 3) * 32),
+                                outputs ? ID_UPD : ID_UPD_S, true);
+                mma_commit(&u_done);
+                last = &u_done; last_par = par;
+                if (next) {
+                    if (!wait_bar(&vt_full, (it + 1) & 1)) break;
+                    issue_uw(it + 1);
+                }
+            }
+            if (*abort_v && last) wait_cycles(last, last_par);   // drain (bounded)
+        }
+        __syncwarp();
+    } else if (warp == kWarpGate) {
+        // ---------------- gates: raw beta / log alpha two chunks ahead (cp.async), the scan of
+        // chunk it into set it % 2 once the chunk two back has been consumed
+        const size_t ntok = (size_t)a.B * a.T * a.H;
+        auto issue_gate = [&](int it) {
+            if (it < n_it) {
+                uint32_t *dst = sGate + (it & 1) * 128;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 2 * lane + e, t = (c_begin + it) * 64 + r;
+                    const bool valid = t < a.T;
+                    const size_t tok = valid ? ((size_t)b * a.T + t) * a.H + h : 0;
+                    if (valid && tok + 1 == ntok && ((2 * tok) & 3) == 0) {
+                        // the 32-bit word would run past the end of beta: load this value alone
+                        dst[r] = (uint32_t)__bfloat16_as_ushort(a.beta[tok]);
+                    } else {
+                        cp_async4(dst + r, reinterpret_cast<const char *>(a.beta) + ((2 * tok) & ~(size_t)3),
+                                  valid ? 4 : 0);
+                    }
+                    cp_async4(dst + 64 + r, GATE == 1 ? (const void *)(a.log_alpha + tok) : (const void *)a.beta,
+                              (GATE == 1 && valid) ? 4 : 0);
+                }
+            }
+            cp_async_commit();
+        };
+        issue_gate(0);
+        issue_gate(1);
+        for (int it = 0; it < n_it; ++it) {
+            if (it >= 2 && !wait_bar(&gset_free[it & 1], ((it - 2) >> 1) & 1)) break;
+            cp_async_wait_group1();
+            __syncwarp();
+            const uint32_t *gw = sGate + (it & 1) * 128;
+            const int t0 = (c_begin + it) * 64;
+            float l[2], bt[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = 2 * lane + e, t = t0 + r;
+                const size_t tok = t < a.T ? ((size_t)b * a.T + t) * a.H + h : 0;
+                const uint32_t wd = gw[r];
+                const uint16_t hb = (uint16_t)(((2 * tok) & 2) ? (wd >> 16) : (wd & 0xffffu));
+                bt[e] = __bfloat162float(__ushort_as_bfloat16(hb));
+                l[e] = __uint_as_float(gw[64 + r]);
+            }
+            __syncwarp();
+            issue_gate(it + 2);
+            float p = l[0] + l[1];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, p, o);
+                if (lane >= o) p += y;
+            }
+            const float g1 = p, g0 = p - l[1];
+            const float glast = __shfl_sync(0xffffffffu, g1, 31);
+            const float gmid = __shfl_sync(0xffffffffu, g1, 15);
+            const float gfirst = __shfl_sync(0xffffffffu, g0, 0);
+            const int r = 2 * lane;
+            float *sG = vec(it, GV_G), *sGam = vec(it, GV_GAM), *sDel = vec(it, GV_DEL), *sBeta = vec(it, GV_BETA),
+                  *sE = vec(it, GV_E), *sF = vec(it, GV_F);
+            sG[r] = g0; sG[r + 1] = g1;
+            sBeta[r] = bt[0]; sBeta[r + 1] = bt[1];
+            sGam[r] = __expf(g0); sGam[r + 1] = __expf(g1);
+            sDel[r] = __expf(glast - g0); sDel[r + 1] = __expf(glast - g1);
+            const bool fac = gfirst - glast < kSpan;
+            if (fac) {
+                sE[r] = __expf(g0 - gmid); sE[r + 1] = __expf(g1 - gmid);
+                sF[r] = __expf(gmid - g0); sF[r + 1] = __expf(gmid - g1);
+            }
+            if (lane == 0) fac_s[it & 1] = fac;
+            mbar_arrive(&g_ready[it & 1]);
+        }
+        cp_async_wait_all();
+    } else if (warp < kWarpO0) {
+        // ---------------- state warps (TMEM lane j = row of S^T, value channel j)
+        {
+            float v[32];
+            for (int part = 0; part < 4; ++part) {
+                const int i0 = 32 * part;
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    v[u] = init_identity ? (i0 + u == row ? 1.f : 0.f)
+                                         : (init_ptr ? init_ptr[(size_t)(i0 + u) * 128 + row] : 0.f);
+                tmem_st32(tm + TM_S + i0, v);
+            }
+            tmem_wait_st();
+        }
+        for (int it = 0; it < n_it; ++it) {
+            const uint32_t par = it & 1;
+            if (it >= 1 && !wait_bar(&u_done, par ^ 1)) break;
+            if (!wait_bar(&g_ready[it & 1], (it >> 1) & 1)) break;
+            // S^T -> bf16 pairs (the A operand of [W S | Q S]) and S^T <- gamma S^T
+            {
+                const float gamma = vec(it, GV_GAM)[63];
+                float v[32];
+#pragma unroll 1
+                for (int part = 0; part < 4; ++part) {
+                    tmem_ld32(tm + TM_S + 32 * part, v);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
+                    tmem_st16u(tm + TM_SB + 16 * part, pk);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) v[u] *= gamma;
+                    tmem_st32(tm + TM_S + 32 * part, v);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            mbar_arrive(&sb_ready);
+            // P(it) from the Q K^T rows of X (lanes 0..63), tf32, into rows 0..63 of [P; Kt^T]
+            if (outputs) {
+                if ((warp & 3) < 2) {
+                    if (!wait_bar(&x_done, par)) break;
+                    float x[64];
+                    tmem_ld32(tm + TM_X, *reinterpret_cast<float(*)[32]>(x));
+                    tmem_ld32(tm + TM_X + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+                    tmem_wait_ld();
+                    const int r = row;
+                    const float *sG = vec(it, GV_G), *sE = vec(it, GV_E), *sF = vec(it, GV_F);
+                    const bool fac = fac_s[it & 1] != 0;
+                    const float er = sE[r], gr = sG[r];
+#pragma unroll
+                    for (int c4 = 0; c4 < 16; ++c4) {
+                        float pv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int s = 4 * c4 + e;
+                            const float dec = fac ? er * sF[s] : __expf(fminf(gr - sG[s], 0.f));
+                            pv[e] = s <= r ? round_tf32(dec * x[s]) : 0.f;
+                        }
+                        *reinterpret_cast<float4 *>(sm + C_BU + (c4 >> 3) * C_BU_KB + sw128_off32(r, 4 * (c4 & 7))) =
+                            make_float4(pv[0], pv[1], pv[2], pv[3]);
+                    }
+                    fence_proxy_async();
+                }
+                tc_fence_before();
+                mbar_arrive(&p_ready);
+            }
+            // E^T = U^T - (W S)^T in place of (W S)^T (fp32, tf32-rounded: the next product's
+            // A operand) and G (Q S)^T in place of (Q S)^T
+            if (!wait_bar(&d_done, par)) break;
+            {
+                const float *sGam = vec(it, GV_GAM);
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    float ws[32], uu[32];
+                    tmem_ld32(tm + TM_WE + 32 * hh, ws);
+                    if (!zero_u) tmem_ld32(tm + TM_U + 32 * hh, uu);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) ws[u] = round_tf32((zero_u ? 0.f : uu[u]) - ws[u]);
+                    tmem_st32(tm + TM_WE + 32 * hh, ws);
+                    if (outputs) {
+                        tmem_ld32(tm + TM_QO + 32 * hh, uu);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) uu[u] *= sGam[32 * hh + u];
+                        tmem_st32(tm + TM_QO + 32 * hh, uu);
+                    }
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            mbar_arrive(&e_ready);
+            mbar_arrive(&gset_free[it & 1]);
+        }
+        if (n_it > 0 && wait_bar(&u_done, (n_it - 1) & 1) && fin_ptr) {
+            float v[32];
+            for (int part = 0; part < 4; ++part) {
+                const int i0 = 32 * part;
+                tmem_ld32(tm + TM_S + i0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 32; ++u) fin_ptr[(size_t)(i0 + u) * 128 + row] = v[u];
+            }
+        }
+    } else {
+        // ---------------- operand / output warps
+        const int to_ = tid - 32 * kWarpO0;   // 0..127: key channel i of Kt^T
+        constexpr int kOutBoxes = sizeof(Tout) == 2 ? 2 : 4;
+        // W^T (lane i = key channel, 64 tokens) -> W (bf16, K-major) in the W slot of stage it
+        auto convert_w = [&](int it) -> bool {
+            if (!wait_bar(&uw_done, it & 1)) return false;
+            float w[64];
+            tmem_ld32(tm + TM_W, *reinterpret_cast<float(*)[32]>(w));
+            tmem_ld32(tm + TM_W + 32, *reinterpret_cast<float(*)[32]>(w + 32));
+            tmem_wait_ld();
+            unsigned char *dst = stage(it) + (row >> 6) * C_KB;
+            const int ic = row & 63;
+#pragma unroll
+            for (int r = 0; r < 64; ++r)
+                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(r, ic)) = __float2bfloat16_rn(w[r]);
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(&w_ready);
+            return true;
+        };
+        // chunk it's output O^T (lane j = value channel, 64 tokens) -> staging -> TMA store
+        auto emit = [&](int it) {
+            float o[64];
+            tmem_ld32(tm + TM_QO, *reinterpret_cast<float(*)[32]>(o));
+            tmem_ld32(tm + TM_QO + 32, *reinterpret_cast<float(*)[32]>(o + 32));
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&o_read);
+            if (to_ == 0) bulk_wait_read_all();   // the previous store has read the staging
+            named_sync(1, 128);
+            const int j = row;
+            if (sizeof(Tout) == 2) {
+                unsigned char *dst = sm + C_OUT + (j >> 6) * 8192;
+#pragma unroll
+                for (int r = 0; r < 64; ++r)
+                    *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(r, j & 63)) = __float2bfloat16_rn(o[r]);
+            } else {
+                unsigned char *dst = sm + C_OUT + (j >> 5) * 8192;
+                const int cj = j & 31;
+#pragma unroll
+                for (int r = 0; r < 64; ++r)
+                    *reinterpret_cast<float *>(dst + r * 128 + ((((cj >> 2) ^ (r & 7)) & 7) << 4) + ((cj & 3) << 2)) =
+                        o[r];
+            }
+            fence_proxy_async();
+            named_sync(1, 128);
+            if (to_ == 0) {
+                constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
+                const int t0 = (c_begin + it) * 64;
+#pragma unroll
+                for (int kb = 0; kb < kOutBoxes; ++kb)
+                    tma_store_4d(&to, sm + C_OUT + kb * 8192, cols * kb, h, t0, b);
+                bulk_commit();
+            }
+        };
+        bool ok = n_it > 0 && convert_w(0);
+        for (int it = 0; ok && it < n_it; ++it) {
+            const uint32_t par = it & 1;
+            if (it >= 1) {
+                if (!wait_bar(&u_done, par ^ 1)) break;
+                if (outputs) emit(it - 1);
+            }
+            // Kt^T (row i = key channel, 64 tokens: delta_r k_r[i]), tf32, into rows 64..191
+            if (!wait_bar(&qkw_full[it & 1], (it >> 1) & 1) || !wait_bar(&g_ready[it & 1], (it >> 1) & 1)) break;
+            {
+                const int i = to_;
+                const unsigned char *src = stage(it) + (i >> 6) * C_KB + C_OFF_K;
+                const int ic = i & 63;
+                const float *sDel = vec(it, GV_DEL);
+#pragma unroll
+                for (int c4 = 0; c4 < 16; ++c4) {
+                    float kv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = 4 * c4 + e;
+                        kv[e] = round_tf32(sDel[r] * __bfloat162float(
+                                                         *reinterpret_cast<const __nv_bfloat16 *>(src + sw128_off(r, ic))));
+                    }
+                    *reinterpret_cast<float4 *>(sm + C_BU + (c4 >> 3) * C_BU_KB + sw128_off32(64 + i, 4 * (c4 & 7))) =
+                        make_float4(kv[0], kv[1], kv[2], kv[3]);
+                }
+                fence_proxy_async();
+            }
+            mbar_arrive(&kt_ready);
+            mbar_arrive(&stage_free[it & 1]);
+            mbar_arrive(&gset_free[it & 1]);
+            if (it + 1 < n_it && !convert_w(it + 1)) break;
+        }
+        if (outputs && n_it > 0 && !*abort_v && wait_bar(&u_done, (n_it - 1) & 1)) emit(n_it - 1);
+        if (to_ == 0) bulk_wait_all();   // the output stores' global writes
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmb, 512);
+}
+
+template <typename Tout, int GATE>
+int launch_chain(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+                 const ChainArgs &ca, unsigned grid, cudaStream_t stream) {
+    const int smem = (int)C_TOTAL + 1024;
+    if (cudaFuncSetAttribute(gdn_chain_kernel<Tout, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return kErrCuda;
+    gdn_chain_kernel<Tout, GATE><<<grid, kChainThreads, smem, stream>>>(mq, mk, mv, mo, ca);
+    return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+}
+
+}  // namespace
+
+// Workspace of the two-kernel path: the segments' states [3][B*H][nseg][128][128] fp32 (when
+// few long chains are split), then the T operands [B*H][NC][16 KB].
+size_t gdn_split_workspace_bytes(const ChunkProblem &p) {
+    int nseg, len;
+    tc_segment_split(p, &nseg, &len);
+    const size_t seg = nseg > 1 ? (size_t)3 * p.B * p.H * nseg * 16384 * sizeof(float) : 0;
+    return seg + (size_t)p.B * p.H * p.NC * 16384;
+}
+
+int launch_gdn_split(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream) {
+    int nseg, seg_len;
+    tc_segment_split(p, &nseg, &seg_len);
+    const unsigned bh = (unsigned)(p.B * p.H);
+    const size_t seg_bytes = nseg > 1 ? (size_t)3 * bh * nseg * 16384 * sizeof(float) : 0;
+    unsigned char *tops = reinterpret_cast<unsigned char *>(workspace) + seg_bytes;
+    {   // every chunk's T operands
+        auto kern = p.gate == 1 ? gdn_prep_kernel<1> : gdn_prep_kernel<0>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PR_TOTAL) != cudaSuccess)
+            return kErrCuda;
+        kern<<<bh * (unsigned)p.NC, kPrepThreads, PR_TOTAL, stream>>>(
+            (const __nv_bfloat16 *)p.k, (const __nv_bfloat16 *)p.beta, p.log_alpha, tops, (int)p.T, (int)p.H, p.NC);
+        if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+    }
+    CUtensorMap mq, mk, mv, mo;
+    if (!tc_make_map(&mq, p.q, p.B, p.T, p.H, false) || !tc_make_map(&mk, p.k, p.B, p.T, p.H, false) ||
+        !tc_make_map(&mv, p.v, p.B, p.T, p.H, false) ||
+        !tc_make_map(&mo, p.out ? p.out : p.q, p.B, p.T, p.H, p.out ? !p.out_bf16 : false))
+        return kErrCuda;
+    ChainArgs ca{p.log_alpha, (const __nv_bfloat16 *)p.beta, p.init_state, p.final_state, tops, status_word,
+                 (int)p.B, (int)p.T, (int)p.H, p.NC, 0, 1, p.NC, nullptr, nullptr, nullptr};
+    auto launch = [&](const ChainArgs &c, unsigned grid) {
+        if (p.out_bf16)
+            return p.gate == 1 ? launch_chain<__nv_bfloat16, 1>(mq, mk, mv, mo, c, grid, stream)
+                               : launch_chain<__nv_bfloat16, 0>(mq, mk, mv, mo, c, grid, stream);
+        return p.gate == 1 ? launch_chain<float, 1>(mq, mk, mv, mo, c, grid, stream)
+                           : launch_chain<float, 0>(mq, mk, mv, mo, c, grid, stream);
+    };
+    if (nseg <= 1) return launch(ca, bh);
+    // segments: end states (two runs per segment), chaining, then outputs
+    float *ws = reinterpret_cast<float *>(workspace);
+    const size_t per = (size_t)bh * nseg * 16384;
+    ca.nseg = nseg;
+    ca.seg_len = seg_len;
+    ca.ws_phi = ws;
+    ca.ws_s0 = ws + per;
+    ca.ws_start = ws + 2 * per;
+    ca.role = 1;
+    int rc = launch(ca, bh * nseg * 2);
+    if (rc != kOk) return rc;
+    rc = tc_launch_seg_combine(p.init_state, ca.ws_phi, ca.ws_s0, ca.ws_start, bh, nseg, stream);
+    if (rc != kOk) return rc;
+    ca.role = 2;
+    return launch(ca, bh * nseg);
+}
+
+}  // namespace dr

@@ -19,6 +19,7 @@
 #include <mutex>
 
 #include "../../include/dr.h"
+#include "chunk_layout.h"
 #include "common.cuh"
 
 namespace {
@@ -52,11 +53,13 @@ extern "C" int dr_chunk_fwd_noalloc(const dr_chunk_desc *desc, const void *q, co
                                     const float *init_state, void *out, float *final_state,
                                     dr_stream_t stream) {
     size_t need = 0;
-    const int rc = dr_chunk_fwd_workspace_bytes(desc, &need);
+    const int rc = dr::chunk_fwd_least_workspace(desc, &need);
     if (rc != DR_OK) return rc;
     if (need > kNoallocScratchBytes) return DR_ERR_WORKSPACE;   // beyond the built-in maximum
     void *scratch = nullptr;
-    if (need > 0) {
+    size_t full = 0;
+    dr_chunk_fwd_workspace_bytes(desc, &full);
+    if (need > 0 || full > 0) {
         const int st = scratch_address(&scratch);
         if (st != DR_OK) return st;
     }

@@ -33,7 +33,7 @@ DR_FUSE_QK_L2NORM, DR_FUSE_BETA_SIGMOID, DR_FUSE_OUT_SILU_GATE = 1, 2, 4
 L2NORM_EPS = 1e-6   # DR_L2NORM_EPS
 
 # Symbols of include/dr.h (checked by tests/test_abi.py against the header).
-EXPORTED = ("dr_version", "dr_chunk_fwd_workspace_bytes", "dr_chunk_fwd",
+EXPORTED = ("dr_version", "dr_chunk_fwd_workspace_bytes", "dr_chunk_fwd_min_workspace_bytes", "dr_chunk_fwd",
             "dr_recurrent_step", "dr_get_device_status", "dr_strerror",
             "dr_chunk_fwd_noalloc", "dr_chunk_fwd_ex", "dr_recurrent_step_ex",
             "dr_chunk_bwd_workspace_bytes", "dr_chunk_bwd", "dr_selftest_bounded_wait",
@@ -60,6 +60,9 @@ _lib.dr_version.restype = ctypes.c_int
 _lib.dr_chunk_fwd_workspace_bytes.argtypes = [ctypes.POINTER(ChunkDesc),
                                               ctypes.POINTER(ctypes.c_size_t)]
 _lib.dr_chunk_fwd_workspace_bytes.restype = ctypes.c_int
+_lib.dr_chunk_fwd_min_workspace_bytes.argtypes = [ctypes.POINTER(ChunkDesc),
+                                                  ctypes.POINTER(ctypes.c_size_t)]
+_lib.dr_chunk_fwd_min_workspace_bytes.restype = ctypes.c_int
 _lib.dr_chunk_fwd.argtypes = [ctypes.POINTER(ChunkDesc), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                               _vp, _vp, ctypes.c_size_t, _vp]
 _lib.dr_chunk_fwd.restype = ctypes.c_int
@@ -161,6 +164,14 @@ def workspace_bytes(desc: ChunkDesc) -> int:
     return n.value
 
 
+def min_workspace_bytes(desc: ChunkDesc) -> int:
+    n = ctypes.c_size_t(0)
+    rc = _lib.dr_chunk_fwd_min_workspace_bytes(ctypes.byref(desc), ctypes.byref(n))
+    if rc != DR_OK:
+        raise DrError(rc, "dr_chunk_fwd_min_workspace_bytes")
+    return n.value
+
+
 def chunk_fwd(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
               out_dtype=None, return_final_state: bool = True, out=None,
               final_state=None, workspace=None, stream=None, qk_l2norm: bool = False,
@@ -198,7 +209,8 @@ def chunk_fwd(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
         out = torch.empty((B, T, H, dv), dtype=_TORCH_DT[odt], device=q.device)
     if final_state is None and return_final_state:
         final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
-    need = workspace_bytes(desc)
+    # the fused neighbours run on paths that need only the least workspace
+    need = min_workspace_bytes(desc) if fuse else workspace_bytes(desc)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

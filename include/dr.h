@@ -106,9 +106,22 @@ enum { DR_FUSE_QK_L2NORM = 1, DR_FUSE_BETA_SIGMOID = 2, DR_FUSE_OUT_SILU_GATE = 
 /* Library version, (major << 16) | minor. */
 int dr_version(void);
 
-/* Bytes of device workspace dr_chunk_fwd needs for *desc; written to *bytes.  The answer
-   depends only on the descriptor.  Returns DR_OK, DR_ERR_INVALID or DR_ERR_UNSUPPORTED. */
+/* Bytes of device workspace dr_chunk_fwd takes for *desc on its fastest path; written to
+   *bytes.  The answer depends only on the descriptor.  Returns DR_OK, DR_ERR_INVALID or
+   DR_ERR_UNSUPPORTED.
+   For bf16 inputs, dk = dv = 128, chunk 64 and a scalar or no gate this is 16 KB per
+   (b, h, chunk) -- every chunk's triangular-solve operands (T = (I + A)^-1 of the WY form,
+   page "Transformer notes (5): linear attention optimisations", KDA paragraph), formed for
+   all chunks at once -- plus 3 * 64 KB per (b, h, segment) when few long chains are split
+   into segments. */
 int dr_chunk_fwd_workspace_bytes(const dr_chunk_desc *desc, size_t *bytes);
+
+/* The least workspace dr_chunk_fwd accepts for *desc; written to *bytes.  Equal to
+   dr_chunk_fwd_workspace_bytes() except for the configuration named there, where a
+   workspace below that size (but at least this one: only the segments' states, 0 unless
+   few long chains are split) selects a single kernel that solves inside each chain, with the
+   same results up to rounding.  Returns as dr_chunk_fwd_workspace_bytes. */
+int dr_chunk_fwd_min_workspace_bytes(const dr_chunk_desc *desc, size_t *bytes);
 
 /*
  * Chunkwise forward over T tokens for all B x H chains.
@@ -117,9 +130,10 @@ int dr_chunk_fwd_workspace_bytes(const dr_chunk_desc *desc, size_t *bytes);
  *   out          [B, T, H, dv] out_dtype (written)
  *   final_state  NULL = not returned, else [B, H, dk, dv] fp32 (written); may equal
  *                init_state for an in-place carry, must not overlap it otherwise
- *   workspace    device scratch of at least dr_chunk_fwd_workspace_bytes(); may be NULL
- *                when that size is 0.  Contents on entry are ignored; it must not be
- *                used by other work until this call's kernels finish on `stream`.
+ *   workspace    device scratch of at least dr_chunk_fwd_min_workspace_bytes() bytes
+ *                (dr_chunk_fwd_workspace_bytes() for the fastest path); may be NULL when
+ *                that size is 0.  Contents on entry are ignored; it must not be used by
+ *                other work until this call's kernels finish on `stream`.
  *
  * The chunk length C only changes rounding, never the result's definition.  A tail chunk
  * (T not a multiple of C) is padded with identity steps (k = 0, beta = 0, log_alpha = 0),
@@ -243,9 +257,10 @@ int dr_recurrent_step_ex(const dr_step_desc *desc, uint32_t fuse,
  * as for dr_chunk_fwd; the scratch comes from one static device array of
  * DR_NOALLOC_SCRATCH_BYTES that libdr.so holds on every GPU it is loaded on until exit.
  *
- *   - Problems whose dr_chunk_fwd_workspace_bytes() exceeds DR_NOALLOC_SCRATCH_BYTES are
- *     rejected with DR_ERR_WORKSPACE before anything is enqueued.  At bf16 inputs,
- *     dk = dv = 128, C = 64: the fused tensor-core path (scalar or no gate) needs none
+ *   - Problems whose dr_chunk_fwd_min_workspace_bytes() exceeds DR_NOALLOC_SCRATCH_BYTES
+ *     are rejected with DR_ERR_WORKSPACE before anything is enqueued; the fastest path is
+ *     taken whenever dr_chunk_fwd_workspace_bytes() fits.  At bf16 inputs,
+ *     dk = dv = 128, C = 64: the tensor-core path (scalar or no gate) needs none
  *     unless few long chains are split into segments; the per-channel gate needs 131,584
  *     bytes per (b, h, chunk), so there B * H * ceil(T / 64) <= 510.  The CUDA-core path
  *     (fp32 inputs, other sizes) needs 147,968 bytes per (b, h, chunk) at dk = dv = 128,

@@ -197,9 +197,29 @@ def test_tc_deterministic(dr):
     assert torch.equal(o1, o2) and torch.equal(f1, f2)
 
 
-def test_tc_needs_no_workspace(dr):
+def test_tc_workspace_sizes(dr):
+    # fastest path: one 16 KB T-operand image per (b, h, chunk); the single-kernel path
+    # needs none while the chains are not split into segments
     desc = dr.chunk_desc(8, 4096, 16, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_SCALAR, 64)
-    assert dr.workspace_bytes(desc) == 0
+    assert dr.workspace_bytes(desc) == 8 * 16 * 64 * 16384
+    assert dr.min_workspace_bytes(desc) == 0
+
+
+@pytest.mark.parametrize("gate", ["none", "scalar"])
+def test_tc_single_kernel_path_without_workspace(dr, gate):
+    """With less workspace than the T operands need, the single kernel solves inside each
+    chain; its results equal the oracle's as well."""
+    d = inputs.chunk_inputs(2, 333, 3, 128, 128, gate=gate, dtype="bf16", init_state=True,
+                            seed=61)
+    g = dev(d)
+    out, fin = dr.chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g["init_state"],
+                            workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    o_ref, f_ref = oracle.forward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                  d["init_state"])
+    assert_close(out, o_ref, "bf16", "out")
+    assert_close(fin, f_ref, "bf16", "final_state")
 
 
 # ------------------------------------------------------------ segmented long sequences
