@@ -151,7 +151,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
                 const PrepArgs a) {
     extern __shared__ unsigned char dsm_raw[];
-    unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *sm = align1024(dsm_raw);
     __shared__ uint64_t bar_ld, bar_mma;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s, diag_exact_s, four_rounds_s;
@@ -675,7 +675,7 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
                  const __grid_constant__ CUtensorMap to, const __grid_constant__ CUtensorMap tz,
                  const StateArgs a) {
     extern __shared__ unsigned char dsm_raw[];
-    unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *sm = align1024(dsm_raw);
     __shared__ uint64_t bar_w, bar_q, bar_u, bar_k, bar_p[2], bar_dw, bar_s, bar_pe, bar_z;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;

@@ -145,7 +145,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 const __grid_constant__ CUtensorMap tz, const TcArgs a) {
     constexpr bool FUSED = MODE == 1, CKPT = MODE == 2;
     extern __shared__ unsigned char dsm_raw[];
-    unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *sm = align1024(dsm_raw);
     // mbarriers: TMA stages; per MMA group its completion (committed by the MMA warp) and,
     // for the groups whose operands the compute warps write, "operands ready" (full_*,
     // arrived by thread 0 after the compute warps' barrier).  Each completes once per chunk.

@@ -38,6 +38,8 @@
 // bf16, as in chunk_tc.cu.  Every wait is bounded by a cycle budget: on expiry the kernel
 // records DR_ERR_TIMEOUT in the status word, stops, drains its own copies and MMAs with the
 // same bound, frees tensor memory and returns.
+#include <algorithm>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -65,134 +67,191 @@ using namespace tc;
 constexpr float kSpan = 80.f;
 
 // ============================================================ prep kernel
-// One CTA of four warps per (chain, chunk), all independent.  X = K K^T on the lower 16 x 16
-// blocks (mma.sync, bf16 in, fp32 out; warp w takes row block w), A_rs = beta_r exp(g_r - g_s)
-// X_rs for s < r (off-diagonal blocks TF32-rounded), then the blocked solve of tc_common.cuh,
-// which writes T diag(beta) | T diag(beta G) in bf16; the 16 KB image is copied to the
-// workspace.  Tokens past T are zero rows of K with beta = 0 (T is then the identity there),
-// as the chain kernel's loads make them.
+// Persistent CTAs of four warps walk the (chain, chunk) pairs; per chunk, all independent:
+// the k tile arrives by TMA (128-byte swizzle; the next chunk's tile is prefetched into L2
+// meanwhile), X = K K^T on the lower 16 x 16 blocks (mma.sync, bf16 in, fp32 out, fragments
+// by ldmatrix; warp w takes row block w), A_rs = beta_r exp(g_r - g_s) X_rs for s < r
+// (off-diagonal blocks TF32-rounded), then the blocked solve of tc_common.cuh, which writes
+// T diag(beta) | T diag(beta G) in bf16; the 16 KB image leaves by one bulk store.  Tokens
+// past T are zero rows of K (the TMA fill) with beta = 0, T being the identity there, as the
+// chain kernel's loads make them.
 constexpr int kPrepThreads = 128;
-constexpr int kLdK = 136;                          // K tile row pitch (bf16): conflict-free fragments
-constexpr uint32_t PR_K = 0;                       // K tile [64][136] bf16; then fp32 T (swizzled)
-constexpr uint32_t PR_A = 64 * kLdK * 2;           // fp32 A (a_index)
+constexpr uint32_t PR_K = 0;                       // k tile (two 64-channel halves, swizzled);
+                                                   // then the fp32 T (swizzled)
+constexpr uint32_t PR_A = 16384;                   // fp32 A (a_index)
 constexpr uint32_t PR_TB = PR_A + 16384;           // the operand image
 constexpr uint32_t PR_M = PR_TB + 16384;           // solve scratch
 constexpr uint32_t PR_V = PR_M + 4096;             // g, G, beta, exp(g - g_31), exp(g_31 - g)
 constexpr uint32_t PR_TOTAL = PR_V + 5 * 256;
-static_assert(PR_A >= 16384, "T fits over the K tile");
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+
+// As ldsm_x4, transposed: thread t receives rows 2 (t % 4), 2 (t % 4) + 1 of column t / 4 of
+// each 8 x 8 matrix.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
 
 template <int GATE>
 __global__ void __launch_bounds__(kPrepThreads, 4)
-gdn_prep_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ beta,
-                const float *__restrict__ log_alpha, unsigned char *__restrict__ tops, int T, int H, int NC) {
-    extern __shared__ float4 prep_sm4[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>(prep_sm4);
-    __shared__ int fac_s;
+gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __nv_bfloat16 *__restrict__ beta,
+                const float *__restrict__ log_alpha, unsigned char *__restrict__ tops, int T, int H, int NC,
+                unsigned nchunks, int *status) {
+    extern __shared__ unsigned char prep_sm[];
+    unsigned char *sm = align1024(prep_sm);
+    __shared__ uint64_t bar_k;
+    __shared__ int fac_s, abort_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = (int)(blockIdx.x % (unsigned)NC), bh = (int)(blockIdx.x / (unsigned)NC);
-    const int h = bh % H, b = bh / H, t0 = c * 64;
-    __nv_bfloat16 *sK = reinterpret_cast<__nv_bfloat16 *>(sm + PR_K);
     float *sA = reinterpret_cast<float *>(sm + PR_A);
     float *sV = reinterpret_cast<float *>(sm + PR_V);
     float *sG = sV, *sGam = sV + 64, *sBeta = sV + 128, *sE = sV + 192, *sF = sV + 256;
-
-    // the K tile: 64 rows of 256 bytes, rows past T zero
-    for (int i = tid; i < 64 * 16; i += kPrepThreads) {
-        const int r = i >> 4, q = i & 15, t = t0 + r;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (t < T) v = *reinterpret_cast<const uint4 *>(k + (((size_t)b * T + t) * H + h) * 128 + 8 * q);
-        *reinterpret_cast<uint4 *>(sK + r * kLdK + 8 * q) = v;
-    }
-    if (warp == 0) {   // the chunk's gates, two tokens per lane
-        float l[2], bt[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int t = t0 + 2 * lane + e;
-            const size_t tok = ((size_t)b * T + t) * H + h;
-            bt[e] = t < T ? __bfloat162float(beta[tok]) : 0.f;
-            l[e] = (GATE == 1 && t < T) ? log_alpha[tok] : 0.f;
-        }
-        float p = l[0] + l[1];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, p, o);
-            if (lane >= o) p += y;
-        }
-        const float g1 = p, g0 = p - l[1];
-        const float glast = __shfl_sync(0xffffffffu, g1, 31);
-        const float gmid = __shfl_sync(0xffffffffu, g1, 15);
-        const float gfirst = __shfl_sync(0xffffffffu, g0, 0);
-        const int r = 2 * lane;
-        sG[r] = g0; sG[r + 1] = g1;
-        sBeta[r] = bt[0]; sBeta[r + 1] = bt[1];
-        sGam[r] = __expf(g0); sGam[r + 1] = __expf(g1);
-        const bool fac = gfirst - glast < kSpan;
-        if (fac) {
-            sE[r] = __expf(g0 - gmid); sE[r + 1] = __expf(g1 - gmid);
-            sF[r] = __expf(gmid - g0); sF[r + 1] = __expf(gmid - g1);
-        }
-        if (lane == 0) fac_s = fac;
+    if (tid == 0) {
+        mbar_init(&bar_k, 1);
+        abort_s = 0;
+        fence_mbar_init();
     }
     __syncthreads();
-
-    // X on the lower blocks and A from it: warp w owns rows 16 w .. 16 w + 15
-    {
-        const int g = lane >> 2, t4 = lane & 3, r0 = 16 * warp;
-        const bool fac = fac_s != 0;
-        auto ld = [&](int r, int col) { return *reinterpret_cast<const uint32_t *>(sK + r * kLdK + col); };
-        for (int cb = 0; cb <= warp; ++cb) {
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int kk = 0; kk < 128; kk += 16) {
-                const uint32_t af[4] = {ld(r0 + g, kk + 2 * t4), ld(r0 + g + 8, kk + 2 * t4),
-                                        ld(r0 + g, kk + 8 + 2 * t4), ld(r0 + g + 8, kk + 8 + 2 * t4)};
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int sr = 16 * cb + 8 * nt + g;
-                    mma_bf16_16x8x16(acc[nt], af, ld(sr, kk + 2 * t4), ld(sr, kk + 8 + 2 * t4));
+    auto coords = [&](unsigned n, int &h, int &b, int &t0) {
+        const int c = (int)(n % (unsigned)NC), bh = (int)(n / (unsigned)NC);
+        h = bh % H; b = bh / H; t0 = c * 64;
+    };
+    uint32_t phase = 0;
+    for (unsigned n = blockIdx.x; n < nchunks; n += gridDim.x, phase ^= 1) {
+        int h, b, t0;
+        coords(n, h, b, t0);
+        if (tid == 0) {
+            // the previous chunk's image must have been read out before the solve rewrites it
+            bulk_wait_read_all();
+            mbar_arrive_expect_tx(&bar_k, 16384);
+            for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + PR_K + kb * 8192, &tk, &bar_k, 64 * kb, h, t0, b);
+            const unsigned nn = n + gridDim.x;
+            if (nn < nchunks) {
+                int h2, b2, t2;
+                coords(nn, h2, b2, t2);
+                for (int kb = 0; kb < 2; ++kb) tma_prefetch_4d(&tk, 64 * kb, h2, t2, b2);
+            }
+        }
+        if (warp == 1) {   // the next chunk's gates into L2 (two tokens per lane)
+            const unsigned nn = n + gridDim.x;
+            if (nn < nchunks) {
+                int h2, b2, t2;
+                coords(nn, h2, b2, t2);
+                const int t = t2 + 2 * lane;
+                if (t < T) {
+                    const size_t tok = ((size_t)b2 * T + t) * H + h2;
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(beta + tok));
+                    if (GATE == 1) asm volatile("prefetch.global.L2 [%0];" ::"l"(log_alpha + tok));
                 }
             }
+        }
+        if (warp == 0) {   // the chunk's gates, two tokens per lane
+            float l[2], bt[2];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int e = 0; e < 2; ++e) {
+                const int t = t0 + 2 * lane + e;
+                const size_t tok = ((size_t)b * T + t) * H + h;
+                bt[e] = t < T ? __bfloat162float(beta[tok]) : 0.f;
+                l[e] = (GATE == 1 && t < T) ? log_alpha[tok] : 0.f;
+            }
+            float p = l[0] + l[1];
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int r = r0 + g + 8 * hf, s0 = 16 * cb + 8 * nt + 2 * t4;
-                    float v[2];
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, p, o);
+                if (lane >= o) p += y;
+            }
+            const float g1 = p, g0 = p - l[1];
+            const float glast = __shfl_sync(0xffffffffu, g1, 31);
+            const float gmid = __shfl_sync(0xffffffffu, g1, 15);
+            const float gfirst = __shfl_sync(0xffffffffu, g0, 0);
+            const int r = 2 * lane;
+            sG[r] = g0; sG[r + 1] = g1;
+            sBeta[r] = bt[0]; sBeta[r + 1] = bt[1];
+            sGam[r] = __expf(g0); sGam[r + 1] = __expf(g1);
+            const bool fac = gfirst - glast < kSpan;
+            if (fac) {
+                sE[r] = __expf(g0 - gmid); sE[r + 1] = __expf(g1 - gmid);
+                sF[r] = __expf(gmid - g0); sF[r + 1] = __expf(gmid - g1);
+            }
+            if (lane == 0) fac_s = fac;
+        }
+        if (!wait_cycles(&bar_k, phase)) {
+            abort_s = 1;
+            atomicExch(status, kErrTimeout);
+        }
+        __syncthreads();
+        if (abort_s) break;
+
+        // X on the lower blocks and A from it: warp w owns rows 16 w .. 16 w + 15
+        {
+            const int g = lane >> 2, t4 = lane & 3, r0 = 16 * warp;
+            const bool fac = fac_s != 0;
+            const uint32_t kbase = smem_u32(sm + PR_K);
+            // ldmatrix row address: tile row `row`, 8-element chunk `kc` (of 16 per row)
+            auto addr = [&](int row, int kc) {
+                return kbase + (uint32_t)((kc >> 3) * 8192 + row * 128 + (((kc & 7) ^ (row & 7)) << 4));
+            };
+            const int mi = lane >> 3, mr = lane & 7;
+            uint32_t af[8][4];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int s = s0 + e;
-                        const float dec = fac ? sE[r] * sF[s] : __expf(fminf(sG[r] - sG[s], 0.f));
-                        v[e] = s < r ? sBeta[r] * dec * acc[nt][2 * hf + e] : 0.f;
-                        if (cb != warp) v[e] = round_tf32(v[e]);
-                    }
-                    *reinterpret_cast<float2 *>(sA + a_index(r, s0)) = make_float2(v[0], v[1]);
+            for (int ks = 0; ks < 8; ++ks) ldsm_x4(addr(r0 + mr + 8 * (mi & 1), 2 * ks + (mi >> 1)), af[ks]);
+            for (int cb = 0; cb <= warp; ++cb) {
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t bf[4];
+                    ldsm_x4(addr(16 * cb + mr + 8 * (mi >> 1), 2 * ks + (mi & 1)), bf);
+                    mma_bf16_16x8x16(acc[0], af[ks], bf[0], bf[1]);
+                    mma_bf16_16x8x16(acc[1], af[ks], bf[2], bf[3]);
                 }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int r = r0 + g + 8 * hf, s0 = 16 * cb + 8 * nt + 2 * t4;
+                        float v[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int s = s0 + e;
+                            const float dec = fac ? sE[r] * sF[s] : __expf(fminf(sG[r] - sG[s], 0.f));
+                            v[e] = s < r ? sBeta[r] * dec * acc[nt][2 * hf + e] : 0.f;
+                            if (cb != warp) v[e] = round_tf32(v[e]);
+                        }
+                        *reinterpret_cast<float2 *>(sA + a_index(r, s0)) = make_float2(v[0], v[1]);
+                    }
+            }
+        }
+        __syncthreads();   // the k tile is dead: T goes over it
+
+        const SolveOut<true, true, true> out{reinterpret_cast<float *>(sm + PR_K), sm + PR_TB, sBeta, sGam, nullptr};
+        solve_diag64(sA, out, tid);          // diagonal blocks 0, 1 (and operand zero blocks)
+        solve_diag64(sA, out, tid + 128);    // diagonal blocks 2, 3
+        __syncthreads();
+        solve_merge64(sA, out, reinterpret_cast<float *>(sm + PR_M), tid, 1);
+        __syncthreads();   // (the merge ends with the operands' proxy fence)
+        if (tid == 0) {
+            bulk_store(tops + (size_t)n * 16384, sm + PR_TB, 16384);
+            bulk_commit();
         }
     }
-    __syncthreads();   // the K tile is dead: T goes over it
-
-    const SolveOut<true, true, true> out{reinterpret_cast<float *>(sm + PR_K), sm + PR_TB, sBeta, sGam, nullptr};
-    solve_diag64(sA, out, tid);          // diagonal blocks 0, 1 (and operand zero blocks)
-    solve_diag64(sA, out, tid + 128);    // diagonal blocks 2, 3
-    __syncthreads();
-    solve_merge64(sA, out, reinterpret_cast<float *>(sm + PR_M), tid, 1);
-    __syncthreads();
-    uint4 *dst = reinterpret_cast<uint4 *>(tops + ((size_t)bh * NC + c) * 16384);
-    const uint4 *src = reinterpret_cast<const uint4 *>(sm + PR_TB);
-#pragma unroll
-    for (int i = tid; i < 1024; i += kPrepThreads) dst[i] = src[i];
+    if (tid == 0) bulk_wait_all();
 }
 
 // ============================================================ chain kernel
 constexpr int kChainThreads = 352;             // 11 warps
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpGate = 2, kWarpS0 = 3, kWarpO0 = 7;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpGate = 2, kWarpO0 = 7;   // state warps: 3..6
 // shared memory (offsets from the 1024-byte-aligned base)
-constexpr uint32_t C_STAGE = 49152;            // one q/k stage: two K-blocks of [W | Q | K]
-constexpr uint32_t C_KB = 24576;               // one K-block (64 of the 128 key channels)
-constexpr uint32_t C_OFF_Q = 8192, C_OFF_K = 16384;
-constexpr uint32_t C_VT = 2 * C_STAGE;         // v tile (two 64-channel halves) and T operands
-constexpr uint32_t C_TB = C_VT + 16384;        // T diag(beta) | T diag(beta G) (bf16, 8 KB each)
-constexpr uint32_t C_BU = C_VT + 32768;        // tf32 [P; Kt^T]: two K-blocks of 32 tokens
+constexpr uint32_t C_STAGE = 49152;            // one q/k stage: two K-blocks of [Q | K], then W^T
+constexpr uint32_t C_KB = 16384;               // one K-block (64 of the 128 key channels)
+constexpr uint32_t C_OFF_Q = 0, C_OFF_K = 8192;
+constexpr uint32_t C_OFF_W = 32768;            // W^T (128 key channels x 64 tokens, bf16, MN-major)
+constexpr uint32_t C_VU = 2 * C_STAGE;         // v tile (two 64-channel halves) and T diag(beta)
+constexpr uint32_t C_TB = C_VU + 16384;        //   T diag(beta) (bf16, 8 KB)
+constexpr uint32_t C_WT = C_VU + 24576;        // T diag(beta G) of two chunks (8 KB each)
+constexpr uint32_t C_BU = C_WT + 16384;        // tf32 [P; Kt^T]: two K-blocks of 32 tokens
 constexpr uint32_t C_BU_KB = 24576;            // 192 rows x 128 bytes
 constexpr uint32_t C_OUT = C_BU + 2 * C_BU_KB; // output staging (bf16: 2 boxes, fp32: 4 boxes)
 constexpr uint32_t C_SMALL = C_OUT + 32768;    // gate vectors [2][6][64] and raw gates [2][128]
@@ -211,7 +270,8 @@ enum { GV_G = 0, GV_GAM = 1, GV_DEL = 2, GV_BETA = 3, GV_E = 4, GV_F = 5 };
 
 constexpr uint32_t ID_X = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_UW = idesc_bf16(128, 64, true, false);
-constexpr uint32_t ID_D = idesc_bf16(128, 128, false, false);
+constexpr uint32_t ID_WS = idesc_bf16(128, 64, false, true);   // B = W^T rows (MN-major)
+constexpr uint32_t ID_QS = idesc_bf16(128, 64, false, false);  // B = Q rows (K-major)
 constexpr uint32_t ID_UPD = idesc_tf32(128, 192);
 constexpr uint32_t ID_UPD_S = idesc_tf32(128, 128);
 
@@ -236,15 +296,21 @@ __device__ __forceinline__ uint32_t sw128_off32(uint32_t row, uint32_t k) {
     return row * 128u + ((((k >> 2) ^ (row & 7u)) & 7u) << 4) + ((k & 3u) << 2);
 }
 
+// Per chunk it (period: from the state update of it - 1 to that of it), the MMA warp issues
+//   [W S | Q S](it)  W(it + 1)  X(it + 1)  update(it)  U(it + 1)
+// so that only the state's own steps sit between two updates: S^T -> bf16 (warps 3..6),
+// [W S | Q S], E (warps 3..6), update.  Everything else is formed a chunk ahead or behind:
+// W(it + 1) and its conversion during chunk it (its T operand has a double buffer), P and
+// Kt^T of chunk it by warps 7..10 while S^T converts, the output of it - 1 by them first.
 template <typename Tout, int GATE>
 __global__ void __launch_bounds__(kChainThreads, 1)
 gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
                  const ChainArgs a) {
     extern __shared__ unsigned char dsm_raw[];
-    unsigned char *sm = (unsigned char *)(((uintptr_t)dsm_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *sm = align1024(dsm_raw);
     // Completed by TMA transactions or tcgen05.commit (count 1) ...
-    __shared__ uint64_t qkw_full[2], vt_full, x_done, uw_done, d_done, u_done;
+    __shared__ uint64_t qkw_full[2], wt_full[2], wt_free[2], vu_full, x_done, w_done, uu_done, d_done, u_done;
     // ... or by every thread of a group (stage_free: the commit of [W S | Q S] and warps
     // 7..10 after Kt^T; gset_free: warps 3..10 after their last use of a gate set).
     __shared__ uint64_t sb_ready, p_ready, e_ready, w_ready, kt_ready, o_read;
@@ -283,13 +349,15 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     }
     const int h = bh % a.H, b = bh / a.H;
     const int n_it = c_end - c_begin;
+    auto tops = [&](int it) { return a.tops + ((size_t)bh * a.NC + c_begin + it) * 16384; };
 
     float *sVec = reinterpret_cast<float *>(sm + C_SMALL);   // [2][6][64]
     auto vec = [&](int it, int k) { return sVec + (it & 1) * 384 + 64 * k; };
     uint32_t *sGate = reinterpret_cast<uint32_t *>(sm + C_SMALL + 3072);   // [2][beta word | log alpha][64]
 
     if (tid == 0) {
-        uint64_t *ones[] = {&qkw_full[0], &qkw_full[1], &vt_full, &x_done, &uw_done, &d_done, &u_done};
+        uint64_t *ones[] = {&qkw_full[0], &qkw_full[1], &wt_full[0], &wt_full[1], &wt_free[0], &wt_free[1],
+                            &vu_full,     &x_done,      &w_done,     &uu_done,    &d_done,     &u_done};
         for (uint64_t *bb : ones) mbar_init(bb, 1);
         uint64_t *groups[] = {&sb_ready, &p_ready, &e_ready, &w_ready, &kt_ready, &o_read};
         for (uint64_t *bb : groups) mbar_init(bb, 128);
@@ -331,12 +399,29 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     };
 
     if (warp == kWarpTma) {
-        // ---------------- TMA: q, k of chunk it into stage it % 2 once the chunk two back has
-        // left it; v and T operands of chunk it once U/W(it - 1) have read the previous ones
+        // ---------------- TMA.  Chunk it's q, k into stage it % 2 and its T diag(beta G) into
+        // its slot once chunk it - 2 has left them; its v and T diag(beta) once U(it - 1) has
+        // read the previous ones.
         if (lane == 0) {
-            int q_last[2] = {-1, -1}, v_last = -1;
+            int q_last[2] = {-1, -1}, w_last[2] = {-1, -1}, v_last = -1;
+            // chunk `it`'s tiles into L2 ahead of their loads (kPrefetch chunks ahead: the
+            // loads themselves run about one chunk ahead, less than the memory latency of a
+            // GPU full of chains)
+            constexpr int kPrefetch = 2;
+            auto prefetch = [&](int it) {
+                if (it >= n_it) return;
+                const int t0 = (c_begin + it) * 64;
+                for (int kb = 0; kb < 2; ++kb) {
+                    tma_prefetch_4d(&tq, 64 * kb, h, t0, b);
+                    tma_prefetch_4d(&tk, 64 * kb, h, t0, b);
+                    if (!zero_u) tma_prefetch_4d(&tv, 64 * kb, h, t0, b);
+                }
+                bulk_prefetch_l2(tops(it), 16384);
+            };
+            for (int it = 1; it < kPrefetch; ++it) prefetch(it);
             for (int it = 0; it < n_it; ++it) {
                 const int s = it & 1, t0 = (c_begin + it) * 64;
+                prefetch(it + kPrefetch);
                 if (it >= 2 && !wait_bar(&stage_free[s], ((it - 2) >> 1) & 1)) break;
                 unsigned char *st = stage(it);
                 mbar_arrive_expect_tx(&qkw_full[s], 32768);
@@ -345,22 +430,28 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     tma_load_4d(st + kb * C_KB + C_OFF_K, &tk, &qkw_full[s], 64 * kb, h, t0, b);
                 }
                 q_last[s] = it;
-                if (it >= 1 && !wait_bar(&uw_done, (it - 1) & 1)) break;
-                mbar_arrive_expect_tx(&vt_full, zero_u ? 16384 : 32768);
-                if (!zero_u)
-                    for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + C_VT + kb * 8192, &tv, &vt_full, 64 * kb, h, t0, b);
-                bulk_load(sm + C_TB, a.tops + ((size_t)bh * a.NC + c_begin + it) * 16384, 16384, &vt_full);
-                v_last = it;
+                if (it >= 2 && !wait_bar(&wt_free[s], ((it - 2) >> 1) & 1)) break;
+                mbar_arrive_expect_tx(&wt_full[s], 8192);
+                bulk_load(sm + C_WT + s * 8192, tops(it) + 8192, 8192, &wt_full[s]);
+                w_last[s] = it;
+                if (it >= 1 && !wait_bar(&uu_done, (it - 1) & 1)) break;
+                if (!zero_u) {
+                    mbar_arrive_expect_tx(&vu_full, 24576);
+                    for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + C_VU + kb * 8192, &tv, &vu_full, 64 * kb, h, t0, b);
+                    bulk_load(sm + C_TB, tops(it), 8192, &vu_full);
+                    v_last = it;
+                }
             }
             if (*abort_v) {   // loads this thread issued may still be in flight (bounded waits)
-                for (int s = 0; s < 2; ++s)
+                for (int s = 0; s < 2; ++s) {
                     if (q_last[s] >= 0) wait_cycles(&qkw_full[s], (q_last[s] >> 1) & 1);
-                if (v_last >= 0) wait_cycles(&vt_full, v_last & 1);
+                    if (w_last[s] >= 0) wait_cycles(&wt_full[s], (w_last[s] >> 1) & 1);
+                }
+                if (v_last >= 0) wait_cycles(&vu_full, v_last & 1);
             }
         }
     } else if (warp == kWarpMma) {
-        // ---------------- MMA issue: per chunk [W S | Q S](it), X(it + 1), the state update and
-        // output product (it), then U/W(it + 1)
+        // ---------------- MMA issue
         if (lane == 0 && n_it > 0) {
             uint64_t *last = nullptr;
             uint32_t last_par = 0;
@@ -374,45 +465,64 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 mma_commit(&x_done);
                 last = &x_done; last_par = it & 1;
             };
-            auto issue_uw = [&](int it) {  // U^T = V^T (T diag beta)^T, W^T = K^T (T diag(beta G))^T
-                const uint32_t sk = (uint32_t)(stage(it) - sm) + C_OFF_K;
+            auto issue_w = [&](int it) {   // W^T = K^T (T diag(beta G))^T
+                const uint32_t sk = (uint32_t)(stage(it) - sm) + C_OFF_K, wt = C_WT + (it & 1) * 8192;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmb + TM_W, desc_add(dMk, sk + ks * 2048), desc_add(dK0, wt + ks * 32), ID_UW, ks > 0);
+                mma_commit(&w_done);
+                mma_commit(&wt_free[it & 1]);
+                last = &w_done; last_par = it & 1;
+            };
+            auto issue_u = [&](int it) {   // U^T = V^T (T diag beta)^T
                 if (!zero_u)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmb + TM_U, desc_add(dMv, C_VT + ks * 2048), desc_add(dK0, C_TB + ks * 32), ID_UW,
+                        mma_bf16(tmb + TM_U, desc_add(dMv, C_VU + ks * 2048), desc_add(dK0, C_TB + ks * 32), ID_UW,
                                  ks > 0);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmb + TM_W, desc_add(dMk, sk + ks * 2048), desc_add(dK0, C_TB + 8192 + ks * 32), ID_UW,
-                             ks > 0);
-                mma_commit(&uw_done);
-                last = &uw_done; last_par = it & 1;
+                mma_commit(&uu_done);
+                last = &uu_done; last_par = it & 1;
             };
             bool ok = true;
             if (outputs) {
                 ok = wait_bar(&qkw_full[0], 0);
                 if (ok) issue_x(0);
             }
-            ok = ok && wait_bar(&vt_full, 0);
-            if (ok) issue_uw(0);
+            ok = ok && wait_bar(&qkw_full[0], 0) && wait_bar(&wt_full[0], 0);
+            if (ok) issue_w(0);
+            ok = ok && (zero_u || wait_bar(&vu_full, 0));
+            if (ok) issue_u(0);
             for (int it = 0; ok && it < n_it; ++it) {
                 const uint32_t par = it & 1;
                 const int s = it & 1;
                 const bool next = it + 1 < n_it;
-                // [W S | Q S](it): A = S^T (bf16 pairs in tensor memory), B = [W; Q] (stage)
+                // (W S)^T and (Q S)^T: A = S^T (bf16 pairs in tensor memory), B = W^T (MN-major
+                // rows written by warps 7..10) and Q (the stage)
                 if (!wait_bar(&sb_ready, par) || !wait_bar(&w_ready, par)) break;
                 if (outputs && it >= 1 && !wait_bar(&o_read, par ^ 1)) break;
                 const uint32_t sw = (uint32_t)(stage(it) - sm);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ts(tmb + TM_WE, tmb + TM_SB + 8 * ks,
-                                desc_add(dK0, sw + (ks >> 2) * C_KB + (ks & 3) * 32), ID_D, ks > 0);
+                    mma_bf16_ts(tmb + TM_WE, tmb + TM_SB + 8 * ks, desc_add(dMk, sw + C_OFF_W + ks * 2048), ID_WS,
+                                ks > 0);
+                if (outputs)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ts(tmb + TM_QO, tmb + TM_SB + 8 * ks,
+                                    desc_add(dK0, sw + C_OFF_Q + (ks >> 2) * C_KB + (ks & 3) * 32), ID_QS, ks > 0);
                 mma_commit(&d_done);
                 mma_commit(&stage_free[s]);
                 last = &d_done; last_par = par;
-                // X(it + 1) once P(it) has been read out of TM_X
+                // W(it + 1): its conversion (warps 7..10) has all of this chunk's time
+                if (next) {
+                    if (!wait_bar(&qkw_full[(it + 1) & 1], ((it + 1) >> 1) & 1) ||
+                        !wait_bar(&wt_full[(it + 1) & 1], ((it + 1) >> 1) & 1))
+                        break;
+                    issue_w(it + 1);
+                }
+                // X(it + 1) once P(it) has been read out of TM_X: it runs while E(it) forms
                 if (outputs && next) {
-                    if (!wait_bar(&qkw_full[(it + 1) & 1], ((it + 1) >> 1) & 1) || !wait_bar(&p_ready, par)) break;
+                    if (!wait_bar(&p_ready, par)) break;
                     issue_x(it + 1);
                 }
                 // [O^T | S^T] += E^T [P; Kt^T]^T  (tf32; E^T from tensor memory)
@@ -425,9 +535,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                                 outputs ? ID_UPD : ID_UPD_S, true);
                 mma_commit(&u_done);
                 last = &u_done; last_par = par;
+                // U(it + 1) (E(it) has read U(it))
                 if (next) {
-                    if (!wait_bar(&vt_full, (it + 1) & 1)) break;
-                    issue_uw(it + 1);
+                    if (!zero_u && !wait_bar(&vu_full, (it + 1) & 1)) break;
+                    issue_u(it + 1);
                 }
             }
             if (*abort_v && last) wait_cycles(last, last_par);   // drain (bounded)
@@ -505,7 +616,8 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
         cp_async_wait_all();
     } else if (warp < kWarpO0) {
-        // ---------------- state warps (TMEM lane j = row of S^T, value channel j)
+        // ---------------- state warps (TMEM lane j = row of S^T, value channel j): the two
+        // steps of the state's own chain
         {
             float v[32];
             for (int part = 0; part < 4; ++part) {
@@ -522,75 +634,50 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const uint32_t par = it & 1;
             if (it >= 1 && !wait_bar(&u_done, par ^ 1)) break;
             if (!wait_bar(&g_ready[it & 1], (it >> 1) & 1)) break;
-            // S^T -> bf16 pairs (the A operand of [W S | Q S]) and S^T <- gamma S^T
+            // S^T -> bf16 pairs (the A operand of [W S | Q S]) and S^T <- gamma S^T, two
+            // 32-column parts per TMEM round trip
             {
                 const float gamma = vec(it, GV_GAM)[63];
-                float v[32];
 #pragma unroll 1
-                for (int part = 0; part < 4; ++part) {
-                    tmem_ld32(tm + TM_S + 32 * part, v);
+                for (int pp = 0; pp < 2; ++pp) {
+                    float v[2][32];
+                    tmem_ld32(tm + TM_S + 64 * pp, v[0]);
+                    tmem_ld32(tm + TM_S + 64 * pp + 32, v[1]);
                     tmem_wait_ld();
-                    uint32_t pk[16];
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
-                    tmem_st16u(tm + TM_SB + 16 * part, pk);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) v[u] *= gamma;
-                    tmem_st32(tm + TM_S + 32 * part, v);
+                        for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(v[hh][2 * u], v[hh][2 * u + 1]);
+                        tmem_st16u(tm + TM_SB + 32 * pp + 16 * hh, pk);
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) v[hh][u] *= gamma;
+                        tmem_st32(tm + TM_S + 64 * pp + 32 * hh, v[hh]);
+                    }
                 }
                 tmem_wait_st();
             }
             tc_fence_before();
             mbar_arrive(&sb_ready);
-            // P(it) from the Q K^T rows of X (lanes 0..63), tf32, into rows 0..63 of [P; Kt^T]
-            if (outputs) {
-                if ((warp & 3) < 2) {
-                    if (!wait_bar(&x_done, par)) break;
-                    float x[64];
-                    tmem_ld32(tm + TM_X, *reinterpret_cast<float(*)[32]>(x));
-                    tmem_ld32(tm + TM_X + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-                    tmem_wait_ld();
-                    const int r = row;
-                    const float *sG = vec(it, GV_G), *sE = vec(it, GV_E), *sF = vec(it, GV_F);
-                    const bool fac = fac_s[it & 1] != 0;
-                    const float er = sE[r], gr = sG[r];
-#pragma unroll
-                    for (int c4 = 0; c4 < 16; ++c4) {
-                        float pv[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int s = 4 * c4 + e;
-                            const float dec = fac ? er * sF[s] : __expf(fminf(gr - sG[s], 0.f));
-                            pv[e] = s <= r ? round_tf32(dec * x[s]) : 0.f;
-                        }
-                        *reinterpret_cast<float4 *>(sm + C_BU + (c4 >> 3) * C_BU_KB + sw128_off32(r, 4 * (c4 & 7))) =
-                            make_float4(pv[0], pv[1], pv[2], pv[3]);
-                    }
-                    fence_proxy_async();
-                }
-                tc_fence_before();
-                mbar_arrive(&p_ready);
-            }
-            // E^T = U^T - (W S)^T in place of (W S)^T (fp32, tf32-rounded: the next product's
-            // A operand) and G (Q S)^T in place of (Q S)^T
+            // E^T = U^T - (W S)^T in place of (W S)^T (fp32: the next product's A operand,
+            // read as tf32) and G (Q S)^T in place of (Q S)^T
             if (!wait_bar(&d_done, par)) break;
             {
                 const float *sGam = vec(it, GV_GAM);
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
-                    float ws[32], uu[32];
+                    float ws[32], uu[32], qs[32];
                     tmem_ld32(tm + TM_WE + 32 * hh, ws);
                     if (!zero_u) tmem_ld32(tm + TM_U + 32 * hh, uu);
+                    if (outputs) tmem_ld32(tm + TM_QO + 32 * hh, qs);
                     tmem_wait_ld();
 #pragma unroll
                     for (int u = 0; u < 32; ++u) ws[u] = round_tf32((zero_u ? 0.f : uu[u]) - ws[u]);
                     tmem_st32(tm + TM_WE + 32 * hh, ws);
                     if (outputs) {
-                        tmem_ld32(tm + TM_QO + 32 * hh, uu);
-                        tmem_wait_ld();
 #pragma unroll
-                        for (int u = 0; u < 32; ++u) uu[u] *= sGam[32 * hh + u];
-                        tmem_st32(tm + TM_QO + 32 * hh, uu);
+                        for (int u = 0; u < 32; ++u) qs[u] *= sGam[32 * hh + u];
+                        tmem_st32(tm + TM_QO + 32 * hh, qs);
                     }
                 }
                 tmem_wait_st();
@@ -611,20 +698,27 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
     } else {
         // ---------------- operand / output warps
-        const int to_ = tid - 32 * kWarpO0;   // 0..127: key channel i of Kt^T
+        const int to_ = tid - 32 * kWarpO0;   // 0..127
         constexpr int kOutBoxes = sizeof(Tout) == 2 ? 2 : 4;
+        const bool prows = (warp & 3) < 2;    // TMEM lanes 0..63: the Q K^T rows of X
         // W^T (lane i = key channel, 64 tokens) -> W (bf16, K-major) in the W slot of stage it
         auto convert_w = [&](int it) -> bool {
-            if (!wait_bar(&uw_done, it & 1)) return false;
-            float w[64];
-            tmem_ld32(tm + TM_W, *reinterpret_cast<float(*)[32]>(w));
-            tmem_ld32(tm + TM_W + 32, *reinterpret_cast<float(*)[32]>(w + 32));
-            tmem_wait_ld();
-            unsigned char *dst = stage(it) + (row >> 6) * C_KB;
-            const int ic = row & 63;
+            if (!wait_bar(&w_done, it & 1)) return false;
+            // row i of W^T (64 tokens, 128 bytes): the MN-major B operand of (W S)^T
+            unsigned char *dst = stage(it) + C_OFF_W + row * 128;
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                float w[32];
+                tmem_ld32(tm + TM_W + 32 * hh, w);
+                tmem_wait_ld();
 #pragma unroll
-            for (int r = 0; r < 64; ++r)
-                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(r, ic)) = __float2bfloat16_rn(w[r]);
+                for (int c = 0; c < 4; ++c) {
+                    const float *f = w + 8 * c;
+                    *reinterpret_cast<uint4 *>(dst + (((4 * hh + c) ^ (row & 7)) << 4)) =
+                        make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                                   pack_bf16(f[6], f[7]));
+                }
+            }
             fence_proxy_async();
             tc_fence_before();
             mbar_arrive(&w_ready);
@@ -632,27 +726,33 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         };
         // chunk it's output O^T (lane j = value channel, 64 tokens) -> staging -> TMA store
         auto emit = [&](int it) {
-            float o[64];
-            tmem_ld32(tm + TM_QO, *reinterpret_cast<float(*)[32]>(o));
-            tmem_ld32(tm + TM_QO + 32, *reinterpret_cast<float(*)[32]>(o + 32));
+            float o[2][32];
+            tmem_ld32(tm + TM_QO, o[0]);
+            tmem_ld32(tm + TM_QO + 32, o[1]);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&o_read);
             if (to_ == 0) bulk_wait_read_all();   // the previous store has read the staging
             named_sync(1, 128);
             const int j = row;
-            if (sizeof(Tout) == 2) {
-                unsigned char *dst = sm + C_OUT + (j >> 6) * 8192;
 #pragma unroll
-                for (int r = 0; r < 64; ++r)
-                    *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(r, j & 63)) = __float2bfloat16_rn(o[r]);
-            } else {
-                unsigned char *dst = sm + C_OUT + (j >> 5) * 8192;
-                const int cj = j & 31;
+            for (int hh = 0; hh < 2; ++hh) {
+                if (sizeof(Tout) == 2) {
+                    unsigned char *dst = sm + C_OUT + (j >> 6) * 8192;
 #pragma unroll
-                for (int r = 0; r < 64; ++r)
-                    *reinterpret_cast<float *>(dst + r * 128 + ((((cj >> 2) ^ (r & 7)) & 7) << 4) + ((cj & 3) << 2)) =
-                        o[r];
+                    for (int r = 0; r < 32; ++r)
+                        *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * hh + r, j & 63)) =
+                            __float2bfloat16_rn(o[hh][r]);
+                } else {
+                    unsigned char *dst = sm + C_OUT + (j >> 5) * 8192;
+                    const int cj = j & 31;
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) {
+                        const int rr = 32 * hh + r;
+                        *reinterpret_cast<float *>(dst + rr * 128 + ((((cj >> 2) ^ (rr & 7)) & 7) << 4) +
+                                                   ((cj & 3) << 2)) = o[hh][r];
+                    }
+                }
             }
             fence_proxy_async();
             named_sync(1, 128);
@@ -665,37 +765,91 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 bulk_commit();
             }
         };
+        // Kt^T of channel blocks [ib0, ib0 + nib) (8 key channels each): ldmatrix.trans of the
+        // k tile gives each thread channel i and two consecutive tokens r, r + 1 of one 8 x 8
+        // block; Kt^T[i][r] = delta_r k_r[i], tf32, into row 64 + i of [P; Kt^T]
+        auto kt_blocks = [&](int it, int ib0, int nib) {
+            const uint32_t kbase = smem_u32(stage(it)) + C_OFF_K;
+            const float *sDel = vec(it, GV_DEL);
+            const int m = lane >> 3;
+#pragma unroll 1
+            for (int ib = ib0; ib < ib0 + nib; ++ib) {
+                const int kb = ib >> 3, c8 = ib & 7, i = 8 * ib + (lane >> 2);
+#pragma unroll
+                for (int rq = 0; rq < 2; ++rq) {
+                    const int rr = 8 * (4 * rq + m) + (lane & 7);   // the token row this lane addresses
+                    uint32_t v[4];
+                    ldsm_x4_trans(kbase + kb * C_KB + rr * 128 + ((c8 ^ (rr & 7)) << 4), v);
+#pragma unroll
+                    for (int mm = 0; mm < 4; ++mm) {
+                        const int r = 8 * (4 * rq + mm) + 2 * (lane & 3);
+                        const float2 d = *reinterpret_cast<const float2 *>(sDel + r);
+                        const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v[mm]));
+                        *reinterpret_cast<float2 *>(sm + C_BU + (r >> 5) * C_BU_KB + sw128_off32(64 + i, r & 31)) =
+                            make_float2(round_tf32(d.x * kv.x), round_tf32(d.y * kv.y));
+                    }
+                }
+            }
+        };
         bool ok = n_it > 0 && convert_w(0);
         for (int it = 0; ok && it < n_it; ++it) {
             const uint32_t par = it & 1;
+            // the previous chunk's output first: its TMEM read releases TM_QO to [W S | Q S](it)
             if (it >= 1) {
                 if (!wait_bar(&u_done, par ^ 1)) break;
                 if (outputs) emit(it - 1);
             }
-            // Kt^T (row i = key channel, 64 tokens: delta_r k_r[i]), tf32, into rows 64..191
             if (!wait_bar(&qkw_full[it & 1], (it >> 1) & 1) || !wait_bar(&g_ready[it & 1], (it >> 1) & 1)) break;
-            {
-                const int i = to_;
-                const unsigned char *src = stage(it) + (i >> 6) * C_KB + C_OFF_K;
-                const int ic = i & 63;
-                const float *sDel = vec(it, GV_DEL);
+            if (outputs && prows) {
+                // P(it) from the Q K^T rows of X (lanes 0..63), tf32, into rows 0..63
+                if (!wait_bar(&x_done, par)) break;
+                const int r = row;
+                const float *sG = vec(it, GV_G), *sF = vec(it, GV_F);
+                const bool fac = fac_s[it & 1] != 0;
+                const float er = vec(it, GV_E)[r], gr = sG[r];
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {   // columns s = 32 hh .. 32 hh + 31 (K-block hh)
+                    float x[32];
+                    tmem_ld32(tm + TM_X + 32 * hh, x);
+                    tmem_wait_ld();
+                    if (fac) {   // exp(g_r - g_s) = exp(g_r - g_31) exp(g_31 - g_s)
 #pragma unroll
-                for (int c4 = 0; c4 < 16; ++c4) {
-                    float kv[4];
+                        for (int c4 = 0; c4 < 8; ++c4) {
+                            const int s0 = 32 * hh + 4 * c4;
+                            const float4 f4 = *reinterpret_cast<const float4 *>(sF + s0);
+                            const float fs[4] = {f4.x, f4.y, f4.z, f4.w};
+                            float pv[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = 4 * c4 + e;
-                        kv[e] = round_tf32(sDel[r] * __bfloat162float(
-                                                         *reinterpret_cast<const __nv_bfloat16 *>(src + sw128_off(r, ic))));
+                            for (int e = 0; e < 4; ++e) pv[e] = s0 + e <= r ? round_tf32(er * fs[e] * x[4 * c4 + e]) : 0.f;
+                            *reinterpret_cast<float4 *>(sm + C_BU + hh * C_BU_KB + sw128_off32(r, 4 * c4)) =
+                                make_float4(pv[0], pv[1], pv[2], pv[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4) {
+                            const int s0 = 32 * hh + 4 * c4;
+                            float pv[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                pv[e] = s0 + e <= r ? round_tf32(__expf(fminf(gr - sG[s0 + e], 0.f)) * x[4 * c4 + e]) : 0.f;
+                            *reinterpret_cast<float4 *>(sm + C_BU + hh * C_BU_KB + sw128_off32(r, 4 * c4)) =
+                                make_float4(pv[0], pv[1], pv[2], pv[3]);
+                        }
                     }
-                    *reinterpret_cast<float4 *>(sm + C_BU + (c4 >> 3) * C_BU_KB + sw128_off32(64 + i, 4 * (c4 & 7))) =
-                        make_float4(kv[0], kv[1], kv[2], kv[3]);
                 }
-                fence_proxy_async();
+                kt_blocks(it, 2 * (warp - 8) + 12, 2);   // warps 8, 9: channel blocks 12..15
+            } else if (outputs) {
+                kt_blocks(it, warp == kWarpO0 ? 0 : 6, 6);   // warps 7, 10: blocks 0..5, 6..11
+            } else {
+                kt_blocks(it, 4 * (warp - kWarpO0), 4);     // no P: four blocks per warp
             }
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(&p_ready);
             mbar_arrive(&kt_ready);
             mbar_arrive(&stage_free[it & 1]);
             mbar_arrive(&gset_free[it & 1]);
+            // W(it + 1), issued after [W S | Q S](it)
             if (it + 1 < n_it && !convert_w(it + 1)) break;
         }
         if (outputs && n_it > 0 && !*abort_v && wait_bar(&u_done, (n_it - 1) & 1)) emit(n_it - 1);
@@ -706,7 +860,6 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmb, 512);
 }
-
 template <typename Tout, int GATE>
 int launch_chain(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
                  const ChainArgs &ca, unsigned grid, cudaStream_t stream) {
@@ -735,19 +888,22 @@ int launch_gdn_split(const ChunkProblem &p, void *workspace, int *status_word, c
     const unsigned bh = (unsigned)(p.B * p.H);
     const size_t seg_bytes = nseg > 1 ? (size_t)3 * bh * nseg * 16384 * sizeof(float) : 0;
     unsigned char *tops = reinterpret_cast<unsigned char *>(workspace) + seg_bytes;
-    {   // every chunk's T operands
-        auto kern = p.gate == 1 ? gdn_prep_kernel<1> : gdn_prep_kernel<0>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PR_TOTAL) != cudaSuccess)
-            return kErrCuda;
-        kern<<<bh * (unsigned)p.NC, kPrepThreads, PR_TOTAL, stream>>>(
-            (const __nv_bfloat16 *)p.k, (const __nv_bfloat16 *)p.beta, p.log_alpha, tops, (int)p.T, (int)p.H, p.NC);
-        if (cudaGetLastError() != cudaSuccess) return kErrCuda;
-    }
     CUtensorMap mq, mk, mv, mo;
     if (!tc_make_map(&mq, p.q, p.B, p.T, p.H, false) || !tc_make_map(&mk, p.k, p.B, p.T, p.H, false) ||
         !tc_make_map(&mv, p.v, p.B, p.T, p.H, false) ||
         !tc_make_map(&mo, p.out ? p.out : p.q, p.B, p.T, p.H, p.out ? !p.out_bf16 : false))
         return kErrCuda;
+    {   // every chunk's T operands: persistent CTAs, four per SM
+        auto kern = p.gate == 1 ? gdn_prep_kernel<1> : gdn_prep_kernel<0>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PR_TOTAL + 1024) !=
+            cudaSuccess)
+            return kErrCuda;
+        const unsigned nchunks = bh * (unsigned)p.NC;
+        const unsigned grid = std::min<unsigned>(nchunks, 4u * 152u);
+        kern<<<grid, kPrepThreads, PR_TOTAL + 1024, stream>>>(mk, (const __nv_bfloat16 *)p.beta, p.log_alpha, tops,
+                                                       (int)p.T, (int)p.H, p.NC, nchunks, status_word);
+        if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+    }
     ChainArgs ca{p.log_alpha, (const __nv_bfloat16 *)p.beta, p.init_state, p.final_state, tops, status_word,
                  (int)p.B, (int)p.T, (int)p.H, p.NC, 0, 1, p.NC, nullptr, nullptr, nullptr};
     auto launch = [&](const ChainArgs &c, unsigned grid) {

@@ -15,9 +15,12 @@ using namespace umma;
 
 constexpr long long kWaitCycles = 2000000000LL;   // ~1 s at the loaded SM clock
 
+// Waits (sleeping between polls, see mbar_try_wait_sleep) for the phase with the given
+// parity; false once about kWaitCycles have passed without it.
 __device__ __forceinline__ bool wait_cycles(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
+    while (!mbar_try_wait_sleep(bar, parity, 1000000u))
         if (clock64() - t0 > kWaitCycles) return false;
     return true;
 }
@@ -33,10 +36,13 @@ __device__ __forceinline__ void pack_hi_lo(float a, float b, uint32_t &hi, uint3
     lo = pack_bf16(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
 }
 
+// x rounded to the nearest TF32 value (ties away from zero, as cvt.rna.tf32.f32), as its bit
+// pattern with the low 13 mantissa bits clear: half a TF32 unit added to the magnitude bits,
+// then the low bits cleared -- two integer operations on the full-rate ALU (infinities and
+// NaNs stay what they are; values within half a unit of the largest float become infinite,
+// as the conversion's rounding makes them).
 __device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
+    return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
 }
 // d += a (16 x 8, row) * b (8 x 8, col), TF32 operands, fp32 accumulate (one warp).
 __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,

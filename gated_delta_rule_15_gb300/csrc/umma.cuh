@@ -14,6 +14,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// The first 1024-byte-aligned byte of a dynamic shared-memory array (1024 bytes of slack
+// allocated), by pointer arithmetic on the array itself: the compiler then still knows the
+// result to be a shared-memory address (an integer round trip would make every access
+// through it a generic one).
+__device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
+    return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
@@ -40,6 +48,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// As mbar_try_wait, but the thread may sleep (up to `suspend_ns`, woken when the phase
+// completes) instead of returning at once: waiting warps then take no issue slots from the
+// warps that work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns) : "memory");
     return ok != 0;
 }
 // Bounded wait for the phase with the given parity; false if `limit` polls passed.
@@ -95,6 +115,10 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, 
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+// Prefetch of `bytes` (a multiple of 16, 16-byte-aligned address) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 // Untiled bulk copy shared -> global (bulk group), same alignment rules.
 __device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
