@@ -352,6 +352,8 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     auto tops = [&](int it) { return a.tops + ((size_t)bh * a.NC + c_begin + it) * 16384; };
 
     float *sVec = reinterpret_cast<float *>(sm + C_SMALL);   // [2][6][64]
+    const uint32_t sm_s = smem_u32(sm);                      // the same bytes by shared address
+    auto vec_s = [&](int it, int k) { return sm_s + C_SMALL + 4u * ((it & 1) * 384 + 64 * k); };
     auto vec = [&](int it, int k) { return sVec + (it & 1) * 384 + 64 * k; };
     uint32_t *sGate = reinterpret_cast<uint32_t *>(sm + C_SMALL + 3072);   // [2][beta word | log alpha][64]
 
@@ -637,7 +639,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             // S^T -> bf16 pairs (the A operand of [W S | Q S]) and S^T <- gamma S^T, two
             // 32-column parts per TMEM round trip
             {
-                const float gamma = vec(it, GV_GAM)[63];
+                const float gamma = lds32f(vec_s(it, GV_GAM) + 4 * 63);
 #pragma unroll 1
                 for (int pp = 0; pp < 2; ++pp) {
                     float v[2][32];
@@ -663,7 +665,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             // read as tf32) and G (Q S)^T in place of (Q S)^T
             if (!wait_bar(&d_done, par)) break;
             {
-                const float *sGam = vec(it, GV_GAM);
+                const uint32_t sGam = vec_s(it, GV_GAM);
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
                     float ws[32], uu[32], qs[32];
@@ -676,7 +678,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     tmem_st32(tm + TM_WE + 32 * hh, ws);
                     if (outputs) {
 #pragma unroll
-                        for (int u = 0; u < 32; ++u) qs[u] *= sGam[32 * hh + u];
+                        for (int u4 = 0; u4 < 8; ++u4) {
+                            const float4 g4 = lds128f(sGam + 4 * (32 * hh + 4 * u4));
+                            qs[4 * u4] *= g4.x; qs[4 * u4 + 1] *= g4.y; qs[4 * u4 + 2] *= g4.z; qs[4 * u4 + 3] *= g4.w;
+                        }
                         tmem_st32(tm + TM_QO + 32 * hh, qs);
                     }
                 }
@@ -705,7 +710,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         auto convert_w = [&](int it) -> bool {
             if (!wait_bar(&w_done, it & 1)) return false;
             // row i of W^T (64 tokens, 128 bytes): the MN-major B operand of (W S)^T
-            unsigned char *dst = stage(it) + C_OFF_W + row * 128;
+            const uint32_t dst = smem_u32(stage(it)) + C_OFF_W + row * 128;
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
                 float w[32];
@@ -714,9 +719,8 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const float *f = w + 8 * c;
-                    *reinterpret_cast<uint4 *>(dst + (((4 * hh + c) ^ (row & 7)) << 4)) =
-                        make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
-                                   pack_bf16(f[6], f[7]));
+                    sts128(dst + (((4 * hh + c) ^ (row & 7)) << 4), pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
+                           pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
                 }
             }
             fence_proxy_async();
@@ -738,19 +742,17 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 if (sizeof(Tout) == 2) {
-                    unsigned char *dst = sm + C_OUT + (j >> 6) * 8192;
+                    const uint32_t dst = sm_s + C_OUT + (j >> 6) * 8192;
 #pragma unroll
                     for (int r = 0; r < 32; ++r)
-                        *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * hh + r, j & 63)) =
-                            __float2bfloat16_rn(o[hh][r]);
+                        sts16(dst + sw128_off(32 * hh + r, j & 63), __bfloat16_as_ushort(__float2bfloat16_rn(o[hh][r])));
                 } else {
-                    unsigned char *dst = sm + C_OUT + (j >> 5) * 8192;
+                    const uint32_t dst = sm_s + C_OUT + (j >> 5) * 8192;
                     const int cj = j & 31;
 #pragma unroll
                     for (int r = 0; r < 32; ++r) {
                         const int rr = 32 * hh + r;
-                        *reinterpret_cast<float *>(dst + rr * 128 + ((((cj >> 2) ^ (rr & 7)) & 7) << 4) +
-                                                   ((cj & 3) << 2)) = o[hh][r];
+                        sts32f(dst + rr * 128 + ((((cj >> 2) ^ (rr & 7)) & 7) << 4) + ((cj & 3) << 2), o[hh][r]);
                     }
                 }
             }
@@ -770,24 +772,27 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         // block; Kt^T[i][r] = delta_r k_r[i], tf32, into row 64 + i of [P; Kt^T]
         auto kt_blocks = [&](int it, int ib0, int nib) {
             const uint32_t kbase = smem_u32(stage(it)) + C_OFF_K;
-            const float *sDel = vec(it, GV_DEL);
+            const uint32_t sDel = vec_s(it, GV_DEL);
             const int m = lane >> 3;
+            // this lane's eight token pairs r = 8 q + 2 (lane % 4), q = 0..7: their decays once
+            float2 d[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) d[q] = lds64f(sDel + 4 * (8 * q + 2 * (lane & 3)));
 #pragma unroll 1
             for (int ib = ib0; ib < ib0 + nib; ++ib) {
                 const int kb = ib >> 3, c8 = ib & 7, i = 8 * ib + (lane >> 2);
+                uint32_t v[2][4];   // all loads first, then the products and stores
 #pragma unroll
                 for (int rq = 0; rq < 2; ++rq) {
                     const int rr = 8 * (4 * rq + m) + (lane & 7);   // the token row this lane addresses
-                    uint32_t v[4];
-                    ldsm_x4_trans(kbase + kb * C_KB + rr * 128 + ((c8 ^ (rr & 7)) << 4), v);
+                    ldsm_x4_trans(kbase + kb * C_KB + rr * 128 + ((c8 ^ (rr & 7)) << 4), v[rq]);
+                }
 #pragma unroll
-                    for (int mm = 0; mm < 4; ++mm) {
-                        const int r = 8 * (4 * rq + mm) + 2 * (lane & 3);
-                        const float2 d = *reinterpret_cast<const float2 *>(sDel + r);
-                        const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v[mm]));
-                        *reinterpret_cast<float2 *>(sm + C_BU + (r >> 5) * C_BU_KB + sw128_off32(64 + i, r & 31)) =
-                            make_float2(round_tf32(d.x * kv.x), round_tf32(d.y * kv.y));
-                    }
+                for (int q = 0; q < 8; ++q) {
+                    const int r = 8 * q + 2 * (lane & 3);
+                    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v[q >> 2][q & 3]));
+                    sts64f(sm_s + C_BU + (r >> 5) * C_BU_KB + sw128_off32(64 + i, r & 31), round_tf32(d[q].x * kv.x),
+                           round_tf32(d[q].y * kv.y));
                 }
             }
         };
@@ -804,25 +809,26 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 // P(it) from the Q K^T rows of X (lanes 0..63), tf32, into rows 0..63
                 if (!wait_bar(&x_done, par)) break;
                 const int r = row;
-                const float *sG = vec(it, GV_G), *sF = vec(it, GV_F);
+                const uint32_t sG = vec_s(it, GV_G), sF = vec_s(it, GV_F);
                 const bool fac = fac_s[it & 1] != 0;
-                const float er = vec(it, GV_E)[r], gr = sG[r];
+                const float er = lds32f(vec_s(it, GV_E) + 4 * r), gr = lds32f(sG + 4 * r);
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {   // columns s = 32 hh .. 32 hh + 31 (K-block hh)
                     float x[32];
                     tmem_ld32(tm + TM_X + 32 * hh, x);
                     tmem_wait_ld();
                     if (fac) {   // exp(g_r - g_s) = exp(g_r - g_31) exp(g_31 - g_s)
+                        float4 f4[8];   // all factor loads first
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4) f4[c4] = lds128f(sF + 4 * (32 * hh + 4 * c4));
 #pragma unroll
                         for (int c4 = 0; c4 < 8; ++c4) {
                             const int s0 = 32 * hh + 4 * c4;
-                            const float4 f4 = *reinterpret_cast<const float4 *>(sF + s0);
-                            const float fs[4] = {f4.x, f4.y, f4.z, f4.w};
+                            const float fs[4] = {f4[c4].x, f4[c4].y, f4[c4].z, f4[c4].w};
                             float pv[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) pv[e] = s0 + e <= r ? round_tf32(er * fs[e] * x[4 * c4 + e]) : 0.f;
-                            *reinterpret_cast<float4 *>(sm + C_BU + hh * C_BU_KB + sw128_off32(r, 4 * c4)) =
-                                make_float4(pv[0], pv[1], pv[2], pv[3]);
+                            sts128f(sm_s + C_BU + hh * C_BU_KB + sw128_off32(r, 4 * c4), pv[0], pv[1], pv[2], pv[3]);
                         }
                     } else {
 #pragma unroll
@@ -831,9 +837,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                             float pv[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                pv[e] = s0 + e <= r ? round_tf32(__expf(fminf(gr - sG[s0 + e], 0.f)) * x[4 * c4 + e]) : 0.f;
-                            *reinterpret_cast<float4 *>(sm + C_BU + hh * C_BU_KB + sw128_off32(r, 4 * c4)) =
-                                make_float4(pv[0], pv[1], pv[2], pv[3]);
+                                pv[e] = s0 + e <= r ? round_tf32(__expf(fminf(gr - lds32f(sG + 4 * (s0 + e)), 0.f)) *
+                                                                 x[4 * c4 + e])
+                                                    : 0.f;
+                            sts128f(sm_s + C_BU + hh * C_BU_KB + sw128_off32(r, 4 * c4), pv[0], pv[1], pv[2], pv[3]);
                         }
                     }
                 }
