@@ -84,8 +84,8 @@ def path_kernels(w):
     if tc_path(w):
         nc, bh = -(-w.T // w.chunk), w.B * w.H
         if bh <= 76 and nc >= 32 and min(nc // 16, 152 // bh) >= 2:
-            return ["chunk_tc_kernel (segment end states)", "seg_combine_kernel",
-                    "chunk_tc_kernel (segment outputs)"]
+            return ["gdn_prep_kernel", "gdn_chain_kernel (segment end states)", "seg_combine_kernel",
+                    "gdn_chain_kernel (segment outputs)"]
         return ["chunk_tc_kernel"]
     if kda_path(w):
         return ["kda_prep_kernel", "kda_state_kernel"]

@@ -839,40 +839,45 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
 // Segment chaining (between the two segment passes): per chain, S_start(0) = S_0 and
 // S_start(p + 1) = Phi_p S_start(p) + S0_p, where Phi_p and S0_p are segment p's transition
-// and zero-start end state.  One CTA per (chain, block of 32 state columns), fp32; each
-// Phi_p is staged in shared memory (64 KB, coalesced) before its product.
+// and zero-start end state.  One CTA per (chain, block of 16 state columns), fp32: each
+// Phi_p is staged in shared memory (64 KB, coalesced; the next one is prefetched into L2
+// meanwhile) before its product, each thread taking 8 rows of one column.
 constexpr int kCombineSmem = 128 * 128 * 4;
+constexpr int kCombineCols = 16;
 __global__ void __launch_bounds__(256) seg_combine_kernel(const float *__restrict__ init_state,
                                                            const float *__restrict__ phi,
                                                            const float *__restrict__ s0,
                                                            float *__restrict__ start, int nseg) {
-    __shared__ float S[128][33];
+    __shared__ float S[128][kCombineCols + 1];
     extern __shared__ float4 phi_s4[];
     const float *phi_s = reinterpret_cast<const float *>(phi_s4);   // [128][128]
-    const int cb = blockIdx.x & 3, bh = blockIdx.x >> 2;
-    const int tid = threadIdx.x, j = tid & 31, rg = tid >> 5;
-    const int col = 32 * cb + j;
-    for (int i = rg; i < 128; i += 8)
+    constexpr int kBlocks = 128 / kCombineCols;
+    const int cb = blockIdx.x % kBlocks, bh = blockIdx.x / kBlocks;
+    const int tid = threadIdx.x, j = tid % kCombineCols, rg = tid / kCombineCols;   // rg 0..15
+    const int col = kCombineCols * cb + j;
+    for (int i = rg; i < 128; i += 16)
         S[i][j] = init_state ? init_state[((size_t)bh * 128 + i) * 128 + col] : 0.f;
     for (int p = 0; p < nseg; ++p) {
         const size_t slot = ((size_t)bh * nseg + p) * 16384;
         __syncthreads();   // S is complete; the previous Phi's readers are done
-        for (int i = rg; i < 128; i += 8) start[slot + i * 128 + col] = S[i][j];
+        for (int i = rg; i < 128; i += 16) start[slot + i * 128 + col] = S[i][j];
         if (p + 1 == nseg) break;
+        if (tid == 0 && p + 2 < nseg) umma::bulk_prefetch_l2(phi + slot + 16384, 65536);
         for (int idx = tid; idx < 4096; idx += 256)
             phi_s4[idx] = reinterpret_cast<const float4 *>(phi + slot)[idx];
-        float acc[16];
+        float acc[8];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc[m] = s0[slot + (size_t)(rg + 8 * m) * 128 + col];
+        for (int m = 0; m < 8; ++m) acc[m] = s0[slot + (size_t)(rg + 16 * m) * 128 + col];
         __syncthreads();
+#pragma unroll 4
         for (int k = 0; k < 128; ++k) {
             const float sk = S[k][j];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) acc[m] = fmaf(phi_s[(rg + 8 * m) * 128 + k], sk, acc[m]);
+            for (int m = 0; m < 8; ++m) acc[m] = fmaf(phi_s[(rg + 16 * m) * 128 + k], sk, acc[m]);
         }
         __syncthreads();
 #pragma unroll
-        for (int m = 0; m < 16; ++m) S[rg + 8 * m][j] = acc[m];
+        for (int m = 0; m < 8; ++m) S[rg + 16 * m][j] = acc[m];
     }
 }
 
@@ -939,7 +944,7 @@ int tc_launch_seg_combine(const float *init_state, const float *phi, const float
     if (cudaFuncSetAttribute(seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCombineSmem) !=
         cudaSuccess)
         return kErrCuda;
-    seg_combine_kernel<<<chains * 4, 256, kCombineSmem, stream>>>(init_state, phi, s0, start, nseg);
+    seg_combine_kernel<<<chains * (128 / kCombineCols), 256, kCombineSmem, stream>>>(init_state, phi, s0, start, nseg);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
@@ -967,11 +972,20 @@ void tc_segment_split(const ChunkProblem &p, int *nseg, int *seg_len) {
 size_t gdn_split_workspace_bytes(const ChunkProblem &p);
 int launch_gdn_split(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream);
 
-// The two-kernel path (gdn_chain.cu) takes the plain forward when the workspace holds every
-// chunk's T operands; the single kernel below (the solve inside the chain) needs only the
-// segments' states, and serves the fused neighbours and the backward's checkpoints.
+// Few long chains split into segments (plain forward) take the two-kernel path of
+// gdn_chain.cu when the workspace holds every chunk's T operands: its chunk-parallel solve
+// keeps all SMs busy and its chain kernel is lighter per chunk (measured on B1 H16 T65536:
+// 1.54 ms against 1.77 ms).  Many chains keep the single kernel below, which solves inside
+// the chain (B8 H16 T4096: 0.364 ms against 0.387 ms) and needs only the segments' states;
+// it also serves the fused neighbours and the backward's checkpoints.
+static bool split_path(const ChunkProblem &p) {
+    int nseg, len;
+    tc_segment_split(p, &nseg, &len);
+    return nseg > 1;
+}
+
 size_t chunk_tc_workspace_bytes(const ChunkProblem &p, bool least) {
-    if (!least) return gdn_split_workspace_bytes(p);
+    if (!least && split_path(p)) return gdn_split_workspace_bytes(p);
     int nseg, len;
     tc_segment_split(p, &nseg, &len);
     return nseg > 1 ? (size_t)3 * p.B * p.H * nseg * 16384 * sizeof(float) : 0;
@@ -979,7 +993,7 @@ size_t chunk_tc_workspace_bytes(const ChunkProblem &p, bool least) {
 
 int launch_chunk_tc(const ChunkProblem &p, void *workspace, size_t workspace_bytes, int *status_word,
                     cudaStream_t stream, float *ckpt) {
-    if (!ckpt && !p.fuse && workspace && workspace_bytes >= gdn_split_workspace_bytes(p))
+    if (!ckpt && !p.fuse && split_path(p) && workspace && workspace_bytes >= gdn_split_workspace_bytes(p))
         return launch_gdn_split(p, workspace, status_word, stream);
     CUtensorMap mq, mk, mv, mo, mz;
     const bool zgate = (p.fuse & kFuseGate) != 0;

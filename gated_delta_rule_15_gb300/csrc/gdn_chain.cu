@@ -361,8 +361,9 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         uint64_t *ones[] = {&qkw_full[0], &qkw_full[1], &wt_full[0], &wt_full[1], &wt_free[0], &wt_free[1],
                             &vu_full,     &x_done,      &w_done,     &uu_done,    &d_done,     &u_done};
         for (uint64_t *bb : ones) mbar_init(bb, 1);
-        uint64_t *groups[] = {&sb_ready, &p_ready, &e_ready, &w_ready, &kt_ready, &o_read};
+        uint64_t *groups[] = {&sb_ready, &e_ready, &w_ready, &kt_ready, &o_read};
         for (uint64_t *bb : groups) mbar_init(bb, 128);
+        mbar_init(&p_ready, 256);   // warps 3..10 (P is built by warps 4, 5, 8, 9)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&stage_free[s], 129);
             mbar_init(&g_ready[s], 32);
@@ -398,6 +399,43 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
         tc_fence_after();
         return true;
+    };
+
+    // P(it), columns 32 hh .. 32 hh + 31 (K-block hh of [P; Kt^T]), from the Q K^T rows of X
+    // (TMEM lanes 0..63: this thread's row r), tf32: P_rs = exp(g_r - g_s) (q_r . k_s), s <= r
+    auto build_p_half = [&](int it, int hh) {
+        const int r = row;
+        const uint32_t sG = vec_s(it, GV_G), sF = vec_s(it, GV_F);
+        const bool fac = fac_s[it & 1] != 0;
+        const float er = lds32f(vec_s(it, GV_E) + 4 * r), gr = lds32f(sG + 4 * r);
+        float x[32];
+        tmem_ld32(tm + TM_X + 32 * hh, x);
+        tmem_wait_ld();
+        if (fac) {   // exp(g_r - g_s) = exp(g_r - g_31) exp(g_31 - g_s)
+            float4 f4[8];   // all factor loads first
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) f4[c4] = lds128f(sF + 4 * (32 * hh + 4 * c4));
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                const int s0 = 32 * hh + 4 * c4;
+                const float fs[4] = {f4[c4].x, f4[c4].y, f4[c4].z, f4[c4].w};
+                float pv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) pv[e] = s0 + e <= r ? round_tf32(er * fs[e] * x[4 * c4 + e]) : 0.f;
+                sts128f(sm_s + C_BU + hh * C_BU_KB + sw128_off32(r, 4 * c4), pv[0], pv[1], pv[2], pv[3]);
+            }
+        } else {
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                const int s0 = 32 * hh + 4 * c4;
+                float pv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    pv[e] = s0 + e <= r ? round_tf32(__expf(fminf(gr - lds32f(sG + 4 * (s0 + e)), 0.f)) * x[4 * c4 + e])
+                                        : 0.f;
+                sts128f(sm_s + C_BU + hh * C_BU_KB + sw128_off32(r, 4 * c4), pv[0], pv[1], pv[2], pv[3]);
+            }
+        }
     };
 
     if (warp == kWarpTma) {
@@ -661,6 +699,16 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             }
             tc_fence_before();
             mbar_arrive(&sb_ready);
+            // P(it), columns 32..63 (warps 4, 5: TMEM lanes 0..63), while [W S | Q S](it) runs
+            if (outputs) {
+                if ((warp & 3) < 2) {
+                    if (!wait_bar(&x_done, par)) break;
+                    build_p_half(it, 1);
+                    fence_proxy_async();
+                }
+                tc_fence_before();
+                mbar_arrive(&p_ready);
+            }
             // E^T = U^T - (W S)^T in place of (W S)^T (fp32: the next product's A operand,
             // read as tf32) and G (Q S)^T in place of (Q S)^T
             if (!wait_bar(&d_done, par)) break;
@@ -806,47 +854,12 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             }
             if (!wait_bar(&qkw_full[it & 1], (it >> 1) & 1) || !wait_bar(&g_ready[it & 1], (it >> 1) & 1)) break;
             if (outputs && prows) {
-                // P(it) from the Q K^T rows of X (lanes 0..63), tf32, into rows 0..63
+                // P(it), columns 0..31 (the state warps take 32..63)
                 if (!wait_bar(&x_done, par)) break;
-                const int r = row;
-                const uint32_t sG = vec_s(it, GV_G), sF = vec_s(it, GV_F);
-                const bool fac = fac_s[it & 1] != 0;
-                const float er = lds32f(vec_s(it, GV_E) + 4 * r), gr = lds32f(sG + 4 * r);
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {   // columns s = 32 hh .. 32 hh + 31 (K-block hh)
-                    float x[32];
-                    tmem_ld32(tm + TM_X + 32 * hh, x);
-                    tmem_wait_ld();
-                    if (fac) {   // exp(g_r - g_s) = exp(g_r - g_31) exp(g_31 - g_s)
-                        float4 f4[8];   // all factor loads first
-#pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4) f4[c4] = lds128f(sF + 4 * (32 * hh + 4 * c4));
-#pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4) {
-                            const int s0 = 32 * hh + 4 * c4;
-                            const float fs[4] = {f4[c4].x, f4[c4].y, f4[c4].z, f4[c4].w};
-                            float pv[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) pv[e] = s0 + e <= r ? round_tf32(er * fs[e] * x[4 * c4 + e]) : 0.f;
-                            sts128f(sm_s + C_BU + hh * C_BU_KB + sw128_off32(r, 4 * c4), pv[0], pv[1], pv[2], pv[3]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4) {
-                            const int s0 = 32 * hh + 4 * c4;
-                            float pv[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                pv[e] = s0 + e <= r ? round_tf32(__expf(fminf(gr - lds32f(sG + 4 * (s0 + e)), 0.f)) *
-                                                                 x[4 * c4 + e])
-                                                    : 0.f;
-                            sts128f(sm_s + C_BU + hh * C_BU_KB + sw128_off32(r, 4 * c4), pv[0], pv[1], pv[2], pv[3]);
-                        }
-                    }
-                }
-                kt_blocks(it, 2 * (warp - 8) + 12, 2);   // warps 8, 9: channel blocks 12..15
+                build_p_half(it, 0);
+                kt_blocks(it, 3 * (warp - 8) + 10, 3);   // warps 8, 9: channel blocks 10..15
             } else if (outputs) {
-                kt_blocks(it, warp == kWarpO0 ? 0 : 6, 6);   // warps 7, 10: blocks 0..5, 6..11
+                kt_blocks(it, warp == kWarpO0 ? 0 : 5, 5);   // warps 7, 10: blocks 0..4, 5..9
             } else {
                 kt_blocks(it, 4 * (warp - kWarpO0), 4);     // no P: four blocks per warp
             }

@@ -15,12 +15,12 @@ using namespace umma;
 
 constexpr long long kWaitCycles = 2000000000LL;   // ~1 s at the loaded SM clock
 
-// Waits (sleeping between polls, see mbar_try_wait_sleep) for the phase with the given
-// parity; false once about kWaitCycles have passed without it.
+// Waits for the phase with the given parity; false once about kWaitCycles have passed
+// without it.  (try_wait with a suspend-time hint was measured slower here: the waiting
+// thread's wake-up lengthens every hand-off between warps.)
 __device__ __forceinline__ bool wait_cycles(uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait_sleep(bar, parity, 1000000u))
+    while (!mbar_try_wait(bar, parity))
         if (clock64() - t0 > kWaitCycles) return false;
     return true;
 }

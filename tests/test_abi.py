@@ -56,11 +56,12 @@ def test_workspace_query(dr):
     n = dr.workspace_bytes(_desc(dr))
     assert n > 0 and n % 16 == 0
     assert dr.workspace_bytes(_desc(dr, T=0)) == 0
-    # the tensor-core path (bf16, d = 128, C = 64, scalar gate): 16 KB of T operands per
-    # (b, h, chunk) on its fastest path (here B2 H3 and two chunks), none on the single-kernel
-    # path it also runs
-    assert dr.workspace_bytes(_desc(dr, gate=dr.DR_GATE_SCALAR)) == 2 * 3 * 2 * 16384
+    # the tensor-core path (bf16, d = 128, C = 64, scalar gate) with many short chains: none
+    assert dr.workspace_bytes(_desc(dr, gate=dr.DR_GATE_SCALAR)) == 0
     assert dr.min_workspace_bytes(_desc(dr, gate=dr.DR_GATE_SCALAR)) == 0
+    # few long chains (segments): the fastest path also holds 16 KB of T operands per chunk
+    long = _desc(dr, B=1, T=64 * 64, H=2, gate=dr.DR_GATE_SCALAR)
+    assert dr.workspace_bytes(long) == dr.min_workspace_bytes(long) + 2 * 64 * 16384
     assert dr.workspace_bytes(_desc(dr, gate=dr.DR_GATE_SCALAR, in_dtype=dr.DR_F32)) > 0
     for d in (_desc(dr), _desc(dr, in_dtype=dr.DR_F32), _desc(dr, T=0)):   # other paths: equal
         assert dr.min_workspace_bytes(d) == dr.workspace_bytes(d)
