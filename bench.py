@@ -88,6 +88,10 @@ def path_kernels(w):
                     "gdn_chain_kernel (segment outputs)"]
         return ["chunk_tc_kernel"]
     if kda_path(w):
+        nc, bh = -(-w.T // w.chunk), w.B * w.H
+        if bh <= 76 and nc >= 32 and min(nc // 16, 152 // bh) >= 2:
+            return ["kda_prep_kernel", "kda_state_kernel (segment end states)", "seg_combine_kernel",
+                    "kda_state_kernel (segment outputs)"]
         return ["kda_prep_kernel", "kda_state_kernel"]
     return ["chunk_prep_kernel", "chunk_state_kernel"]
 
@@ -392,7 +396,8 @@ def run_native(args):
             "what": "dr_chunk_bwd (fp32 sums, TF32 tensor-core tiles): every input gradient",
             "ms_per_call": round(bms, 3), "tokens_per_s": w.B * w.T / (bms * 1e-3),
             "vs_forward": round(bms / ms, 1)}
-        for name in ("kda_bf16_B4_H32_T8192_d128", "gdn_bf16_B1_H16_T65536_d128_init"):
+        for name in ("kda_bf16_B4_H32_T8192_d128", "gdn_bf16_B1_H16_T65536_d128_init",
+                     "kda_bf16_B1_H16_T65536_d128_init"):
             wx = inputs.WORKLOADS[name]
             rx = bench_chunk(wx, max(2, args.steps // 3), 3, world)
             bx, fx = chunk_bytes(wx), chunk_flops(wx)

@@ -654,6 +654,14 @@ struct StateArgs {
     int *status;
     int T, H, NC;
     bool zgate;   // multiply the outputs by silu(z)
+    // Sequence segments (few long chains, chain_segments of chunk_layout.h): role 0 runs whole
+    // sequences; role 1 runs each segment twice without outputs, CTA 2i from S_0 = 0 (end
+    // state to ws_s0) and CTA 2i + 1 from S_0 = I with no value term (U = 0: the segment's
+    // transition, to ws_phi); role 2 runs each segment from its start state (ws_start),
+    // writing outputs.  [B*H][nseg][128][128] fp32, element [i][j] as in the state.
+    int role, nseg, seg_len;
+    float *ws_phi, *ws_s0;
+    const float *ws_start;
 };
 
 // Per chunk c, in order (thread 0 issues the MMAs, thread 224 the TMA loads):
@@ -683,7 +691,31 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
     const int row = 32 * quarter + lane;
-    const int bh = blockIdx.x, h = bh % a.H, b = bh / a.H;
+    // this CTA's chain and chunk range [c_begin, c_begin + nc), its start state (NULL: zero;
+    // `identity`: I) and where its end state goes
+    int bh = blockIdx.x, c_begin = 0, nc = a.NC;
+    const float *s_init = a.init_state ? a.init_state + (size_t)bh * 16384 : nullptr;
+    float *s_fin = a.final_state ? a.final_state + (size_t)bh * 16384 : nullptr;
+    bool identity = false, use_u = true, outputs = true;
+    if (a.role != 0) {
+        const int idx = a.role == 1 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+        const int seg = idx % a.nseg;
+        bh = idx / a.nseg;
+        c_begin = seg * a.seg_len;
+        nc = min(a.NC, c_begin + a.seg_len) - c_begin;
+        const size_t slot = ((size_t)bh * a.nseg + seg) * 16384;
+        if (a.role == 1) {
+            outputs = false;
+            s_init = nullptr;
+            identity = (blockIdx.x & 1) != 0;
+            use_u = !identity;
+            s_fin = (identity ? a.ws_phi : a.ws_s0) + slot;
+        } else {
+            s_init = a.ws_start + slot;
+            s_fin = (seg == a.nseg - 1 && a.final_state) ? a.final_state + (size_t)bh * 16384 : nullptr;
+        }
+    }
+    const int h = bh % a.H, b = bh / a.H;
     constexpr int kTmaThread = 224;
     constexpr int kOutBoxes = sizeof(Tout) == 2 ? 2 : 4;
     float *sGam = reinterpret_cast<float *>(sm + S2_SMALL);   // [2][128]
@@ -721,21 +753,24 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
             const int i0 = 64 * half + 32 * part;
 #pragma unroll
             for (int u = 0; u < 32; ++u)
-                v[u] = a.init_state ? a.init_state[((size_t)bh * 128 + i0 + u) * 128 + row] : 0.f;
+                v[u] = s_init ? s_init[(size_t)(i0 + u) * 128 + row] : (identity && i0 + u == row ? 1.f : 0.f);
             tmem_st32(tm + S2_TM_S + i0, v);
         }
         tmem_wait_st();
     }
 
-    const int64_t n0 = (int64_t)bh * a.NC;   // first chunk of this chain in the workspace
-    auto rowc = [&](int c) { return (int)((n0 + c) * 64); };
+    // first chunk of this CTA's range in the workspace; loads and buffers are indexed by the
+    // step `it` within the range (chunk c_begin + it)
+    const int64_t n0 = (int64_t)bh * a.NC + c_begin;
+    auto rowc = [&](int it) { return (int)((n0 + it) * 64); };
     // (TMA thread) loads issued per barrier: w, q, u, k, p[0], p[1], z -- on an abort it
     // waits (bounded) for the last phase of each
     int issued[7] = {0, 0, 0, 0, 0, 0, 0};
-    auto load_z = [&](int c) {
+    auto load_z = [&](int it) {
         ++issued[6];
         mbar_arrive_expect_tx(&bar_z, 16384);
-        for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + S2_Z + kb * 8192, &tz, &bar_z, 64 * kb, h, c * 64, b);
+        for (int kb = 0; kb < 2; ++kb)
+            tma_load_4d(sm + S2_Z + kb * 8192, &tz, &bar_z, 64 * kb, h, (c_begin + it) * 64, b);
     };
     auto load_w = [&](int c) {
         ++issued[0];
@@ -771,21 +806,23 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         tma_load_2d(dst, &mph, bb, 0, rowc(c));
         tma_load_2d(dst + 8192, &mpl, bb, 0, rowc(c));
     };
-    if (tid == kTmaThread && a.NC > 0) {
+    if (tid == kTmaThread && nc > 0) {
         load_w(0);
-        load_q(0);
-        load_u(0);
+        if (outputs) load_q(0);
+        if (use_u) load_u(0);
         load_k(0);
-        load_p(0);
-        if (a.NC > 1) load_p(1);
-        if (a.zgate) load_z(0);
+        if (outputs) {
+            load_p(0);
+            if (nc > 1) load_p(1);
+            if (a.zgate) load_z(0);
+        }
     }
-    if (tid < 128 && a.NC > 0) cp_async4(sGam + tid, a.gam + n0 * 128 + tid, 4);
+    if (tid < 128 && nc > 0) cp_async4(sGam + tid, a.gam + n0 * 128 + tid, 4);
     cp_async_commit();
 
     bool store_outstanding = false;   // thread 0: a TMA store from ST may still be reading it
     // output of chunk c from its DQ / PE buffers, staged in ST (free: see the callers)
-    auto emit = [&](int c) {
+    auto emit = [&](int c) {   // c: the step within the range
         float o[32], pe[32];   // (QH S)^T + E^T P^T, and (QL S)^T
         tmem_ld32(tm + S2_TM_D + S2_TM_DSTRIDE * (c & 1) + 64 + 32 * half, o);
         tmem_ld32(tm + S2_TM_D + S2_TM_DSTRIDE * (c & 1) + 128 + 32 * half, pe);
@@ -820,18 +857,18 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
-        if (tid == kTmaThread && a.zgate && c + 1 < a.NC) load_z(c + 1);   // the z tile is read
+        if (tid == kTmaThread && a.zgate && c + 1 < nc) load_z(c + 1);   // the z tile is read
         if (tid == 0) {
             constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
 #pragma unroll
             for (int kb = 0; kb < kOutBoxes; ++kb)
-                tma_store_4d(&to, sm + S2_ST + kb * 8192, cols * kb, h, c * 64, b);
+                tma_store_4d(&to, sm + S2_ST + kb * 8192, cols * kb, h, (c_begin + c) * 64, b);
             bulk_commit();
             store_outstanding = true;
         }
     };
 
-    for (int c = 0; c < a.NC; ++c) {
+    for (int c = 0; c < nc; ++c) {   // step c: chunk c_begin + c
         const uint32_t par = c & 1;
         // ---- 1. S^T to bf16 (ST, free once the previous output's store has read it);
         //         S^T <- S^T Diag(G_C)
@@ -841,7 +878,7 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         }
         cp_async_wait_all();
         __syncthreads();   // G_C of this chunk visible; ST free
-        if (tid < 128 && c + 1 < a.NC)   // prefetch the next chunk's G_C
+        if (tid < 128 && c + 1 < nc)   // prefetch the next chunk's G_C
             cp_async4(sGam + ((c + 1) & 1) * 128 + tid, a.gam + (n0 + c + 1) * 128 + tid, 4);
         cp_async_commit();
         {
@@ -870,34 +907,38 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         __syncthreads();
         if (abort_s) break;
 
-        // ---- 2. D[c % 2] = S^T [W; QH; QL]^T in one N = 192 product
+        // ---- 2. D[c % 2] = S^T [W; QH; QL]^T in one N = 192 product (without outputs:
+        //         (W S)^T alone)
         if (tid == 0) {
             if (!wait_cycles(&bar_w, par)) fail();
-            if (!wait_cycles(&bar_q, par)) fail();
+            if (outputs && !wait_cycles(&bar_q, par)) fail();
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kk = (ks & 3) * 32;
                 mma_bf16(tmb + S2_TM_D + S2_TM_DSTRIDE * par, desc_add(dK0, S2_ST + (ks >> 2) * 16384 + kk),
-                         desc_add(dK0, S2_WQ + (ks >> 2) * S2_WQ_KB + kk), ID_KK_N192, ks > 0);
+                         desc_add(dK0, S2_WQ + (ks >> 2) * S2_WQ_KB + kk), outputs ? ID_KK_N192 : ID_KK_N64,
+                         ks > 0);
             }
             mma_commit(&bar_dw);
         }
         wait_bar(&bar_dw, par);
         // ---- 3. refills: W and Q for c + 1; P for c + 1 into the buffer chunk c - 1 read
-        if (tid == kTmaThread && c + 1 < a.NC) {
+        if (tid == kTmaThread && c + 1 < nc) {
             load_w(c + 1);
-            load_q(c + 1);
-            if (c >= 1) {
-                if (!wait_cycles(&bar_pe, (c - 1) & 1)) fail();
-                load_p(c + 1);
+            if (outputs) {
+                load_q(c + 1);
+                if (c >= 1) {
+                    if (!wait_cycles(&bar_pe, (c - 1) & 1)) fail();
+                    load_p(c + 1);
+                }
             }
         }
 
-        // ---- 4. E^T = U^T - (W S)^T as a bf16 pair (lane j = value channel, columns = tokens);
-        //         E^T P^T of chunk c - 1 must have read E first
-        if (c >= 1) wait_bar(&bar_pe, (c - 1) & 1);
-        if (!wait_cycles(&bar_u, par)) fail();
+        // ---- 4. E^T = U^T - (W S)^T as a bf16 pair (lane j = value channel, columns = tokens;
+        //         U = 0 for a segment's transition); E^T P^T of chunk c - 1 must have read E first
+        if (outputs && c >= 1) wait_bar(&bar_pe, (c - 1) & 1);
+        if (use_u && !wait_cycles(&bar_u, par)) fail();
         {
             float ws[32];
             tmem_ld32(tm + S2_TM_D + S2_TM_DSTRIDE * par + 32 * half, ws);
@@ -910,7 +951,7 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int r = 32 * half + 8 * q4 + u;
-                    e[u] = U[(j >> 5) * 2048 + r * 32 + (j & 31)] - ws[8 * q4 + u];
+                    e[u] = (use_u ? U[(j >> 5) * 2048 + r * 32 + (j & 31)] : 0.f) - ws[8 * q4 + u];
                 }
                 uint32_t eh[4], el[4];
 #pragma unroll
@@ -923,13 +964,13 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
-        if (tid == kTmaThread && c + 1 < a.NC) load_u(c + 1);   // U buffer is free
+        if (tid == kTmaThread && use_u && c + 1 < nc) load_u(c + 1);   // U buffer is free
 
         // ---- 5. S^T += E^T (K*G_C/G) [bar_s];  E^T P^T -> PE[c % 2] [bar_pe]
         //         (bf16 pairs: hi.hi + hi.lo + lo.hi)
         if (tid == 0) {
             if (!wait_cycles(&bar_k, par)) fail();
-            if (!wait_cycles(&bar_p[par], (c >> 1) & 1)) fail();
+            if (outputs && !wait_cycles(&bar_p[par], (c >> 1) & 1)) fail();
             tc_fence_after();
             const uint32_t pb = S2_P + par * 16384;
             const uint32_t ea[3] = {S2_EH, S2_EH, S2_EL}, kbuf[3] = {S2_KH, S2_KL, S2_KH},
@@ -941,40 +982,42 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
                     mma_bf16(tmb + S2_TM_S, desc_add(dK0, ea[part] + ks * 32),
                              desc_add(dM0, kbuf[part] + ks * 2048), ID_KM_N128, 1);
             mma_commit(&bar_s);
-            const uint32_t pe = tmb + S2_TM_D + S2_TM_DSTRIDE * par + 64;   // onto (QH S)^T
+            if (outputs) {
+                const uint32_t pe = tmb + S2_TM_D + S2_TM_DSTRIDE * par + 64;   // onto (QH S)^T
 #pragma unroll
-            for (int part = 0; part < 3; ++part)
+                for (int part = 0; part < 3; ++part)
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(pe, desc_add(dK0, ea[part] + ks * 32),
-                             desc_add(dK0, pbuf[part] + ks * 32), ID_KK_N64, 1);
-            mma_commit(&bar_pe);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(pe, desc_add(dK0, ea[part] + ks * 32),
+                                 desc_add(dK0, pbuf[part] + ks * 32), ID_KK_N64, 1);
+                mma_commit(&bar_pe);
+            }
         }
 
         // ---- 6. output of chunk c - 1 (ST is free: this chunk's D product has completed)
-        if (c >= 1) emit(c - 1);
+        if (outputs && c >= 1) emit(c - 1);
 
         // ---- 7. state update done; K buffer is free
         wait_bar(&bar_s, par);
-        if (tid == kTmaThread && c + 1 < a.NC) load_k(c + 1);
+        if (tid == kTmaThread && c + 1 < nc) load_k(c + 1);
     }
-    if (!abort_s && a.NC > 0) {   // output of the last chunk
-        wait_bar(&bar_pe, (a.NC - 1) & 1);
+    if (!abort_s && outputs && nc > 0) {   // output of the last chunk
+        wait_bar(&bar_pe, (nc - 1) & 1);
         if (tid == 0 && store_outstanding) {
             bulk_wait_read_all();
             store_outstanding = false;
         }
         __syncthreads();
-        emit(a.NC - 1);
+        emit(nc - 1);
     }
-    if (!abort_s && a.final_state) {
+    if (!abort_s && s_fin) {
         float v[32];
         for (int part = 0; part < 2; ++part) {
             const int i0 = 64 * half + 32 * part;
             tmem_ld32(tm + S2_TM_S + i0, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int u = 0; u < 32; ++u) a.final_state[((size_t)bh * 128 + i0 + u) * 128 + row] = v[u];
+            for (int u = 0; u < 32; ++u) s_fin[(size_t)(i0 + u) * 128 + row] = v[u];
         }
     }
     cp_async_wait_all();
@@ -1041,8 +1084,13 @@ bool chunk_kda_supported(const ChunkProblem &p) {
     return p.in_bf16 && p.dk == 128 && p.dv == 128 && p.C == 64 && p.T > 0 && p.gate == 2;
 }
 
+// The per-chunk operand slabs, then (few long chains split into segments) the segments'
+// transitions, zero-start end states and start states, [B*H][nseg][128][128] fp32 each.
 size_t chunk_kda_workspace_bytes(const ChunkProblem &p) {
-    return (size_t)(p.B * p.H * p.NC) * kKdaBytesPerChunk;
+    int nseg, len;
+    chain_segments(p.B * p.H, p.NC, &nseg, &len);
+    const size_t seg = nseg > 1 ? (size_t)3 * p.B * p.H * nseg * 16384 * sizeof(float) : 0;
+    return (size_t)(p.B * p.H * p.NC) * kKdaBytesPerChunk + seg;
 }
 
 int launch_chunk_kda(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream) {
@@ -1071,20 +1119,34 @@ int launch_chunk_kda(const ChunkProblem &p, void *workspace, int *status_word, c
     kda_prep_kernel<<<(unsigned)nch, kThreads, s1, stream>>>(tq, tk, tv, tla, mw, mu, pa);
     if (cudaGetLastError() != cudaSuccess) return kErrCuda;
 
-    StateArgs sa{p.init_state, p.final_state, ws.GAM, status_word, (int)p.T, (int)p.H, p.NC, zgate};
-    const unsigned grid = (unsigned)(p.B * p.H);
-    if (p.out_bf16) {
-        if (cudaFuncSetAttribute(kda_state_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 s2max) != cudaSuccess)
-            return kErrCuda;
-        kda_state_kernel<__nv_bfloat16><<<grid, kThreads, s2, stream>>>(mw, mqh, mql, mkh, mkl, mph, mpl, mu, to, tz, sa);
-    } else {
-        if (cudaFuncSetAttribute(kda_state_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, s2max) !=
-            cudaSuccess)
-            return kErrCuda;
-        kda_state_kernel<float><<<grid, kThreads, s2, stream>>>(mw, mqh, mql, mkh, mkl, mph, mpl, mu, to, tz, sa);
-    }
-    return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+    StateArgs sa{p.init_state, p.final_state, ws.GAM, status_word, (int)p.T, (int)p.H, p.NC, zgate,
+                 0, 1, p.NC, nullptr, nullptr, nullptr};
+    auto state = [&](const StateArgs &sa_, unsigned grid) {
+        auto kern = p.out_bf16 ? kda_state_kernel<__nv_bfloat16> : kda_state_kernel<float>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s2max) != cudaSuccess)
+            return (int)kErrCuda;
+        kern<<<grid, kThreads, s2, stream>>>(mw, mqh, mql, mkh, mkl, mph, mpl, mu, to, tz, sa_);
+        return cudaGetLastError() == cudaSuccess ? (int)kOk : (int)kErrCuda;
+    };
+    const unsigned bh = (unsigned)(p.B * p.H);
+    int nseg, seg_len;
+    chain_segments(bh, p.NC, &nseg, &seg_len);
+    if (nseg <= 1) return state(sa, bh);
+    // segments: end states (two runs per segment), chaining, then outputs
+    float *seg = reinterpret_cast<float *>(reinterpret_cast<char *>(workspace) + (size_t)nch * kKdaBytesPerChunk);
+    const size_t per = (size_t)bh * nseg * 16384;
+    sa.nseg = nseg;
+    sa.seg_len = seg_len;
+    sa.ws_phi = seg;
+    sa.ws_s0 = seg + per;
+    sa.ws_start = seg + 2 * per;
+    sa.role = 1;
+    int rc = state(sa, bh * nseg * 2);
+    if (rc != kOk) return rc;
+    rc = tc_launch_seg_combine(p.init_state, sa.ws_phi, sa.ws_s0, seg + 2 * per, bh, nseg, stream);
+    if (rc != kOk) return rc;
+    sa.role = 2;
+    return state(sa, bh * nseg);
 }
 
 }  // namespace dr

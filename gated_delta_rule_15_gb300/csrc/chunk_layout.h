@@ -94,6 +94,29 @@ size_t chunk_tc_workspace_bytes(const ChunkProblem &p, bool least = false);
 // the outputs (the backward's recompute).
 int launch_chunk_tc(const ChunkProblem &p, void *workspace, size_t workspace_bytes, int *status_word,
                     cudaStream_t stream, float *ckpt = nullptr);
+// Few long chains leave most of the GPU's 152 SMs idle while each chain walks its chunks one
+// after another; the tensor-core paths then split every chain into `nseg` segments of
+// `seg_len` chunks (at least 16 each) so that about 152 CTAs work at once.  A segment's end
+// state is affine in its start state, S_end = Phi S_start + S0 (S0: the end state from a zero
+// start; Phi: the run from the identity with no value term), so the segments run in three
+// passes: end states of every segment in parallel, the chaining of the affine maps along each
+// chain (tc_launch_seg_combine), then every segment again from its true start, writing outputs.
+// nseg = 1 when the problem is not split.
+inline void chain_segments(int64_t chains, int NC, int *nseg, int *seg_len) {
+    constexpr int kGpuSms = 152;
+    *nseg = 1;
+    *seg_len = NC;
+    if (chains > kGpuSms / 2 || NC < 32) return;
+    const int n = (int)(NC / 16 < kGpuSms / chains ? NC / 16 : kGpuSms / chains);
+    if (n < 2) return;
+    const int len = (NC + n - 1) / n;
+    *seg_len = len;
+    *nseg = (NC + len - 1) / len;
+}
+// Per chain, S_start(0) = S_0 (NULL: zero) and S_start(p + 1) = Phi_p S_start(p) + S0_p over
+// the [chains][nseg][128][128] fp32 arrays phi, s0 and start (chunk_tc.cu).
+int tc_launch_seg_combine(const float *init_state, const float *phi, const float *s0, float *start,
+                          unsigned chains, int nseg, cudaStream_t stream);
 // The least workspace dr_chunk_fwd accepts for *desc (dr_api.cu).
 int chunk_fwd_least_workspace(const dr_chunk_desc *desc, size_t *bytes);
 // Two-kernel tensor-core path for the per-channel gate (chunk_kda.cu): bf16 inputs,

@@ -953,20 +953,10 @@ bool chunk_tc_supported(const ChunkProblem &p) {
            (p.gate == 0 || p.gate == 1);
 }
 
-// Few long chains leave most of the GPU's 152 SMs idle while each chain walks its chunks
-// one after another; such problems are split into `nseg` segments per chain (at least 16
-// chunks each) so that about 152 CTAs work at once.
-static constexpr int kGpuSms = 152;
 void tc_segment_split(const ChunkProblem &p, int *nseg, int *seg_len) {
     *nseg = 1;
     *seg_len = p.NC;
-    const int64_t bh = p.B * p.H;
-    if (!chunk_tc_supported(p) || bh > kGpuSms / 2 || p.NC < 32) return;
-    int n = (int)std::min<int64_t>(p.NC / 16, kGpuSms / bh);
-    if (n < 2) return;
-    const int len = (p.NC + n - 1) / n;
-    *seg_len = len;
-    *nseg = (p.NC + len - 1) / len;
+    if (chunk_tc_supported(p)) chain_segments(p.B * p.H, p.NC, nseg, seg_len);
 }
 
 size_t gdn_split_workspace_bytes(const ChunkProblem &p);

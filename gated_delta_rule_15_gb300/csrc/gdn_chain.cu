@@ -50,12 +50,10 @@
 
 namespace dr {
 
-// chunk_tc.cu: the tensor map of a [B, T, H, 128] tensor (64-token boxes, 128-byte swizzle),
-// the segment split of few long chains, and the segment chaining kernel's launch.
+// chunk_tc.cu: the tensor map of a [B, T, H, 128] tensor (64-token boxes, 128-byte swizzle)
+// and the segment split of few long chains.
 bool tc_make_map(CUtensorMap *m, const void *base, int64_t B, int64_t T, int64_t H, bool fp32);
 void tc_segment_split(const ChunkProblem &p, int *nseg, int *seg_len);
-int tc_launch_seg_combine(const float *init_state, const float *phi, const float *s0, float *start,
-                          unsigned chains, int nseg, cudaStream_t stream);
 
 namespace {
 

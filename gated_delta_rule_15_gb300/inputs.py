@@ -64,7 +64,8 @@ class DecodeWorkload:
 
 # The workloads the method is measured on (single sequence fp32; Gated DeltaNet at
 # T = 4096; KDA per-channel gate at T = 8192; long-context Gated DeltaNet with a carried
-# state at T = 65536; batched decode against a 512 MiB state).
+# state at T = 65536; batched decode against a 512 MiB state), and the long-context shape
+# with the per-channel gate, which exercises that gate's segment-parallel form.
 WORKLOADS = {
     "gdn_f32_B1_H1_T256_d64": ChunkWorkload(
         "gdn_f32_B1_H1_T256_d64", B=1, T=256, H=1, dk=64, dv=64, gate="scalar",
@@ -78,6 +79,9 @@ WORKLOADS = {
     "gdn_bf16_B1_H16_T65536_d128_init": ChunkWorkload(
         "gdn_bf16_B1_H16_T65536_d128_init", B=1, T=65536, H=16, dk=128, dv=128,
         gate="scalar", dtype="bf16", init_state=True),
+    "kda_bf16_B1_H16_T65536_d128_init": ChunkWorkload(
+        "kda_bf16_B1_H16_T65536_d128_init", B=1, T=65536, H=16, dk=128, dv=128,
+        gate="channel", dtype="bf16", init_state=True),
 }
 DECODE_WORKLOADS = {
     "decode_scalar_B256_H32_d128": DecodeWorkload(

@@ -136,7 +136,8 @@ def sampled_chains(w, n, seed=0):
 @pytest.mark.parametrize("name,nsample", [
     ("gdn_bf16_B8_H16_T4096_d128", 6),
     ("kda_bf16_B4_H32_T8192_d128", 4),
-    ("gdn_bf16_B1_H16_T65536_d128_init", 2)])
+    ("gdn_bf16_B1_H16_T65536_d128_init", 2),
+    ("kda_bf16_B1_H16_T65536_d128_init", 2)])
 def test_full_size_sampled_chains(dr, name, nsample, out_dtype):
     """The workload at full size, in the launch configuration the benchmark times; the
     oracle recomputes a sample of whole (b, h) chains.  With an fp32-stored output the
@@ -334,3 +335,54 @@ def test_kda_tc_workspace_bytes(dr):
     desc = dr.chunk_desc(4, 8192, 32, 128, 128, dr.DR_BF16, dr.DR_BF16,
                          dr.DR_GATE_CHANNEL, 64)
     assert dr.workspace_bytes(desc) == 4 * 32 * 128 * 131584
+    # few long chains add three segment-state slabs of 64 KiB per (b, h, segment): 16 chains
+    # of 1024 chunks split into 9 segments of 114 chunks
+    desc = dr.chunk_desc(1, 65536, 16, 128, 128, dr.DR_BF16, dr.DR_BF16,
+                         dr.DR_GATE_CHANNEL, 64)
+    seg = 3 * 16 * 9 * 65536
+    assert dr.workspace_bytes(desc) == 16 * 1024 * 131584 + seg
+    assert dr.min_workspace_bytes(desc) == dr.workspace_bytes(desc)
+
+
+# Few long per-channel chains are split into segments too (end states of every segment from
+# a zero start and from the identity, the chaining of the affine maps, then the outputs).
+@pytest.mark.parametrize("B,T,H,la_range,out_dtype", [
+    (1, 4096, 2, (0.001, 0.1), None),            # 2 chains x 64 chunks -> 4 segments of 16
+    (1, 3000, 2, (0.0, 0.02), None),             # weak decay, ragged tail (47 chunks: 2 + 1)
+    (1, 16384, 4, (0.001, 0.1), torch.float32),  # 4 chains x 256 chunks -> 16 segments
+    (2, 2048, 3, (0.0, 0.005), torch.float32),   # very weak decay: the carry dominates
+])
+def test_kda_tc_segmented_long(dr, B, T, H, la_range, out_dtype):
+    d = inputs.chunk_inputs(B, T, H, 128, 128, gate="channel", dtype="bf16", init_state=True,
+                            seed=33 + T, log_alpha_range=la_range)
+    desc = dr.chunk_desc(B, T, H, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_CHANNEL, 64)
+    nch = B * H * -(-T // 64)
+    assert dr.workspace_bytes(desc) > nch * 131584    # the segmented path is taken
+    e1, e2 = check(dr, d, "bf16", out_dtype=out_dtype)
+    record(f"kda_segmented_B{B}_T{T}_H{H}", "out" if out_dtype is None else "out_f32",
+           err=e1, state=e2)
+
+
+def test_kda_tc_segmented_mixed_decay(dr):
+    """Half of the channels barely decay across the whole sequence, half decay steeply:
+    the segments' transitions keep the slow channels' state and drop the others."""
+    d = inputs.chunk_inputs(1, 4096, 2, 128, 128, gate="channel", dtype="bf16",
+                            init_state=True, seed=34, log_alpha_range=(0.0, 0.001))
+    d["log_alpha"][..., 64:] *= 1000.0      # -U(0, 1) on channels 64..127
+    check(dr, d, "bf16", out_dtype=torch.float32)
+
+
+def test_kda_tc_segmented_in_place_carry(dr):
+    """final_state == init_state on the segmented per-channel path."""
+    d = inputs.chunk_inputs(1, 2048, 2, 128, 128, gate="channel", dtype="bf16",
+                            init_state=True, seed=35, log_alpha_range=(0.0, 0.02))
+    g = dev(d)
+    st = g["init_state"].clone()
+    out, _ = dr.chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], st,
+                          final_state=st)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    o_ref, f_ref = oracle.forward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                  d["init_state"])
+    assert_close(out, o_ref, "bf16", "out")
+    assert_close(st, f_ref, "bf16", "final_state")

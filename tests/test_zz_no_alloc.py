@@ -42,9 +42,15 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
                              init_state=True, seed=43)
     desc3 = dr.chunk_desc(1, 4096, 2, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_SCALAR, 64)
     assert dr.workspace_bytes(desc3) > 0
+    # The per-channel gate's segment states follow its per-chunk operands in the scratch.
+    d4 = inputs.chunk_inputs(1, 4096, 2, 128, 128, gate="channel", dtype="bf16",
+                             init_state=True, seed=44)
+    desc4 = dr.chunk_desc(1, 4096, 2, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_CHANNEL, 64)
+    assert dr.workspace_bytes(desc4) > 2 * 64 * 131584
     _run_both(dr, d1, "bf16")
     _run_both(dr, d2, "f32")
     _run_both(dr, d3, "bf16")
+    _run_both(dr, d4, "bf16")
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
