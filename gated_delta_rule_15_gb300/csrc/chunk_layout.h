@@ -64,8 +64,13 @@ inline ChunkWorkspace simt_workspace_carve(void *base, int64_t B, int64_t H, int
 
 // CUDA-core path (chunk_simt.cu).  For the backward, `T_out` ([n][C][C]) and `ckpt`
 // ([n][dk][dv], the state at each chunk's start) are also written; `p.out` may then be NULL.
+// With `seg_ws` (simt_segment_floats(p) floats; NULL: whole chains) few long chains are split
+// into segments (the split rule is simt_segments).
 int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStream_t stream,
-                      float *T_out = nullptr, float *ckpt = nullptr, bool prep_only = false);
+                      float *T_out = nullptr, float *ckpt = nullptr, bool prep_only = false,
+                      float *seg_ws = nullptr);
+void simt_segments(int64_t chains, int dk, int dv, int NC, int *nseg, int *seg_len);
+size_t simt_segment_floats(const ChunkProblem &p);
 // Backward of the chunk forward on the CUDA cores (chunk_bwd.cu): gradients of
 // <d_out, out> + <d_final, final_state>.  Workspace: bwd_workspace_bytes(p).
 struct BwdIo {

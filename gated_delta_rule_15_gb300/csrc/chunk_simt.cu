@@ -36,6 +36,8 @@
 // Fused neighbours (DR_FUSE_* of include/dr.h): the prep kernel takes beta = sigmoid(logit)
 // (stored in beta's dtype) and divides each q and k row by its norm as soon as the rows are
 // in shared memory (fp32); the state kernel multiplies each output by silu(z).
+#include <algorithm>
+
 #include "common.cuh"
 #include "chunk_layout.h"
 #include "tc_common.cuh"
@@ -71,6 +73,14 @@ struct StateArgs {
     ChunkWorkspace ws;
     float *ckpt;     // backward only: the state at each chunk's start, [n][dk][dv] (NULL
                      // otherwise); with it, `out` may be NULL (no outputs written)
+    // Sequence segments (few long chains): role 0 runs whole sequences; role 1 runs each
+    // segment without outputs, its first dv/32 CTAs from S_0 = 0 (end state to ws_s0,
+    // [chains][nseg][dk][dv]) and its next dk/32 CTAs as the transition, from S_0 = I with
+    // no value term (U = 0; end state to ws_phi, [chains][nseg][dk][dk]); role 2 runs each
+    // segment from its start state (ws_start, [chains][nseg][dk][dv]), writing outputs.
+    int role, nseg, seg_len;
+    float *ws_phi, *ws_s0;
+    const float *ws_start;
 };
 
 // The per-channel gate needs its [64][dk] cumulative decays, the sub-chunk pair factors and
@@ -474,18 +484,49 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(StateArgs a) {
     float *sGam = sP + 64 * kLdA;                  // [DK]
 
     const int tiles = a.dv / kDvt;
-    const int jt = blockIdx.x % tiles;
-    const int64_t bh = blockIdx.x / tiles;
-    const int64_t h = bh % a.H, b = bh / a.H;
     const int C = a.C, NC = a.NC, dv = a.dv, tid = threadIdx.x;
     const int j = tid & 31, rg = tid >> 5;  // column in tile, row group (8 groups)
-    const int col = jt * kDvt + j;
     Tout *out = (Tout *)a.out;
+    // this CTA's chain, column tile and chunk range [c_begin, c_end); its start state (NULL:
+    // zero; `identity`: I) and end state, both with row stride `ld`
+    int64_t bh = blockIdx.x / tiles;
+    int jt = blockIdx.x % tiles, c_begin = 0, c_end = NC, ld = dv;
+    const float *s_init = a.init_state ? a.init_state + bh * DK * dv : nullptr;
+    float *s_fin = a.final_state ? a.final_state + bh * DK * dv : nullptr;
+    bool identity = false, use_u = true;
+    if (a.role != 0) {
+        const int per = a.role == 1 ? tiles + DK / kDvt : tiles;
+        const int64_t idx = blockIdx.x / per;
+        const int seg = (int)(idx % a.nseg);
+        jt = blockIdx.x % per;
+        bh = idx / a.nseg;
+        c_begin = seg * a.seg_len;
+        c_end = min(NC, c_begin + a.seg_len);
+        const size_t slot = (size_t)(bh * a.nseg + seg);
+        if (a.role == 1) {
+            out = nullptr;
+            s_init = nullptr;
+            if (jt >= tiles) {   // the transition: DK columns
+                jt -= tiles;
+                identity = true;
+                use_u = false;
+                ld = DK;
+                s_fin = a.ws_phi + slot * DK * DK;
+            } else {
+                s_fin = a.ws_s0 + slot * DK * dv;
+            }
+        } else {
+            s_init = a.ws_start + slot * DK * dv;
+            s_fin = (seg == a.nseg - 1 && a.final_state) ? a.final_state + bh * DK * dv : nullptr;
+        }
+    }
+    const int64_t h = bh % a.H, b = bh / a.H;
+    const int col = jt * kDvt + j;
 
     for (int i = rg; i < DK; i += 8)
-        sS[i * kDvt + j] = a.init_state ? a.init_state[(bh * DK + i) * dv + col] : 0.f;
+        sS[i * kDvt + j] = s_init ? s_init[(int64_t)i * ld + col] : (identity && i == col ? 1.f : 0.f);
 
-    for (int c = 0; c < NC; ++c) {
+    for (int c = c_begin; c < c_end; ++c) {
         const int64_t n = bh * NC + c;
         const int64_t t0 = (int64_t)c * C;
         const int Lc = (int)(a.T - t0 < (int64_t)C ? a.T - t0 : (int64_t)C);
@@ -502,7 +543,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(StateArgs a) {
             *reinterpret_cast<float4 *>(sKd + r * LD + c4) = load4(Kd + r * DK + c4);
         }
         for (int idx = tid; idx < C * kDvt; idx += kThreads)
-            sU[idx] = U[(idx / kDvt) * dv + jt * kDvt + idx % kDvt];
+            sU[idx] = use_u ? U[(idx / kDvt) * dv + jt * kDvt + idx % kDvt] : 0.f;
         for (int idx = tid; idx < C * C; idx += kThreads) sP[(idx / C) * kLdA + idx % C] = P[idx];
         for (int i = tid; i < DK; i += kThreads) sGam[i] = a.ws.gam[n * DK + i];
         if (a.ckpt)   // the state at this chunk's start (sS is final after the barrier above)
@@ -573,14 +614,56 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(StateArgs a) {
             for (int m = 0; m < NR; ++m) sS[(rg + 8 * m) * kDvt + j] = acc[m];
         }
     }
-    if (a.final_state) {
+    if (s_fin) {
         __syncthreads();
-        for (int i = rg; i < DK; i += 8) a.final_state[(bh * DK + i) * dv + col] = sS[i * kDvt + j];
+        for (int i = rg; i < DK; i += 8) s_fin[(int64_t)i * ld + col] = sS[i * kDvt + j];
+    }
+}
+
+// Segment chaining: per chain, S_start(0) = S_0 and S_start(p + 1) = Phi_p S_start(p) + S0_p
+// (Phi_p [DK][DK], S0_p and S_start [DK][dv], fp32).  One CTA per (chain, 32 state columns);
+// each Phi_p is staged in shared memory (combine_smem_bytes), each thread keeping DK / 8 rows
+// of one column.
+constexpr size_t combine_smem_bytes(int dk) { return sizeof(float) * (size_t)dk * (dk + 1); }
+template <int DK>
+__global__ void __launch_bounds__(kThreads) seg_combine_simt_kernel(const float *__restrict__ init_state,
+                                                                    const float *__restrict__ phi,
+                                                                    const float *__restrict__ s0,
+                                                                    float *__restrict__ start, int dv,
+                                                                    int nseg) {
+    __shared__ float S[DK][kDvt + 1];
+    extern __shared__ float4 phi_s4[];
+    float (*P)[DK + 1] = reinterpret_cast<float (*)[DK + 1]>(phi_s4);
+    constexpr int NR = DK / 8;
+    const int tiles = dv / kDvt;
+    const int jt = blockIdx.x % tiles;
+    const int64_t bh = blockIdx.x / tiles;
+    const int tid = threadIdx.x, j = tid & 31, rg = tid >> 5;
+    const int col = jt * kDvt + j;
+    for (int i = rg; i < DK; i += 8) S[i][j] = init_state ? init_state[(bh * DK + i) * dv + col] : 0.f;
+    for (int p = 0; p < nseg; ++p) {
+        const int64_t slot = bh * nseg + p;
+        __syncthreads();   // S is complete; the previous Phi's readers are done
+        for (int i = rg; i < DK; i += 8) start[(slot * DK + i) * dv + col] = S[i][j];
+        if (p + 1 == nseg) break;
+        for (int idx = tid; idx < DK * DK; idx += kThreads) P[idx / DK][idx % DK] = phi[slot * DK * DK + idx];
+        float acc[NR];
+#pragma unroll
+        for (int m = 0; m < NR; ++m) acc[m] = s0[(slot * DK + rg + 8 * m) * dv + col];
+        __syncthreads();
+        for (int k = 0; k < DK; ++k) {
+            const float sk = S[k][j];
+#pragma unroll
+            for (int m = 0; m < NR; ++m) acc[m] = fmaf(P[rg + 8 * m][k], sk, acc[m]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < NR; ++m) S[rg + 8 * m][j] = acc[m];
     }
 }
 
 template <int DK, typename Tin, typename Tout>
-int launch_simt_t(const PrepArgs &pa, const StateArgs &sa, cudaStream_t stream, bool prep_only) {
+int launch_simt_t(const PrepArgs &pa, StateArgs sa, cudaStream_t stream, bool prep_only, float *seg_ws) {
     const size_t ps = prep_smem_bytes(DK, pa.gate), ss = state_smem_bytes(DK);
     if (cudaFuncSetAttribute(chunk_prep_kernel<DK, Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)prep_smem_bytes(DK, 2)) != cudaSuccess ||
@@ -591,33 +674,82 @@ int launch_simt_t(const PrepArgs &pa, const StateArgs &sa, cudaStream_t stream, 
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss) != cudaSuccess)
         return kErrCuda;
     const int64_t nprep = pa.B * pa.H * pa.NC;
-    const int64_t nstate = sa.B * sa.H * (sa.dv / kDvt);
+    const int64_t bh = sa.B * sa.H, tiles = sa.dv / kDvt;
     if (nprep > 0) chunk_prep_kernel<DK, Tin><<<(unsigned)nprep, kThreads, ps, stream>>>(pa);
-    if (!prep_only) chunk_state_kernel<DK, Tout><<<(unsigned)nstate, kThreads, ss, stream>>>(sa);
+    if (prep_only) return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+    int nseg = 1, seg_len = sa.NC;
+    if (seg_ws) simt_segments(bh, DK, sa.dv, sa.NC, &nseg, &seg_len);
+    if (nseg <= 1) {
+        chunk_state_kernel<DK, Tout><<<(unsigned)(bh * tiles), kThreads, ss, stream>>>(sa);
+        return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+    }
+    // segments: end states and transitions, chaining, then outputs
+    const size_t ns = (size_t)bh * nseg;
+    sa.nseg = nseg;
+    sa.seg_len = seg_len;
+    sa.ws_phi = seg_ws;
+    sa.ws_s0 = seg_ws + ns * DK * DK;
+    float *start = sa.ws_s0 + ns * DK * sa.dv;
+    sa.ws_start = start;
+    sa.role = 1;
+    chunk_state_kernel<DK, Tout><<<(unsigned)(ns * (tiles + DK / kDvt)), kThreads, ss, stream>>>(sa);
+    constexpr int cs = (int)combine_smem_bytes(DK);
+    if (cudaFuncSetAttribute(seg_combine_simt_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, cs) !=
+        cudaSuccess)
+        return kErrCuda;
+    seg_combine_simt_kernel<DK><<<(unsigned)(bh * tiles), kThreads, cs, stream>>>(
+        sa.init_state, sa.ws_phi, sa.ws_s0, start, sa.dv, nseg);
+    sa.role = 2;
+    chunk_state_kernel<DK, Tout><<<(unsigned)(ns * tiles), kThreads, ss, stream>>>(sa);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
 }  // namespace
 
+// Few long chains: segments of at least 16 chunks, as many as let the first segment pass (one
+// CTA per 32 columns of the end state and of the transition, per segment) fill the 152 SMs
+// once.  nseg = 1: not split.
+void simt_segments(int64_t chains, int dk, int dv, int NC, int *nseg, int *seg_len) {
+    constexpr int64_t kGpuSms = 152;
+    *nseg = 1;
+    *seg_len = NC;
+    const int64_t per = chains * ((dv + dk) / kDvt);
+    if (NC < 32 || per > kGpuSms / 2) return;
+    const int n = (int)std::min<int64_t>(NC / 16, kGpuSms / per);
+    if (n < 2) return;
+    const int len = (NC + n - 1) / n;
+    *seg_len = len;
+    *nseg = (NC + len - 1) / len;
+}
+
+size_t simt_segment_floats(const ChunkProblem &p) {
+    int nseg, len;
+    simt_segments(p.B * p.H, p.dk, p.dv, p.NC, &nseg, &len);
+    if (nseg <= 1) return 0;
+    const size_t ns = (size_t)(p.B * p.H) * nseg;
+    return ns * p.dk * p.dk + 2 * ns * p.dk * p.dv;
+}
+
 int launch_chunk_simt(const ChunkProblem &p, const ChunkWorkspace &ws, cudaStream_t stream,
-                      float *T_out, float *ckpt, bool prep_only) {
+                      float *T_out, float *ckpt, bool prep_only, float *seg_ws) {
     PrepArgs pa{p.q, p.k, p.v, p.log_alpha, p.beta, p.B, p.T, p.H, p.dv, p.C, p.NC, p.gate, p.fuse, ws,
                 T_out};
     StateArgs sa{p.init_state, p.out, p.final_state, (p.fuse & kFuseGate) ? p.z : nullptr, p.in_bf16,
-                 p.B, p.T, p.H, p.dv, p.C, p.NC, ws, ckpt};
+                 p.B, p.T, p.H, p.dv, p.C, p.NC, ws, ckpt, 0, 1, p.NC, nullptr, nullptr, nullptr};
+    if (ckpt) seg_ws = nullptr;   // the backward's recompute walks whole chains
     using bf = __nv_bfloat16;
     const bool ib = p.in_bf16, ob = p.out_bf16;
     if (p.dk == 128) {
-        if (ib && ob) return launch_simt_t<128, bf, bf>(pa, sa, stream, prep_only);
-        if (ib) return launch_simt_t<128, bf, float>(pa, sa, stream, prep_only);
-        if (ob) return launch_simt_t<128, float, bf>(pa, sa, stream, prep_only);
-        return launch_simt_t<128, float, float>(pa, sa, stream, prep_only);
+        if (ib && ob) return launch_simt_t<128, bf, bf>(pa, sa, stream, prep_only, seg_ws);
+        if (ib) return launch_simt_t<128, bf, float>(pa, sa, stream, prep_only, seg_ws);
+        if (ob) return launch_simt_t<128, float, bf>(pa, sa, stream, prep_only, seg_ws);
+        return launch_simt_t<128, float, float>(pa, sa, stream, prep_only, seg_ws);
     }
     if (p.dk == 64) {
-        if (ib && ob) return launch_simt_t<64, bf, bf>(pa, sa, stream, prep_only);
-        if (ib) return launch_simt_t<64, bf, float>(pa, sa, stream, prep_only);
-        if (ob) return launch_simt_t<64, float, bf>(pa, sa, stream, prep_only);
-        return launch_simt_t<64, float, float>(pa, sa, stream, prep_only);
+        if (ib && ob) return launch_simt_t<64, bf, bf>(pa, sa, stream, prep_only, seg_ws);
+        if (ib) return launch_simt_t<64, bf, float>(pa, sa, stream, prep_only, seg_ws);
+        if (ob) return launch_simt_t<64, float, bf>(pa, sa, stream, prep_only, seg_ws);
+        return launch_simt_t<64, float, float>(pa, sa, stream, prep_only, seg_ws);
     }
     return kErrUnsupported;
 }

@@ -85,7 +85,8 @@ extern "C" int dr_chunk_fwd_workspace_bytes(const dr_chunk_desc *desc, size_t *b
     else if (chunk_kda_supported(p))
         *bytes = chunk_kda_workspace_bytes(p);
     else
-        *bytes = sizeof(float) * simt_workspace_floats(p.B, p.H, p.NC, p.C, p.dk, p.dv);
+        *bytes = sizeof(float) * (simt_workspace_floats(p.B, p.H, p.NC, p.C, p.dk, p.dv) +
+                                  simt_segment_floats(p));
     return kOk;
 }
 
@@ -156,7 +157,10 @@ extern "C" int dr_chunk_fwd_ex(const dr_chunk_desc *desc, uint32_t fuse, const v
         return launch_chunk_kda(p, workspace, status, (cudaStream_t)stream);
     }
     const ChunkWorkspace ws = simt_workspace_carve(workspace, p.B, p.H, p.NC, p.C, p.dk, p.dv);
-    return launch_chunk_simt(p, ws, (cudaStream_t)stream);
+    float *seg = simt_segment_floats(p) > 0
+                     ? (float *)workspace + simt_workspace_floats(p.B, p.H, p.NC, p.C, p.dk, p.dv)
+                     : nullptr;
+    return launch_chunk_simt(p, ws, (cudaStream_t)stream, nullptr, nullptr, false, seg);
 }
 
 extern "C" int dr_chunk_bwd_workspace_bytes(const dr_chunk_desc *desc, size_t *bytes) {

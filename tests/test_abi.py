@@ -65,6 +65,17 @@ def test_workspace_query(dr):
     assert dr.workspace_bytes(_desc(dr, gate=dr.DR_GATE_SCALAR, in_dtype=dr.DR_F32)) > 0
     for d in (_desc(dr), _desc(dr, in_dtype=dr.DR_F32), _desc(dr, T=0)):   # other paths: equal
         assert dr.min_workspace_bytes(d) == dr.workspace_bytes(d)
+    # few long chains on the per-channel tensor-core path: the segments' transitions,
+    # zero-start end states and start states, 64 KB each per (b, h, segment): 2 chains of 64
+    # chunks -> 4 segments
+    kda = _desc(dr, B=1, T=64 * 64, H=2)
+    assert dr.workspace_bytes(kda) == 2 * 64 * 131584 + 3 * 2 * 4 * 65536
+    # ... and on the CUDA-core path (fp32 slabs per chunk: W, Q*G, K*G_C/G [C][dk], U [C][dv],
+    # P [C][C], G_C [dk]; per segment Phi [dk][dk], S0 and the start [dk][dv]): 1 chain of 64
+    # chunks, dk = 64, dv = 128 -> 4 segments
+    simt = _desc(dr, B=1, T=64 * 64, H=1, dk=64, dv=128, in_dtype=dr.DR_F32, out_dtype=dr.DR_F32)
+    slabs = 64 * (64 * 64 * 3 + 64 * 128 + 64 * 64 + 64)
+    assert dr.workspace_bytes(simt) == 4 * (slabs + 4 * (64 * 64 + 2 * 64 * 128))
 
 
 @pytest.mark.parametrize("bad,status", [

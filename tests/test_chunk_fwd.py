@@ -243,6 +243,42 @@ def test_tc_segmented_long(dr, gate, T, la_range):
     check(dr, d, "bf16")
 
 
+# The CUDA-core path (fp32 inputs, or head sizes the tensor-core kernels do not take) splits
+# few long chains the same way: one CTA per 32 columns of each segment's end state and of its
+# transition, the chaining, then one CTA per 32 output columns of each segment.
+@pytest.mark.parametrize("B,T,H,dk,dv,gate,dtype,la_range", [
+    (1, 4096, 1, 128, 128, "scalar", "f32", (0.001, 0.1)),   # 1 chain x 64 chunks -> 4 segments
+    (1, 3000, 2, 64, 128, "channel", "f32", (0.0, 0.02)),    # dk != dv, weak decay, ragged: 2
+    (1, 8192, 1, 64, 64, "channel", "bf16", (0.001, 0.1)),   # 128 chunks -> 8 segments
+    (2, 2048, 1, 64, 64, "none", "f32", (0.001, 0.1)),       # DeltaNet: no decay at all
+])
+def test_simt_segmented_long(dr, B, T, H, dk, dv, gate, dtype, la_range):
+    d = inputs.chunk_inputs(B, T, H, dk, dv, gate=gate, dtype=dtype, init_state=True,
+                            seed=36 + T, log_alpha_range=la_range)
+    it = dr.DR_F32 if dtype == "f32" else dr.DR_BF16
+    desc = dr.chunk_desc(B, T, H, dk, dv, it, it, inputs.GATE_CODE[gate], 64)
+    nch, C = B * H * -(-T // 64), 64
+    base = 4 * nch * (C * dk * 3 + C * dv + C * C + dk)     # the per-chunk fp32 slabs
+    assert dr.workspace_bytes(desc) > base                  # the segmented path is taken
+    e1, e2 = check(dr, d, dtype)
+    record(f"simt_segmented_B{B}_T{T}_H{H}_d{dk}x{dv}_{gate}_{dtype}", "out", err=e1, state=e2)
+
+
+def test_simt_segmented_in_place_carry(dr):
+    d = inputs.chunk_inputs(1, 2048, 1, 64, 64, gate="scalar", dtype="f32", init_state=True,
+                            seed=37, log_alpha_range=(0.0, 0.02))
+    g = dev(d)
+    st = g["init_state"].clone()
+    out, _ = dr.chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], st,
+                          final_state=st)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    o_ref, f_ref = oracle.forward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                  d["init_state"])
+    assert_close(out, o_ref, "f32", "out")
+    assert_close(st, f_ref, "f32", "final_state")
+
+
 def test_tc_segmented_in_place_carry(dr):
     """final_state == init_state on the segmented path."""
     d = inputs.chunk_inputs(1, 2048, 2, 128, 128, gate="scalar", dtype="bf16",
