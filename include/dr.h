@@ -109,18 +109,25 @@ int dr_version(void);
 /* Bytes of device workspace dr_chunk_fwd takes for *desc on its fastest path; written to
    *bytes.  The answer depends only on the descriptor.  Returns DR_OK, DR_ERR_INVALID or
    DR_ERR_UNSUPPORTED.
-   For bf16 inputs, dk = dv = 128, chunk 64 and a scalar or no gate this is 16 KB per
-   (b, h, chunk) -- every chunk's triangular-solve operands (T = (I + A)^-1 of the WY form,
-   page "Transformer notes (5): linear attention optimisations", KDA paragraph), formed for
-   all chunks at once -- plus 3 * 64 KB per (b, h, segment) when few long chains are split
-   into segments. */
+   Few long chains (at most 76 for the tensor-core paths, at least 32 chunks each) are split
+   into segments that run side by side; each (b, h, segment) then takes three dk x dv fp32
+   states (the segment's transition dk x dk, its end state from a zero start, its start
+   state).  Besides those:
+     - bf16 inputs, dk = dv = 128, chunk 64, scalar or no gate: nothing for many chains; for
+       chains split into segments, also 16 KB per (b, h, chunk): every chunk's
+       triangular-solve operands (T = (I + A)^-1 of the WY form, page "Transformer notes
+       (5): linear attention optimisations", KDA paragraph), formed for all chunks at once;
+     - the same with the per-channel gate: 131,584 bytes of tensor-core operands per
+       (b, h, chunk);
+     - every other configuration (the CUDA-core path): the fp32 operands W, Q*G, K*G_C/G
+       [C][dk], U [C][dv], P [C][C] and G_C [dk] per (b, h, chunk). */
 int dr_chunk_fwd_workspace_bytes(const dr_chunk_desc *desc, size_t *bytes);
 
 /* The least workspace dr_chunk_fwd accepts for *desc; written to *bytes.  Equal to
-   dr_chunk_fwd_workspace_bytes() except for the configuration named there, where a
-   workspace below that size (but at least this one: only the segments' states, 0 unless
-   few long chains are split) selects a single kernel that solves inside each chain, with the
-   same results up to rounding.  Returns as dr_chunk_fwd_workspace_bytes. */
+   dr_chunk_fwd_workspace_bytes() except for the scalar / no-gate tensor-core configuration
+   with chains split into segments, where a workspace below that size (but at least this
+   one: the segments' states alone) selects a single kernel that solves inside each chain,
+   with the same results up to rounding.  Returns as dr_chunk_fwd_workspace_bytes. */
 int dr_chunk_fwd_min_workspace_bytes(const dr_chunk_desc *desc, size_t *bytes);
 
 /*
