@@ -242,10 +242,12 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __nv_bfloat16 *__r
 constexpr int kChainThreads = 352;             // 11 warps
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpGate = 2, kWarpO0 = 7;   // state warps: 3..6
 // shared memory (offsets from the 1024-byte-aligned base)
-constexpr uint32_t C_STAGE = 49152;            // one q/k stage: two K-blocks of [Q | K], then W^T
-constexpr uint32_t C_KB = 16384;               // one K-block (64 of the 128 key channels)
-constexpr uint32_t C_OFF_Q = 0, C_OFF_K = 8192;
-constexpr uint32_t C_OFF_W = 32768;            // W^T (128 key channels x 64 tokens, bf16, MN-major)
+// One stage: two K-blocks (64 of the 128 key channels each) of [W | Q | K], every part 64
+// rows (tokens) x 128 bytes, K-major with the 128-byte swizzle, so that [W; Q] is one
+// 128-row B operand ((W S)^T and (Q S)^T in one product) and [Q; K] one 128-row A operand.
+constexpr uint32_t C_STAGE = 49152;
+constexpr uint32_t C_KB = 24576;
+constexpr uint32_t C_OFF_W = 0, C_OFF_Q = 8192, C_OFF_K = 16384;
 constexpr uint32_t C_VU = 2 * C_STAGE;         // v tile (two 64-channel halves) and T diag(beta)
 constexpr uint32_t C_TB = C_VU + 16384;        //   T diag(beta) (bf16, 8 KB)
 constexpr uint32_t C_WT = C_VU + 24576;        // T diag(beta G) of two chunks (8 KB each)
@@ -268,8 +270,8 @@ enum { GV_G = 0, GV_GAM = 1, GV_DEL = 2, GV_BETA = 3, GV_E = 4, GV_F = 5 };
 
 constexpr uint32_t ID_X = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_UW = idesc_bf16(128, 64, true, false);
-constexpr uint32_t ID_WS = idesc_bf16(128, 64, false, true);   // B = W^T rows (MN-major)
-constexpr uint32_t ID_QS = idesc_bf16(128, 64, false, false);  // B = Q rows (K-major)
+constexpr uint32_t ID_D = idesc_bf16(128, 128, false, false);  // B = [W; Q] rows (K-major)
+constexpr uint32_t ID_DW = idesc_bf16(128, 64, false, false);  // B = W rows alone (no outputs)
 constexpr uint32_t ID_UPD = idesc_tf32(128, 192);
 constexpr uint32_t ID_UPD_S = idesc_tf32(128, 128);
 
@@ -390,6 +392,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     };
     // bounded wait; false (and nothing further to do) once the CTA has failed
     auto wait_bar = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) {   // already complete: the common case, no further reads
+            tc_fence_after();
+            return true;
+        }
         if (*abort_v) return false;
         if (!wait_cycles(bar, parity)) {
             fail();
@@ -491,9 +497,22 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     } else if (warp == kWarpMma) {
         // ---------------- MMA issue
         if (lane == 0 && n_it > 0) {
+            // waits without the tcgen05 fence (about 250 cycles each in this thread, whose
+            // own MMAs are in flight); one fence before each group of MMAs orders it after
+            // the waits before it
+            auto wait_m = [&](uint64_t *bar, uint32_t parity) -> bool {
+                if (mbar_try_wait(bar, parity)) return true;
+                if (*abort_v) return false;
+                if (!wait_cycles(bar, parity)) {
+                    fail();
+                    return false;
+                }
+                return true;
+            };
             uint64_t *last = nullptr;
             uint32_t last_par = 0;
             auto issue_x = [&](int it) {   // X = [Q; K] K^T (rows 0..63: Q K^T)
+                tc_fence_after();
                 unsigned char *st = stage(it);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -504,6 +523,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 last = &x_done; last_par = it & 1;
             };
             auto issue_w = [&](int it) {   // W^T = K^T (T diag(beta G))^T
+                tc_fence_after();
                 const uint32_t sk = (uint32_t)(stage(it) - sm) + C_OFF_K, wt = C_WT + (it & 1) * 8192;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
@@ -513,6 +533,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 last = &w_done; last_par = it & 1;
             };
             auto issue_u = [&](int it) {   // U^T = V^T (T diag beta)^T
+                tc_fence_after();
                 if (!zero_u)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
@@ -523,49 +544,48 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             };
             bool ok = true;
             if (outputs) {
-                ok = wait_bar(&qkw_full[0], 0);
+                ok = wait_m(&qkw_full[0], 0);
                 if (ok) issue_x(0);
             }
-            ok = ok && wait_bar(&qkw_full[0], 0) && wait_bar(&wt_full[0], 0);
+            ok = ok && wait_m(&qkw_full[0], 0) && wait_m(&wt_full[0], 0);
             if (ok) issue_w(0);
-            ok = ok && (zero_u || wait_bar(&vu_full, 0));
+            ok = ok && (zero_u || wait_m(&vu_full, 0));
             if (ok) issue_u(0);
             for (int it = 0; ok && it < n_it; ++it) {
                 const uint32_t par = it & 1;
                 const int s = it & 1;
                 const bool next = it + 1 < n_it;
-                // (W S)^T and (Q S)^T: A = S^T (bf16 pairs in tensor memory), B = W^T (MN-major
-                // rows written by warps 7..10) and Q (the stage)
-                if (!wait_bar(&sb_ready, par) || !wait_bar(&w_ready, par)) break;
-                if (outputs && it >= 1 && !wait_bar(&o_read, par ^ 1)) break;
+                // [(W S)^T | (Q S)^T] in one N = 128 product: A = S^T (bf16 pairs in tensor
+                // memory), B = [W; Q] (W written by warps 7..10 above Q in the stage); without
+                // outputs (W S)^T alone
+                if (!wait_m(&sb_ready, par) || !wait_m(&w_ready, par)) break;
+                if (outputs && it >= 1 && !wait_m(&o_read, par ^ 1)) break;
+                tc_fence_after();
                 const uint32_t sw = (uint32_t)(stage(it) - sm);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ts(tmb + TM_WE, tmb + TM_SB + 8 * ks, desc_add(dMk, sw + C_OFF_W + ks * 2048), ID_WS,
+                    mma_bf16_ts(tmb + TM_WE, tmb + TM_SB + 8 * ks,
+                                desc_add(dK0, sw + C_OFF_W + (ks >> 2) * C_KB + (ks & 3) * 32), outputs ? ID_D : ID_DW,
                                 ks > 0);
-                if (outputs)
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ts(tmb + TM_QO, tmb + TM_SB + 8 * ks,
-                                    desc_add(dK0, sw + C_OFF_Q + (ks >> 2) * C_KB + (ks & 3) * 32), ID_QS, ks > 0);
                 mma_commit(&d_done);
                 mma_commit(&stage_free[s]);
                 last = &d_done; last_par = par;
-                // W(it + 1): its conversion (warps 7..10) has all of this chunk's time
+                // The tensor pipe runs one CTA's MMAs in issue order, and issuing blocks this
+                // thread while earlier MMAs drain, so the order below keeps the state's own
+                // products (D, the update) from queueing behind work for the next chunk that
+                // can wait: W(it + 1) (its conversion by warps 7..10 feeds D(it + 1)) runs
+                // while E(it) forms; X(it + 1) and U(it + 1) follow the update and run while
+                // the next S^T operand forms.
                 if (next) {
-                    if (!wait_bar(&qkw_full[(it + 1) & 1], ((it + 1) >> 1) & 1) ||
-                        !wait_bar(&wt_full[(it + 1) & 1], ((it + 1) >> 1) & 1))
+                    if (!wait_m(&qkw_full[(it + 1) & 1], ((it + 1) >> 1) & 1) ||
+                        !wait_m(&wt_full[(it + 1) & 1], ((it + 1) >> 1) & 1))
                         break;
                     issue_w(it + 1);
                 }
-                // X(it + 1) once P(it) has been read out of TM_X: it runs while E(it) forms
-                if (outputs && next) {
-                    if (!wait_bar(&p_ready, par)) break;
-                    issue_x(it + 1);
-                }
                 // [O^T | S^T] += E^T [P; Kt^T]^T  (tf32; E^T from tensor memory)
-                if (!wait_bar(&e_ready, par) || !wait_bar(&kt_ready, par)) break;
-                if (outputs && !wait_bar(&p_ready, par)) break;
+                if (!wait_m(&e_ready, par) || !wait_m(&kt_ready, par)) break;
+                if (outputs && !wait_m(&p_ready, par)) break;
+                tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     mma_tf32_ts(tmb + (outputs ? TM_QO : TM_S), tmb + TM_WE + 8 * ks,
@@ -573,9 +593,11 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                                 outputs ? ID_UPD : ID_UPD_S, true);
                 mma_commit(&u_done);
                 last = &u_done; last_par = par;
+                // X(it + 1): P(it) has been read out of TM_X (p_ready above)
+                if (outputs && next) issue_x(it + 1);
                 // U(it + 1) (E(it) has read U(it))
                 if (next) {
-                    if (!zero_u && !wait_bar(&vu_full, (it + 1) & 1)) break;
+                    if (!zero_u && !wait_m(&vu_full, (it + 1) & 1)) break;
                     issue_u(it + 1);
                 }
             }
@@ -752,22 +774,20 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         const int to_ = tid - 32 * kWarpO0;   // 0..127
         constexpr int kOutBoxes = sizeof(Tout) == 2 ? 2 : 4;
         const bool prows = (warp & 3) < 2;    // TMEM lanes 0..63: the Q K^T rows of X
-        // W^T (lane i = key channel, 64 tokens) -> W (bf16, K-major) in the W slot of stage it
+        // W^T (lane i = key channel, 64 tokens) -> W (bf16, K-major) in the W slot of stage it:
+        // column i of the 64 token rows (a warp's 32 channels fill 64 contiguous bytes of a row)
         auto convert_w = [&](int it) -> bool {
             if (!wait_bar(&w_done, it & 1)) return false;
-            // row i of W^T (64 tokens, 128 bytes): the MN-major B operand of (W S)^T
-            const uint32_t dst = smem_u32(stage(it)) + C_OFF_W + row * 128;
+            const uint32_t dst = smem_u32(stage(it)) + C_OFF_W + (row >> 6) * C_KB;
+            const uint32_t ci = row & 63;
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
                 float w[32];
                 tmem_ld32(tm + TM_W + 32 * hh, w);
                 tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float *f = w + 8 * c;
-                    sts128(dst + (((4 * hh + c) ^ (row & 7)) << 4), pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
-                           pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
-                }
+                for (int u = 0; u < 32; ++u)
+                    sts16(dst + sw128_off(32 * hh + u, ci), __bfloat16_as_ushort(__float2bfloat16_rn(w[u])));
             }
             fence_proxy_async();
             tc_fence_before();
