@@ -307,9 +307,13 @@ def bench_fused(w, steps, warmup, world):
                             init_state=w.init_state, log_alpha_range=w.log_alpha_range, raw=True)
     g = {k: (None if t is None else t.cuda()) for k, t in d.items()}
     out = torch.empty((w.B, w.T, w.H, w.dv), dtype=g["q"].dtype, device="cuda")
+    fin = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+    desc = dr.chunk_desc(w.B, w.T, w.H, w.dk, w.dv, dr._DT[g["q"].dtype], dr._DT[out.dtype],
+                         inputs.GATE_CODE[w.gate], w.chunk)
+    ws = torch.empty(max(16, dr.ex_workspace_bytes(desc, dr.DR_FUSE_ALL)), dtype=torch.uint8, device="cuda")
     call = lambda: dr.chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"],
-                                g["init_state"], chunk=w.chunk, out=out, qk_l2norm=True,
-                                beta_sigmoid=True, z=g["z"])
+                                g["init_state"], chunk=w.chunk, out=out, final_state=fin,
+                                workspace=ws, qk_l2norm=True, beta_sigmoid=True, z=g["z"])
     ms, _ = time_calls(call, steps, warmup, world)
     return ms
 

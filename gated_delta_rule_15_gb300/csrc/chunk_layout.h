@@ -95,6 +95,8 @@ int launch_chunk_bwd(const ChunkProblem &p, const BwdIo &g, void *workspace, int
 // DR_ERR_TIMEOUT there).
 bool chunk_tc_supported(const ChunkProblem &p);
 size_t chunk_tc_workspace_bytes(const ChunkProblem &p, bool least = false);
+// The workspace of the fastest path for the fused neighbours p.fuse (the two-kernel path).
+size_t chunk_tc_fused_workspace_bytes(const ChunkProblem &p);
 // With `ckpt` ([B*H][NC][dk][dv] fp32), it writes the state at every chunk's start instead of
 // the outputs (the backward's recompute).
 int launch_chunk_tc(const ChunkProblem &p, void *workspace, size_t workspace_bytes, int *status_word,

@@ -960,14 +960,18 @@ void tc_segment_split(const ChunkProblem &p, int *nseg, int *seg_len) {
 }
 
 size_t gdn_split_workspace_bytes(const ChunkProblem &p);
+bool gdn_split_fuse_supported(const ChunkProblem &p);
 int launch_gdn_split(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream);
 
-// Few long chains split into segments (plain forward) take the two-kernel path of
-// gdn_chain.cu when the workspace holds every chunk's T operands: its chunk-parallel solve
-// keeps all SMs busy and its chain kernel is lighter per chunk (measured on B1 H16 T65536:
-// 1.54 ms against 1.77 ms).  Many chains keep the single kernel below, which solves inside
-// the chain (B8 H16 T4096: 0.364 ms against 0.387 ms) and needs only the segments' states;
-// it also serves the fused neighbours and the backward's checkpoints.
+// Few long chains split into segments take the two-kernel path of gdn_chain.cu when the
+// workspace holds every chunk's T operands: its chunk-parallel solve keeps all SMs busy and
+// its chain kernel is lighter per chunk (measured on B1 H16 T65536: 1.43 ms against 1.73 ms).
+// Many chains keep the single kernel below for the plain forward, which solves inside the
+// chain (B8 H16 T4096: 0.373 ms against 0.398 ms) and needs only the segments' states.  The
+// fused neighbours cost the two-kernel path little (its prep kernel applies the L2 norm and
+// the sigmoid; the chain folds the norms into factors it applies anyway), so they take it
+// whenever the workspace allows; otherwise the single kernel serves them, as it serves the
+// backward's checkpoints.
 static bool split_path(const ChunkProblem &p) {
     int nseg, len;
     tc_segment_split(p, &nseg, &len);
@@ -981,9 +985,14 @@ size_t chunk_tc_workspace_bytes(const ChunkProblem &p, bool least) {
     return nseg > 1 ? (size_t)3 * p.B * p.H * nseg * 16384 * sizeof(float) : 0;
 }
 
+size_t chunk_tc_fused_workspace_bytes(const ChunkProblem &p) {
+    return gdn_split_fuse_supported(p) ? gdn_split_workspace_bytes(p) : chunk_tc_workspace_bytes(p, true);
+}
+
 int launch_chunk_tc(const ChunkProblem &p, void *workspace, size_t workspace_bytes, int *status_word,
                     cudaStream_t stream, float *ckpt) {
-    if (!ckpt && !p.fuse && split_path(p) && workspace && workspace_bytes >= gdn_split_workspace_bytes(p))
+    if (!ckpt && (p.fuse ? gdn_split_fuse_supported(p) : split_path(p)) && workspace &&
+        workspace_bytes >= gdn_split_workspace_bytes(p))
         return launch_gdn_split(p, workspace, status_word, stream);
     CUtensorMap mq, mk, mv, mo, mz;
     const bool zgate = (p.fuse & kFuseGate) != 0;

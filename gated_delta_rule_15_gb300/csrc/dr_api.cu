@@ -108,6 +108,19 @@ extern "C" int dr_chunk_fwd_min_workspace_bytes(const dr_chunk_desc *desc, size_
     return chunk_fwd_least_workspace(desc, bytes);
 }
 
+extern "C" int dr_chunk_fwd_ex_workspace_bytes(const dr_chunk_desc *desc, uint32_t fuse, size_t *bytes) {
+    if (!bytes || (fuse & ~DR_FUSE_ALL)) return kErrInvalid;
+    ChunkProblem p{};
+    const int rc = check_chunk_desc(desc, &p);
+    if (rc != kOk) return rc;
+    p.fuse = fuse;
+    if (fuse && chunk_tc_supported(p)) {
+        *bytes = chunk_tc_fused_workspace_bytes(p);
+        return kOk;
+    }
+    return dr_chunk_fwd_workspace_bytes(desc, bytes);
+}
+
 // Whether byte ranges [a, a + na) and [b, b + nb) overlap.
 static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     const char *a0 = (const char *)a, *b0 = (const char *)b;

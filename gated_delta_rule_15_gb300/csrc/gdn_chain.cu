@@ -73,14 +73,22 @@ constexpr float kSpan = 80.f;
 // T diag(beta) | T diag(beta G) in bf16; the 16 KB image leaves by one bulk store.  Tokens
 // past T are zero rows of K (the TMA fill) with beta = 0, T being the identity there, as the
 // chain kernel's loads make them.
+// Fused neighbours (DR_FUSE_* of include/dr.h): beta = sigmoid(logit) rounded to beta's bf16;
+// with the L2 norm the q tile arrives too, each thread takes 1 / |x| of one row of [Q; K]
+// (written to the workspace's norm vectors for the chain kernel), A takes the normalised
+// rows' products n_r n_s (k_r . k_s), and the second operand becomes T diag(beta G n), so
+// that W = T diag(beta G) diag(n) K is formed from the raw k tile.
 constexpr int kPrepThreads = 128;
 constexpr uint32_t PR_K = 0;                       // k tile (two 64-channel halves, swizzled);
                                                    // then the fp32 T (swizzled)
 constexpr uint32_t PR_A = 16384;                   // fp32 A (a_index)
 constexpr uint32_t PR_TB = PR_A + 16384;           // the operand image
 constexpr uint32_t PR_M = PR_TB + 16384;           // solve scratch
-constexpr uint32_t PR_V = PR_M + 4096;             // g, G, beta, exp(g - g_31), exp(g_31 - g)
-constexpr uint32_t PR_TOTAL = PR_V + 5 * 256;
+constexpr uint32_t PR_V = PR_M + 4096;             // g, G, beta, exp(g - g_31), exp(g_31 - g),
+                                                   // 1/|q|, 1/|k|, G/|k|
+constexpr uint32_t PR_TOTAL = PR_V + 8 * 256;
+constexpr uint32_t PR_Q = (PR_TOTAL + 1023) / 1024 * 1024;   // q tile (fused L2 norm only)
+constexpr uint32_t PR_TOTAL_L2 = PR_Q + 16384;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -96,9 +104,10 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
 
 template <int GATE>
 __global__ void __launch_bounds__(kPrepThreads, 4)
-gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __nv_bfloat16 *__restrict__ beta,
-                const float *__restrict__ log_alpha, unsigned char *__restrict__ tops, int T, int H, int NC,
-                unsigned nchunks, int *status) {
+gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tq,
+                const __nv_bfloat16 *__restrict__ beta, const float *__restrict__ log_alpha,
+                unsigned char *__restrict__ tops, float *__restrict__ norms, int T, int H, int NC,
+                unsigned nchunks, uint32_t fuse, int *status) {
     extern __shared__ unsigned char prep_sm[];
     unsigned char *sm = align1024(prep_sm);
     __shared__ uint64_t bar_k;
@@ -107,6 +116,8 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __nv_bfloat16 *__r
     float *sA = reinterpret_cast<float *>(sm + PR_A);
     float *sV = reinterpret_cast<float *>(sm + PR_V);
     float *sG = sV, *sGam = sV + 64, *sBeta = sV + 128, *sE = sV + 192, *sF = sV + 256;
+    float *sNq = sV + 320, *sNk = sV + 384, *sGn = sV + 448;
+    const bool l2 = (fuse & kFuseL2) != 0, sig = (fuse & kFuseSigmoid) != 0;
     if (tid == 0) {
         mbar_init(&bar_k, 1);
         abort_s = 0;
@@ -124,13 +135,18 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __nv_bfloat16 *__r
         if (tid == 0) {
             // the previous chunk's image must have been read out before the solve rewrites it
             bulk_wait_read_all();
-            mbar_arrive_expect_tx(&bar_k, 16384);
+            mbar_arrive_expect_tx(&bar_k, l2 ? 32768 : 16384);
             for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + PR_K + kb * 8192, &tk, &bar_k, 64 * kb, h, t0, b);
+            if (l2)
+                for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + PR_Q + kb * 8192, &tq, &bar_k, 64 * kb, h, t0, b);
             const unsigned nn = n + gridDim.x;
             if (nn < nchunks) {
                 int h2, b2, t2;
                 coords(nn, h2, b2, t2);
-                for (int kb = 0; kb < 2; ++kb) tma_prefetch_4d(&tk, 64 * kb, h2, t2, b2);
+                for (int kb = 0; kb < 2; ++kb) {
+                    tma_prefetch_4d(&tk, 64 * kb, h2, t2, b2);
+                    if (l2) tma_prefetch_4d(&tq, 64 * kb, h2, t2, b2);
+                }
             }
         }
         if (warp == 1) {   // the next chunk's gates into L2 (two tokens per lane)
@@ -153,6 +169,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __nv_bfloat16 *__r
                 const int t = t0 + 2 * lane + e;
                 const size_t tok = ((size_t)b * T + t) * H + h;
                 bt[e] = t < T ? __bfloat162float(beta[tok]) : 0.f;
+                if (sig && t < T) bt[e] = round_bf16(sigmoid_f(bt[e]));
                 l[e] = (GATE == 1 && t < T) ? log_alpha[tok] : 0.f;
             }
             float p = l[0] + l[1];
@@ -182,6 +199,32 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __nv_bfloat16 *__r
         }
         __syncthreads();
         if (abort_s) break;
+        if (l2) {   // 1 / |x| of row tid of [Q; K] (zero rows past T give 1 / sqrt(eps), unused)
+            const unsigned char *src = sm + (tid < 64 ? PR_Q : PR_K) + (tid & 63) * 128;
+            float ss = 0.f;
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(src + kb * 8192 + 16 * (j ^ (tid & 7)));
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+                        ss = fmaf(f.x, f.x, ss);
+                        ss = fmaf(f.y, f.y, ss);
+                    }
+                }
+            const float inv = rsqrtf(ss + kL2NormEps);
+            if (tid < 64) {
+                sNq[tid] = inv;
+            } else {
+                sNk[tid - 64] = inv;
+                sGn[tid - 64] = sGam[tid - 64] * inv;
+            }
+            norms[(size_t)n * 128 + tid] = inv;
+            __syncthreads();
+        }
 
         // X on the lower blocks and A from it: warp w owns rows 16 w .. 16 w + 15
         {
@@ -214,7 +257,8 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __nv_bfloat16 *__r
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const int s = s0 + e;
-                            const float dec = fac ? sE[r] * sF[s] : __expf(fminf(sG[r] - sG[s], 0.f));
+                            float dec = fac ? sE[r] * sF[s] : __expf(fminf(sG[r] - sG[s], 0.f));
+                            if (l2) dec *= sNk[r] * sNk[s];
                             v[e] = s < r ? sBeta[r] * dec * acc[nt][2 * hf + e] : 0.f;
                             if (cb != warp) v[e] = round_tf32(v[e]);
                         }
@@ -224,7 +268,8 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __nv_bfloat16 *__r
         }
         __syncthreads();   // the k tile is dead: T goes over it
 
-        const SolveOut<true, true, true> out{reinterpret_cast<float *>(sm + PR_K), sm + PR_TB, sBeta, sGam, nullptr};
+        const SolveOut<true, true, true> out{reinterpret_cast<float *>(sm + PR_K), sm + PR_TB, sBeta,
+                                             l2 ? sGn : sGam, nullptr};
         solve_diag64(sA, out, tid);          // diagonal blocks 0, 1 (and operand zero blocks)
         solve_diag64(sA, out, tid + 128);    // diagonal blocks 2, 3
         __syncthreads();
@@ -254,8 +299,11 @@ constexpr uint32_t C_WT = C_VU + 24576;        // T diag(beta G) of two chunks (
 constexpr uint32_t C_BU = C_WT + 16384;        // tf32 [P; Kt^T]: two K-blocks of 32 tokens
 constexpr uint32_t C_BU_KB = 24576;            // 192 rows x 128 bytes
 constexpr uint32_t C_OUT = C_BU + 2 * C_BU_KB; // output staging (bf16: 2 boxes, fp32: 4 boxes)
-constexpr uint32_t C_SMALL = C_OUT + 32768;    // gate vectors [2][6][64] and raw gates [2][128]
-constexpr uint32_t C_TOTAL = C_SMALL + 4096;
+constexpr uint32_t C_Z = C_OUT + 16384;        // (bf16 outputs, fused output gate) the z tile
+constexpr uint32_t C_SMALL = C_OUT + 32768;    // gate vectors [2][8][64], raw gates [2][128],
+                                               // row norms [2][128]
+constexpr uint32_t C_GATE = C_SMALL + 4096, C_NORM = C_SMALL + 5120;
+constexpr uint32_t C_TOTAL = C_SMALL + 6144;
 static_assert(C_TOTAL + 1024 <= 227 * 1024, "layout");
 // tensor memory columns
 constexpr uint32_t TM_WE = 0;     // (W S)^T, then E^T (fp32)
@@ -265,8 +313,10 @@ constexpr uint32_t TM_SB = 256;   // S^T as bf16 pairs (the A operand of [W S | 
 constexpr uint32_t TM_X = 320;    // [Q; K] K^T
 constexpr uint32_t TM_W = 384;    // W^T
 constexpr uint32_t TM_U = 448;    // U^T
-// gate vector slots of one set
-enum { GV_G = 0, GV_GAM = 1, GV_DEL = 2, GV_BETA = 3, GV_E = 4, GV_F = 5 };
+// gate vector slots of one set: g, G, delta/|k|, G/|q|, exp(g - g_31)/|q|, exp(g_31 - g)/|k|,
+// 1/|q|, 1/|k| (the norms are 1 without the fused L2 norm)
+enum { GV_G = 0, GV_GAM = 1, GV_DEL = 2, GV_GQ = 3, GV_E = 4, GV_F = 5, GV_NQ = 6, GV_NK = 7 };
+constexpr int kGvSet = 8 * 64;
 
 constexpr uint32_t ID_X = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_UW = idesc_bf16(128, 64, true, false);
@@ -289,6 +339,12 @@ struct ChainArgs {
     // segment from its true start state (ws_start) writing outputs.
     int role, nseg, seg_len;
     float *ws_phi, *ws_s0, *ws_start;
+    // fused neighbours (DR_FUSE_*): the prep kernel has applied beta = sigmoid(logit) and the
+    // L2 norm's effect on A and W; with the L2 norm the chain scales P, Kt and Q S by the row
+    // norms the prep kernel wrote to `norms` ([B*H][NC][1/|q| x 64, 1/|k| x 64]); with the
+    // output gate (bf16 outputs) each output is multiplied by silu(z), z's tile by TMA
+    uint32_t fuse;
+    const float *norms;
 };
 
 // byte offset of fp32 element (row, k), k < 32, in a 128-byte-swizzled K-major tf32 tile
@@ -297,7 +353,7 @@ __device__ __forceinline__ uint32_t sw128_off32(uint32_t row, uint32_t k) {
 }
 
 // Per chunk it (period: from the state update of it - 1 to that of it), the MMA warp issues
-//   [W S | Q S](it)  W(it + 1)  X(it + 1)  update(it)  U(it + 1)
+//   [W S | Q S](it)  W(it + 1)  update(it)  X(it + 1)  U(it + 1)
 // so that only the state's own steps sit between two updates: S^T -> bf16 (warps 3..6),
 // [W S | Q S], E (warps 3..6), update.  Everything else is formed a chunk ahead or behind:
 // W(it + 1) and its conversion during chunk it (its T operand has a double buffer), P and
@@ -306,7 +362,7 @@ template <typename Tout, int GATE>
 __global__ void __launch_bounds__(kChainThreads, 1)
 gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
-                 const ChainArgs a) {
+                 const __grid_constant__ CUtensorMap tz, const ChainArgs a) {
     extern __shared__ unsigned char dsm_raw[];
     unsigned char *sm = align1024(dsm_raw);
     // Completed by TMA transactions or tcgen05.commit (count 1) ...
@@ -314,7 +370,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     // ... or by every thread of a group (stage_free: the commit of [W S | Q S] and warps
     // 7..10 after Kt^T; gset_free: warps 3..10 after their last use of a gate set).
     __shared__ uint64_t sb_ready, p_ready, e_ready, w_ready, kt_ready, o_read;
-    __shared__ uint64_t stage_free[2], g_ready[2], gset_free[2];
+    __shared__ uint64_t stage_free[2], g_ready[2], gset_free[2], z_full;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s, fac_s[2];
 
@@ -351,16 +407,20 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     const int n_it = c_end - c_begin;
     auto tops = [&](int it) { return a.tops + ((size_t)bh * a.NC + c_begin + it) * 16384; };
 
-    float *sVec = reinterpret_cast<float *>(sm + C_SMALL);   // [2][6][64]
+    float *sVec = reinterpret_cast<float *>(sm + C_SMALL);   // [2][8][64]
     const uint32_t sm_s = smem_u32(sm);                      // the same bytes by shared address
-    auto vec_s = [&](int it, int k) { return sm_s + C_SMALL + 4u * ((it & 1) * 384 + 64 * k); };
-    auto vec = [&](int it, int k) { return sVec + (it & 1) * 384 + 64 * k; };
-    uint32_t *sGate = reinterpret_cast<uint32_t *>(sm + C_SMALL + 3072);   // [2][beta word | log alpha][64]
+    auto vec_s = [&](int it, int k) { return sm_s + C_SMALL + 4u * ((it & 1) * kGvSet + 64 * k); };
+    auto vec = [&](int it, int k) { return sVec + (it & 1) * kGvSet + 64 * k; };
+    uint32_t *sGate = reinterpret_cast<uint32_t *>(sm + C_GATE);   // [2][beta word | log alpha][64]
+    float *sNorm = reinterpret_cast<float *>(sm + C_NORM);         // [2][1/|q| | 1/|k|][64]
+    const bool l2 = (a.fuse & kFuseL2) != 0;
+    const bool zgate = (a.fuse & kFuseGate) != 0 && outputs;
 
     if (tid == 0) {
         uint64_t *ones[] = {&qkw_full[0], &qkw_full[1], &wt_full[0], &wt_full[1], &wt_free[0], &wt_free[1],
                             &vu_full,     &x_done,      &w_done,     &uu_done,    &d_done,     &u_done};
         for (uint64_t *bb : ones) mbar_init(bb, 1);
+        mbar_init(&z_full, 1);
         uint64_t *groups[] = {&sb_ready, &e_ready, &w_ready, &kt_ready, &o_read};
         for (uint64_t *bb : groups) mbar_init(bb, 128);
         mbar_init(&p_ready, 256);   // warps 3..10 (P is built by warps 4, 5, 8, 9)
@@ -428,14 +488,17 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int e = 0; e < 4; ++e) pv[e] = s0 + e <= r ? round_tf32(er * fs[e] * x[4 * c4 + e]) : 0.f;
                 sts128f(sm_s + C_BU + hh * C_BU_KB + sw128_off32(r, 4 * c4), pv[0], pv[1], pv[2], pv[3]);
             }
-        } else {
+        } else {   // with the row norms 1/|q_r| and 1/|k_s|
+            const uint32_t sNk = vec_s(it, GV_NK);
+            const float nqr = lds32f(vec_s(it, GV_NQ) + 4 * r);
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
                 const int s0 = 32 * hh + 4 * c4;
                 float pv[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    pv[e] = s0 + e <= r ? round_tf32(__expf(fminf(gr - lds32f(sG + 4 * (s0 + e)), 0.f)) * x[4 * c4 + e])
+                    pv[e] = s0 + e <= r ? round_tf32(__expf(fminf(gr - lds32f(sG + 4 * (s0 + e)), 0.f)) * x[4 * c4 + e] *
+                                                     nqr * lds32f(sNk + 4 * (s0 + e)))
                                         : 0.f;
                 sts128f(sm_s + C_BU + hh * C_BU_KB + sw128_off32(r, 4 * c4), pv[0], pv[1], pv[2], pv[3]);
             }
@@ -459,6 +522,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     tma_prefetch_4d(&tq, 64 * kb, h, t0, b);
                     tma_prefetch_4d(&tk, 64 * kb, h, t0, b);
                     if (!zero_u) tma_prefetch_4d(&tv, 64 * kb, h, t0, b);
+                    if (zgate) tma_prefetch_4d(&tz, 64 * kb, h, t0, b);
                 }
                 bulk_prefetch_l2(tops(it), 16384);
             };
@@ -626,6 +690,9 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     cp_async4(dst + 64 + r, GATE == 1 ? (const void *)(a.log_alpha + tok) : (const void *)a.beta,
                               (GATE == 1 && valid) ? 4 : 0);
                 }
+                if (l2)   // the chunk's 128 row norms, 16 bytes per lane
+                    cp_async16(sNorm + (it & 1) * 128 + 4 * lane,
+                               a.norms + ((size_t)bh * a.NC + c_begin + it) * 128 + 4 * lane);
             }
             cp_async_commit();
         };
@@ -647,6 +714,13 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 bt[e] = __bfloat162float(__ushort_as_bfloat16(hb));
                 l[e] = __uint_as_float(gw[64 + r]);
             }
+            // the row norms of the fused L2 norm (1 otherwise), read before the set is refilled
+            float nq[2] = {1.f, 1.f}, nk[2] = {1.f, 1.f};
+            if (l2) {
+                const float *nv = sNorm + (it & 1) * 128;
+                nq[0] = nv[2 * lane]; nq[1] = nv[2 * lane + 1];
+                nk[0] = nv[64 + 2 * lane]; nk[1] = nv[64 + 2 * lane + 1];
+            }
             __syncwarp();
             issue_gate(it + 2);
             float p = l[0] + l[1];
@@ -660,16 +734,20 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const float gmid = __shfl_sync(0xffffffffu, g1, 15);
             const float gfirst = __shfl_sync(0xffffffffu, g0, 0);
             const int r = 2 * lane;
-            float *sG = vec(it, GV_G), *sGam = vec(it, GV_GAM), *sDel = vec(it, GV_DEL), *sBeta = vec(it, GV_BETA),
-                  *sE = vec(it, GV_E), *sF = vec(it, GV_F);
+            float *sG = vec(it, GV_G), *sGam = vec(it, GV_GAM), *sDel = vec(it, GV_DEL), *sGq = vec(it, GV_GQ),
+                  *sE = vec(it, GV_E), *sF = vec(it, GV_F), *sNq = vec(it, GV_NQ), *sNk = vec(it, GV_NK);
+            (void)bt;   // beta enters through the prep kernel's T operands only
             sG[r] = g0; sG[r + 1] = g1;
-            sBeta[r] = bt[0]; sBeta[r + 1] = bt[1];
-            sGam[r] = __expf(g0); sGam[r + 1] = __expf(g1);
-            sDel[r] = __expf(glast - g0); sDel[r + 1] = __expf(glast - g1);
+            sNq[r] = nq[0]; sNq[r + 1] = nq[1];
+            sNk[r] = nk[0]; sNk[r + 1] = nk[1];
+            const float G0 = __expf(g0), G1 = __expf(g1);
+            sGam[r] = G0; sGam[r + 1] = G1;
+            sGq[r] = G0 * nq[0]; sGq[r + 1] = G1 * nq[1];
+            sDel[r] = __expf(glast - g0) * nk[0]; sDel[r + 1] = __expf(glast - g1) * nk[1];
             const bool fac = gfirst - glast < kSpan;
             if (fac) {
-                sE[r] = __expf(g0 - gmid); sE[r + 1] = __expf(g1 - gmid);
-                sF[r] = __expf(gmid - g0); sF[r + 1] = __expf(gmid - g1);
+                sE[r] = __expf(g0 - gmid) * nq[0]; sE[r + 1] = __expf(g1 - gmid) * nq[1];
+                sF[r] = __expf(gmid - g0) * nk[0]; sF[r + 1] = __expf(gmid - g1) * nk[1];
             }
             if (lane == 0) fac_s[it & 1] = fac;
             mbar_arrive(&g_ready[it & 1]);
@@ -733,7 +811,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             // read as tf32) and G (Q S)^T in place of (Q S)^T
             if (!wait_bar(&d_done, par)) break;
             {
-                const uint32_t sGam = vec_s(it, GV_GAM);
+                const uint32_t sGam = vec_s(it, GV_GQ);
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
                     float ws[32], uu[32], qs[32];
@@ -794,6 +872,14 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             mbar_arrive(&w_ready);
             return true;
         };
+        // (thread 0 of these warps) chunk it's z tile into the z slot
+        int z_last = -1;
+        auto load_z = [&](int it) {
+            mbar_arrive_expect_tx(&z_full, 16384);
+            for (int kb = 0; kb < 2; ++kb)
+                tma_load_4d(sm + C_Z + kb * 8192, &tz, &z_full, 64 * kb, h, (c_begin + it) * 64, b);
+            z_last = it;
+        };
         // chunk it's output O^T (lane j = value channel, 64 tokens) -> staging -> TMA store
         auto emit = [&](int it) {
             float o[2][32];
@@ -805,6 +891,15 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             if (to_ == 0) bulk_wait_read_all();   // the previous store has read the staging
             named_sync(1, 128);
             const int j = row;
+            if (sizeof(Tout) == 2 && zgate) {   // out = o silu(z); z(r, j) from the z tile
+                if (!wait_bar(&z_full, it & 1)) return;
+                const uint32_t zt = sm_s + C_Z + (j >> 6) * 8192;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int r = 0; r < 32; ++r)
+                        o[hh][r] *= silu_tanh(__bfloat162float(__ushort_as_bfloat16(lds16(zt + sw128_off(32 * hh + r, j & 63)))));
+            }
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 if (sizeof(Tout) == 2) {
@@ -831,6 +926,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int kb = 0; kb < kOutBoxes; ++kb)
                     tma_store_4d(&to, sm + C_OUT + kb * 8192, cols * kb, h, t0, b);
                 bulk_commit();
+                if (sizeof(Tout) == 2 && zgate && it + 1 < n_it) load_z(it + 1);   // the z tile is read
             }
         };
         // Kt^T of channel blocks [ib0, ib0 + nib) (8 key channels each): ldmatrix.trans of the
@@ -862,6 +958,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
             }
         };
+        if (sizeof(Tout) == 2 && zgate && to_ == 0 && n_it > 0) load_z(0);
         bool ok = n_it > 0 && convert_w(0);
         for (int it = 0; ok && it < n_it; ++it) {
             const uint32_t par = it & 1;
@@ -891,7 +988,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             if (it + 1 < n_it && !convert_w(it + 1)) break;
         }
         if (outputs && n_it > 0 && !*abort_v && wait_bar(&u_done, (n_it - 1) & 1)) emit(n_it - 1);
-        if (to_ == 0) bulk_wait_all();   // the output stores' global writes
+        if (to_ == 0) {
+            bulk_wait_all();   // the output stores' global writes
+            if (z_last >= 0) wait_cycles(&z_full, (uint32_t)z_last & 1);   // (bounded) a z load in flight
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -900,25 +1000,29 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 }
 template <typename Tout, int GATE>
 int launch_chain(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
-                 const ChainArgs &ca, unsigned grid, cudaStream_t stream) {
+                 const CUtensorMap &mz, const ChainArgs &ca, unsigned grid, cudaStream_t stream) {
     const int smem = (int)C_TOTAL + 1024;
     if (cudaFuncSetAttribute(gdn_chain_kernel<Tout, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return kErrCuda;
-    gdn_chain_kernel<Tout, GATE><<<grid, kChainThreads, smem, stream>>>(mq, mk, mv, mo, ca);
+    gdn_chain_kernel<Tout, GATE><<<grid, kChainThreads, smem, stream>>>(mq, mk, mv, mo, mz, ca);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
 }  // namespace
 
 // Workspace of the two-kernel path: the segments' states [3][B*H][nseg][128][128] fp32 (when
-// few long chains are split), then the T operands [B*H][NC][16 KB].
+// few long chains are split), then the T operands [B*H][NC][16 KB], then the row norms of the
+// fused L2 norm [B*H][NC][128] fp32.
 size_t gdn_split_workspace_bytes(const ChunkProblem &p) {
     int nseg, len;
     tc_segment_split(p, &nseg, &len);
     const size_t seg = nseg > 1 ? (size_t)3 * p.B * p.H * nseg * 16384 * sizeof(float) : 0;
-    return seg + (size_t)p.B * p.H * p.NC * 16384;
+    return seg + (size_t)p.B * p.H * p.NC * (16384 + 512);
 }
+
+// The output gate's z tile takes the free half of the bf16 output staging.
+bool gdn_split_fuse_supported(const ChunkProblem &p) { return !(p.fuse & kFuseGate) || p.out_bf16; }
 
 int launch_gdn_split(const ChunkProblem &p, void *workspace, int *status_word, cudaStream_t stream) {
     int nseg, seg_len;
@@ -926,30 +1030,35 @@ int launch_gdn_split(const ChunkProblem &p, void *workspace, int *status_word, c
     const unsigned bh = (unsigned)(p.B * p.H);
     const size_t seg_bytes = nseg > 1 ? (size_t)3 * bh * nseg * 16384 * sizeof(float) : 0;
     unsigned char *tops = reinterpret_cast<unsigned char *>(workspace) + seg_bytes;
-    CUtensorMap mq, mk, mv, mo;
+    const unsigned nchunks = bh * (unsigned)p.NC;
+    float *norms = reinterpret_cast<float *>(tops + (size_t)nchunks * 16384);
+    const bool zgate = (p.fuse & kFuseGate) != 0;
+    CUtensorMap mq, mk, mv, mo, mz;
     if (!tc_make_map(&mq, p.q, p.B, p.T, p.H, false) || !tc_make_map(&mk, p.k, p.B, p.T, p.H, false) ||
         !tc_make_map(&mv, p.v, p.B, p.T, p.H, false) ||
-        !tc_make_map(&mo, p.out ? p.out : p.q, p.B, p.T, p.H, p.out ? !p.out_bf16 : false))
+        !tc_make_map(&mo, p.out ? p.out : p.q, p.B, p.T, p.H, p.out ? !p.out_bf16 : false) ||
+        !tc_make_map(&mz, zgate ? p.z : p.q, p.B, p.T, p.H, false))   // (unused unless gated)
         return kErrCuda;
-    {   // every chunk's T operands: persistent CTAs, four per SM
+    {   // every chunk's T operands: persistent CTAs, four per SM (three with the q tile)
         auto kern = p.gate == 1 ? gdn_prep_kernel<1> : gdn_prep_kernel<0>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PR_TOTAL + 1024) !=
+        const bool l2 = (p.fuse & kFuseL2) != 0;
+        const int smem = (int)(l2 ? PR_TOTAL_L2 : PR_TOTAL) + 1024;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PR_TOTAL_L2 + 1024) !=
             cudaSuccess)
             return kErrCuda;
-        const unsigned nchunks = bh * (unsigned)p.NC;
-        const unsigned grid = std::min<unsigned>(nchunks, 4u * 152u);
-        kern<<<grid, kPrepThreads, PR_TOTAL + 1024, stream>>>(mk, (const __nv_bfloat16 *)p.beta, p.log_alpha, tops,
-                                                       (int)p.T, (int)p.H, p.NC, nchunks, status_word);
+        const unsigned grid = std::min<unsigned>(nchunks, (l2 ? 3u : 4u) * 152u);
+        kern<<<grid, kPrepThreads, smem, stream>>>(mk, mq, (const __nv_bfloat16 *)p.beta, p.log_alpha, tops, norms,
+                                                   (int)p.T, (int)p.H, p.NC, nchunks, p.fuse, status_word);
         if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     }
     ChainArgs ca{p.log_alpha, (const __nv_bfloat16 *)p.beta, p.init_state, p.final_state, tops, status_word,
-                 (int)p.B, (int)p.T, (int)p.H, p.NC, 0, 1, p.NC, nullptr, nullptr, nullptr};
+                 (int)p.B, (int)p.T, (int)p.H, p.NC, 0, 1, p.NC, nullptr, nullptr, nullptr, p.fuse, norms};
     auto launch = [&](const ChainArgs &c, unsigned grid) {
         if (p.out_bf16)
-            return p.gate == 1 ? launch_chain<__nv_bfloat16, 1>(mq, mk, mv, mo, c, grid, stream)
-                               : launch_chain<__nv_bfloat16, 0>(mq, mk, mv, mo, c, grid, stream);
-        return p.gate == 1 ? launch_chain<float, 1>(mq, mk, mv, mo, c, grid, stream)
-                           : launch_chain<float, 0>(mq, mk, mv, mo, c, grid, stream);
+            return p.gate == 1 ? launch_chain<__nv_bfloat16, 1>(mq, mk, mv, mo, mz, c, grid, stream)
+                               : launch_chain<__nv_bfloat16, 0>(mq, mk, mv, mo, mz, c, grid, stream);
+        return p.gate == 1 ? launch_chain<float, 1>(mq, mk, mv, mo, mz, c, grid, stream)
+                           : launch_chain<float, 0>(mq, mk, mv, mo, mz, c, grid, stream);
     };
     if (nseg <= 1) return launch(ca, bh);
     // segments: end states (two runs per segment), chaining, then outputs

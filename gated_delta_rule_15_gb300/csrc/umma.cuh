@@ -35,6 +35,11 @@ __device__ __forceinline__ void sts64f(uint32_t a, float x, float y) {
 __device__ __forceinline__ void sts16(uint32_t a, uint16_t x) {
     asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(x) : "memory");
 }
+__device__ __forceinline__ uint16_t lds16(uint32_t a) {
+    uint16_t x;
+    asm volatile("ld.shared.b16 %0, [%1];" : "=h"(x) : "r"(a) : "memory");
+    return x;
+}
 __device__ __forceinline__ void sts32f(uint32_t a, float x) {
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(x) : "memory");
 }
@@ -173,6 +178,10 @@ __device__ __forceinline__ void bulk_wait_all() {
 __device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
                  ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes) : "memory");
+}
+// 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");

@@ -30,10 +30,12 @@ DR_OK, DR_ERR_INVALID, DR_ERR_UNSUPPORTED, DR_ERR_CUDA, DR_ERR_TIMEOUT, DR_ERR_W
     0, -1, -2, -3, -4, -5
 # fused neighbours (flags of dr_chunk_fwd_ex / dr_recurrent_step_ex)
 DR_FUSE_QK_L2NORM, DR_FUSE_BETA_SIGMOID, DR_FUSE_OUT_SILU_GATE = 1, 2, 4
+DR_FUSE_ALL = 7
 L2NORM_EPS = 1e-6   # DR_L2NORM_EPS
 
 # Symbols of include/dr.h (checked by tests/test_abi.py against the header).
-EXPORTED = ("dr_version", "dr_chunk_fwd_workspace_bytes", "dr_chunk_fwd_min_workspace_bytes", "dr_chunk_fwd",
+EXPORTED = ("dr_version", "dr_chunk_fwd_workspace_bytes", "dr_chunk_fwd_min_workspace_bytes",
+            "dr_chunk_fwd_ex_workspace_bytes", "dr_chunk_fwd",
             "dr_recurrent_step", "dr_get_device_status", "dr_strerror",
             "dr_chunk_fwd_noalloc", "dr_chunk_fwd_ex", "dr_recurrent_step_ex",
             "dr_chunk_bwd_workspace_bytes", "dr_chunk_bwd", "dr_selftest_bounded_wait",
@@ -63,6 +65,9 @@ _lib.dr_chunk_fwd_workspace_bytes.restype = ctypes.c_int
 _lib.dr_chunk_fwd_min_workspace_bytes.argtypes = [ctypes.POINTER(ChunkDesc),
                                                   ctypes.POINTER(ctypes.c_size_t)]
 _lib.dr_chunk_fwd_min_workspace_bytes.restype = ctypes.c_int
+_lib.dr_chunk_fwd_ex_workspace_bytes.argtypes = [ctypes.POINTER(ChunkDesc), ctypes.c_uint32,
+                                                 ctypes.POINTER(ctypes.c_size_t)]
+_lib.dr_chunk_fwd_ex_workspace_bytes.restype = ctypes.c_int
 _lib.dr_chunk_fwd.argtypes = [ctypes.POINTER(ChunkDesc), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                               _vp, _vp, ctypes.c_size_t, _vp]
 _lib.dr_chunk_fwd.restype = ctypes.c_int
@@ -172,6 +177,14 @@ def min_workspace_bytes(desc: ChunkDesc) -> int:
     return n.value
 
 
+def ex_workspace_bytes(desc: ChunkDesc, fuse: int) -> int:
+    n = ctypes.c_size_t(0)
+    rc = _lib.dr_chunk_fwd_ex_workspace_bytes(ctypes.byref(desc), fuse, ctypes.byref(n))
+    if rc != DR_OK:
+        raise DrError(rc, "dr_chunk_fwd_ex_workspace_bytes")
+    return n.value
+
+
 def chunk_fwd(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
               out_dtype=None, return_final_state: bool = True, out=None,
               final_state=None, workspace=None, stream=None, qk_l2norm: bool = False,
@@ -209,8 +222,7 @@ def chunk_fwd(q, k, v, log_alpha, beta, init_state=None, *, chunk: int = 64,
         out = torch.empty((B, T, H, dv), dtype=_TORCH_DT[odt], device=q.device)
     if final_state is None and return_final_state:
         final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
-    # the fused neighbours run on paths that need only the least workspace
-    need = min_workspace_bytes(desc) if fuse else workspace_bytes(desc)
+    need = ex_workspace_bytes(desc, fuse) if fuse else workspace_bytes(desc)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

@@ -114,9 +114,10 @@ int dr_version(void);
    states (the segment's transition dk x dk, its end state from a zero start, its start
    state).  Besides those:
      - bf16 inputs, dk = dv = 128, chunk 64, scalar or no gate: nothing for many chains; for
-       chains split into segments, also 16 KB per (b, h, chunk): every chunk's
+       chains split into segments, also 16.5 KB per (b, h, chunk): every chunk's
        triangular-solve operands (T = (I + A)^-1 of the WY form, page "Transformer notes
-       (5): linear attention optimisations", KDA paragraph), formed for all chunks at once;
+       (5): linear attention optimisations", KDA paragraph), formed for all chunks at once,
+       and the row norms of the fused L2 norm;
      - the same with the per-channel gate: 131,584 bytes of tensor-core operands per
        (b, h, chunk);
      - every other configuration (the CUDA-core path): the fp32 operands W, Q*G, K*G_C/G
@@ -181,10 +182,20 @@ int dr_chunk_fwd_host(const dr_chunk_desc *desc, int pieces,
  * dr_chunk_fwd with fused neighbours: `fuse` is an OR of DR_FUSE_* (0 makes the call
  * identical to dr_chunk_fwd); `z` is the output gate's input, [B, T, H, dv] in_dtype, read
  * only, required (non-NULL, 16-byte aligned, not overlapping `out`) when DR_FUSE_OUT_SILU_GATE
- * is set and ignored otherwise.  Every configuration dr_chunk_fwd accepts takes every flag; the workspace size
- * does not depend on them.  Returns the statuses of dr_chunk_fwd; DR_ERR_INVALID also for
- * bits outside DR_FUSE_ALL or a missing z.
+ * is set and ignored otherwise.  Every configuration dr_chunk_fwd accepts takes every flag.
+ * The least workspace is dr_chunk_fwd_min_workspace_bytes() whatever the flags; the fastest
+ * path with flags set may take more, dr_chunk_fwd_ex_workspace_bytes().  Returns the
+ * statuses of dr_chunk_fwd; DR_ERR_INVALID also for bits outside DR_FUSE_ALL or a missing z.
  */
+/* Bytes of device workspace dr_chunk_fwd_ex takes for *desc and the flags `fuse` on its
+   fastest path; written to *bytes.  With fuse = 0, dr_chunk_fwd_workspace_bytes().  For bf16
+   inputs, dk = dv = 128, chunk 64 and a scalar or no gate, with any flag set (and bf16
+   outputs when the output gate is fused): the two-kernel path's 16 KB of triangular-solve
+   operands plus 512 bytes of row norms per (b, h, chunk), and the segments' states when few
+   long chains are split.  Returns DR_OK, DR_ERR_INVALID (also for bits outside DR_FUSE_ALL)
+   or DR_ERR_UNSUPPORTED. */
+int dr_chunk_fwd_ex_workspace_bytes(const dr_chunk_desc *desc, uint32_t fuse, size_t *bytes);
+
 int dr_chunk_fwd_ex(const dr_chunk_desc *desc, uint32_t fuse,
                     const void *q, const void *k, const void *v,
                     const float *log_alpha, const void *beta, const void *z,

@@ -59,9 +59,23 @@ def test_workspace_query(dr):
     # the tensor-core path (bf16, d = 128, C = 64, scalar gate) with many short chains: none
     assert dr.workspace_bytes(_desc(dr, gate=dr.DR_GATE_SCALAR)) == 0
     assert dr.min_workspace_bytes(_desc(dr, gate=dr.DR_GATE_SCALAR)) == 0
-    # few long chains (segments): the fastest path also holds 16 KB of T operands per chunk
+    # few long chains (segments): the fastest path also holds 16 KB of T operands and 512 B
+    # of row norms per chunk
     long = _desc(dr, B=1, T=64 * 64, H=2, gate=dr.DR_GATE_SCALAR)
-    assert dr.workspace_bytes(long) == dr.min_workspace_bytes(long) + 2 * 64 * 16384
+    assert dr.workspace_bytes(long) == dr.min_workspace_bytes(long) + 2 * 64 * (16384 + 512)
+    # the fused neighbours' fastest path (two kernels) takes them for many chains too; a fused
+    # output gate with fp32 outputs stays on the single kernel
+    many = _desc(dr, gate=dr.DR_GATE_SCALAR)
+    assert dr.ex_workspace_bytes(many, 0) == 0
+    for fl in (dr.DR_FUSE_QK_L2NORM, dr.DR_FUSE_BETA_SIGMOID, dr.DR_FUSE_OUT_SILU_GATE, 7):
+        assert dr.ex_workspace_bytes(many, fl) == 2 * 3 * 2 * (16384 + 512)
+    f32out = _desc(dr, gate=dr.DR_GATE_SCALAR, out_dtype=dr.DR_F32)
+    assert dr.ex_workspace_bytes(f32out, dr.DR_FUSE_OUT_SILU_GATE) == 0
+    assert dr.ex_workspace_bytes(f32out, dr.DR_FUSE_QK_L2NORM) == 2 * 3 * 2 * (16384 + 512)
+    for d in (_desc(dr), _desc(dr, in_dtype=dr.DR_F32)):   # other paths: the plain answer
+        assert dr.ex_workspace_bytes(d, 7) == dr.workspace_bytes(d)
+    with pytest.raises(dr.DrError):
+        dr.ex_workspace_bytes(many, 8)
     assert dr.workspace_bytes(_desc(dr, gate=dr.DR_GATE_SCALAR, in_dtype=dr.DR_F32)) > 0
     for d in (_desc(dr), _desc(dr, in_dtype=dr.DR_F32), _desc(dr, T=0)):   # other paths: equal
         assert dr.min_workspace_bytes(d) == dr.workspace_bytes(d)

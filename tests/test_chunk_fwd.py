@@ -203,11 +203,12 @@ def test_tc_workspace_sizes(dr):
     desc = dr.chunk_desc(8, 4096, 16, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_SCALAR, 64)
     assert dr.workspace_bytes(desc) == 0 and dr.min_workspace_bytes(desc) == 0
     # few long chains: three segment-state slabs of 64 KB per (b, h, segment), plus, on the
-    # fastest path, one 16 KB T-operand image per (b, h, chunk): 9 segments of 114 chunks
+    # fastest path, one 16 KB T-operand image and 512 B of row norms per (b, h, chunk): 9
+    # segments of 114 chunks
     desc = dr.chunk_desc(1, 65536, 16, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_SCALAR, 64)
     seg = 3 * 16 * 9 * 65536
     assert dr.min_workspace_bytes(desc) == seg
-    assert dr.workspace_bytes(desc) == seg + 16 * 1024 * 16384
+    assert dr.workspace_bytes(desc) == seg + 16 * 1024 * (16384 + 512)
 
 
 @pytest.mark.parametrize("gate", ["none", "scalar"])

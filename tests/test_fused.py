@@ -80,6 +80,29 @@ def test_tensor_core_paths(dr, gate, flags):
 
 
 @pytest.mark.parametrize("flags", FLAGS, ids=FLAG_IDS)
+@pytest.mark.parametrize("gate", ["none", "scalar"])
+def test_tensor_core_single_kernel(dr, gate, flags):
+    """The scalar / no-gate configurations run the fused neighbours on the two-kernel path
+    when the workspace holds its operands (dr_chunk_fwd_ex_workspace_bytes), and on the
+    single kernel otherwise: that path too, with the least workspace."""
+    d = problem(2, 200, 3, 128, 128, flags, gate=gate, dtype="bf16", init_state=True, seed=22)
+    desc = dr.chunk_desc(2, 200, 3, 128, 128, dr.DR_BF16, dr.DR_BF16, inputs.GATE_CODE[gate], 64)
+    fl = dr.fuse_flags(*flags[:2], flags[2] or None)
+    assert dr.min_workspace_bytes(desc) == 0 and dr.ex_workspace_bytes(desc, fl) > 0
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    check(dr, d, flags, "bf16", workspace=ws)
+
+
+@pytest.mark.parametrize("la_range", [(0.001, 0.1), (0.0, 3.0)])
+def test_two_kernel_path_decay_forms_all_flags(dr, la_range):
+    """The two-kernel path folds the row norms into the decay factors of P: around the
+    chunk's middle token for spans up to 80 (log space), per pair beyond."""
+    d = problem(2, 190, 2, 128, 128, FLAGS[-1], gate="scalar", dtype="bf16", init_state=True,
+                seed=23, log_alpha_range=la_range)
+    check(dr, d, FLAGS[-1], "bf16", out_dtype=torch.float32)
+
+
+@pytest.mark.parametrize("flags", FLAGS, ids=FLAG_IDS)
 @pytest.mark.parametrize("dtype,dk,dv,chunk", [("f32", 128, 128, 64), ("f32", 64, 64, 32),
                                                ("bf16", 64, 128, 64), ("bf16", 128, 128, 16)])
 def test_cuda_core_path(dr, flags, dtype, dk, dv, chunk):
@@ -102,12 +125,18 @@ def test_fp32_output(dr, gate):
     check(dr, d, FLAGS[-1], "bf16", out_dtype=torch.float32)
 
 
-def test_segment_parallel_all_flags(dr):
+@pytest.mark.parametrize("least", [False, True])
+def test_segment_parallel_all_flags(dr, least):
     # two chains of 64 chunks: split into segments whose end states are chained; the
     # normalisation and sigmoid enter the segment transitions, the gate only the outputs
+    # (the two-kernel path, or with the least workspace the single kernel)
     d = problem(1, 4096, 2, 128, 128, FLAGS[-1], gate="scalar", dtype="bf16", init_state=True,
                 seed=12)
-    check(dr, d, FLAGS[-1], "bf16")
+    kw = {}
+    if least:
+        desc = dr.chunk_desc(1, 4096, 2, 128, 128, dr.DR_BF16, dr.DR_BF16, dr.DR_GATE_SCALAR, 64)
+        kw["workspace"] = torch.empty(dr.min_workspace_bytes(desc), dtype=torch.uint8, device="cuda")
+    check(dr, d, FLAGS[-1], "bf16", **kw)
 
 
 def test_strong_decay_all_flags(dr):
