@@ -74,21 +74,21 @@ constexpr float kSpan = 80.f;
 // past T are zero rows of K (the TMA fill) with beta = 0, T being the identity there, as the
 // chain kernel's loads make them.
 // Fused neighbours (DR_FUSE_* of include/dr.h): beta = sigmoid(logit) rounded to beta's bf16;
-// with the L2 norm the q tile arrives too, each thread takes 1 / |x| of one row of [Q; K]
+// with the L2 norm the q tile arrives too (over A's buffer, free until the A build), each
+// thread takes 1 / |x| of one row of [Q; K]
 // (written to the workspace's norm vectors for the chain kernel), A takes the normalised
 // rows' products n_r n_s (k_r . k_s), and the second operand becomes T diag(beta G n), so
 // that W = T diag(beta G) diag(n) K is formed from the raw k tile.
 constexpr int kPrepThreads = 128;
 constexpr uint32_t PR_K = 0;                       // k tile (two 64-channel halves, swizzled);
                                                    // then the fp32 T (swizzled)
-constexpr uint32_t PR_A = 16384;                   // fp32 A (a_index)
+constexpr uint32_t PR_A = 16384;                   // (fused L2 norm) the q tile, until the norms;
+                                                   // then fp32 A (a_index)
 constexpr uint32_t PR_TB = PR_A + 16384;           // the operand image
 constexpr uint32_t PR_M = PR_TB + 16384;           // solve scratch
 constexpr uint32_t PR_V = PR_M + 4096;             // g, G, beta, exp(g - g_31), exp(g_31 - g),
                                                    // 1/|q|, 1/|k|, G/|k|
 constexpr uint32_t PR_TOTAL = PR_V + 8 * 256;
-constexpr uint32_t PR_Q = (PR_TOTAL + 1023) / 1024 * 1024;   // q tile (fused L2 norm only)
-constexpr uint32_t PR_TOTAL_L2 = PR_Q + 16384;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -138,7 +138,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ 
             mbar_arrive_expect_tx(&bar_k, l2 ? 32768 : 16384);
             for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + PR_K + kb * 8192, &tk, &bar_k, 64 * kb, h, t0, b);
             if (l2)
-                for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + PR_Q + kb * 8192, &tq, &bar_k, 64 * kb, h, t0, b);
+                for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + PR_A + kb * 8192, &tq, &bar_k, 64 * kb, h, t0, b);
             const unsigned nn = n + gridDim.x;
             if (nn < nchunks) {
                 int h2, b2, t2;
@@ -200,7 +200,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ 
         __syncthreads();
         if (abort_s) break;
         if (l2) {   // 1 / |x| of row tid of [Q; K] (zero rows past T give 1 / sqrt(eps), unused)
-            const unsigned char *src = sm + (tid < 64 ? PR_Q : PR_K) + (tid & 63) * 128;
+            const unsigned char *src = sm + (tid < 64 ? PR_A : PR_K) + (tid & 63) * 128;
             float ss = 0.f;
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb)
@@ -1039,14 +1039,12 @@ int launch_gdn_split(const ChunkProblem &p, void *workspace, int *status_word, c
         !tc_make_map(&mo, p.out ? p.out : p.q, p.B, p.T, p.H, p.out ? !p.out_bf16 : false) ||
         !tc_make_map(&mz, zgate ? p.z : p.q, p.B, p.T, p.H, false))   // (unused unless gated)
         return kErrCuda;
-    {   // every chunk's T operands: persistent CTAs, four per SM (three with the q tile)
+    {   // every chunk's T operands: persistent CTAs, four per SM
         auto kern = p.gate == 1 ? gdn_prep_kernel<1> : gdn_prep_kernel<0>;
-        const bool l2 = (p.fuse & kFuseL2) != 0;
-        const int smem = (int)(l2 ? PR_TOTAL_L2 : PR_TOTAL) + 1024;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PR_TOTAL_L2 + 1024) !=
-            cudaSuccess)
+        const int smem = (int)PR_TOTAL + 1024;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return kErrCuda;
-        const unsigned grid = std::min<unsigned>(nchunks, (l2 ? 3u : 4u) * 152u);
+        const unsigned grid = std::min<unsigned>(nchunks, 4u * 152u);
         kern<<<grid, kPrepThreads, smem, stream>>>(mk, mq, (const __nv_bfloat16 *)p.beta, p.log_alpha, tops, norms,
                                                    (int)p.T, (int)p.H, p.NC, nchunks, p.fuse, status_word);
         if (cudaGetLastError() != cudaSuccess) return kErrCuda;
