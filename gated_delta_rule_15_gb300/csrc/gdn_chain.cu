@@ -133,8 +133,6 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ 
         int h, b, t0;
         coords(n, h, b, t0);
         if (tid == 0) {
-            // the previous chunk's image must have been read out before the solve rewrites it
-            bulk_wait_read_all();
             mbar_arrive_expect_tx(&bar_k, l2 ? 32768 : 16384);
             for (int kb = 0; kb < 2; ++kb) tma_load_4d(sm + PR_K + kb * 8192, &tk, &bar_k, 64 * kb, h, t0, b);
             if (l2)
@@ -266,6 +264,8 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ 
                     }
             }
         }
+        // the previous chunk's image has been read out by its store before the solve rewrites it
+        if (tid == 0) bulk_wait_read_all();
         __syncthreads();   // the k tile is dead: T goes over it
 
         const SolveOut<true, true, true> out{reinterpret_cast<float *>(sm + PR_K), sm + PR_TB, sBeta,
