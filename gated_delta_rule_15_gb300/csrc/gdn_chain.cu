@@ -327,7 +327,6 @@ constexpr uint32_t ID_UPD_S = idesc_tf32(128, 128);
 
 struct ChainArgs {
     const float *log_alpha;
-    const __nv_bfloat16 *beta;
     const float *init_state;
     float *final_state;
     const unsigned char *tops;   // [B*H][NC][16384]: T diag(beta) | T diag(beta G) per chunk
@@ -411,7 +410,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     const uint32_t sm_s = smem_u32(sm);                      // the same bytes by shared address
     auto vec_s = [&](int it, int k) { return sm_s + C_SMALL + 4u * ((it & 1) * kGvSet + 64 * k); };
     auto vec = [&](int it, int k) { return sVec + (it & 1) * kGvSet + 64 * k; };
-    uint32_t *sGate = reinterpret_cast<uint32_t *>(sm + C_GATE);   // [2][beta word | log alpha][64]
+    uint32_t *sGate = reinterpret_cast<uint32_t *>(sm + C_GATE);   // [2][(unused) | log alpha][64]
     float *sNorm = reinterpret_cast<float *>(sm + C_NORM);         // [2][1/|q| | 1/|k|][64]
     const bool l2 = (a.fuse & kFuseL2) != 0;
     const bool zgate = (a.fuse & kFuseGate) != 0 && outputs;
@@ -669,27 +668,20 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
         __syncwarp();
     } else if (warp == kWarpGate) {
-        // ---------------- gates: raw beta / log alpha two chunks ahead (cp.async), the scan of
-        // chunk it into set it % 2 once the chunk two back has been consumed
-        const size_t ntok = (size_t)a.B * a.T * a.H;
+        // ---------------- gates: log alpha two chunks ahead (cp.async; beta enters through the
+        // prep kernel's T operands only), the scan of chunk it into set it % 2 once the chunk
+        // two back has been consumed
         auto issue_gate = [&](int it) {
             if (it < n_it) {
                 uint32_t *dst = sGate + (it & 1) * 128;
+                if (GATE == 1)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int r = 2 * lane + e, t = (c_begin + it) * 64 + r;
-                    const bool valid = t < a.T;
-                    const size_t tok = valid ? ((size_t)b * a.T + t) * a.H + h : 0;
-                    if (valid && tok + 1 == ntok && ((2 * tok) & 3) == 0) {
-                        // the 32-bit word would run past the end of beta: load this value alone
-                        dst[r] = (uint32_t)__bfloat16_as_ushort(a.beta[tok]);
-                    } else {
-                        cp_async4(dst + r, reinterpret_cast<const char *>(a.beta) + ((2 * tok) & ~(size_t)3),
-                                  valid ? 4 : 0);
+                    for (int e = 0; e < 2; ++e) {
+                        const int r = 2 * lane + e, t = (c_begin + it) * 64 + r;
+                        const bool valid = t < a.T;
+                        const size_t tok = valid ? ((size_t)b * a.T + t) * a.H + h : 0;
+                        cp_async4(dst + 64 + r, a.log_alpha + tok, valid ? 4 : 0);   // zeros past T
                     }
-                    cp_async4(dst + 64 + r, GATE == 1 ? (const void *)(a.log_alpha + tok) : (const void *)a.beta,
-                              (GATE == 1 && valid) ? 4 : 0);
-                }
                 if (l2)   // the chunk's 128 row norms, 16 bytes per lane
                     cp_async16(sNorm + (it & 1) * 128 + 4 * lane,
                                a.norms + ((size_t)bh * a.NC + c_begin + it) * 128 + 4 * lane);
@@ -703,16 +695,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             cp_async_wait_group1();
             __syncwarp();
             const uint32_t *gw = sGate + (it & 1) * 128;
-            const int t0 = (c_begin + it) * 64;
-            float l[2], bt[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int r = 2 * lane + e, t = t0 + r;
-                const size_t tok = t < a.T ? ((size_t)b * a.T + t) * a.H + h : 0;
-                const uint32_t wd = gw[r];
-                const uint16_t hb = (uint16_t)(((2 * tok) & 2) ? (wd >> 16) : (wd & 0xffffu));
-                bt[e] = __bfloat162float(__ushort_as_bfloat16(hb));
-                l[e] = __uint_as_float(gw[64 + r]);
+            float l[2] = {0.f, 0.f};
+            if (GATE == 1) {
+                l[0] = __uint_as_float(gw[64 + 2 * lane]);
+                l[1] = __uint_as_float(gw[64 + 2 * lane + 1]);
             }
             // the row norms of the fused L2 norm (1 otherwise), read before the set is refilled
             float nq[2] = {1.f, 1.f}, nk[2] = {1.f, 1.f};
@@ -736,7 +722,6 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const int r = 2 * lane;
             float *sG = vec(it, GV_G), *sGam = vec(it, GV_GAM), *sDel = vec(it, GV_DEL), *sGq = vec(it, GV_GQ),
                   *sE = vec(it, GV_E), *sF = vec(it, GV_F), *sNq = vec(it, GV_NQ), *sNk = vec(it, GV_NK);
-            (void)bt;   // beta enters through the prep kernel's T operands only
             sG[r] = g0; sG[r + 1] = g1;
             sNq[r] = nq[0]; sNq[r + 1] = nq[1];
             sNk[r] = nk[0]; sNk[r + 1] = nk[1];
@@ -1049,7 +1034,7 @@ int launch_gdn_split(const ChunkProblem &p, void *workspace, int *status_word, c
                                                    (int)p.T, (int)p.H, p.NC, nchunks, p.fuse, status_word);
         if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     }
-    ChainArgs ca{p.log_alpha, (const __nv_bfloat16 *)p.beta, p.init_state, p.final_state, tops, status_word,
+    ChainArgs ca{p.log_alpha, p.init_state, p.final_state, tops, status_word,
                  (int)p.B, (int)p.T, (int)p.H, p.NC, 0, 1, p.NC, nullptr, nullptr, nullptr, p.fuse, norms};
     auto launch = [&](const ChainArgs &c, unsigned grid) {
         if (p.out_bf16)
