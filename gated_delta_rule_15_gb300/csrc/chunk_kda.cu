@@ -972,9 +972,7 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
             if (!wait_cycles(&bar_k, par)) fail();
             if (outputs && !wait_cycles(&bar_p[par], (c >> 1) & 1)) fail();
             tc_fence_after();
-            const uint32_t pb = S2_P + par * 16384;
-            const uint32_t ea[3] = {S2_EH, S2_EH, S2_EL}, kbuf[3] = {S2_KH, S2_KL, S2_KH},
-                           pbuf[3] = {pb, pb + 8192, pb};
+            const uint32_t ea[3] = {S2_EH, S2_EH, S2_EL}, kbuf[3] = {S2_KH, S2_KL, S2_KH};
 #pragma unroll
             for (int part = 0; part < 3; ++part)
 #pragma unroll
@@ -982,20 +980,27 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
                     mma_bf16(tmb + S2_TM_S, desc_add(dK0, ea[part] + ks * 32),
                              desc_add(dM0, kbuf[part] + ks * 2048), ID_KM_N128, 1);
             mma_commit(&bar_s);
-            if (outputs) {
-                const uint32_t pe = tmb + S2_TM_D + S2_TM_DSTRIDE * par + 64;   // onto (QH S)^T
-#pragma unroll
-                for (int part = 0; part < 3; ++part)
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(pe, desc_add(dK0, ea[part] + ks * 32),
-                                 desc_add(dK0, pbuf[part] + ks * 32), ID_KK_N64, 1);
-                mma_commit(&bar_pe);
-            }
         }
 
         // ---- 6. output of chunk c - 1 (ST is free: this chunk's D product has completed)
         if (outputs && c >= 1) emit(c - 1);
+
+        // ---- 6b. E^T P^T -> PE[c % 2] [bar_pe], after the output: issuing blocks the issuing
+        //          thread while the pipe drains the state update, which would hold the
+        //          output's barriers
+        if (tid == 0 && outputs) {
+            tc_fence_after();
+            const uint32_t pb = S2_P + par * 16384;
+            const uint32_t ea[3] = {S2_EH, S2_EH, S2_EL}, pbuf[3] = {pb, pb + 8192, pb};
+            const uint32_t pe = tmb + S2_TM_D + S2_TM_DSTRIDE * par + 64;   // onto (QH S)^T
+#pragma unroll
+            for (int part = 0; part < 3; ++part)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(pe, desc_add(dK0, ea[part] + ks * 32),
+                             desc_add(dK0, pbuf[part] + ks * 32), ID_KK_N64, 1);
+            mma_commit(&bar_pe);
+        }
 
         // ---- 7. state update done; K buffer is free
         wait_bar(&bar_s, par);
