@@ -13,7 +13,8 @@
 //
 // kda_prep_kernel (one CTA per (b, h, chunk), all chunks in parallel) computes everything
 // that does not depend on S and stores it, ready for the tensor core, in the workspace:
-// W (bf16), U (fp32), P, Q*G and K*G_C/G (bf16 high/low pairs) and G_C.  The exponentials
+// W (bf16), U (fp32), Q*G (a bf16 high/low pair), P and (K*G_C/G)^T (TF32-rounded fp32, the
+// B operands of two kind::tf32 products) and G_C.  The exponentials
 // inside A and P are split per 16-token block j of the column index s, against the
 // reference g_ref = g at the block's last token: exp(g_ref - g_s) <= 1 for s in the block and
 // exp(g_r - g_ref) <= 1 for every row r below it, so the off-diagonal blocks take no factor
@@ -25,9 +26,10 @@
 // N = 16) on high/low bf16 pairs.
 //
 // kda_state_kernel (one CTA per (b, h), chunks in sequence) keeps S^T in TMEM and, per
-// chunk, TMA-loads the stored operands: D = S^T [W; Q*G]^T, E^T = U^T - (W S)^T,
-// S^T <- S^T Diag(G_C) + E^T (K*G_C/G), O^T = (Q*G S)^T + E^T P^T, with the operand
-// buffers of the next chunk refilled as soon as each is consumed.
+// chunk, TMA-loads the stored operands: D = S^T [W; Q*G]^T, E^T = U^T - (W S)^T (fp32 in
+// TMEM, the A operand of the next two products), S^T <- S^T Diag(G_C) + E^T (K*G_C/G) and
+// O^T = (Q*G S)^T + E^T P^T as kind::tf32 products, with the operand buffers of the next
+// chunk refilled as soon as each is consumed.
 //
 // Fused neighbours (DR_FUSE_* of include/dr.h; page "linear-attention gated-deltanet
 // guide", section 4): the prep kernel computes 1 / |q_r| and 1 / |k_r| from the bf16 tiles
@@ -53,10 +55,11 @@ using namespace tc;
 constexpr int kThreads = 256;
 
 // ---------------------------------------------------------------- workspace (per chunk n)
-// W [64][128] bf16, U [64][128] fp32, PH/PL [64][64] bf16, QH/QL/KH/KL [64][128] bf16, GAM [128]
+// W [64][128] bf16, U [64][128] fp32, P [64][64] fp32 (TF32-rounded), QH/QL [64][128] bf16,
+// KT = (K*G_C/G)^T [128][64] fp32 (TF32-rounded), GAM [128]
 struct KdaWorkspace {
-    __nv_bfloat16 *W, *PH, *PL, *QH, *QL, *KH, *KL;
-    float *U, *GAM;
+    __nv_bfloat16 *W, *QH, *QL;
+    float *U, *P, *KT, *GAM;
 };
 constexpr size_t kKdaBytesPerChunk = 16384 + 32768 + 2 * 8192 + 4 * 16384 + 512;
 
@@ -65,12 +68,10 @@ KdaWorkspace kda_carve(void *base, int64_t nch) {
     KdaWorkspace w;
     w.W = (__nv_bfloat16 *)p;   p += nch * 16384;
     w.U = (float *)p;           p += nch * 32768;
-    w.PH = (__nv_bfloat16 *)p;  p += nch * 8192;
-    w.PL = (__nv_bfloat16 *)p;  p += nch * 8192;
+    w.P = (float *)p;           p += nch * 16384;
     w.QH = (__nv_bfloat16 *)p;  p += nch * 16384;
     w.QL = (__nv_bfloat16 *)p;  p += nch * 16384;
-    w.KH = (__nv_bfloat16 *)p;  p += nch * 16384;
-    w.KL = (__nv_bfloat16 *)p;  p += nch * 16384;
+    w.KT = (float *)p;          p += nch * 32768;
     w.GAM = (float *)p;
     return w;
 }
@@ -316,17 +317,20 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                         *reinterpret_cast<uint4 *>(a.ws.QH + go + 32 * p + 8 * i) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
                         *reinterpret_cast<uint4 *>(a.ws.QL + go + 32 * p + 8 * i) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
                     } else {
+                        float kt[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) kt[u] = x8[u] * ex2(gl[u] - g8[u]);
 #pragma unroll
                         for (int u = 0; u < 8; u += 2) {
                             kg_keep[w + (u >> 1)] = pack_bf16(e8[u] * sGamC[c + u], e8[u + 1] * sGamC[c + u + 1]);
-                            pack_hi_lo(x8[u] * ex2(gl[u] - g8[u]), x8[u + 1] * ex2(gl[u + 1] - g8[u + 1]),
-                                       oh[u >> 1], ol[u >> 1]);
+                            pack_hi_lo(kt[u], kt[u + 1], oh[u >> 1], ol[u >> 1]);
                         }
                         const uint32_t so = (c >> 6) * 16384 + sw128_off(t_row, c & 63);
                         *reinterpret_cast<uint4 *>(sm + P1_R1 + so) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
                         *reinterpret_cast<uint4 *>(sm + P1_R1 + 8192 + so) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
-                        *reinterpret_cast<uint4 *>(a.ws.KH + go + 32 * p + 8 * i) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
-                        *reinterpret_cast<uint4 *>(a.ws.KL + go + 32 * p + 8 * i) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+                        // row c + u of K*G_C/G transposed (a warp's 32 tokens: 128 contiguous bytes)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) a.ws.KT[(n * 128 + c + u) * 64 + t_row] = round_tf32(kt[u]);
                     }
                 }
                 tmem_st16u(tm + P1_TM_LH + 32 * half + 16 * p, hi);
@@ -394,17 +398,14 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 } else {
                     float gl[8];
                     load8_g(LA, 63, c, gl);
-                    uint32_t kg[4], hi[4], lo[4];
+                    uint32_t kg[4];
     #pragma unroll
-                    for (int u = 0; u < 8; u += 2) {
-                        kg[u >> 1] = pack_bf16(e8[u], e8[u + 1]);
-                        pack_hi_lo(x8[u] * ex2(gl[u] - g8[u]), x8[u + 1] * ex2(gl[u + 1] - g8[u + 1]),
-                                   hi[u >> 1], lo[u >> 1]);
-                    }
+                    for (int u = 0; u < 8; u += 2) kg[u >> 1] = pack_bf16(e8[u], e8[u + 1]);
                     *reinterpret_cast<uint4 *>(sm + P1_KG + (c >> 6) * 8192 + sw128_off(t_row, c & 63)) =
                         make_uint4(kg[0], kg[1], kg[2], kg[3]);
-                    *reinterpret_cast<uint4 *>(a.ws.KH + go + 8 * i) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4 *>(a.ws.KL + go + 8 * i) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        a.ws.KT[(n * 128 + c + u) * 64 + t_row] = round_tf32(x8[u] * ex2(gl[u] - g8[u]));
                 }
             }
         }
@@ -522,7 +523,7 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     }
     __syncthreads();   // Q, K and g are dead from here on
 
-    // ---- P (rows 0..63 of X) to the workspace as a bf16 pair; A (rows 64..127) in fp32
+    // ---- P (rows 0..63 of X) to the workspace, TF32-rounded; A (rows 64..127) in fp32
     {
         float x[32];
         tmem_ld32(tm + P1_TM_X + 32 * half, x);
@@ -541,18 +542,15 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             for (int u = 0; u < 32; ++u)
                 if (((c0 + u) >> 4) == (r >> 4)) x[u] = Xd[part * 1024 + r * 16 + ((c0 + u) & 15)];
         }
-        if (quarter < 2) {
+        if (quarter < 2) {   // P row r, TF32-rounded, zero above the diagonal
             const int r = row;
-            uint32_t ph[16], pl[16];
+            float4 *dp = reinterpret_cast<float4 *>(a.ws.P + (n * 64 + r) * 64 + c0);
 #pragma unroll
-            for (int u = 0; u < 32; u += 2)
-                pack_hi_lo(c0 + u <= r ? x[u] : 0.f, c0 + u + 1 <= r ? x[u + 1] : 0.f, ph[u >> 1], pl[u >> 1]);
-            uint4 *dh = reinterpret_cast<uint4 *>(a.ws.PH + (n * 64 + r) * 64 + c0);
-            uint4 *dl = reinterpret_cast<uint4 *>(a.ws.PL + (n * 64 + r) * 64 + c0);
+            for (int q4 = 0; q4 < 8; ++q4) {
+                float v[4];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                dh[q4] = make_uint4(ph[4 * q4], ph[4 * q4 + 1], ph[4 * q4 + 2], ph[4 * q4 + 3]);
-                dl[q4] = make_uint4(pl[4 * q4], pl[4 * q4 + 1], pl[4 * q4 + 2], pl[4 * q4 + 3]);
+                for (int e = 0; e < 4; ++e) v[e] = c0 + 4 * q4 + e <= r ? round_tf32(x[4 * q4 + e]) : 0.f;
+                dp[q4] = make_float4(v[0], v[1], v[2], v[3]);
             }
         } else {
             const int r = row - 64;
@@ -631,21 +629,21 @@ done:
 // [W; Q*G high; Q*G low] as one 192-row K-major B operand: per K-block of 64 channels
 // [W (8 KB) | QH (8 KB) | QL (8 KB)], the two K-blocks 24 KB apart
 constexpr uint32_t S2_WQ = 0, S2_WQ_KB = 24576;
-constexpr uint32_t S2_KH = 49152, S2_KL = 65536;             // MN-major [64 tok][128 ch]
-constexpr uint32_t S2_P = 81920;                             // 2 buffers of [P high | P low]
+constexpr uint32_t S2_KT = 49152;   // (K*G_C/G)^T, tf32 K-major: [2 token blocks][128 ch][32 tok]
+constexpr uint32_t S2_P = 81920;    // 2 buffers of P, tf32 K-major: [2 token blocks][64][32]
 constexpr uint32_t S2_U = 114688;                            // [64][128] fp32, 4 boxes of 32
 constexpr uint32_t S2_ST = 147456;                           // S^T bf16 [128][128]; output staging
-constexpr uint32_t S2_EH = 180224, S2_EL = 196608;           // E^T bf16 pair [128][64]
 constexpr uint32_t S2_SMALL = 212992;                        // G_C of two chunks
 constexpr uint32_t S2_TOTAL = S2_SMALL + 1024;
 constexpr uint32_t S2_Z = S2_TOTAL;                          // output gate: z tile [64][128] bf16
 constexpr uint32_t S2_TOTAL_Z = S2_Z + 16384;
 static_assert(S2_TOTAL_Z + 1024 <= 227 * 1024, "state layout");
-// tensor memory: S^T, then two buffers of [(W S)^T | (QH S)^T + E^T P^T | (QL S)^T]
+// tensor memory: S^T, then two buffers of [(W S)^T, then E^T | (QH S)^T + E^T P^T | (QL S)^T]
 constexpr uint32_t S2_TM_S = 0, S2_TM_D = 128, S2_TM_DSTRIDE = 192;
 
-constexpr uint32_t ID_KM_N128 = idesc_bf16(128, 128, false, true);
 constexpr uint32_t ID_KK_N192 = idesc_bf16(128, 192, false, false);
+constexpr uint32_t ID_TF_N128 = idesc_tf32(128, 128);
+constexpr uint32_t ID_TF_N64 = idesc_tf32(128, 64);
 
 struct StateArgs {
     const float *init_state;
@@ -668,18 +666,18 @@ struct StateArgs {
 //   1. S^T -> bf16 operand (ST), S^T <- S^T Diag(G_C)
 //   2. D[c % 2] = S^T [W; QH; QL]^T, one N = 192 product [bar_dw]
 //   3. refill W and Q for c + 1; refill P for c + 1 (its buffer was read by chunk c - 1)
-//   4. E^T = U^T - (W S)^T as a bf16 pair; refill U
-//   5. S^T += E^T (K*G_C/G) [bar_s];  E^T P^T accumulated onto (QH S)^T in D[c % 2] [bar_pe]
+//   4. E^T = U^T - (W S)^T in place of (W S)^T (TF32-rounded fp32); refill U
+//   5. S^T += E^T (K*G_C/G), kind::tf32 [bar_s]
 //   6. output of chunk c - 1 = the sum of its D buffer's two (Q*G S)^T halves, staged in ST
-//      (free: D[c % 2] is done reading it) and stored by TMA (overlaps step 5's MMAs)
+//      (free: D[c % 2] is done reading it) and stored by TMA (overlaps step 5's MMAs); then
+//      E^T P^T accumulated onto (QH S)^T in D[c % 2], kind::tf32 [bar_pe]
 //   7. wait for the state update; refill K
 // Every parity wait is placed where its barrier can be at most one phase ahead.
 template <typename Tout>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mqh,
-                 const __grid_constant__ CUtensorMap mql, const __grid_constant__ CUtensorMap mkh,
-                 const __grid_constant__ CUtensorMap mkl, const __grid_constant__ CUtensorMap mph,
-                 const __grid_constant__ CUtensorMap mpl, const __grid_constant__ CUtensorMap mu,
+                 const __grid_constant__ CUtensorMap mql, const __grid_constant__ CUtensorMap mkt,
+                 const __grid_constant__ CUtensorMap mp, const __grid_constant__ CUtensorMap mu,
                  const __grid_constant__ CUtensorMap to, const __grid_constant__ CUtensorMap tz,
                  const StateArgs a) {
     extern __shared__ unsigned char dsm_raw[];
@@ -736,8 +734,8 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
     tc_fence_after();
     const uint32_t tmb = tmem_base_s;
     const uint32_t tm = tmb + ((uint32_t)(32 * quarter) << 16);
-    // operand descriptors of the shared-memory base: K-major and MN-major (two 64-wide atoms)
-    const uint64_t dK0 = smem_desc_sw128(smem_u32(sm), 16, 1024), dM0 = smem_desc_sw128(smem_u32(sm), 8192, 1024);
+    // operand descriptor of the shared-memory base: K-major, 128-byte swizzle
+    const uint64_t dK0 = smem_desc_sw128(smem_u32(sm), 16, 1024);
     auto fail = [&]() {
         abort_s = 1;
         atomicExch(a.status, kErrTimeout);
@@ -790,21 +788,20 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         mbar_arrive_expect_tx(&bar_u, 32768);
         for (int bx = 0; bx < 4; ++bx) tma_load_2d(sm + S2_U + bx * 8192, &mu, &bar_u, 32 * bx, rowc(c));
     };
-    auto load_k = [&](int c) {
+    auto load_k = [&](int c) {   // four boxes: token block kb, channel half hf
         ++issued[3];
         mbar_arrive_expect_tx(&bar_k, 32768);
-        for (int kb = 0; kb < 2; ++kb) {
-            tma_load_2d(sm + S2_KH + kb * 8192, &mkh, &bar_k, 64 * kb, rowc(c));
-            tma_load_2d(sm + S2_KL + kb * 8192, &mkl, &bar_k, 64 * kb, rowc(c));
-        }
+        for (int kb = 0; kb < 2; ++kb)
+            for (int hf = 0; hf < 2; ++hf)
+                tma_load_2d(sm + S2_KT + kb * 16384 + hf * 8192, &mkt, &bar_k, 32 * kb,
+                            (int)((n0 + c) * 128 + 64 * hf));
     };
     auto load_p = [&](int c) {
         uint64_t *bb = &bar_p[c & 1];
         ++issued[4 + (c & 1)];
         unsigned char *dst = sm + S2_P + (c & 1) * 16384;
         mbar_arrive_expect_tx(bb, 16384);
-        tma_load_2d(dst, &mph, bb, 0, rowc(c));
-        tma_load_2d(dst + 8192, &mpl, bb, 0, rowc(c));
+        for (int kb = 0; kb < 2; ++kb) tma_load_2d(dst + kb * 8192, &mp, bb, 32 * kb, rowc(c));
     };
     if (tid == kTmaThread && nc > 0) {
         load_w(0);
@@ -935,50 +932,42 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
             }
         }
 
-        // ---- 4. E^T = U^T - (W S)^T as a bf16 pair (lane j = value channel, columns = tokens;
-        //         U = 0 for a segment's transition); E^T P^T of chunk c - 1 must have read E first
+        // ---- 4. E^T = U^T - (W S)^T in place of (W S)^T, TF32-rounded (lane j = value channel,
+        //         columns = tokens; U = 0 for a segment's transition): the A operand, in tensor
+        //         memory, of the state update and of E^T P^T.  (E^T P^T of chunk c - 1 must be
+        //         done before the next D product reuses its buffer.)
         if (outputs && c >= 1) wait_bar(&bar_pe, (c - 1) & 1);
         if (use_u && !wait_cycles(&bar_u, par)) fail();
         {
+            const uint32_t te = tm + S2_TM_D + S2_TM_DSTRIDE * par + 32 * half;
             float ws[32];
-            tmem_ld32(tm + S2_TM_D + S2_TM_DSTRIDE * par + 32 * half, ws);
+            tmem_ld32(te, ws);
             tmem_wait_ld();
             const float *U = reinterpret_cast<const float *>(sm + S2_U);
             const int j = row;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float e[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int r = 32 * half + 8 * q4 + u;
-                    e[u] = (use_u ? U[(j >> 5) * 2048 + r * 32 + (j & 31)] : 0.f) - ws[8 * q4 + u];
-                }
-                uint32_t eh[4], el[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) pack_hi_lo(e[2 * u], e[2 * u + 1], eh[u], el[u]);
-                const uint32_t off = sw128_off(row, 32 * half + 8 * q4);
-                *reinterpret_cast<uint4 *>(sm + S2_EH + off) = make_uint4(eh[0], eh[1], eh[2], eh[3]);
-                *reinterpret_cast<uint4 *>(sm + S2_EL + off) = make_uint4(el[0], el[1], el[2], el[3]);
+            for (int u = 0; u < 32; ++u) {
+                const int r = 32 * half + u;
+                ws[u] = round_tf32((use_u ? U[(j >> 5) * 2048 + r * 32 + (j & 31)] : 0.f) - ws[u]);
             }
+            tmem_st32(te, ws);
+            tmem_wait_st();
         }
-        fence_proxy_async();
         tc_fence_before();
         __syncthreads();
         if (tid == kTmaThread && use_u && c + 1 < nc) load_u(c + 1);   // U buffer is free
 
-        // ---- 5. S^T += E^T (K*G_C/G) [bar_s];  E^T P^T -> PE[c % 2] [bar_pe]
-        //         (bf16 pairs: hi.hi + hi.lo + lo.hi)
+        // ---- 5. S^T += E^T (K*G_C/G) [bar_s]: kind::tf32, A = E^T in tensor memory, B the
+        //         TF32 (K*G_C/G)^T tile (K-major: channels x tokens)
+        const uint32_t tE = tmb + S2_TM_D + S2_TM_DSTRIDE * par;
         if (tid == 0) {
             if (!wait_cycles(&bar_k, par)) fail();
             if (outputs && !wait_cycles(&bar_p[par], (c >> 1) & 1)) fail();
             tc_fence_after();
-            const uint32_t ea[3] = {S2_EH, S2_EH, S2_EL}, kbuf[3] = {S2_KH, S2_KL, S2_KH};
 #pragma unroll
-            for (int part = 0; part < 3; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmb + S2_TM_S, desc_add(dK0, ea[part] + ks * 32),
-                             desc_add(dM0, kbuf[part] + ks * 2048), ID_KM_N128, 1);
+            for (int ks = 0; ks < 8; ++ks)
+                mma_tf32_ts(tmb + S2_TM_S, tE + 8 * ks, desc_add(dK0, S2_KT + (ks >> 2) * 16384 + (ks & 3) * 32),
+                            ID_TF_N128, true);
             mma_commit(&bar_s);
         }
 
@@ -988,17 +977,13 @@ kda_state_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__
         // ---- 6b. E^T P^T -> PE[c % 2] [bar_pe], after the output: issuing blocks the issuing
         //          thread while the pipe drains the state update, which would hold the
         //          output's barriers
-        if (tid == 0 && outputs) {
+        if (tid == 0 && outputs) {   // (kind::tf32, A = E^T in tensor memory, B = P)
             tc_fence_after();
             const uint32_t pb = S2_P + par * 16384;
-            const uint32_t ea[3] = {S2_EH, S2_EH, S2_EL}, pbuf[3] = {pb, pb + 8192, pb};
-            const uint32_t pe = tmb + S2_TM_D + S2_TM_DSTRIDE * par + 64;   // onto (QH S)^T
 #pragma unroll
-            for (int part = 0; part < 3; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(pe, desc_add(dK0, ea[part] + ks * 32),
-                             desc_add(dK0, pbuf[part] + ks * 32), ID_KK_N64, 1);
+            for (int ks = 0; ks < 8; ++ks)
+                mma_tf32_ts(tE + 64, tE + 8 * ks, desc_add(dK0, pb + (ks >> 2) * 8192 + (ks & 3) * 32), ID_TF_N64,
+                            true);   // onto (QH S)^T
             mma_commit(&bar_pe);
         }
 
@@ -1108,12 +1093,11 @@ int launch_chunk_kda(const ChunkProblem &p, void *workspace, int *status_word, c
         !map4(&to, p.out, p.B, p.T, p.H, p.out_bf16 ? 2 : 4, true) ||
         !map4(&tz, zgate ? p.z : p.q, p.B, p.T, p.H, 2, true))   // (unused unless gated)
         return kErrCuda;
-    CUtensorMap mw, mqh, mql, mkh, mkl, mph, mpl, mu;
+    CUtensorMap mw, mqh, mql, mkt, mp, mu;
     const int64_t rows = nch * 64;
     if (!map2(&mw, ws.W, rows, 128, 2, true) || !map2(&mqh, ws.QH, rows, 128, 2, true) ||
-        !map2(&mql, ws.QL, rows, 128, 2, true) || !map2(&mkh, ws.KH, rows, 128, 2, true) ||
-        !map2(&mkl, ws.KL, rows, 128, 2, true) || !map2(&mph, ws.PH, rows, 64, 2, true) ||
-        !map2(&mpl, ws.PL, rows, 64, 2, true) || !map2(&mu, ws.U, rows, 128, 4, false))
+        !map2(&mql, ws.QL, rows, 128, 2, true) || !map2(&mkt, ws.KT, nch * 128, 64, 4, true) ||
+        !map2(&mp, ws.P, rows, 64, 4, true) || !map2(&mu, ws.U, rows, 128, 4, false))
         return kErrCuda;
 
     const int s1 = (int)P1_TOTAL + 1024, s2 = (int)(zgate ? S2_TOTAL_Z : S2_TOTAL) + 1024;
@@ -1130,7 +1114,7 @@ int launch_chunk_kda(const ChunkProblem &p, void *workspace, int *status_word, c
         auto kern = p.out_bf16 ? kda_state_kernel<__nv_bfloat16> : kda_state_kernel<float>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s2max) != cudaSuccess)
             return (int)kErrCuda;
-        kern<<<grid, kThreads, s2, stream>>>(mw, mqh, mql, mkh, mkl, mph, mpl, mu, to, tz, sa_);
+        kern<<<grid, kThreads, s2, stream>>>(mw, mqh, mql, mkt, mp, mu, to, tz, sa_);
         return cudaGetLastError() == cudaSuccess ? (int)kOk : (int)kErrCuda;
     };
     const unsigned bh = (unsigned)(p.B * p.H);

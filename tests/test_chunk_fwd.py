@@ -367,8 +367,8 @@ def test_kda_tc_in_place_carry(dr):
 
 
 def test_kda_tc_workspace_bytes(dr):
-    # per (b, h, chunk): W 16 KiB, U 32 KiB, P pair 16 KiB, Q*G and K*G_C/G pairs 64 KiB,
-    # G_C 512 B
+    # per (b, h, chunk): W 16 KiB (bf16), U 32 KiB (fp32), P 16 KiB (fp32), the Q*G pair
+    # 32 KiB, (K*G_C/G)^T 32 KiB (fp32), G_C 512 B
     desc = dr.chunk_desc(4, 8192, 32, 128, 128, dr.DR_BF16, dr.DR_BF16,
                          dr.DR_GATE_CHANNEL, 64)
     assert dr.workspace_bytes(desc) == 4 * 32 * 128 * 131584
