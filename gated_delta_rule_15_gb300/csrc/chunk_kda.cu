@@ -89,18 +89,25 @@ constexpr uint32_t P1_TOTAL = P1_SMALL + 256 + 4096 + 512 + 512;   // + G_C[128]
 // the exact diagonal blocks over the right factors; staging of W and U at the end
 constexpr uint32_t P1_A = 0, P1_T = 16384, P1_TB = 34816, P1_XD = P1_R;
 constexpr uint32_t P1_WST = 0, P1_UST = 16384;
-// one-product chunks: the right factor as a 128-row B operand [R high; R low], K-block 0
-// over V and K-block 1 over K*G (16 KB apart)
+// one-product chunks: the right factor as a K-major tf32 B operand (64 token rows, four
+// 8 KB blocks of 32 channels) over V and K*G
 constexpr uint32_t P1_R1 = P1_V;
-// tensor memory: X = [Q; K] R^T (one product: [X_hh + X_lh | X_hl + X_ll], 128 columns; four
-// rounds: 64 columns), the left factor's high and low halves; U^T, W^T afterwards
+// tensor memory: X = [Q; K] R^T (64 columns), the left factor (one product: fp32, 128
+// columns; four rounds: high and low bf16 halves); U^T, W^T afterwards
 constexpr uint32_t P1_TM_X = 0, P1_TM_LH = 128, P1_TM_LL = 192, P1_TM_U = 128, P1_TM_W = 192;
+// (one-product chunks) the left factor as fp32, the tf32 A operand: 128 columns
+constexpr uint32_t P1_TM_L1 = 128;
 static_assert(P1_T + 64 * kTs * 4 <= P1_TB && P1_TB + 8192 <= P1_V, "prep layout");
 static_assert(P1_UST + 32768 <= P1_V && P1_TOTAL + 1024 <= 113 * 1024, "prep layout");
 
 constexpr uint32_t ID_KK_N16 = idesc_bf16(128, 16, false, false);
+constexpr uint32_t ID_TF_N128 = idesc_tf32(128, 128);
+constexpr uint32_t ID_TF_N64 = idesc_tf32(128, 64);
+// byte offset of fp32 element (row, k), k < 32, in a 128-byte-swizzled K-major tf32 tile
+__device__ __forceinline__ uint32_t sw128_off32(uint32_t row, uint32_t k) {
+    return row * 128u + ((((k >> 2) ^ (row & 7u)) & 7u) << 4) + ((k & 3u) << 2);
+}
 constexpr uint32_t ID_KK_N64 = idesc_bf16(128, 64, false, false);
-constexpr uint32_t ID_KK_N128 = idesc_bf16(128, 128, false, false);
 // Largest per-channel decay (natural log) inside one 16-token block that the tensor-core
 // products of the diagonal blocks take; beyond it the chunk recomputes those entries.
 constexpr float kDiagLimit = 64.f;
@@ -287,14 +294,15 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         // ---- one product for the whole chunk against ref = g_63 (no channel decays by more
         //      than kDiagLimit across the chunk): left factor xE_t = x_t exp(g_t - g_63) in
         //      [|x|, |x| e^kDiagLimit] (tensor memory), right factor k_s exp(g_63 - g_s) =
-        //      (K*G_C/G)_s <= |k_s| (shared memory, and the workspace's pair).  Q rows also
-        //      write Q*G = xE G_C; K rows keep K*G = xE G_C for the W operand.
+        //      (K*G_C/G)_s <= |k_s| (shared memory, and the workspace's transposed copy), both
+        //      TF32-rounded fp32 for one kind::tf32 product.  Q rows also write Q*G = xE G_C;
+        //      K rows keep K*G = xE G_C for the W operand.
         uint32_t kg_keep[32];
         {
             const size_t go = ((size_t)n * 64 + t_row) * 128 + 64 * half;
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
-                uint32_t hi[16], lo[16];
+                float lf[32];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int c = 64 * half + 32 * p + 8 * i, w = 4 * (4 * p + i);
@@ -305,10 +313,10 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     load8_g(LA, t_row, c, g8);
                     load8_g(LA, 63, c, gl);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) e8[u] = x8[u] * ex2(g8[u] - gl[u]);
-#pragma unroll
-                    for (int u = 0; u < 8; u += 2)
-                        pack_hi_lo(e8[u], e8[u + 1], hi[4 * i + (u >> 1)], lo[4 * i + (u >> 1)]);
+                    for (int u = 0; u < 8; ++u) {
+                        e8[u] = x8[u] * ex2(g8[u] - gl[u]);
+                        lf[8 * i + u] = round_tf32(e8[u]);
+                    }
                     uint32_t oh[4], ol[4];
                     if (qrow) {
 #pragma unroll
@@ -321,20 +329,23 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
                         for (int u = 0; u < 8; ++u) kt[u] = x8[u] * ex2(gl[u] - g8[u]);
 #pragma unroll
-                        for (int u = 0; u < 8; u += 2) {
+                        for (int u = 0; u < 8; u += 2)
                             kg_keep[w + (u >> 1)] = pack_bf16(e8[u] * sGamC[c + u], e8[u + 1] * sGamC[c + u + 1]);
-                            pack_hi_lo(kt[u], kt[u + 1], oh[u >> 1], ol[u >> 1]);
-                        }
-                        const uint32_t so = (c >> 6) * 16384 + sw128_off(t_row, c & 63);
-                        *reinterpret_cast<uint4 *>(sm + P1_R1 + so) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
-                        *reinterpret_cast<uint4 *>(sm + P1_R1 + 8192 + so) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) kt[u] = round_tf32(kt[u]);
+                        // the right factor, row t_row of a K-major tf32 tile (32 channels per
+                        // 128-byte row, four channel blocks 8 KB apart)
+                        const uint32_t sb = P1_R1 + (c >> 5) * 8192;
+                        *reinterpret_cast<float4 *>(sm + sb + sw128_off32(t_row, c & 31)) =
+                            make_float4(kt[0], kt[1], kt[2], kt[3]);
+                        *reinterpret_cast<float4 *>(sm + sb + sw128_off32(t_row, (c & 31) + 4)) =
+                            make_float4(kt[4], kt[5], kt[6], kt[7]);
                         // row c + u of K*G_C/G transposed (a warp's 32 tokens: 128 contiguous bytes)
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) a.ws.KT[(n * 128 + c + u) * 64 + t_row] = round_tf32(kt[u]);
+                        for (int u = 0; u < 8; ++u) a.ws.KT[(n * 128 + c + u) * 64 + t_row] = kt[u];
                     }
                 }
-                tmem_st16u(tm + P1_TM_LH + 32 * half + 16 * p, hi);
-                tmem_st16u(tm + P1_TM_LL + 32 * half + 16 * p, lo);
+                tmem_st32(tm + P1_TM_L1 + 64 * half + 32 * p, lf);
             }
             tmem_wait_st();
         }
@@ -343,14 +354,11 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
-            // [L high; L low] x [R high; R low]^T: two N = 128 products into one accumulator
+            // X = L R^T: one N = 64 kind::tf32 product over the 128 channels
 #pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ts(tmb + P1_TM_X, tmb + (part ? P1_TM_LL : P1_TM_LH) + 8 * ks,
-                                desc_add(dK0, P1_R1 + (ks >> 2) * 16384 + (ks & 3) * 32), ID_KK_N128,
-                                (part | ks) != 0);
+            for (int ks = 0; ks < 16; ++ks)
+                mma_tf32_ts(tmb + P1_TM_X, tmb + P1_TM_L1 + 8 * ks,
+                            desc_add(dK0, P1_R1 + (ks >> 2) * 8192 + (ks & 3) * 32), ID_TF_N64, ks > 0);
             mma_commit(&bar_mma);
         }
         if (!wait_cycles(&bar_mma, mma_phase)) fail();
@@ -527,13 +535,6 @@ kda_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     {
         float x[32];
         tmem_ld32(tm + P1_TM_X + 32 * half, x);
-        if (!four_rounds_s) {   // one product: X = X_hh + X_lh + (X_hl + X_ll)
-            float x2[32];
-            tmem_ld32(tm + P1_TM_X + 64 + 32 * half, x2);
-            tmem_wait_ld();
-#pragma unroll
-            for (int u = 0; u < 32; ++u) x[u] += x2[u];
-        }
         tmem_wait_ld();
         const int c0 = 32 * half;
         if (diag_exact) {
@@ -642,8 +643,6 @@ static_assert(S2_TOTAL_Z + 1024 <= 227 * 1024, "state layout");
 constexpr uint32_t S2_TM_S = 0, S2_TM_D = 128, S2_TM_DSTRIDE = 192;
 
 constexpr uint32_t ID_KK_N192 = idesc_bf16(128, 192, false, false);
-constexpr uint32_t ID_TF_N128 = idesc_tf32(128, 128);
-constexpr uint32_t ID_TF_N64 = idesc_tf32(128, 64);
 
 struct StateArgs {
     const float *init_state;
