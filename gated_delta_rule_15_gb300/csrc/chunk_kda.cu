@@ -103,10 +103,6 @@ static_assert(P1_UST + 32768 <= P1_V && P1_TOTAL + 1024 <= 113 * 1024, "prep lay
 constexpr uint32_t ID_KK_N16 = idesc_bf16(128, 16, false, false);
 constexpr uint32_t ID_TF_N128 = idesc_tf32(128, 128);
 constexpr uint32_t ID_TF_N64 = idesc_tf32(128, 64);
-// byte offset of fp32 element (row, k), k < 32, in a 128-byte-swizzled K-major tf32 tile
-__device__ __forceinline__ uint32_t sw128_off32(uint32_t row, uint32_t k) {
-    return row * 128u + ((((k >> 2) ^ (row & 7u)) & 7u) << 4) + ((k & 3u) << 2);
-}
 constexpr uint32_t ID_KK_N64 = idesc_bf16(128, 64, false, false);
 // Largest per-channel decay (natural log) inside one 16-token block that the tensor-core
 // products of the diagonal blocks take; beyond it the chunk recomputes those entries.

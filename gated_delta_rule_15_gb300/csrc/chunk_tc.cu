@@ -16,26 +16,27 @@
 //   W^T = K^T (T diag(beta G))^T         (128 x 64)  = (T diag(beta) (K*G))^T
 //   D   = S^T [W; Q]^T                   (128 x 128) = [(W S)^T | (Q S)^T]
 //   E^T = U^T - (W S)^T
-//   S^T <- gamma S^T + (E^T diag(delta)) K                 (state carried to the next chunk)
-//   O^T = (Q S)^T diag(G) + E^T P^T                        (chunk output)
+//   [O^T | S^T] <- [(Q S)^T diag(G) | gamma S^T] + E^T [P; Kt^T]^T,  Kt = diag(delta) K
 //
-// Precision: P, E^T and E^T diag(delta) enter their products as a bf16 pair (high part and
-// the bf16 rounding of the remainder), so those products carry ~2^-16 relative error
-// instead of bf16's 2^-8; S^T, W and the T factors enter as single bf16 operands, Q exactly
-// (its decay G is applied to Q S in fp32).  A rounding model of this arithmetic against the
-// fp64 oracle puts the output error at ~1e-2 x RMS (about 3e-2 without the pairs).
+// Precision: the state update and the output's intra-chunk term take E, P and Kt as tf32
+// (10 explicit mantissa bits): E^T stays fp32 in tensor memory, where it is the A operand,
+// and [P; Kt^T] is one K-major fp32 B operand; S^T (a bf16 A operand in tensor memory), W
+// and the T factors enter as single bf16 operands, Q exactly (its decay G is applied to Q S
+// in fp32).
 //
 // One CTA per (b, h): eight compute warps and one warp that only issues the tcgen05 MMAs.
 // The chunk steps are software-pipelined across two chunks, so that the MMA groups of one
 // run while the CUDA cores work on the other.  In the iteration of chunk c the compute warps
-//   1. convert S^T to the bf16 operand of D and decay S^T in TMEM,
+//   1. convert S^T to the bf16 operand of D (in TMEM) and decay S^T,
 //   2. write W (from TMEM) as the B operand of D            -> MMA warp: D(c)
-//   3. build the next chunk's A from its X (already in TMEM),
-//   4. build E^T and E^T diag(delta)                          -> MMA warp: state update,
-//                                                                E^T P^T (c)
-//   5. solve the next chunk's T = (I + A)^-1                  -> MMA warp: U/W(c+1)
-//   6. write chunk c's output and the next chunk's P          -> MMA warp: X(c+2),
-//                                                                stage of c takes c + 2
+//   3. build this chunk's Kt^T and the next chunk's A from its X (already in TMEM), and
+//      solve the diagonal blocks of the next chunk's T = (I + A)^-1 while D runs,
+//   4. form E^T and G (Q S)^T in TMEM                        -> MMA warp: [O^T | S^T] (c)
+//   5. merge the next chunk's T (warps 0..3) while warps 4..7 build the next chunk's P
+//                                                           -> MMA warp: X(c+2)
+//      and write chunk c's output,
+//   6. hand off                                             -> MMA warp: U/W(c+1), stage of
+//                                                              c takes c + 2
 // and the gate warp scans the gates two chunks ahead.  T = (I + A)^-1 is built by 16 x 16
 // blocks (tc_common.cuh).  q, k, v tiles (64 tokens x 128, bf16) arrive by TMA with 128-byte
 // swizzle into two stages; operands written by the CUDA cores use the same swizzled K-major
@@ -83,20 +84,16 @@ constexpr uint32_t kStageBytes = 49152;
 // stage layout: [Q kb0 | K kb0 | Q kb1 | K kb1 | V kb0 | V kb1], 8 KB each (64 x 64 bf16)
 constexpr uint32_t OFF_K0 = 8192, OFF_V0 = 32768;
 // Beyond the two stages (lifetimes within the iteration of chunk c, steps as above):
-constexpr uint32_t SM_ST = 2 * kStageBytes;   // 32 KB: S^T bf16 128 x 128 K-major (steps 1 ->
-                                              // D(c)); then, from step 5, the next chunk's fp32
-                                              // T (16 KB, swizzled) and T diag beta | T diag
-                                              // beta G (16 KB, until U/W(c+1))
-constexpr uint32_t SM_T = SM_ST, SM_TB = SM_ST + 16384;
-constexpr uint32_t SM_WQ = SM_ST + 32768;     // 32 KB: W^T 128 x 64 (MN-major B operand of
-                                              // (W S)^T; step 2 -> D(c)); then E^T high |
-                                              // E^T low (step 4 -> E^T P^T)
-constexpr uint32_t SM_ET2 = SM_WQ + 32768;    // E^T diag(delta) high (its low part goes to the
-                                              // stage's V tile, read by U/W(c) already)
-constexpr uint32_t SM_A = SM_ET2 + 16384;     // the next chunk's fp32 A (step 3 -> step 5)
-constexpr uint32_t SM_P = SM_A + 16384;       // the next chunk's P high | P low (step 6 ->
-                                              // its E^T P^T)
-constexpr uint32_t SM_SMALL = SM_P + 16384;   // gate vectors of two chunks, solve scratch
+constexpr uint32_t SM_T = 2 * kStageBytes;    // the next chunk's fp32 T (16 KB, swizzled; step 3
+constexpr uint32_t SM_TB = SM_T + 16384;      // on) and T diag beta | T diag beta G (16 KB,
+                                              // until U/W(c+1))
+constexpr uint32_t SM_W = SM_T + 32768;       // 16 KB: W^T 128 x 64 (MN-major B operand of
+                                              // (W S)^T; step 2 -> D(c))
+constexpr uint32_t SM_A = SM_W + 16384;       // the next chunk's fp32 A (step 3)
+constexpr uint32_t SM_BU = SM_A + 16384;      // [P; Kt^T] (tf32, K-major): two K-blocks of 32
+constexpr uint32_t BU_KB = 24576;             // tokens, 192 rows x 128 bytes each; P rows
+                                              // (step 5 of the chunk before), Kt^T rows (step 3)
+constexpr uint32_t SM_SMALL = SM_BU + 2 * BU_KB;   // gate vectors of two chunks, solve scratch
 constexpr uint32_t SM_TOTAL = SM_SMALL + 8192;
 // fused neighbours only: norm vectors of two chunks [2][7][64]: nq, nk, G nq, beta nk,
 // G nk, |k| (1 / nk) and delta nk
@@ -104,15 +101,18 @@ constexpr uint32_t SM_NRM = SM_TOTAL;
 constexpr uint32_t SM_TOTAL_FUSED = SM_NRM + 3584;
 static_assert(SM_TOTAL_FUSED + 1024 <= 227 * 1024, "layout");
 enum { NV_NQ = 0, NV_NK = 1, NV_GQ = 2, NV_BK = 3, NV_GK = 4, NV_RK = 5, NV_DK = 6 };
-constexpr uint32_t TM_S = 0, TM_D = 128, TM_X = 256, TM_U = 320, TM_W = 384, TM_PE = 448;
-// TM_D: [ (W S)^T | (Q S)^T ];  TM_X: [Q; K] K^T;  TM_PE: E^T P^T
+constexpr uint32_t TM_WE = 0, TM_QO = 64, TM_S = 128, TM_SB = 256, TM_X = 320, TM_U = 384, TM_W = 448;
+// TM_WE: (W S)^T, then E^T (fp32, the A operand of the state update);  TM_QO: (Q S)^T, then
+// G (Q S)^T, then O^T: [TM_QO | TM_S] is the accumulator of the state update;  TM_SB: S^T as
+// bf16 pairs (the A operand of D);  TM_X: [Q; K] K^T
 // Largest in-chunk log-decay span for which exp(g_r - g_s) is formed as a product of two
 // exponentials around the chunk's middle token (both factors stay within fp32 range).
 constexpr float kFactorSpan = 80.f;
 
 constexpr uint32_t ID_KK_N64 = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_MK_N64 = idesc_bf16(128, 64, true, false);
-constexpr uint32_t ID_KM_N128 = idesc_bf16(128, 128, false, true);
+constexpr uint32_t ID_UPD = idesc_tf32(128, 192);     // [O^T | S^T]: B = [P; Kt^T]
+constexpr uint32_t ID_UPD_S = idesc_tf32(128, 128);   // S^T alone (no outputs): B = Kt^T
 constexpr uint32_t ID_KM_N64 = idesc_bf16(128, 64, false, true);
 
 struct TcArgs {
@@ -149,7 +149,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     // mbarriers: TMA stages; per MMA group its completion (committed by the MMA warp) and,
     // for the groups whose operands the compute warps write, "operands ready" (full_*,
     // arrived by thread 0 after the compute warps' barrier).  Each completes once per chunk.
-    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_q, bar_s, bar_pe;
+    __shared__ uint64_t bar_tma[2], bar_x, bar_uw, bar_d, bar_q, bar_s;
     __shared__ uint64_t full_x, full_uw, full_d, full_s, bar_z;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s, factored_s[2];
@@ -187,7 +187,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const int h = bh % a.H, b = bh / a.H;
     const int n_it = c_end - c_begin;            // this CTA's chunks, indexed 0 .. n_it - 1
     constexpr int kTmaThread = 224;              // lane 0 of warp 7 issues the TMA loads
-    constexpr int kGateWarp = 1;                 // warp 1 scans the gates
+    constexpr int kGateWarp = 6;                 // warp 6 scans the gates (idle after its output)
     // gate vectors of two chunks (chunk `it` in set it % 2): g_r, exp(g_r), exp(g_63 - g_r),
     // beta_r, and the factors exp(g_r - g_31), exp(g_31 - g_r)
     float *sVec = reinterpret_cast<float *>(sm + SM_SMALL);   // [2][6][64]
@@ -203,7 +203,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
     if (tid == 0) {
         uint64_t *bars[] = {&bar_tma[0], &bar_tma[1], &bar_x, &bar_uw, &bar_d, &bar_q, &bar_s,
-                            &bar_pe, &full_x, &full_uw, &full_d, &full_s, &bar_z};
+                            &full_x, &full_uw, &full_d, &full_s, &bar_z};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         abort_s = 0;
         fence_mbar_init();
@@ -243,6 +243,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             if (zgate) tma_prefetch_4d(&tz, 64 * kb, h, t0, b);
         }
     };
+    auto prefetch_tiles = [&](int it) {   // chunk `it`'s q, k, v tiles into L2
+        const int t0 = (c_begin + it) * 64;
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_prefetch_4d(&tq, 64 * kb, h, t0, b);
+            tma_prefetch_4d(&tk, 64 * kb, h, t0, b);
+            tma_prefetch_4d(&tv, 64 * kb, h, t0, b);
+        }
+    };
+    // Without the output gate the stage of chunk c is free once (Q S)^T(c) has read it (step 4)
+    // and takes chunk c + 2 then (X(c + 2) may then be issued once P(c + 1) has read TM_X);
+    // with the gate the stage is released after the output (step 6).
+    const bool early = !zgate;
     // (MMA warp) chunk `it`'s output gate input into its stage's Q tiles (dead once (Q S)^T
     // has read them)
     auto issue_z = [&](int it) {
@@ -251,13 +263,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         for (int kb = 0; kb < 2; ++kb)
             tma_load_4d(stage(it) + kb * 16384, &tz, &bar_z, 64 * kb, h, t0, b);
     };
-    // byte offset in the stage of output box kb: the Q tiles (bf16) or the Q and K tiles
-    // (fp32); with the gate, whose z holds the Q tiles, the V slot (bf16) or the K tiles and
-    // the V slot (fp32) -- all dead once E^T P^T has completed
-    auto obox = [&](int kb) -> uint32_t {
-        if (!zgate) return (uint32_t)kb * (sizeof(Tout) == 2 ? 16384u : 8192u);
-        if (sizeof(Tout) == 2) return OFF_V0 + 8192u * kb;
-        return kb < 2 ? OFF_K0 + 16384u * kb : OFF_V0 + 8192u * (kb - 2);
+    // Output box kb (8 KB: 64 tokens x 64 bf16 or 32 fp32 channels) of chunk `it`.  Without the
+    // output gate: Kt^T rows of [P; Kt^T] (free once the state update has read them), so that
+    // the stage is released after (Q S)^T and takes the chunk after next early -- for bf16 the
+    // rows of key channels 64..127 (two 8 KB runs), which the next chunk's Kt^T build
+    // rewrites only in its step 3, for fp32 all four.  With the gate, whose z holds the
+    // stage's Q tiles: the V slot (bf16) or the K tiles and the V slot (fp32) of the stage,
+    // which then takes the chunk after next once the output has left.
+    auto obox = [&](int it, int kb) -> unsigned char * {
+        if (!zgate && sizeof(Tout) == 2) return sm + SM_BU + 16384u + kb * BU_KB;
+        if (!zgate) return sm + SM_BU + (kb >> 1) * BU_KB + 8192u * (1 + (kb & 1));
+        if (sizeof(Tout) == 2) return stage(it) + OFF_V0 + 8192u * kb;
+        return stage(it) + (kb < 2 ? OFF_K0 + 16384u * kb : OFF_V0 + 8192u * (kb - 2));
     };
     // beta (the aligned 32-bit word holding it) and log alpha of chunk `it`, two tokens per
     // lane of the gate warp, copied asynchronously two chunks ahead; one commit group per
@@ -384,7 +401,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     };
     // (compute warps) rows of X for chunk `it` (whose X is in TMEM, gate set it % 2): the
     // A rows (64..127, fp32, at SM_A; warps of lane quarters 2 and 3) or the P rows (0..63,
-    // bf16 high/low at SM_P; quarters 0 and 1)
+    // tf32, rows 0..63 of [P; Kt^T], K-block col_half; quarters 0 and 1)
     auto build_pa = [&](int it, bool rows_a, int col_half) {
         if ((quarter >= 2) != rows_a) return;
         const int r = quarter < 2 ? row : row - 64;
@@ -424,21 +441,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             for (int u = 0; u < 32; ++u) dec[u] = __expf(fminf(gr - sG[c0 + u], 0.f));
         }
         if (!rows_a) {
-            uint32_t pk[16], pl[16];
+            const uint32_t pb = smem_u32(sm + SM_BU + col_half * BU_KB);
 #pragma unroll
-            for (int u = 0; u < 32; u += 2) {
-                const int s0 = c0 + u;
-                const float p0 = s0 <= r ? dec[u] * x[u] : 0.f;
-                const float p1 = s0 + 1 <= r ? dec[u + 1] * x[u + 1] : 0.f;
-                pack_hi_lo(p0, p1, pk[u >> 1], pl[u >> 1]);
-            }
+            for (int q4 = 0; q4 < 8; ++q4) {
+                float pv[4];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const uint32_t off = sw128_off(r, c0 + 8 * q4);
-                *reinterpret_cast<uint4 *>(sm + SM_P + off) =
-                    make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-                *reinterpret_cast<uint4 *>(sm + SM_P + 8192 + off) =
-                    make_uint4(pl[4 * q4], pl[4 * q4 + 1], pl[4 * q4 + 2], pl[4 * q4 + 3]);
+                for (int e = 0; e < 4; ++e)
+                    pv[e] = c0 + 4 * q4 + e <= r ? round_tf32(dec[4 * q4 + e] * x[4 * q4 + e]) : 0.f;
+                sts128f(pb + sw128_off32(r, 4 * q4), pv[0], pv[1], pv[2], pv[3]);
             }
         } else {
             const float br = sBeta[r] * nk2;   // B_rs = beta_r nk_r^2 ... with the fused norm
@@ -456,6 +466,39 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     v4.z = round_tf32(v4.z); v4.w = round_tf32(v4.w);
                 }
                 *reinterpret_cast<float4 *>(sA + a_index(r, s0)) = v4;
+            }
+        }
+    };
+    // (compute warps) Kt^T of chunk `it` into rows 64..191 of [P; Kt^T]: Kt^T[i][r] =
+    // delta_r k_r[i] (tf32; delta_r / |k_r| with the fused norm), key-channel blocks ib and
+    // ib + nb - 1 (eight channels each; nb = 1 or 2): ldmatrix.trans of the k tile gives
+    // each lane channel i and the tokens r, r + 1 of one 8 x 8 block.
+    auto kt_build = [&](int it, int ib0, int nb) {
+        wait_bar(&bar_tma[it & 1], (it >> 1) & 1);
+        const uint32_t kbase = smem_u32(stage(it) + OFF_K0);
+        const uint32_t bu = smem_u32(sm + SM_BU);
+        const uint32_t sDel = smem_u32(l2 ? nvec(it, NV_DK) : vec(it, 2));
+        uint32_t v[2][2][4];   // [block][token half][matrix]: all loads first
+#pragma unroll
+        for (int bq = 0; bq < 2; ++bq) {
+            const int ib = ib0 + (bq < nb ? bq : 0), kb = ib >> 3, c8 = ib & 7;
+#pragma unroll
+            for (int rq = 0; rq < 2; ++rq) {
+                const int rr = 8 * (4 * rq + (lane >> 3)) + (lane & 7);   // the token row this lane addresses
+                ldsm_x4_trans(kbase + kb * 16384 + rr * 128 + ((c8 ^ (rr & 7)) << 4), v[bq][rq]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {   // this lane's token pair r, r + 1 of token block q
+            const int r = 8 * q + 2 * (lane & 3);
+            const float2 dq = lds64f(sDel + 4 * r);
+#pragma unroll
+            for (int bq = 0; bq < 2; ++bq) {
+                if (bq >= nb) break;
+                const int i = 8 * (ib0 + bq) + (lane >> 2);
+                const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v[bq][q >> 2][q & 3]));
+                sts64f(bu + (r >> 5) * BU_KB + sw128_off32(64 + i, r & 31), round_tf32(dq.x * kv.x),
+                       round_tf32(dq.y * kv.y));
             }
         }
     };
@@ -498,8 +541,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
     // ---------------- MMA warp: issues every tcgen05.mma group, each once its operands are
     // ready, in the order the compute warps produce them, and commits it to the barrier
-    // they wait on.  Chunk c's D, state update and E^T P^T; then chunk c + 1's U/W; then
-    // chunk c + 2's X.
+    // they wait on.  Chunk c's D and [O^T | S^T]; then chunk c + 2's X and chunk c + 1's U/W.
     if (warp == kMmaWarp) {
         if (lane == 0 && n_it > 0) {
             uint64_t *last = &bar_x;   // most recent commit (drained on abort)
@@ -538,15 +580,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16(tmb + TM_D, desc_add(dK0, SM_ST + (ks >> 2) * 16384 + (ks & 3) * 32),
-                             desc_add(dM8, SM_WQ + ks * 2048), ID_KM_N64, ks > 0);
+                    mma_bf16_ts(tmb + TM_WE, tmb + TM_SB + 8 * ks, desc_add(dM8, SM_W + ks * 2048), ID_KM_N64, ks > 0);
                 mma_commit(&bar_d);
                 if (outputs)
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16(tmb + TM_D + 64, desc_add(dK0, SM_ST + o),
-                                 desc_add(dK0, (uint32_t)((st + o) - sm)), ID_KK_N64, ks > 0);
+                        mma_bf16_ts(tmb + TM_QO, tmb + TM_SB + 8 * ks, desc_add(dK0, (uint32_t)((st + o) - sm)),
+                                    ID_KK_N64, ks > 0);
                     }
                 mma_commit(&bar_q);
                 last = &bar_q; last_par = par;
@@ -555,40 +596,35 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     issue_z(it);
                     z_last = it;
                 }
-                // S^T += (E^T diag delta) K, then PE = E^T P^T  (high/low pairs)
+                // [O^T | S^T] += E^T [P; Kt^T]^T  (tf32; E^T from tensor memory); without
+                // outputs S^T += E^T Kt
                 if (!wait_cycles(&full_s, par)) { fail(); break; }
                 tc_fence_after();
-                unsigned char *e2[2] = {sm + SM_ET2, st + OFF_V0};
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmb + TM_S, desc_add(dK0, (uint32_t)((e2[part] + ks * 32) - sm)),
-                                 desc_add(dM16, (uint32_t)((st + OFF_K0 + ks * 2048) - sm)), ID_KM_N128, 1);
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_tf32_ts(tmb + (outputs ? TM_QO : TM_S), tmb + TM_WE + 8 * ks,
+                                desc_add(dK0, SM_BU + (outputs ? 0u : 8192u) + (ks >> 2) * BU_KB + (ks & 3) * 32),
+                                outputs ? ID_UPD : ID_UPD_S, true);
                 mma_commit(&bar_s);
-                const uint32_t ea[3] = {SM_WQ, SM_WQ, SM_WQ + 16384}, pb[3] = {SM_P, SM_P + 8192, SM_P};
-                if (outputs)
-#pragma unroll
-                    for (int part = 0; part < 3; ++part)
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            mma_bf16(tmb + TM_PE, desc_add(dK0, ea[part] + ks * 32),
-                                     desc_add(dK0, pb[part] + ks * 32), ID_KK_N64, (part | ks) != 0);
-                mma_commit(&bar_pe);
-                last = &bar_pe; last_par = par;
-                // the next chunk's U/W, then the chunk after's X
-                if (it + 1 < n_it) {
-                    if (!wait_cycles(&full_uw, (it + 1) & 1)) { fail(); break; }
-                    tc_fence_after();
-                    issue_uw(it + 1);
-                    last = &bar_uw; last_par = (it + 1) & 1;
+                last = &bar_s; last_par = par;
+                // the next chunk's U/W (the next D waits for it), then the chunk after next's X
+                bool ok = true;
+                for (int g = 0; g < 2 && ok; ++g) {
+                    if (g == 1) {
+                        if (it + 2 < n_it) {
+                            if (!wait_cycles(&full_x, (it + 1) & 1)) { fail(); ok = false; break; }
+                            tc_fence_after();
+                            issue_x(it + 2);
+                            last = &bar_x; last_par = it & 1;
+                        }
+                    } else if (it + 1 < n_it) {
+                        if (!wait_cycles(&full_uw, (it + 1) & 1)) { fail(); ok = false; break; }
+                        tc_fence_after();
+                        issue_uw(it + 1);
+                        last = &bar_uw; last_par = (it + 1) & 1;
+                    }
                 }
-                if (it + 2 < n_it) {
-                    if (!wait_cycles(&full_x, (it + 1) & 1)) { fail(); break; }
-                    tc_fence_after();
-                    issue_x(it + 2);
-                    last = &bar_x; last_par = it & 1;
-                }
+                if (!ok) break;
             }
             if (abort_s) {   // drain this warp's MMAs and copies (bounded)
                 wait_cycles(last, last_par);
@@ -636,15 +672,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         unsigned char *st = stage(it);
         const int t0 = (c_begin + it) * 64;
         const bool next = it + 1 < n_it;
+        if (tid == kTmaThread && it + 2 < n_it) prefetch_tiles(it + 2);
 
-        // ---- 1. S^T to bf16 (SM_ST) and S^T <- gamma S^T in TMEM: after the previous state
-        //         update, and after this chunk's U/W products have read T diag beta (SM_TB)
+        // ---- 1. S^T to bf16 pairs (TM_SB: 32-bit column c holds S^T columns 2c, 2c + 1) and
+        //         S^T <- gamma S^T: after the previous state update (D(c - 1), which read
+        //         TM_SB, completed before it)
         if (it >= 1) wait_bar(&bar_s, par ^ 1);
-        wait_bar(&bar_uw, par);
         {
             const float gamma = vec(it, 1)[63];
             float v[32];
-            unsigned char *dst = sm + SM_ST + half * 16384;
             for (int part = 0; part < 2; ++part) {
                 const int i0 = 64 * half + 32 * part;
                 tmem_ld32(tm + TM_S + i0, v);
@@ -654,12 +690,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
                     for (int u = 0; u < 32; ++u) ck[(size_t)u * 128] = v[u];
                 }
+                {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const float *f = v + 8 * q4;
-                    *reinterpret_cast<uint4 *>(dst + sw128_off(row, 32 * part + 8 * q4)) =
-                        make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
-                                   pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                    for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
+                    tmem_st16u(tm + TM_SB + i0 / 2, pk);
                 }
 #pragma unroll
                 for (int u = 0; u < 32; ++u) v[u] *= gamma;
@@ -667,8 +702,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             }
             tmem_wait_st();
         }
+        // ---- 1b. this chunk's Kt^T, key channels 0..63 (the previous state update has read
+        //          [P; Kt^T], and the output staged over its rows has left), while U/W(c) runs
+        kt_build(it, warp, 1);
         // ---- 2. W^T (lane i = key channel, columns = tokens r) as the MN-major B operand of
         //         (W S)^T: this lane's row of 64 tokens, 16 bytes at a time
+        wait_bar(&bar_uw, par);
         {
             float w[32];
             tmem_ld32(tm + TM_W + 32 * half, w);
@@ -676,88 +715,93 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 const float *f = w + 8 * q4;
-                *reinterpret_cast<uint4 *>(sm + SM_WQ + sw128_off(row, 32 * half + 8 * q4)) =
+                *reinterpret_cast<uint4 *>(sm + SM_W + sw128_off(row, 32 * half + 8 * q4)) =
                     make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
                                pack_bf16(f[6], f[7]));
             }
         }
-        fence_proxy_async();
+        fence_proxy_async();   // W and Kt^T for the tensor core
+        // (bf16, no gate) the previous output's store has read its staging before step 3
+        // rewrites those rows
+        if (early && sizeof(Tout) == 2 && tid == kTmaThread) bulk_wait_read_all();
         tc_fence_before();
         named_sync(1, kThreads);
         if (abort_s) break;
         if (tid == 0) mbar_arrive(&full_d);   // D = S^T [W; Q]^T (MMA warp)
 
-        // ---- 3. A of the next chunk (its X arrived meanwhile)
+        // ---- 3. Kt^T, key channels 64..127 (lane quarters 0 and 1), while the other warps build
+        //         the next chunk's A (its X arrived before D was issued); then the diagonal
+        //         blocks of the next chunk's T (U/W(c) has read SM_TB), all while D runs
+        if (quarter < 2) kt_build(it, 8 + 2 * ((warp & 1) + 2 * half), 2);
         if (next) {
-            if (l2 && quarter < 2) norm_vecs(it + 1);   // read from step 5 on
+            if (l2 && quarter < 2) norm_vecs(it + 1);   // read by the solve
             wait_bar(&bar_x, (it + 1) & 1);
             build_pa(it + 1, true, half);
+            tc_fence_before();
+            named_sync(1, kThreads);
+            // without outputs X(c + 1) has no other reader: X(c + 2) may overwrite TM_X
+            if (!outputs && tid == 0 && it + 2 < n_it) mbar_arrive(&full_x);
+            solve_diag(it + 1);
         }
 
-        // ---- 4. E^T = U^T - (W S)^T, and E^T diag(delta)  (bf16 high/low pairs)
+        // ---- 4. E^T = U^T - (W S)^T in place of (W S)^T (fp32, TF32-rounded: the A operand of
+        //         the state update) and G (Q S)^T in place of (Q S)^T (the update accumulates
+        //         the output onto it)
         wait_bar(&bar_d, par);
         {
-            const float *sDel = l2 ? nvec(it, NV_DK) : vec(it, 2);
             float ws[32], uu[32];
-            tmem_ld32(tm + TM_D + 32 * half, ws);
-            tmem_ld32(tm + TM_U + 32 * half, uu);
+            tmem_ld32(tm + TM_WE + 32 * half, ws);
+            if (!zero_u) tmem_ld32(tm + TM_U + 32 * half, uu);
             tmem_wait_ld();
-            if (zero_u)
 #pragma unroll
-                for (int u = 0; u < 32; ++u) uu[u] = 0.f;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float e[8], ed[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int r = 32 * half + 8 * q4 + u;
-                    e[u] = uu[8 * q4 + u] - ws[8 * q4 + u];
-                    ed[u] = e[u] * sDel[r];
-                }
-                const uint32_t off = sw128_off(row, 32 * half + 8 * q4);
-                uint32_t eh[4], el[4], dh[4], dlo[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    pack_hi_lo(e[2 * u], e[2 * u + 1], eh[u], el[u]);
-                    pack_hi_lo(ed[2 * u], ed[2 * u + 1], dh[u], dlo[u]);
-                }
-                *reinterpret_cast<uint4 *>(sm + SM_WQ + off) = make_uint4(eh[0], eh[1], eh[2], eh[3]);
-                *reinterpret_cast<uint4 *>(sm + SM_WQ + 16384 + off) = make_uint4(el[0], el[1], el[2], el[3]);
-                *reinterpret_cast<uint4 *>(sm + SM_ET2 + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
-                *reinterpret_cast<uint4 *>(st + OFF_V0 + off) = make_uint4(dlo[0], dlo[1], dlo[2], dlo[3]);
-            }
+            for (int u = 0; u < 32; ++u) ws[u] = round_tf32((zero_u ? 0.f : uu[u]) - ws[u]);
+            tmem_st32(tm + TM_WE + 32 * half, ws);
         }
-        fence_proxy_async();
+        if (outputs) {
+            wait_bar(&bar_q, par);
+            const float *sGam = (l2 ? nvec(it, NV_GQ) : vec(it, 1)) + 32 * half;
+            float qs[32];
+            tmem_ld32(tm + TM_QO + 32 * half, qs);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u4 = 0; u4 < 8; ++u4) {
+                const float4 g4 = *reinterpret_cast<const float4 *>(sGam + 4 * u4);
+                qs[4 * u4] *= g4.x; qs[4 * u4 + 1] *= g4.y; qs[4 * u4 + 2] *= g4.z; qs[4 * u4 + 3] *= g4.w;
+            }
+            tmem_st32(tm + TM_QO + 32 * half, qs);
+        }
+        tmem_wait_st();
+        fence_proxy_async();   // Kt^T (step 3) for the tensor core
         tc_fence_before();
         named_sync(1, kThreads);
-        if (tid == 0) mbar_arrive(&full_s);   // state update, E^T P^T (MMA warp)
+        if (tid == 0) mbar_arrive(&full_s);   // [O^T | S^T] (MMA warp)
+        // the stage's last readers, (Q S)^T and the Kt^T build, are done: it takes the chunk
+        // after next
+        if (early && tid == kTmaThread && it + 2 < n_it) issue_tma(it + 2);
 
-        // ---- 5. the next chunk's solve (its T goes over S^T, which D must have read): the diagonal
-        //         blocks on all warps, then the merges on warps 0..3 while warps 4..7 write
-        //         this chunk's output o = G_r (Q S)^T + E^T P^T (staged in the stage's Q and K
-        //         tiles, dead once E^T P^T is done) and the next chunk's P (E^T P^T has read
-        //         SM_P)
-        if (next) {
-            wait_bar(&bar_q, par);
-            solve_diag(it + 1);
-            named_sync(1, kThreads);
-        }
+        // ---- 5. the merges of the next chunk's T on warps 0..3, while warps 4..7 build the
+        //         next chunk's P (the update has read [P; Kt^T]; then X(c + 2) may overwrite
+        //         TM_X) and write this chunk's output O^T (staged in the stage's Q and K tiles,
+        //         dead once the state update is done)
         if (warp < 4) {
             if (next) solve_merge(it + 1);
         } else {
-            wait_bar(&bar_pe, par);
+            wait_bar(&bar_s, par);
             if (outputs) {
+                if (next && quarter < 2) {   // P rows: lanes 0..63 (warps 4 and 5), both column halves
+                    build_pa(it + 1, false, 0);
+                    build_pa(it + 1, false, 1);
+                    tc_fence_before();
+                    named_sync(4, 64);
+                    if (early && warp == 4 && lane == 0 && it + 2 < n_it) mbar_arrive(&full_x);
+                }
                 const int j = row;   // value channel; all 64 tokens of this lane
-                const float *sGam = l2 ? nvec(it, NV_GQ) : vec(it, 1);
                 if (zgate) wait_bar(&bar_z, it & 1);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    float o[32], pe[32];
-                    tmem_ld32(tm + TM_D + 64 + 32 * hh, o);
-                    tmem_ld32(tm + TM_PE + 32 * hh, pe);
+                    float o[32];
+                    tmem_ld32(tm + TM_QO + 32 * hh, o);
                     tmem_wait_ld();
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) o[u] = fmaf(sGam[32 * hh + u], o[u], pe[u]);
                     if (zgate) {
                         const unsigned char *zt = st + (j >> 6) * 16384;
 #pragma unroll
@@ -766,13 +810,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                                 *reinterpret_cast<const __nv_bfloat16 *>(zt + sw128_off(32 * hh + u, j & 63))));
                     }
                     if (sizeof(Tout) == 2) {
-                        unsigned char *dst = st + obox(j >> 6);
+                        unsigned char *dst = obox(it, j >> 6);
 #pragma unroll
                         for (int u = 0; u < 32; ++u)
                             *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * hh + u, j & 63)) =
                                 __float2bfloat16_rn(o[u]);
                     } else {
-                        unsigned char *dst = st + obox(j >> 5);
+                        unsigned char *dst = obox(it, j >> 5);
                         const int cj = j & 31;
 #pragma unroll
                         for (int u = 0; u < 32; ++u) {
@@ -782,34 +826,33 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                         }
                     }
                 }
-                if (next) {   // P rows: lanes 0..63 (warps 4 and 5), both column halves
-                    build_pa(it + 1, false, 0);
-                    build_pa(it + 1, false, 1);
-                }
                 fence_proxy_async();
+                // the gates of the chunk after next (into this chunk's set, which no later step
+                // of this chunk reads), while warps 4 and 5 are still busy with P
+                if (warp == kGateWarp && it + 2 < n_it) scan_gates(it + 2);
                 named_sync(3, 128);
                 if (tid == kTmaThread) {
                     constexpr int cols = sizeof(Tout) == 2 ? 64 : 32;
 #pragma unroll
                     for (int kb = 0; kb < kOutBoxes; ++kb)
-                        tma_store_4d(&to, st + obox(kb), cols * kb, h, t0, b);
+                        tma_store_4d(&to, obox(it, kb), cols * kb, h, t0, b);
                     bulk_commit();
-                    bulk_wait_read_all();   // the stage is reloaded next
+                    if (early && sizeof(Tout) == 4) bulk_wait_read_all();   // step 1b rewrites the staging
                 }
             }
+            if (!outputs && warp == kGateWarp && it + 2 < n_it) scan_gates(it + 2);
         }
         tc_fence_before();
         named_sync(1, kThreads);
 
-        // ---- 6. hand-offs: the next chunk's U/W and the chunk after next's X (MMA warp); the
-        //         stage of this chunk takes the chunk after next
-        if (tid == 0) {
-            if (next) mbar_arrive(&full_uw);
-            if (it + 2 < n_it) mbar_arrive(&full_x);
+        // ---- 6. hand-offs: the next chunk's U/W (MMA warp); with the output gate, the chunk
+        //         after next's X and that chunk's tiles into this chunk's stage
+        if (tid == 0 && next) mbar_arrive(&full_uw);
+        if (!early && tid == 0 && it + 2 < n_it) mbar_arrive(&full_x);
+        if (!early && tid == kTmaThread && it + 2 < n_it) {
+            bulk_wait_read_all();   // the output has left the stage
+            issue_tma(it + 2);
         }
-        if (tid == kTmaThread && it + 2 < n_it) issue_tma(it + 2);
-        // ---- 7. gates of the chunk after next (into this chunk's set, now free)
-        if (warp == kGateWarp && it + 2 < n_it) scan_gates(it + 2);
     }
 
     if (!abort_s && n_it > 0) {

@@ -95,12 +95,6 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
 }
 
-// As ldsm_x4, transposed: thread t receives rows 2 (t % 4), 2 (t % 4) + 1 of column t / 4 of
-// each 8 x 8 matrix.
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
 
 template <int GATE>
 __global__ void __launch_bounds__(kPrepThreads, 4)
@@ -346,10 +340,6 @@ struct ChainArgs {
     const float *norms;
 };
 
-// byte offset of fp32 element (row, k), k < 32, in a 128-byte-swizzled K-major tf32 tile
-__device__ __forceinline__ uint32_t sw128_off32(uint32_t row, uint32_t k) {
-    return row * 128u + ((((k >> 2) ^ (row & 7u)) & 7u) << 4) + ((k & 3u) << 2);
-}
 
 // Per chunk it (period: from the state update of it - 1 to that of it), the MMA warp issues
 //   [W S | Q S](it)  W(it + 1)  update(it)  X(it + 1)  U(it + 1)

@@ -277,6 +277,14 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[1
           "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
+// 32 lanes x 32 consecutive 32-bit columns set to zero (one source register throughout).
+__device__ __forceinline__ void tmem_zero32(uint32_t taddr) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,"
+        "%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};"
+        ::"r"(taddr), "r"(0u) : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -356,6 +364,17 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 // 128 bytes (bf16): the 16-byte chunk index is XORed with row % 8.
 __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t col) {
     return row * 128u + ((((col >> 3) ^ (row & 7u)) & 7u) << 4) + ((col & 7u) << 1);
+}
+// Byte offset of fp32 element (row, k), k < 32, in a 128-byte-swizzled K-major tf32 tile.
+__device__ __forceinline__ uint32_t sw128_off32(uint32_t row, uint32_t k) {
+    return row * 128u + ((((k >> 2) ^ (row & 7u)) & 7u) << 4) + ((k & 3u) << 2);
+}
+
+// ldmatrix of four 8 x 8 bf16 matrices, transposed: thread t receives rows 2 (t % 4),
+// 2 (t % 4) + 1 of column t / 4 of each matrix.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
 }
 
 }  // namespace umma
