@@ -40,7 +40,7 @@ HBM_NOMINAL_GBS = 7900.0
 # of the headline's launch shape (128 chains) at half its head-tokens (B8 H16 T2048); the
 # kernel's traffic is proportional to head-tokens, so the figure is twice the captured one.  Valid only while the kernel
 # sources hash to `src`; otherwise the bench reports null.
-TRAFFIC = {"chunk_fwd": {"bytes": 2 * (203372800 + 50517248), "src": "68b10373da4d1b2b"}}
+TRAFFIC = {"chunk_fwd": {"bytes": 2 * (203420928 + 50164736), "src": "8430003d72717142"}}
 
 
 def peaks():
