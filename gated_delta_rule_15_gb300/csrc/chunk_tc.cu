@@ -781,8 +781,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
         // ---- 5. the merges of the next chunk's T on warps 0..3, while warps 4..7 build the
         //         next chunk's P (the update has read [P; Kt^T]; then X(c + 2) may overwrite
-        //         TM_X) and write this chunk's output O^T (staged in the stage's Q and K tiles,
-        //         dead once the state update is done)
+        //         TM_X) and write this chunk's output O^T (staged as obox() places it)
         if (warp < 4) {
             if (next) solve_merge(it + 1);
         } else {

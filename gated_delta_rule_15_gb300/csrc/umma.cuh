@@ -277,14 +277,6 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[1
           "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
-// 32 lanes x 32 consecutive 32-bit columns set to zero (one source register throughout).
-__device__ __forceinline__ void tmem_zero32(uint32_t taddr) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,"
-        "%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};"
-        ::"r"(taddr), "r"(0u) : "memory");
-}
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
