@@ -788,15 +788,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             wait_bar(&bar_s, par);
             if (outputs) {
                 if (next && quarter < 2) {   // P rows: lanes 0..63 (warps 4 and 5), both column halves
-                    build_pa(it + 1, false, 0);
-                    build_pa(it + 1, false, 1);
+                    // (one copy of the build for both column halves: the loop body's code
+                    // size, not its instruction count, limits this kernel -- see below)
+#pragma unroll 1
+                    for (int ch = 0; ch < 2; ++ch) build_pa(it + 1, false, ch);
                     tc_fence_before();
                     named_sync(4, 64);
                     if (early && warp == 4 && lane == 0 && it + 2 < n_it) mbar_arrive(&full_x);
                 }
                 const int j = row;   // value channel; all 64 tokens of this lane
                 if (zgate) wait_bar(&bar_z, it & 1);
-#pragma unroll
+                // The two 32-token halves share one copy of the code.  Nine warps run
+                // different parts of a ~155 KB kernel at once, and instruction fetch is the
+                // largest stall ("no instruction"): keeping this loop and the P build above
+                // rolled (7 KB less code) cut the call by 6.5 %.
+#pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
                     float o[32];
                     tmem_ld32(tm + TM_QO + 32 * hh, o);
