@@ -41,7 +41,7 @@ HBM_NOMINAL_GBS = 7900.0
 # kernel's traffic is proportional to head-tokens, so the figure is twice the captured one.  Valid only while the kernel
 # sources hash to `src` (moved only for edits that leave the compiled kernel byte-identical); otherwise the bench
 # reports null.
-TRAFFIC = {"chunk_fwd": {"bytes": 2 * (203137280 + 49185280), "src": "3d52a35c3b8fb049"}}
+TRAFFIC = {"chunk_fwd": {"bytes": 2 * (203137280 + 49185280), "src": "c4ff1e6ef8947858"}}
 
 
 def peaks():

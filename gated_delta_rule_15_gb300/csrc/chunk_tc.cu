@@ -100,8 +100,16 @@ constexpr uint32_t SM_TOTAL = SM_SMALL + 8192;
 constexpr uint32_t SM_NRM = SM_TOTAL;
 constexpr uint32_t SM_TOTAL_FUSED = SM_NRM + 3584;
 static_assert(SM_TOTAL_FUSED + 1024 <= 227 * 1024, "layout");
+// 128-byte-swizzled operands and TMA boxes start on 1024-byte boundaries; [P; Kt^T] holds
+// 192 rows of 128 bytes per K-block, the bf16 output staging its rows 128..191 of each
+static_assert(SM_T % 1024 == 0 && SM_TB % 1024 == 0 && SM_W % 1024 == 0 && SM_BU % 1024 == 0 &&
+              BU_KB % 1024 == 0 && BU_KB == 192 * 128, "layout");
+static_assert(16384 + BU_KB + 8192 <= 2 * BU_KB, "output staging inside [P; Kt^T]");
 enum { NV_NQ = 0, NV_NK = 1, NV_GQ = 2, NV_BK = 3, NV_GK = 4, NV_RK = 5, NV_DK = 6 };
 constexpr uint32_t TM_WE = 0, TM_QO = 64, TM_S = 128, TM_SB = 256, TM_X = 320, TM_U = 384, TM_W = 448;
+static_assert(TM_QO == TM_WE + 64 && TM_S == TM_QO + 64 && TM_SB == TM_S + 128 && TM_X == TM_SB + 64 &&
+              TM_U == TM_X + 64 && TM_W == TM_U + 64 && TM_W + 64 == 512,
+              "TMEM: [O^T | S^T] contiguous (one N = 192 accumulator), 512 columns in all");
 // TM_WE: (W S)^T, then E^T (fp32, the A operand of the state update);  TM_QO: (Q S)^T, then
 // G (Q S)^T, then O^T: [TM_QO | TM_S] is the accumulator of the state update;  TM_SB: S^T as
 // bf16 pairs (the A operand of D);  TM_X: [Q; K] K^T
